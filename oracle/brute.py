@@ -1,0 +1,82 @@
+"""Pure-Python scalar restatement of the oracle, for tiny shapes only.
+
+TEST INFRASTRUCTURE ONLY. Shares no code with ``w4a16_oracle``: fp16 rounding
+goes through ``struct``'s half-precision format (CPython rounds a double to
+the nearest half, ties to even), rounding to integers through the built-in
+``round`` (ties to even), sums are plain Python-float loops. It follows the
+same steps as ``w4a16_oracle`` -- the linear quantization formula of "LLM
+Quantization: A Deep Dive into GPTQ, AWQ, and Post-Training Quantization"
+(section "The Math of Quantization") applied per group of input columns as in
+"AWQ + GPTQ Quantization, in depth" (section "What W4A16 buys and why
+decoding gets faster") -- written out element by element so that a slip in
+the vectorised version (an index, a sign, a transposed operand) shows up as a
+mismatch.
+"""
+
+from __future__ import annotations
+
+import struct
+
+
+def f16(v: float) -> float:
+    """Nearest fp16 value of a double, ties to even (via struct 'e')."""
+    return struct.unpack("<e", struct.pack("<e", v))[0]
+
+
+def _clamp(v: int, lo: int, hi: int) -> int:
+    return lo if v < lo else hi if v > hi else v
+
+
+def quantize(W, group_size, sym, g_idx=None):
+    """W: list of rows of Python floats (fp16 values). Returns q, s, z lists."""
+    N, K = len(W), len(W[0])
+    if g_idx is None:
+        g_idx = [k // group_size for k in range(K)]
+    G = max(g_idx) + 1
+    q = [[0] * K for _ in range(N)]
+    s_out = [[0.0] * G for _ in range(N)]
+    z_out = [[0] * G for _ in range(N)]
+    for n in range(N):
+        for t in range(G):
+            cols = [k for k in range(K) if g_idx[k] == t]
+            vals = [W[n][k] for k in cols]
+            if sym:
+                a = max(abs(v) for v in vals)
+                s = f16(2.0 * a / 15.0)
+            else:
+                lo, hi = min(vals), max(vals)
+                s = f16((hi - lo) / 15.0)
+            if s == 0.0:
+                s = 1.0
+            z = 8 if sym else _clamp(round(-lo / s), 0, 15)
+            s_out[n][t] = s
+            z_out[n][t] = z
+            for k in cols:
+                q[n][k] = _clamp(round(W[n][k] / s) + z, 0, 15)
+    return q, s_out, z_out
+
+
+def dequant(q, s, z, g_idx):
+    return [[f16((q[n][k] - z[n][g_idx[k]]) * s[n][g_idx[k]])
+             for k in range(len(q[0]))] for n in range(len(q))]
+
+
+def linear(x, w_hat):
+    """y[m][n] = sum_k x[m][k] * w_hat[n][k] (W is out x in)."""
+    M, N, K = len(x), len(w_hat), len(x[0])
+    y = [[0.0] * N for _ in range(M)]
+    for m in range(M):
+        for n in range(N):
+            acc = 0.0
+            for k in range(K):
+                acc += x[m][k] * w_hat[n][k]
+            y[m][n] = acc
+    return y
+
+
+def pack_word(codes8):
+    """Eight codes -> one uint32, code i in bits 4i..4i+3."""
+    w = 0
+    for i, c in enumerate(codes8):
+        w |= (c & 0xF) << (4 * i)
+    return w

@@ -1,0 +1,243 @@
+"""NumPy fp64 oracle for the W4A16 group-quantized linear layer.
+
+TEST INFRASTRUCTURE ONLY (see the package docstring): nothing in the library
+imports this module.
+
+What it computes, step by step, and where each step comes from:
+
+1. Group map. By default input column j belongs to group j // g: "each run of
+   128 consecutive input weights in a row typically shares one scale"
+   ("AWQ + GPTQ Quantization, in depth", section "What W4A16 buys and why
+   decoding gets faster"). With GPTQ act order a column->group map ``g_idx``
+   is given instead ("The two algorithms, compactly": act order; the Q&A page
+   "How do GPTQ and AWQ differ ...", option ``desc_act``). Every group must
+   hold exactly g columns.
+2. Scale and zero per (row, group), round to nearest ("LLM Quantization:
+   INT8, GPTQ, and AWQ Explained", section "What quantization actually does":
+   find the range, pick the scale that spreads the integer grid over it, round
+   each weight to the nearest grid point):
+   asymmetric: s = fp16((max - min) / 15), z = clamp(rint(-min / s), 0, 15);
+   symmetric:  s = fp16(2 * max|w| / 15), z = 8.
+   A scale that is zero (constant group, or a range that rounds to 0 in fp16)
+   is replaced by 1.0: the pages do not treat this case.
+3. Codes q = clamp(rint(w / s) + z, 0, 15), the linear quantization formula
+   q = round(x / S) + Z ("LLM Quantization: A Deep Dive into GPTQ, AWQ, and
+   Post-Training Quantization", section "The Math of Quantization") with the
+   clamp of the int8 example on the INT8/GPTQ/AWQ page. ``rint`` rounds half
+   to even (the pages' own code rounds with torch.round, which does), and the
+   division is fp64 with the *stored* fp16 scale.
+4. Canonical packing: 8 nibbles per uint32, nibble j of word k // 8 holds
+   column k with k % 8 == j; zero points packed the same way along the group
+   axis, padded with zero nibbles.
+5. Dequantization w_hat = fp16((q - z) * s) ("The Math of Quantization":
+   x_approx = (q - Z) * S). The fp64 product is exact; one round to nearest
+   even gives the fp16 weight ("the actual matrix multiply still happens in
+   fp16: each block is dequantized back to fp16", INT8/GPTQ/AWQ page).
+6. Output y = x . w_hat^T in fp64 (W is "out x in", "The two algorithms,
+   compactly"), with the per-element bound B = |x| . |w_hat|^T used by the
+   acceptance test |y_gpu - y| <= 2e-3 * B + 1e-3.
+
+No blocking, fusion or reordering beyond these definitions; library matmuls
+(``@``) are used for the sums.
+"""
+
+from __future__ import annotations
+
+import numpy as np
+
+QMAX = 15  # 4-bit codes are 0..15
+SYM_ZERO = 8  # symmetric scheme: zero point fixed at 8
+TOL_REL = 2e-3  # |y_gpu - y_ref| <= TOL_REL * sum|x * w_hat| + TOL_ABS
+TOL_ABS = 1e-3
+
+
+# ---------------------------------------------------------------------------
+# fp16 rounding
+# ---------------------------------------------------------------------------
+def fp16_rne(a) -> np.ndarray:
+    """Round fp64 values to the nearest fp16 value, ties to even.
+
+    NumPy converts float64 -> float16 directly (no detour through float32),
+    rounding to nearest even. This is pinned in the tests against an
+    exhaustive nearest-value search over all finite fp16 values and against
+    ``struct``'s half-precision packing.
+    """
+    return np.asarray(a, dtype=np.float64).astype(np.float16)
+
+
+# ---------------------------------------------------------------------------
+# Step 1: group map
+# ---------------------------------------------------------------------------
+def group_map(K: int, group_size: int, g_idx=None) -> tuple[np.ndarray, int]:
+    """Return (g_idx as int64 [K], number of groups G).
+
+    Without ``g_idx`` column j is in group j // group_size. With ``g_idx``
+    (act order) the map is validated: values in [0, G) and exactly
+    ``group_size`` members per group, G = K / group_size.
+    """
+    if group_size <= 0:
+        raise ValueError("group_size must be positive")
+    if g_idx is None:
+        G = -(-K // group_size)
+        return np.arange(K, dtype=np.int64) // group_size, G
+    g_idx = np.asarray(g_idx, dtype=np.int64)
+    if g_idx.shape != (K,):
+        raise ValueError("g_idx must have shape [K]")
+    if K % group_size != 0:
+        raise ValueError("act order needs K divisible by group_size")
+    G = K // group_size
+    if g_idx.min(initial=0) < 0 or g_idx.max(initial=0) >= G:
+        raise ValueError("g_idx out of range")
+    counts = np.bincount(g_idx, minlength=G)
+    if not np.all(counts == group_size):
+        raise ValueError("every group must have exactly group_size members")
+    return g_idx, G
+
+
+def group_members(g_idx: np.ndarray, G: int) -> list[np.ndarray]:
+    """Columns of each group, in increasing column order."""
+    return [np.flatnonzero(g_idx == t) for t in range(G)]
+
+
+# ---------------------------------------------------------------------------
+# Steps 2-3: round-to-nearest quantization
+# ---------------------------------------------------------------------------
+def quantize_codes(w: np.ndarray, s: np.ndarray, z: np.ndarray) -> np.ndarray:
+    """q = clamp(rint(w / s) + z, 0, 15); w, s, z broadcast, fp64 division."""
+    w = np.asarray(w, dtype=np.float64)
+    s = np.asarray(s, dtype=np.float64)
+    q = np.rint(w / s) + np.asarray(z, dtype=np.float64)
+    return np.clip(q, 0, QMAX).astype(np.uint8)
+
+
+def group_scale_zero(w: np.ndarray, sym: bool) -> tuple[np.ndarray, np.ndarray]:
+    """Scale (fp16) and zero (uint8) of each row of ``w`` ([rows, members])."""
+    w = np.asarray(w, dtype=np.float64)
+    if sym:
+        a = np.max(np.abs(w), axis=1)
+        s = fp16_rne(2.0 * a / QMAX)
+    else:
+        mn = np.min(w, axis=1)
+        mx = np.max(w, axis=1)
+        s = fp16_rne((mx - mn) / QMAX)
+    s = np.where(s == 0, np.float16(1.0), s).astype(np.float16)
+    if sym:
+        z = np.full(w.shape[0], SYM_ZERO, dtype=np.uint8)
+    else:
+        z = np.clip(np.rint(-mn / s.astype(np.float64)), 0, QMAX).astype(np.uint8)
+    return s, z
+
+
+def rtn_quantize(W, group_size: int, sym: bool, g_idx=None):
+    """Round-to-nearest group quantization of fp16 ``W`` [N, K].
+
+    Returns codes q uint8 [N, K] (original column order), scales fp16 [N, G]
+    and zeros uint8 [N, G] (all 8 when ``sym``).
+    """
+    W = np.asarray(W)
+    if W.dtype != np.float16:
+        raise TypeError("W must be float16")
+    N, K = W.shape
+    gi, G = group_map(K, group_size, g_idx)
+    Wd = W.astype(np.float64)
+    q = np.zeros((N, K), dtype=np.uint8)
+    scales = np.zeros((N, G), dtype=np.float16)
+    zeros = np.zeros((N, G), dtype=np.uint8)
+    for t, cols in enumerate(group_members(gi, G)):
+        w = Wd[:, cols]
+        s, z = group_scale_zero(w, sym)
+        scales[:, t] = s
+        zeros[:, t] = z
+        q[:, cols] = quantize_codes(w, s.astype(np.float64)[:, None], z[:, None])
+    return q, scales, zeros
+
+
+# ---------------------------------------------------------------------------
+# Step 4: canonical packing (8 nibbles per uint32, along the packed axis)
+# ---------------------------------------------------------------------------
+def pack_nibbles(codes: np.ndarray) -> np.ndarray:
+    """Pack uint8 codes [R, C] (0..15) into uint32 [R, ceil(C/8)].
+
+    Nibble j (bits 4j..4j+3) of word c // 8 holds column c with c % 8 == j;
+    missing columns of the last word are zero.
+    """
+    codes = np.asarray(codes, dtype=np.uint8)
+    if codes.max(initial=0) > QMAX:
+        raise ValueError("codes must be 0..15")
+    R, C = codes.shape
+    W8 = -(-C // 8)
+    padded = np.zeros((R, W8 * 8), dtype=np.uint32)
+    padded[:, :C] = codes
+    out = np.zeros((R, W8), dtype=np.uint32)
+    for j in range(8):
+        out |= padded[:, j::8] << np.uint32(4 * j)
+    return out
+
+
+def unpack_nibbles(words: np.ndarray, C: int) -> np.ndarray:
+    """Inverse of ``pack_nibbles``: uint32 [R, ceil(C/8)] -> uint8 [R, C]."""
+    words = np.asarray(words, dtype=np.uint32)
+    R, W8 = words.shape
+    out = np.zeros((R, W8 * 8), dtype=np.uint8)
+    for j in range(8):
+        out[:, j::8] = (words >> np.uint32(4 * j)) & np.uint32(0xF)
+    return out[:, :C]
+
+
+# ---------------------------------------------------------------------------
+# Step 5: dequantization
+# ---------------------------------------------------------------------------
+def dequant(q, scales, zeros, group_size: int, g_idx=None) -> np.ndarray:
+    """w_hat[n, k] = fp16((q[n,k] - z[n, g(k)]) * s[n, g(k)]), fp16 [N, K]."""
+    q = np.asarray(q)
+    N, K = q.shape
+    gi, G = group_map(K, group_size, g_idx)
+    s = np.asarray(scales, dtype=np.float16).astype(np.float64)[:, gi]
+    z = np.asarray(zeros, dtype=np.float64)[:, gi]
+    return fp16_rne((q.astype(np.float64) - z) * s)
+
+
+# ---------------------------------------------------------------------------
+# Step 6: the linear layer and its acceptance bound
+# ---------------------------------------------------------------------------
+def linear_ref(x, w_hat) -> tuple[np.ndarray, np.ndarray]:
+    """(y, B): y = x . w_hat^T and B = |x| . |w_hat|^T, both fp64 [M, N]."""
+    xd = np.asarray(x, dtype=np.float64)
+    wd = np.asarray(w_hat, dtype=np.float64)
+    return xd @ wd.T, np.abs(xd) @ np.abs(wd).T
+
+
+def tolerance(B) -> np.ndarray:
+    """Per-element acceptance bound 2e-3 * B + 1e-3."""
+    return TOL_REL * np.asarray(B, dtype=np.float64) + TOL_ABS
+
+
+def error_ratio(y_test, y_ref, B) -> np.ndarray:
+    """|y_test - y_ref| / (2e-3 * B + 1e-3): passes where <= 1."""
+    return np.abs(np.asarray(y_test, dtype=np.float64) - y_ref) / tolerance(B)
+
+
+def w4a16_linear(x, W, group_size: int, sym: bool, g_idx=None):
+    """End to end: quantize fp16 W, dequantize, multiply by fp16 x.
+
+    Returns (y, B, (q, scales, zeros), w_hat).
+    """
+    q, s, z = rtn_quantize(W, group_size, sym, g_idx)
+    w_hat = dequant(q, s, z, group_size, g_idx)
+    y, B = linear_ref(x, w_hat)
+    return y, B, (q, s, z), w_hat
+
+
+# ---------------------------------------------------------------------------
+# Byte budget (closed form)
+# ---------------------------------------------------------------------------
+def packed_bytes_closed_form(N: int, K: int, group_size: int, sym: bool) -> float:
+    """Bytes of one packed linear: codes N*K/2, fp16 scales N*G*2, 4-bit zeros
+    N*G/2 (none when symmetric), G = K / group_size ("What W4A16 buys":
+    16-bit scale per 128 weights = 0.125 bit/weight, 4-bit zero ~0.03)."""
+    G = K / group_size
+    return N * K / 2 + N * G * 2 + (0 if sym else N * G / 2)
+
+
+def bits_per_weight(group_size: int, sym: bool) -> float:
+    return 4 + 16 / group_size + (0 if sym else 4 / group_size)

@@ -1,0 +1,417 @@
+"""Pins for the CPU oracle: checks against what the pages and the mathematics
+fix, not against the oracle itself. CPU only."""
+
+import json
+import os
+import struct
+
+import numpy as np
+import pytest
+
+from oracle import brute
+from oracle import w4a16_oracle as O
+from weight_only_bit_04_b300 import synth
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+# All finite fp16 values, ascending, with their bit patterns.
+_BITS = np.arange(0x10000, dtype=np.uint32).astype(np.uint16)
+_VALS = _BITS.view(np.float16)
+_FIN = np.isfinite(_VALS)
+_ORDER = np.argsort(_VALS[_FIN].astype(np.float64), kind="stable")
+F16_SORTED = _VALS[_FIN].astype(np.float64)[_ORDER]
+F16_BITS = _BITS[_FIN][_ORDER]
+
+
+def nearest_fp16_by_search(v: float) -> float:
+    """Nearest finite fp16 to v, ties to the even bit pattern (brute force)."""
+    i = np.searchsorted(F16_SORTED, v)
+    cands = [j for j in (i - 1, i) if 0 <= j < F16_SORTED.size]
+    best = min(cands, key=lambda j: abs(F16_SORTED[j] - v))
+    d = abs(F16_SORTED[best] - v)
+    ties = [j for j in cands if abs(F16_SORTED[j] - v) == d]
+    if len(ties) > 1:
+        # +0 and -0 are both at distance |v| from a tiny v; both even, same value
+        ties = [j for j in ties if F16_BITS[j] % 2 == 0] or ties
+        best = ties[0]
+    return float(F16_SORTED[best])
+
+
+# ---------------------------------------------------------------------------
+# fp16 rounding
+# ---------------------------------------------------------------------------
+def test_fp16_rne_matches_exhaustive_search_and_struct():
+    rng = np.random.default_rng(1)
+    vals = list(rng.normal(0, 0.02, 300)) + list(rng.normal(0, 3, 300))
+    vals += list(rng.uniform(-65000, 65000, 200))
+    # exact midpoints between adjacent fp16 values (ties), incl. subnormals
+    idx = rng.integers(0, F16_SORTED.size - 1, 400)
+    vals += list((F16_SORTED[idx] + F16_SORTED[idx + 1]) / 2)
+    vals += [1024.5, 1025.5, 2049.0, 2051.0, 2.0 ** -25, 3 * 2.0 ** -25]
+    got = O.fp16_rne(np.array(vals)).astype(np.float64)
+    for v, g in zip(vals, got):
+        assert g == nearest_fp16_by_search(v), v
+        assert g == brute.f16(v), v
+
+
+def test_fp16_rne_ties_go_to_even():
+    # 2049 lies halfway between 2048 and 2050 (spacing 2 at 2^11): even -> 2048
+    assert float(O.fp16_rne(2049.0)) == 2048.0
+    assert float(O.fp16_rne(2051.0)) == 2052.0
+    assert float(O.fp16_rne(1.0 + 2.0 ** -11)) == 1.0
+
+
+# ---------------------------------------------------------------------------
+# Byte budget: closed form against the pages' printed numbers
+# ---------------------------------------------------------------------------
+def _golden():
+    with open(os.path.join(GOLDEN, "byte_budget.json")) as f:
+        return json.load(f)
+
+
+def test_bits_per_weight_closed_form():
+    g = _golden()["bits_per_weight_g128"]
+    bpw = O.bits_per_weight(128, sym=False)
+    assert bpw == 4 + 0.125 + 0.03125 == 4.15625
+    lo, hi = g["printed_range"]
+    assert lo <= bpw <= hi
+    assert O.bits_per_weight(128, sym=True) == 4.125  # scale only, no zero point
+    assert 16 / 128 == g["scale_bits_per_weight"]
+    assert abs(4 / 128 - g["zero_bits_per_weight_about"]) < 0.005
+    # smaller groups cost more bits
+    assert O.bits_per_weight(64, False) == 4.3125
+    assert O.bits_per_weight(32, False) == 4.625
+    assert O.packed_bytes_closed_form(4096, 4096, 128, False) * 8 / 4096 ** 2 == bpw
+
+
+def test_worked_example_1p5b_model():
+    g = _golden()["model_1p5b"]
+    p = g["printed"]
+    h, f, L = g["hidden"], g["mlp"], g["layers"]
+    kv = g["kv_heads"] * g["head_dim"]
+    # linears of one layer as (N, K): q, k, v, o, gate, up, down
+    lin = [(h, h), (kv, h), (kv, h), (h, h), (f, h), (f, h), (h, f)]
+    attn = sum(n * k for n, k in lin[:4])
+    mlp = sum(n * k for n, k in lin[4:])
+    assert attn == h * 3584 and round(attn / 1e6, 1) == p["attention_weights_per_layer_M"]
+    assert round(mlp / 1e6, 1) == p["mlp_weights_per_layer_M"]
+    n_lin = L * (attn + mlp)
+    assert round(n_lin / 1e9, 2) == p["linear_weights_B"]
+    emb = g["vocab"] * h
+    assert round(emb / 1e6) == p["embedding_M"]
+    assert round((n_lin + emb) / 1e9, 2) == p["total_params_B"]
+    assert round((n_lin + emb) * 2 / 1e9, 2) == p["bf16_GB"]
+    q_lin = L * sum(O.packed_bytes_closed_form(n, k, 128, False) for n, k in lin)
+    assert round(q_lin / 1e9, 2) == p["w4a16_linears_GB"]
+    assert round(emb * 2 / 1e9, 2) == p["embedding_bf16_GB"]
+    total = q_lin + emb * 2
+    # the page says "about 1.14 GB"; the closed form gives 1.147
+    assert abs(total / 1e9 - p["quantized_model_GB"]) < 0.01
+    assert round((n_lin + emb) * 2 / total, 1) == p["shrink_factor"]
+    assert round(100 * emb / (n_lin + emb)) == p["embedding_share_of_params_pct"]
+    assert round(100 * emb * 2 / total) == p["embedding_share_of_file_pct"]
+
+
+def test_70b_and_7b_byte_budgets():
+    gd = _golden()
+    p70 = gd["model_70b"]["printed"]
+    assert gd["model_70b"]["params_B"] * 2 == p70["fp16_GB"]
+    assert gd["model_70b"]["params_B"] * 0.5 == p70["int4_GB_about"]
+    q70 = synth.LLAMA_70B_LAYERS * sum(
+        O.packed_bytes_closed_form(n, k, 128, False) for _, n, k in synth.LLAMA_70B_LINEARS)
+    assert p70["int4_GB_about"] <= q70 / 1e9 <= p70["int4_with_metadata_GB_call_it"]
+    g7 = gd["model_llama2_7b"]
+    lin7 = synth.LLAMA2_7B_LAYERS * sum(
+        O.packed_bytes_closed_form(n, k, 128, False) for _, n, k in synth.LLAMA2_7B_LINEARS)
+    emb_head = 2 * g7["vocab"] * g7["hidden"] * 2  # fp16 embedding + head
+    assert abs((lin7 + emb_head) / 1e9 - g7["printed"]["awq_GB_about"]) < 0.5
+    n7 = synth.LLAMA2_7B_LAYERS * sum(n * k for _, n, k in synth.LLAMA2_7B_LINEARS)
+    assert abs((n7 + 2 * g7["vocab"] * g7["hidden"]) * 2 / 1e9 - g7["printed"]["fp16_GB_about"]) < 0.6
+
+
+# ---------------------------------------------------------------------------
+# Packing
+# ---------------------------------------------------------------------------
+def test_pack_every_nibble_in_every_position():
+    for pos in range(8):
+        for v in range(16):
+            codes = np.zeros((1, 8), dtype=np.uint8)
+            codes[0, pos] = v
+            w = O.pack_nibbles(codes)
+            assert int(w[0, 0]) == v << (4 * pos)
+            assert int(w[0, 0]) == brute.pack_word(codes[0].tolist())
+            assert np.array_equal(O.unpack_nibbles(w, 8), codes)
+
+
+def test_pack_roundtrip_random_and_ragged():
+    rng = np.random.default_rng(2)
+    for C in (8, 16, 43, 86, 1):
+        q = rng.integers(0, 16, (5, C)).astype(np.uint8)
+        w = O.pack_nibbles(q)
+        assert w.shape == (5, -(-C // 8))
+        assert np.array_equal(O.unpack_nibbles(w, C), q)
+        for r in range(5):
+            for c in range(C):
+                assert (int(w[r, c // 8]) >> (4 * (c % 8))) & 0xF == q[r, c]
+
+
+# ---------------------------------------------------------------------------
+# Quantizer
+# ---------------------------------------------------------------------------
+def test_roundtrip_quantize_of_dequant_is_identity_exhaustive_q_z():
+    """quantize(dequant(q)) == q with the stored (s, z), every q and z."""
+    rng = np.random.default_rng(3)
+    s_samples = np.concatenate([
+        O.fp16_rne(rng.uniform(1e-4, 0.02, 40)),
+        O.fp16_rne(rng.uniform(0.02, 4000.0, 20)),
+        np.array([1.0, 2.0 ** -14, 2.0 ** -24, 0.5, 4364.0], dtype=np.float16),
+    ]).astype(np.float16)
+    q = np.arange(16, dtype=np.float64)
+    for s in s_samples:
+        sd = float(s)
+        for z in range(16):
+            w_hat = O.fp16_rne((q - z) * sd)
+            back = O.quantize_codes(w_hat.astype(np.float64), sd, z)
+            assert np.array_equal(back, q.astype(np.uint8)), (sd, z)
+
+
+def test_rtn_codes_in_range_and_error_bound():
+    rng = np.random.default_rng(4)
+    for sym in (False, True):
+        for g in (32, 64, 128):
+            W = (rng.standard_normal((16, 256)) * 0.02).astype(np.float16)
+            q, s, z = O.rtn_quantize(W, g, sym)
+            assert q.max() <= 15 and z.max() <= 15
+            if sym:
+                assert np.all(z == 8)
+            w_hat = O.dequant(q, s, z, g).astype(np.float64)
+            sd = np.repeat(s.astype(np.float64), g, axis=1)
+            err = np.abs(W.astype(np.float64) - w_hat)
+            pre = np.rint(W.astype(np.float64) / sd) + np.repeat(z.astype(np.float64), g, axis=1)
+            inside = (pre >= 0) & (pre <= 15)
+            u = 2.0 ** -11
+            # unclamped: half a grid step plus the fp16 rounding of w_hat
+            assert np.all(err[inside] <= sd[inside] * (0.5 + 1e-12) + u * np.abs(w_hat[inside]))
+            # clamped (range ends): the scale's own fp16 rounding adds at most 15u steps
+            assert np.all(err <= sd * (0.5 + 16 * u) + u * np.abs(w_hat) + 1e-300)
+
+
+def test_asym_scale_and_zero_formula_on_a_hand_example():
+    # one group of 8: min -0.75, max 3.0 -> s = 3.75/15 = 0.25, z = rint(3) = 3
+    W = np.array([[-0.75, 3.0, 0.0, 0.125, 0.375, -0.5, 1.0, 2.5]], dtype=np.float16)
+    q, s, z = O.rtn_quantize(W, 8, sym=False)
+    assert float(s[0, 0]) == 0.25 and int(z[0, 0]) == 3
+    # w / s: -3, 12, 0, 0.5 (tie -> 0), 1.5 (tie -> 2), -2, 4, 10
+    assert q[0].tolist() == [0, 15, 3, 3, 5, 1, 7, 13]
+
+
+def test_rounding_ties_are_half_to_even():
+    # s = (8 - -7) / 15 = 1 exactly, z = rint(7) = 7.
+    W = np.array([[-7.0, 8.0, 2.5, 3.5, -0.5, 0.5, -1.5, 1.5]], dtype=np.float16)
+    q, s, z = O.rtn_quantize(W, 8, sym=False)
+    assert float(s[0, 0]) == 1.0 and int(z[0, 0]) == 7
+    # half-even: 2.5->2, 3.5->4, -0.5->-0, 0.5->0, -1.5->-2, 1.5->2
+    assert q[0].tolist() == [0, 15, 9, 11, 7, 7, 5, 9]
+    # a tie in the zero point: -min/s = 6.5 -> 6 (half-away would give 7)
+    W2 = np.array([[-6.5, 8.5] + [0.0] * 6], dtype=np.float16)
+    q2, s2, z2 = O.rtn_quantize(W2, 8, sym=False)
+    assert float(s2[0, 0]) == 1.0 and int(z2[0, 0]) == 6
+
+
+def test_symmetric_scheme():
+    rng = np.random.default_rng(5)
+    W = (rng.standard_normal((4, 128)) * 0.02).astype(np.float16)
+    q, s, z = O.rtn_quantize(W, 128, sym=True)
+    a = np.max(np.abs(W.astype(np.float64)), axis=1)
+    assert np.array_equal(s[:, 0], O.fp16_rne(2 * a / 15))
+    assert np.all(z == 8)
+    # the largest |w| sits at about +-7.5 grid steps from code 8: code 0 or 1
+    # when negative, 15 (clamped from 15 or 16) when positive
+    am = np.argmax(np.abs(W.astype(np.float64)), axis=1)
+    for n in range(4):
+        c = int(q[n, am[n]])
+        assert c in ((0, 1) if W[n, am[n]] < 0 else (15,))
+
+
+def test_zero_range_group_uses_unit_scale():
+    W = np.full((2, 8), 0.25, dtype=np.float16)
+    W[1] = 0.0
+    q, s, z = O.rtn_quantize(W, 8, sym=False)
+    assert np.all(s == 1.0)
+    # -min / s = -0.25 -> rint -> -0 -> z = 0; q = rint(0.25) + 0 = 0
+    assert np.all(z == 0) and np.all(q == 0)
+    qs, ss, zs = O.rtn_quantize(np.zeros((1, 8), np.float16), 8, sym=True)
+    assert np.all(ss == 1.0) and np.all(zs == 8) and np.all(qs == 8)
+
+
+def test_group_map_validation():
+    with pytest.raises(ValueError):
+        O.group_map(8, 4, [0, 0, 0, 1, 1, 1, 1, 1])  # group 0 has 3 members
+    with pytest.raises(ValueError):
+        O.group_map(8, 4, [0, 0, 0, 0, 1, 1, 1, 2])  # out of range
+    gi, G = O.group_map(8, 4, [1, 0, 1, 0, 1, 0, 1, 0])
+    assert G == 2 and gi.tolist() == [1, 0, 1, 0, 1, 0, 1, 0]
+
+
+# ---------------------------------------------------------------------------
+# Brute force (pure Python) against NumPy on tiny shapes
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("sym", [False, True])
+@pytest.mark.parametrize("g", [8, 32, 64])
+@pytest.mark.parametrize("act_order", [False, True])
+def test_numpy_oracle_matches_pure_python(sym, g, act_order):
+    N, K, M = 6, 128, 3
+    W = synth.weights_np(N, K, synth.seed_for("brute", N, K, g, sym, act_order))
+    x = synth.activations_np(M, K, 0.05, synth.seed_for("brute-x", g))
+    gidx = synth.act_order_g_idx(x, g) if act_order else None
+    y, B, (q, s, z), w_hat = O.w4a16_linear(x, W, g, sym, gidx)
+    Wl = W.astype(np.float64).tolist()
+    qb, sb, zb = brute.quantize(Wl, g, sym, None if gidx is None else gidx.tolist())
+    assert q.tolist() == qb
+    assert s.astype(np.float64).tolist() == sb
+    assert z.tolist() == zb
+    gl = (np.arange(K) // g).tolist() if gidx is None else gidx.tolist()
+    wb = brute.dequant(qb, sb, zb, gl)
+    assert w_hat.astype(np.float64).tolist() == wb
+    yb = np.array(brute.linear(x.astype(np.float64).tolist(), wb))
+    assert np.allclose(y, yb, rtol=1e-12, atol=1e-12)
+    assert np.all(B >= np.abs(y) - 1e-12)
+
+
+def test_exact_special_case_integer_weights():
+    """s = 1, z = 8 so w_hat = q - 8; x in {-1, 0, 1}: y is an exact integer."""
+    rng = np.random.default_rng(6)
+    N, K, M = 8, 256, 4
+    q = rng.integers(0, 16, (N, K)).astype(np.uint8)
+    s = np.ones((N, K // 128), dtype=np.float16)
+    z = np.full((N, K // 128), 8, dtype=np.uint8)
+    x = np.zeros((M, K), dtype=np.float16)
+    for m in range(M):
+        nz = rng.choice(K, 128, replace=False)
+        x[m, nz] = rng.choice([-1.0, 1.0], 128)
+    w_hat = O.dequant(q, s, z, 128)
+    assert np.array_equal(w_hat.astype(np.float64), q.astype(np.float64) - 8)
+    y, _ = O.linear_ref(x, w_hat)
+    expect = [[sum(int(x[m, k]) * (int(q[n, k]) - 8) for k in range(K)) for n in range(N)]
+              for m in range(M)]
+    assert np.array_equal(y, np.array(expect, dtype=np.float64))
+
+
+def test_linearity_in_x():
+    rng = np.random.default_rng(7)
+    W = synth.weights_np(16, 256, 11)
+    q, s, z = O.rtn_quantize(W, 128, False)
+    w_hat = O.dequant(q, s, z, 128)
+    x1 = rng.standard_normal((2, 256))
+    x2 = rng.standard_normal((2, 256))
+    y12, _ = O.linear_ref(x1 + x2, w_hat)
+    y1, _ = O.linear_ref(x1, w_hat)
+    y2, _ = O.linear_ref(x2, w_hat)
+    assert np.allclose(y12, y1 + y2, rtol=1e-12, atol=1e-12)
+
+
+def test_act_order_identity_map_equals_default():
+    W = synth.weights_np(8, 256, 12)
+    ident = (np.arange(256) // 64).astype(np.int32)
+    a = O.rtn_quantize(W, 64, False)
+    b = O.rtn_quantize(W, 64, False, ident)
+    for u, v in zip(a, b):
+        assert np.array_equal(u, v)
+
+
+def test_act_order_consistent_permutation_leaves_y_unchanged():
+    rng = np.random.default_rng(8)
+    W = synth.weights_np(8, 256, 13)
+    x = synth.activations_np(2, 256, 0.02, 14)
+    gidx = synth.act_order_g_idx(x, 64)
+    y, _, _, _ = O.w4a16_linear(x, W, 64, False, gidx)
+    p = rng.permutation(256)
+    yp, _, _, _ = O.w4a16_linear(x[:, p], W[:, p], 64, False, gidx[p])
+    assert np.allclose(y, yp, rtol=1e-12, atol=1e-13)
+
+
+def test_act_order_map_from_synthetic_hessian_diagonal():
+    x = np.zeros((2, 8), dtype=np.float16)
+    x[:, 5] = 10
+    x[:, 2] = 3
+    x[:, 7] = 3  # tie with column 2: lower index ranks first
+    x[:, 0] = 1
+    gi = synth.act_order_g_idx(x, 4)
+    # order by descending d: 5, 2, 7, 0, then 1, 3, 4, 6 (zeros, by index)
+    assert gi.tolist() == [0, 1, 0, 1, 1, 0, 1, 0]
+
+
+# ---------------------------------------------------------------------------
+# Planted mistakes: each mutant of the oracle must fail at least one pin
+# ---------------------------------------------------------------------------
+def _brute_agrees(quant_fn, deq_fn, lin_fn):
+    W = synth.weights_np(4, 64, 21)
+    x = synth.activations_np(2, 64, 0.05, 22)
+    q, s, z = quant_fn(W, 32, False)
+    w_hat = deq_fn(q, s, z, 32)
+    y, _ = lin_fn(x, w_hat)
+    qb, sb, zb = brute.quantize(W.astype(np.float64).tolist(), 32, False)
+    wb = brute.dequant(qb, sb, zb, (np.arange(64) // 32).tolist())
+    yb = np.array(brute.linear(x.astype(np.float64).tolist(), wb))
+    return (q.tolist() == qb and np.asarray(w_hat, np.float64).tolist() == wb
+            and np.shape(y) == yb.shape and np.allclose(y, yb, rtol=1e-12, atol=1e-12))
+
+
+def test_unmutated_oracle_agrees():
+    assert _brute_agrees(O.rtn_quantize, O.dequant, O.linear_ref)
+
+
+def test_mutant_dropped_zero_point_is_caught():
+    def deq(q, s, z, g):
+        return O.dequant(q, s, np.zeros_like(z), g)
+    assert not _brute_agrees(O.rtn_quantize, deq, O.linear_ref)
+
+
+def test_mutant_zero_point_sign_is_caught():
+    def quant(W, g, sym):
+        q, s, z = O.rtn_quantize(W, g, sym)
+        Wd = W.astype(np.float64)
+        mn = Wd.reshape(W.shape[0], -1, g).min(axis=2)
+        z2 = np.clip(np.rint(mn / s.astype(np.float64)), 0, 15).astype(np.uint8)
+        q2 = O.quantize_codes(Wd, np.repeat(s.astype(np.float64), g, 1), np.repeat(z2, g, 1))
+        return q2, s, z2
+    assert not _brute_agrees(quant, O.dequant, O.linear_ref)
+
+
+def test_mutant_transposed_operand_is_caught():
+    def lin(x, w_hat):
+        wt = np.asarray(w_hat, np.float64).reshape(-1)[: x.shape[1] * w_hat.shape[0]]
+        wt = wt.reshape(x.shape[1], w_hat.shape[0])  # K x N reinterpretation
+        return np.asarray(x, np.float64) @ wt, None
+    assert not _brute_agrees(O.rtn_quantize, O.dequant, lin)
+
+
+def test_mutant_missing_final_fp16_rounding_is_caught():
+    def deq(q, s, z, g):
+        gi = np.arange(q.shape[1]) // g
+        return (q.astype(np.float64) - z[:, gi]) * s.astype(np.float64)[:, gi]
+    assert not _brute_agrees(O.rtn_quantize, deq, O.linear_ref)
+
+
+def test_mutant_half_away_rounding_is_caught():
+    W = np.array([[-7.0, 8.0, 2.5, 3.5, -0.5, 0.5, -1.5, 1.5]], dtype=np.float16)
+    s = np.float64(1.0)
+    half_away = np.clip(np.sign(W / s) * np.floor(np.abs(W.astype(np.float64) / s) + 0.5) + 7, 0, 15)
+    q, _, _ = O.rtn_quantize(W, 8, False)
+    assert half_away.astype(np.uint8).tolist() != q.tolist()
+
+
+def test_mutant_reversed_nibble_order_is_caught():
+    codes = np.arange(8, dtype=np.uint8)[None, :]
+    good = int(O.pack_nibbles(codes)[0, 0])
+    rev = 0
+    for i, c in enumerate(codes[0]):
+        rev |= int(c) << (4 * (7 - i))
+    assert good == brute.pack_word(codes[0].tolist()) and rev != good
+
+
+def test_struct_half_rounding_is_the_ieee_one():
+    # struct 'e' must itself round to nearest even (independent of numpy)
+    assert struct.unpack("<e", struct.pack("<e", 2049.0))[0] == 2048.0
+    assert struct.unpack("<e", struct.pack("<e", 2051.0))[0] == 2052.0
+    assert struct.unpack("<e", struct.pack("<e", 1.0 + 2.0 ** -11))[0] == 1.0
