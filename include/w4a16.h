@@ -1,0 +1,224 @@
+/*
+ * w4a16.h -- C ABI of libw4a16.so: a W4A16 group-quantized linear layer for
+ * NVIDIA B300 (sm_103a).
+ *
+ * The layer computes y = x . W_hat^T, where W_hat[n][k] = (q[n][k] - z) * s:
+ * 4-bit codes q, one fp16 scale s and one 4-bit zero point z per (row, group)
+ * of `group_size` input columns, fp16 activations x and outputs y, fp32
+ * accumulation. The format follows "AWQ + GPTQ Quantization, in depth",
+ * section "What W4A16 buys and why decoding gets faster" (packed 4-bit weights
+ * expanded to 16 bits in registers with the group's scale and zero point; one
+ * scale per run of 128 consecutive input weights of a row) and "LLM
+ * Quantization: A Deep Dive into GPTQ, AWQ, and Post-Training Quantization",
+ * section "The Math of Quantization" (q = round(x/S) + Z, x ~ (q - Z) * S).
+ * The knobs -- bits, group_size, symmetric/zero point, act order (desc_act,
+ * g_idx) -- are those of the Q&A page "How do GPTQ and AWQ differ when
+ * quantizing Llama weights to 4 bits?", section "GPTQ: quantize then
+ * compensate".
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - Ownership: the caller allocates and frees every buffer. The library
+ *   allocates no memory and keeps no state besides a per-device cache of
+ *   device attributes.
+ * - Pointers are device pointers unless the argument says "host".
+ * - Every call is asynchronous on `stream` (a cudaStream_t; NULL = legacy
+ *   default stream) except where noted, and is reentrant.
+ * - Arguments are validated on the host before anything is launched; on any
+ *   error nothing is launched and nothing is written.
+ * - Unsupported combinations return W4A16_ERR_UNSUPPORTED; there is no slower
+ *   fallback path (a silent fallback is the failure mode named in "AWQ + GPTQ
+ *   Quantization, in depth", section "Failure modes": "Kernel fallback").
+ * - A failed CUDA launch returns W4A16_ERR_CUDA; w4a16_last_cuda_error() then
+ *   gives the cudaError_t (per calling thread). Nothing aborts, prints or traps.
+ * - Results are deterministic for a given (format, M, device): fixed reduction
+ *   order, no floating-point atomics.
+ *
+ * Element types: fp16 values are passed as uint16_t bit patterns (IEEE binary16).
+ */
+#ifndef W4A16_H
+#define W4A16_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define W4A16_API __attribute__((visibility("default")))
+#else
+#define W4A16_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st* w4a16_stream_t;
+
+typedef enum {
+  W4A16_OK = 0,
+  W4A16_ERR_INVALID_ARG = 1,     /* NULL pointer, bad size, M out of range, bad g_idx */
+  W4A16_ERR_UNSUPPORTED = 2,     /* valid but not implemented (bits != 4, group size, ...) */
+  W4A16_ERR_MISALIGNED = 3,      /* a pointer is not aligned as documented */
+  W4A16_ERR_BUFFER_TOO_SMALL = 4,/* packed_bytes or workspace_bytes below the requirement */
+  W4A16_ERR_CUDA = 5             /* a CUDA call failed; see w4a16_last_cuda_error() */
+} w4a16_status;
+
+/*
+ * Quantization format of one linear layer (out features N x in features K).
+ *   bits        must be 4.
+ *   group_size  32, 64 or 128; K must be a multiple of it (G = K / group_size
+ *               groups per row). 128 is the common default; smaller groups
+ *               track the weights more closely and cost more bits ("What W4A16
+ *               buys ...").
+ *   symmetric   0: asymmetric, one 4-bit zero point per (row, group);
+ *               1: symmetric, zero point fixed at 8, no zero points stored.
+ *   has_g_idx   0: column k belongs to group k / group_size;
+ *               1: GPTQ act order -- a column-to-group map g_idx is given at
+ *                  pack time ("The two algorithms, compactly": act order
+ *                  quantizes the columns with the largest activations first).
+ *   N, K        1 <= N <= 2^20, group_size <= K <= 2^20.
+ */
+typedef struct {
+  int32_t bits;
+  int32_t group_size;
+  int32_t symmetric;
+  int32_t has_g_idx;
+  int64_t N;
+  int64_t K;
+} w4a16_format;
+
+/*
+ * Packed blob (device memory, 256-byte aligned, produced by w4a16_pack).
+ * With NR = ceil(N / 128) row blocks, KB = ceil(K / 64) column blocks and
+ * G = K / group_size, it holds four sub-arrays, each starting on a 256-byte
+ * boundary, in this order:
+ *   qweight  NR*KB*4096 bytes: for every (row block, column block) a 4 KiB
+ *            tile of 128 rows x 64 columns of 4-bit codes, arranged so that a
+ *            warp's 16-byte loads yield tensor-core operand fragments.
+ *   scales   NR*G*256 bytes: fp16 scales, 128 rows per (row block, group).
+ *   zeros    NR*G*64 bytes (asymmetric only): 4-bit zero points.
+ *   perm     K*4 bytes (act order only): packed column -> original column.
+ * Rows beyond N and columns beyond K are padding. The blob's meaning is fixed
+ * by w4a16_dequant; its internal arrangement is private and may change.
+ */
+
+/* Bytes the packed blob needs for format f; 0 if f is invalid or unsupported. */
+W4A16_API size_t w4a16_packed_bytes(const w4a16_format* f);
+
+/* W4A16_OK if f is valid and supported, else the error w4a16_pack would return. */
+W4A16_API w4a16_status w4a16_check_format(const w4a16_format* f);
+
+/* Static, human-readable name of a status code. Never NULL. */
+W4A16_API const char* w4a16_status_string(w4a16_status s);
+
+/* cudaError_t of the calling thread's most recent W4A16_ERR_CUDA (0 if none). */
+W4A16_API int w4a16_last_cuda_error(void);
+
+/*
+ * Round-to-nearest group quantization of fp16 weights (the step before the
+ * path: "LLM Quantization: INT8, GPTQ, and AWQ Explained", section "What
+ * quantization actually does" -- find each group's range, pick the scale,
+ * round to the nearest grid point, clamp). Per (row n, group t), in fp64:
+ *   asymmetric: s = fp16_rne((max - min) / 15), z = clamp(rint(-min / s), 0, 15)
+ *   symmetric:  s = fp16_rne(2 * max|w| / 15),  z = 8
+ *   (s == 0 is replaced by 1.0), and q = clamp(rint(w / s) + z, 0, 15),
+ *   rint = round half to even.
+ *   w        fp16 [N][K] row-major, 16-byte aligned.
+ *   g_idx    HOST int32 [K] (act order) or NULL; group t's members are the
+ *            columns k with g_idx[k] == t, exactly group_size of them.
+ *   q        uint8 [N][K] codes 0..15, original column order.
+ *   scales   fp16 [N][G], 2-byte aligned.
+ *   zeros    uint8 [N][G]; must be NULL when f->symmetric.
+ *   workspace / workspace_bytes: >= w4a16_quantize_workspace_bytes(f)
+ *            (K*4 bytes for act order, else 0; may be NULL when 0),
+ *            16-byte aligned.
+ * With g_idx the call copies a host-built column list to the workspace with
+ * cudaMemcpyAsync from pageable memory, so it synchronises with the host.
+ */
+W4A16_API size_t w4a16_quantize_workspace_bytes(const w4a16_format* f);
+W4A16_API w4a16_status w4a16_quantize_rtn(const w4a16_format* f, const uint16_t* w,
+                                const int32_t* g_idx, uint8_t* q, uint16_t* scales,
+                                uint8_t* zeros, void* workspace, size_t workspace_bytes,
+                                w4a16_stream_t stream);
+
+/*
+ * Pack canonical codes, scales and zero points into the device blob.
+ *   q        uint8 [N][K], codes 0..15 (only the low 4 bits are used).
+ *   scales   fp16 [N][G], 2-byte aligned.
+ *   zeros    uint8 [N][G] codes 0..15 when asymmetric; NULL when symmetric.
+ *   g_idx    HOST int32 [K] when f->has_g_idx, else NULL. Every group
+ *            0..G-1 must have exactly group_size members (checked here);
+ *            the blob stores the columns sorted by group (stable), so that
+ *            each group is contiguous in the packed order.
+ *   packed / packed_bytes: 256-byte aligned, >= w4a16_packed_bytes(f).
+ * With g_idx the call copies the column order from pageable host memory
+ * (cudaMemcpyAsync), so it synchronises with the host.
+ */
+W4A16_API w4a16_status w4a16_pack(const w4a16_format* f, const uint8_t* q, const uint16_t* scales,
+                        const uint8_t* zeros, const int32_t* g_idx, void* packed,
+                        size_t packed_bytes, w4a16_stream_t stream);
+
+/*
+ * Expand the blob to fp16 weights: w_out[n][k] = fp16_rne((q - z) * s), in
+ * the original column order; bit-exact ("The Math of Quantization":
+ * x_approx = (q - Z) * S, rounded once to fp16).
+ *   w_out    fp16 [N][K] row-major, 16-byte aligned.
+ */
+W4A16_API w4a16_status w4a16_dequant(const w4a16_format* f, const void* packed, size_t packed_bytes,
+                           uint16_t* w_out, w4a16_stream_t stream);
+
+/*
+ * Decode-sized product y = x . W_hat^T for 1 <= M <= 16 tokens: every packed
+ * weight is read from HBM once, expanded in registers and multiplied on the
+ * tensor cores with fp32 accumulation ("What W4A16 buys ...": one token at
+ * batch one reads every weight once, about two flops per weight, so decode
+ * is bandwidth-bound).
+ *   x        fp16 [M][K] row-major, 16-byte aligned.
+ *   y        fp16 [M][N] row-major, 16-byte aligned; must not overlap x.
+ * Error per element is within 2e-3 * sum_k |x[m][k] * W_hat[n][k]| + 1e-3 of
+ * the exact product with the dequantized weights. M * K must be <= 2^19.
+ */
+W4A16_API w4a16_status w4a16_gemv(const w4a16_format* f, const void* packed, size_t packed_bytes,
+                        const uint16_t* x, uint16_t* y, int64_t M, w4a16_stream_t stream);
+
+/*
+ * Prefill-sized product y = x . W_hat^T for M >= 1 tokens on the tcgen05
+ * tensor cores (weights dequantized into tensor memory, fp32 accumulators in
+ * tensor memory). Same arguments and error bound as w4a16_gemv, plus
+ *   workspace / workspace_bytes: >= w4a16_gemm_workspace_bytes(f, M)
+ *            (the activations reordered to the packed column order when the
+ *            format has act order: M*K*2 bytes; else 0, may be NULL),
+ *            16-byte aligned.
+ * 1 <= M <= 2^20.
+ */
+W4A16_API size_t w4a16_gemm_workspace_bytes(const w4a16_format* f, int64_t M);
+W4A16_API w4a16_status w4a16_gemm(const w4a16_format* f, const void* packed, size_t packed_bytes,
+                        const uint16_t* x, uint16_t* y, int64_t M, void* workspace,
+                        size_t workspace_bytes, w4a16_stream_t stream);
+
+/*
+ * w4a16_gemv with options.
+ *   rows16   16-row tiles per CTA: 2, 4 or 8; 0 = default.
+ *   ksplit   CTAs per thread-block cluster splitting K: 1, 2, 4, 8 or 16;
+ *            0 = default.
+ *   flags    0 or W4A16_GEMV_WEIGHTS_READY.
+ * The GEMV kernels are launched with programmatic dependent launch, so a GEMV
+ * may start while the previous kernel on the stream is still running; by
+ * default it reads nothing from global memory before that kernel is done.
+ * W4A16_GEMV_WEIGHTS_READY promises that no kernel still in flight on the
+ * stream writes `packed` (true once the weights were packed before the
+ * preceding kernel started, as in a decode loop); the GEMV then starts
+ * streaming weights before the previous kernel finishes. `x` is always read
+ * after it. Results equal w4a16_gemv's up to summation order.
+ */
+#define W4A16_GEMV_WEIGHTS_READY 1u
+W4A16_API w4a16_status w4a16_gemv_ex(const w4a16_format* f, const void* packed, size_t packed_bytes,
+                           const uint16_t* x, uint16_t* y, int64_t M, int32_t rows16,
+                           int32_t ksplit, uint32_t flags, w4a16_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* W4A16_H */

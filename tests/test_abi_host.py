@@ -1,0 +1,159 @@
+"""Host-side tests of the C ABI: the library loads, exports every declared
+symbol, and rejects bad arguments before touching the GPU. No GPU needed."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from oracle import w4a16_oracle as O
+from weight_only_bit_04_b300 import w4a16 as W
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "w4a16.h")
+
+OK, INVALID, UNSUPPORTED, MISALIGNED, SMALL = 0, 1, 2, 3, 4
+FAKE = 0x10000  # aligned, never dereferenced: every call below fails validation first
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"W4A16_API\s+[\w\s\*]+?\b(w4a16_\w+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from weight_only_bit_04_b300 import build
+    build.build()
+    return W.lib()
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for required in ("w4a16_pack", "w4a16_dequant", "w4a16_gemv", "w4a16_gemm"):
+        assert required in names
+    assert set(names) == set(W.SIGNATURES)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def fmt(N=256, K=512, g=128, sym=False, act=False, bits=4):
+    return W.make_format(N, K, g, sym, act, bits)
+
+
+def test_packed_bytes_layout(lib):
+    f = fmt(4096, 4096)
+    nr, kb, G = 32, 64, 32
+    q = nr * kb * 4096
+    s = nr * G * 256
+    z = nr * G * 64
+    assert W.packed_bytes(f) == q + s + z  # all multiples of 256
+    # For N a multiple of 128 the blob is exactly the closed-form byte count.
+    assert W.packed_bytes(f) == O.packed_bytes_closed_form(4096, 4096, 128, False)
+    assert W.packed_bytes(fmt(4096, 4096, sym=True)) == O.packed_bytes_closed_form(4096, 4096, 128, True)
+    fa = fmt(4096, 4096, act=True)
+    assert W.packed_bytes(fa) == q + s + z + 4096 * 4
+    # padding rows / columns are counted
+    # (zeros: 2*3*64 = 384 bytes, the blob end is rounded up to 256)
+    assert W.packed_bytes(fmt(200, 96, g=32)) == 2 * 2 * 4096 + 2 * 3 * 256 + 512
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(bits=8), UNSUPPORTED),
+    (dict(bits=3), UNSUPPORTED),
+    (dict(g=16), UNSUPPORTED),
+    (dict(g=256), UNSUPPORTED),
+    (dict(K=96, g=64), UNSUPPORTED),   # ragged last group
+    (dict(N=0), INVALID),
+    (dict(K=0), INVALID),
+    (dict(N=(1 << 20) + 1), INVALID),
+])
+def test_bad_formats(lib, kw, status):
+    f = fmt(**kw)
+    assert W.check_format(f) == status
+    assert W.packed_bytes(f) == 0
+
+
+def test_status_strings(lib):
+    for code, name in W.STATUS.items():
+        assert lib.w4a16_status_string(code).decode() == name
+    assert lib.w4a16_status_string(99).decode() == "W4A16_ERR_UNKNOWN"
+
+
+def _call(lib, name, *args):
+    return getattr(lib, name)(*args)
+
+
+def test_pack_argument_checks(lib):
+    f = fmt()
+    nb = W.packed_bytes(f)
+    r = lambda *a: _call(lib, "w4a16_pack", ctypes.byref(f), *a)
+    assert r(None, FAKE, FAKE, None, FAKE, nb, None) == INVALID        # q NULL
+    assert r(FAKE, FAKE, None, None, FAKE, nb, None) == INVALID        # zeros NULL (asym)
+    assert r(FAKE, FAKE, FAKE, None, FAKE + 16, nb, None) == MISALIGNED
+    assert r(FAKE, FAKE + 1, FAKE, None, FAKE, nb, None) == MISALIGNED
+    assert r(FAKE, FAKE, FAKE, None, FAKE, nb - 1, None) == SMALL
+    fs = fmt(sym=True)
+    assert _call(lib, "w4a16_pack", ctypes.byref(fs), FAKE, FAKE, FAKE, None, FAKE,
+                 W.packed_bytes(fs), None) == INVALID                  # zeros given (sym)
+    fa = fmt(act=True)
+    nba = W.packed_bytes(fa)
+    assert _call(lib, "w4a16_pack", ctypes.byref(fa), FAKE, FAKE, FAKE, None, FAKE, nba,
+                 None) == INVALID                                     # g_idx missing
+
+
+def test_pack_rejects_bad_g_idx_on_host(lib):
+    f = fmt(N=8, K=256, g=128, act=True)
+    nb = W.packed_bytes(f)
+    bad = (ctypes.c_int32 * 256)(*([0] * 129 + [1] * 127))            # group 0 has 129 members
+    assert lib.w4a16_pack(ctypes.byref(f), FAKE, FAKE, FAKE, bad, FAKE, nb, None) == INVALID
+    oob = (ctypes.c_int32 * 256)(*([0] * 128 + [2] * 128))
+    assert lib.w4a16_pack(ctypes.byref(f), FAKE, FAKE, FAKE, oob, FAKE, nb, None) == INVALID
+
+
+def test_gemv_argument_checks(lib):
+    f = fmt()
+    nb = W.packed_bytes(f)
+    g = lambda packed, nbytes, x, y, M: lib.w4a16_gemv(ctypes.byref(f), packed, nbytes, x, y, M, None)
+    X, Y = FAKE * 16, FAKE * 64
+    assert g(None, nb, X, Y, 1) == INVALID
+    assert g(FAKE, nb, X, Y, 0) == INVALID
+    assert g(FAKE, nb, X, Y, 17) == INVALID
+    assert g(FAKE, nb - 1, X, Y, 1) == SMALL
+    assert g(FAKE + 128, nb, X, Y, 1) == MISALIGNED
+    assert g(FAKE, nb, X + 2, Y, 1) == MISALIGNED
+    assert g(FAKE, nb, X, Y + 8, 1) == MISALIGNED
+    assert g(FAKE, nb, X, X, 1) == INVALID                              # y overlaps x
+    bad = fmt(bits=2)
+    assert lib.w4a16_gemv(ctypes.byref(bad), FAKE, nb, X, Y, 1, None) == UNSUPPORTED
+    # explicit launch shapes are validated too
+    assert lib.w4a16_gemv_ex(ctypes.byref(f), FAKE, nb, X, Y, 1, 3, 1, 0, None) == INVALID
+    assert lib.w4a16_gemv_ex(ctypes.byref(f), FAKE, nb, X, Y, 1, 8, 32, 0, None) == INVALID
+    assert lib.w4a16_gemv_ex(ctypes.byref(f), FAKE, nb, X, Y, 1, 0, 0, 2, None) == INVALID
+
+
+def test_gemm_and_workspace_checks(lib):
+    f = fmt(act=True)
+    nb = W.packed_bytes(f)
+    assert lib.w4a16_gemm_workspace_bytes(ctypes.byref(f), 2048) == 2048 * 512 * 2
+    assert lib.w4a16_gemm_workspace_bytes(ctypes.byref(fmt()), 2048) == 0
+    X, Y = FAKE * 16, FAKE * 4096
+    assert lib.w4a16_gemm(ctypes.byref(f), FAKE, nb, X, Y, 2048, None, 0, None) == SMALL
+    assert lib.w4a16_gemm(ctypes.byref(f), FAKE, nb, X, Y, 0, None, 0, None) == INVALID
+    assert lib.w4a16_gemm(ctypes.byref(f), FAKE, nb, X, Y, 2048, FAKE + 4, 2048 * 1024,
+                          None) == MISALIGNED
+    assert lib.w4a16_quantize_workspace_bytes(ctypes.byref(f)) == 512 * 4
+    assert lib.w4a16_quantize_rtn(ctypes.byref(f), FAKE, None, FAKE, FAKE, FAKE, FAKE, 2048,
+                                  None) == INVALID                    # g_idx missing
+
+
+def test_dequant_checks(lib):
+    f = fmt()
+    nb = W.packed_bytes(f)
+    assert lib.w4a16_dequant(ctypes.byref(f), FAKE, nb, None, None) == INVALID
+    assert lib.w4a16_dequant(ctypes.byref(f), FAKE, nb, FAKE + 2, None) == MISALIGNED
+    assert lib.w4a16_dequant(ctypes.byref(f), FAKE, 10, FAKE, None) == SMALL

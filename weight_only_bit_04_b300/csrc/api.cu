@@ -1,0 +1,249 @@
+// C ABI of libw4a16.so: argument validation on the host, then one launch on
+// the caller's stream. See include/w4a16.h for the contract of each call.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <atomic>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "internal.h"
+
+namespace w4a16 {
+namespace {
+
+thread_local int g_last_cuda_error = 0;
+
+w4a16_status cuda_fail(cudaError_t e) {
+  g_last_cuda_error = int(e);
+  return W4A16_ERR_CUDA;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+constexpr int kMaxDevices = 64;
+std::once_flag g_dev_once[kMaxDevices];
+DeviceInfo g_dev[kMaxDevices];
+cudaError_t g_dev_err[kMaxDevices];
+
+w4a16_status format_status(const w4a16_format* f) {
+  if (f == nullptr) return W4A16_ERR_INVALID_ARG;
+  if (f->symmetric != 0 && f->symmetric != 1) return W4A16_ERR_INVALID_ARG;
+  if (f->has_g_idx != 0 && f->has_g_idx != 1) return W4A16_ERR_INVALID_ARG;
+  if (f->N < 1 || f->K < 1 || f->N > (int64_t(1) << 20) || f->K > (int64_t(1) << 20))
+    return W4A16_ERR_INVALID_ARG;
+  if (f->bits != 4) return W4A16_ERR_UNSUPPORTED;
+  if (f->group_size != 32 && f->group_size != 64 && f->group_size != 128) return W4A16_ERR_UNSUPPORTED;
+  if (f->K % f->group_size != 0) return W4A16_ERR_UNSUPPORTED;  // no ragged last group
+  return W4A16_OK;
+}
+
+// Common checks for calls that read a packed blob.
+w4a16_status blob_status(const w4a16_format* f, const void* packed, size_t packed_bytes) {
+  w4a16_status s = format_status(f);
+  if (s != W4A16_OK) return s;
+  if (packed == nullptr) return W4A16_ERR_INVALID_ARG;
+  if (!aligned(packed, 256)) return W4A16_ERR_MISALIGNED;
+  if (packed_bytes < make_layout(*f).total) return W4A16_ERR_BUFFER_TOO_SMALL;
+  return W4A16_OK;
+}
+
+// Host-side group map check and the stable group-sorted column order.
+bool build_perm(const w4a16_format& f, const int32_t* g_idx, std::vector<int32_t>& perm) {
+  const int64_t K = f.K, G = f.K / f.group_size;
+  std::vector<int64_t> count(static_cast<size_t>(G), 0);
+  for (int64_t k = 0; k < K; ++k) {
+    const int32_t t = g_idx[k];
+    if (t < 0 || t >= G) return false;
+    ++count[size_t(t)];
+  }
+  for (int64_t t = 0; t < G; ++t)
+    if (count[size_t(t)] != f.group_size) return false;
+  perm.resize(size_t(K));
+  std::vector<int64_t> next_slot(static_cast<size_t>(G));
+  for (int64_t t = 0; t < G; ++t) next_slot[size_t(t)] = t * f.group_size;
+  for (int64_t k = 0; k < K; ++k) perm[size_t(next_slot[size_t(g_idx[k])]++)] = int32_t(k);
+  return true;
+}
+
+}  // namespace
+
+cudaError_t device_info(DeviceInfo* out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::call_once(g_dev_once[dev], [dev]() {
+    DeviceInfo d{};
+    cudaError_t err = cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev);
+    if (err == cudaSuccess)
+      err = cudaDeviceGetAttribute(&d.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    if (err == cudaSuccess) err = cudaDeviceGetAttribute(&d.cc_major, cudaDevAttrComputeCapabilityMajor, dev);
+    if (err == cudaSuccess) err = cudaDeviceGetAttribute(&d.cc_minor, cudaDevAttrComputeCapabilityMinor, dev);
+    g_dev[dev] = d;
+    g_dev_err[dev] = err;
+  });
+  if (g_dev_err[dev] != cudaSuccess) return g_dev_err[dev];
+  *out = g_dev[dev];
+  return cudaSuccess;
+}
+
+}  // namespace w4a16
+
+using namespace w4a16;
+
+extern "C" {
+
+size_t w4a16_packed_bytes(const w4a16_format* f) {
+  if (format_status(f) != W4A16_OK) return 0;
+  return make_layout(*f).total;
+}
+
+w4a16_status w4a16_check_format(const w4a16_format* f) { return format_status(f); }
+
+const char* w4a16_status_string(w4a16_status s) {
+  switch (s) {
+    case W4A16_OK: return "W4A16_OK";
+    case W4A16_ERR_INVALID_ARG: return "W4A16_ERR_INVALID_ARG";
+    case W4A16_ERR_UNSUPPORTED: return "W4A16_ERR_UNSUPPORTED";
+    case W4A16_ERR_MISALIGNED: return "W4A16_ERR_MISALIGNED";
+    case W4A16_ERR_BUFFER_TOO_SMALL: return "W4A16_ERR_BUFFER_TOO_SMALL";
+    case W4A16_ERR_CUDA: return "W4A16_ERR_CUDA";
+  }
+  return "W4A16_ERR_UNKNOWN";
+}
+
+int w4a16_last_cuda_error(void) { return g_last_cuda_error; }
+
+size_t w4a16_quantize_workspace_bytes(const w4a16_format* f) {
+  if (format_status(f) != W4A16_OK) return 0;
+  return f->has_g_idx ? size_t(f->K) * 4 : 0;
+}
+
+w4a16_status w4a16_quantize_rtn(const w4a16_format* f, const uint16_t* w, const int32_t* g_idx,
+                                uint8_t* q, uint16_t* scales, uint8_t* zeros, void* workspace,
+                                size_t workspace_bytes, w4a16_stream_t stream) {
+  w4a16_status s = format_status(f);
+  if (s != W4A16_OK) return s;
+  if (w == nullptr || q == nullptr || scales == nullptr) return W4A16_ERR_INVALID_ARG;
+  if ((zeros == nullptr) != (f->symmetric != 0)) return W4A16_ERR_INVALID_ARG;
+  if ((g_idx == nullptr) != (f->has_g_idx == 0)) return W4A16_ERR_INVALID_ARG;
+  if (!aligned(w, 16) || !aligned(scales, 2)) return W4A16_ERR_MISALIGNED;
+  const size_t need = f->has_g_idx ? size_t(f->K) * 4 : 0;
+  if (workspace_bytes < need) return W4A16_ERR_BUFFER_TOO_SMALL;
+  if (need > 0 && workspace == nullptr) return W4A16_ERR_INVALID_ARG;
+  if (need > 0 && !aligned(workspace, 16)) return W4A16_ERR_MISALIGNED;
+  const Layout L = make_layout(*f);
+  const int32_t* perm_dev = nullptr;
+  if (f->has_g_idx) {
+    std::vector<int32_t> perm;
+    if (!build_perm(*f, g_idx, perm)) return W4A16_ERR_INVALID_ARG;
+    cudaError_t e = cudaMemcpyAsync(workspace, perm.data(), need, cudaMemcpyHostToDevice, stream);
+    if (e != cudaSuccess) return cuda_fail(e);
+    perm_dev = static_cast<const int32_t*>(workspace);
+  }
+  cudaError_t e = launch_quantize_rtn(L, w, perm_dev, q, scales, zeros, stream);
+  return e == cudaSuccess ? W4A16_OK : cuda_fail(e);
+}
+
+w4a16_status w4a16_pack(const w4a16_format* f, const uint8_t* q, const uint16_t* scales,
+                        const uint8_t* zeros, const int32_t* g_idx, void* packed, size_t packed_bytes,
+                        w4a16_stream_t stream) {
+  w4a16_status s = format_status(f);
+  if (s != W4A16_OK) return s;
+  if (q == nullptr || scales == nullptr || packed == nullptr) return W4A16_ERR_INVALID_ARG;
+  if ((zeros == nullptr) != (f->symmetric != 0)) return W4A16_ERR_INVALID_ARG;
+  if ((g_idx == nullptr) != (f->has_g_idx == 0)) return W4A16_ERR_INVALID_ARG;
+  if (!aligned(packed, 256) || !aligned(scales, 2)) return W4A16_ERR_MISALIGNED;
+  const Layout L = make_layout(*f);
+  if (packed_bytes < L.total) return W4A16_ERR_BUFFER_TOO_SMALL;
+  if (f->has_g_idx) {
+    std::vector<int32_t> perm;
+    if (!build_perm(*f, g_idx, perm)) return W4A16_ERR_INVALID_ARG;
+    cudaError_t e = cudaMemcpyAsync(static_cast<char*>(packed) + L.p_off, perm.data(), L.p_bytes,
+                                    cudaMemcpyHostToDevice, stream);
+    if (e != cudaSuccess) return cuda_fail(e);
+  }
+  cudaError_t e = launch_pack(L, q, scales, zeros, packed, stream);
+  return e == cudaSuccess ? W4A16_OK : cuda_fail(e);
+}
+
+w4a16_status w4a16_dequant(const w4a16_format* f, const void* packed, size_t packed_bytes,
+                           uint16_t* w_out, w4a16_stream_t stream) {
+  w4a16_status s = blob_status(f, packed, packed_bytes);
+  if (s != W4A16_OK) return s;
+  if (w_out == nullptr) return W4A16_ERR_INVALID_ARG;
+  if (!aligned(w_out, 16)) return W4A16_ERR_MISALIGNED;
+  cudaError_t e = launch_dequant(make_layout(*f), packed, w_out, stream);
+  return e == cudaSuccess ? W4A16_OK : cuda_fail(e);
+}
+
+static w4a16_status gemv_common(const w4a16_format* f, const void* packed, size_t packed_bytes,
+                                const uint16_t* x, uint16_t* y, int64_t M, int32_t rows16,
+                                int32_t ksplit, uint32_t flags, w4a16_stream_t stream) {
+  w4a16_status s = blob_status(f, packed, packed_bytes);
+  if (s != W4A16_OK) return s;
+  if (x == nullptr || y == nullptr) return W4A16_ERR_INVALID_ARG;
+  if (M < 1 || M > 16) return W4A16_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(y, 16)) return W4A16_ERR_MISALIGNED;
+  const char* xb = reinterpret_cast<const char*>(x);
+  const char* yb = reinterpret_cast<const char*>(y);
+  const size_t xbytes = size_t(M) * size_t(f->K) * 2, ybytes = size_t(M) * size_t(f->N) * 2;
+  if (xb < yb + ybytes && yb < xb + xbytes) return W4A16_ERR_INVALID_ARG;  // overlap
+  if (M * f->K > (int64_t(1) << 19)) return W4A16_ERR_UNSUPPORTED;
+  if (rows16 != 0 && rows16 != 2 && rows16 != 4 && rows16 != 8) return W4A16_ERR_INVALID_ARG;
+  if (ksplit != 0 && ksplit != 1 && ksplit != 2 && ksplit != 4 && ksplit != 8 && ksplit != 16)
+    return W4A16_ERR_INVALID_ARG;
+  if ((flags & ~uint32_t(W4A16_GEMV_WEIGHTS_READY)) != 0) return W4A16_ERR_INVALID_ARG;
+  const Layout L = make_layout(*f);
+  DeviceInfo dev;
+  cudaError_t e = device_info(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  GemvPlan plan = gemv_default_plan(L, int(M), dev);
+  if (rows16 != 0) plan.rows16 = rows16;
+  if (ksplit != 0) plan.ksplit = ksplit;
+  if (!gemv_plan_ok(L, int(M), plan)) return (rows16 || ksplit) ? W4A16_ERR_INVALID_ARG : W4A16_ERR_UNSUPPORTED;
+  e = launch_gemv(L, packed, x, y, int(M), plan, flags, stream);
+  return e == cudaSuccess ? W4A16_OK : cuda_fail(e);
+}
+
+w4a16_status w4a16_gemv(const w4a16_format* f, const void* packed, size_t packed_bytes,
+                        const uint16_t* x, uint16_t* y, int64_t M, w4a16_stream_t stream) {
+  return gemv_common(f, packed, packed_bytes, x, y, M, 0, 0, 0, stream);
+}
+
+w4a16_status w4a16_gemv_ex(const w4a16_format* f, const void* packed, size_t packed_bytes,
+                           const uint16_t* x, uint16_t* y, int64_t M, int32_t rows16, int32_t ksplit,
+                           uint32_t flags, w4a16_stream_t stream) {
+  return gemv_common(f, packed, packed_bytes, x, y, M, rows16, ksplit, flags, stream);
+}
+
+size_t w4a16_gemm_workspace_bytes(const w4a16_format* f, int64_t M) {
+  if (format_status(f) != W4A16_OK || M < 1) return 0;
+  return f->has_g_idx ? size_t(M) * size_t(f->K) * 2 : 0;
+}
+
+w4a16_status w4a16_gemm(const w4a16_format* f, const void* packed, size_t packed_bytes,
+                        const uint16_t* x, uint16_t* y, int64_t M, void* workspace,
+                        size_t workspace_bytes, w4a16_stream_t stream) {
+  w4a16_status s = blob_status(f, packed, packed_bytes);
+  if (s != W4A16_OK) return s;
+  if (x == nullptr || y == nullptr) return W4A16_ERR_INVALID_ARG;
+  if (M < 1 || M > (int64_t(1) << 20)) return W4A16_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(y, 16)) return W4A16_ERR_MISALIGNED;
+  const size_t xbytes = size_t(M) * size_t(f->K) * 2, ybytes = size_t(M) * size_t(f->N) * 2;
+  const char* xb = reinterpret_cast<const char*>(x);
+  const char* yb = reinterpret_cast<const char*>(y);
+  if (xb < yb + ybytes && yb < xb + xbytes) return W4A16_ERR_INVALID_ARG;
+  const size_t need = w4a16_gemm_workspace_bytes(f, M);
+  if (workspace_bytes < need) return W4A16_ERR_BUFFER_TOO_SMALL;
+  if (need > 0 && workspace == nullptr) return W4A16_ERR_INVALID_ARG;
+  if (need > 0 && !aligned(workspace, 16)) return W4A16_ERR_MISALIGNED;
+  cudaError_t e = launch_gemm(make_layout(*f), packed, x, y, M, workspace, stream);
+  if (e == cudaErrorNotSupported) return W4A16_ERR_UNSUPPORTED;
+  return e == cudaSuccess ? W4A16_OK : cuda_fail(e);
+}
+
+}  // extern "C"

@@ -1,0 +1,42 @@
+// Launchers implemented in the kernel files and called by the C ABI (api.cu).
+// Every launcher only enqueues work on `stream` and returns the launch status.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include "layout.h"
+
+namespace w4a16 {
+
+// Device attributes cached per device.
+struct DeviceInfo {
+  int sm_count;
+  int max_smem_optin;
+  int cc_major, cc_minor;
+};
+cudaError_t device_info(DeviceInfo* out);
+
+cudaError_t launch_quantize_rtn(const Layout& L, const uint16_t* w, const int32_t* perm_dev,
+                                uint8_t* q, uint16_t* scales, uint8_t* zeros,
+                                cudaStream_t stream);
+
+cudaError_t launch_pack(const Layout& L, const uint8_t* q, const uint16_t* scales,
+                        const uint8_t* zeros, void* blob, cudaStream_t stream);
+
+cudaError_t launch_dequant(const Layout& L, const void* blob, uint16_t* w_out,
+                           cudaStream_t stream);
+
+struct GemvPlan {
+  int rows16;   // 16-row tiles per CTA (1, 2, 4, 8)
+  int ksplit;   // CTAs per cluster along K
+};
+GemvPlan gemv_default_plan(const Layout& L, int M, const DeviceInfo& dev);
+bool gemv_plan_ok(const Layout& L, int M, const GemvPlan& p);
+constexpr uint32_t kGemvWeightsReady = W4A16_GEMV_WEIGHTS_READY;
+cudaError_t launch_gemv(const Layout& L, const void* blob, const uint16_t* x, uint16_t* y,
+                        int M, const GemvPlan& plan, uint32_t flags, cudaStream_t stream);
+
+cudaError_t launch_gemm(const Layout& L, const void* blob, const uint16_t* x, uint16_t* y,
+                        int64_t M, void* workspace, cudaStream_t stream);
+
+}  // namespace w4a16

@@ -1,0 +1,213 @@
+// One-shot kernels around the hot path: round-to-nearest quantization,
+// packing into the device blob, and bit-exact dequantization.
+//
+// Quantization follows "LLM Quantization: INT8, GPTQ, and AWQ Explained",
+// section "What quantization actually does" (find the range, pick the scale,
+// round to the nearest grid point, clamp) with the linear formula
+// q = round(w / s) + z of "LLM Quantization: A Deep Dive into GPTQ, AWQ, and
+// Post-Training Quantization", section "The Math of Quantization"; groups of
+// input columns per "AWQ + GPTQ Quantization, in depth", section "What W4A16
+// buys and why decoding gets faster".
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include "device_util.cuh"
+#include "internal.h"
+
+namespace w4a16 {
+namespace {
+
+// ---------------------------------------------------------------------------
+// Round-to-nearest quantization: one warp per (row, group).
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) quantize_rtn_kernel(Layout L, const uint16_t* __restrict__ w,
+                                                           const int32_t* __restrict__ perm,
+                                                           uint8_t* __restrict__ q,
+                                                           uint16_t* __restrict__ scales,
+                                                           uint8_t* __restrict__ zeros) {
+  const int lane = threadIdx.x & 31;
+  const int64_t item = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  if (item >= L.N * L.G) return;
+  const int64_t n = item / L.G;
+  const int64_t t = item - n * L.G;
+  const int gs = L.gsize;
+  const int per_lane = gs / 32;  // 1, 2 or 4 members per lane
+
+  int64_t col[4];
+  float v[4];
+  float mn = INFINITY, mx = -INFINITY, amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    if (i < per_lane) {
+      const int64_t p = t * gs + i * 32 + lane;  // position in group-sorted order
+      col[i] = perm ? perm[p] : p;
+      v[i] = __half2float(__ushort_as_half(w[n * L.K + col[i]]));
+      mn = fminf(mn, v[i]);
+      mx = fmaxf(mx, v[i]);
+      amax = fmaxf(amax, fabsf(v[i]));
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  }
+  // fp64 from here on; every fp16 value and difference of two is exact in fp64.
+  double range = L.sym ? 2.0 * double(amax) : double(mx) - double(mn);
+  __half s_h = __double2half(range / 15.0);  // round to nearest even
+  if (__half2float(s_h) == 0.0f) s_h = __float2half(1.0f);
+  const double s = double(__half2float(s_h));
+  double z;
+  if (L.sym) {
+    z = 8.0;
+  } else {
+    z = rint(-double(mn) / s);
+    z = fmin(fmax(z, 0.0), 15.0);
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    if (i < per_lane) {
+      double c = rint(double(v[i]) / s) + z;
+      c = fmin(fmax(c, 0.0), 15.0);
+      q[n * L.K + col[i]] = uint8_t(c);
+    }
+  }
+  if (lane == 0) {
+    scales[n * L.G + t] = __half_as_ushort(s_h);
+    if (zeros) zeros[n * L.G + t] = uint8_t(z);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Packing: one thread per 32-bit word of the qweight tiles.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) pack_qweight_kernel(Layout L, const uint8_t* __restrict__ q,
+                                                           const int32_t* __restrict__ perm,
+                                                           uint32_t* __restrict__ qweight) {
+  const int64_t wi = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (wi >= L.NR * L.KB * kTileWords) return;
+  const int64_t tile = wi / kTileWords;
+  const int within = int(wi - tile * kTileWords);
+  const int64_t R = tile / L.KB;
+  const int64_t b = tile - R * L.KB;
+  const int r16 = within >> 7;
+  const int lane = (within >> 2) & 31;
+  const int j = within & 3;
+  const int g = lane >> 2, t = lane & 3;
+  const int64_t n0 = R * kRowsPerBlock + r16 * 16 + g;
+  const int64_t p0 = b * kColsPerBlock + j * 16 + 4 * t;
+  uint32_t word = 0;
+#pragma unroll
+  for (int kk = 0; kk < 4; ++kk) {
+    const int64_t p = p0 + kk;
+    if (p >= L.K) continue;
+    const int64_t c = perm ? perm[p] : p;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int64_t n = n0 + 8 * h;
+      if (n < L.N) word |= uint32_t(q[n * L.K + c] & 0xF) << (4 * nibble_index(kk, h));
+    }
+  }
+  qweight[wi] = word;
+}
+
+// One thread per (row block, group, 16-row tile, lane group): a scale pair and a zero byte.
+__global__ void __launch_bounds__(256) pack_meta_kernel(Layout L, const uint16_t* __restrict__ scales,
+                                                        const uint8_t* __restrict__ zeros,
+                                                        uint32_t* __restrict__ s_out,
+                                                        uint8_t* __restrict__ z_out) {
+  const int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= L.NR * L.G * 64) return;
+  const int g = int(i & 7);
+  const int r16 = int((i >> 3) & 7);
+  const int64_t rg = i >> 6;  // R * G + gi
+  const int64_t R = rg / L.G;
+  const int64_t gi = rg - R * L.G;
+  const int64_t n0 = R * kRowsPerBlock + r16 * 16 + g;
+  const int64_t n1 = n0 + 8;
+  const uint32_t s0 = n0 < L.N ? scales[n0 * L.G + gi] : 0u;
+  const uint32_t s1 = n1 < L.N ? scales[n1 * L.G + gi] : 0u;
+  s_out[i] = s0 | (s1 << 16);
+  if (z_out) {
+    const uint32_t z0 = n0 < L.N ? (zeros[n0 * L.G + gi] & 0xF) : 0u;
+    const uint32_t z1 = n1 < L.N ? (zeros[n1 * L.G + gi] & 0xF) : 0u;
+    z_out[i] = uint8_t(z0 | (z1 << 4));
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Dequantization: one thread per packed word, w_hat = fp16_rne((q - z) * s).
+// (1024 + q) - (1024 + z) is exact in fp16, the product is rounded once.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) dequant_kernel(Layout L, BlobView B, uint16_t* __restrict__ out) {
+  const int64_t wi = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (wi >= L.NR * L.KB * kTileWords) return;
+  const int64_t tile = wi / kTileWords;
+  const int within = int(wi - tile * kTileWords);
+  const int64_t R = tile / L.KB;
+  const int64_t b = tile - R * L.KB;
+  const int r16 = within >> 7;
+  const int lane = (within >> 2) & 31;
+  const int j = within & 3;
+  const int g = lane >> 2, t = lane & 3;
+  const int64_t n0 = R * kRowsPerBlock + r16 * 16 + g;
+  const int64_t p0 = b * kColsPerBlock + j * 16 + 4 * t;
+  const uint32_t word = B.qweight[wi];
+#pragma unroll
+  for (int kk = 0; kk < 4; ++kk) {
+    const int64_t p = p0 + kk;
+    if (p >= L.K) continue;
+    const int64_t gi = p / L.gsize;
+    const int64_t mi = ((R * L.G + gi) * 8 + r16) * 8 + g;
+    const int64_t c = B.perm ? B.perm[p] : p;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int64_t n = n0 + 8 * h;
+      if (n >= L.N) continue;
+      const uint32_t code = (word >> (4 * nibble_index(kk, h))) & 0xF;
+      const uint32_t z = B.zeros ? ((B.zeros[mi] >> (4 * h)) & 0xF) : 8u;
+      const __half s = __ushort_as_half(B.scales[2 * mi + h]);
+      const __half d = __hsub(__ushort_as_half(uint16_t(0x6400u | code)),
+                              __ushort_as_half(uint16_t(0x6400u | z)));
+      out[n * L.K + c] = __half_as_ushort(__hmul(d, s));
+    }
+  }
+}
+
+inline unsigned blocks_for(int64_t threads, int per_block) {
+  return unsigned((threads + per_block - 1) / per_block);
+}
+
+}  // namespace
+
+cudaError_t launch_quantize_rtn(const Layout& L, const uint16_t* w, const int32_t* perm_dev,
+                                uint8_t* q, uint16_t* scales, uint8_t* zeros, cudaStream_t stream) {
+  const int64_t threads = L.N * L.G * 32;
+  quantize_rtn_kernel<<<blocks_for(threads, 256), 256, 0, stream>>>(L, w, perm_dev, q, scales, zeros);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_pack(const Layout& L, const uint8_t* q, const uint16_t* scales,
+                        const uint8_t* zeros, void* blob, cudaStream_t stream) {
+  char* b = static_cast<char*>(blob);
+  const int32_t* perm = L.act ? reinterpret_cast<const int32_t*>(b + L.p_off) : nullptr;
+  const int64_t words = L.NR * L.KB * kTileWords;
+  pack_qweight_kernel<<<blocks_for(words, 256), 256, 0, stream>>>(
+      L, q, perm, reinterpret_cast<uint32_t*>(b + L.q_off));
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const int64_t metas = L.NR * L.G * 64;
+  pack_meta_kernel<<<blocks_for(metas, 256), 256, 0, stream>>>(
+      L, scales, L.sym ? nullptr : zeros, reinterpret_cast<uint32_t*>(b + L.s_off),
+      L.sym ? nullptr : reinterpret_cast<uint8_t*>(b + L.z_off));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dequant(const Layout& L, const void* blob, uint16_t* w_out, cudaStream_t stream) {
+  const int64_t words = L.NR * L.KB * kTileWords;
+  dequant_kernel<<<blocks_for(words, 256), 256, 0, stream>>>(L, view_of(L, blob), w_out);
+  return cudaGetLastError();
+}
+
+}  // namespace w4a16

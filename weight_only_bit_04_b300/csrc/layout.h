@@ -1,0 +1,87 @@
+// Device layout of the packed W4A16 blob, shared by the host API and the kernels.
+//
+// The blob holds, each on a 256-byte boundary:
+//   qweight  [NR][KB] tiles of 4096 bytes (128 rows x 64 columns of 4-bit codes)
+//   scales   [NR][G][8 r16][8 g][2] fp16: for 16-row tile r16 and lane group g
+//            the pair (row r16*16+g, row r16*16+g+8)
+//   zeros    [NR][G][8 r16][8 g] bytes: low nibble row r16*16+g, high nibble
+//            row r16*16+g+8 (asymmetric formats only)
+//   perm     [K] int32: packed column -> original column (act order only)
+//
+// Inside a 4096-byte tile the 1024 32-bit words are ordered [r16 (8)][lane (32)][j (4)]:
+// lane L = 4*g + t of the warp owning 16-row tile r16 loads its four words (j = 0..3,
+// one per 16-column step) with one 16-byte load. Word (r16, L, j) holds the codes of
+// rows r16*16 + {g, g+8} and columns 16*j + 4*t + {0, 1, 2, 3} of the tile:
+//   nibble (kk & 1) * 4 + (kk >> 1) * 2 + h   <->   column 4t + kk, row g + 8h
+// so that (w & 0x000f000f) and (w & 0x00f000f0) give the half2 pairs of the
+// m16n8k16 A fragment (rows g / g+8, column pairs {4t, 4t+1}; after w >> 8 the
+// pairs {4t+2, 4t+3}), and the same four registers are the 16x256b tensor-memory
+// fragment of a 16-row x 16-column fp16 tile.
+#pragma once
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/w4a16.h"
+
+namespace w4a16 {
+
+constexpr int kRowsPerBlock = 128;
+constexpr int kColsPerBlock = 64;
+constexpr int kTileBytes = 4096;
+constexpr int kTileWords = 1024;
+constexpr int kScaleBytesPerGroupBlock = 256;
+constexpr int kZeroBytesPerGroupBlock = 64;
+
+__host__ __device__ inline size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
+
+__host__ __device__ inline int nibble_index(int kk, int h) { return (kk & 1) * 4 + (kk >> 1) * 2 + h; }
+
+struct Layout {
+  int64_t N, K, NR, KB, G;
+  int gsize;
+  bool sym, act;
+  size_t q_off, q_bytes, s_off, s_bytes, z_off, z_bytes, p_off, p_bytes, total;
+};
+
+inline Layout make_layout(const w4a16_format& f) {
+  Layout L{};
+  L.N = f.N;
+  L.K = f.K;
+  L.gsize = f.group_size;
+  L.sym = f.symmetric != 0;
+  L.act = f.has_g_idx != 0;
+  L.NR = (f.N + kRowsPerBlock - 1) / kRowsPerBlock;
+  L.KB = (f.K + kColsPerBlock - 1) / kColsPerBlock;
+  L.G = f.K / f.group_size;
+  L.q_off = 0;
+  L.q_bytes = size_t(L.NR) * size_t(L.KB) * kTileBytes;
+  L.s_off = align256(L.q_off + L.q_bytes);
+  L.s_bytes = size_t(L.NR) * size_t(L.G) * kScaleBytesPerGroupBlock;
+  L.z_off = align256(L.s_off + L.s_bytes);
+  L.z_bytes = L.sym ? 0 : size_t(L.NR) * size_t(L.G) * kZeroBytesPerGroupBlock;
+  L.p_off = align256(L.z_off + L.z_bytes);
+  L.p_bytes = L.act ? size_t(L.K) * 4 : 0;
+  L.total = align256(L.p_off + L.p_bytes);
+  return L;
+}
+
+// Pointers into one blob, as the kernels see it.
+struct BlobView {
+  const uint32_t* qweight;
+  const uint16_t* scales;   // fp16 bits
+  const uint8_t* zeros;     // nullptr when symmetric
+  const int32_t* perm;      // nullptr without act order
+};
+
+inline BlobView view_of(const Layout& L, const void* blob) {
+  const char* b = static_cast<const char*>(blob);
+  BlobView v;
+  v.qweight = reinterpret_cast<const uint32_t*>(b + L.q_off);
+  v.scales = reinterpret_cast<const uint16_t*>(b + L.s_off);
+  v.zeros = L.sym ? nullptr : reinterpret_cast<const uint8_t*>(b + L.z_off);
+  v.perm = L.act ? reinterpret_cast<const int32_t*>(b + L.p_off) : nullptr;
+  return v;
+}
+
+}  // namespace w4a16

@@ -1,0 +1,276 @@
+"""Python binding of libw4a16.so (ctypes).
+
+Argument marshalling only: tensors are checked, their device pointers and the
+current CUDA stream are passed to the C ABI declared in include/w4a16.h, and a
+non-OK status becomes a ``W4A16Error``. Every step of the computation runs in
+the library's CUDA kernels; PyTorch provides device memory and streams.
+If the shared library is missing this module raises on first use -- there is
+no fallback.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libw4a16.so")
+
+STATUS = {
+    0: "W4A16_OK",
+    1: "W4A16_ERR_INVALID_ARG",
+    2: "W4A16_ERR_UNSUPPORTED",
+    3: "W4A16_ERR_MISALIGNED",
+    4: "W4A16_ERR_BUFFER_TOO_SMALL",
+    5: "W4A16_ERR_CUDA",
+}
+
+# Exported entry points (name -> (restype, argtypes)).
+_P = ctypes.c_void_p
+_I32 = ctypes.c_int32
+_I64 = ctypes.c_int64
+_SZ = ctypes.c_size_t
+
+
+class Format(ctypes.Structure):
+    """Mirror of ``w4a16_format``."""
+
+    _fields_ = [
+        ("bits", ctypes.c_int32),
+        ("group_size", ctypes.c_int32),
+        ("symmetric", ctypes.c_int32),
+        ("has_g_idx", ctypes.c_int32),
+        ("N", ctypes.c_int64),
+        ("K", ctypes.c_int64),
+    ]
+
+    def __repr__(self):
+        return (f"Format(bits={self.bits}, group_size={self.group_size}, symmetric={self.symmetric}, "
+                f"has_g_idx={self.has_g_idx}, N={self.N}, K={self.K})")
+
+    @property
+    def G(self) -> int:
+        return self.K // self.group_size
+
+
+_FP = ctypes.POINTER(Format)
+
+SIGNATURES = {
+    "w4a16_packed_bytes": (_SZ, [_FP]),
+    "w4a16_check_format": (ctypes.c_int, [_FP]),
+    "w4a16_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "w4a16_last_cuda_error": (ctypes.c_int, []),
+    "w4a16_quantize_workspace_bytes": (_SZ, [_FP]),
+    "w4a16_quantize_rtn": (ctypes.c_int, [_FP, _P, _P, _P, _P, _P, _P, _SZ, _P]),
+    "w4a16_pack": (ctypes.c_int, [_FP, _P, _P, _P, _P, _P, _SZ, _P]),
+    "w4a16_dequant": (ctypes.c_int, [_FP, _P, _SZ, _P, _P]),
+    "w4a16_gemv": (ctypes.c_int, [_FP, _P, _SZ, _P, _P, _I64, _P]),
+    "w4a16_gemv_ex": (ctypes.c_int, [_FP, _P, _SZ, _P, _P, _I64, _I32, _I32, ctypes.c_uint32, _P]),
+    "w4a16_gemm_workspace_bytes": (_SZ, [_FP, _I64]),
+    "w4a16_gemm": (ctypes.c_int, [_FP, _P, _SZ, _P, _P, _I64, _P, _SZ, _P]),
+}
+
+_lib = None
+_lock = threading.Lock()
+
+
+class W4A16Error(RuntimeError):
+    def __init__(self, fn: str, status: int, cuda_error: int = 0):
+        self.status = status
+        self.cuda_error = cuda_error
+        msg = f"{fn} returned {STATUS.get(status, status)}"
+        if status == 5:
+            msg += f" (cudaError {cuda_error})"
+        super().__init__(msg)
+
+
+def lib() -> ctypes.CDLL:
+    """Load libw4a16.so (once). Raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        with _lock:
+            if _lib is None:
+                if not os.path.exists(LIB_PATH):
+                    raise RuntimeError(
+                        f"{LIB_PATH} is missing: build it with `python -m weight_only_bit_04_b300.build`")
+                handle = ctypes.CDLL(LIB_PATH)
+                for name, (res, args) in SIGNATURES.items():
+                    fn = getattr(handle, name)
+                    fn.restype = res
+                    fn.argtypes = args
+                _lib = handle
+    return _lib
+
+
+def _check(fn: str, status: int) -> None:
+    if status != 0:
+        raise W4A16Error(fn, status, lib().w4a16_last_cuda_error() if status == 5 else 0)
+
+
+def make_format(N: int, K: int, group_size: int = 128, symmetric: bool = False,
+                has_g_idx: bool = False, bits: int = 4) -> Format:
+    return Format(bits, group_size, int(bool(symmetric)), int(bool(has_g_idx)), N, K)
+
+
+def packed_bytes(fmt: Format) -> int:
+    return int(lib().w4a16_packed_bytes(ctypes.byref(fmt)))
+
+
+def check_format(fmt: Format) -> int:
+    return int(lib().w4a16_check_format(ctypes.byref(fmt)))
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _dev(t: torch.Tensor, dtype: torch.dtype, name: str, shape=None) -> int:
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    return t.data_ptr()
+
+
+def _host_gidx(g_idx, K: int):
+    if g_idx is None:
+        return None, None
+    arr = torch.as_tensor(g_idx).to(device="cpu", dtype=torch.int32).contiguous()
+    if arr.shape != (K,):
+        raise ValueError("g_idx must have shape [K]")
+    return arr, arr.data_ptr()
+
+
+def quantize_rtn(fmt: Format, w: torch.Tensor, g_idx=None, stream=None):
+    """Round-to-nearest group quantization on the GPU -> (q uint8, scales fp16, zeros uint8|None)."""
+    N, K, G = fmt.N, fmt.K, fmt.G
+    dev = w.device
+    wp = _dev(w, torch.float16, "w", (N, K))
+    q = torch.empty((N, K), dtype=torch.uint8, device=dev)
+    scales = torch.empty((N, G), dtype=torch.float16, device=dev)
+    zeros = None if fmt.symmetric else torch.empty((N, G), dtype=torch.uint8, device=dev)
+    ws_bytes = int(lib().w4a16_quantize_workspace_bytes(ctypes.byref(fmt)))
+    ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
+    gi, gip = _host_gidx(g_idx, K)
+    st = lib().w4a16_quantize_rtn(ctypes.byref(fmt), wp, gip, q.data_ptr(), scales.data_ptr(),
+                                  None if zeros is None else zeros.data_ptr(),
+                                  ws.data_ptr() if ws_bytes else None, ws_bytes, _stream(stream))
+    _check("w4a16_quantize_rtn", st)
+    if ws_bytes and isinstance(stream, torch.cuda.Stream):
+        ws.record_stream(stream)
+    return q, scales, zeros
+
+
+def pack(fmt: Format, q: torch.Tensor, scales: torch.Tensor, zeros=None, g_idx=None,
+         out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Pack canonical codes/scales/zeros into a new (or given) device blob."""
+    N, K, G = fmt.N, fmt.K, fmt.G
+    nbytes = packed_bytes(fmt)
+    if nbytes == 0:
+        _check("w4a16_pack", check_format(fmt))
+    qp = _dev(q, torch.uint8, "q", (N, K))
+    sp = _dev(scales, torch.float16, "scales", (N, G))
+    zp = None if zeros is None else _dev(zeros, torch.uint8, "zeros", (N, G))
+    if out is None:
+        out = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
+    op = _dev(out, torch.uint8, "out")
+    gi, gip = _host_gidx(g_idx, K)
+    st = lib().w4a16_pack(ctypes.byref(fmt), qp, sp, zp, gip, op, out.numel(), _stream(stream))
+    _check("w4a16_pack", st)
+    return out
+
+
+def dequant(fmt: Format, packed: torch.Tensor, out: torch.Tensor | None = None, stream=None):
+    pp = _dev(packed, torch.uint8, "packed")
+    if out is None:
+        out = torch.empty((fmt.N, fmt.K), dtype=torch.float16, device=packed.device)
+    op = _dev(out, torch.float16, "out", (fmt.N, fmt.K))
+    _check("w4a16_dequant", lib().w4a16_dequant(ctypes.byref(fmt), pp, packed.numel(), op, _stream(stream)))
+    return out
+
+
+GEMV_WEIGHTS_READY = 1
+
+
+def gemv(fmt: Format, packed: torch.Tensor, x: torch.Tensor, out: torch.Tensor | None = None,
+         rows16: int = 0, ksplit: int = 0, weights_ready: bool = False, stream=None) -> torch.Tensor:
+    """y = x . W_hat^T for x fp16 [M, K], 1 <= M <= 16.
+
+    ``weights_ready``: the packed weights were complete before the previous
+    kernel on the stream started, so the GEMV may stream them early.
+    """
+    M = x.shape[0]
+    pp = _dev(packed, torch.uint8, "packed")
+    xp = _dev(x, torch.float16, "x", (M, fmt.K))
+    if out is None:
+        out = torch.empty((M, fmt.N), dtype=torch.float16, device=x.device)
+    yp = _dev(out, torch.float16, "out", (M, fmt.N))
+    if rows16 or ksplit or weights_ready:
+        st = lib().w4a16_gemv_ex(ctypes.byref(fmt), pp, packed.numel(), xp, yp, M, rows16, ksplit,
+                                 GEMV_WEIGHTS_READY if weights_ready else 0, _stream(stream))
+    else:
+        st = lib().w4a16_gemv(ctypes.byref(fmt), pp, packed.numel(), xp, yp, M, _stream(stream))
+    _check("w4a16_gemv", st)
+    return out
+
+
+def gemm_workspace_bytes(fmt: Format, M: int) -> int:
+    return int(lib().w4a16_gemm_workspace_bytes(ctypes.byref(fmt), M))
+
+
+def gemm(fmt: Format, packed: torch.Tensor, x: torch.Tensor, out: torch.Tensor | None = None,
+         workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """y = x . W_hat^T for x fp16 [M, K] on the tcgen05 tensor cores."""
+    M = x.shape[0]
+    pp = _dev(packed, torch.uint8, "packed")
+    xp = _dev(x, torch.float16, "x", (M, fmt.K))
+    if out is None:
+        out = torch.empty((M, fmt.N), dtype=torch.float16, device=x.device)
+    yp = _dev(out, torch.float16, "out", (M, fmt.N))
+    need = gemm_workspace_bytes(fmt, M)
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=x.device)
+    wp = None if not need else _dev(workspace, torch.uint8, "workspace")
+    st = lib().w4a16_gemm(ctypes.byref(fmt), pp, packed.numel(), xp, yp, M, wp,
+                          0 if not need else workspace.numel(), _stream(stream))
+    _check("w4a16_gemm", st)
+    return out
+
+
+def linear(fmt: Format, packed: torch.Tensor, x: torch.Tensor, out=None, workspace=None, stream=None):
+    """Dispatch by token count: the bandwidth-bound GEMV for M <= 16, else the GEMM."""
+    if x.shape[0] <= 16:
+        return gemv(fmt, packed, x, out=out, stream=stream)
+    return gemm(fmt, packed, x, out=out, workspace=workspace, stream=stream)
+
+
+class W4A16Linear:
+    """A packed W4A16 linear layer resident in device memory."""
+
+    def __init__(self, fmt: Format, packed: torch.Tensor):
+        self.fmt = fmt
+        self.packed = packed
+
+    @classmethod
+    def from_float(cls, w: torch.Tensor, group_size: int = 128, symmetric: bool = False, g_idx=None):
+        """Quantize fp16 weights [N, K] (round to nearest) and pack them."""
+        N, K = w.shape
+        fmt = make_format(N, K, group_size, symmetric, g_idx is not None)
+        q, s, z = quantize_rtn(fmt, w, g_idx)
+        return cls(fmt, pack(fmt, q, s, z, g_idx))
+
+    def __call__(self, x: torch.Tensor, out=None) -> torch.Tensor:
+        return linear(self.fmt, self.packed, x, out=out)
