@@ -177,7 +177,10 @@ W4A16_API w4a16_status w4a16_dequant(const w4a16_format* f, const void* packed, 
  *   x        fp16 [M][K] row-major, 16-byte aligned.
  *   y        fp16 [M][N] row-major, 16-byte aligned; must not overlap x.
  * Error per element is within 2e-3 * sum_k |x[m][k] * W_hat[n][k]| + 1e-3 of
- * the exact product with the dequantized weights. M * K must be <= 2^19.
+ * the exact product with the dequantized weights. Under act order (or when K
+ * is not a multiple of 64) a thread block gathers its slice of x into shared
+ * memory, which bounds M * K / ksplit; a shape beyond that bound returns
+ * W4A16_ERR_UNSUPPORTED.
  */
 W4A16_API w4a16_status w4a16_gemv(const w4a16_format* f, const void* packed, size_t packed_bytes,
                         const uint16_t* x, uint16_t* y, int64_t M, w4a16_stream_t stream);

@@ -192,7 +192,6 @@ static w4a16_status gemv_common(const w4a16_format* f, const void* packed, size_
   const char* yb = reinterpret_cast<const char*>(y);
   const size_t xbytes = size_t(M) * size_t(f->K) * 2, ybytes = size_t(M) * size_t(f->N) * 2;
   if (xb < yb + ybytes && yb < xb + xbytes) return W4A16_ERR_INVALID_ARG;  // overlap
-  if (M * f->K > (int64_t(1) << 19)) return W4A16_ERR_UNSUPPORTED;
   if (rows16 != 0 && rows16 != 2 && rows16 != 4 && rows16 != 8) return W4A16_ERR_INVALID_ARG;
   if (ksplit != 0 && ksplit != 1 && ksplit != 2 && ksplit != 4 && ksplit != 8 && ksplit != 16)
     return W4A16_ERR_INVALID_ARG;

@@ -7,29 +7,37 @@
 //
 //  * Each warp owns two 16-row tiles (32 rows) and a contiguous run of
 //    64-column blocks. Per block it issues one coalesced 16-byte load per lane
-//    and tile (1 KiB contiguous per warp), kept kPF blocks ahead in registers.
+//    and tile (1 KiB contiguous per warp). The loads of four blocks, with the
+//    scales and zero points of their groups, stay in flight in a register
+//    ring; the loop structure follows the group size at compile time.
 //  * A 32-bit word holds the codes of one lane's m16n8k16 A fragment. Masking
 //    its nibbles with AND gives fp16 bit patterns 0x000q (= q * 2^-24) and
 //    0x00q0 (= q * 2^-20): exact subnormal values, so four ANDs and one shift
 //    expand eight weights. The tensor cores multiply them with the activations
-//    (B fragment, tokens in the n dimension) into fp32 accumulators.
+//    (B fragment, tokens in the n dimension, read through L1) into fp32
+//    accumulators.
 //  * Per (row, group) the accumulator holds sum_k x_k q_k scaled by 2^-24
 //    (rows g) or 2^-20 (rows g+8); one more MMA per 16 columns with a constant
 //    all-2^-24 operand gives the group's activation sum X. The dequantization
-//    (q - z) * s is applied once per group: y += s * (sum x q - z * X), from
-//    scales and zero points staged in shared memory by cp.async. Summation
-//    order differs from the dequantize-then-multiply definition; the error
-//    stays within the stated tolerance (products are exact, sums are fp32).
-//  * Warps sharing rows reduce through shared memory; CTAs of a thread-block
+//    (q - z) * s is applied once per group: y += s * (sum x q - z * X).
+//    Summation order differs from the dequantize-then-multiply definition;
+//    the error stays within the stated tolerance (products are exact, sums
+//    are fp32).
+//  * Under act order (and when K is not a multiple of 64) a thread block
+//    first gathers its columns of x into shared memory in packed order, with
+//    the padding columns zero.
+//  * Warps sharing rows reduce through shared memory; thread blocks of a
 //    cluster that split K reduce through distributed shared memory in rank
 //    order (deterministic, no atomics).
-//  * Programmatic dependent launch: the next kernel's CTAs become resident
-//    while this one finishes. By default a CTA waits for the previous kernel
+//  * Programmatic dependent launch: the next kernel's blocks become resident
+//    while this one finishes. By default a block waits for the previous kernel
 //    before its first global read. With kGemvWeightsReady (the caller vouches
 //    that no kernel still in flight writes the packed weights) it issues its
 //    first weight loads before that wait; activations are always read after.
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
+
+#include <cmath>
 
 #include "device_util.cuh"
 #include "internal.h"
@@ -39,21 +47,18 @@ namespace {
 
 constexpr int kWarps = 8;
 constexpr int kThreads = kWarps * 32;
-constexpr int kPF = 4;         // 64-column blocks in flight per warp
 constexpr int kTilesPerWarp = 2;
 
 struct GemvArgs {
   const uint32_t* qweight;
   const uint32_t* scales2;  // scale pairs (row g, row g+8)
-  const uint8_t* zeros;
-  const int32_t* perm;
+  const uint8_t* zeros;     // nullptr when symmetric
+  const int32_t* perm;      // packed -> original column, or nullptr
   const uint16_t* x;
   uint16_t* y;
   int M, N, K, G, KB;
-  int rows16;      // 16-row tiles per CTA (2, 4 or 8)
-  int kb_per_cta;  // 64-column blocks per CTA (the last CTAs of a cluster may get fewer)
-  int gl_per_cta;  // groups a CTA's column range can touch
-  int mpad_log2;   // log2 of M rounded up to a power of two
+  int rows16;      // 16-row tiles per thread block (2, 4 or 8)
+  int kb_per_cta;  // 64-column blocks per thread block (the last blocks of a cluster may get fewer)
   uint32_t flags;  // kGemvWeightsReady
 };
 
@@ -64,16 +69,19 @@ struct GroupFactors {
   float za, zb;  // -s_g * z_g * 2^24, -s_{g+8} * z_{g+8} * 2^24   (cx holds x-sums at 2^-24)
 };
 
+// Exact float of a 4-bit value without an int-to-float conversion.
+__device__ __forceinline__ float nib_to_float(uint32_t v) { return __uint_as_float(0x4B000000u | v) - 8388608.f; }
+
 template <bool SYM>
 __device__ __forceinline__ GroupFactors make_factors(uint32_t s2, uint32_t zbyte) {
   const float2 sf = __half22float2(*reinterpret_cast<const __half2*>(&s2));
-  const float zg = SYM ? 8.f : float(zbyte & 0xF);
-  const float zh = SYM ? 8.f : float(zbyte >> 4);
+  const float zg = SYM ? 8.f : nib_to_float(zbyte & 0xF);
+  const float zh = SYM ? 8.f : nib_to_float(zbyte >> 4);
   GroupFactors f;
   f.sa = sf.x * 16777216.f;
   f.sb = sf.y * 1048576.f;
-  f.za = -sf.x * zg * 16777216.f;
-  f.zb = -sf.y * zh * 16777216.f;
+  f.za = f.sa * -zg;
+  f.zb = sf.y * -zh * 16777216.f;
   return f;
 }
 
@@ -102,181 +110,196 @@ __device__ __forceinline__ uint32_t word_of(const uint4& v, int j) {
   return j == 0 ? v.x : j == 1 ? v.y : j == 2 ? v.z : v.w;
 }
 
-template <int NB, int GS, bool SYM>
+template <bool SMEM>
+__device__ __forceinline__ uint2 ld_x(const uint16_t* p) {
+  if (SMEM) return *reinterpret_cast<const uint2*>(p);
+  uint2 v;
+  asm volatile("ld.global.nc.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
+  return v;
+}
+
+// Unit of the weight stream: the blocks of one group (two 64-column blocks for
+// 128-column groups), or one block holding one (64) or two (32) groups.
+template <int GS>
+struct Unit {
+  static constexpr int kBlocks = GS == 128 ? 2 : 1;
+  static constexpr int kGroups = GS == 32 ? 2 : 1;
+  static constexpr int kInFlight = GS == 128 ? 2 : 4;  // units in flight per warp (4 blocks)
+};
+
+template <int GS>
+struct UnitRegs {
+  uint4 w[Unit<GS>::kBlocks][kTilesPerWarp];
+  uint32_t s[Unit<GS>::kGroups][kTilesPerWarp];
+  uint32_t z[Unit<GS>::kGroups][kTilesPerWarp];
+};
+
+// Issue the loads of one unit: codes of both tiles, scale pairs and zero bytes.
+template <int GS, bool SYM>
+__device__ __forceinline__ void load_unit(UnitRegs<GS>& r, const uint32_t* qp, const uint32_t* sp,
+                                          const uint8_t* zp, int unit, int gmax) {
+  using U = Unit<GS>;
+#pragma unroll
+  for (int bb = 0; bb < U::kBlocks; ++bb)
+#pragma unroll
+    for (int tt = 0; tt < kTilesPerWarp; ++tt)
+      r.w[bb][tt] = ldg_stream_u4(qp + (unit * U::kBlocks + bb) * 1024 + tt * 128);
+#pragma unroll
+  for (int gg = 0; gg < U::kGroups; ++gg) {
+    // (32-column groups only: a ragged last block's second half has no group;
+    // its codes and staged activations are zero, any scale will do)
+    const int gi = GS == 32 ? min(unit * U::kGroups + gg, gmax) : unit * U::kGroups + gg;
+#pragma unroll
+    for (int tt = 0; tt < kTilesPerWarp; ++tt) {
+      r.s[gg][tt] = ldg_nc_u32(sp + gi * 64 + tt * 8);
+      r.z[gg][tt] = SYM ? 0u : ldg_nc_u8(zp + gi * 64 + tt * 8);
+    }
+  }
+}
+
+// Multiply-accumulate one unit. xl0 / xl1 point at this lane's x fragment
+// (token rows g and g+8, column 4t) for the unit's first column.
+template <int NB, int GS, bool SYM, bool STAGED>
+__device__ __forceinline__ void compute_unit(const UnitRegs<GS>& r, const uint16_t* xl0, const uint16_t* xl1,
+                                             float tot[kTilesPerWarp][NB][4]) {
+  using U = Unit<GS>;
+  const uint32_t ones[4] = {0x00010001u, 0x00010001u, 0x00010001u, 0x00010001u};  // 2^-24 each
+  const float zero4[4] = {0.f, 0.f, 0.f, 0.f};
+  float acc[kTilesPerWarp][NB][4];
+  float cx[NB][4];
+#pragma unroll
+  for (int bb = 0; bb < U::kBlocks; ++bb) {
+    uint2 bx[4][NB];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int off = bb * 64 + j * 16;
+      bx[j][0] = ld_x<STAGED>(xl0 + off);
+      if (NB > 1) bx[j][NB - 1] = ld_x<STAGED>(xl1 + off);
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      // first 16-column step of a group: start fresh accumulators
+      const bool fresh = (GS == 32) ? (j == 0 || j == 2) : (j == 0 && bb == 0);
+#pragma unroll
+      for (int nb = 0; nb < NB; ++nb) mma_16816(cx[nb], ones, bx[j][nb].x, bx[j][nb].y, fresh ? zero4 : cx[nb]);
+#pragma unroll
+      for (int tt = 0; tt < kTilesPerWarp; ++tt) {
+        uint32_t af[4];
+        extract_word(word_of(r.w[bb][tt], j), af);
+#pragma unroll
+        for (int nb = 0; nb < NB; ++nb)
+          mma_16816(acc[tt][nb], af, bx[j][nb].x, bx[j][nb].y, fresh ? zero4 : acc[tt][nb]);
+      }
+      const bool group_end = (GS == 32) ? (j == 1 || j == 3) : (j == 3 && bb == U::kBlocks - 1);
+      if (group_end) {
+        const int gg = (GS == 32) ? (j >> 1) : 0;
+#pragma unroll
+        for (int tt = 0; tt < kTilesPerWarp; ++tt)
+          finalize<NB>(acc[tt], cx, make_factors<SYM>(r.s[gg][tt], r.z[gg][tt]), tot[tt]);
+      }
+    }
+  }
+}
+
+// STAGED: gather x into shared memory first (act order, or K not a multiple of 64).
+template <int MP, int GS, bool SYM, bool STAGED>
 __global__ void __launch_bounds__(kThreads) gemv_kernel(const GemvArgs a) {
   extern __shared__ __align__(16) unsigned char smem[];
-  constexpr int kBlocksPerGroup = GS == 128 ? 2 : 1;
+  constexpr int NB = MP > 8 ? 2 : 1;
+  using U = Unit<GS>;
+  constexpr int PF = U::kInFlight;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int g = lane >> 2, t = lane & 3;
   const int RT = a.rows16;
-  const int WR = RT / kTilesPerWarp;  // warp row groups per CTA
+  const int WR = RT / kTilesPerWarp;  // warp row groups per block
   const int WK = kWarps / WR;         // warps splitting K per row group
   const int wr = warp % WR;
   const int wk = warp / WR;
-  const int Tc = int(blockIdx.x) * RT;            // first 16-row tile of the CTA
+  const int Tc = int(blockIdx.x) * RT;  // first 16-row tile of the block
   const int R = Tc >> 3;
-  const int r16c = Tc & 7;
-  const int r16 = r16c + wr * kTilesPerWarp;      // this warp's first tile within the row block
+  const int r16 = (Tc & 7) + wr * kTilesPerWarp;
 
+  // Block column range (whole units), then this warp's contiguous share of it.
   const int kb_lo = int(blockIdx.y) * a.kb_per_cta;
   const int kb_hi = min(kb_lo + a.kb_per_cta, a.KB);
-  const int span = max(kb_hi - kb_lo, 0);
-  // This warp's contiguous blocks, in whole groups.
-  const int units = (span + kBlocksPerGroup - 1) / kBlocksPerGroup;
-  const int u_lo = (units * wk) / WK, u_hi = (units * (wk + 1)) / WK;
-  const int b_lo = kb_lo + min(u_lo * kBlocksPerGroup, span);
-  const int b_hi = kb_lo + min(u_hi * kBlocksPerGroup, span);
-  const int nblk = b_hi - b_lo;
+  const int span_blk = max(kb_hi - kb_lo, 0);
+  const int cta_units = (span_blk + U::kBlocks - 1) / U::kBlocks;
+  const int u0 = kb_lo / U::kBlocks + (cta_units * wk) / WK;
+  const int nunit = (cta_units * (wk + 1)) / WK - (cta_units * wk) / WK;
+
   const int G = a.G;
-  // Groups touched by this CTA: [g_lo, g_lo + ngl).
-  const int g_lo = (kb_lo * kColsPerBlock) / GS;
-  const int ngl = span > 0 ? (min(kb_hi * kColsPerBlock, G * GS) - 1) / GS - g_lo + 1 : 0;
+  const int gmax = G - 1 - u0 * U::kGroups;  // last group, relative to this warp's first
+  const uint32_t* qp =
+      a.qweight + (size_t(R) * a.KB * 8 + r16) * 128 + lane * 4 + size_t(u0) * U::kBlocks * 1024;
+  const uint32_t* sp = a.scales2 + (size_t(R) * G * 8 + r16) * 8 + g + size_t(u0) * U::kGroups * 64;
+  const uint8_t* zp = SYM ? nullptr : a.zeros + (size_t(R) * G * 8 + r16) * 8 + g + size_t(u0) * U::kGroups * 64;
 
-  // Shared memory: x fragments [bj][t][tok], then scales [gl][RT*8] and zeros [gl][RT*8].
-  const int mp_log = a.mpad_log2;
-  const int MP = 1 << mp_log;
-  uint2* xs = reinterpret_cast<uint2*>(smem);
-  uint32_t* s_sm = reinterpret_cast<uint32_t*>(smem + size_t(a.kb_per_cta) * 16 * MP * 8);
-  uint8_t* z_sm = reinterpret_cast<uint8_t*>(s_sm + size_t(a.gl_per_cta) * RT * 8);
-
-  const uint32_t* qp = a.qweight + (size_t(R) * a.KB * 8 + r16) * 128 + lane * 4;  // block 0
   const bool early = (a.flags & kGemvWeightsReady) != 0;
   if (!early) {
     pdl_wait();
     pdl_launch_dependents();
   }
-  uint4 wq[kPF][kTilesPerWarp];
+  UnitRegs<GS> ring[PF];
 #pragma unroll
-  for (int u = 0; u < kPF; ++u) {
-    if (u < nblk) {
-#pragma unroll
-      for (int tt = 0; tt < kTilesPerWarp; ++tt)
-        wq[u][tt] = ldg_stream_u4(qp + size_t(b_lo + u) * 1024 + tt * 128);
-    }
-  }
-  // Scales and zero points of the CTA's tiles and groups, 16-byte async copies.
-  {
-    const int s_chunks = RT * 2;            // 32*RT bytes per group
-    const int z_chunks = (RT * 8) / 16;     // 8*RT bytes per group (RT >= 2)
-    const char* sg = reinterpret_cast<const char*>(a.scales2) + (size_t(R) * G * 8 + r16c) * 32;
-    for (int c = threadIdx.x; c < ngl * s_chunks; c += kThreads) {
-      const int gl = c / s_chunks, k = c - gl * s_chunks;
-      cp_async_16(s_sm + gl * RT * 8 + k * 4, sg + size_t(g_lo + gl) * 256 + k * 16);
-    }
-    if (!SYM) {
-      const char* zg = reinterpret_cast<const char*>(a.zeros) + (size_t(R) * G * 8 + r16c) * 8;
-      for (int c = threadIdx.x; c < ngl * z_chunks; c += kThreads) {
-        const int gl = c / z_chunks, k = c - gl * z_chunks;
-        cp_async_16(z_sm + gl * RT * 8 + k * 16, zg + size_t(g_lo + gl) * 64 + k * 16);
-      }
-    }
-    cp_async_commit();
-  }
+  for (int s = 0; s < PF; ++s)
+    if (s < nunit) load_unit<GS, SYM>(ring[s], qp, sp, zp, s, gmax);
   if (early) {
-    pdl_launch_dependents();
     pdl_wait();
+    pdl_launch_dependents();
   }
 
-  // Stage this CTA's slice of x (in packed column order) as B fragments:
-  // unit (bj = 16-column step, t, token) = 4 consecutive halves.
+  // Activations: lanes of absent tokens read a real row (their outputs are
+  // never stored), so no masking is needed.
   const int M = a.M;
-  const int nunits = span * 16 << mp_log;
-  for (int u = threadIdx.x; u < nunits; u += kThreads) {
-    const int tok = u & (MP - 1);
-    const int rest = u >> mp_log;
-    const int tq = rest & 3;
-    const int bj = rest >> 2;
-    const int p0 = kb_lo * kColsPerBlock + bj * 16 + 4 * tq;
-    uint2 v = make_uint2(0u, 0u);
-    if (tok < M && p0 < a.K) {
-      if (a.perm == nullptr) {
-        v = *reinterpret_cast<const uint2*>(a.x + size_t(tok) * a.K + p0);
-      } else {
-        const uint16_t* xr = a.x + size_t(tok) * a.K;
-        v.x = uint32_t(xr[a.perm[p0]]) | (uint32_t(xr[a.perm[p0 + 1]]) << 16);
-        v.y = uint32_t(xr[a.perm[p0 + 2]]) | (uint32_t(xr[a.perm[p0 + 3]]) << 16);
-      }
+  const int tok0 = min(g, M - 1);
+  const int tok1 = min(g + 8, M - 1);
+  const uint16_t* xl0;
+  const uint16_t* xl1;
+  if (STAGED) {
+    // Gather this block's columns of x in packed order: xs[tok][c], row stride
+    // span + 8 halves (keeps the lanes' reads on distinct banks).
+    const int span = span_blk * kColsPerBlock;
+    const int stride = span + 8;
+    uint16_t* xs = reinterpret_cast<uint16_t*>(smem);
+    for (int e = threadIdx.x; e < M * span; e += kThreads) {
+      const int tok = e / span, c = e - tok * span;
+      const int p = kb_lo * kColsPerBlock + c;
+      xs[tok * stride + c] = p < a.K ? a.x[size_t(tok) * a.K + (a.perm ? a.perm[p] : p)] : uint16_t(0);
     }
-    xs[u] = v;
+    __syncthreads();
+    const int c0 = (u0 * U::kBlocks - kb_lo) * kColsPerBlock + 4 * t;
+    xl0 = xs + tok0 * stride + c0;
+    xl1 = xs + tok1 * stride + c0;
+  } else {
+    const int c0 = u0 * U::kBlocks * kColsPerBlock + 4 * t;
+    xl0 = a.x + size_t(tok0) * a.K + c0;
+    xl1 = a.x + size_t(tok1) * a.K + c0;
   }
-  cp_async_wait_all();
-  __syncthreads();
 
   float tot[kTilesPerWarp][NB][4];
-  float acc[kTilesPerWarp][NB][4];
-  float cx[NB][4];  // 2^-24 * (sum of x over the current group), all rows alike
 #pragma unroll
-  for (int nb = 0; nb < NB; ++nb) {
+  for (int tt = 0; tt < kTilesPerWarp; ++tt)
 #pragma unroll
-    for (int i = 0; i < 4; ++i) cx[nb][i] = 0.f;
+    for (int nb = 0; nb < NB; ++nb)
 #pragma unroll
-    for (int tt = 0; tt < kTilesPerWarp; ++tt)
-#pragma unroll
-      for (int i = 0; i < 4; ++i) tot[tt][nb][i] = 0.f, acc[tt][nb][i] = 0.f;
-  }
-  const uint32_t ones[4] = {0x00010001u, 0x00010001u, 0x00010001u, 0x00010001u};  // 2^-24 each
+      for (int i = 0; i < 4; ++i) tot[tt][nb][i] = 0.f;
 
-  const bool tok_ok0 = g < M;
-  const bool tok_ok1 = NB > 1 && g + 8 < M;
-  for (int i0 = 0; i0 < nblk; i0 += kPF) {
+  for (int i0 = 0; i0 < nunit; i0 += PF) {
 #pragma unroll
-    for (int u = 0; u < kPF; ++u) {
-      const int i = i0 + u;
-      if (i < nblk) {
-        const int b = b_lo + i;
-        const uint2* xb = xs + ((b - kb_lo) * 16 << mp_log);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          uint2 bx[NB];
-          bx[0] = tok_ok0 ? xb[((j * 4 + t) << mp_log) + g] : make_uint2(0u, 0u);
-          if (NB > 1) bx[NB - 1] = tok_ok1 ? xb[((j * 4 + t) << mp_log) + g + 8] : make_uint2(0u, 0u);
-#pragma unroll
-          for (int nb = 0; nb < NB; ++nb) mma_16816(cx[nb], ones, bx[nb].x, bx[nb].y, cx[nb]);
-#pragma unroll
-          for (int tt = 0; tt < kTilesPerWarp; ++tt) {
-            uint32_t af[4];
-            extract_word(word_of(wq[u][tt], j), af);
-#pragma unroll
-            for (int nb = 0; nb < NB; ++nb) mma_16816(acc[tt][nb], af, bx[nb].x, bx[nb].y, acc[tt][nb]);
-          }
-          // Group boundary (or end of this warp's run) after this 16-column step?
-          const bool last = (j == 3) && (i == nblk - 1);
-          const bool group_end = (GS == 32) ? (j == 1 || j == 3) : (j == 3 && (GS == 64 || (b & 1)));
-          if (group_end || last) {
-            const int gl = min((b * kColsPerBlock + j * 16) / GS, G - 1) - g_lo;
-#pragma unroll
-            for (int tt = 0; tt < kTilesPerWarp; ++tt) {
-              const int mi = gl * RT * 8 + (wr * kTilesPerWarp + tt) * 8 + g;
-              const uint32_t s2 = s_sm[mi];
-              const uint32_t zb = SYM ? 0u : z_sm[mi];
-              const GroupFactors f = make_factors<SYM>(s2, zb);
-              finalize<NB>(acc[tt], cx, f, tot[tt]);
-#pragma unroll
-              for (int nb = 0; nb < NB; ++nb)
-#pragma unroll
-                for (int q = 0; q < 4; ++q) acc[tt][nb][q] = 0.f;
-            }
-#pragma unroll
-            for (int nb = 0; nb < NB; ++nb)
-#pragma unroll
-              for (int q = 0; q < 4; ++q) cx[nb][q] = 0.f;
-          }
-        }
-        const int inext = i + kPF;
-        if (inext < nblk) {
-#pragma unroll
-          for (int tt = 0; tt < kTilesPerWarp; ++tt)
-            wq[u][tt] = ldg_stream_u4(qp + size_t(b_lo + inext) * 1024 + tt * 128);
-        }
+    for (int s = 0; s < PF; ++s) {
+      const int i = i0 + s;
+      if (i < nunit) {
+        const int xo = i * U::kBlocks * kColsPerBlock;
+        compute_unit<NB, GS, SYM, STAGED>(ring[s], xl0 + xo, xl1 + xo, tot);
+        if (i + PF < nunit) load_unit<GS, SYM>(ring[s], qp, sp, zp, i + PF, gmax);
       }
     }
   }
 
-  // Reduce: per-warp partials -> per-CTA partials (fixed order) -> cluster.
-  // The buffers reuse the staging area (offset 0 in every CTA of the cluster,
-  // where peers read red_c).
-  __syncthreads();
+  // Reduce: per-warp partials -> per-block partials (fixed order) -> cluster.
+  // The buffers sit at offset 0 in every block of the cluster (peers read red_c).
+  if (STAGED) __syncthreads();  // the staged activations are no longer needed
   float* red_w = reinterpret_cast<float*>(smem);  // [warp][32 rows][16 tokens]
   float* red_c = red_w + kWarps * 512;            // [tok][RT*16 rows]
 #pragma unroll
@@ -298,9 +321,9 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const GemvArgs a) {
     const int tok = e / rows;
     const int row = e - tok * rows;           // (wr * 2 + tt) * 16 + r
     const int w_r = row >> 5, rr = row & 31;  // warp row group, row within its 32
-    float s = 0.f;
-    for (int k = 0; k < WK; ++k) s += red_w[(k * WR + w_r) * 512 + rr * 16 + tok];
-    red_c[e] = s;
+    float acc = 0.f;
+    for (int k = 0; k < WK; ++k) acc += red_w[(k * WR + w_r) * 512 + rr * 16 + tok];
+    red_c[e] = acc;
   }
   const int KS = int(gridDim.y);
   if (KS > 1) {
@@ -310,13 +333,13 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const GemvArgs a) {
     const int e_lo = rank * per;
     const int e_hi = min(e_lo + per, nout);
     for (int e = e_lo + threadIdx.x; e < e_hi; e += kThreads) {
-      float s = 0.f;
-      for (int rk = 0; rk < KS; ++rk) s += ld_dsmem_f32(red_c + e, uint32_t(rk));
+      float acc = 0.f;
+      for (int rk = 0; rk < KS; ++rk) acc += ld_dsmem_f32(red_c + e, uint32_t(rk));
       const int tok = e / rows;
       const int n = int(blockIdx.x) * rows + (e - tok * rows);
-      if (n < a.N) a.y[size_t(tok) * a.N + n] = __half_as_ushort(__float2half_rn(s));
+      if (n < a.N) a.y[size_t(tok) * a.N + n] = __half_as_ushort(__float2half_rn(acc));
     }
-    cluster_sync_all();  // keep this CTA's shared memory alive until peers are done
+    cluster_sync_all();  // keep this block's shared memory alive until peers are done
   } else {
     __syncthreads();
     for (int e = threadIdx.x; e < nout; e += kThreads) {
@@ -327,25 +350,15 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const GemvArgs a) {
   }
 }
 
-int mpad_log2_of(int M) {
-  int l = 0;
-  while ((1 << l) < M) ++l;
-  return l;
-}
-
-int gl_per_cta_of(int kb_per_cta, int gs) { return (kb_per_cta * kColsPerBlock + gs - 1) / gs + 1; }
-
-size_t gemv_smem_bytes(int M, int kb_per_cta, int gs, int rows16) {
-  const size_t xs = size_t(kb_per_cta) * 16 * (size_t(1) << mpad_log2_of(M)) * 8;
-  const size_t meta = size_t(gl_per_cta_of(kb_per_cta, gs)) * rows16 * 8 * 5;
+size_t gemv_smem_bytes(int M, int kb_per_cta, bool staged) {
   const size_t red = size_t(kWarps) * 512 * 4 + size_t(8) * 256 * 4;
-  const size_t stage = (xs + meta + 15) / 16 * 16;
-  return stage > red ? stage : red;
+  const size_t xs = staged ? size_t(M) * (size_t(kb_per_cta) * kColsPerBlock + 8) * 2 : 0;
+  return xs > red ? xs : red;
 }
 
-template <int NB, int GS, bool SYM>
+template <int MP, int GS, bool SYM, bool STAGED>
 cudaError_t launch_typed(const GemvArgs& a, int KS, size_t smem_bytes, cudaStream_t stream) {
-  auto kern = gemv_kernel<NB, GS, SYM>;
+  auto kern = gemv_kernel<MP, GS, SYM, STAGED>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem_bytes));
   if (e != cudaSuccess) return e;
   if (KS > 8) {
@@ -377,25 +390,33 @@ cudaError_t launch_typed(const GemvArgs& a, int KS, size_t smem_bytes, cudaStrea
   return cudaGetLastError();
 }
 
-template <int NB, int GS>
-cudaError_t launch_sym(const GemvArgs& a, bool sym, int KS, size_t smem, cudaStream_t stream) {
-  return sym ? launch_typed<NB, GS, true>(a, KS, smem, stream)
-             : launch_typed<NB, GS, false>(a, KS, smem, stream);
+template <int MP, int GS>
+cudaError_t launch_flags(const GemvArgs& a, bool sym, bool staged, int KS, size_t smem, cudaStream_t stream) {
+  if (staged) {
+    return sym ? launch_typed<MP, GS, true, true>(a, KS, smem, stream)
+               : launch_typed<MP, GS, false, true>(a, KS, smem, stream);
+  }
+  return sym ? launch_typed<MP, GS, true, false>(a, KS, smem, stream)
+             : launch_typed<MP, GS, false, false>(a, KS, smem, stream);
 }
 
-template <int NB>
-cudaError_t launch_gs(const GemvArgs& a, int gs, bool sym, int KS, size_t smem, cudaStream_t stream) {
+template <int MP>
+cudaError_t launch_gs(const GemvArgs& a, int gs, bool sym, bool staged, int KS, size_t smem,
+                      cudaStream_t stream) {
   switch (gs) {
-    case 32: return launch_sym<NB, 32>(a, sym, KS, smem, stream);
-    case 64: return launch_sym<NB, 64>(a, sym, KS, smem, stream);
-    default: return launch_sym<NB, 128>(a, sym, KS, smem, stream);
+    case 32: return launch_flags<MP, 32>(a, sym, staged, KS, smem, stream);
+    case 64: return launch_flags<MP, 64>(a, sym, staged, KS, smem, stream);
+    default: return launch_flags<MP, 128>(a, sym, staged, KS, smem, stream);
   }
 }
 
 constexpr size_t kMaxGemvSmem = 100 * 1024;
 
-// 64-column blocks per CTA of a K split; a whole number of groups so that the
-// per-CTA group sums line up with the groups.
+// Activations go through shared memory under act order, or when the last
+// 64-column block is ragged (its padding columns must read as zero).
+bool gemv_staged(const Layout& L) { return L.act || (L.K % kColsPerBlock) != 0; }
+
+// 64-column blocks per thread block of a K split: whole groups.
 int kb_per_cta_of(const Layout& L, int ksplit) {
   const int unit = L.gsize == 128 ? 2 : 1;
   const int kbc = int((L.KB + ksplit - 1) / ksplit);
@@ -407,28 +428,29 @@ int kb_per_cta_of(const Layout& L, int ksplit) {
 bool gemv_plan_ok(const Layout& L, int M, const GemvPlan& p) {
   if (p.rows16 != 2 && p.rows16 != 4 && p.rows16 != 8) return false;
   if (p.ksplit != 1 && p.ksplit != 2 && p.ksplit != 4 && p.ksplit != 8 && p.ksplit != 16) return false;
-  return gemv_smem_bytes(M, kb_per_cta_of(L, p.ksplit), L.gsize, p.rows16) <= kMaxGemvSmem;
+  return gemv_smem_bytes(M, kb_per_cta_of(L, p.ksplit), gemv_staged(L)) <= kMaxGemvSmem;
 }
 
 GemvPlan gemv_default_plan(const Layout& L, int M, const DeviceInfo& dev) {
-  // Aim for about four resident CTAs per SM with at least a few 64-column
-  // blocks per warp; prefer fewer K splits.
+  // Measured on B300 (graph-replayed sweeps of 4096..28672-row layers): the
+  // stream runs best with about 1.35 thread blocks per SM, each warp keeping
+  // at least two 64-column blocks; among equally close plans, fewer K splits
+  // and then fewer rows per block win.
   const int64_t ntiles = L.NR * 8;
-  const int64_t target = int64_t(dev.sm_count) * 4;
+  const double target = 1.35 * dev.sm_count;
   GemvPlan best{8, 1};
-  int64_t best_score = -1;
-  for (int rt : {8, 4, 2}) {
-    for (int ks : {1, 2, 4, 8, 16}) {
+  double best_dist = 1e30;
+  for (int ks : {1, 2, 4, 8, 16}) {
+    for (int rt : {2, 4, 8}) {
       GemvPlan p{rt, ks};
       if (!gemv_plan_ok(L, M, p)) continue;
       const int64_t ctas = (ntiles / rt) * ks;
       const int64_t kbc = kb_per_cta_of(L, ks);
       const int64_t per_warp = kbc / (kWarps / (rt / kTilesPerWarp));
-      if (per_warp < 2 && !(ks == 1 && rt == 8)) continue;
-      int64_t score = ctas >= target ? 4 * target - (ctas - target) / 4 : 4 * ctas;
-      score = score * 64 - ks - (8 - rt);
-      if (score > best_score) {
-        best_score = score;
+      if (per_warp < 2) continue;
+      const double d = std::fabs(std::log(double(ctas) / target));
+      if (d < best_dist - 1e-9) {
+        best_dist = d;
         best = p;
       }
     }
@@ -453,12 +475,15 @@ cudaError_t launch_gemv(const Layout& L, const void* blob, const uint16_t* x, ui
   a.KB = int(L.KB);
   a.rows16 = plan.rows16;
   a.kb_per_cta = kb_per_cta_of(L, plan.ksplit);
-  a.gl_per_cta = gl_per_cta_of(a.kb_per_cta, L.gsize);
-  a.mpad_log2 = mpad_log2_of(M);
   a.flags = flags;
-  const size_t smem = gemv_smem_bytes(M, a.kb_per_cta, L.gsize, plan.rows16);
-  if (M > 8) return launch_gs<2>(a, L.gsize, L.sym, plan.ksplit, smem, stream);
-  return launch_gs<1>(a, L.gsize, L.sym, plan.ksplit, smem, stream);
+  const bool staged = gemv_staged(L);
+  const size_t smem = gemv_smem_bytes(M, a.kb_per_cta, staged);
+  const int gs = L.gsize;
+  if (M <= 1) return launch_gs<1>(a, gs, L.sym, staged, plan.ksplit, smem, stream);
+  if (M <= 2) return launch_gs<2>(a, gs, L.sym, staged, plan.ksplit, smem, stream);
+  if (M <= 4) return launch_gs<4>(a, gs, L.sym, staged, plan.ksplit, smem, stream);
+  if (M <= 8) return launch_gs<8>(a, gs, L.sym, staged, plan.ksplit, smem, stream);
+  return launch_gs<16>(a, gs, L.sym, staged, plan.ksplit, smem, stream);
 }
 
 }  // namespace w4a16
