@@ -143,6 +143,31 @@ W4A16_API w4a16_status w4a16_quantize_rtn(const w4a16_format* f, const uint16_t*
                                 w4a16_stream_t stream);
 
 /*
+ * w4a16_quantize_rtn for callers that cannot allocate device memory -- for
+ * example code inside a framework or plugin that owns every device
+ * allocation, or a path that must not allocate at all. The act-order column
+ * list that w4a16_quantize_rtn keeps in caller workspace lives here in a fixed
+ * 256 KiB array of device memory owned by the library (held by every GPU that
+ * loads it until the process exits). The pages have no counterpart; this is a
+ * deployment variant only, with the same arguments and results as
+ * w4a16_quantize_rtn minus the workspace.
+ *   Limit: with act order K <= 65536; larger K returns
+ *   W4A16_ERR_BUFFER_TOO_SMALL (without act order there is no limit beyond
+ *   the format's).
+ *   No cudaMalloc/cudaFree or other allocation, on the device or the host.
+ *   The first call on a device looks up the array's device address
+ *   (cudaGetSymbolAddress) with that device current; make that first call
+ *   before any stream capture.
+ *   Every call shares the one array and leaves its column list there. Calls
+ *   that may run at the same time on the GPU (different streams, or different
+ *   host threads with their own streams) race on it; calls on one stream do
+ *   not. Host-side staging is serialised by a lock.
+ */
+W4A16_API w4a16_status w4a16_quantize_rtn_noalloc(const w4a16_format* f, const uint16_t* w,
+                                const int32_t* g_idx, uint8_t* q, uint16_t* scales,
+                                uint8_t* zeros, w4a16_stream_t stream);
+
+/*
  * Pack canonical codes, scales and zero points into the device blob.
  *   q        uint8 [N][K], codes 0..15 (only the low 4 bits are used).
  *   scales   fp16 [N][G], 2-byte aligned.

@@ -70,6 +70,8 @@ bool build_perm(const w4a16_format& f, const int32_t* g_idx, std::vector<int32_t
 
 }  // namespace
 
+w4a16_status cuda_error_status(cudaError_t e) { return cuda_fail(e); }
+
 cudaError_t device_info(DeviceInfo* out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);

@@ -16,6 +16,9 @@ struct DeviceInfo {
 };
 cudaError_t device_info(DeviceInfo* out);
 
+// Record e for w4a16_last_cuda_error() (calling thread) and return W4A16_ERR_CUDA.
+w4a16_status cuda_error_status(cudaError_t e);
+
 cudaError_t launch_quantize_rtn(const Layout& L, const uint16_t* w, const int32_t* perm_dev,
                                 uint8_t* q, uint16_t* scales, uint8_t* zeros,
                                 cudaStream_t stream);

@@ -65,6 +65,7 @@ SIGNATURES = {
     "w4a16_last_cuda_error": (ctypes.c_int, []),
     "w4a16_quantize_workspace_bytes": (_SZ, [_FP]),
     "w4a16_quantize_rtn": (ctypes.c_int, [_FP, _P, _P, _P, _P, _P, _P, _SZ, _P]),
+    "w4a16_quantize_rtn_noalloc": (ctypes.c_int, [_FP, _P, _P, _P, _P, _P, _P]),
     "w4a16_pack": (ctypes.c_int, [_FP, _P, _P, _P, _P, _P, _SZ, _P]),
     "w4a16_dequant": (ctypes.c_int, [_FP, _P, _SZ, _P, _P]),
     "w4a16_gemv": (ctypes.c_int, [_FP, _P, _SZ, _P, _P, _I64, _P]),
