@@ -212,18 +212,46 @@ W4A16_API w4a16_status w4a16_gemv(const w4a16_format* f, const void* packed, siz
 
 /*
  * Prefill-sized product y = x . W_hat^T for M >= 1 tokens on the tcgen05
- * tensor cores (weights dequantized into tensor memory, fp32 accumulators in
- * tensor memory). Same arguments and error bound as w4a16_gemv, plus
+ * tensor cores ("AWQ + GPTQ Quantization, in depth", section "What W4A16 buys
+ * and why decoding gets faster": the 4-bit weights are expanded to 16 bits
+ * before the multiply; with many tokens the product is compute-bound). The
+ * weights are dequantized -- w_hat = fp16((q - z) * s), the same values as
+ * w4a16_dequant -- straight into tensor memory, where they are the MMA's A
+ * operand; the activations are streamed by TMA; fp32 accumulators live in
+ * tensor memory. Same arguments and error bound as w4a16_gemv, plus
  *   workspace / workspace_bytes: >= w4a16_gemm_workspace_bytes(f, M)
  *            (the activations reordered to the packed column order when the
  *            format has act order: M*K*2 bytes; else 0, may be NULL),
- *            16-byte aligned.
- * 1 <= M <= 2^20.
+ *            16-byte aligned, overlapping neither x nor y.
+ * 1 <= M <= 2^20. Needs a Blackwell GPU (compute capability 10.x); returns
+ * W4A16_ERR_UNSUPPORTED on older devices.
+ * Every pipeline wait inside the kernel is bounded (1 s); a wait that gives
+ * up leaves y unwritten for its tile and is counted on the device, see
+ * w4a16_pipeline_timeouts().
  */
 W4A16_API size_t w4a16_gemm_workspace_bytes(const w4a16_format* f, int64_t M);
 W4A16_API w4a16_status w4a16_gemm(const w4a16_format* f, const void* packed, size_t packed_bytes,
                         const uint16_t* x, uint16_t* y, int64_t M, void* workspace,
                         size_t workspace_bytes, w4a16_stream_t stream);
+
+/*
+ * w4a16_gemm with the thread-block tile chosen by the caller:
+ *   tile  0 = default, 1 = 128 weight rows x 256 tokens,
+ *         2 = 256 weight rows x 128 tokens.
+ * Results equal w4a16_gemm's up to summation order (bit-identical in
+ * practice: every tile sums the same products in the same K order).
+ */
+W4A16_API w4a16_status w4a16_gemm_ex(const w4a16_format* f, const void* packed, size_t packed_bytes,
+                           const uint16_t* x, uint16_t* y, int64_t M, void* workspace,
+                           size_t workspace_bytes, int32_t tile, w4a16_stream_t stream);
+
+/*
+ * Number of bounded pipeline waits on the current device that gave up since
+ * the previous call (each one means a tile of some w4a16_gemm output was not
+ * written); the count is reset. Synchronous: waits for the device's pending
+ * work to finish. Not expected to be nonzero in correct operation.
+ */
+W4A16_API w4a16_status w4a16_pipeline_timeouts(uint32_t* count);
 
 /*
  * w4a16_gemv with options.

@@ -226,13 +226,14 @@ size_t w4a16_gemm_workspace_bytes(const w4a16_format* f, int64_t M) {
   return f->has_g_idx ? size_t(M) * size_t(f->K) * 2 : 0;
 }
 
-w4a16_status w4a16_gemm(const w4a16_format* f, const void* packed, size_t packed_bytes,
-                        const uint16_t* x, uint16_t* y, int64_t M, void* workspace,
-                        size_t workspace_bytes, w4a16_stream_t stream) {
+static w4a16_status gemm_common(const w4a16_format* f, const void* packed, size_t packed_bytes,
+                                const uint16_t* x, uint16_t* y, int64_t M, void* workspace,
+                                size_t workspace_bytes, int32_t tile, w4a16_stream_t stream) {
   w4a16_status s = blob_status(f, packed, packed_bytes);
   if (s != W4A16_OK) return s;
   if (x == nullptr || y == nullptr) return W4A16_ERR_INVALID_ARG;
   if (M < 1 || M > (int64_t(1) << 20)) return W4A16_ERR_INVALID_ARG;
+  if (tile < 0 || tile > 2) return W4A16_ERR_INVALID_ARG;
   if (!aligned(x, 16) || !aligned(y, 16)) return W4A16_ERR_MISALIGNED;
   const size_t xbytes = size_t(M) * size_t(f->K) * 2, ybytes = size_t(M) * size_t(f->N) * 2;
   const char* xb = reinterpret_cast<const char*>(x);
@@ -242,9 +243,37 @@ w4a16_status w4a16_gemm(const w4a16_format* f, const void* packed, size_t packed
   if (workspace_bytes < need) return W4A16_ERR_BUFFER_TOO_SMALL;
   if (need > 0 && workspace == nullptr) return W4A16_ERR_INVALID_ARG;
   if (need > 0 && !aligned(workspace, 16)) return W4A16_ERR_MISALIGNED;
-  cudaError_t e = launch_gemm(make_layout(*f), packed, x, y, M, workspace, stream);
-  if (e == cudaErrorNotSupported) return W4A16_ERR_UNSUPPORTED;
+  if (need > 0) {
+    const char* wb = static_cast<const char*>(workspace);
+    if ((wb < yb + ybytes && yb < wb + need) || (wb < xb + xbytes && xb < wb + need)) return W4A16_ERR_INVALID_ARG;
+  }
+  DeviceInfo dev;
+  cudaError_t e = device_info(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (dev.cc_major * 10 + dev.cc_minor < 100) return W4A16_ERR_UNSUPPORTED;  // tcgen05 needs Blackwell
+  e = launch_gemm(make_layout(*f), packed, x, y, M, workspace, tile == 0 ? 1 : tile, stream);
   return e == cudaSuccess ? W4A16_OK : cuda_fail(e);
+}
+
+w4a16_status w4a16_gemm(const w4a16_format* f, const void* packed, size_t packed_bytes,
+                        const uint16_t* x, uint16_t* y, int64_t M, void* workspace,
+                        size_t workspace_bytes, w4a16_stream_t stream) {
+  return gemm_common(f, packed, packed_bytes, x, y, M, workspace, workspace_bytes, 0, stream);
+}
+
+w4a16_status w4a16_gemm_ex(const w4a16_format* f, const void* packed, size_t packed_bytes,
+                           const uint16_t* x, uint16_t* y, int64_t M, void* workspace,
+                           size_t workspace_bytes, int32_t tile, w4a16_stream_t stream) {
+  return gemm_common(f, packed, packed_bytes, x, y, M, workspace, workspace_bytes, tile, stream);
+}
+
+w4a16_status w4a16_pipeline_timeouts(uint32_t* count) {
+  if (count == nullptr) return W4A16_ERR_INVALID_ARG;
+  unsigned int c = 0;
+  cudaError_t e = take_pipeline_timeouts(&c);
+  if (e != cudaSuccess) return cuda_fail(e);
+  *count = c;
+  return W4A16_OK;
 }
 
 }  // extern "C"

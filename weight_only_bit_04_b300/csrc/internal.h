@@ -39,7 +39,11 @@ constexpr uint32_t kGemvWeightsReady = W4A16_GEMV_WEIGHTS_READY;
 cudaError_t launch_gemv(const Layout& L, const void* blob, const uint16_t* x, uint16_t* y,
                         int M, const GemvPlan& plan, uint32_t flags, cudaStream_t stream);
 
+// tile: 1 = 128 weight rows x 256 tokens per thread block, 2 = 256 rows x 128 tokens.
 cudaError_t launch_gemm(const Layout& L, const void* blob, const uint16_t* x, uint16_t* y,
-                        int64_t M, void* workspace, cudaStream_t stream);
+                        int64_t M, void* workspace, int tile, cudaStream_t stream);
+
+// Device-side count of bounded pipeline waits that gave up (k_gemm.cu).
+cudaError_t take_pipeline_timeouts(unsigned int* count);
 
 }  // namespace w4a16

@@ -1,13 +1,475 @@
-// Prefill-sized W4A16 product on the tcgen05 tensor cores (not built yet).
+// Prefill-sized W4A16 product y[M][N] = x[M][K] . W_hat^T on the tcgen05
+// tensor cores.
+//
+// With many tokens the product is a dense contraction and the tensor cores set
+// the pace ("AWQ + GPTQ Quantization, in depth", section "What W4A16 buys and
+// why decoding gets faster": 4-bit weights are expanded to 16 bits before the
+// multiply). The weights enter the MMA from tensor memory:
+//
+//  * One thread block owns WR x 128 weight rows and NT tokens. Per 64-column
+//    step, dequantization warps read the 4 KiB packed tile of each 128-row
+//    block (coalesced 16-byte loads, several steps ahead in registers), expand
+//    the nibbles to w_hat = fp16((q - z) * s) -- the same rounding as
+//    w4a16_dequant -- and store them into tensor memory with tcgen05.st: they
+//    are the MMA's A operand (lane = weight row, two fp16 per 32-bit column).
+//  * A TMA warp streams the activations (NT tokens x 64 columns, 128-byte
+//    swizzle) into a ring of shared-memory stages; they are the B operand.
+//  * One thread issues tcgen05.mma (M = 128 weight rows, N = NT tokens,
+//    K = 16) into fp32 accumulators in tensor memory and releases each
+//    stage with tcgen05.commit.
+//  * The epilogue reads the accumulators back (tcgen05.ld), rounds to fp16,
+//    transposes through shared memory (one slice per warp) and writes y with
+//    16-byte stores.
+//  * Under act order the packed columns are in group order; a gather kernel
+//    first writes x with its columns in that order to the caller's workspace.
+//  * Every wait is bounded in time: a wait that gives up raises the device's
+//    pipeline-timeout count (w4a16_pipeline_timeouts), the block drains what
+//    it has in flight and returns without writing y.
+#include <cuda.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
+#include <mutex>
+
+#include "device_util.cuh"
 #include "internal.h"
+#include "tc_util.cuh"
 
 namespace w4a16 {
 
-cudaError_t launch_gemm(const Layout&, const void*, const uint16_t*, uint16_t*, int64_t, void*,
-                        cudaStream_t) {
-  return cudaErrorNotSupported;
+__device__ unsigned int g_pipeline_timeouts;
+
+namespace {
+
+constexpr uint64_t kWaitLimitNs = 1000ull * 1000ull * 1000ull;  // 1 s per wait
+constexpr int kTmemCols = 512;
+constexpr int kPrefetch = 4;  // packed steps each dequantization warp keeps in flight
+
+// WR: 128-row weight blocks per thread block; NT: tokens per thread block;
+// SA: tensor-memory stages of dequantized weights; SB: shared-memory stages of activations.
+template <int WR, int NT, int SA, int SB>
+struct Cfg {
+  static constexpr int kDeqWarps = 4 * WR;
+  static constexpr int kTmaWarp = kDeqWarps;
+  static constexpr int kMmaWarp = kDeqWarps + 1;
+  static constexpr int kThreads = (kDeqWarps + 2) * 32;
+  static constexpr int kDCols = WR * NT;          // fp32 accumulators
+  static constexpr int kACol0 = kDCols;           // first A column
+  static constexpr int kBStage = NT * 128;        // NT rows x 64 fp16
+  static constexpr int kBarBytes = 8 * (SA * 2 + SB * 2 + 1) + 16;
+  static constexpr int kSmem = SB * kBStage + 1024 + kBarBytes;
+  static_assert(kDCols + SA * WR * 32 <= kTmemCols, "tensor memory budget");
+  static_assert(kDeqWarps * NT * 32 * 2 <= SB * kBStage, "epilogue staging must fit in the activation stages");
+  static_assert(NT % 32 == 0 && NT >= 32 && NT <= 256, "MMA N");
+};
+
+struct GemmArgs {
+  const uint32_t* qweight;
+  const uint32_t* scales2;  // scale pairs (row g, row g+8)
+  const uint8_t* zeros;     // nullptr when symmetric
+  uint16_t* y;
+  int M, N, NR, G, KB;
+  int tok_blocks;
+};
+
+// Instruction descriptor of tcgen05.mma kind::f16: fp32 D, fp16 A and B, both
+// K-major, M = 128, N = NT.
+template <int NT>
+__device__ __forceinline__ uint32_t idesc_f16() {
+  return (1u << 4)                      // D format: f32
+         | (0u << 7) | (0u << 10)       // A, B format: f16
+         | (uint32_t(NT >> 3) << 17)    // N / 8
+         | (uint32_t(128 >> 4) << 24);  // M / 16
+}
+
+// Shared-memory descriptor of a K-major operand stored with the 128-byte
+// swizzle: rows of 128 bytes, 8-row groups 1024 bytes apart.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+  return uint64_t((saddr & 0x3FFFFu) >> 4)  // start address
+         | (uint64_t(1) << 16)              // leading byte offset (unused with this swizzle)
+         | (uint64_t(1024 >> 4) << 32)      // stride byte offset: 8 rows
+         | (uint64_t(1) << 46)              // descriptor version
+         | (uint64_t(2) << 61);             // 128-byte swizzle
+}
+
+__device__ __forceinline__ void note_timeout(volatile int* abort_flag) {
+  *abort_flag = 1;
+  atomicAdd(&g_pipeline_timeouts, 1u);
+}
+
+// Bounded wait that also gives up once another role of the block has.
+__device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+  if (*abort_flag) return false;
+  if (mbar_wait_bounded(bar, parity, kWaitLimitNs)) return true;
+  note_timeout(abort_flag);
+  return false;
+}
+
+template <int GS, bool SYM>
+struct StepRegs {
+  static constexpr int kGroups = GS == 32 ? 2 : 1;  // groups in one 64-column step
+  uint4 w[2];                 // packed words of the warp's two 16-row tiles
+  uint32_t s[2][kGroups];     // scale pairs
+  uint32_t z[2][kGroups];     // zero bytes
+};
+
+template <int GS, bool SYM>
+__device__ __forceinline__ void load_step(StepRegs<GS, SYM>& r, const uint32_t* qp, const uint32_t* sp,
+                                          const uint8_t* zp, int kb, int G) {
+#pragma unroll
+  for (int i = 0; i < 2; ++i) r.w[i] = ldg_stream_u4(qp + size_t(kb) * 1024 + i * 128);
+#pragma unroll
+  for (int gg = 0; gg < StepRegs<GS, SYM>::kGroups; ++gg) {
+    // the padding half of a ragged last step (32-column groups) reuses the last group
+    const int gi = GS == 128 ? (kb >> 1) : GS == 64 ? kb : min(2 * kb + gg, G - 1);
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      r.s[i][gg] = ldg_nc_u32(sp + size_t(gi) * 64 + i * 8);
+      r.z[i][gg] = SYM ? 0u : ldg_nc_u8(zp + size_t(gi) * 64 + i * 8);
+    }
+  }
+}
+
+// Dequantize one step of one 16-row tile into the 16 registers of a
+// tcgen05.st 16x256b.x4: per 16-column group j, (row g, columns 4t..4t+1),
+// (row g, 4t+2..4t+3), (row g+8, 4t..4t+1), (row g+8, 4t+2..4t+3).
+template <int GS, bool SYM>
+__device__ __forceinline__ void dequant_tile(const StepRegs<GS, SYM>& r, int i, uint32_t (&v)[16]) {
+  constexpr int NG = StepRegs<GS, SYM>::kGroups;
+  uint32_t za[NG], zb[NG], sg[NG], sh[NG];
+#pragma unroll
+  for (int gg = 0; gg < NG; ++gg) {
+    const uint32_t zlo = SYM ? 8u : (r.z[i][gg] & 0xFu);
+    const uint32_t zhi = SYM ? 8u : (r.z[i][gg] >> 4);
+    za[gg] = zero_lo_const(zlo);
+    zb[gg] = zero_hi_const(zhi);
+    sg[gg] = (r.s[i][gg] & 0xFFFFu) * 0x00010001u;
+    sh[gg] = (r.s[i][gg] >> 16) * 0x00010001u;
+  }
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int gg = NG == 2 ? (j >> 1) : 0;
+    const uint32_t w = j == 0 ? r.w[i].x : j == 1 ? r.w[i].y : j == 2 ? r.w[i].z : r.w[i].w;
+    uint32_t a[4];
+    expand_word(w, za[gg], zb[gg], a);  // exact (q - z) in fp16
+    v[4 * j + 0] = hmul2_u32(a[0], sg[gg]);
+    v[4 * j + 1] = hmul2_u32(a[2], sg[gg]);
+    v[4 * j + 2] = hmul2_u32(a[1], sh[gg]);
+    v[4 * j + 3] = hmul2_u32(a[3], sh[gg]);
+  }
+}
+
+template <int WR, int NT, int SA, int SB, int GS, bool SYM>
+__global__ void __launch_bounds__(Cfg<WR, NT, SA, SB>::kThreads, 1)
+    gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const GemmArgs a) {
+  using C = Cfg<WR, NT, SA, SB>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_addr(smem_raw);
+  uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);  // 1024-byte aligned for the swizzle
+  const uint32_t sbase = smem_addr(smem);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + SB * C::kBStage);
+  // barriers: full_a[SA], empty_a[SA], full_b[SB], empty_b[SB], acc
+  const uint32_t bar0 = smem_addr(bars);
+  auto full_a = [&](int s) { return bar0 + 8u * uint32_t(s); };
+  auto empty_a = [&](int s) { return bar0 + 8u * uint32_t(SA + s); };
+  auto full_b = [&](int s) { return bar0 + 8u * uint32_t(2 * SA + s); };
+  auto empty_b = [&](int s) { return bar0 + 8u * uint32_t(2 * SA + SB + s); };
+  const uint32_t acc_bar = bar0 + 8u * uint32_t(2 * SA + 2 * SB);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * SA + 2 * SB + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = int(threadIdx.x >> 5), lane = int(threadIdx.x & 31);
+  const int tb = int(blockIdx.x) % a.tok_blocks;
+  const int rg = int(blockIdx.x) / a.tok_blocks;
+  const int m0 = tb * NT;
+  const int KB = a.KB;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < SA; ++s) {
+      mbar_init(full_a(s), C::kDeqWarps * 32);
+      mbar_init(empty_a(s), 1);
+    }
+    for (int s = 0; s < SB; ++s) {
+      mbar_init(full_b(s), 1);
+      mbar_init(empty_b(s), 1);
+    }
+    mbar_init(acc_bar, 1);
+    *abort_flag = 0;
+    fence_mbarrier_init();
+  }
+  if (warp == C::kTmaWarp) {
+    tmem_alloc(smem_addr(tmem_slot), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp < C::kDeqWarps) {
+    // ---------------- dequantization into tensor memory, then the epilogue
+    const int at = warp >> 2;  // 128-row tile of this block
+    const int q4 = warp & 3;   // tensor-memory lane quarter: rows 32*q4 .. 32*q4+31 of the tile
+    const int R = rg * WR + at;
+    const bool live = R < a.NR;
+    const int g = lane >> 2;
+    const uint32_t* qp = a.qweight + (size_t(R) * KB * 8 + 2 * q4) * 128 + lane * 4;
+    const uint32_t* sp = a.scales2 + (size_t(R) * a.G * 8 + 2 * q4) * 8 + g;
+    const uint8_t* zp = SYM ? nullptr : a.zeros + (size_t(R) * a.G * 8 + 2 * q4) * 8 + g;
+
+    StepRegs<GS, SYM> ring[kPrefetch];
+#pragma unroll
+    for (int p = 0; p < kPrefetch; ++p)
+      if (live && p < KB) load_step<GS, SYM>(ring[p], qp, sp, zp, p, a.G);
+
+    bool ok = true;
+    for (int kb0 = 0; kb0 < KB && ok; kb0 += kPrefetch) {
+#pragma unroll
+      for (int p = 0; p < kPrefetch; ++p) {
+        const int kb = kb0 + p;
+        if (kb < KB && ok) {
+          const int s = kb % SA;
+          const int n = kb / SA;
+          if (kb >= SA && !wait_or_abort(empty_a(s), uint32_t(n - 1) & 1u, abort_flag)) {
+            ok = false;
+          } else {
+            tc_fence_after();
+            const uint32_t col = tmem + uint32_t(C::kACol0 + (s * WR + at) * 32);
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+              uint32_t v[16];
+              if (live) {
+                dequant_tile<GS, SYM>(ring[p], i, v);
+              } else {
+#pragma unroll
+                for (int e = 0; e < 16; ++e) v[e] = 0u;
+              }
+              tmem_st_16x256b_x4(col + (uint32_t(32 * q4 + 16 * i) << 16), v);
+            }
+            if (live && kb + kPrefetch < KB) load_step<GS, SYM>(ring[p], qp, sp, zp, kb + kPrefetch, a.G);
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(full_a(s));
+          }
+        }
+      }
+    }
+
+    // ---------------- epilogue: each warp transposes its 32 rows x NT tokens
+    // through a private shared-memory slice (no block-wide barrier, so a warp
+    // that gave up cannot stall the others) and writes 64-byte row segments.
+    if (ok && wait_or_abort(acc_bar, 0u, abort_flag)) {
+      tc_fence_after();
+      uint16_t* wst = reinterpret_cast<uint16_t*>(smem) + warp * NT * 32;  // [NT tokens][32 rows]
+      const int n_warp = (rg * WR + at) * 128 + 32 * q4;
+      const int m_live = min(NT, a.M - m0);
+#pragma unroll 1
+      for (int c = 0; c < NT / 32; ++c) {
+        if (c * 32 >= m_live) break;
+        uint32_t v[32];
+        tmem_ld_32x32b_x32(tmem + (uint32_t(32 * q4) << 16) + uint32_t(at * NT + c * 32), v);
+        tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          wst[(c * 32 + i) * 32 + lane] = __half_as_ushort(__float2half_rn(__uint_as_float(v[i])));
+      }
+      __syncwarp();
+      const bool vec = (a.N % 8) == 0;
+      for (int e = lane; e < m_live * 4; e += 32) {
+        const int m = e >> 2, gn = n_warp + (e & 3) * 8;
+        if (gn >= a.N) continue;
+        const uint16_t* src = wst + m * 32 + (e & 3) * 8;
+        uint16_t* dst = a.y + size_t(m0 + m) * a.N + gn;
+        if (vec) {
+          *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(src);
+        } else {
+          for (int i = 0; i < 8 && gn + i < a.N; ++i) dst[i] = src[i];
+        }
+      }
+    }
+  } else if (warp == C::kTmaWarp) {
+    // ---------------- activation stream (one thread)
+    if (lane == 0) {
+      tma_prefetch_desc(&tmap_x);
+      int issued = 0;
+      for (int kb = 0; kb < KB; ++kb) {
+        const int s = kb % SB;
+        const int n = kb / SB;
+        if (kb >= SB && !wait_or_abort(empty_b(s), uint32_t(n - 1) & 1u, abort_flag)) break;
+        mbar_arrive_expect_tx(full_b(s), uint32_t(C::kBStage));
+        tma_load_2d(sbase + uint32_t(s * C::kBStage), &tmap_x, kb * 64, m0, full_b(s));
+        ++issued;
+      }
+      if (*abort_flag) {
+        // drain: the last loads issued must land before the block's shared memory goes away
+        for (int kb = max(issued - SB, 0); kb < issued; ++kb)
+          mbar_wait_bounded(full_b(kb % SB), uint32_t(kb / SB) & 1u, kWaitLimitNs);
+      }
+    }
+  } else if (warp == C::kMmaWarp) {
+    // ---------------- MMA issue (one thread)
+    if (lane == 0) {
+      const uint32_t idesc = idesc_f16<NT>();
+      for (int kb = 0; kb < KB; ++kb) {
+        const int sa = kb % SA, sb = kb % SB;
+        if (!wait_or_abort(full_b(sb), uint32_t(kb / SB) & 1u, abort_flag)) break;
+        if (!wait_or_abort(full_a(sa), uint32_t(kb / SA) & 1u, abort_flag)) break;
+        tc_fence_after();
+        const uint32_t b_addr = sbase + uint32_t(sb * C::kBStage);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          const uint64_t bdesc = sw128_desc(b_addr + uint32_t(kk * 32));
+#pragma unroll
+          for (int t = 0; t < WR; ++t)
+            mma_ts_f16(tmem + uint32_t(t * NT), tmem + uint32_t(C::kACol0 + (sa * WR + t) * 32 + kk * 8), bdesc,
+                       idesc, uint32_t(kb | kk));
+        }
+        mma_commit(empty_a(sa));
+        mma_commit(empty_b(sb));
+      }
+      mma_commit(acc_bar);
+      // on abort, let every MMA issued so far finish before tensor memory is freed
+      if (*abort_flag) mbar_wait_bounded(acc_bar, 0u, kWaitLimitNs);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == C::kTmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// x_perm[m][p] = x[m][perm[p]]: activations in the packed (group-sorted) column order.
+__global__ void __launch_bounds__(256) gather_cols_kernel(const uint16_t* __restrict__ x,
+                                                          const int32_t* __restrict__ perm,
+                                                          uint16_t* __restrict__ xp, int64_t M, int K) {
+  const int64_t chunks = int64_t(K) / 8;
+  const int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= M * chunks) return;
+  const int64_t m = i / chunks;
+  const int p0 = int(i - m * chunks) * 8;
+  const uint16_t* row = x + m * K;
+  uint32_t w[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+    w[j] = uint32_t(row[perm[p0 + 2 * j]]) | (uint32_t(row[perm[p0 + 2 * j + 1]]) << 16);
+  *reinterpret_cast<uint4*>(xp + m * K + p0) = make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+std::once_flag g_encode_once;
+EncodeTiledFn g_encode = nullptr;
+cudaError_t g_encode_err = cudaSuccess;
+
+cudaError_t encode_fn(EncodeTiledFn* out) {
+  std::call_once(g_encode_once, []() {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    g_encode_err = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+    if (g_encode_err == cudaSuccess && (q != cudaDriverEntryPointSuccess || fn == nullptr))
+      g_encode_err = cudaErrorNotSupported;
+    g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+  });
+  *out = g_encode;
+  return g_encode_err;
+}
+
+// Tensor map of x [M][K] fp16, box of NT rows x 64 columns, 128-byte swizzle;
+// rows and columns beyond the tensor read as zero.
+cudaError_t make_x_map(CUtensorMap* map, const uint16_t* x, int64_t M, int64_t K, int NT) {
+  EncodeTiledFn enc = nullptr;
+  cudaError_t e = encode_fn(&enc);
+  if (e != cudaSuccess) return e;
+  const cuuint64_t dims[2] = {cuuint64_t(K), cuuint64_t(M)};
+  const cuuint64_t strides[1] = {cuuint64_t(K) * 2};
+  const cuuint32_t box[2] = {64u, cuuint32_t(NT)};
+  const cuuint32_t estr[2] = {1u, 1u};
+  const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<uint16_t*>(x), dims, strides, box,
+                         estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+template <int WR, int NT, int SA, int SB, int GS, bool SYM>
+cudaError_t launch_cfg(const Layout& L, const GemmArgs& base, const uint16_t* xa, int64_t M, cudaStream_t stream) {
+  using C = Cfg<WR, NT, SA, SB>;
+  CUtensorMap map;
+  cudaError_t e = make_x_map(&map, xa, M, L.K, NT);
+  if (e != cudaSuccess) return e;
+  auto kern = gemm_kernel<WR, NT, SA, SB, GS, SYM>;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+  if (e != cudaSuccess) return e;
+  GemmArgs a = base;
+  a.tok_blocks = int((M + NT - 1) / NT);
+  const int64_t row_groups = (L.NR + WR - 1) / WR;
+  const int64_t blocks = row_groups * a.tok_blocks;
+  if (blocks > 0x7FFFFFFF) return cudaErrorInvalidConfiguration;
+  kern<<<unsigned(blocks), C::kThreads, C::kSmem, stream>>>(map, a);
+  return cudaGetLastError();
+}
+
+template <int WR, int NT, int SA, int SB>
+cudaError_t launch_scheme(const Layout& L, const GemmArgs& a, const uint16_t* xa, int64_t M, cudaStream_t stream) {
+  switch (L.gsize) {
+    case 32:
+      return L.sym ? launch_cfg<WR, NT, SA, SB, 32, true>(L, a, xa, M, stream)
+                   : launch_cfg<WR, NT, SA, SB, 32, false>(L, a, xa, M, stream);
+    case 64:
+      return L.sym ? launch_cfg<WR, NT, SA, SB, 64, true>(L, a, xa, M, stream)
+                   : launch_cfg<WR, NT, SA, SB, 64, false>(L, a, xa, M, stream);
+    default:
+      return L.sym ? launch_cfg<WR, NT, SA, SB, 128, true>(L, a, xa, M, stream)
+                   : launch_cfg<WR, NT, SA, SB, 128, false>(L, a, xa, M, stream);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_gemm(const Layout& L, const void* blob, const uint16_t* x, uint16_t* y, int64_t M,
+                        void* workspace, int tile, cudaStream_t stream) {
+  const BlobView B = view_of(L, blob);
+  const uint16_t* xa = x;
+  if (L.act) {
+    uint16_t* xp = static_cast<uint16_t*>(workspace);
+    const int64_t chunks = M * (L.K / 8);
+    gather_cols_kernel<<<unsigned((chunks + 255) / 256), 256, 0, stream>>>(x, B.perm, xp, M, int(L.K));
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    xa = xp;
+  }
+  GemmArgs a{};
+  a.qweight = B.qweight;
+  a.scales2 = reinterpret_cast<const uint32_t*>(B.scales);
+  a.zeros = B.zeros;
+  a.y = y;
+  a.M = int(M);
+  a.N = int(L.N);
+  a.NR = int(L.NR);
+  a.G = int(L.G);
+  a.KB = int(L.KB);
+  if (tile == 2) return launch_scheme<2, 128, 4, 12>(L, a, xa, M, stream);
+  return launch_scheme<1, 256, 8, 6>(L, a, xa, M, stream);
+}
+
+cudaError_t take_pipeline_timeouts(unsigned int* count) {
+  unsigned int c = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(&c, g_pipeline_timeouts, sizeof(c));
+  if (e != cudaSuccess) return e;
+  if (c != 0) {
+    const unsigned int zero = 0;
+    e = cudaMemcpyToSymbol(g_pipeline_timeouts, &zero, sizeof(zero));
+    if (e != cudaSuccess) return e;
+  }
+  *count = c;
+  return cudaSuccess;
 }
 
 }  // namespace w4a16

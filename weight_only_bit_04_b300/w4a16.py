@@ -72,6 +72,8 @@ SIGNATURES = {
     "w4a16_gemv_ex": (ctypes.c_int, [_FP, _P, _SZ, _P, _P, _I64, _I32, _I32, ctypes.c_uint32, _P]),
     "w4a16_gemm_workspace_bytes": (_SZ, [_FP, _I64]),
     "w4a16_gemm": (ctypes.c_int, [_FP, _P, _SZ, _P, _P, _I64, _P, _SZ, _P]),
+    "w4a16_gemm_ex": (ctypes.c_int, [_FP, _P, _SZ, _P, _P, _I64, _P, _SZ, _I32, _P]),
+    "w4a16_pipeline_timeouts": (ctypes.c_int, [ctypes.POINTER(ctypes.c_uint32)]),
 }
 
 _lib = None
@@ -233,8 +235,11 @@ def gemm_workspace_bytes(fmt: Format, M: int) -> int:
 
 
 def gemm(fmt: Format, packed: torch.Tensor, x: torch.Tensor, out: torch.Tensor | None = None,
-         workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
-    """y = x . W_hat^T for x fp16 [M, K] on the tcgen05 tensor cores."""
+         workspace: torch.Tensor | None = None, tile: int = 0, stream=None) -> torch.Tensor:
+    """y = x . W_hat^T for x fp16 [M, K] on the tcgen05 tensor cores.
+
+    ``tile``: 0 default, 1 = 128 weight rows x 256 tokens, 2 = 256 x 128.
+    """
     M = x.shape[0]
     pp = _dev(packed, torch.uint8, "packed")
     xp = _dev(x, torch.float16, "x", (M, fmt.K))
@@ -245,10 +250,21 @@ def gemm(fmt: Format, packed: torch.Tensor, x: torch.Tensor, out: torch.Tensor |
     if need and workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=x.device)
     wp = None if not need else _dev(workspace, torch.uint8, "workspace")
-    st = lib().w4a16_gemm(ctypes.byref(fmt), pp, packed.numel(), xp, yp, M, wp,
-                          0 if not need else workspace.numel(), _stream(stream))
+    wbytes = 0 if not need else workspace.numel()
+    if tile:
+        st = lib().w4a16_gemm_ex(ctypes.byref(fmt), pp, packed.numel(), xp, yp, M, wp, wbytes, tile,
+                                 _stream(stream))
+    else:
+        st = lib().w4a16_gemm(ctypes.byref(fmt), pp, packed.numel(), xp, yp, M, wp, wbytes, _stream(stream))
     _check("w4a16_gemm", st)
     return out
+
+
+def pipeline_timeouts() -> int:
+    """Bounded in-kernel waits that gave up on the current device since the last call (resets)."""
+    c = ctypes.c_uint32(0)
+    _check("w4a16_pipeline_timeouts", lib().w4a16_pipeline_timeouts(ctypes.byref(c)))
+    return int(c.value)
 
 
 def linear(fmt: Format, packed: torch.Tensor, x: torch.Tensor, out=None, workspace=None, stream=None):
