@@ -236,8 +236,9 @@ W4A16_API w4a16_status w4a16_gemm(const w4a16_format* f, const void* packed, siz
 
 /*
  * w4a16_gemm with the thread-block tile chosen by the caller:
- *   tile  0 = default, 1 = 128 weight rows x 256 tokens,
- *         2 = 256 weight rows x 128 tokens.
+ *   tile  0 = default (3), 1 = 128 weight rows x 256 tokens,
+ *         2 = 256 weight rows x 128 tokens, 3 = 128 x 256 with twice the
+ *         dequantization warps of 1, 4 = 128 x 256 with half of them.
  * Results equal w4a16_gemm's up to summation order (bit-identical in
  * practice: every tile sums the same products in the same K order).
  */

@@ -15,7 +15,7 @@ from weight_only_bit_04_b300 import w4a16 as W
 
 pytestmark = pytest.mark.gpu
 
-TILES = (1, 2)
+TILES = (1, 2, 3, 4)
 
 
 def to_dev(a):
@@ -109,7 +109,7 @@ def test_tiles_agree_and_deterministic(cuda_ok):
     packed = W.pack(fmt, q, s, z)
     xd = to_dev(x)
     a = W.gemm(fmt, packed, xd, tile=1).cpu().numpy()
-    for tile in (1, 2, 0):
+    for tile in (1, 2, 3, 4, 0):
         b = W.gemm(fmt, packed, xd, tile=tile).cpu().numpy()
         assert np.array_equal(a.view(np.uint16), b.view(np.uint16)), tile
     no_timeouts()

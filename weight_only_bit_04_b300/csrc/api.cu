@@ -233,7 +233,7 @@ static w4a16_status gemm_common(const w4a16_format* f, const void* packed, size_
   if (s != W4A16_OK) return s;
   if (x == nullptr || y == nullptr) return W4A16_ERR_INVALID_ARG;
   if (M < 1 || M > (int64_t(1) << 20)) return W4A16_ERR_INVALID_ARG;
-  if (tile < 0 || tile > 2) return W4A16_ERR_INVALID_ARG;
+  if (tile < 0 || tile > 4) return W4A16_ERR_INVALID_ARG;
   if (!aligned(x, 16) || !aligned(y, 16)) return W4A16_ERR_MISALIGNED;
   const size_t xbytes = size_t(M) * size_t(f->K) * 2, ybytes = size_t(M) * size_t(f->N) * 2;
   const char* xb = reinterpret_cast<const char*>(x);
@@ -251,7 +251,7 @@ static w4a16_status gemm_common(const w4a16_format* f, const void* packed, size_
   cudaError_t e = device_info(&dev);
   if (e != cudaSuccess) return cuda_fail(e);
   if (dev.cc_major * 10 + dev.cc_minor < 100) return W4A16_ERR_UNSUPPORTED;  // tcgen05 needs Blackwell
-  e = launch_gemm(make_layout(*f), packed, x, y, M, workspace, tile == 0 ? 1 : tile, stream);
+  e = launch_gemm(make_layout(*f), packed, x, y, M, workspace, tile == 0 ? 3 : tile, stream);
   return e == cudaSuccess ? W4A16_OK : cuda_fail(e);
 }
 

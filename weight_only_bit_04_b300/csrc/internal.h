@@ -39,7 +39,8 @@ constexpr uint32_t kGemvWeightsReady = W4A16_GEMV_WEIGHTS_READY;
 cudaError_t launch_gemv(const Layout& L, const void* blob, const uint16_t* x, uint16_t* y,
                         int M, const GemvPlan& plan, uint32_t flags, cudaStream_t stream);
 
-// tile: 1 = 128 weight rows x 256 tokens per thread block, 2 = 256 rows x 128 tokens.
+// tile: 1 = 128 weight rows x 256 tokens per thread block (2 dequantization warp
+// sets), 2 = 256 rows x 128 tokens (2 sets), 3 = 128 x 256 with 4 sets, 4 = 128 x 256 with 1 set.
 cudaError_t launch_gemm(const Layout& L, const void* blob, const uint16_t* x, uint16_t* y,
                         int64_t M, void* workspace, int tile, cudaStream_t stream);
 

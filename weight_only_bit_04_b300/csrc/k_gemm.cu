@@ -43,13 +43,16 @@ namespace {
 
 constexpr uint64_t kWaitLimitNs = 1000ull * 1000ull * 1000ull;  // 1 s per wait
 constexpr int kTmemCols = 512;
-constexpr int kPrefetch = 4;  // packed steps each dequantization warp keeps in flight
 
 // WR: 128-row weight blocks per thread block; NT: tokens per thread block;
-// SA: tensor-memory stages of dequantized weights; SB: shared-memory stages of activations.
-template <int WR, int NT, int SA, int SB>
+// SA: tensor-memory stages of dequantized weights; SB: shared-memory stages of
+// activations; DS: dequantization warp sets, set d producing the 64-column
+// steps kb = d (mod DS), so that each scheduler interleaves DS independent
+// dequantization streams.
+template <int WR, int NT, int SA, int SB, int DS>
 struct Cfg {
-  static constexpr int kDeqWarps = 4 * WR;
+  static constexpr int kSetWarps = 4 * WR;        // one warp per (128-row tile, lane quarter)
+  static constexpr int kDeqWarps = kSetWarps * DS;
   static constexpr int kTmaWarp = kDeqWarps;
   static constexpr int kMmaWarp = kDeqWarps + 1;
   static constexpr int kThreads = (kDeqWarps + 2) * 32;
@@ -58,8 +61,14 @@ struct Cfg {
   static constexpr int kBStage = NT * 128;        // NT rows x 64 fp16
   static constexpr int kBarBytes = 8 * (SA * 2 + SB * 2 + 1) + 16;
   static constexpr int kSmem = SB * kBStage + 1024 + kBarBytes;
+  static constexpr int kEpiTokens = NT / DS;      // tokens each set writes back
+  // packed steps each dequantization warp keeps in flight (fewer when the
+  // block is large enough for the register file to cap every thread at 96)
+  static constexpr int kPrefetch = kThreads > 512 ? 2 : 4;
   static_assert(kDCols + SA * WR * 32 <= kTmemCols, "tensor memory budget");
-  static_assert(kDeqWarps * NT * 32 * 2 <= SB * kBStage, "epilogue staging must fit in the activation stages");
+  static_assert(SA % DS == 0, "each tensor-memory stage belongs to one set");
+  static_assert(kEpiTokens % 32 == 0, "epilogue in 32-token chunks");
+  static_assert(kDeqWarps * kEpiTokens * 32 * 2 <= SB * kBStage, "epilogue staging must fit in the activation stages");
   static_assert(NT % 32 == 0 && NT >= 32 && NT <= 256, "MMA N");
 };
 
@@ -159,10 +168,10 @@ __device__ __forceinline__ void dequant_tile(const StepRegs<GS, SYM>& r, int i, 
   }
 }
 
-template <int WR, int NT, int SA, int SB, int GS, bool SYM>
-__global__ void __launch_bounds__(Cfg<WR, NT, SA, SB>::kThreads, 1)
+template <int WR, int NT, int SA, int SB, int DS, int GS, bool SYM>
+__global__ void __launch_bounds__(Cfg<WR, NT, SA, SB, DS>::kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const GemmArgs a) {
-  using C = Cfg<WR, NT, SA, SB>;
+  using C = Cfg<WR, NT, SA, SB, DS>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_addr(smem_raw);
   uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);  // 1024-byte aligned for the swizzle
@@ -186,7 +195,7 @@ __global__ void __launch_bounds__(Cfg<WR, NT, SA, SB>::kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < SA; ++s) {
-      mbar_init(full_a(s), C::kDeqWarps * 32);
+      mbar_init(full_a(s), C::kSetWarps * 32);
       mbar_init(empty_a(s), 1);
     }
     for (int s = 0; s < SB; ++s) {
@@ -208,7 +217,8 @@ __global__ void __launch_bounds__(Cfg<WR, NT, SA, SB>::kThreads, 1)
 
   if (warp < C::kDeqWarps) {
     // ---------------- dequantization into tensor memory, then the epilogue
-    const int at = warp >> 2;  // 128-row tile of this block
+    const int ds = warp / C::kSetWarps;  // warp set: steps kb = ds (mod DS)
+    const int at = (warp % C::kSetWarps) >> 2;  // 128-row tile of this block
     const int q4 = warp & 3;   // tensor-memory lane quarter: rows 32*q4 .. 32*q4+31 of the tile
     const int R = rg * WR + at;
     const bool live = R < a.NR;
@@ -216,18 +226,21 @@ __global__ void __launch_bounds__(Cfg<WR, NT, SA, SB>::kThreads, 1)
     const uint32_t* qp = a.qweight + (size_t(R) * KB * 8 + 2 * q4) * 128 + lane * 4;
     const uint32_t* sp = a.scales2 + (size_t(R) * a.G * 8 + 2 * q4) * 8 + g;
     const uint8_t* zp = SYM ? nullptr : a.zeros + (size_t(R) * a.G * 8 + 2 * q4) * 8 + g;
+    const int nsteps = KB > ds ? (KB - ds + DS - 1) / DS : 0;  // steps of this set
 
+    constexpr int kPrefetch = C::kPrefetch;
     StepRegs<GS, SYM> ring[kPrefetch];
 #pragma unroll
     for (int p = 0; p < kPrefetch; ++p)
-      if (live && p < KB) load_step<GS, SYM>(ring[p], qp, sp, zp, p, a.G);
+      if (live && p < nsteps) load_step<GS, SYM>(ring[p], qp, sp, zp, ds + p * DS, a.G);
 
     bool ok = true;
-    for (int kb0 = 0; kb0 < KB && ok; kb0 += kPrefetch) {
+    for (int i0 = 0; i0 < nsteps && ok; i0 += kPrefetch) {
 #pragma unroll
       for (int p = 0; p < kPrefetch; ++p) {
-        const int kb = kb0 + p;
-        if (kb < KB && ok) {
+        const int i = i0 + p;
+        if (i < nsteps && ok) {
+          const int kb = ds + i * DS;
           const int s = kb % SA;
           const int n = kb / SA;
           if (kb >= SA && !wait_or_abort(empty_a(s), uint32_t(n - 1) & 1u, abort_flag)) {
@@ -236,17 +249,17 @@ __global__ void __launch_bounds__(Cfg<WR, NT, SA, SB>::kThreads, 1)
             tc_fence_after();
             const uint32_t col = tmem + uint32_t(C::kACol0 + (s * WR + at) * 32);
 #pragma unroll
-            for (int i = 0; i < 2; ++i) {
+            for (int h = 0; h < 2; ++h) {
               uint32_t v[16];
               if (live) {
-                dequant_tile<GS, SYM>(ring[p], i, v);
+                dequant_tile<GS, SYM>(ring[p], h, v);
               } else {
 #pragma unroll
                 for (int e = 0; e < 16; ++e) v[e] = 0u;
               }
-              tmem_st_16x256b_x4(col + (uint32_t(32 * q4 + 16 * i) << 16), v);
+              tmem_st_16x256b_x4(col + (uint32_t(32 * q4 + 16 * h) << 16), v);
             }
-            if (live && kb + kPrefetch < KB) load_step<GS, SYM>(ring[p], qp, sp, zp, kb + kPrefetch, a.G);
+            if (live && i + kPrefetch < nsteps) load_step<GS, SYM>(ring[p], qp, sp, zp, kb + kPrefetch * DS, a.G);
             tmem_wait_st();
             tc_fence_before();
             mbar_arrive(full_a(s));
@@ -255,19 +268,22 @@ __global__ void __launch_bounds__(Cfg<WR, NT, SA, SB>::kThreads, 1)
       }
     }
 
-    // ---------------- epilogue: each warp transposes its 32 rows x NT tokens
-    // through a private shared-memory slice (no block-wide barrier, so a warp
-    // that gave up cannot stall the others) and writes 64-byte row segments.
+    // ---------------- epilogue: set ds writes tokens [ds*NT/DS, (ds+1)*NT/DS).
+    // Each warp transposes its 32 rows x NT/DS tokens through a private
+    // shared-memory slice (no block-wide barrier, so a warp that gave up
+    // cannot stall the others) and writes 64-byte row segments.
     if (ok && wait_or_abort(acc_bar, 0u, abort_flag)) {
       tc_fence_after();
-      uint16_t* wst = reinterpret_cast<uint16_t*>(smem) + warp * NT * 32;  // [NT tokens][32 rows]
+      constexpr int ET = C::kEpiTokens;
+      uint16_t* wst = reinterpret_cast<uint16_t*>(smem) + warp * ET * 32;  // [ET tokens][32 rows]
       const int n_warp = (rg * WR + at) * 128 + 32 * q4;
-      const int m_live = min(NT, a.M - m0);
+      const int t0 = ds * ET;                                 // first token of this set
+      const int m_live = max(0, min(ET, a.M - m0 - t0));      // tokens of this set that exist
 #pragma unroll 1
-      for (int c = 0; c < NT / 32; ++c) {
+      for (int c = 0; c < ET / 32; ++c) {
         if (c * 32 >= m_live) break;
         uint32_t v[32];
-        tmem_ld_32x32b_x32(tmem + (uint32_t(32 * q4) << 16) + uint32_t(at * NT + c * 32), v);
+        tmem_ld_32x32b_x32(tmem + (uint32_t(32 * q4) << 16) + uint32_t(at * NT + t0 + c * 32), v);
         tmem_wait_ld();
 #pragma unroll
         for (int i = 0; i < 32; ++i)
@@ -279,7 +295,7 @@ __global__ void __launch_bounds__(Cfg<WR, NT, SA, SB>::kThreads, 1)
         const int m = e >> 2, gn = n_warp + (e & 3) * 8;
         if (gn >= a.N) continue;
         const uint16_t* src = wst + m * 32 + (e & 3) * 8;
-        uint16_t* dst = a.y + size_t(m0 + m) * a.N + gn;
+        uint16_t* dst = a.y + size_t(m0 + t0 + m) * a.N + gn;
         if (vec) {
           *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(src);
         } else {
@@ -291,6 +307,7 @@ __global__ void __launch_bounds__(Cfg<WR, NT, SA, SB>::kThreads, 1)
     // ---------------- activation stream (one thread)
     if (lane == 0) {
       tma_prefetch_desc(&tmap_x);
+      pdl_wait();  // x may come from the preceding gather kernel
       int issued = 0;
       for (int kb = 0; kb < KB; ++kb) {
         const int s = kb % SB;
@@ -341,10 +358,38 @@ __global__ void __launch_bounds__(Cfg<WR, NT, SA, SB>::kThreads, 1)
   }
 }
 
-// x_perm[m][p] = x[m][perm[p]]: activations in the packed (group-sorted) column order.
-__global__ void __launch_bounds__(256) gather_cols_kernel(const uint16_t* __restrict__ x,
-                                                          const int32_t* __restrict__ perm,
-                                                          uint16_t* __restrict__ xp, int64_t M, int K) {
+// x_perm[m][p] = x[m][perm[p]]: activations in the packed (group-sorted)
+// column order. One thread block per token row: the row is staged in shared
+// memory with 16-byte loads, then written back permuted with 16-byte stores.
+constexpr int kGatherThreads = 256;
+__global__ void __launch_bounds__(kGatherThreads) gather_cols_kernel(const uint16_t* __restrict__ x,
+                                                                     const int32_t* __restrict__ perm,
+                                                                     uint16_t* __restrict__ xp, int K) {
+  extern __shared__ __align__(16) uint16_t row_s[];
+  pdl_launch_dependents();
+  const int64_t m = blockIdx.x;
+  const uint4* src = reinterpret_cast<const uint4*>(x + m * K);
+  const int chunks = K / 8;
+  for (int c = threadIdx.x; c < chunks; c += kGatherThreads) reinterpret_cast<uint4*>(row_s)[c] = src[c];
+  __syncthreads();
+  uint4* dst = reinterpret_cast<uint4*>(xp + m * K);
+  const int4* pv = reinterpret_cast<const int4*>(perm);
+  for (int c = threadIdx.x; c < chunks; c += kGatherThreads) {
+    const int4 p0 = pv[2 * c], p1 = pv[2 * c + 1];
+    uint4 o;
+    o.x = uint32_t(row_s[p0.x]) | (uint32_t(row_s[p0.y]) << 16);
+    o.y = uint32_t(row_s[p0.z]) | (uint32_t(row_s[p0.w]) << 16);
+    o.z = uint32_t(row_s[p1.x]) | (uint32_t(row_s[p1.y]) << 16);
+    o.w = uint32_t(row_s[p1.z]) | (uint32_t(row_s[p1.w]) << 16);
+    dst[c] = o;
+  }
+}
+
+// The same gather for rows too long to stage in shared memory.
+__global__ void __launch_bounds__(256) gather_cols_global_kernel(const uint16_t* __restrict__ x,
+                                                                 const int32_t* __restrict__ perm,
+                                                                 uint16_t* __restrict__ xp, int64_t M, int K) {
+  pdl_launch_dependents();
   const int64_t chunks = int64_t(K) / 8;
   const int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
   if (i >= M * chunks) return;
@@ -357,6 +402,7 @@ __global__ void __launch_bounds__(256) gather_cols_kernel(const uint16_t* __rest
     w[j] = uint32_t(row[perm[p0 + 2 * j]]) | (uint32_t(row[perm[p0 + 2 * j + 1]]) << 16);
   *reinterpret_cast<uint4*>(xp + m * K + p0) = make_uint4(w[0], w[1], w[2], w[3]);
 }
+constexpr size_t kGatherMaxSmem = 160 * 1024;
 
 // ---------------------------------------------------------------------------
 // host side
@@ -398,13 +444,14 @@ cudaError_t make_x_map(CUtensorMap* map, const uint16_t* x, int64_t M, int64_t K
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-template <int WR, int NT, int SA, int SB, int GS, bool SYM>
-cudaError_t launch_cfg(const Layout& L, const GemmArgs& base, const uint16_t* xa, int64_t M, cudaStream_t stream) {
-  using C = Cfg<WR, NT, SA, SB>;
+template <int WR, int NT, int SA, int SB, int DS, int GS, bool SYM>
+cudaError_t launch_cfg(const Layout& L, const GemmArgs& base, const uint16_t* xa, int64_t M, bool after_gather,
+                       cudaStream_t stream) {
+  using C = Cfg<WR, NT, SA, SB, DS>;
   CUtensorMap map;
   cudaError_t e = make_x_map(&map, xa, M, L.K, NT);
   if (e != cudaSuccess) return e;
-  auto kern = gemm_kernel<WR, NT, SA, SB, GS, SYM>;
+  auto kern = gemm_kernel<WR, NT, SA, SB, DS, GS, SYM>;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   if (e != cudaSuccess) return e;
   GemmArgs a = base;
@@ -412,22 +459,37 @@ cudaError_t launch_cfg(const Layout& L, const GemmArgs& base, const uint16_t* xa
   const int64_t row_groups = (L.NR + WR - 1) / WR;
   const int64_t blocks = row_groups * a.tok_blocks;
   if (blocks > 0x7FFFFFFF) return cudaErrorInvalidConfiguration;
-  kern<<<unsigned(blocks), C::kThreads, C::kSmem, stream>>>(map, a);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(unsigned(blocks), 1, 1);
+  cfg.blockDim = dim3(C::kThreads, 1, 1);
+  cfg.dynamicSmemBytes = C::kSmem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  // After our own gather kernel (which writes only the workspace), the
+  // block's set-up and weight stream may start before the gather ends; the
+  // activation loads wait for it.
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = after_gather ? 1 : 0;
+  e = cudaLaunchKernelEx(&cfg, kern, map, a);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
-template <int WR, int NT, int SA, int SB>
-cudaError_t launch_scheme(const Layout& L, const GemmArgs& a, const uint16_t* xa, int64_t M, cudaStream_t stream) {
+template <int WR, int NT, int SA, int SB, int DS>
+cudaError_t launch_scheme(const Layout& L, const GemmArgs& a, const uint16_t* xa, int64_t M, bool after_gather,
+                          cudaStream_t stream) {
   switch (L.gsize) {
     case 32:
-      return L.sym ? launch_cfg<WR, NT, SA, SB, 32, true>(L, a, xa, M, stream)
-                   : launch_cfg<WR, NT, SA, SB, 32, false>(L, a, xa, M, stream);
+      return L.sym ? launch_cfg<WR, NT, SA, SB, DS, 32, true>(L, a, xa, M, after_gather, stream)
+                   : launch_cfg<WR, NT, SA, SB, DS, 32, false>(L, a, xa, M, after_gather, stream);
     case 64:
-      return L.sym ? launch_cfg<WR, NT, SA, SB, 64, true>(L, a, xa, M, stream)
-                   : launch_cfg<WR, NT, SA, SB, 64, false>(L, a, xa, M, stream);
+      return L.sym ? launch_cfg<WR, NT, SA, SB, DS, 64, true>(L, a, xa, M, after_gather, stream)
+                   : launch_cfg<WR, NT, SA, SB, DS, 64, false>(L, a, xa, M, after_gather, stream);
     default:
-      return L.sym ? launch_cfg<WR, NT, SA, SB, 128, true>(L, a, xa, M, stream)
-                   : launch_cfg<WR, NT, SA, SB, 128, false>(L, a, xa, M, stream);
+      return L.sym ? launch_cfg<WR, NT, SA, SB, DS, 128, true>(L, a, xa, M, after_gather, stream)
+                   : launch_cfg<WR, NT, SA, SB, DS, 128, false>(L, a, xa, M, after_gather, stream);
   }
 }
 
@@ -439,9 +501,18 @@ cudaError_t launch_gemm(const Layout& L, const void* blob, const uint16_t* x, ui
   const uint16_t* xa = x;
   if (L.act) {
     uint16_t* xp = static_cast<uint16_t*>(workspace);
-    const int64_t chunks = M * (L.K / 8);
-    gather_cols_kernel<<<unsigned((chunks + 255) / 256), 256, 0, stream>>>(x, B.perm, xp, M, int(L.K));
-    cudaError_t e = cudaGetLastError();
+    const size_t smem = size_t(L.K) * 2;
+    cudaError_t e = cudaSuccess;
+    if (smem <= kGatherMaxSmem && M <= 0x7FFFFFFF) {
+      if (smem > 48 * 1024)
+        e = cudaFuncSetAttribute(gather_cols_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+      if (e != cudaSuccess) return e;
+      gather_cols_kernel<<<unsigned(M), kGatherThreads, smem, stream>>>(x, B.perm, xp, int(L.K));
+    } else {
+      const int64_t chunks = M * (L.K / 8);
+      gather_cols_global_kernel<<<unsigned((chunks + 255) / 256), 256, 0, stream>>>(x, B.perm, xp, M, int(L.K));
+    }
+    e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     xa = xp;
   }
@@ -455,8 +526,13 @@ cudaError_t launch_gemm(const Layout& L, const void* blob, const uint16_t* x, ui
   a.NR = int(L.NR);
   a.G = int(L.G);
   a.KB = int(L.KB);
-  if (tile == 2) return launch_scheme<2, 128, 4, 12>(L, a, xa, M, stream);
-  return launch_scheme<1, 256, 8, 6>(L, a, xa, M, stream);
+  const bool g = L.act;
+  switch (tile) {
+    case 2: return launch_scheme<2, 128, 4, 12, 2>(L, a, xa, M, g, stream);
+    case 3: return launch_scheme<1, 256, 8, 6, 4>(L, a, xa, M, g, stream);
+    case 4: return launch_scheme<1, 256, 8, 6, 1>(L, a, xa, M, g, stream);
+    default: return launch_scheme<1, 256, 8, 6, 2>(L, a, xa, M, g, stream);
+  }
 }
 
 cudaError_t take_pipeline_timeouts(unsigned int* count) {
