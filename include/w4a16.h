@@ -256,22 +256,34 @@ W4A16_API w4a16_status w4a16_pipeline_timeouts(uint32_t* count);
 
 /*
  * w4a16_gemv with options.
- *   rows16   16-row tiles per CTA: 2, 4 or 8; 0 = default.
- *   ksplit   CTAs per thread-block cluster splitting K: 1, 2, 4, 8 or 16;
+ *   shape    0 = default. Default kernel (weights loaded straight into a
+ *            ring of registers): 16-row tiles per thread block, 2, 4 or 8.
+ *            With W4A16_GEMV_BULK_COPY: the depth of the shared-memory ring
+ *            in 16 KiB stages, 2..8.
+ *   ksplit   thread blocks per cluster splitting K: 1, 2, 4, 8 or 16;
  *            0 = default.
- *   flags    0 or W4A16_GEMV_WEIGHTS_READY.
+ *   flags    0 or an OR of
+ *            W4A16_GEMV_WEIGHTS_READY: no kernel still in flight on the
+ *              stream writes `packed` (true once the weights were packed
+ *              before the preceding kernel started, as in a decode loop);
+ *              the GEMV then starts streaming weights before the previous
+ *              kernel finishes. `x` is always read after it.
+ *            W4A16_GEMV_BULK_COPY: use the variant in which a producer warp
+ *              streams each thread block's weights (and activations) with
+ *              bulk copies into a ring of shared-memory stages.
+ *            W4A16_GEMV_STAGE_ACTIVATIONS: default kernel only: copy each
+ *              thread block's activations to shared memory before the
+ *              weight stream.
  * The GEMV kernels are launched with programmatic dependent launch, so a GEMV
  * may start while the previous kernel on the stream is still running; by
  * default it reads nothing from global memory before that kernel is done.
- * W4A16_GEMV_WEIGHTS_READY promises that no kernel still in flight on the
- * stream writes `packed` (true once the weights were packed before the
- * preceding kernel started, as in a decode loop); the GEMV then starts
- * streaming weights before the previous kernel finishes. `x` is always read
- * after it. Results equal w4a16_gemv's up to summation order.
+ * Results equal w4a16_gemv's up to summation order.
  */
 #define W4A16_GEMV_WEIGHTS_READY 1u
+#define W4A16_GEMV_BULK_COPY 2u
+#define W4A16_GEMV_STAGE_ACTIVATIONS 4u
 W4A16_API w4a16_status w4a16_gemv_ex(const w4a16_format* f, const void* packed, size_t packed_bytes,
-                           const uint16_t* x, uint16_t* y, int64_t M, int32_t rows16,
+                           const uint16_t* x, uint16_t* y, int64_t M, int32_t shape,
                            int32_t ksplit, uint32_t flags, w4a16_stream_t stream);
 
 #ifdef __cplusplus

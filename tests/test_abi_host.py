@@ -131,9 +131,13 @@ def test_gemv_argument_checks(lib):
     bad = fmt(bits=2)
     assert lib.w4a16_gemv(ctypes.byref(bad), FAKE, nb, X, Y, 1, None) == UNSUPPORTED
     # explicit launch shapes are validated too
-    assert lib.w4a16_gemv_ex(ctypes.byref(f), FAKE, nb, X, Y, 1, 3, 1, 0, None) == INVALID
+    bulk, stage_x = 2, 4
+    assert lib.w4a16_gemv_ex(ctypes.byref(f), FAKE, nb, X, Y, 1, 9, 1, bulk, None) == INVALID   # ring depth
+    assert lib.w4a16_gemv_ex(ctypes.byref(f), FAKE, nb, X, Y, 1, 1, 1, bulk, None) == INVALID
+    assert lib.w4a16_gemv_ex(ctypes.byref(f), FAKE, nb, X, Y, 1, 3, 1, 0, None) == INVALID      # rows16
     assert lib.w4a16_gemv_ex(ctypes.byref(f), FAKE, nb, X, Y, 1, 8, 32, 0, None) == INVALID
-    assert lib.w4a16_gemv_ex(ctypes.byref(f), FAKE, nb, X, Y, 1, 0, 0, 2, None) == INVALID
+    assert lib.w4a16_gemv_ex(ctypes.byref(f), FAKE, nb, X, Y, 1, 0, 0, 8, None) == INVALID     # unknown flag
+    assert lib.w4a16_gemv_ex(ctypes.byref(f), FAKE, nb, X, Y, 1, 0, 0, bulk | stage_x | 16, None) == INVALID
 
 
 def test_gemm_and_workspace_checks(lib):

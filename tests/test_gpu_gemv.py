@@ -19,14 +19,22 @@ def to_dev(a):
     return torch.from_numpy(np.ascontiguousarray(a)).cuda()
 
 
-def run_case(N, K, M, g, sym, act, frac=0.01, tag="gemv", rows16=0, ksplit=0):
+# register ring (default) / register ring with staged activations / shared-memory bulk-copy ring
+VARIANTS = ("ring", "ring_sx", "bulk")
+
+
+def variant_kw(variant):
+    return dict(bulk_copy=variant == "bulk", stage_activations=variant == "ring_sx")
+
+
+def run_case(N, K, M, g, sym, act, frac=0.01, tag="gemv", shape=0, ksplit=0, variant="ring"):
     W16 = synth.weights_np(N, K, synth.seed_for(tag, "w", N, K, g, sym, act))
     x = synth.activations_np(M, K, frac, synth.seed_for(tag, "x", M, K))
     gidx = synth.act_order_g_idx(x, g) if act else None
     y_ref, B, (q, s, z), _ = O.w4a16_linear(x, W16, g, sym, gidx)
     fmt = W.make_format(N, K, g, sym, act)
     packed = W.pack(fmt, to_dev(q), to_dev(s), None if sym else to_dev(z), gidx)
-    y = W.gemv(fmt, packed, to_dev(x), rows16=rows16, ksplit=ksplit)
+    y = W.gemv(fmt, packed, to_dev(x), shape=shape, ksplit=ksplit, **variant_kw(variant))
     torch.cuda.synchronize()
     return y.cpu().numpy(), y_ref, B
 
@@ -37,49 +45,65 @@ def assert_within(y, y_ref, B):
     assert r.max() <= 1.0, f"max error ratio {r.max():.3f} at {np.unravel_index(r.argmax(), r.shape)}"
 
 
-def test_single_linear_batch1(cuda_ok):
-    y, y_ref, B = run_case(256, 512, 1, 128, False, False, tag="single")
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_single_linear_batch1(cuda_ok, variant):
+    y, y_ref, B = run_case(256, 512, 1, 128, False, False, tag="single", variant=variant)
     assert_within(y, y_ref, B)
 
 
 @pytest.mark.parametrize("M", [1, 2, 3, 4, 7, 8, 9, 12, 16])
-def test_token_counts(cuda_ok, M):
-    y, y_ref, B = run_case(384, 1024, M, 128, False, False)
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_token_counts(cuda_ok, M, variant):
+    y, y_ref, B = run_case(384, 1024, M, 128, False, False, variant=variant)
     assert_within(y, y_ref, B)
 
 
 @pytest.mark.parametrize("g", [32, 64, 128])
 @pytest.mark.parametrize("sym", [False, True])
 @pytest.mark.parametrize("M", [1, 16])
-def test_group_sizes_and_schemes(cuda_ok, g, sym, M):
-    y, y_ref, B = run_case(256, 1024, M, g, sym, False)
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_group_sizes_and_schemes(cuda_ok, g, sym, M, variant):
+    y, y_ref, B = run_case(256, 1024, M, g, sym, False, variant=variant)
     assert_within(y, y_ref, B)
 
 
 @pytest.mark.parametrize("N,K,g", [(200, 96, 32), (130, 320, 64), (1, 128, 128), (17, 64, 32),
                                    (1000, 1152, 128)])
-def test_ragged_shapes(cuda_ok, N, K, g):
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_ragged_shapes(cuda_ok, N, K, g, variant):
     for M in (1, 5):
-        y, y_ref, B = run_case(N, K, M, g, False, False, tag="ragged")
+        y, y_ref, B = run_case(N, K, M, g, False, False, tag="ragged", variant=variant)
         assert_within(y, y_ref, B)
 
 
 @pytest.mark.parametrize("M", [1, 4, 16])
-def test_act_order(cuda_ok, M):
-    y, y_ref, B = run_case(512, 1024, M, 128, False, True, tag="act")
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_act_order(cuda_ok, M, variant):
+    y, y_ref, B = run_case(512, 1024, M, 128, False, True, tag="act", variant=variant)
     assert_within(y, y_ref, B)
-    y, y_ref, B = run_case(256, 512, M, 32, True, True, tag="act")
+    y, y_ref, B = run_case(256, 512, M, 32, True, True, tag="act", variant=variant)
     assert_within(y, y_ref, B)
 
 
 @pytest.mark.parametrize("rows16", [2, 4, 8])
 @pytest.mark.parametrize("ksplit", [1, 2, 4, 8, 16])
-def test_every_launch_shape(cuda_ok, rows16, ksplit):
-    y, y_ref, B = run_case(256, 2048, 3, 64, False, False, tag="plan", rows16=rows16, ksplit=ksplit)
-    assert_within(y, y_ref, B)
+def test_every_register_ring_launch_shape(cuda_ok, rows16, ksplit):
+    for variant in ("ring", "ring_sx"):
+        y, y_ref, B = run_case(256, 2048, 3, 64, False, False, tag="plan", shape=rows16, ksplit=ksplit,
+                               variant=variant)
+        assert_within(y, y_ref, B)
 
 
-def test_exact_integer_special_case(cuda_ok):
+@pytest.mark.parametrize("stages", [2, 3, 4, 6, 8])
+@pytest.mark.parametrize("ksplit", [1, 2, 4, 8, 16])
+def test_every_bulk_copy_launch_shape(cuda_ok, stages, ksplit):
+    for g, act in ((64, False), (32, True)):
+        y, y_ref, B = run_case(256, 2048, 3, g, False, act, tag="plan", shape=stages, ksplit=ksplit, variant="bulk")
+        assert_within(y, y_ref, B)
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_exact_integer_special_case(cuda_ok, variant):
     """s = 1, z = 8, x in {-1, 0, 1} with <= 128 nonzeros per row: y is exact."""
     rng = np.random.default_rng(5)
     N, K = 384, 2048
@@ -94,7 +118,7 @@ def test_exact_integer_special_case(cuda_ok):
         y_ref, _ = O.linear_ref(x, O.dequant(q, s, z, 128))
         fmt = W.make_format(N, K, 128, False, False)
         packed = W.pack(fmt, to_dev(q), to_dev(s), to_dev(z))
-        y = W.gemv(fmt, packed, to_dev(x)).cpu().numpy().astype(np.float64)
+        y = W.gemv(fmt, packed, to_dev(x), **variant_kw(variant)).cpu().numpy().astype(np.float64)
         assert np.array_equal(y, y_ref)
 
 

@@ -183,7 +183,7 @@ w4a16_status w4a16_dequant(const w4a16_format* f, const void* packed, size_t pac
 }
 
 static w4a16_status gemv_common(const w4a16_format* f, const void* packed, size_t packed_bytes,
-                                const uint16_t* x, uint16_t* y, int64_t M, int32_t rows16,
+                                const uint16_t* x, uint16_t* y, int64_t M, int32_t shape,
                                 int32_t ksplit, uint32_t flags, w4a16_stream_t stream) {
   w4a16_status s = blob_status(f, packed, packed_bytes);
   if (s != W4A16_OK) return s;
@@ -194,19 +194,23 @@ static w4a16_status gemv_common(const w4a16_format* f, const void* packed, size_
   const char* yb = reinterpret_cast<const char*>(y);
   const size_t xbytes = size_t(M) * size_t(f->K) * 2, ybytes = size_t(M) * size_t(f->N) * 2;
   if (xb < yb + ybytes && yb < xb + xbytes) return W4A16_ERR_INVALID_ARG;  // overlap
-  if (rows16 != 0 && rows16 != 2 && rows16 != 4 && rows16 != 8) return W4A16_ERR_INVALID_ARG;
+  if ((flags & ~uint32_t(W4A16_GEMV_WEIGHTS_READY | W4A16_GEMV_BULK_COPY | W4A16_GEMV_STAGE_ACTIVATIONS)) != 0)
+    return W4A16_ERR_INVALID_ARG;
+  const bool ring = (flags & W4A16_GEMV_BULK_COPY) == 0;
+  if (ring ? (shape != 0 && shape != 2 && shape != 4 && shape != 8) : (shape != 0 && (shape < 2 || shape > 8)))
+    return W4A16_ERR_INVALID_ARG;
   if (ksplit != 0 && ksplit != 1 && ksplit != 2 && ksplit != 4 && ksplit != 8 && ksplit != 16)
     return W4A16_ERR_INVALID_ARG;
-  if ((flags & ~uint32_t(W4A16_GEMV_WEIGHTS_READY)) != 0) return W4A16_ERR_INVALID_ARG;
   const Layout L = make_layout(*f);
   DeviceInfo dev;
   cudaError_t e = device_info(&dev);
   if (e != cudaSuccess) return cuda_fail(e);
-  GemvPlan plan = gemv_default_plan(L, int(M), dev);
-  if (rows16 != 0) plan.rows16 = rows16;
+  GemvPlan plan = gemv_default_plan(L, int(M), dev, ring ? kGemvRegisterRing : kGemvBulkCopy);
+  if (shape != 0) (ring ? plan.rows16 : plan.stages) = shape;
+  if (ring && (flags & W4A16_GEMV_STAGE_ACTIVATIONS) != 0) plan.stage_x = true;
   if (ksplit != 0) plan.ksplit = ksplit;
-  if (!gemv_plan_ok(L, int(M), plan)) return (rows16 || ksplit) ? W4A16_ERR_INVALID_ARG : W4A16_ERR_UNSUPPORTED;
-  e = launch_gemv(L, packed, x, y, int(M), plan, flags, stream);
+  if (!gemv_plan_ok(L, int(M), plan)) return (shape || ksplit) ? W4A16_ERR_INVALID_ARG : W4A16_ERR_UNSUPPORTED;
+  e = launch_gemv(L, packed, x, y, int(M), plan, flags & W4A16_GEMV_WEIGHTS_READY, stream);
   return e == cudaSuccess ? W4A16_OK : cuda_fail(e);
 }
 
@@ -216,9 +220,9 @@ w4a16_status w4a16_gemv(const w4a16_format* f, const void* packed, size_t packed
 }
 
 w4a16_status w4a16_gemv_ex(const w4a16_format* f, const void* packed, size_t packed_bytes,
-                           const uint16_t* x, uint16_t* y, int64_t M, int32_t rows16, int32_t ksplit,
+                           const uint16_t* x, uint16_t* y, int64_t M, int32_t shape, int32_t ksplit,
                            uint32_t flags, w4a16_stream_t stream) {
-  return gemv_common(f, packed, packed_bytes, x, y, M, rows16, ksplit, flags, stream);
+  return gemv_common(f, packed, packed_bytes, x, y, M, shape, ksplit, flags, stream);
 }
 
 size_t w4a16_gemm_workspace_bytes(const w4a16_format* f, int64_t M) {

@@ -29,13 +29,19 @@ cudaError_t launch_pack(const Layout& L, const uint8_t* q, const uint16_t* scale
 cudaError_t launch_dequant(const Layout& L, const void* blob, uint16_t* w_out,
                            cudaStream_t stream);
 
+constexpr int kGemvBulkCopy = 0;     // weights streamed by cp.async.bulk into a shared-memory ring
+constexpr int kGemvRegisterRing = 1; // weights loaded straight into a register ring
 struct GemvPlan {
-  int rows16;   // 16-row tiles per CTA (1, 2, 4, 8)
+  int kind;     // kGemvBulkCopy or kGemvRegisterRing
+  int rows16;   // register ring: 16-row tiles per CTA (2, 4, 8)
+  int stages;   // bulk copy: 16 KiB stages in the ring (2..8)
   int ksplit;   // CTAs per cluster along K
+  bool stage_x; // register ring: copy the block's activations to shared memory first
 };
-GemvPlan gemv_default_plan(const Layout& L, int M, const DeviceInfo& dev);
+GemvPlan gemv_default_plan(const Layout& L, int M, const DeviceInfo& dev, int kind);
 bool gemv_plan_ok(const Layout& L, int M, const GemvPlan& p);
 constexpr uint32_t kGemvWeightsReady = W4A16_GEMV_WEIGHTS_READY;
+constexpr uint32_t kGemvStageActivationsFlag = W4A16_GEMV_STAGE_ACTIVATIONS;
 cudaError_t launch_gemv(const Layout& L, const void* blob, const uint16_t* x, uint16_t* y,
                         int M, const GemvPlan& plan, uint32_t flags, cudaStream_t stream);
 
@@ -44,7 +50,9 @@ cudaError_t launch_gemv(const Layout& L, const void* blob, const uint16_t* x, ui
 cudaError_t launch_gemm(const Layout& L, const void* blob, const uint16_t* x, uint16_t* y,
                         int64_t M, void* workspace, int tile, cudaStream_t stream);
 
-// Device-side count of bounded pipeline waits that gave up (k_gemm.cu).
+// Device-side counts of bounded pipeline waits that gave up, read and reset
+// (k_gemm.cu for the GEMM, k_gemv.cu for the bulk-copy GEMV).
 cudaError_t take_pipeline_timeouts(unsigned int* count);
+cudaError_t take_gemv_timeouts(unsigned int* count);
 
 }  // namespace w4a16

@@ -544,7 +544,10 @@ cudaError_t take_pipeline_timeouts(unsigned int* count) {
     e = cudaMemcpyToSymbol(g_pipeline_timeouts, &zero, sizeof(zero));
     if (e != cudaSuccess) return e;
   }
-  *count = c;
+  unsigned int cv = 0;
+  e = take_gemv_timeouts(&cv);
+  if (e != cudaSuccess) return e;
+  *count = c + cv;
   return cudaSuccess;
 }
 

@@ -206,14 +206,21 @@ def dequant(fmt: Format, packed: torch.Tensor, out: torch.Tensor | None = None, 
 
 
 GEMV_WEIGHTS_READY = 1
+GEMV_BULK_COPY = 2
+GEMV_STAGE_ACTIVATIONS = 4
 
 
 def gemv(fmt: Format, packed: torch.Tensor, x: torch.Tensor, out: torch.Tensor | None = None,
-         rows16: int = 0, ksplit: int = 0, weights_ready: bool = False, stream=None) -> torch.Tensor:
+         shape: int = 0, ksplit: int = 0, weights_ready: bool = False, bulk_copy: bool = False,
+         stage_activations: bool = False, stream=None) -> torch.Tensor:
     """y = x . W_hat^T for x fp16 [M, K], 1 <= M <= 16.
 
     ``weights_ready``: the packed weights were complete before the previous
     kernel on the stream started, so the GEMV may stream them early.
+    ``bulk_copy``: the variant that streams weights into a shared-memory ring
+    with bulk copies; ``shape`` is then the ring depth in stages, else the
+    16-row tiles per thread block. ``stage_activations`` (default variant
+    only): copy the activations to shared memory first.
     """
     M = x.shape[0]
     pp = _dev(packed, torch.uint8, "packed")
@@ -221,9 +228,11 @@ def gemv(fmt: Format, packed: torch.Tensor, x: torch.Tensor, out: torch.Tensor |
     if out is None:
         out = torch.empty((M, fmt.N), dtype=torch.float16, device=x.device)
     yp = _dev(out, torch.float16, "out", (M, fmt.N))
-    if rows16 or ksplit or weights_ready:
-        st = lib().w4a16_gemv_ex(ctypes.byref(fmt), pp, packed.numel(), xp, yp, M, rows16, ksplit,
-                                 GEMV_WEIGHTS_READY if weights_ready else 0, _stream(stream))
+    flags = ((GEMV_WEIGHTS_READY if weights_ready else 0) | (GEMV_BULK_COPY if bulk_copy else 0)
+             | (GEMV_STAGE_ACTIVATIONS if stage_activations else 0))
+    if shape or ksplit or flags:
+        st = lib().w4a16_gemv_ex(ctypes.byref(fmt), pp, packed.numel(), xp, yp, M, shape, ksplit, flags,
+                                 _stream(stream))
     else:
         st = lib().w4a16_gemv(ctypes.byref(fmt), pp, packed.numel(), xp, yp, M, _stream(stream))
     _check("w4a16_gemv", st)
