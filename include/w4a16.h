@@ -256,8 +256,8 @@ W4A16_API w4a16_status w4a16_pipeline_timeouts(uint32_t* count);
 
 /*
  * w4a16_gemv with options.
- *   shape    0 = default. Default kernel (weights loaded straight into a
- *            ring of registers): 16-row tiles per thread block, 2, 4 or 8.
+ *   shape    0 = default. Register-ring and asynchronous-copy kernels:
+ *            16-row tiles per thread block, 2, 4 or 8.
  *            With W4A16_GEMV_BULK_COPY: the depth of the shared-memory ring
  *            in 16 KiB stages, 2..8.
  *   ksplit   thread blocks per cluster splitting K: 1, 2, 4, 8 or 16;
@@ -274,6 +274,24 @@ W4A16_API w4a16_status w4a16_pipeline_timeouts(uint32_t* count);
  *            W4A16_GEMV_STAGE_ACTIVATIONS: default kernel only: copy each
  *              thread block's activations to shared memory before the
  *              weight stream.
+ *            W4A16_GEMV_INPUTS_READY: stronger than WEIGHTS_READY: no
+ *              kernel still in flight on the stream writes `packed` or `x`,
+ *              or reads or writes `y` (for example k and v after q, which
+ *              read the same activations). The GEMV then does not wait for
+ *              the previous kernel at all and may run alongside it. A later
+ *              kernel that waits for this GEMV through programmatic
+ *              dependent launch no longer waits, through it, for the kernels
+ *              before it; work that depends on those must follow an
+ *              ordinary stream dependency.
+ *            W4A16_GEMV_ASYNC_COPY: the default kernel's plan, but every
+ *              thread lands its next units (codes, scales, zero points) with
+ *              asynchronous copies (cp.async) in a ring of shared-memory slots
+ *              instead of registers; `shape` stays the 16-row tiles per
+ *              thread block.
+ * With neither W4A16_GEMV_BULK_COPY nor W4A16_GEMV_ASYNC_COPY and shape 0,
+ * layers of at least 64 row blocks of 128 (N >= 8065) use the
+ * asynchronous-copy ring and smaller ones the register ring (measured on
+ * B300); w4a16_gemv always takes that default.
  * The GEMV kernels are launched with programmatic dependent launch, so a GEMV
  * may start while the previous kernel on the stream is still running; by
  * default it reads nothing from global memory before that kernel is done.
@@ -282,6 +300,8 @@ W4A16_API w4a16_status w4a16_pipeline_timeouts(uint32_t* count);
 #define W4A16_GEMV_WEIGHTS_READY 1u
 #define W4A16_GEMV_BULK_COPY 2u
 #define W4A16_GEMV_STAGE_ACTIVATIONS 4u
+#define W4A16_GEMV_ASYNC_COPY 8u
+#define W4A16_GEMV_INPUTS_READY 16u
 W4A16_API w4a16_status w4a16_gemv_ex(const w4a16_format* f, const void* packed, size_t packed_bytes,
                            const uint16_t* x, uint16_t* y, int64_t M, int32_t shape,
                            int32_t ksplit, uint32_t flags, w4a16_stream_t stream);

@@ -136,8 +136,9 @@ def test_gemv_argument_checks(lib):
     assert lib.w4a16_gemv_ex(ctypes.byref(f), FAKE, nb, X, Y, 1, 1, 1, bulk, None) == INVALID
     assert lib.w4a16_gemv_ex(ctypes.byref(f), FAKE, nb, X, Y, 1, 3, 1, 0, None) == INVALID      # rows16
     assert lib.w4a16_gemv_ex(ctypes.byref(f), FAKE, nb, X, Y, 1, 8, 32, 0, None) == INVALID
-    assert lib.w4a16_gemv_ex(ctypes.byref(f), FAKE, nb, X, Y, 1, 0, 0, 8, None) == INVALID     # unknown flag
-    assert lib.w4a16_gemv_ex(ctypes.byref(f), FAKE, nb, X, Y, 1, 0, 0, bulk | stage_x | 16, None) == INVALID
+    assert lib.w4a16_gemv_ex(ctypes.byref(f), FAKE, nb, X, Y, 1, 0, 0, 64, None) == INVALID    # unknown flag
+    assert lib.w4a16_gemv_ex(ctypes.byref(f), FAKE, nb, X, Y, 1, 0, 0, bulk | stage_x | 32, None) == INVALID
+    assert lib.w4a16_gemv_ex(ctypes.byref(f), FAKE, nb, X, Y, 1, 0, 0, bulk | 8, None) == INVALID  # two variants
 
 
 def test_gemm_and_workspace_checks(lib):

@@ -19,12 +19,13 @@ def to_dev(a):
     return torch.from_numpy(np.ascontiguousarray(a)).cuda()
 
 
-# register ring (default) / register ring with staged activations / shared-memory bulk-copy ring
-VARIANTS = ("ring", "ring_sx", "bulk")
+# register ring (default) / register ring with staged activations / shared-memory
+# bulk-copy ring fed by a producer warp / per-warp bulk-copy rings
+VARIANTS = ("ring", "ring_sx", "bulk", "async")
 
 
 def variant_kw(variant):
-    return dict(bulk_copy=variant == "bulk", stage_activations=variant == "ring_sx")
+    return dict(bulk_copy=variant == "bulk", stage_activations=variant == "ring_sx", async_copy=variant == "async")
 
 
 def run_case(N, K, M, g, sym, act, frac=0.01, tag="gemv", shape=0, ksplit=0, variant="ring"):
@@ -88,7 +89,7 @@ def test_act_order(cuda_ok, M, variant):
 @pytest.mark.parametrize("rows16", [2, 4, 8])
 @pytest.mark.parametrize("ksplit", [1, 2, 4, 8, 16])
 def test_every_register_ring_launch_shape(cuda_ok, rows16, ksplit):
-    for variant in ("ring", "ring_sx"):
+    for variant in ("ring", "ring_sx", "async"):
         y, y_ref, B = run_case(256, 2048, 3, 64, False, False, tag="plan", shape=rows16, ksplit=ksplit,
                                variant=variant)
         assert_within(y, y_ref, B)
@@ -188,3 +189,39 @@ def test_weights_ready_flag_matches_default(cuda_ok):
         b = W.gemv(fmt, packed, xd, weights_ready=True)
     assert np.array_equal(b.cpu().numpy().view(np.uint16), a.view(np.uint16))
     assert_within(a, y_ref, B)
+
+
+def test_inputs_ready_chain_matches(cuda_ok):
+    """GEMVs that read the same activations, launched without waiting for one
+    another (inputs ready), give the same outputs as when each waits."""
+    N, K = 1024, 4096
+    x = synth.activations_np(1, K, 0.01, 93)
+    xd = to_dev(x)
+    packs, fmt = [], W.make_format(N, K, 128, False, False)
+    for i in range(3):
+        q, s, z = W.quantize_rtn(fmt, to_dev(synth.weights_np(N, K, 94 + i)))
+        packs.append(W.pack(fmt, q, s, z))
+    torch.cuda.synchronize()
+    ref = [W.gemv(fmt, p, xd).cpu().numpy() for p in packs]
+    for variant in VARIANTS:
+        outs = [torch.empty((1, N), dtype=torch.float16, device="cuda") for _ in packs]
+        for i, p in enumerate(packs):
+            W.gemv(fmt, p, xd, out=outs[i], inputs_ready=i > 0, weights_ready=True, **variant_kw(variant))
+        torch.cuda.synchronize()
+        for i, (o, r) in enumerate(zip(outs, ref)):
+            got = o.cpu().numpy()
+            if variant == "ring":  # the default plan of this shape: same kernel, same order
+                assert np.array_equal(got.view(np.uint16), r.view(np.uint16))
+            else:
+                q, s, z = O.rtn_quantize(synth.weights_np(N, K, 94 + i), 128, False)
+                y_ref, B = O.linear_ref(x, O.dequant(q, s, z, 128))
+                assert_within(got, y_ref, B)
+    assert W.pipeline_timeouts() == 0
+
+
+def test_default_picks_async_ring_for_large_layers(cuda_ok):
+    """The default plan switches kernels at 64 row blocks; both sides match the oracle."""
+    for N in (8064, 8192):
+        K = 1024
+        y, y_ref, B = run_case(N, K, 1, 128, False, False, tag="switch")
+        assert_within(y, y_ref, B)

@@ -31,10 +31,11 @@ cudaError_t launch_dequant(const Layout& L, const void* blob, uint16_t* w_out,
 
 constexpr int kGemvBulkCopy = 0;     // weights streamed by cp.async.bulk into a shared-memory ring
 constexpr int kGemvRegisterRing = 1; // weights loaded straight into a register ring
+constexpr int kGemvAsyncCopy = 2;    // each thread lands its own weight loads in a shared-memory ring (cp.async)
 struct GemvPlan {
   int kind;     // kGemvBulkCopy or kGemvRegisterRing
   int rows16;   // register ring: 16-row tiles per CTA (2, 4, 8)
-  int stages;   // bulk copy: 16 KiB stages in the ring (2..8)
+  int stages;   // bulk copy: 16 KiB stages in the ring (2..8); async copy: units in flight (fixed at 4)
   int ksplit;   // CTAs per cluster along K
   bool stage_x; // register ring: copy the block's activations to shared memory first
 };
@@ -42,6 +43,8 @@ GemvPlan gemv_default_plan(const Layout& L, int M, const DeviceInfo& dev, int ki
 bool gemv_plan_ok(const Layout& L, int M, const GemvPlan& p);
 constexpr uint32_t kGemvWeightsReady = W4A16_GEMV_WEIGHTS_READY;
 constexpr uint32_t kGemvStageActivationsFlag = W4A16_GEMV_STAGE_ACTIVATIONS;
+constexpr uint32_t kGemvAsyncCopyFlag = W4A16_GEMV_ASYNC_COPY;
+constexpr uint32_t kGemvInputsReady = W4A16_GEMV_INPUTS_READY;
 cudaError_t launch_gemv(const Layout& L, const void* blob, const uint16_t* x, uint16_t* y,
                         int M, const GemvPlan& plan, uint32_t flags, cudaStream_t stream);
 

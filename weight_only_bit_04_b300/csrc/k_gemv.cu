@@ -49,6 +49,8 @@ namespace {
 constexpr int kWarps = 8;
 constexpr int kThreads = kWarps * 32;
 constexpr int kTilesPerWarp = 2;
+constexpr uint64_t kTWaitLimitNs = 1000ull * 1000ull * 1000ull;  // every pipeline wait gives up after 1 s
+__device__ unsigned int g_gemv_timeouts;  // bounded waits that gave up (see w4a16_pipeline_timeouts)
 
 struct GemvArgs {
   const uint32_t* qweight;
@@ -61,6 +63,9 @@ struct GemvArgs {
   int rows16;      // 16-row tiles per thread block (2, 4 or 8)
   int kb_per_cta;  // 64-column blocks per thread block (the last blocks of a cluster may get fewer)
   uint32_t flags;  // kGemvWeightsReady
+  int depth;       // warp bulk-copy ring: units in flight per warp
+  int wb_off;      // warp bulk-copy ring: byte offset of the rings in shared memory
+  int slot_bytes;  // warp bulk-copy ring: bytes of one slot
 };
 
 // Scale and zero for the rows (g, g+8) of one tile and one group, folded into
@@ -234,14 +239,43 @@ __device__ __forceinline__ void stage_activations(const uint16_t* __restrict__ x
   }
 }
 
+// Asynchronous-copy ring (WB): instead of holding the next units in
+// registers, every thread lands its own 16-byte code loads, scale pairs and
+// zero-point words with cp.async (LDGSTS) in a ring of shared-memory slots and
+// reads back only what it copied itself: the bytes in flight no longer cost
+// registers, and no thread waits for another (cp.async.wait_group only).
+// Slot layout, per field, one entry per thread of the block (conflict-free):
+//   codes [kBlocks][2 tiles] 16 B, scales [kGroups][2 tiles] 4 B,
+//   zero words [kGroups][2 tiles] 4 B (the word holding this row pair's byte).
+template <int GS>
+struct WbSlot {
+  static constexpr int kCodeFields = Unit<GS>::kBlocks * kTilesPerWarp;
+  static constexpr int kMetaFields = Unit<GS>::kGroups * kTilesPerWarp;
+  static constexpr int kScaleOff = kCodeFields * kThreads * 16;
+  static constexpr int kZeroOff = kScaleOff + kMetaFields * kThreads * 4;
+  static constexpr int kBytes = kZeroOff + kMetaFields * kThreads * 4;
+};
+__host__ __device__ inline int wb_slot_bytes(int GS) {
+  return GS == 128 ? WbSlot<128>::kBytes : GS == 64 ? WbSlot<64>::kBytes : WbSlot<32>::kBytes;
+}
+
+__device__ __forceinline__ void cp_async_4(void* smem_dst, const void* gmem_src) {
+  const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(smem_dst));
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(d), "l"(gmem_src) : "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait_group() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
 // STAGED: gather x into shared memory first (act order, K not a multiple of
 // 64, or on request).
-template <int MP, int GS, bool SYM, bool STAGED>
+template <int MP, int GS, bool SYM, bool STAGED, bool WB>
 __global__ void __launch_bounds__(kThreads) gemv_kernel(const GemvArgs a) {
-  extern __shared__ __align__(16) unsigned char smem[];
+  extern __shared__ __align__(128) unsigned char smem[];
   constexpr int NB = MP > 8 ? 2 : 1;
   using U = Unit<GS>;
-  constexpr int PF = U::kInFlight;
+  constexpr int PF = WB ? 1 : U::kInFlight;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int g = lane >> 2, t = lane & 3;
@@ -270,22 +304,57 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const GemvArgs a) {
   const uint8_t* zp = SYM ? nullptr : a.zeros + (size_t(R) * G * 8 + r16) * 8 + g + size_t(u0) * U::kGroups * 64;
 
   const bool early = (a.flags & kGemvWeightsReady) != 0;
-  if (!early) {
-    pdl_wait();
-    pdl_launch_dependents();
-  }
-  UnitRegs<GS> ring[PF];
+  const int M = a.M;
+
+  // ---- asynchronous-copy ring: this thread's entries of every slot
+  using SL = WbSlot<GS>;
+  constexpr int D = 4;  // units in flight per thread
+  const int tid = int(threadIdx.x);
+  unsigned char* ringb = smem + a.wb_off;
+  auto issue_unit = [&](int i) {  // unit u0 + i into slot i % D, one commit group
+    if (i < nunit) {
+      unsigned char* slot = ringb + size_t(i % D) * SL::kBytes;
 #pragma unroll
-  for (int s = 0; s < PF; ++s)
-    if (s < nunit) load_unit<GS, SYM>(ring[s], qp, sp, zp, s, gmax);
-  if (early) {
-    pdl_wait();
-    pdl_launch_dependents();
+      for (int bb = 0; bb < U::kBlocks; ++bb)
+#pragma unroll
+        for (int tt = 0; tt < kTilesPerWarp; ++tt)
+          cp_async_16(slot + ((bb * kTilesPerWarp + tt) * kThreads + tid) * 16,
+                      qp + (i * U::kBlocks + bb) * 1024 + tt * 128);
+#pragma unroll
+      for (int gg = 0; gg < U::kGroups; ++gg) {
+        const int gi = GS == 32 ? min(i * U::kGroups + gg, gmax) : i * U::kGroups + gg;
+#pragma unroll
+        for (int tt = 0; tt < kTilesPerWarp; ++tt) {
+          const int f = gg * kTilesPerWarp + tt;
+          cp_async_4(slot + SL::kScaleOff + (f * kThreads + tid) * 4, sp + gi * 64 + tt * 8);
+          if (!SYM)  // the aligned word holding this lane's zero byte
+            cp_async_4(slot + SL::kZeroOff + (f * kThreads + tid) * 4,
+                       reinterpret_cast<const uint32_t*>(reinterpret_cast<uintptr_t>(zp + gi * 64 + tt * 8) & ~uintptr_t(3)));
+        }
+      }
+    }
+    cp_async_commit();
+  };
+
+  // The next kernel may be scheduled right away: its griddepcontrol.wait still
+  // waits for this grid to complete, but its blocks can become resident and
+  // start their own weight stream while this one runs.
+  pdl_launch_dependents();
+  const bool inputs_ready = (a.flags & kGemvInputsReady) != 0;  // nothing in flight writes x: no wait at all
+  if (!early && !inputs_ready) pdl_wait();
+  UnitRegs<GS> ring[PF];
+  if (WB) {
+#pragma unroll
+    for (int i = 0; i < D; ++i) issue_unit(i);
+  } else {
+#pragma unroll
+    for (int s = 0; s < PF; ++s)
+      if (s < nunit) load_unit<GS, SYM>(ring[s], qp, sp, zp, s, gmax);
   }
+  if (early && !inputs_ready) pdl_wait();
 
   // Activations: lanes of absent tokens read a real row (their outputs are
   // never stored), so no masking is needed.
-  const int M = a.M;
   const int tok0 = min(g, M - 1);
   const int tok1 = min(g + 8, M - 1);
   const uint16_t* xl0;
@@ -315,14 +384,42 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const GemvArgs a) {
 #pragma unroll
       for (int i = 0; i < 4; ++i) tot[tt][nb][i] = 0.f;
 
-  for (int i0 = 0; i0 < nunit; i0 += PF) {
+  if (WB) {
+    const int zshift = int((reinterpret_cast<uintptr_t>(zp) & 3u) * 8);  // this lane's byte in its zero word
+    for (int i = 0; i < nunit; ++i) {
+      cp_async_wait_group<D - 1>();  // unit i has landed (this thread's copies)
+      const unsigned char* slot = ringb + size_t(i % D) * SL::kBytes;
+      UnitRegs<GS> r;
 #pragma unroll
-    for (int s = 0; s < PF; ++s) {
-      const int i = i0 + s;
-      if (i < nunit) {
-        const int xo = i * U::kBlocks * kColsPerBlock;
-        compute_unit<NB, GS, SYM, STAGED>(ring[s], xl0 + xo, xl1 + xo, tot);
-        if (i + PF < nunit) load_unit<GS, SYM>(ring[s], qp, sp, zp, i + PF, gmax);
+      for (int bb = 0; bb < U::kBlocks; ++bb)
+#pragma unroll
+        for (int tt = 0; tt < kTilesPerWarp; ++tt)
+          r.w[bb][tt] = *reinterpret_cast<const uint4*>(slot + ((bb * kTilesPerWarp + tt) * kThreads + tid) * 16);
+#pragma unroll
+      for (int gg = 0; gg < U::kGroups; ++gg)
+#pragma unroll
+        for (int tt = 0; tt < kTilesPerWarp; ++tt) {
+          const int f = gg * kTilesPerWarp + tt;
+          r.s[gg][tt] = *reinterpret_cast<const uint32_t*>(slot + SL::kScaleOff + (f * kThreads + tid) * 4);
+          r.z[gg][tt] = SYM ? 0u
+                            : (*reinterpret_cast<const uint32_t*>(slot + SL::kZeroOff + (f * kThreads + tid) * 4) >>
+                               zshift) & 0xFFu;
+        }
+      const int xo = i * U::kBlocks * kColsPerBlock;
+      compute_unit<NB, GS, SYM, STAGED>(r, xl0 + xo, xl1 + xo, tot);
+      issue_unit(i + D);  // refills the slot just read (this thread's own entries)
+    }
+    cp_async_wait_all();
+  } else {
+    for (int i0 = 0; i0 < nunit; i0 += PF) {
+#pragma unroll
+      for (int s = 0; s < PF; ++s) {
+        const int i = i0 + s;
+        if (i < nunit) {
+          const int xo = i * U::kBlocks * kColsPerBlock;
+          compute_unit<NB, GS, SYM, STAGED>(ring[s], xl0 + xo, xl1 + xo, tot);
+          if (i + PF < nunit) load_unit<GS, SYM>(ring[s], qp, sp, zp, i + PF, gmax);
+        }
       }
     }
   }
@@ -391,7 +488,6 @@ constexpr int kTConsumers = 8;                      // one warp per 16-row tile 
 constexpr int kTThreads = (kTConsumers + 1) * 32;   // + one producer warp
 constexpr int kTStageBlocks = 4;                    // 64-column blocks per stage (16 KiB of codes)
 constexpr int kTMaxStages = 8;
-constexpr uint64_t kTWaitLimitNs = 1000ull * 1000ull * 1000ull;
 
 template <int GS>
 struct TStage {
@@ -433,7 +529,6 @@ __host__ __device__ inline size_t tma_xs_bytes(bool staged, int M, int kb_per_ct
 }
 constexpr int kXsumTokens = 8;  // activation sums are precomputed for up to 8 tokens
 
-__device__ unsigned int g_gemv_timeouts;  // bounded waits that gave up (see w4a16_pipeline_timeouts)
 
 template <int MP, int GS, bool SYM, bool STAGED>
 __global__ void __launch_bounds__(kTThreads) gemv_tma_kernel(const GemvTmaArgs a) {
@@ -501,10 +596,10 @@ __global__ void __launch_bounds__(kTThreads) gemv_tma_kernel(const GemvTmaArgs a
         // the weights of the first stages stream while the previous kernel finishes
         issued = min(NS, nst);
         for (int st = 0; st < issued; ++st) issue_weights(st);
-        pdl_wait();
+        if ((a.flags & kGemvInputsReady) == 0) pdl_wait();
         if (!STAGED)
           for (int st = 0; st < issued; ++st) issue_acts(st);
-      } else {
+      } else if ((a.flags & kGemvInputsReady) == 0) {
         pdl_wait();
       }
       for (int st = issued; st < nst; ++st) {
@@ -526,7 +621,8 @@ __global__ void __launch_bounds__(kTThreads) gemv_tma_kernel(const GemvTmaArgs a
     }
   } else {
     // ------------------------------------------------ consumers
-    pdl_wait();  // activations (and, under act order, the column order) may come from the previous kernel
+    // activations (and, under act order, the column order) may come from the previous kernel
+    if ((a.flags & kGemvInputsReady) == 0) pdl_wait();
     const int g = lane >> 2, t = lane & 3;
     const int M = a.M;
     const int tok0 = min(g, M - 1);
@@ -730,9 +826,9 @@ size_t gemv_smem_bytes(int M, int kb_per_cta, bool staged) {
   return xs > red ? xs : red;
 }
 
-template <int MP, int GS, bool SYM, bool STAGED>
+template <int MP, int GS, bool SYM, bool STAGED, bool WB>
 cudaError_t launch_typed(const GemvArgs& a, int KS, size_t smem_bytes, cudaStream_t stream) {
-  auto kern = gemv_kernel<MP, GS, SYM, STAGED>;
+  auto kern = gemv_kernel<MP, GS, SYM, STAGED, WB>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem_bytes));
   if (e != cudaSuccess) return e;
   if (KS > 8) {
@@ -764,27 +860,54 @@ cudaError_t launch_typed(const GemvArgs& a, int KS, size_t smem_bytes, cudaStrea
   return cudaGetLastError();
 }
 
-template <int MP, int GS>
+template <int MP, int GS, bool WB>
 cudaError_t launch_flags(const GemvArgs& a, bool sym, bool staged, int KS, size_t smem, cudaStream_t stream) {
   if (staged) {
-    return sym ? launch_typed<MP, GS, true, true>(a, KS, smem, stream)
-               : launch_typed<MP, GS, false, true>(a, KS, smem, stream);
+    return sym ? launch_typed<MP, GS, true, true, WB>(a, KS, smem, stream)
+               : launch_typed<MP, GS, false, true, WB>(a, KS, smem, stream);
   }
-  return sym ? launch_typed<MP, GS, true, false>(a, KS, smem, stream)
-             : launch_typed<MP, GS, false, false>(a, KS, smem, stream);
+  return sym ? launch_typed<MP, GS, true, false, WB>(a, KS, smem, stream)
+             : launch_typed<MP, GS, false, false, WB>(a, KS, smem, stream);
 }
 
 template <int MP>
-cudaError_t launch_gs(const GemvArgs& a, int gs, bool sym, bool staged, int KS, size_t smem,
+cudaError_t launch_gs(const GemvArgs& a, int gs, bool sym, bool staged, bool wb, int KS, size_t smem,
                       cudaStream_t stream) {
+  if (wb) {
+    switch (gs) {
+      case 32: return launch_flags<MP, 32, true>(a, sym, staged, KS, smem, stream);
+      case 64: return launch_flags<MP, 64, true>(a, sym, staged, KS, smem, stream);
+      default: return launch_flags<MP, 128, true>(a, sym, staged, KS, smem, stream);
+    }
+  }
   switch (gs) {
-    case 32: return launch_flags<MP, 32>(a, sym, staged, KS, smem, stream);
-    case 64: return launch_flags<MP, 64>(a, sym, staged, KS, smem, stream);
-    default: return launch_flags<MP, 128>(a, sym, staged, KS, smem, stream);
+    case 32: return launch_flags<MP, 32, false>(a, sym, staged, KS, smem, stream);
+    case 64: return launch_flags<MP, 64, false>(a, sym, staged, KS, smem, stream);
+    default: return launch_flags<MP, 128, false>(a, sym, staged, KS, smem, stream);
   }
 }
 
-constexpr size_t kMaxGemvSmem = 100 * 1024;
+// Shared memory of the register / warp-bulk kernel: staged activations or the
+// reduction buffers at offset 0, then (WB) the warps' rings and barriers.
+struct RingSmem {
+  size_t total;
+  int wb_off, slot_bytes;
+};
+RingSmem ring_smem(const Layout& L, int M, int kb_per_cta, bool staged, bool wb, int depth) {
+  RingSmem r{};
+  const size_t base = gemv_smem_bytes(M, kb_per_cta, staged);
+  if (!wb) {
+    r.total = base;
+    return r;
+  }
+  r.wb_off = int((base + 127) / 128 * 128);
+  r.slot_bytes = wb_slot_bytes(L.gsize);
+  r.total = size_t(r.wb_off) + size_t(4) * r.slot_bytes;  // 4 slots
+  (void)depth;
+  return r;
+}
+
+constexpr size_t kMaxGemvSmem = 200 * 1024;
 
 // Activations go through shared memory under act order, or when the last
 // 64-column block is ragged (its padding columns must read as zero).
@@ -872,27 +995,31 @@ bool valid_ksplit(int ks) { return ks == 1 || ks == 2 || ks == 4 || ks == 8 || k
 
 bool gemv_plan_ok(const Layout& L, int M, const GemvPlan& p) {
   if (!valid_ksplit(p.ksplit)) return false;
-  if (p.kind == kGemvRegisterRing) {
+  if (p.kind == kGemvRegisterRing || p.kind == kGemvAsyncCopy) {
     if (p.rows16 != 2 && p.rows16 != 4 && p.rows16 != 8) return false;
-    return gemv_smem_bytes(M, kb_per_cta_of(L, p.ksplit), gemv_staged(L) || p.stage_x) <= kMaxGemvSmem;
+    const bool wb = p.kind == kGemvAsyncCopy;
+    if (wb && (p.stages < 2 || p.stages > kTMaxStages)) return false;
+    return ring_smem(L, M, kb_per_cta_of(L, p.ksplit), gemv_staged(L) || p.stage_x, wb, p.stages).total <=
+           kMaxGemvSmem;
   }
   if (p.stages < 2 || p.stages > kTMaxStages) return false;
   return tma_smem_bytes(L, M, p.stages, kb_per_cta_of(L, p.ksplit)) <= kMaxTmaSmem;
 }
 
 GemvPlan gemv_default_plan(const Layout& L, int M, const DeviceInfo& dev, int kind) {
-  if (kind == kGemvRegisterRing) {
+  if (kind == kGemvRegisterRing || kind == kGemvAsyncCopy) {
     // Measured on B300 (graph-replayed sweeps of 4096..28672-row layers): the
     // register-ring stream runs best with about 1.35 thread blocks per SM,
     // each warp keeping at least two 64-column blocks; among equally close
     // plans, fewer K splits and then fewer rows per block win.
     const int64_t ntiles = L.NR * 8;
     const double target = 1.35 * dev.sm_count;
-    GemvPlan best{kGemvRegisterRing, 8, 0, 1, false};
+    const int depth = kind == kGemvAsyncCopy ? 4 : 0;
+    GemvPlan best{kind, 8, depth, 1, false};
     double best_dist = 1e30;
     for (int ks : {1, 2, 4, 8, 16}) {
       for (int rt : {2, 4, 8}) {
-        GemvPlan p{kGemvRegisterRing, rt, 0, ks, false};
+        GemvPlan p{kind, rt, depth, ks, false};
         if (!gemv_plan_ok(L, M, p)) continue;
         const int64_t ctas = (ntiles / rt) * ks;
         const int64_t kbc = kb_per_cta_of(L, ks);
@@ -972,12 +1099,17 @@ cudaError_t launch_gemv(const Layout& L, const void* blob, const uint16_t* x, ui
   a.kb_per_cta = kb_per_cta_of(L, plan.ksplit);
   a.flags = flags;
   const bool ring_staged = staged || plan.stage_x;
-  const size_t smem = gemv_smem_bytes(M, a.kb_per_cta, ring_staged);
-  if (M <= 1) return launch_gs<1>(a, gs, L.sym, ring_staged, plan.ksplit, smem, stream);
-  if (M <= 2) return launch_gs<2>(a, gs, L.sym, ring_staged, plan.ksplit, smem, stream);
-  if (M <= 4) return launch_gs<4>(a, gs, L.sym, ring_staged, plan.ksplit, smem, stream);
-  if (M <= 8) return launch_gs<8>(a, gs, L.sym, ring_staged, plan.ksplit, smem, stream);
-  return launch_gs<16>(a, gs, L.sym, ring_staged, plan.ksplit, smem, stream);
+  const bool wb = plan.kind == kGemvAsyncCopy;
+  const RingSmem rs = ring_smem(L, M, a.kb_per_cta, ring_staged, wb, plan.stages);
+  a.depth = wb ? plan.stages : 1;
+  a.wb_off = rs.wb_off;
+  a.slot_bytes = rs.slot_bytes;
+  const size_t smem = rs.total;
+  if (M <= 1) return launch_gs<1>(a, gs, L.sym, ring_staged, wb, plan.ksplit, smem, stream);
+  if (M <= 2) return launch_gs<2>(a, gs, L.sym, ring_staged, wb, plan.ksplit, smem, stream);
+  if (M <= 4) return launch_gs<4>(a, gs, L.sym, ring_staged, wb, plan.ksplit, smem, stream);
+  if (M <= 8) return launch_gs<8>(a, gs, L.sym, ring_staged, wb, plan.ksplit, smem, stream);
+  return launch_gs<16>(a, gs, L.sym, ring_staged, wb, plan.ksplit, smem, stream);
 }
 
 cudaError_t take_gemv_timeouts(unsigned int* count) {
