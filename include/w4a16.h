@@ -235,16 +235,23 @@ W4A16_API w4a16_status w4a16_gemm(const w4a16_format* f, const void* packed, siz
                         size_t workspace_bytes, w4a16_stream_t stream);
 
 /*
- * w4a16_gemm with the thread-block tile chosen by the caller:
- *   tile  0 = default (3), 1 = 128 weight rows x 256 tokens,
- *         2 = 256 weight rows x 128 tokens, 3 = 128 x 256 with twice the
- *         dequantization warps of 1, 4 = 128 x 256 with half of them.
- * Results equal w4a16_gemm's up to summation order (bit-identical in
- * practice: every tile sums the same products in the same K order).
+ * w4a16_gemm with the launch shape chosen by the caller:
+ *   tile    0 = default, 1 = 128 weight rows x 256 tokens per thread block,
+ *           2 = 256 x 128, 3 = 128 x 256 with twice the dequantization warps
+ *           of 1, 4 = 128 x 256 with half of them, 5 = 128 x 128 and
+ *           6 = 128 x 64 (two thread blocks per SM).
+ *   ksplit  thread blocks of a cluster that split K (1, 2, 4, 8 or 16; their
+ *           fp32 partial sums are added in rank order through distributed
+ *           shared memory); 0 = default (1 when `tile` is given).
+ * By default up to 64 tokens use tile 6, up to 128 tile 5 and more tokens
+ * tile 3, with K split so that the grid covers the SMs (at least 8 steps of
+ * 64 columns per thread block). Results match w4a16_gemm's within the
+ * error bound (the summation order depends on ksplit).
  */
 W4A16_API w4a16_status w4a16_gemm_ex(const w4a16_format* f, const void* packed, size_t packed_bytes,
                            const uint16_t* x, uint16_t* y, int64_t M, void* workspace,
-                           size_t workspace_bytes, int32_t tile, w4a16_stream_t stream);
+                           size_t workspace_bytes, int32_t tile, int32_t ksplit,
+                           w4a16_stream_t stream);
 
 /*
  * Number of bounded pipeline waits on the current device that gave up since

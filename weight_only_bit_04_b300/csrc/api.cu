@@ -242,12 +242,14 @@ size_t w4a16_gemm_workspace_bytes(const w4a16_format* f, int64_t M) {
 
 static w4a16_status gemm_common(const w4a16_format* f, const void* packed, size_t packed_bytes,
                                 const uint16_t* x, uint16_t* y, int64_t M, void* workspace,
-                                size_t workspace_bytes, int32_t tile, w4a16_stream_t stream) {
+                                size_t workspace_bytes, int32_t tile, int32_t ksplit, w4a16_stream_t stream) {
   w4a16_status s = blob_status(f, packed, packed_bytes);
   if (s != W4A16_OK) return s;
   if (x == nullptr || y == nullptr) return W4A16_ERR_INVALID_ARG;
   if (M < 1 || M > (int64_t(1) << 20)) return W4A16_ERR_INVALID_ARG;
-  if (tile < 0 || tile > 4) return W4A16_ERR_INVALID_ARG;
+  if (tile < 0 || tile > 6) return W4A16_ERR_INVALID_ARG;
+  if (ksplit != 0 && ksplit != 1 && ksplit != 2 && ksplit != 4 && ksplit != 8 && ksplit != 16)
+    return W4A16_ERR_INVALID_ARG;
   if (!aligned(x, 16) || !aligned(y, 16)) return W4A16_ERR_MISALIGNED;
   const size_t xbytes = size_t(M) * size_t(f->K) * 2, ybytes = size_t(M) * size_t(f->N) * 2;
   const char* xb = reinterpret_cast<const char*>(x);
@@ -264,21 +266,29 @@ static w4a16_status gemm_common(const w4a16_format* f, const void* packed, size_
   DeviceInfo dev;
   cudaError_t e = device_info(&dev);
   if (e != cudaSuccess) return cuda_fail(e);
-  if (dev.cc_major * 10 + dev.cc_minor < 100) return W4A16_ERR_UNSUPPORTED;  // tcgen05 needs Blackwell
-  e = launch_gemm(make_layout(*f), packed, x, y, M, workspace, tile == 0 ? 3 : tile, stream);
+  if (dev.cc_major != 10) return W4A16_ERR_UNSUPPORTED;  // tcgen05 needs a Blackwell datacenter GPU
+  const Layout L = make_layout(*f);
+  GemmPlan plan = gemm_default_plan(L, M, dev.sm_count);
+  if (tile != 0) {
+    plan.tile = tile;
+    if (ksplit == 0) plan.ksplit = 1;
+  }
+  if (ksplit != 0) plan.ksplit = ksplit;
+  if (!gemm_plan_ok(L, plan)) return W4A16_ERR_INVALID_ARG;
+  e = launch_gemm(L, packed, x, y, M, workspace, plan, stream);
   return e == cudaSuccess ? W4A16_OK : cuda_fail(e);
 }
 
 w4a16_status w4a16_gemm(const w4a16_format* f, const void* packed, size_t packed_bytes,
                         const uint16_t* x, uint16_t* y, int64_t M, void* workspace,
                         size_t workspace_bytes, w4a16_stream_t stream) {
-  return gemm_common(f, packed, packed_bytes, x, y, M, workspace, workspace_bytes, 0, stream);
+  return gemm_common(f, packed, packed_bytes, x, y, M, workspace, workspace_bytes, 0, 0, stream);
 }
 
 w4a16_status w4a16_gemm_ex(const w4a16_format* f, const void* packed, size_t packed_bytes,
                            const uint16_t* x, uint16_t* y, int64_t M, void* workspace,
-                           size_t workspace_bytes, int32_t tile, w4a16_stream_t stream) {
-  return gemm_common(f, packed, packed_bytes, x, y, M, workspace, workspace_bytes, tile, stream);
+                           size_t workspace_bytes, int32_t tile, int32_t ksplit, w4a16_stream_t stream) {
+  return gemm_common(f, packed, packed_bytes, x, y, M, workspace, workspace_bytes, tile, ksplit, stream);
 }
 
 w4a16_status w4a16_pipeline_timeouts(uint32_t* count) {

@@ -48,10 +48,19 @@ constexpr uint32_t kGemvInputsReady = W4A16_GEMV_INPUTS_READY;
 cudaError_t launch_gemv(const Layout& L, const void* blob, const uint16_t* x, uint16_t* y,
                         int M, const GemvPlan& plan, uint32_t flags, cudaStream_t stream);
 
-// tile: 1 = 128 weight rows x 256 tokens per thread block (2 dequantization warp
-// sets), 2 = 256 rows x 128 tokens (2 sets), 3 = 128 x 256 with 4 sets, 4 = 128 x 256 with 1 set.
+// GEMM plan. tile: 1 = 128 weight rows x 256 tokens per thread block (2
+// dequantization warp sets), 2 = 256 rows x 128 tokens (2 sets), 3 = 128 x 256
+// with 4 sets, 4 = 128 x 256 with 1 set, 5 = 128 x 128 (2 sets, two blocks per
+// SM), 6 = 128 x 64 (2 sets, two blocks per SM). ksplit: blocks of a cluster
+// splitting K (1, 2, 4, 8, 16).
+struct GemmPlan {
+  int tile;
+  int ksplit;
+};
+GemmPlan gemm_default_plan(const Layout& L, int64_t M, int sm_count);
+bool gemm_plan_ok(const Layout& L, const GemmPlan& p);
 cudaError_t launch_gemm(const Layout& L, const void* blob, const uint16_t* x, uint16_t* y,
-                        int64_t M, void* workspace, int tile, cudaStream_t stream);
+                        int64_t M, void* workspace, const GemmPlan& plan, cudaStream_t stream);
 
 // Device-side counts of bounded pipeline waits that gave up, read and reset
 // (k_gemm.cu for the GEMM, k_gemv.cu for the bulk-copy GEMV).

@@ -6,14 +6,15 @@
 // why decoding gets faster": 4-bit weights are expanded to 16 bits before the
 // multiply). The weights enter the MMA from tensor memory:
 //
-//  * One thread block owns WR x 128 weight rows and NT tokens. Per 64-column
-//    step, dequantization warps read the 4 KiB packed tile of each 128-row
-//    block (coalesced 16-byte loads, several steps ahead in registers), expand
-//    the nibbles to w_hat = fp16((q - z) * s) -- the same rounding as
+//  * One thread block owns WR x 128 weight rows and NT tokens. A TMA warp
+//    streams, per 64-column step, the activations (NT tokens x 64 columns,
+//    128-byte swizzle: the MMA's B operand) and the 4 KiB packed tile of each
+//    128-row block with its scales and zero points (bulk copies) into a ring
+//    of shared-memory stages, several steps ahead.
+//  * Dequantization warps read a stage's packed tile from shared memory,
+//    expand the nibbles to w_hat = fp16((q - z) * s) -- the same rounding as
 //    w4a16_dequant -- and store them into tensor memory with tcgen05.st: they
 //    are the MMA's A operand (lane = weight row, two fp16 per 32-bit column).
-//  * A TMA warp streams the activations (NT tokens x 64 columns, 128-byte
-//    swizzle) into a ring of shared-memory stages; they are the B operand.
 //  * One thread issues tcgen05.mma (M = 128 weight rows, N = NT tokens,
 //    K = 16) into fp32 accumulators in tensor memory and releases each
 //    stage with tcgen05.commit.
@@ -29,6 +30,7 @@
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
+#include <cmath>
 #include <mutex>
 
 #include "device_util.cuh"
@@ -42,13 +44,19 @@ __device__ unsigned int g_pipeline_timeouts;
 namespace {
 
 constexpr uint64_t kWaitLimitNs = 1000ull * 1000ull * 1000ull;  // 1 s per wait
-constexpr int kTmemCols = 512;
 
 // WR: 128-row weight blocks per thread block; NT: tokens per thread block;
 // SA: tensor-memory stages of dequantized weights; SB: shared-memory stages of
 // activations; DS: dequantization warp sets, set d producing the 64-column
 // steps kb = d (mod DS), so that each scheduler interleaves DS independent
 // dequantization streams.
+// Packed-weight part of a stage, per 128-row tile: the 4 KiB code tile, then
+// up to two groups of scale pairs (256 B each) and of zero bytes (64 B each).
+constexpr int kWCodes = 4096;
+constexpr int kWScaleOff = kWCodes;
+constexpr int kWZeroOff = kWScaleOff + 2 * 256;
+constexpr int kWTile = kWZeroOff + 2 * 64;
+
 template <int WR, int NT, int SA, int SB, int DS>
 struct Cfg {
   static constexpr int kSetWarps = 4 * WR;        // one warp per (128-row tile, lane quarter)
@@ -58,17 +66,19 @@ struct Cfg {
   static constexpr int kThreads = (kDeqWarps + 2) * 32;
   static constexpr int kDCols = WR * NT;          // fp32 accumulators
   static constexpr int kACol0 = kDCols;           // first A column
-  static constexpr int kBStage = NT * 128;        // NT rows x 64 fp16
+  static constexpr int kBStage = NT * 128;        // activations: NT rows x 64 fp16 (128-byte swizzle)
+  static constexpr int kStage = (kBStage + WR * kWTile + 1023) / 1024 * 1024;  // + packed weights
   static constexpr int kBarBytes = 8 * (SA * 2 + SB * 2 + 1) + 16;
-  static constexpr int kSmem = SB * kBStage + 1024 + kBarBytes;
+  static constexpr int kSmem = SB * kStage + 1024 + kBarBytes;
   static constexpr int kEpiTokens = NT / DS;      // tokens each set writes back
-  // packed steps each dequantization warp keeps in flight (fewer when the
-  // block is large enough for the register file to cap every thread at 96)
-  static constexpr int kPrefetch = kThreads > 512 ? 2 : 4;
-  static_assert(kDCols + SA * WR * 32 <= kTmemCols, "tensor memory budget");
+  // tensor-memory columns allocated: 256 lets two blocks share an SM
+  static constexpr int kTmemCols = kDCols + SA * WR * 32 <= 256 ? 256 : 512;
+  static_assert(kDCols + SA * WR * 32 <= 512, "tensor memory budget");
+  static_assert(kSmem <= 232448, "shared memory per block");
+  static_assert(NT * WR * 128 * 4 <= SB * kStage, "split-K partial sums must fit in the stages");
   static_assert(SA % DS == 0, "each tensor-memory stage belongs to one set");
   static_assert(kEpiTokens % 32 == 0, "epilogue in 32-token chunks");
-  static_assert(kDeqWarps * kEpiTokens * 32 * 2 <= SB * kBStage, "epilogue staging must fit in the activation stages");
+  static_assert(kDeqWarps * kEpiTokens * 32 * 2 <= SB * kStage, "epilogue staging must fit in the stages");
   static_assert(NT % 32 == 0 && NT >= 32 && NT <= 256, "MMA N");
 };
 
@@ -79,6 +89,9 @@ struct GemmArgs {
   uint16_t* y;
   int M, N, NR, G, KB;
   int tok_blocks;
+  // K split over the blocks of a cluster (gridDim.y): block r takes the
+  // 64-column steps [KB*r/ks, KB*(r+1)/ks); the partial sums are added
+  // through distributed shared memory in rank order.
 };
 
 // Instruction descriptor of tcgen05.mma kind::f16: fp32 D, fp16 A and B, both
@@ -122,21 +135,11 @@ struct StepRegs {
   uint32_t z[2][kGroups];     // zero bytes
 };
 
-template <int GS, bool SYM>
-__device__ __forceinline__ void load_step(StepRegs<GS, SYM>& r, const uint32_t* qp, const uint32_t* sp,
-                                          const uint8_t* zp, int kb, int G) {
-#pragma unroll
-  for (int i = 0; i < 2; ++i) r.w[i] = ldg_stream_u4(qp + size_t(kb) * 1024 + i * 128);
-#pragma unroll
-  for (int gg = 0; gg < StepRegs<GS, SYM>::kGroups; ++gg) {
-    // the padding half of a ragged last step (32-column groups) reuses the last group
-    const int gi = GS == 128 ? (kb >> 1) : GS == 64 ? kb : min(2 * kb + gg, G - 1);
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      r.s[i][gg] = ldg_nc_u32(sp + size_t(gi) * 64 + i * 8);
-      r.z[i][gg] = SYM ? 0u : ldg_nc_u8(zp + size_t(gi) * 64 + i * 8);
-    }
-  }
+// Groups whose metadata a 64-column step carries: one, or two for 32-column
+// groups (one at a ragged end of K).
+template <int GS>
+__device__ __forceinline__ int step_groups(int kb, int G) {
+  return GS == 32 ? min(2, G - 2 * kb) : 1;
 }
 
 // Dequantize one step of one 16-row tile into the 16 registers of a
@@ -176,7 +179,7 @@ __global__ void __launch_bounds__(Cfg<WR, NT, SA, SB, DS>::kThreads, 1)
   const uint32_t raw = smem_addr(smem_raw);
   uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);  // 1024-byte aligned for the swizzle
   const uint32_t sbase = smem_addr(smem);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + SB * C::kBStage);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + SB * C::kStage);
   // barriers: full_a[SA], empty_a[SA], full_b[SB], empty_b[SB], acc
   const uint32_t bar0 = smem_addr(bars);
   auto full_a = [&](int s) { return bar0 + 8u * uint32_t(s); };
@@ -191,7 +194,9 @@ __global__ void __launch_bounds__(Cfg<WR, NT, SA, SB, DS>::kThreads, 1)
   const int tb = int(blockIdx.x) % a.tok_blocks;
   const int rg = int(blockIdx.x) / a.tok_blocks;
   const int m0 = tb * NT;
-  const int KB = a.KB;
+  const int KS = int(gridDim.y);
+  const int kb_lo = int((int64_t(a.KB) * blockIdx.y) / KS);
+  const int KB = int((int64_t(a.KB) * (blockIdx.y + 1)) / KS) - kb_lo;  // steps of this block (>= 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < SA; ++s) {
@@ -207,7 +212,7 @@ __global__ void __launch_bounds__(Cfg<WR, NT, SA, SB, DS>::kThreads, 1)
     fence_mbarrier_init();
   }
   if (warp == C::kTmaWarp) {
-    tmem_alloc(smem_addr(tmem_slot), kTmemCols);
+    tmem_alloc(smem_addr(tmem_slot), C::kTmemCols);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -223,49 +228,54 @@ __global__ void __launch_bounds__(Cfg<WR, NT, SA, SB, DS>::kThreads, 1)
     const int R = rg * WR + at;
     const bool live = R < a.NR;
     const int g = lane >> 2;
-    const uint32_t* qp = a.qweight + (size_t(R) * KB * 8 + 2 * q4) * 128 + lane * 4;
-    const uint32_t* sp = a.scales2 + (size_t(R) * a.G * 8 + 2 * q4) * 8 + g;
-    const uint8_t* zp = SYM ? nullptr : a.zeros + (size_t(R) * a.G * 8 + 2 * q4) * 8 + g;
     const int nsteps = KB > ds ? (KB - ds + DS - 1) / DS : 0;  // steps of this set
 
-    constexpr int kPrefetch = C::kPrefetch;
-    StepRegs<GS, SYM> ring[kPrefetch];
-#pragma unroll
-    for (int p = 0; p < kPrefetch; ++p)
-      if (live && p < nsteps) load_step<GS, SYM>(ring[p], qp, sp, zp, ds + p * DS, a.G);
-
+    // The packed weights of a step arrive with its activations (TMA warp);
+    // this warp only expands them and writes tensor memory.
     bool ok = true;
-    for (int i0 = 0; i0 < nsteps && ok; i0 += kPrefetch) {
+    for (int i = 0; i < nsteps && ok; ++i) {
+      const int kb = ds + i * DS;  // local step
+      const int sb = kb % SB, sa = kb % SA;
+      if (!wait_or_abort(full_b(sb), uint32_t(kb / SB) & 1u, abort_flag)) {
+        ok = false;
+        break;
+      }
+      if (kb >= SA && !wait_or_abort(empty_a(sa), uint32_t(kb / SA - 1) & 1u, abort_flag)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const unsigned char* ws = smem + size_t(sb) * C::kStage + C::kBStage + at * kWTile;
+      const int ng = step_groups<GS>(kb_lo + kb, a.G);
+      StepRegs<GS, SYM> r;
+      if (live) {
 #pragma unroll
-      for (int p = 0; p < kPrefetch; ++p) {
-        const int i = i0 + p;
-        if (i < nsteps && ok) {
-          const int kb = ds + i * DS;
-          const int s = kb % SA;
-          const int n = kb / SA;
-          if (kb >= SA && !wait_or_abort(empty_a(s), uint32_t(n - 1) & 1u, abort_flag)) {
-            ok = false;
-          } else {
-            tc_fence_after();
-            const uint32_t col = tmem + uint32_t(C::kACol0 + (s * WR + at) * 32);
+        for (int h = 0; h < 2; ++h) {
+          const int r16 = 2 * q4 + h;
+          r.w[h] = *reinterpret_cast<const uint4*>(ws + r16 * 512 + lane * 16);
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              uint32_t v[16];
-              if (live) {
-                dequant_tile<GS, SYM>(ring[p], h, v);
-              } else {
-#pragma unroll
-                for (int e = 0; e < 16; ++e) v[e] = 0u;
-              }
-              tmem_st_16x256b_x4(col + (uint32_t(32 * q4 + 16 * h) << 16), v);
-            }
-            if (live && i + kPrefetch < nsteps) load_step<GS, SYM>(ring[p], qp, sp, zp, kb + kPrefetch * DS, a.G);
-            tmem_wait_st();
-            tc_fence_before();
-            mbar_arrive(full_a(s));
+          for (int gg = 0; gg < StepRegs<GS, SYM>::kGroups; ++gg) {
+            const int gs = min(gg, ng - 1);  // the padding half of a ragged last step reuses the last group
+            r.s[h][gg] = *reinterpret_cast<const uint32_t*>(ws + kWScaleOff + gs * 256 + (r16 * 8 + g) * 4);
+            r.z[h][gg] = SYM ? 0u : uint32_t(ws[kWZeroOff + gs * 64 + r16 * 8 + g]);
           }
         }
       }
+      const uint32_t col = tmem + uint32_t(C::kACol0 + (sa * WR + at) * 32);
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        uint32_t v[16];
+        if (live) {
+          dequant_tile<GS, SYM>(r, h, v);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 16; ++e) v[e] = 0u;
+        }
+        tmem_st_16x256b_x4(col + (uint32_t(32 * q4 + 16 * h) << 16), v);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(full_a(sa));
     }
 
     // ---------------- epilogue: set ds writes tokens [ds*NT/DS, (ds+1)*NT/DS).
@@ -275,31 +285,46 @@ __global__ void __launch_bounds__(Cfg<WR, NT, SA, SB, DS>::kThreads, 1)
     if (ok && wait_or_abort(acc_bar, 0u, abort_flag)) {
       tc_fence_after();
       constexpr int ET = C::kEpiTokens;
-      uint16_t* wst = reinterpret_cast<uint16_t*>(smem) + warp * ET * 32;  // [ET tokens][32 rows]
-      const int n_warp = (rg * WR + at) * 128 + 32 * q4;
-      const int t0 = ds * ET;                                 // first token of this set
-      const int m_live = max(0, min(ET, a.M - m0 - t0));      // tokens of this set that exist
+      const int t0 = ds * ET;  // first token of this set
+      if (KS > 1) {
+        // split K: this block's fp32 partial sums, part[token][row], for the
+        // cluster reduction below (the activation stages are free by now)
+        float* part = reinterpret_cast<float*>(smem);
+        const int nl = at * 128 + 32 * q4 + lane;
 #pragma unroll 1
-      for (int c = 0; c < ET / 32; ++c) {
-        if (c * 32 >= m_live) break;
-        uint32_t v[32];
-        tmem_ld_32x32b_x32(tmem + (uint32_t(32 * q4) << 16) + uint32_t(at * NT + t0 + c * 32), v);
-        tmem_wait_ld();
+        for (int c = 0; c < ET / 32; ++c) {
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(tmem + (uint32_t(32 * q4) << 16) + uint32_t(at * NT + t0 + c * 32), v);
+          tmem_wait_ld();
 #pragma unroll
-        for (int i = 0; i < 32; ++i)
-          wst[(c * 32 + i) * 32 + lane] = __half_as_ushort(__float2half_rn(__uint_as_float(v[i])));
-      }
-      __syncwarp();
-      const bool vec = (a.N % 8) == 0;
-      for (int e = lane; e < m_live * 4; e += 32) {
-        const int m = e >> 2, gn = n_warp + (e & 3) * 8;
-        if (gn >= a.N) continue;
-        const uint16_t* src = wst + m * 32 + (e & 3) * 8;
-        uint16_t* dst = a.y + size_t(m0 + t0 + m) * a.N + gn;
-        if (vec) {
-          *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(src);
-        } else {
-          for (int i = 0; i < 8 && gn + i < a.N; ++i) dst[i] = src[i];
+          for (int i = 0; i < 32; ++i) part[(t0 + c * 32 + i) * (WR * 128) + nl] = __uint_as_float(v[i]);
+        }
+      } else {
+        uint16_t* wst = reinterpret_cast<uint16_t*>(smem) + warp * ET * 32;  // [ET tokens][32 rows]
+        const int n_warp = (rg * WR + at) * 128 + 32 * q4;
+        const int m_live = max(0, min(ET, a.M - m0 - t0));  // tokens of this set that exist
+#pragma unroll 1
+        for (int c = 0; c < ET / 32; ++c) {
+          if (c * 32 >= m_live) break;
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(tmem + (uint32_t(32 * q4) << 16) + uint32_t(at * NT + t0 + c * 32), v);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            wst[(c * 32 + i) * 32 + lane] = __half_as_ushort(__float2half_rn(__uint_as_float(v[i])));
+        }
+        __syncwarp();
+        const bool vec = (a.N % 8) == 0;
+        for (int e = lane; e < m_live * 4; e += 32) {
+          const int m = e >> 2, gn = n_warp + (e & 3) * 8;
+          if (gn >= a.N) continue;
+          const uint16_t* src = wst + m * 32 + (e & 3) * 8;
+          uint16_t* dst = a.y + size_t(m0 + t0 + m) * a.N + gn;
+          if (vec) {
+            *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(src);
+          } else {
+            for (int i = 0; i < 8 && gn + i < a.N; ++i) dst[i] = src[i];
+          }
         }
       }
     }
@@ -309,12 +334,31 @@ __global__ void __launch_bounds__(Cfg<WR, NT, SA, SB, DS>::kThreads, 1)
       tma_prefetch_desc(&tmap_x);
       pdl_wait();  // x may come from the preceding gather kernel
       int issued = 0;
+      const unsigned char* qbytes = reinterpret_cast<const unsigned char*>(a.qweight);
+      const unsigned char* sbytes = reinterpret_cast<const unsigned char*>(a.scales2);
       for (int kb = 0; kb < KB; ++kb) {
         const int s = kb % SB;
         const int n = kb / SB;
         if (kb >= SB && !wait_or_abort(empty_b(s), uint32_t(n - 1) & 1u, abort_flag)) break;
-        mbar_arrive_expect_tx(full_b(s), uint32_t(C::kBStage));
-        tma_load_2d(sbase + uint32_t(s * C::kBStage), &tmap_x, kb * 64, m0, full_b(s));
+        const int kbg = kb_lo + kb;  // global 64-column step
+        const int g0 = kbg * 64 / GS;
+        const int ng = step_groups<GS>(kbg, a.G);
+        const uint32_t wbytes = uint32_t(kWCodes + ng * 256 + (SYM ? 0 : ng * 64));
+        int live_tiles = 0;
+#pragma unroll
+        for (int t = 0; t < WR; ++t) live_tiles += (rg * WR + t < a.NR) ? 1 : 0;
+        const uint32_t stage = sbase + uint32_t(s * C::kStage);
+        mbar_arrive_expect_tx(full_b(s), uint32_t(C::kBStage) + uint32_t(live_tiles) * wbytes);
+        tma_load_2d(stage, &tmap_x, (kb_lo + kb) * 64, m0, full_b(s));
+#pragma unroll
+        for (int t = 0; t < WR; ++t) {
+          const int R = rg * WR + t;
+          if (R >= a.NR) continue;
+          const uint32_t wdst = stage + uint32_t(C::kBStage + t * kWTile);
+          bulk_copy_g2s(wdst, qbytes + (size_t(R) * a.KB + kbg) * kWCodes, kWCodes, full_b(s));
+          bulk_copy_g2s(wdst + kWScaleOff, sbytes + (size_t(R) * a.G + g0) * 256, uint32_t(ng * 256), full_b(s));
+          if (!SYM) bulk_copy_g2s(wdst + kWZeroOff, a.zeros + (size_t(R) * a.G + g0) * 64, uint32_t(ng * 64), full_b(s));
+        }
         ++issued;
       }
       if (*abort_flag) {
@@ -332,7 +376,7 @@ __global__ void __launch_bounds__(Cfg<WR, NT, SA, SB, DS>::kThreads, 1)
         if (!wait_or_abort(full_b(sb), uint32_t(kb / SB) & 1u, abort_flag)) break;
         if (!wait_or_abort(full_a(sa), uint32_t(kb / SA) & 1u, abort_flag)) break;
         tc_fence_after();
-        const uint32_t b_addr = sbase + uint32_t(sb * C::kBStage);
+        const uint32_t b_addr = sbase + uint32_t(sb * C::kStage);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
           const uint64_t bdesc = sw128_desc(b_addr + uint32_t(kk * 32));
@@ -352,9 +396,27 @@ __global__ void __launch_bounds__(Cfg<WR, NT, SA, SB, DS>::kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
+  if (KS > 1) {
+    // Every block of the cluster holds its partial sums; rank r adds its
+    // share of (token, row) pairs over all ranks in rank order and writes y.
+    cluster_sync_all();
+    const float* part = reinterpret_cast<const float*>(smem);
+    constexpr int kRows = WR * 128;
+    const int E = max(0, min(NT, a.M - m0)) * kRows;
+    const int rank = int(cluster_ctarank());
+    const int e_lo = int((int64_t(E) * rank) / KS), e_hi = int((int64_t(E) * (rank + 1)) / KS);
+    for (int e = e_lo + int(threadIdx.x); e < e_hi; e += C::kThreads) {
+      float acc = 0.f;
+      for (int rk = 0; rk < KS; ++rk) acc += ld_dsmem_f32(part + e, uint32_t(rk));
+      const int tok = e / kRows;
+      const int n = rg * kRows + (e - tok * kRows);
+      if (n < a.N) a.y[size_t(m0 + tok) * a.N + n] = __half_as_ushort(__float2half_rn(acc));
+    }
+    cluster_sync_all();  // peers are done reading this block's partial sums
+  }
   if (warp == C::kTmaWarp) {
     tc_fence_after();
-    tmem_dealloc(tmem, kTmemCols);
+    tmem_dealloc(tmem, C::kTmemCols);
   }
 }
 
@@ -445,8 +507,8 @@ cudaError_t make_x_map(CUtensorMap* map, const uint16_t* x, int64_t M, int64_t K
 }
 
 template <int WR, int NT, int SA, int SB, int DS, int GS, bool SYM>
-cudaError_t launch_cfg(const Layout& L, const GemmArgs& base, const uint16_t* xa, int64_t M, bool after_gather,
-                       cudaStream_t stream) {
+cudaError_t launch_cfg(const Layout& L, const GemmArgs& base, const uint16_t* xa, int64_t M, int ks,
+                       bool after_gather, cudaStream_t stream) {
   using C = Cfg<WR, NT, SA, SB, DS>;
   CUtensorMap map;
   cudaError_t e = make_x_map(&map, xa, M, L.K, NT);
@@ -454,49 +516,95 @@ cudaError_t launch_cfg(const Layout& L, const GemmArgs& base, const uint16_t* xa
   auto kern = gemm_kernel<WR, NT, SA, SB, DS, GS, SYM>;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, int(cudaSharedmemCarveoutMaxShared));
+  if (e != cudaSuccess) return e;
+  if (ks > 8) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return e;
+  }
   GemmArgs a = base;
   a.tok_blocks = int((M + NT - 1) / NT);
   const int64_t row_groups = (L.NR + WR - 1) / WR;
   const int64_t blocks = row_groups * a.tok_blocks;
   if (blocks > 0x7FFFFFFF) return cudaErrorInvalidConfiguration;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(unsigned(blocks), 1, 1);
+  cfg.gridDim = dim3(unsigned(blocks), unsigned(ks), 1);
   cfg.blockDim = dim3(C::kThreads, 1, 1);
   cfg.dynamicSmemBytes = C::kSmem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  // After our own gather kernel (which writes only the workspace), the
-  // block's set-up and weight stream may start before the gather ends; the
-  // activation loads wait for it.
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchAttribute attr[2];
+  int na = 0;
+  if (after_gather) {
+    // After our own gather kernel (which writes only the workspace), the
+    // block's set-up and weight stream may start before the gather ends; the
+    // activation loads wait for it.
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+  }
+  if (ks > 1) {
+    attr[na].id = cudaLaunchAttributeClusterDimension;
+    attr[na].val.clusterDim.x = 1;
+    attr[na].val.clusterDim.y = unsigned(ks);
+    attr[na].val.clusterDim.z = 1;
+    ++na;
+  }
   cfg.attrs = attr;
-  cfg.numAttrs = after_gather ? 1 : 0;
+  cfg.numAttrs = na;
   e = cudaLaunchKernelEx(&cfg, kern, map, a);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
 template <int WR, int NT, int SA, int SB, int DS>
-cudaError_t launch_scheme(const Layout& L, const GemmArgs& a, const uint16_t* xa, int64_t M, bool after_gather,
-                          cudaStream_t stream) {
+cudaError_t launch_scheme(const Layout& L, const GemmArgs& a, const uint16_t* xa, int64_t M, int ks,
+                          bool after_gather, cudaStream_t stream) {
   switch (L.gsize) {
     case 32:
-      return L.sym ? launch_cfg<WR, NT, SA, SB, DS, 32, true>(L, a, xa, M, after_gather, stream)
-                   : launch_cfg<WR, NT, SA, SB, DS, 32, false>(L, a, xa, M, after_gather, stream);
+      return L.sym ? launch_cfg<WR, NT, SA, SB, DS, 32, true>(L, a, xa, M, ks, after_gather, stream)
+                   : launch_cfg<WR, NT, SA, SB, DS, 32, false>(L, a, xa, M, ks, after_gather, stream);
     case 64:
-      return L.sym ? launch_cfg<WR, NT, SA, SB, DS, 64, true>(L, a, xa, M, after_gather, stream)
-                   : launch_cfg<WR, NT, SA, SB, DS, 64, false>(L, a, xa, M, after_gather, stream);
+      return L.sym ? launch_cfg<WR, NT, SA, SB, DS, 64, true>(L, a, xa, M, ks, after_gather, stream)
+                   : launch_cfg<WR, NT, SA, SB, DS, 64, false>(L, a, xa, M, ks, after_gather, stream);
     default:
-      return L.sym ? launch_cfg<WR, NT, SA, SB, DS, 128, true>(L, a, xa, M, after_gather, stream)
-                   : launch_cfg<WR, NT, SA, SB, DS, 128, false>(L, a, xa, M, after_gather, stream);
+      return L.sym ? launch_cfg<WR, NT, SA, SB, DS, 128, true>(L, a, xa, M, ks, after_gather, stream)
+                   : launch_cfg<WR, NT, SA, SB, DS, 128, false>(L, a, xa, M, ks, after_gather, stream);
   }
 }
 
+// Tokens per block of each tile.
+int tile_tokens(int tile) { return tile == 2 ? 128 : tile == 5 ? 128 : tile == 6 ? 64 : 256; }
+int tile_rows(int tile) { return tile == 2 ? 256 : 128; }
+
 }  // namespace
 
+GemmPlan gemm_default_plan(const Layout& L, int64_t M, int sm_count) {
+  // Few tokens: a narrow tile (two blocks per SM) and K split over a cluster
+  // so that every SM dequantizes; many tokens: the 128 x 256 tile.
+  GemmPlan p{M <= 64 ? 6 : M <= 128 ? 5 : 3, 1};
+  const int64_t blocks = ((L.NR * 128 + tile_rows(p.tile) - 1) / tile_rows(p.tile)) *
+                         ((M + tile_tokens(p.tile) - 1) / tile_tokens(p.tile));
+  const double target = (p.tile >= 5 ? 2.0 : 1.0) * sm_count;
+  double best = 1e30;
+  for (int ks : {1, 2, 4, 8, 16}) {
+    if (ks > 1 && L.KB / ks < 8) break;  // at least 8 steps of 64 columns per block
+    const double d = std::fabs(std::log(double(blocks * ks) / target));
+    if (d < best - 1e-9) {
+      best = d;
+      p.ksplit = ks;
+    }
+  }
+  return p;
+}
+
+bool gemm_plan_ok(const Layout& L, const GemmPlan& p) {
+  if (p.tile < 1 || p.tile > 6) return false;
+  if (p.ksplit != 1 && p.ksplit != 2 && p.ksplit != 4 && p.ksplit != 8 && p.ksplit != 16) return false;
+  return p.ksplit <= L.KB;
+}
+
 cudaError_t launch_gemm(const Layout& L, const void* blob, const uint16_t* x, uint16_t* y, int64_t M,
-                        void* workspace, int tile, cudaStream_t stream) {
+                        void* workspace, const GemmPlan& plan, cudaStream_t stream) {
   const BlobView B = view_of(L, blob);
   const uint16_t* xa = x;
   if (L.act) {
@@ -527,11 +635,14 @@ cudaError_t launch_gemm(const Layout& L, const void* blob, const uint16_t* x, ui
   a.G = int(L.G);
   a.KB = int(L.KB);
   const bool g = L.act;
-  switch (tile) {
-    case 2: return launch_scheme<2, 128, 4, 12, 2>(L, a, xa, M, g, stream);
-    case 3: return launch_scheme<1, 256, 8, 6, 4>(L, a, xa, M, g, stream);
-    case 4: return launch_scheme<1, 256, 8, 6, 1>(L, a, xa, M, g, stream);
-    default: return launch_scheme<1, 256, 8, 6, 2>(L, a, xa, M, g, stream);
+  const int ks = plan.ksplit;
+  switch (plan.tile) {
+    case 1: return launch_scheme<1, 256, 8, 6, 2>(L, a, xa, M, ks, g, stream);
+    case 2: return launch_scheme<2, 128, 4, 8, 2>(L, a, xa, M, ks, g, stream);
+    case 4: return launch_scheme<1, 256, 8, 6, 1>(L, a, xa, M, ks, g, stream);
+    case 5: return launch_scheme<1, 128, 4, 5, 2>(L, a, xa, M, ks, g, stream);
+    case 6: return launch_scheme<1, 64, 4, 8, 2>(L, a, xa, M, ks, g, stream);
+    default: return launch_scheme<1, 256, 8, 6, 4>(L, a, xa, M, ks, g, stream);
   }
 }
 

@@ -72,7 +72,7 @@ SIGNATURES = {
     "w4a16_gemv_ex": (ctypes.c_int, [_FP, _P, _SZ, _P, _P, _I64, _I32, _I32, ctypes.c_uint32, _P]),
     "w4a16_gemm_workspace_bytes": (_SZ, [_FP, _I64]),
     "w4a16_gemm": (ctypes.c_int, [_FP, _P, _SZ, _P, _P, _I64, _P, _SZ, _P]),
-    "w4a16_gemm_ex": (ctypes.c_int, [_FP, _P, _SZ, _P, _P, _I64, _P, _SZ, _I32, _P]),
+    "w4a16_gemm_ex": (ctypes.c_int, [_FP, _P, _SZ, _P, _P, _I64, _P, _SZ, _I32, _I32, _P]),
     "w4a16_pipeline_timeouts": (ctypes.c_int, [ctypes.POINTER(ctypes.c_uint32)]),
 }
 
@@ -251,10 +251,10 @@ def gemm_workspace_bytes(fmt: Format, M: int) -> int:
 
 
 def gemm(fmt: Format, packed: torch.Tensor, x: torch.Tensor, out: torch.Tensor | None = None,
-         workspace: torch.Tensor | None = None, tile: int = 0, stream=None) -> torch.Tensor:
+         workspace: torch.Tensor | None = None, tile: int = 0, ksplit: int = 0, stream=None) -> torch.Tensor:
     """y = x . W_hat^T for x fp16 [M, K] on the tcgen05 tensor cores.
 
-    ``tile``: 0 default, 1 = 128 weight rows x 256 tokens, 2 = 256 x 128.
+    ``tile`` / ``ksplit``: launch shape (0 = default), see ``w4a16_gemm_ex``.
     """
     M = x.shape[0]
     pp = _dev(packed, torch.uint8, "packed")
@@ -267,8 +267,8 @@ def gemm(fmt: Format, packed: torch.Tensor, x: torch.Tensor, out: torch.Tensor |
         workspace = torch.empty(need, dtype=torch.uint8, device=x.device)
     wp = None if not need else _dev(workspace, torch.uint8, "workspace")
     wbytes = 0 if not need else workspace.numel()
-    if tile:
-        st = lib().w4a16_gemm_ex(ctypes.byref(fmt), pp, packed.numel(), xp, yp, M, wp, wbytes, tile,
+    if tile or ksplit:
+        st = lib().w4a16_gemm_ex(ctypes.byref(fmt), pp, packed.numel(), xp, yp, M, wp, wbytes, tile, ksplit,
                                  _stream(stream))
     else:
         st = lib().w4a16_gemm(ctypes.byref(fmt), pp, packed.numel(), xp, yp, M, wp, wbytes, _stream(stream))
