@@ -263,10 +263,7 @@ W4A16_API w4a16_status w4a16_pipeline_timeouts(uint32_t* count);
 
 /*
  * w4a16_gemv with options.
- *   shape    0 = default. Register-ring and asynchronous-copy kernels:
- *            16-row tiles per thread block, 2, 4 or 8.
- *            With W4A16_GEMV_BULK_COPY: the depth of the shared-memory ring
- *            in 16 KiB stages, 2..8.
+ *   shape    16-row tiles per thread block, 2, 4 or 8; 0 = default.
  *   ksplit   thread blocks per cluster splitting K: 1, 2, 4, 8 or 16;
  *            0 = default.
  *   flags    0 or an OR of
@@ -275,12 +272,6 @@ W4A16_API w4a16_status w4a16_pipeline_timeouts(uint32_t* count);
  *              before the preceding kernel started, as in a decode loop);
  *              the GEMV then starts streaming weights before the previous
  *              kernel finishes. `x` is always read after it.
- *            W4A16_GEMV_BULK_COPY: use the variant in which a producer warp
- *              streams each thread block's weights (and activations) with
- *              bulk copies into a ring of shared-memory stages.
- *            W4A16_GEMV_STAGE_ACTIVATIONS: default kernel only: copy each
- *              thread block's activations to shared memory before the
- *              weight stream.
  *            W4A16_GEMV_INPUTS_READY: stronger than WEIGHTS_READY: no
  *              kernel still in flight on the stream writes `packed` or `x`,
  *              or reads or writes `y` (for example k and v after q, which
@@ -290,22 +281,24 @@ W4A16_API w4a16_status w4a16_pipeline_timeouts(uint32_t* count);
  *              dependent launch no longer waits, through it, for the kernels
  *              before it; work that depends on those must follow an
  *              ordinary stream dependency.
- *            W4A16_GEMV_ASYNC_COPY: the default kernel's plan, but every
- *              thread lands its next units (codes, scales, zero points) with
- *              asynchronous copies (cp.async) in a ring of shared-memory slots
- *              instead of registers; `shape` stays the 16-row tiles per
- *              thread block.
- * With neither W4A16_GEMV_BULK_COPY nor W4A16_GEMV_ASYNC_COPY and shape 0,
- * layers of at least 64 row blocks of 128 (N >= 8065) use the
- * asynchronous-copy ring and smaller ones the register ring (measured on
- * B300); w4a16_gemv always takes that default.
+ *            W4A16_GEMV_REGISTER_RING: the kernel that loads the next weight
+ *              units straight into a ring of registers.
+ *            W4A16_GEMV_ASYNC_COPY: the kernel in which every thread lands
+ *              its next units (codes, scales, zero points) with asynchronous
+ *              copies (cp.async) in a ring of shared-memory slots instead of
+ *              registers (more bytes in flight per SM).
+ *            W4A16_GEMV_STAGE_ACTIVATIONS: copy each thread block's
+ *              activations to shared memory before the weight stream.
+ * Without REGISTER_RING or ASYNC_COPY, layers of at least 64 row blocks of
+ * 128 (N > 8064) use the asynchronous-copy kernel and smaller ones the
+ * register ring (measured on B300); w4a16_gemv always takes that default.
  * The GEMV kernels are launched with programmatic dependent launch, so a GEMV
  * may start while the previous kernel on the stream is still running; by
  * default it reads nothing from global memory before that kernel is done.
  * Results equal w4a16_gemv's up to summation order.
  */
 #define W4A16_GEMV_WEIGHTS_READY 1u
-#define W4A16_GEMV_BULK_COPY 2u
+#define W4A16_GEMV_REGISTER_RING 2u
 #define W4A16_GEMV_STAGE_ACTIVATIONS 4u
 #define W4A16_GEMV_ASYNC_COPY 8u
 #define W4A16_GEMV_INPUTS_READY 16u

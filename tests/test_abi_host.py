@@ -131,14 +131,13 @@ def test_gemv_argument_checks(lib):
     bad = fmt(bits=2)
     assert lib.w4a16_gemv(ctypes.byref(bad), FAKE, nb, X, Y, 1, None) == UNSUPPORTED
     # explicit launch shapes are validated too
-    bulk, stage_x = 2, 4
-    assert lib.w4a16_gemv_ex(ctypes.byref(f), FAKE, nb, X, Y, 1, 9, 1, bulk, None) == INVALID   # ring depth
-    assert lib.w4a16_gemv_ex(ctypes.byref(f), FAKE, nb, X, Y, 1, 1, 1, bulk, None) == INVALID
+    ring, stage_x, async_copy = 2, 4, 8
     assert lib.w4a16_gemv_ex(ctypes.byref(f), FAKE, nb, X, Y, 1, 3, 1, 0, None) == INVALID      # rows16
+    assert lib.w4a16_gemv_ex(ctypes.byref(f), FAKE, nb, X, Y, 1, 16, 1, ring, None) == INVALID
     assert lib.w4a16_gemv_ex(ctypes.byref(f), FAKE, nb, X, Y, 1, 8, 32, 0, None) == INVALID
     assert lib.w4a16_gemv_ex(ctypes.byref(f), FAKE, nb, X, Y, 1, 0, 0, 64, None) == INVALID    # unknown flag
-    assert lib.w4a16_gemv_ex(ctypes.byref(f), FAKE, nb, X, Y, 1, 0, 0, bulk | stage_x | 32, None) == INVALID
-    assert lib.w4a16_gemv_ex(ctypes.byref(f), FAKE, nb, X, Y, 1, 0, 0, bulk | 8, None) == INVALID  # two variants
+    assert lib.w4a16_gemv_ex(ctypes.byref(f), FAKE, nb, X, Y, 1, 0, 0, ring | stage_x | 32, None) == INVALID
+    assert lib.w4a16_gemv_ex(ctypes.byref(f), FAKE, nb, X, Y, 1, 0, 0, ring | async_copy, None) == INVALID
 
 
 def test_gemm_and_workspace_checks(lib):

@@ -19,13 +19,14 @@ def to_dev(a):
     return torch.from_numpy(np.ascontiguousarray(a)).cuda()
 
 
-# register ring (default) / register ring with staged activations / shared-memory
-# bulk-copy ring fed by a producer warp / per-warp bulk-copy rings
-VARIANTS = ("ring", "ring_sx", "bulk", "async")
+# register ring / register ring with staged activations / asynchronous-copy ring
+# / asynchronous-copy ring with staged activations
+VARIANTS = ("ring", "ring_sx", "async", "async_sx")
 
 
 def variant_kw(variant):
-    return dict(bulk_copy=variant == "bulk", stage_activations=variant == "ring_sx", async_copy=variant == "async")
+    return dict(register_ring=variant.startswith("ring"), async_copy=variant.startswith("async"),
+                stage_activations=variant.endswith("_sx"))
 
 
 def run_case(N, K, M, g, sym, act, frac=0.01, tag="gemv", shape=0, ksplit=0, variant="ring"):
@@ -89,17 +90,9 @@ def test_act_order(cuda_ok, M, variant):
 @pytest.mark.parametrize("rows16", [2, 4, 8])
 @pytest.mark.parametrize("ksplit", [1, 2, 4, 8, 16])
 def test_every_register_ring_launch_shape(cuda_ok, rows16, ksplit):
-    for variant in ("ring", "ring_sx", "async"):
+    for variant in VARIANTS:
         y, y_ref, B = run_case(256, 2048, 3, 64, False, False, tag="plan", shape=rows16, ksplit=ksplit,
                                variant=variant)
-        assert_within(y, y_ref, B)
-
-
-@pytest.mark.parametrize("stages", [2, 3, 4, 6, 8])
-@pytest.mark.parametrize("ksplit", [1, 2, 4, 8, 16])
-def test_every_bulk_copy_launch_shape(cuda_ok, stages, ksplit):
-    for g, act in ((64, False), (32, True)):
-        y, y_ref, B = run_case(256, 2048, 3, g, False, act, tag="plan", shape=stages, ksplit=ksplit, variant="bulk")
         assert_within(y, y_ref, B)
 
 
@@ -210,7 +203,7 @@ def test_inputs_ready_chain_matches(cuda_ok):
         torch.cuda.synchronize()
         for i, (o, r) in enumerate(zip(outs, ref)):
             got = o.cpu().numpy()
-            if variant == "ring":  # the default plan of this shape: same kernel, same order
+            if variant == "ring":  # the default kernel of this shape: same kernel, same order
                 assert np.array_equal(got.view(np.uint16), r.view(np.uint16))
             else:
                 q, s, z = O.rtn_quantize(synth.weights_np(N, K, 94 + i), 128, False)

@@ -194,28 +194,26 @@ static w4a16_status gemv_common(const w4a16_format* f, const void* packed, size_
   const char* yb = reinterpret_cast<const char*>(y);
   const size_t xbytes = size_t(M) * size_t(f->K) * 2, ybytes = size_t(M) * size_t(f->N) * 2;
   if (xb < yb + ybytes && yb < xb + xbytes) return W4A16_ERR_INVALID_ARG;  // overlap
-  if ((flags & ~uint32_t(W4A16_GEMV_WEIGHTS_READY | W4A16_GEMV_BULK_COPY | W4A16_GEMV_STAGE_ACTIVATIONS |
-                         W4A16_GEMV_ASYNC_COPY | W4A16_GEMV_INPUTS_READY)) != 0)
+  if ((flags & ~uint32_t(W4A16_GEMV_WEIGHTS_READY | W4A16_GEMV_STAGE_ACTIVATIONS | W4A16_GEMV_ASYNC_COPY |
+                         W4A16_GEMV_REGISTER_RING | W4A16_GEMV_INPUTS_READY)) != 0)
     return W4A16_ERR_INVALID_ARG;
-  if ((flags & W4A16_GEMV_BULK_COPY) && (flags & W4A16_GEMV_ASYNC_COPY)) return W4A16_ERR_INVALID_ARG;
-  const bool ring = (flags & W4A16_GEMV_BULK_COPY) == 0;
+  if ((flags & W4A16_GEMV_REGISTER_RING) && (flags & W4A16_GEMV_ASYNC_COPY)) return W4A16_ERR_INVALID_ARG;
+  if (shape != 0 && shape != 2 && shape != 4 && shape != 8) return W4A16_ERR_INVALID_ARG;
   const Layout L0 = make_layout(*f);
   // Without a variant flag: the asynchronous-copy ring for layers of 64 or
   // more 128-row blocks (it keeps more bytes in flight), else the register
   // ring (fewer instructions; small layers are bound by launch latency).
-  const bool by_default = (flags & (W4A16_GEMV_BULK_COPY | W4A16_GEMV_ASYNC_COPY)) == 0 && shape == 0;
-  const bool wbulk = (flags & W4A16_GEMV_ASYNC_COPY) != 0 || (by_default && L0.NR >= 64);
-  if (ring ? (shape != 0 && shape != 2 && shape != 4 && shape != 8) : (shape != 0 && (shape < 2 || shape > 8)))
-    return W4A16_ERR_INVALID_ARG;
+  const bool wbulk = (flags & W4A16_GEMV_ASYNC_COPY) != 0 ||
+                     ((flags & W4A16_GEMV_REGISTER_RING) == 0 && L0.NR >= 64);
   if (ksplit != 0 && ksplit != 1 && ksplit != 2 && ksplit != 4 && ksplit != 8 && ksplit != 16)
     return W4A16_ERR_INVALID_ARG;
   const Layout L = make_layout(*f);
   DeviceInfo dev;
   cudaError_t e = device_info(&dev);
   if (e != cudaSuccess) return cuda_fail(e);
-  GemvPlan plan = gemv_default_plan(L, int(M), dev, wbulk ? kGemvAsyncCopy : ring ? kGemvRegisterRing : kGemvBulkCopy);
-  if (shape != 0) (ring ? plan.rows16 : plan.stages) = shape;
-  if (ring && (flags & W4A16_GEMV_STAGE_ACTIVATIONS) != 0) plan.stage_x = true;
+  GemvPlan plan = gemv_default_plan(L, int(M), dev, wbulk ? kGemvAsyncCopy : kGemvRegisterRing);
+  if (shape != 0) plan.rows16 = shape;
+  if ((flags & W4A16_GEMV_STAGE_ACTIVATIONS) != 0) plan.stage_x = true;
   if (ksplit != 0) plan.ksplit = ksplit;
   if (!gemv_plan_ok(L, int(M), plan)) return (shape || ksplit) ? W4A16_ERR_INVALID_ARG : W4A16_ERR_UNSUPPORTED;
   uint32_t kflags = flags & (W4A16_GEMV_WEIGHTS_READY | W4A16_GEMV_INPUTS_READY);

@@ -29,13 +29,12 @@ cudaError_t launch_pack(const Layout& L, const uint8_t* q, const uint16_t* scale
 cudaError_t launch_dequant(const Layout& L, const void* blob, uint16_t* w_out,
                            cudaStream_t stream);
 
-constexpr int kGemvBulkCopy = 0;     // weights streamed by cp.async.bulk into a shared-memory ring
 constexpr int kGemvRegisterRing = 1; // weights loaded straight into a register ring
 constexpr int kGemvAsyncCopy = 2;    // each thread lands its own weight loads in a shared-memory ring (cp.async)
 struct GemvPlan {
-  int kind;     // kGemvBulkCopy or kGemvRegisterRing
+  int kind;     // kGemvRegisterRing or kGemvAsyncCopy
   int rows16;   // register ring: 16-row tiles per CTA (2, 4, 8)
-  int stages;   // bulk copy: 16 KiB stages in the ring (2..8); async copy: units in flight (fixed at 4)
+  int stages;   // async copy: units in flight (fixed at 4)
   int ksplit;   // CTAs per cluster along K
   bool stage_x; // register ring: copy the block's activations to shared memory first
 };

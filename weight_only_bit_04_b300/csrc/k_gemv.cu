@@ -9,7 +9,9 @@
 //    64-column blocks. Per block it issues one coalesced 16-byte load per lane
 //    and tile (1 KiB contiguous per warp). The loads of four blocks, with the
 //    scales and zero points of their groups, stay in flight in a register
-//    ring; the loop structure follows the group size at compile time.
+//    ring; the loop structure follows the group size at compile time. The
+//    asynchronous-copy variant (WB) lands the same loads with cp.async in a
+//    shared-memory ring instead, so more bytes stay in flight per SM.
 //  * A 32-bit word holds the codes of one lane's m16n8k16 A fragment. Masking
 //    its nibbles with AND gives fp16 bit patterns 0x000q (= q * 2^-24) and
 //    0x00q0 (= q * 2^-20): exact subnormal values, so four ANDs and one shift
@@ -477,349 +479,6 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const GemvArgs a) {
   }
 }
 
-// ===========================================================================
-// Bulk-copy variant (the default): the weight stream of a thread block is one
-// contiguous run of 4 KiB tiles (one 128-row block, a range of 64-column
-// blocks), which a producer warp moves into a ring of shared-memory stages
-// with cp.async.bulk -- tens of KiB in flight per block, no registers held --
-// while eight consumer warps, one per 16-row tile, expand and multiply them.
-// ===========================================================================
-constexpr int kTConsumers = 8;                      // one warp per 16-row tile of the block
-constexpr int kTThreads = (kTConsumers + 1) * 32;   // + one producer warp
-constexpr int kTStageBlocks = 4;                    // 64-column blocks per stage (16 KiB of codes)
-constexpr int kTMaxStages = 8;
-
-template <int GS>
-struct TStage {
-  static constexpr int kGroups = kTStageBlocks * 64 / GS;  // groups per stage: 2, 4 or 8
-  static constexpr int kScaleOff = kTStageBlocks * kTileBytes;
-  static constexpr int kZeroOff = kScaleOff + kGroups * kScaleBytesPerGroupBlock;
-  static constexpr int kBytes = kZeroOff + kGroups * kZeroBytesPerGroupBlock;  // a multiple of 128
-};
-
-struct GemvTmaArgs {
-  const uint8_t* qweight;
-  const uint8_t* scales;
-  const uint8_t* zeros;     // nullptr when symmetric
-  const int32_t* perm;      // packed -> original column, or nullptr
-  const uint16_t* x;
-  uint16_t* y;
-  int M, N, K, G, KB;
-  int kb_per_cta;  // 64-column blocks per thread block (stage-aligned, group-aligned)
-  int stages;      // ring depth, 2..kTMaxStages
-  int stage_bytes; // bytes of one ring stage (codes, scales, zeros, activations)
-  uint32_t flags;  // kGemvWeightsReady
-};
-
-// Shared memory of one block: the ring, the barriers and abort flag, then
-// (act order or a ragged K) the staged activations, then (up to 8 tokens) the
-// per-group activation sums.
-__host__ __device__ inline size_t tma_xs_offset(int stages, int stage_bytes) {
-  return size_t(stages) * stage_bytes + 2 * kTMaxStages * 8 + 16;
-}
-// Activations travel with the weights: each stage also holds the stage's
-// columns of every token, one row of 264 halves per token (256 + 8 of
-// padding, so that the lanes' 8-byte reads of eight tokens hit distinct banks).
-constexpr int kStageXRow = 264;
-__host__ __device__ inline int tma_stage_bytes(int base, bool staged, int M) {
-  return staged ? base : base + (M * kStageXRow * 2 + 127) / 128 * 128;
-}
-__host__ __device__ inline size_t tma_xs_bytes(bool staged, int M, int kb_per_cta) {
-  return staged ? (size_t(M) * (size_t(kb_per_cta) * kColsPerBlock + 8) * 2 + 15) / 16 * 16 : 0;
-}
-constexpr int kXsumTokens = 8;  // activation sums are precomputed for up to 8 tokens
-
-
-template <int MP, int GS, bool SYM, bool STAGED>
-__global__ void __launch_bounds__(kTThreads) gemv_tma_kernel(const GemvTmaArgs a) {
-  extern __shared__ __align__(128) unsigned char smem[];
-  using ST = TStage<GS>;
-  constexpr int NB = MP > 8 ? 2 : 1;
-  const int NS = a.stages;
-  const int SBY = a.stage_bytes;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + size_t(NS) * SBY);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 2 * kTMaxStages);
-  const uint32_t bar0 = smem_addr(bars);
-  const int warp = int(threadIdx.x >> 5), lane = int(threadIdx.x & 31);
-  const int R = int(blockIdx.x);
-  const int kb_lo = int(blockIdx.y) * a.kb_per_cta;
-  const int kb_hi = min(kb_lo + a.kb_per_cta, a.KB);
-  const int nblk = max(kb_hi - kb_lo, 0);
-  const int nst = (nblk + kTStageBlocks - 1) / kTStageBlocks;
-
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < NS; ++s) {
-      mbar_init(bar0 + 8u * s, STAGED ? 1 : 2);               // full: weight copies (+ activation copies)
-      mbar_init(bar0 + 8u * (kTMaxStages + s), kTConsumers);  // empty: one arrival per consumer warp
-    }
-    *abort_flag = 0;
-    fence_mbarrier_init();
-  }
-  __syncthreads();
-  if (threadIdx.x == 0) pdl_launch_dependents();
-
-  if (warp == kTConsumers) {
-    // ------------------------------------------------ producer (one thread)
-    if (lane == 0) {
-      auto issue_weights = [&](int st) {
-        const int s = st % NS;
-        const int kb0 = kb_lo + st * kTStageBlocks;
-        const int nb = min(kTStageBlocks, kb_hi - kb0);
-        const int g0 = kb0 * kColsPerBlock / GS;
-        const int ng = min((nb * kColsPerBlock + GS - 1) / GS, a.G - g0);
-        const uint32_t bytes = uint32_t(nb * kTileBytes + ng * kScaleBytesPerGroupBlock +
-                                        (SYM ? 0 : ng * kZeroBytesPerGroupBlock));
-        const uint32_t full = bar0 + 8u * s;
-        const uint32_t dst = smem_addr(smem + size_t(s) * SBY);
-        mbar_arrive_expect_tx(full, bytes);
-        bulk_copy_g2s(dst, a.qweight + (size_t(R) * a.KB + kb0) * kTileBytes, uint32_t(nb * kTileBytes), full);
-        bulk_copy_g2s(dst + ST::kScaleOff, a.scales + (size_t(R) * a.G + g0) * kScaleBytesPerGroupBlock,
-                      uint32_t(ng * kScaleBytesPerGroupBlock), full);
-        if (!SYM)
-          bulk_copy_g2s(dst + ST::kZeroOff, a.zeros + (size_t(R) * a.G + g0) * kZeroBytesPerGroupBlock,
-                        uint32_t(ng * kZeroBytesPerGroupBlock), full);
-      };
-      auto issue_acts = [&](int st) {
-        const int s = st % NS;
-        const int kb0 = kb_lo + st * kTStageBlocks;
-        const int nb = min(kTStageBlocks, kb_hi - kb0);
-        const uint32_t full = bar0 + 8u * s;
-        const uint32_t dst = smem_addr(smem + size_t(s) * SBY + ST::kBytes);
-        const uint32_t row = uint32_t(nb * kColsPerBlock * 2);
-        mbar_arrive_expect_tx(full, row * uint32_t(a.M));
-        for (int tok = 0; tok < a.M; ++tok)
-          bulk_copy_g2s(dst + uint32_t(tok * kStageXRow * 2), a.x + size_t(tok) * a.K + size_t(kb0) * kColsPerBlock,
-                        row, full);
-      };
-      int issued = 0;
-      if ((a.flags & kGemvWeightsReady) != 0) {
-        // the weights of the first stages stream while the previous kernel finishes
-        issued = min(NS, nst);
-        for (int st = 0; st < issued; ++st) issue_weights(st);
-        if ((a.flags & kGemvInputsReady) == 0) pdl_wait();
-        if (!STAGED)
-          for (int st = 0; st < issued; ++st) issue_acts(st);
-      } else if ((a.flags & kGemvInputsReady) == 0) {
-        pdl_wait();
-      }
-      for (int st = issued; st < nst; ++st) {
-        const int s = st % NS;
-        if (st >= NS && !mbar_wait_bounded(bar0 + 8u * (kTMaxStages + s), uint32_t(st / NS - 1) & 1u, kTWaitLimitNs)) {
-          *abort_flag = 1;
-          atomicAdd(&g_gemv_timeouts, 1u);
-          break;
-        }
-        if (*abort_flag) break;
-        issue_weights(st);
-        if (!STAGED) issue_acts(st);
-        ++issued;
-      }
-      if (*abort_flag) {  // copies in flight must land before the block's shared memory is released
-        for (int st = max(issued - NS, 0); st < issued; ++st)
-          mbar_wait_bounded(bar0 + 8u * (st % NS), uint32_t(st / NS) & 1u, kTWaitLimitNs);
-      }
-    }
-  } else {
-    // ------------------------------------------------ consumers
-    // activations (and, under act order, the column order) may come from the previous kernel
-    if ((a.flags & kGemvInputsReady) == 0) pdl_wait();
-    const int g = lane >> 2, t = lane & 3;
-    const int M = a.M;
-    const int tok0 = min(g, M - 1);
-    const int tok1 = min(g + 8, M - 1);
-    const uint16_t* xl0;
-    const uint16_t* xl1;
-    if (STAGED) {
-      const int span = nblk * kColsPerBlock;
-      const int stride = span + 8;
-      uint16_t* xs = reinterpret_cast<uint16_t*>(smem + tma_xs_offset(NS, SBY));
-      stage_activations(a.x, a.perm, xs, M, a.K, kb_lo * kColsPerBlock, span, stride, int(threadIdx.x),
-                        kTConsumers * 32);
-      named_bar_sync(1, kTConsumers * 32);
-      xl0 = xs + tok0 * stride + 4 * t;
-      xl1 = xs + tok1 * stride + 4 * t;
-    } else {
-      // offsets of this lane's fragment inside a stage's activation rows
-      xl0 = nullptr;
-      xl1 = nullptr;
-    }
-    // Up to 8 tokens, the activation sum of every (group, token) of this
-    // block's columns is computed once, here, into shared memory: one warp
-    // per 128-column window and token, lanes reducing 4 columns each, then a
-    // shuffle reduction within each group. Above 8 tokens an extra MMA per
-    // 16 columns with an all-2^-24 operand accumulates it instead.
-    constexpr bool XPRE = MP <= kXsumTokens;
-    float* xsum = reinterpret_cast<float*>(smem + tma_xs_offset(NS, SBY) + tma_xs_bytes(STAGED, M, a.kb_per_cta));
-    if (XPRE) {
-      const int span = nblk * kColsPerBlock;
-      const int nwin = (span + 127) / 128;
-      for (int it = warp; it < M * nwin; it += kTConsumers) {
-        const int tok = it / nwin, wi = it - tok * nwin;
-        const int c = wi * 128 + lane * 4;
-        float v = 0.f;
-        if (c < span) {
-          const uint16_t* src = STAGED ? xl0 - tok0 * (span + 8) - 4 * t + tok * (span + 8) + c
-                                       : a.x + size_t(tok) * a.K + kb_lo * kColsPerBlock + c;
-          const uint2 xv = STAGED ? *reinterpret_cast<const uint2*>(src) : ld_x<false>(src);
-          const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&xv.x));
-          const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&xv.y));
-          v = (f0.x + f0.y) + (f1.x + f1.y);
-        }
-#pragma unroll
-        for (int o = GS / 8; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-        if ((lane & (GS / 4 - 1)) == 0 && c < span) xsum[(c / GS) * kXsumTokens + tok] = v;
-      }
-      named_bar_sync(1, kTConsumers * 32);
-    }
-    const int xt0 = min(2 * t, M - 1), xt1 = min(2 * t + 1, M - 1);  // c-fragment tokens (absent ones reuse a real row)
-
-    // Warp w owns the 16-row tiles 2*(w%4) and 2*(w%4)+1 and, of every stage,
-    // the blocks 2*(w/4) and 2*(w/4)+1 (a whole 128-column group): the
-    // activation fragments, the barrier traffic and the loop are shared by two
-    // tiles. The two K halves are summed through shared memory at the end.
-    const int tp = warp & 3;   // tile pair
-    const int kh = warp >> 2;  // which half of each stage
-    const uint32_t ones[4] = {0x00010001u, 0x00010001u, 0x00010001u, 0x00010001u};  // 2^-24 each
-    const float zero4[4] = {0.f, 0.f, 0.f, 0.f};
-    float tot[2][NB][4];
-    float acc[2][NB][4], cx[NB][4];
-#pragma unroll
-    for (int tt = 0; tt < 2; ++tt)
-#pragma unroll
-      for (int nb = 0; nb < NB; ++nb)
-#pragma unroll
-        for (int i = 0; i < 4; ++i) tot[tt][nb][i] = acc[tt][nb][i] = cx[nb][i] = 0.f;
-
-    for (int st = 0; st < nst; ++st) {
-      const int s = st % NS;
-      if (*abort_flag) break;
-      if (!mbar_wait_bounded(bar0 + 8u * s, uint32_t(st / NS) & 1u, kTWaitLimitNs)) {
-        *abort_flag = 1;
-        atomicAdd(&g_gemv_timeouts, 1u);
-        break;
-      }
-      const unsigned char* rs = smem + size_t(s) * SBY;
-      const int kb0 = kb_lo + st * kTStageBlocks;
-      const int nb_st = min(kTStageBlocks, kb_hi - kb0);
-      const int g0 = kb0 * kColsPerBlock / GS;
-      const uint16_t* xst = reinterpret_cast<const uint16_t*>(rs + ST::kBytes);  // this stage's activations
-      uint4 wv[2][2];  // [block][tile]
-#pragma unroll
-      for (int bb = 0; bb < 2; ++bb) {
-        const int b = 2 * kh + bb;
-        if (b < nb_st) {
-#pragma unroll
-          for (int tt = 0; tt < 2; ++tt)
-            wv[bb][tt] = *reinterpret_cast<const uint4*>(rs + b * kTileBytes + (2 * tp + tt) * 512 + lane * 16);
-        }
-      }
-#pragma unroll
-      for (int bb = 0; bb < 2; ++bb) {
-        const int b = 2 * kh + bb;
-        if (b < nb_st) {
-          const int xo = (kb0 - kb_lo + b) * kColsPerBlock;
-          const uint16_t* x0 = STAGED ? xl0 + xo : xst + tok0 * kStageXRow + b * kColsPerBlock + 4 * t;
-          const uint16_t* x1 = STAGED ? xl1 + xo : xst + tok1 * kStageXRow + b * kColsPerBlock + 4 * t;
-          uint2 bx[4][NB];
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            bx[j][0] = ld_x<true>(x0 + j * 16);
-            if (NB > 1) bx[j][NB - 1] = ld_x<true>(x1 + j * 16);
-          }
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const int col = b * kColsPerBlock + j * 16;  // column within the stage
-            const bool fresh = (col % GS) == 0;
-            const bool last = ((col + 16) % GS) == 0;
-            if (!XPRE) {
-#pragma unroll
-              for (int nb = 0; nb < NB; ++nb) mma_16816(cx[nb], ones, bx[j][nb].x, bx[j][nb].y, fresh ? zero4 : cx[nb]);
-            }
-#pragma unroll
-            for (int tt = 0; tt < 2; ++tt) {
-              uint32_t af[4];
-              extract_word(word_of(wv[bb][tt], j), af);
-#pragma unroll
-              for (int nb = 0; nb < NB; ++nb)
-                mma_16816(acc[tt][nb], af, bx[j][nb].x, bx[j][nb].y, fresh ? zero4 : acc[tt][nb]);
-            }
-            if (last) {
-              const int gl = col / GS;  // group within the stage
-              if (g0 + gl < a.G) {
-                if (XPRE) {
-                  // X is the plain activation sum: bring it to the accumulator's 2^-24 scale (exact)
-                  const float* xg = xsum + (g0 + gl - kb_lo * kColsPerBlock / GS) * kXsumTokens;
-                  const float X0 = xg[xt0] * 5.9604644775390625e-8f, X1 = xg[xt1] * 5.9604644775390625e-8f;
-                  cx[0][0] = cx[0][2] = X0;
-                  cx[0][1] = cx[0][3] = X1;
-                }
-#pragma unroll
-                for (int tt = 0; tt < 2; ++tt) {
-                  const int r16 = 2 * tp + tt;
-                  const uint32_t s2 = *reinterpret_cast<const uint32_t*>(rs + ST::kScaleOff + (gl * 64 + r16 * 8 + g) * 4);
-                  const uint32_t zb = SYM ? 0u : uint32_t(rs[ST::kZeroOff + gl * 64 + r16 * 8 + g]);
-                  finalize<NB>(acc[tt], cx, make_factors<SYM>(s2, zb), tot[tt]);
-                }
-              }
-            }
-          }
-        }
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar0 + 8u * (kTMaxStages + s));
-    }
-
-    // K halves -> red[tok][row] (row = 16 * r16 + (g, g + 8)); the buffers
-    // alias the ring, which every consumer is done with after the barrier.
-    named_bar_sync(1, kTConsumers * 32);
-    float* red = reinterpret_cast<float*>(smem);         // [16 tokens][128 rows]
-    float* part = red + 16 * 128;                          // [16 tokens][128 rows], K half 1
-    float* dst = kh == 0 ? red : part;
-#pragma unroll
-    for (int tt = 0; tt < 2; ++tt) {
-      const int row = (2 * tp + tt) * 16 + g;
-#pragma unroll
-      for (int nb = 0; nb < NB; ++nb) {
-        const int tk = nb * 8 + 2 * t;
-        dst[tk * 128 + row] = tot[tt][nb][0];
-        dst[(tk + 1) * 128 + row] = tot[tt][nb][1];
-        dst[tk * 128 + row + 8] = tot[tt][nb][2];
-        dst[(tk + 1) * 128 + row + 8] = tot[tt][nb][3];
-      }
-    }
-    named_bar_sync(1, kTConsumers * 32);
-    for (int e = int(threadIdx.x); e < M * 128; e += kTConsumers * 32) red[e] += part[e];
-  }
-  __syncthreads();
-
-  // Partial sums of the thread blocks that split K reduce through distributed
-  // shared memory in rank order (deterministic); rows beyond N are dropped.
-  const float* red = reinterpret_cast<const float*>(smem);
-  const int nout = a.M * 128;
-  const int KS = int(gridDim.y);
-  if (KS > 1) {
-    cluster_sync_all();
-    const int rank = int(cluster_ctarank());
-    const int per = (nout + KS - 1) / KS;
-    const int e_lo = rank * per;
-    const int e_hi = min(e_lo + per, nout);
-    for (int e = e_lo + int(threadIdx.x); e < e_hi; e += kTThreads) {
-      float acc = 0.f;
-      for (int rk = 0; rk < KS; ++rk) acc += ld_dsmem_f32(red + e, uint32_t(rk));
-      const int tok = e >> 7;
-      const int n = R * 128 + (e & 127);
-      if (n < a.N) a.y[size_t(tok) * a.N + n] = __half_as_ushort(__float2half_rn(acc));
-    }
-    cluster_sync_all();  // keep this block's shared memory alive until its peers are done
-  } else {
-    for (int e = int(threadIdx.x); e < nout; e += kTThreads) {
-      const int tok = e >> 7;
-      const int n = R * 128 + (e & 127);
-      if (n < a.N) a.y[size_t(tok) * a.N + n] = __half_as_ushort(__float2half_rn(red[e]));
-    }
-  }
-}
-
 size_t gemv_smem_bytes(int M, int kb_per_cta, bool staged) {
   const size_t red = size_t(kWarps) * 512 * 4 + size_t(8) * 256 * 4;
   const size_t xs = staged ? size_t(M) * (size_t(kb_per_cta) * kColsPerBlock + 8) * 2 : 0;
@@ -920,75 +579,6 @@ int kb_per_cta_of(const Layout& L, int ksplit) {
   return (kbc + unit - 1) / unit * unit;
 }
 
-template <int MP, int GS, bool SYM, bool STAGED>
-cudaError_t launch_tma_typed(const GemvTmaArgs& a, int NR, int KS, size_t smem_bytes, cudaStream_t stream) {
-  auto kern = gemv_tma_kernel<MP, GS, SYM, STAGED>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem_bytes));
-  if (e != cudaSuccess) return e;
-  if (KS > 8) {
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-    if (e != cudaSuccess) return e;
-  }
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(unsigned(NR), unsigned(KS), 1);
-  cfg.blockDim = dim3(kTThreads, 1, 1);
-  cfg.dynamicSmemBytes = smem_bytes;
-  cfg.stream = stream;
-  cudaLaunchAttribute attrs[2];
-  int na = 0;
-  attrs[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attrs[na].val.programmaticStreamSerializationAllowed = 1;
-  ++na;
-  if (KS > 1) {
-    attrs[na].id = cudaLaunchAttributeClusterDimension;
-    attrs[na].val.clusterDim.x = 1;
-    attrs[na].val.clusterDim.y = unsigned(KS);
-    attrs[na].val.clusterDim.z = 1;
-    ++na;
-  }
-  cfg.attrs = attrs;
-  cfg.numAttrs = na;
-  e = cudaLaunchKernelEx(&cfg, kern, a);
-  if (e != cudaSuccess) return e;
-  return cudaGetLastError();
-}
-
-template <int MP, int GS>
-cudaError_t launch_tma_flags(const GemvTmaArgs& a, bool sym, bool staged, int NR, int KS, size_t smem,
-                             cudaStream_t stream) {
-  if (staged) {
-    return sym ? launch_tma_typed<MP, GS, true, true>(a, NR, KS, smem, stream)
-               : launch_tma_typed<MP, GS, false, true>(a, NR, KS, smem, stream);
-  }
-  return sym ? launch_tma_typed<MP, GS, true, false>(a, NR, KS, smem, stream)
-             : launch_tma_typed<MP, GS, false, false>(a, NR, KS, smem, stream);
-}
-
-template <int MP>
-cudaError_t launch_tma_gs(const GemvTmaArgs& a, int gs, bool sym, bool staged, int NR, int KS, size_t smem,
-                          cudaStream_t stream) {
-  switch (gs) {
-    case 32: return launch_tma_flags<MP, 32>(a, sym, staged, NR, KS, smem, stream);
-    case 64: return launch_tma_flags<MP, 64>(a, sym, staged, NR, KS, smem, stream);
-    default: return launch_tma_flags<MP, 128>(a, sym, staged, NR, KS, smem, stream);
-  }
-}
-
-constexpr size_t kMaxTmaSmem = 200 * 1024;
-
-int tma_stage_bytes_of(const Layout& L, int M) {
-  const int base = L.gsize == 128 ? TStage<128>::kBytes : L.gsize == 64 ? TStage<64>::kBytes : TStage<32>::kBytes;
-  return tma_stage_bytes(base, gemv_staged(L), M);
-}
-
-size_t tma_smem_bytes(const Layout& L, int M, int stages, int kb_per_cta) {
-  const size_t xs_off = tma_xs_offset(stages, tma_stage_bytes_of(L, M));
-  const size_t xs = tma_xs_bytes(gemv_staged(L), M, kb_per_cta);
-  const size_t groups = (size_t(kb_per_cta) * kColsPerBlock + L.gsize - 1) / L.gsize;
-  const size_t xsum = M <= kXsumTokens ? groups * kXsumTokens * 4 : 0;
-  return xs_off + xs + xsum;
-}
-
 bool valid_ksplit(int ks) { return ks == 1 || ks == 2 || ks == 4 || ks == 8 || ks == 16; }
 
 }  // namespace
@@ -998,12 +588,10 @@ bool gemv_plan_ok(const Layout& L, int M, const GemvPlan& p) {
   if (p.kind == kGemvRegisterRing || p.kind == kGemvAsyncCopy) {
     if (p.rows16 != 2 && p.rows16 != 4 && p.rows16 != 8) return false;
     const bool wb = p.kind == kGemvAsyncCopy;
-    if (wb && (p.stages < 2 || p.stages > kTMaxStages)) return false;
     return ring_smem(L, M, kb_per_cta_of(L, p.ksplit), gemv_staged(L) || p.stage_x, wb, p.stages).total <=
            kMaxGemvSmem;
   }
-  if (p.stages < 2 || p.stages > kTMaxStages) return false;
-  return tma_smem_bytes(L, M, p.stages, kb_per_cta_of(L, p.ksplit)) <= kMaxTmaSmem;
+  return false;
 }
 
 GemvPlan gemv_default_plan(const Layout& L, int M, const DeviceInfo& dev, int kind) {
@@ -1034,23 +622,7 @@ GemvPlan gemv_default_plan(const Layout& L, int M, const DeviceInfo& dev, int ki
     }
     return best;
   }
-  // Bulk-copy kernel: one thread block per (128-row block, K slice). Aim for
-  // about two blocks per SM, every block streaming at least two 64-column
-  // blocks; among equally close plans the one with fewer K splits wins.
-  const double target = 2.0 * dev.sm_count;
-  GemvPlan best{kGemvBulkCopy, 0, 4, 1, false};
-  double best_dist = 1e30;
-  for (int ks : {1, 2, 4, 8, 16}) {
-    GemvPlan p{kGemvBulkCopy, 0, 4, ks, false};
-    if (!gemv_plan_ok(L, M, p)) continue;
-    if (ks > 1 && kb_per_cta_of(L, ks) < 2) continue;
-    const double d = std::fabs(std::log(double(L.NR * ks) / target));
-    if (d < best_dist - 1e-9) {
-      best_dist = d;
-      best = p;
-    }
-  }
-  return best;
+  return GemvPlan{kGemvRegisterRing, 8, 0, 1, false};
 }
 
 cudaError_t launch_gemv(const Layout& L, const void* blob, const uint16_t* x, uint16_t* y, int M,
@@ -1058,31 +630,6 @@ cudaError_t launch_gemv(const Layout& L, const void* blob, const uint16_t* x, ui
   const BlobView B = view_of(L, blob);
   const bool staged = gemv_staged(L);
   const int gs = L.gsize;
-  if (plan.kind == kGemvBulkCopy) {
-    GemvTmaArgs a;
-    a.qweight = reinterpret_cast<const uint8_t*>(B.qweight);
-    a.scales = reinterpret_cast<const uint8_t*>(B.scales);
-    a.zeros = B.zeros;
-    a.perm = B.perm;
-    a.x = x;
-    a.y = y;
-    a.M = M;
-    a.N = int(L.N);
-    a.K = int(L.K);
-    a.G = int(L.G);
-    a.KB = int(L.KB);
-    a.kb_per_cta = kb_per_cta_of(L, plan.ksplit);
-    a.stages = plan.stages;
-    a.stage_bytes = tma_stage_bytes_of(L, M);
-    a.flags = flags;
-    const size_t smem = tma_smem_bytes(L, M, plan.stages, a.kb_per_cta);
-    const int NR = int(L.NR), KS = plan.ksplit;
-    if (M <= 1) return launch_tma_gs<1>(a, gs, L.sym, staged, NR, KS, smem, stream);
-    if (M <= 2) return launch_tma_gs<2>(a, gs, L.sym, staged, NR, KS, smem, stream);
-    if (M <= 4) return launch_tma_gs<4>(a, gs, L.sym, staged, NR, KS, smem, stream);
-    if (M <= 8) return launch_tma_gs<8>(a, gs, L.sym, staged, NR, KS, smem, stream);
-    return launch_tma_gs<16>(a, gs, L.sym, staged, NR, KS, smem, stream);
-  }
   GemvArgs a;
   a.qweight = B.qweight;
   a.scales2 = reinterpret_cast<const uint32_t*>(B.scales);

@@ -1,7 +1,7 @@
 """Small, fixed invocations of the library for profiling one kernel at a time.
 
     python -m weight_only_bit_04_b300.profile_cases gemm N K M [--act] [--tile T] [--calls C]
-    python -m weight_only_bit_04_b300.profile_cases gemv N K M [--bulk] [--shape S] [--ksplit S] [--calls C]
+    python -m weight_only_bit_04_b300.profile_cases gemv N K M [--ring | --async] [--shape S] [--ksplit S] [--calls C]
 
 Each run packs one seeded layer (asymmetric uint4, group 128), makes `calls`
 calls of the chosen entry point on the current stream and exits 0 when the
@@ -28,7 +28,9 @@ def main(argv=None) -> int:
     p.add_argument("M", type=int)
     p.add_argument("--act", action="store_true", help="GPTQ act order (gemm)")
     p.add_argument("--tile", type=int, default=0)
-    p.add_argument("--bulk", action="store_true", help="bulk-copy GEMV variant")
+    p.add_argument("--gemm-ksplit", type=int, default=0)
+    p.add_argument("--ring", action="store_true", help="register-ring GEMV kernel")
+    p.add_argument("--async", dest="async_copy", action="store_true", help="asynchronous-copy GEMV kernel")
     p.add_argument("--shape", type=int, default=0)
     p.add_argument("--ksplit", type=int, default=0)
     p.add_argument("--calls", type=int, default=3)
@@ -44,9 +46,10 @@ def main(argv=None) -> int:
     y = torch.empty((a.M, a.N), dtype=torch.float16, device=dev)
     for _ in range(a.calls):
         if a.kind == "gemm":
-            W.gemm(fmt, packed, x, out=y, tile=a.tile)
+            W.gemm(fmt, packed, x, out=y, tile=a.tile, ksplit=a.gemm_ksplit)
         else:
-            W.gemv(fmt, packed, x, out=y, shape=a.shape, ksplit=a.ksplit, bulk_copy=a.bulk)
+            W.gemv(fmt, packed, x, out=y, shape=a.shape, ksplit=a.ksplit, register_ring=a.ring,
+                   async_copy=a.async_copy)
     torch.cuda.synchronize()
     n = W.pipeline_timeouts()
     print(f"{a.kind} {a.N}x{a.K} M={a.M}: {a.calls} calls, pipeline timeouts {n}")

@@ -206,25 +206,23 @@ def dequant(fmt: Format, packed: torch.Tensor, out: torch.Tensor | None = None, 
 
 
 GEMV_WEIGHTS_READY = 1
-GEMV_BULK_COPY = 2
+GEMV_REGISTER_RING = 2
 GEMV_STAGE_ACTIVATIONS = 4
 GEMV_ASYNC_COPY = 8
 GEMV_INPUTS_READY = 16
 
 
 def gemv(fmt: Format, packed: torch.Tensor, x: torch.Tensor, out: torch.Tensor | None = None,
-         shape: int = 0, ksplit: int = 0, weights_ready: bool = False, bulk_copy: bool = False,
+         shape: int = 0, ksplit: int = 0, weights_ready: bool = False, register_ring: bool = False,
          stage_activations: bool = False, async_copy: bool = False, inputs_ready: bool = False,
          stream=None) -> torch.Tensor:
     """y = x . W_hat^T for x fp16 [M, K], 1 <= M <= 16.
 
     ``weights_ready``: the packed weights were complete before the previous
     kernel on the stream started, so the GEMV may stream them early.
-    ``bulk_copy``: the variant that streams weights into a shared-memory ring
-    with bulk copies; ``shape`` is then the ring depth in stages, else the
-    16-row tiles per thread block. ``stage_activations`` (default variant
-    only): copy the activations to shared memory first. ``async_copy``: the
-    default plan with asynchronous-copy rings in shared memory.
+    ``shape``: 16-row tiles per thread block. ``register_ring`` /
+    ``async_copy``: force one of the two kernels (default: by layer size).
+    ``stage_activations``: copy the activations to shared memory first.
     ``inputs_ready``: nothing in flight on the stream writes the weights or
     x or touches y, so the GEMV need not wait for the previous kernel.
     """
@@ -234,7 +232,7 @@ def gemv(fmt: Format, packed: torch.Tensor, x: torch.Tensor, out: torch.Tensor |
     if out is None:
         out = torch.empty((M, fmt.N), dtype=torch.float16, device=x.device)
     yp = _dev(out, torch.float16, "out", (M, fmt.N))
-    flags = ((GEMV_WEIGHTS_READY if weights_ready else 0) | (GEMV_BULK_COPY if bulk_copy else 0)
+    flags = ((GEMV_WEIGHTS_READY if weights_ready else 0) | (GEMV_REGISTER_RING if register_ring else 0)
              | (GEMV_STAGE_ACTIVATIONS if stage_activations else 0) | (GEMV_ASYNC_COPY if async_copy else 0)
              | (GEMV_INPUTS_READY if inputs_ready else 0))
     if shape or ksplit or flags:
