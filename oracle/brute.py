@@ -27,8 +27,13 @@ def _clamp(v: int, lo: int, hi: int) -> int:
     return lo if v < lo else hi if v > hi else v
 
 
-def quantize(W, group_size, sym, g_idx=None):
-    """W: list of rows of Python floats (fp16 values). Returns q, s, z lists."""
+def quantize(W, group_size, sym, g_idx=None, bits=4):
+    """W: list of rows of Python floats (fp16 values). Returns q, s, z lists.
+
+    b-bit codes, top = 2^b - 1. Symmetric: 4 bits s = f16(2a/15), z = 8;
+    8 bits (the int8 absmax code) s = f16(a/127), q = clamp(round(w/s), -127, 127) + 128.
+    """
+    top = (1 << bits) - 1
     N, K = len(W), len(W[0])
     if g_idx is None:
         g_idx = [k // group_size for k in range(K)]
@@ -42,17 +47,23 @@ def quantize(W, group_size, sym, g_idx=None):
             vals = [W[n][k] for k in cols]
             if sym:
                 a = max(abs(v) for v in vals)
-                s = f16(2.0 * a / 15.0)
+                s = f16(2.0 * a / 15.0) if bits == 4 else f16(a / 127.0)
             else:
                 lo, hi = min(vals), max(vals)
-                s = f16((hi - lo) / 15.0)
+                s = f16((hi - lo) / top)
             if s == 0.0:
                 s = 1.0
-            z = 8 if sym else _clamp(round(-lo / s), 0, 15)
+            if sym:
+                z = 8 if bits == 4 else 128
+            else:
+                z = _clamp(round(-lo / s), 0, top)
             s_out[n][t] = s
             z_out[n][t] = z
             for k in cols:
-                q[n][k] = _clamp(round(W[n][k] / s) + z, 0, 15)
+                if sym and bits == 8:
+                    q[n][k] = _clamp(round(W[n][k] / s), -127, 127) + 128
+                else:
+                    q[n][k] = _clamp(round(W[n][k] / s) + z, 0, top)
     return q, s_out, z_out
 
 
@@ -74,9 +85,9 @@ def linear(x, w_hat):
     return y
 
 
-def pack_word(codes8):
-    """Eight codes -> one uint32, code i in bits 4i..4i+3."""
+def pack_word(codes, bits=4):
+    """32/b codes -> one uint32, code i in bits b*i .. b*i+b-1."""
     w = 0
-    for i, c in enumerate(codes8):
-        w |= (c & 0xF) << (4 * i)
+    for i, c in enumerate(codes):
+        w |= (c & ((1 << bits) - 1)) << (bits * i)
     return w

@@ -15,20 +15,23 @@ What it computes, step by step, and where each step comes from:
 2. Scale and zero per (row, group), round to nearest ("LLM Quantization:
    INT8, GPTQ, and AWQ Explained", section "What quantization actually does":
    find the range, pick the scale that spreads the integer grid over it, round
-   each weight to the nearest grid point):
-   asymmetric: s = fp16((max - min) / 15), z = clamp(rint(-min / s), 0, 15);
-   symmetric:  s = fp16(2 * max|w| / 15), z = 8.
+   each weight to the nearest grid point). With b-bit codes, qmax = 2^b - 1:
+   asymmetric: s = fp16((max - min) / qmax), z = clamp(rint(-min / s), 0, qmax);
+   symmetric, 4 bits: s = fp16(2 * max|w| / 15), z = 8 (the linear formula
+     over [-a, a], which reproduces the fixed zero point 8);
+   symmetric, 8 bits: the page's own int8 absmax code, s = fp16(max|w| / 127),
+     codes clamp(rint(w / s), -127, 127), stored with the offset z = 128.
    A scale that is zero (constant group, or a range that rounds to 0 in fp16)
    is replaced by 1.0: the pages do not treat this case.
-3. Codes q = clamp(rint(w / s) + z, 0, 15), the linear quantization formula
+3. Codes q = clamp(rint(w / s) + z, 0, qmax), the linear quantization formula
    q = round(x / S) + Z ("LLM Quantization: A Deep Dive into GPTQ, AWQ, and
    Post-Training Quantization", section "The Math of Quantization") with the
    clamp of the int8 example on the INT8/GPTQ/AWQ page. ``rint`` rounds half
    to even (the pages' own code rounds with torch.round, which does), and the
    division is fp64 with the *stored* fp16 scale.
-4. Canonical packing: 8 nibbles per uint32, nibble j of word k // 8 holds
-   column k with k % 8 == j; zero points packed the same way along the group
-   axis, padded with zero nibbles.
+4. Canonical packing: 32/b codes per uint32 along the packed axis, code j of
+   word k // (32/b) in bits b*j .. b*j+b-1 for column k with k % (32/b) == j;
+   zero points packed the same way along the group axis, padded with zeros.
 5. Dequantization w_hat = fp16((q - z) * s) ("The Math of Quantization":
    x_approx = (q - Z) * S). The fp64 product is exact; one round to nearest
    even gives the fp16 weight ("the actual matrix multiply still happens in
@@ -46,7 +49,19 @@ from __future__ import annotations
 import numpy as np
 
 QMAX = 15  # 4-bit codes are 0..15
-SYM_ZERO = 8  # symmetric scheme: zero point fixed at 8
+SYM_ZERO = 8  # symmetric 4-bit scheme: zero point fixed at 8
+BITS = (4, 8)  # code widths: W4A16 and W8A16 ("4-bit bigger or 8-bit smaller")
+
+
+def qmax(bits: int) -> int:
+    if bits not in BITS:
+        raise ValueError("bits must be 4 or 8")
+    return (1 << bits) - 1
+
+
+def sym_zero(bits: int) -> int:
+    """Fixed zero point of the symmetric scheme: 8 (4 bits), 128 (8 bits)."""
+    return 1 << (bits - 1)
 TOL_REL = 2e-3  # |y_gpu - y_ref| <= TOL_REL * sum|x * w_hat| + TOL_ABS
 TOL_ABS = 1e-3
 
@@ -102,37 +117,46 @@ def group_members(g_idx: np.ndarray, G: int) -> list[np.ndarray]:
 # ---------------------------------------------------------------------------
 # Steps 2-3: round-to-nearest quantization
 # ---------------------------------------------------------------------------
-def quantize_codes(w: np.ndarray, s: np.ndarray, z: np.ndarray) -> np.ndarray:
-    """q = clamp(rint(w / s) + z, 0, 15); w, s, z broadcast, fp64 division."""
+def quantize_codes(w: np.ndarray, s: np.ndarray, z: np.ndarray, bits: int = 4) -> np.ndarray:
+    """q = clamp(rint(w / s) + z, 0, qmax); w, s, z broadcast, fp64 division."""
     w = np.asarray(w, dtype=np.float64)
     s = np.asarray(s, dtype=np.float64)
     q = np.rint(w / s) + np.asarray(z, dtype=np.float64)
-    return np.clip(q, 0, QMAX).astype(np.uint8)
+    return np.clip(q, 0, qmax(bits)).astype(np.uint8)
 
 
-def group_scale_zero(w: np.ndarray, sym: bool) -> tuple[np.ndarray, np.ndarray]:
+def sym8_codes(w: np.ndarray, s: np.ndarray) -> np.ndarray:
+    """8-bit symmetric codes: clamp(rint(w / s), -127, 127) + 128 (the int8
+    absmax code of "What quantization actually does", offset to unsigned)."""
+    w = np.asarray(w, dtype=np.float64)
+    s = np.asarray(s, dtype=np.float64)
+    return (np.clip(np.rint(w / s), -127, 127) + 128).astype(np.uint8)
+
+
+def group_scale_zero(w: np.ndarray, sym: bool, bits: int = 4) -> tuple[np.ndarray, np.ndarray]:
     """Scale (fp16) and zero (uint8) of each row of ``w`` ([rows, members])."""
     w = np.asarray(w, dtype=np.float64)
+    qm = qmax(bits)
     if sym:
         a = np.max(np.abs(w), axis=1)
-        s = fp16_rne(2.0 * a / QMAX)
+        s = fp16_rne(2.0 * a / qm) if bits == 4 else fp16_rne(a / 127.0)
     else:
         mn = np.min(w, axis=1)
         mx = np.max(w, axis=1)
-        s = fp16_rne((mx - mn) / QMAX)
+        s = fp16_rne((mx - mn) / qm)
     s = np.where(s == 0, np.float16(1.0), s).astype(np.float16)
     if sym:
-        z = np.full(w.shape[0], SYM_ZERO, dtype=np.uint8)
+        z = np.full(w.shape[0], sym_zero(bits), dtype=np.uint8)
     else:
-        z = np.clip(np.rint(-mn / s.astype(np.float64)), 0, QMAX).astype(np.uint8)
+        z = np.clip(np.rint(-mn / s.astype(np.float64)), 0, qm).astype(np.uint8)
     return s, z
 
 
-def rtn_quantize(W, group_size: int, sym: bool, g_idx=None):
+def rtn_quantize(W, group_size: int, sym: bool, g_idx=None, bits: int = 4):
     """Round-to-nearest group quantization of fp16 ``W`` [N, K].
 
     Returns codes q uint8 [N, K] (original column order), scales fp16 [N, G]
-    and zeros uint8 [N, G] (all 8 when ``sym``).
+    and zeros uint8 [N, G] (all 8, or 128 at 8 bits, when ``sym``).
     """
     W = np.asarray(W)
     if W.dtype != np.float16:
@@ -145,10 +169,11 @@ def rtn_quantize(W, group_size: int, sym: bool, g_idx=None):
     zeros = np.zeros((N, G), dtype=np.uint8)
     for t, cols in enumerate(group_members(gi, G)):
         w = Wd[:, cols]
-        s, z = group_scale_zero(w, sym)
+        s, z = group_scale_zero(w, sym, bits)
         scales[:, t] = s
         zeros[:, t] = z
-        q[:, cols] = quantize_codes(w, s.astype(np.float64)[:, None], z[:, None])
+        sd = s.astype(np.float64)[:, None]
+        q[:, cols] = sym8_codes(w, sd) if (sym and bits == 8) else quantize_codes(w, sd, z[:, None], bits)
     return q, scales, zeros
 
 
@@ -181,6 +206,36 @@ def unpack_nibbles(words: np.ndarray, C: int) -> np.ndarray:
     out = np.zeros((R, W8 * 8), dtype=np.uint8)
     for j in range(8):
         out[:, j::8] = (words >> np.uint32(4 * j)) & np.uint32(0xF)
+    return out[:, :C]
+
+
+def pack_codes(codes: np.ndarray, bits: int) -> np.ndarray:
+    """Pack b-bit codes [R, C] into uint32 [R, ceil(C / (32/b))], code j of a
+    word in bits b*j .. b*j+b-1; missing columns of the last word are zero."""
+    if bits == 4:
+        return pack_nibbles(codes)
+    codes = np.asarray(codes, dtype=np.uint8)
+    per = 32 // bits
+    R, C = codes.shape
+    nw = -(-C // per)
+    padded = np.zeros((R, nw * per), dtype=np.uint32)
+    padded[:, :C] = codes
+    out = np.zeros((R, nw), dtype=np.uint32)
+    for j in range(per):
+        out |= padded[:, j::per] << np.uint32(bits * j)
+    return out
+
+
+def unpack_codes(words: np.ndarray, C: int, bits: int) -> np.ndarray:
+    """Inverse of ``pack_codes``."""
+    if bits == 4:
+        return unpack_nibbles(words, C)
+    words = np.asarray(words, dtype=np.uint32)
+    per = 32 // bits
+    R, nw = words.shape
+    out = np.zeros((R, nw * per), dtype=np.uint8)
+    for j in range(per):
+        out[:, j::per] = (words >> np.uint32(bits * j)) & np.uint32((1 << bits) - 1)
     return out[:, :C]
 
 
@@ -217,12 +272,12 @@ def error_ratio(y_test, y_ref, B) -> np.ndarray:
     return np.abs(np.asarray(y_test, dtype=np.float64) - y_ref) / tolerance(B)
 
 
-def w4a16_linear(x, W, group_size: int, sym: bool, g_idx=None):
-    """End to end: quantize fp16 W, dequantize, multiply by fp16 x.
+def w4a16_linear(x, W, group_size: int, sym: bool, g_idx=None, bits: int = 4):
+    """End to end: quantize fp16 W (b-bit codes), dequantize, multiply by fp16 x.
 
     Returns (y, B, (q, scales, zeros), w_hat).
     """
-    q, s, z = rtn_quantize(W, group_size, sym, g_idx)
+    q, s, z = rtn_quantize(W, group_size, sym, g_idx, bits)
     w_hat = dequant(q, s, z, group_size, g_idx)
     y, B = linear_ref(x, w_hat)
     return y, B, (q, s, z), w_hat
@@ -231,13 +286,13 @@ def w4a16_linear(x, W, group_size: int, sym: bool, g_idx=None):
 # ---------------------------------------------------------------------------
 # Byte budget (closed form)
 # ---------------------------------------------------------------------------
-def packed_bytes_closed_form(N: int, K: int, group_size: int, sym: bool) -> float:
-    """Bytes of one packed linear: codes N*K/2, fp16 scales N*G*2, 4-bit zeros
-    N*G/2 (none when symmetric), G = K / group_size ("What W4A16 buys":
-    16-bit scale per 128 weights = 0.125 bit/weight, 4-bit zero ~0.03)."""
+def packed_bytes_closed_form(N: int, K: int, group_size: int, sym: bool, bits: int = 4) -> float:
+    """Bytes of one packed linear: codes N*K*b/8, fp16 scales N*G*2, b-bit
+    zeros N*G*b/8 (none when symmetric), G = K / group_size ("What W4A16
+    buys": 16-bit scale per 128 weights = 0.125 bit/weight, 4-bit zero ~0.03)."""
     G = K / group_size
-    return N * K / 2 + N * G * 2 + (0 if sym else N * G / 2)
+    return N * K * bits / 8 + N * G * 2 + (0 if sym else N * G * bits / 8)
 
 
-def bits_per_weight(group_size: int, sym: bool) -> float:
-    return 4 + 16 / group_size + (0 if sym else 4 / group_size)
+def bits_per_weight(group_size: int, sym: bool, bits: int = 4) -> float:
+    return bits + 16 / group_size + (0 if sym else bits / group_size)

@@ -415,3 +415,95 @@ def test_struct_half_rounding_is_the_ieee_one():
     assert struct.unpack("<e", struct.pack("<e", 2049.0))[0] == 2048.0
     assert struct.unpack("<e", struct.pack("<e", 2051.0))[0] == 2052.0
     assert struct.unpack("<e", struct.pack("<e", 1.0 + 2.0 ** -11))[0] == 1.0
+
+
+# ---------------------------------------------------------------------------
+# 8-bit codes (W8A16): the same group machinery with 256 levels
+# ---------------------------------------------------------------------------
+def test_levels_and_8bit_bits_per_weight():
+    lv = _golden()["levels"]["printed"]
+    assert O.qmax(8) + 1 == lv["levels_8bit"] and O.qmax(4) + 1 == lv["levels_4bit"]
+    assert O.bits_per_weight(128, False, 8) == 8 + 0.125 + 0.0625 == 8.1875
+    assert O.bits_per_weight(128, True, 8) == 8.125
+    assert O.packed_bytes_closed_form(4096, 4096, 128, False, 8) * 8 / 4096 ** 2 == 8.1875
+
+
+def test_w4_bigger_vs_w8_smaller_use_similar_memory():
+    g = _golden()["w4_3b_vs_w8_1p5b"]["params_B"]
+    b4 = g["w4"] * 1e9 * O.bits_per_weight(128, False, 4) / 8
+    b8 = g["w8"] * 1e9 * O.bits_per_weight(128, False, 8) / 8
+    assert abs(b4 / b8 - 1) < 0.05  # "similar memory": 1.559 vs 1.535 GB
+
+
+def test_int8_absmax_hand_example():
+    """max|w| = 127 * 2^-7, so s = max|w| / 127 = 2^-7 exactly; w / s below are
+    -127, -1, 1.5 (tie -> 2), 2.5 (tie -> 2), 127; stored with the offset 128."""
+    a = 127 * 2.0 ** -7
+    W = np.array([[-a, -2.0 ** -7, 3 * 2.0 ** -8, 5 * 2.0 ** -8, a, 0, 0, 0]], dtype=np.float16)
+    q, s, z = O.rtn_quantize(W, 8, sym=True, bits=8)
+    i8 = _golden()["int8_absmax"]["printed"]
+    assert float(s[0, 0]) == a / i8["scale_divisor"] == 2.0 ** -7
+    assert int(z[0, 0]) == 128
+    assert q[0].tolist() == [1, 127, 130, 130, 255, 128, 128, 128]
+    assert (q.astype(int) - 128).min() >= i8["clamp"][0] and (q.astype(int) - 128).max() <= i8["clamp"][1]
+    # the 4-bit symmetric rule applied at 8 bits (2a/255) would give another scale
+    assert float(O.fp16_rne(2 * a / 255)) != float(s[0, 0])
+
+
+def test_int8_codes_stay_inside_plus_minus_127():
+    """With s = fp16(a / 127) the largest |w| / s is within 127 * (1 + 2^-11),
+    so every symmetric 8-bit code lies in -127..127 (stored 1..255): code 0
+    (-128) never appears, as the page's clamp range requires."""
+    rng = np.random.default_rng(9)
+    for _ in range(50):
+        W = (rng.standard_normal((4, 64)) * rng.uniform(0.001, 3.0)).astype(np.float16)
+        q, s, z = O.rtn_quantize(W, 64, sym=True, bits=8)
+        assert q.min() >= 1 and np.all(z == 128)
+        am = np.argmax(np.abs(W.astype(np.float64)), axis=1)
+        for n in range(4):  # the largest magnitude maps to the end of the range
+            assert int(q[n, am[n]]) in (1, 255)
+
+
+def test_8bit_roundtrip_and_error_bound():
+    rng = np.random.default_rng(10)
+    for s in O.fp16_rne(rng.uniform(1e-4, 0.5, 16)).astype(np.float64):
+        for z in (0, 1, 77, 128, 200, 255):
+            q = np.arange(256, dtype=np.uint8)
+            w_hat = O.fp16_rne((q.astype(np.float64) - z) * s)
+            assert np.array_equal(O.quantize_codes(w_hat.astype(np.float64), s, z, 8), q)
+    W = synth.weights_np(16, 512, 11)
+    for sym in (False, True):
+        q, sc, zz = O.rtn_quantize(W, 128, sym, bits=8)
+        w_hat = O.dequant(q, sc, zz, 128).astype(np.float64)
+        sd = np.repeat(sc.astype(np.float64), 128, axis=1)
+        u = 2.0 ** -11
+        assert np.all(np.abs(W.astype(np.float64) - w_hat) <= sd * (0.5 + 256 * u) + u * np.abs(w_hat))
+
+
+@pytest.mark.parametrize("sym", [False, True])
+@pytest.mark.parametrize("g", [8, 32, 64])
+@pytest.mark.parametrize("act_order", [False, True])
+def test_numpy_oracle_matches_pure_python_8bit(sym, g, act_order):
+    N, K, M = 6, 128, 3
+    W = synth.weights_np(N, K, synth.seed_for("brute8", N, K, g, sym, act_order))
+    x = synth.activations_np(M, K, 0.05, synth.seed_for("brute8-x", g))
+    gidx = synth.act_order_g_idx(x, g) if act_order else None
+    y, B, (q, s, z), w_hat = O.w4a16_linear(x, W, g, sym, gidx, bits=8)
+    qb, sb, zb = brute.quantize(W.astype(np.float64).tolist(), g, sym, None if gidx is None else gidx.tolist(), 8)
+    assert q.tolist() == qb and s.astype(np.float64).tolist() == sb and z.tolist() == zb
+    gl = (np.arange(K) // g).tolist() if gidx is None else gidx.tolist()
+    wb = brute.dequant(qb, sb, zb, gl)
+    assert w_hat.astype(np.float64).tolist() == wb
+    assert np.allclose(y, np.array(brute.linear(x.astype(np.float64).tolist(), wb)), rtol=1e-12, atol=1e-12)
+
+
+def test_pack_codes_8bit_every_byte_position_and_roundtrip():
+    for pos in range(4):
+        for v in (1, 0x5A, 0xFF):
+            codes = np.zeros((1, 4), dtype=np.uint8)
+            codes[0, pos] = v
+            w = O.pack_codes(codes, 8)
+            assert int(w[0, 0]) == v << (8 * pos) == brute.pack_word(codes[0].tolist(), 8)
+    rng = np.random.default_rng(12)
+    c = rng.integers(0, 256, (5, 37)).astype(np.uint8)
+    assert np.array_equal(O.unpack_codes(O.pack_codes(c, 8), 37, 8), c)
