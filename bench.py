@@ -45,8 +45,10 @@ FALLBACK_HBM_GBPS = 6400.0
 FALLBACK_BF16_TFLOPS = 1800.0
 # ncu DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of the GEMV
 # kernel, bytes per launch averaged over one layer's seven launches of the
-# Llama-2-7B sweep; valid only for the kernel source it was taken on.
+# Llama-2-7B sweep (4-bit codes); valid only for the kernel sources it was
+# taken on (GEMV_SOURCES).
 GEMV_TRAFFIC = {"source_sha1": "8f5c0995a1a8d601d2dcce6bdbadec135cd15ee3", "bytes_per_launch": 15054446}
+GEMV_SOURCES = ("gemv_impl.cuh", "k_gemv.cu", "k_gemv_b4.cu")
 L2_FLUSH_BYTES = 256 << 20
 
 
@@ -59,12 +61,13 @@ def parse_args():
     p.add_argument("--workload", default="llama2-7b", choices=["llama2-7b", "llama70b", "sweep8192"])
     p.add_argument("--no-gemm", action="store_true")
     p.add_argument("--no-shapes", action="store_true")
+    p.add_argument("--bits", type=int, default=4, choices=[4, 8], help="code width of every packed linear")
     return p.parse_args()
 
 
-def gemv_bytes(N: int, K: int, M: int = 1, g: int = 128, sym: bool = False) -> int:
+def gemv_bytes(N: int, K: int, M: int = 1, g: int = 128, sym: bool = False, bits: int = 4) -> int:
     G = K // g
-    return N * K // 2 + N * G * 2 + (0 if sym else N * G // 2) + M * K * 2 + M * N * 2
+    return N * K * bits // 8 + N * G * 2 + (0 if sym else N * G * bits // 8) + M * K * 2 + M * N * 2
 
 
 def measured_peaks():
@@ -77,9 +80,12 @@ def measured_peaks():
         return FALLBACK_HBM_GBPS, FALLBACK_BF16_TFLOPS, "fallback"
 
 
-def source_sha1(name: str) -> str:
-    with open(os.path.join(ROOT, "weight_only_bit_04_b300", "csrc", name), "rb") as f:
-        return hashlib.sha1(f.read()).hexdigest()
+def source_sha1(names) -> str:
+    h = hashlib.sha1()
+    for name in names:
+        with open(os.path.join(ROOT, "weight_only_bit_04_b300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
 
 
 class ClockSampler:
@@ -133,8 +139,8 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 # our arm
 # ---------------------------------------------------------------------------
-def build_stack(torch, W, synth, dev, workload):
-    """Pack every linear of the decode stack on the GPU (RTN, asym uint4, g128)."""
+def build_stack(torch, W, synth, dev, workload, bits=4):
+    """Pack every linear of the decode stack on the GPU (RTN, asymmetric, g128)."""
     if workload == "llama70b":
         linears, nlayers, frac, tag = synth.LLAMA_70B_LINEARS, synth.LLAMA_70B_LAYERS, synth.LLAMA_70B_OUTLIER_FRAC, "llama70b"
     else:
@@ -143,7 +149,7 @@ def build_stack(torch, W, synth, dev, workload):
     for layer in range(nlayers):
         lins = []
         for name, N, K in linears:
-            fmt = W.make_format(N, K, 128, False, False)
+            fmt = W.make_format(N, K, 128, False, False, bits=bits)
             w = synth.weights_cuda(N, K, synth.seed_for(tag, layer, name, "w"), device=dev)
             q, s, z = W.quantize_rtn(fmt, w)
             packed = W.pack(fmt, q, s, z)
@@ -204,7 +210,7 @@ def per_shape(torch, W, layers, xs, dev):
             g.replay()
         torch.cuda.synchronize()
         ms = time_graph(torch, g, stream, 20) / len(layers)
-        nb = gemv_bytes(fmt.N, fmt.K)
+        nb = gemv_bytes(fmt.N, fmt.K, bits=fmt.bits)
         res[key] = {"us": round(ms * 1e3, 2), "GB/s": round(nb / (ms * 1e-3) / 1e9, 1), "linears": name}
         del g
     return res
@@ -225,9 +231,9 @@ def run_ours(args, rank, world, local_rank):
         run_sweep8192(torch, W, synth, dev, args, rank, world, dist)
         return
 
-    layers, xs, ys, yall = build_stack(torch, W, synth, dev, args.workload)
+    layers, xs, ys, yall = build_stack(torch, W, synth, dev, args.workload, args.bits)
     n_launch = sum(len(l) for l in layers)
-    step_bytes = sum(gemv_bytes(fmt.N, fmt.K) for lins in layers for _, fmt, _ in lins)
+    step_bytes = sum(gemv_bytes(fmt.N, fmt.K, bits=fmt.bits) for lins in layers for _, fmt, _ in lins)
 
     # Dependency schedules of the sweep. "decode": the launches that read the
     # same activations as the one before (k and v after q, up after gate) do
@@ -317,7 +323,7 @@ def run_ours(args, rank, world, local_rank):
     if rank == 0:
         hbm, bf16, peak_kind = measured_peaks()
         traffic = None
-        if GEMV_TRAFFIC["source_sha1"] == source_sha1("k_gemv.cu"):
+        if args.bits == 4 and GEMV_TRAFFIC["source_sha1"] == source_sha1(GEMV_SOURCES):
             traffic = GEMV_TRAFFIC["bytes_per_launch"]
         per_rank = step_bytes / (ms * 1e-3) / 1e9
         if args.workload == "llama70b":
@@ -329,7 +335,7 @@ def run_ours(args, rank, world, local_rank):
                         "down 4096x11008), 224 GEMVs per step")
             frac = synth.LLAMA2_7B_OUTLIER_FRAC
         line = {
-            "metric": METRIC,
+            "metric": METRIC if args.bits == 4 else METRIC.replace("W4A16", "W8A16"),
             "value": round(value, 1),
             "unit": "GB/s",
             "n_gpus": world,
@@ -339,11 +345,11 @@ def run_ours(args, rank, world, local_rank):
             "higher_is_better": True,
             "scaling": "weak",
             "vs_baseline": None,
-            "dtype": "fp16 activations x uint4 weights, fp32 accumulate",
+            "dtype": f"fp16 activations x uint{args.bits} weights, fp32 accumulate",
             "data": (f"synthetic: seeded N(0,0.02) weights RTN-quantized on the GPU, N(0,1) fp16 activations "
                      f"with {100 * frac:g}% outlier channels x20"),
             "config": {"workload": workload,
-                       "M": 1, "group_size": 128, "scheme": "asymmetric uint4, fp16 scales",
+                       "M": 1, "group_size": 128, "scheme": f"asymmetric uint{args.bits}, fp16 scales",
                        "bytes_per_step": step_bytes, "launches_per_step": n_launch,
                        "l2": f"inputs larger than L2 ({step_bytes / 1e9:.2f} GB of packed weights per step vs 126 MB L2)",
                        "timing": "CUDA graph replay per step, CUDA events on the launching stream",
@@ -400,7 +406,7 @@ def run_gemm(torch, W, synth, dev, args):
     for N, K in synth.PREFILL_SHAPES:
         x = synth.activations_cuda(M, K, 0.01, synth.seed_for("prefill", "x", N, K), device=dev)
         gidx = synth.act_order_g_idx(x.float().cpu().numpy(), 128)
-        fmt = W.make_format(N, K, 128, False, True)
+        fmt = W.make_format(N, K, 128, False, True, bits=args.bits)
         w = synth.weights_cuda(N, K, synth.seed_for("prefill", "w", N, K), device=dev)
         q, s, z = W.quantize_rtn(fmt, w, gidx)
         packed = W.pack(fmt, q, s, z, gidx)

@@ -5,7 +5,9 @@
  * The layer computes y = x . W_hat^T, where W_hat[n][k] = (q[n][k] - z) * s:
  * 4-bit codes q, one fp16 scale s and one 4-bit zero point z per (row, group)
  * of `group_size` input columns, fp16 activations x and outputs y, fp32
- * accumulation. The format follows "AWQ + GPTQ Quantization, in depth",
+ * accumulation. The same entry points take 8-bit codes (W8A16, the wider
+ * choice weighed in "AWQ + GPTQ Quantization, in depth", section "4-bit bigger
+ * or 8-bit smaller"). The format follows "AWQ + GPTQ Quantization, in depth",
  * section "What W4A16 buys and why decoding gets faster" (packed 4-bit weights
  * expanded to 16 bits in registers with the group's scale and zero point; one
  * scale per run of 128 consecutive input weights of a row) and "LLM
@@ -58,7 +60,7 @@ typedef struct CUstream_st* w4a16_stream_t;
 typedef enum {
   W4A16_OK = 0,
   W4A16_ERR_INVALID_ARG = 1,     /* NULL pointer, bad size, M out of range, bad g_idx */
-  W4A16_ERR_UNSUPPORTED = 2,     /* valid but not implemented (bits != 4, group size, ...) */
+  W4A16_ERR_UNSUPPORTED = 2,     /* valid but not implemented (bits not 4 or 8, group size, ...) */
   W4A16_ERR_MISALIGNED = 3,      /* a pointer is not aligned as documented */
   W4A16_ERR_BUFFER_TOO_SMALL = 4,/* packed_bytes or workspace_bytes below the requirement */
   W4A16_ERR_CUDA = 5             /* a CUDA call failed; see w4a16_last_cuda_error() */
@@ -66,13 +68,14 @@ typedef enum {
 
 /*
  * Quantization format of one linear layer (out features N x in features K).
- *   bits        must be 4.
+ *   bits        4 or 8 (b below; codes 0 .. 2^b - 1).
  *   group_size  32, 64 or 128; K must be a multiple of it (G = K / group_size
  *               groups per row). 128 is the common default; smaller groups
  *               track the weights more closely and cost more bits ("What W4A16
  *               buys ...").
- *   symmetric   0: asymmetric, one 4-bit zero point per (row, group);
- *               1: symmetric, zero point fixed at 8, no zero points stored.
+ *   symmetric   0: asymmetric, one b-bit zero point per (row, group);
+ *               1: symmetric, zero point fixed at 2^(b-1) (8 or 128), no
+ *                  zero points stored.
  *   has_g_idx   0: column k belongs to group k / group_size;
  *               1: GPTQ act order -- a column-to-group map g_idx is given at
  *                  pack time ("The two algorithms, compactly": act order
@@ -93,11 +96,12 @@ typedef struct {
  * With NR = ceil(N / 128) row blocks, KB = ceil(K / 64) column blocks and
  * G = K / group_size, it holds four sub-arrays, each starting on a 256-byte
  * boundary, in this order:
- *   qweight  NR*KB*4096 bytes: for every (row block, column block) a 4 KiB
- *            tile of 128 rows x 64 columns of 4-bit codes, arranged so that a
- *            warp's 16-byte loads yield tensor-core operand fragments.
+ *   qweight  NR*KB*512*b bytes: for every (row block, column block) a tile
+ *            of 128 rows x 64 columns of b-bit codes (4 or 8 KiB), arranged
+ *            so that a warp's 16-byte loads yield tensor-core operand
+ *            fragments.
  *   scales   NR*G*256 bytes: fp16 scales, 128 rows per (row block, group).
- *   zeros    NR*G*64 bytes (asymmetric only): 4-bit zero points.
+ *   zeros    NR*G*16*b bytes (asymmetric only): b-bit zero points.
  *   perm     K*4 bytes (act order only): packed column -> original column.
  * Rows beyond N and columns beyond K are padding. The blob's meaning is fixed
  * by w4a16_dequant; its internal arrangement is private and may change.
@@ -119,15 +123,19 @@ W4A16_API int w4a16_last_cuda_error(void);
  * Round-to-nearest group quantization of fp16 weights (the step before the
  * path: "LLM Quantization: INT8, GPTQ, and AWQ Explained", section "What
  * quantization actually does" -- find each group's range, pick the scale,
- * round to the nearest grid point, clamp). Per (row n, group t), in fp64:
- *   asymmetric: s = fp16_rne((max - min) / 15), z = clamp(rint(-min / s), 0, 15)
- *   symmetric:  s = fp16_rne(2 * max|w| / 15),  z = 8
- *   (s == 0 is replaced by 1.0), and q = clamp(rint(w / s) + z, 0, 15),
+ * round to the nearest grid point, clamp). Per (row n, group t), in fp64,
+ * with qmax = 2^b - 1:
+ *   asymmetric: s = fp16_rne((max - min) / qmax), z = clamp(rint(-min / s), 0, qmax)
+ *   symmetric, 4 bits: s = fp16_rne(2 * max|w| / 15), z = 8
+ *   symmetric, 8 bits: s = fp16_rne(max|w| / 127), z = 128 (the int8 absmax
+ *               code of the same section, stored offset by 128), and
+ *               q = clamp(rint(w / s), -127, 127) + 128 (codes 1 .. 255)
+ *   (s == 0 is replaced by 1.0), otherwise q = clamp(rint(w / s) + z, 0, qmax),
  *   rint = round half to even.
  *   w        fp16 [N][K] row-major, 16-byte aligned.
  *   g_idx    HOST int32 [K] (act order) or NULL; group t's members are the
  *            columns k with g_idx[k] == t, exactly group_size of them.
- *   q        uint8 [N][K] codes 0..15, original column order.
+ *   q        uint8 [N][K] codes 0 .. qmax, original column order.
  *   scales   fp16 [N][G], 2-byte aligned.
  *   zeros    uint8 [N][G]; must be NULL when f->symmetric.
  *   workspace / workspace_bytes: >= w4a16_quantize_workspace_bytes(f)
@@ -169,9 +177,11 @@ W4A16_API w4a16_status w4a16_quantize_rtn_noalloc(const w4a16_format* f, const u
 
 /*
  * Pack canonical codes, scales and zero points into the device blob.
- *   q        uint8 [N][K], codes 0..15 (only the low 4 bits are used).
+ *   q        uint8 [N][K], codes 0 .. 2^b - 1 (4 bits: only the low 4 bits
+ *            are used).
  *   scales   fp16 [N][G], 2-byte aligned.
- *   zeros    uint8 [N][G] codes 0..15 when asymmetric; NULL when symmetric.
+ *   zeros    uint8 [N][G] codes when asymmetric (4 bits: low 4 bits used);
+ *            NULL when symmetric.
  *   g_idx    HOST int32 [K] when f->has_g_idx, else NULL. Every group
  *            0..G-1 must have exactly group_size members (checked here);
  *            the blob stores the columns sorted by group (stable), so that

@@ -62,9 +62,20 @@ def test_packed_bytes_layout(lib):
     assert W.packed_bytes(fmt(200, 96, g=32)) == 2 * 2 * 4096 + 2 * 3 * 256 + 512
 
 
+def test_packed_bytes_8bit(lib):
+    """8-bit codes: twice the code and zero-point bytes, the same scales."""
+    for sym in (False, True):
+        f8 = fmt(4096, 4096, sym=sym, bits=8)
+        assert W.check_format(f8) == 0
+        assert W.packed_bytes(f8) == O.packed_bytes_closed_form(4096, 4096, 128, sym, bits=8)
+    # padding: 2 x 2 tiles of 8 KiB, scales 2*3*256, zeros 2*3*128 = 768 (a multiple of 256)
+    assert W.packed_bytes(fmt(200, 96, g=32, bits=8)) == 2 * 2 * 8192 + 2 * 3 * 256 + 768
+
+
 @pytest.mark.parametrize("kw,status", [
-    (dict(bits=8), UNSUPPORTED),
     (dict(bits=3), UNSUPPORTED),
+    (dict(bits=2), UNSUPPORTED),
+    (dict(bits=16), UNSUPPORTED),
     (dict(g=16), UNSUPPORTED),
     (dict(g=256), UNSUPPORTED),
     (dict(K=96, g=64), UNSUPPORTED),   # ragged last group

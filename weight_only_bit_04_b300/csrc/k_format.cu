@@ -54,22 +54,31 @@ __global__ void __launch_bounds__(256) quantize_rtn_kernel(Layout L, const uint1
     amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
   }
   // fp64 from here on; every fp16 value and difference of two is exact in fp64.
-  double range = L.sym ? 2.0 * double(amax) : double(mx) - double(mn);
-  __half s_h = __double2half(range / 15.0);  // round to nearest even
+  // b-bit codes, qmax = 2^b - 1. Symmetric: 4 bits s = 2a/15, z = 8; 8 bits
+  // the int8 absmax code, s = a/127, codes clamp(rint(w/s), -127, 127) + 128.
+  const double qmax = double((1 << L.bits) - 1);
+  const bool sym8 = L.sym && L.bits == 8;
+  const double range = L.sym ? (sym8 ? double(amax) / 127.0 : 2.0 * double(amax) / qmax) : (double(mx) - double(mn)) / qmax;
+  __half s_h = __double2half(range);  // round to nearest even
   if (__half2float(s_h) == 0.0f) s_h = __float2half(1.0f);
   const double s = double(__half2float(s_h));
   double z;
   if (L.sym) {
-    z = 8.0;
+    z = double(1 << (L.bits - 1));
   } else {
     z = rint(-double(mn) / s);
-    z = fmin(fmax(z, 0.0), 15.0);
+    z = fmin(fmax(z, 0.0), qmax);
   }
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     if (i < per_lane) {
-      double c = rint(double(v[i]) / s) + z;
-      c = fmin(fmax(c, 0.0), 15.0);
+      double c;
+      if (sym8) {
+        c = fmin(fmax(rint(double(v[i]) / s), -127.0), 127.0) + 128.0;
+      } else {
+        c = rint(double(v[i]) / s) + z;
+        c = fmin(fmax(c, 0.0), qmax);
+      }
       q[n * L.K + col[i]] = uint8_t(c);
     }
   }
@@ -85,34 +94,55 @@ __global__ void __launch_bounds__(256) quantize_rtn_kernel(Layout L, const uint1
 __global__ void __launch_bounds__(256) pack_qweight_kernel(Layout L, const uint8_t* __restrict__ q,
                                                            const int32_t* __restrict__ perm,
                                                            uint32_t* __restrict__ qweight) {
+  const int tile_words = kTileWords * L.bits / 4;
   const int64_t wi = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (wi >= L.NR * L.KB * kTileWords) return;
-  const int64_t tile = wi / kTileWords;
-  const int within = int(wi - tile * kTileWords);
+  if (wi >= L.NR * L.KB * tile_words) return;
+  const int64_t tile = wi / tile_words;
+  const int within = int(wi - tile * tile_words);
   const int64_t R = tile / L.KB;
   const int64_t b = tile - R * L.KB;
-  const int r16 = within >> 7;
-  const int lane = (within >> 2) & 31;
-  const int j = within & 3;
-  const int g = lane >> 2, t = lane & 3;
-  const int64_t n0 = R * kRowsPerBlock + r16 * 16 + g;
-  const int64_t p0 = b * kColsPerBlock + j * 16 + 4 * t;
   uint32_t word = 0;
+  if (L.bits == 4) {
+    const int r16 = within >> 7;
+    const int lane = (within >> 2) & 31;
+    const int j = within & 3;
+    const int g = lane >> 2, t = lane & 3;
+    const int64_t n0 = R * kRowsPerBlock + r16 * 16 + g;
+    const int64_t p0 = b * kColsPerBlock + j * 16 + 4 * t;
 #pragma unroll
-  for (int kk = 0; kk < 4; ++kk) {
-    const int64_t p = p0 + kk;
-    if (p >= L.K) continue;
-    const int64_t c = perm ? perm[p] : p;
+    for (int kk = 0; kk < 4; ++kk) {
+      const int64_t p = p0 + kk;
+      if (p >= L.K) continue;
+      const int64_t c = perm ? perm[p] : p;
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int64_t n = n0 + 8 * h;
-      if (n < L.N) word |= uint32_t(q[n * L.K + c] & 0xF) << (4 * nibble_index(kk, h));
+      for (int h = 0; h < 2; ++h) {
+        const int64_t n = n0 + 8 * h;
+        if (n < L.N) word |= uint32_t(q[n * L.K + c] & 0xF) << (4 * nibble_index(kk, h));
+      }
+    }
+  } else {
+    // word (r16, p, lane, jj, h): row r16*16 + g + 8h, columns 16j + 4t + kk
+    // in byte kk, j = 2p + jj
+    const int r16 = within >> 8;
+    const int lane = (within >> 2) & 31;
+    const int j = 2 * ((within >> 7) & 1) + ((within >> 1) & 1);
+    const int h = within & 1;
+    const int g = lane >> 2, t = lane & 3;
+    const int64_t n = R * kRowsPerBlock + r16 * 16 + g + 8 * h;
+    const int64_t p0 = b * kColsPerBlock + j * 16 + 4 * t;
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) {
+      const int64_t p = p0 + kk;
+      if (p >= L.K || n >= L.N) continue;
+      const int64_t c = perm ? perm[p] : p;
+      word |= uint32_t(q[n * L.K + c]) << (8 * kk);
     }
   }
   qweight[wi] = word;
 }
 
-// One thread per (row block, group, 16-row tile, lane group): a scale pair and a zero byte.
+// One thread per (row block, group, 16-row tile, lane group): a scale pair and
+// the zero points of the two rows (one byte of two nibbles, or two bytes).
 __global__ void __launch_bounds__(256) pack_meta_kernel(Layout L, const uint16_t* __restrict__ scales,
                                                         const uint8_t* __restrict__ zeros,
                                                         uint32_t* __restrict__ s_out,
@@ -130,9 +160,14 @@ __global__ void __launch_bounds__(256) pack_meta_kernel(Layout L, const uint16_t
   const uint32_t s1 = n1 < L.N ? scales[n1 * L.G + gi] : 0u;
   s_out[i] = s0 | (s1 << 16);
   if (z_out) {
-    const uint32_t z0 = n0 < L.N ? (zeros[n0 * L.G + gi] & 0xF) : 0u;
-    const uint32_t z1 = n1 < L.N ? (zeros[n1 * L.G + gi] & 0xF) : 0u;
-    z_out[i] = uint8_t(z0 | (z1 << 4));
+    if (L.bits == 4) {
+      const uint32_t z0 = n0 < L.N ? (zeros[n0 * L.G + gi] & 0xF) : 0u;
+      const uint32_t z1 = n1 < L.N ? (zeros[n1 * L.G + gi] & 0xF) : 0u;
+      z_out[i] = uint8_t(z0 | (z1 << 4));
+    } else {
+      z_out[2 * i] = n0 < L.N ? zeros[n0 * L.G + gi] : uint8_t(0);
+      z_out[2 * i + 1] = n1 < L.N ? zeros[n1 * L.G + gi] : uint8_t(0);
+    }
   }
 }
 
@@ -141,15 +176,18 @@ __global__ void __launch_bounds__(256) pack_meta_kernel(Layout L, const uint16_t
 // (1024 + q) - (1024 + z) is exact in fp16, the product is rounded once.
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) dequant_kernel(Layout L, BlobView B, uint16_t* __restrict__ out) {
+  const int tile_words = kTileWords * L.bits / 4;
   const int64_t wi = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (wi >= L.NR * L.KB * kTileWords) return;
-  const int64_t tile = wi / kTileWords;
-  const int within = int(wi - tile * kTileWords);
+  if (wi >= L.NR * L.KB * tile_words) return;
+  const int64_t tile = wi / tile_words;
+  const int within = int(wi - tile * tile_words);
   const int64_t R = tile / L.KB;
   const int64_t b = tile - R * L.KB;
-  const int r16 = within >> 7;
+  const bool b8 = L.bits == 8;
+  const int r16 = b8 ? within >> 8 : within >> 7;
   const int lane = (within >> 2) & 31;
-  const int j = within & 3;
+  const int j = b8 ? 2 * ((within >> 7) & 1) + ((within >> 1) & 1) : within & 3;
+  const int hw = b8 ? within & 1 : 0;  // 8-bit: the word's row (g or g+8)
   const int g = lane >> 2, t = lane & 3;
   const int64_t n0 = R * kRowsPerBlock + r16 * 16 + g;
   const int64_t p0 = b * kColsPerBlock + j * 16 + 4 * t;
@@ -162,11 +200,19 @@ __global__ void __launch_bounds__(256) dequant_kernel(Layout L, BlobView B, uint
     const int64_t mi = ((R * L.G + gi) * 8 + r16) * 8 + g;
     const int64_t c = B.perm ? B.perm[p] : p;
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
+    for (int hh = 0; hh < 2; ++hh) {
+      if (b8 && hh != hw) continue;
+      const int h = hh;
       const int64_t n = n0 + 8 * h;
       if (n >= L.N) continue;
-      const uint32_t code = (word >> (4 * nibble_index(kk, h))) & 0xF;
-      const uint32_t z = B.zeros ? ((B.zeros[mi] >> (4 * h)) & 0xF) : 8u;
+      uint32_t code, z;
+      if (b8) {
+        code = (word >> (8 * kk)) & 0xFF;
+        z = B.zeros ? B.zeros[2 * mi + h] : 128u;
+      } else {
+        code = (word >> (4 * nibble_index(kk, h))) & 0xF;
+        z = B.zeros ? ((B.zeros[mi] >> (4 * h)) & 0xF) : 8u;
+      }
       const __half s = __ushort_as_half(B.scales[2 * mi + h]);
       const __half d = __hsub(__ushort_as_half(uint16_t(0x6400u | code)),
                               __ushort_as_half(uint16_t(0x6400u | z)));
@@ -192,7 +238,7 @@ cudaError_t launch_pack(const Layout& L, const uint8_t* q, const uint16_t* scale
                         const uint8_t* zeros, void* blob, cudaStream_t stream) {
   char* b = static_cast<char*>(blob);
   const int32_t* perm = L.act ? reinterpret_cast<const int32_t*>(b + L.p_off) : nullptr;
-  const int64_t words = L.NR * L.KB * kTileWords;
+  const int64_t words = L.NR * L.KB * kTileWords * L.bits / 4;
   pack_qweight_kernel<<<blocks_for(words, 256), 256, 0, stream>>>(
       L, q, perm, reinterpret_cast<uint32_t*>(b + L.q_off));
   cudaError_t e = cudaGetLastError();
@@ -205,7 +251,7 @@ cudaError_t launch_pack(const Layout& L, const uint8_t* q, const uint16_t* scale
 }
 
 cudaError_t launch_dequant(const Layout& L, const void* blob, uint16_t* w_out, cudaStream_t stream) {
-  const int64_t words = L.NR * L.KB * kTileWords;
+  const int64_t words = L.NR * L.KB * kTileWords * L.bits / 4;
   dequant_kernel<<<blocks_for(words, 256), 256, 0, stream>>>(L, view_of(L, blob), w_out);
   return cudaGetLastError();
 }

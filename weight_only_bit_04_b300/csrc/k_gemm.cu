@@ -50,14 +50,32 @@ constexpr uint64_t kWaitLimitNs = 1000ull * 1000ull * 1000ull;  // 1 s per wait
 // activations; DS: dequantization warp sets, set d producing the 64-column
 // steps kb = d (mod DS), so that each scheduler interleaves DS independent
 // dequantization streams.
-// Packed-weight part of a stage, per 128-row tile: the 4 KiB code tile, then
-// up to two groups of scale pairs (256 B each) and of zero bytes (64 B each).
-constexpr int kWCodes = 4096;
-constexpr int kWScaleOff = kWCodes;
-constexpr int kWZeroOff = kWScaleOff + 2 * 256;
-constexpr int kWTile = kWZeroOff + 2 * 64;
+// Packed-weight part of a stage, per 128-row tile: the code tile (4 KiB of
+// 4-bit or 8 KiB of 8-bit codes), then up to two groups of scale pairs (256 B
+// each) and of zero points (64 B of nibble pairs or 128 B of byte pairs each).
+template <int BITS>
+struct WTile {
+  static constexpr int kCodes = 4096 * BITS / 4;
+  static constexpr int kR16 = kCodes / 8;  // bytes of one 16-row tile
+  static constexpr int kScaleOff = kCodes;
+  static constexpr int kZeroGroup = 64 * BITS / 4;
+  static constexpr int kZeroOff = kScaleOff + 2 * 256;
+  static constexpr int kBytes = kZeroOff + 2 * kZeroGroup;
+};
 
-template <int WR, int NT, int SA, int SB, int DS>
+constexpr int kMaxSmem = 232448;
+constexpr int stage_bytes(int WR, int NT, int BITS) {
+  return (NT * 128 + WR * (4096 * BITS / 4 + 512 + 2 * 64 * BITS / 4) + 1023) / 1024 * 1024;
+}
+// Activation stages of a tile, reduced for 8-bit codes until the block's
+// shared memory fits.
+constexpr int fit_sb(int WR, int NT, int SA, int SB, int BITS) {
+  int s = SB;
+  while (s > 2 && s * stage_bytes(WR, NT, BITS) + 1024 + 8 * (SA * 2 + s * 2 + 1) + 16 > kMaxSmem) --s;
+  return s;
+}
+
+template <int WR, int NT, int SA, int SB, int DS, int BITS>
 struct Cfg {
   static constexpr int kSetWarps = 4 * WR;        // one warp per (128-row tile, lane quarter)
   static constexpr int kDeqWarps = kSetWarps * DS;
@@ -67,14 +85,15 @@ struct Cfg {
   static constexpr int kDCols = WR * NT;          // fp32 accumulators
   static constexpr int kACol0 = kDCols;           // first A column
   static constexpr int kBStage = NT * 128;        // activations: NT rows x 64 fp16 (128-byte swizzle)
-  static constexpr int kStage = (kBStage + WR * kWTile + 1023) / 1024 * 1024;  // + packed weights
+  static constexpr int kStage = stage_bytes(WR, NT, BITS);  // + packed weights
+  static_assert(kStage == (kBStage + WR * WTile<BITS>::kBytes + 1023) / 1024 * 1024, "stage layout");
   static constexpr int kBarBytes = 8 * (SA * 2 + SB * 2 + 1) + 16;
   static constexpr int kSmem = SB * kStage + 1024 + kBarBytes;
   static constexpr int kEpiTokens = NT / DS;      // tokens each set writes back
   // tensor-memory columns allocated: 256 lets two blocks share an SM
   static constexpr int kTmemCols = kDCols + SA * WR * 32 <= 256 ? 256 : 512;
   static_assert(kDCols + SA * WR * 32 <= 512, "tensor memory budget");
-  static_assert(kSmem <= 232448, "shared memory per block");
+  static_assert(kSmem <= kMaxSmem, "shared memory per block");
   static_assert(NT * WR * 128 * 4 <= SB * kStage, "split-K partial sums must fit in the stages");
   static_assert(SA % DS == 0, "each tensor-memory stage belongs to one set");
   static_assert(kEpiTokens % 32 == 0, "epilogue in 32-token chunks");
@@ -127,13 +146,19 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, vol
   return false;
 }
 
-template <int GS, bool SYM>
+template <int GS, bool SYM, int BITS>
 struct StepRegs {
   static constexpr int kGroups = GS == 32 ? 2 : 1;  // groups in one 64-column step
-  uint4 w[2];                 // packed words of the warp's two 16-row tiles
+  uint4 w[2][BITS / 4];       // packed words of the warp's two 16-row tiles
   uint32_t s[2][kGroups];     // scale pairs
-  uint32_t z[2][kGroups];     // zero bytes
+  uint32_t z[2][kGroups];     // zero points (nibble pair, or byte pair)
 };
+
+__device__ __forceinline__ uint32_t prmt_u32(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
+}
 
 // Groups whose metadata a 64-column step carries: one, or two for 32-column
 // groups (one at a ragged end of K).
@@ -145,36 +170,57 @@ __device__ __forceinline__ int step_groups(int kb, int G) {
 // Dequantize one step of one 16-row tile into the 16 registers of a
 // tcgen05.st 16x256b.x4: per 16-column group j, (row g, columns 4t..4t+1),
 // (row g, 4t+2..4t+3), (row g+8, 4t..4t+1), (row g+8, 4t+2..4t+3).
-template <int GS, bool SYM>
-__device__ __forceinline__ void dequant_tile(const StepRegs<GS, SYM>& r, int i, uint32_t (&v)[16]) {
-  constexpr int NG = StepRegs<GS, SYM>::kGroups;
+// 8-bit codes: PRMT places code bytes under the exponent byte 0x64, giving
+// fp16 1024 + q; subtracting 1024 + z leaves the exact q - z.
+template <int GS, bool SYM, int BITS>
+__device__ __forceinline__ void dequant_tile(const StepRegs<GS, SYM, BITS>& r, int i, uint32_t (&v)[16]) {
+  constexpr int NG = StepRegs<GS, SYM, BITS>::kGroups;
   uint32_t za[NG], zb[NG], sg[NG], sh[NG];
 #pragma unroll
   for (int gg = 0; gg < NG; ++gg) {
-    const uint32_t zlo = SYM ? 8u : (r.z[i][gg] & 0xFu);
-    const uint32_t zhi = SYM ? 8u : (r.z[i][gg] >> 4);
-    za[gg] = zero_lo_const(zlo);
-    zb[gg] = zero_hi_const(zhi);
+    if (BITS == 4) {
+      const uint32_t zlo = SYM ? 8u : (r.z[i][gg] & 0xFu);
+      const uint32_t zhi = SYM ? 8u : (r.z[i][gg] >> 4);
+      za[gg] = zero_lo_const(zlo);
+      zb[gg] = zero_hi_const(zhi);
+    } else {
+      const uint32_t zg = SYM ? 128u : (r.z[i][gg] & 0xFFu);
+      const uint32_t zh = SYM ? 128u : (r.z[i][gg] >> 8);
+      za[gg] = (0x6400u + zg) * 0x00010001u;
+      zb[gg] = (0x6400u + zh) * 0x00010001u;
+    }
     sg[gg] = (r.s[i][gg] & 0xFFFFu) * 0x00010001u;
     sh[gg] = (r.s[i][gg] >> 16) * 0x00010001u;
   }
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
     const int gg = NG == 2 ? (j >> 1) : 0;
-    const uint32_t w = j == 0 ? r.w[i].x : j == 1 ? r.w[i].y : j == 2 ? r.w[i].z : r.w[i].w;
-    uint32_t a[4];
-    expand_word(w, za[gg], zb[gg], a);  // exact (q - z) in fp16
-    v[4 * j + 0] = hmul2_u32(a[0], sg[gg]);
-    v[4 * j + 1] = hmul2_u32(a[2], sg[gg]);
-    v[4 * j + 2] = hmul2_u32(a[1], sh[gg]);
-    v[4 * j + 3] = hmul2_u32(a[3], sh[gg]);
+    if (BITS == 4) {
+      const uint4& wv = r.w[i][0];
+      const uint32_t w = j == 0 ? wv.x : j == 1 ? wv.y : j == 2 ? wv.z : wv.w;
+      uint32_t a[4];
+      expand_word(w, za[gg], zb[gg], a);  // exact (q - z) in fp16
+      v[4 * j + 0] = hmul2_u32(a[0], sg[gg]);
+      v[4 * j + 1] = hmul2_u32(a[2], sg[gg]);
+      v[4 * j + 2] = hmul2_u32(a[1], sh[gg]);
+      v[4 * j + 3] = hmul2_u32(a[3], sh[gg]);
+    } else {
+      const uint4& wv = r.w[i][(BITS / 4 - 1) & (j >> 1)];
+      const uint32_t wg = (j & 1) ? wv.z : wv.x;  // row g, columns 4t .. 4t+3
+      const uint32_t wh = (j & 1) ? wv.w : wv.y;  // row g+8
+      v[4 * j + 0] = hmul2_u32(hsub2_u32(prmt_u32(wg, 0x64646464u, 0x5150u), za[gg]), sg[gg]);
+      v[4 * j + 1] = hmul2_u32(hsub2_u32(prmt_u32(wg, 0x64646464u, 0x5352u), za[gg]), sg[gg]);
+      v[4 * j + 2] = hmul2_u32(hsub2_u32(prmt_u32(wh, 0x64646464u, 0x5150u), zb[gg]), sh[gg]);
+      v[4 * j + 3] = hmul2_u32(hsub2_u32(prmt_u32(wh, 0x64646464u, 0x5352u), zb[gg]), sh[gg]);
+    }
   }
 }
 
-template <int WR, int NT, int SA, int SB, int DS, int GS, bool SYM>
-__global__ void __launch_bounds__(Cfg<WR, NT, SA, SB, DS>::kThreads, 1)
+template <int WR, int NT, int SA, int SB, int DS, int GS, bool SYM, int BITS>
+__global__ void __launch_bounds__(Cfg<WR, NT, SA, SB, DS, BITS>::kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const GemmArgs a) {
-  using C = Cfg<WR, NT, SA, SB, DS>;
+  using C = Cfg<WR, NT, SA, SB, DS, BITS>;
+  using WT = WTile<BITS>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_addr(smem_raw);
   uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);  // 1024-byte aligned for the swizzle
@@ -245,19 +291,24 @@ __global__ void __launch_bounds__(Cfg<WR, NT, SA, SB, DS>::kThreads, 1)
         break;
       }
       tc_fence_after();
-      const unsigned char* ws = smem + size_t(sb) * C::kStage + C::kBStage + at * kWTile;
+      const unsigned char* ws = smem + size_t(sb) * C::kStage + C::kBStage + at * WT::kBytes;
       const int ng = step_groups<GS>(kb_lo + kb, a.G);
-      StepRegs<GS, SYM> r;
+      StepRegs<GS, SYM, BITS> r;
       if (live) {
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           const int r16 = 2 * q4 + h;
-          r.w[h] = *reinterpret_cast<const uint4*>(ws + r16 * 512 + lane * 16);
 #pragma unroll
-          for (int gg = 0; gg < StepRegs<GS, SYM>::kGroups; ++gg) {
+          for (int part = 0; part < BITS / 4; ++part)
+            r.w[h][part] = *reinterpret_cast<const uint4*>(ws + r16 * WT::kR16 + part * 512 + lane * 16);
+#pragma unroll
+          for (int gg = 0; gg < StepRegs<GS, SYM, BITS>::kGroups; ++gg) {
             const int gs = min(gg, ng - 1);  // the padding half of a ragged last step reuses the last group
-            r.s[h][gg] = *reinterpret_cast<const uint32_t*>(ws + kWScaleOff + gs * 256 + (r16 * 8 + g) * 4);
-            r.z[h][gg] = SYM ? 0u : uint32_t(ws[kWZeroOff + gs * 64 + r16 * 8 + g]);
+            r.s[h][gg] = *reinterpret_cast<const uint32_t*>(ws + WT::kScaleOff + gs * 256 + (r16 * 8 + g) * 4);
+            r.z[h][gg] = SYM ? 0u
+                         : BITS == 4
+                             ? uint32_t(ws[WT::kZeroOff + gs * 64 + r16 * 8 + g])
+                             : uint32_t(*reinterpret_cast<const uint16_t*>(ws + WT::kZeroOff + gs * 128 + (r16 * 8 + g) * 2));
           }
         }
       }
@@ -266,7 +317,7 @@ __global__ void __launch_bounds__(Cfg<WR, NT, SA, SB, DS>::kThreads, 1)
       for (int h = 0; h < 2; ++h) {
         uint32_t v[16];
         if (live) {
-          dequant_tile<GS, SYM>(r, h, v);
+          dequant_tile<GS, SYM, BITS>(r, h, v);
         } else {
 #pragma unroll
           for (int e = 0; e < 16; ++e) v[e] = 0u;
@@ -343,7 +394,7 @@ __global__ void __launch_bounds__(Cfg<WR, NT, SA, SB, DS>::kThreads, 1)
         const int kbg = kb_lo + kb;  // global 64-column step
         const int g0 = kbg * 64 / GS;
         const int ng = step_groups<GS>(kbg, a.G);
-        const uint32_t wbytes = uint32_t(kWCodes + ng * 256 + (SYM ? 0 : ng * 64));
+        const uint32_t wbytes = uint32_t(WT::kCodes + ng * 256 + (SYM ? 0 : ng * WT::kZeroGroup));
         int live_tiles = 0;
 #pragma unroll
         for (int t = 0; t < WR; ++t) live_tiles += (rg * WR + t < a.NR) ? 1 : 0;
@@ -354,10 +405,12 @@ __global__ void __launch_bounds__(Cfg<WR, NT, SA, SB, DS>::kThreads, 1)
         for (int t = 0; t < WR; ++t) {
           const int R = rg * WR + t;
           if (R >= a.NR) continue;
-          const uint32_t wdst = stage + uint32_t(C::kBStage + t * kWTile);
-          bulk_copy_g2s(wdst, qbytes + (size_t(R) * a.KB + kbg) * kWCodes, kWCodes, full_b(s));
-          bulk_copy_g2s(wdst + kWScaleOff, sbytes + (size_t(R) * a.G + g0) * 256, uint32_t(ng * 256), full_b(s));
-          if (!SYM) bulk_copy_g2s(wdst + kWZeroOff, a.zeros + (size_t(R) * a.G + g0) * 64, uint32_t(ng * 64), full_b(s));
+          const uint32_t wdst = stage + uint32_t(C::kBStage + t * WT::kBytes);
+          bulk_copy_g2s(wdst, qbytes + (size_t(R) * a.KB + kbg) * WT::kCodes, WT::kCodes, full_b(s));
+          bulk_copy_g2s(wdst + WT::kScaleOff, sbytes + (size_t(R) * a.G + g0) * 256, uint32_t(ng * 256), full_b(s));
+          if (!SYM)
+            bulk_copy_g2s(wdst + WT::kZeroOff, a.zeros + (size_t(R) * a.G + g0) * WT::kZeroGroup,
+                          uint32_t(ng * WT::kZeroGroup), full_b(s));
         }
         ++issued;
       }
@@ -506,14 +559,14 @@ cudaError_t make_x_map(CUtensorMap* map, const uint16_t* x, int64_t M, int64_t K
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-template <int WR, int NT, int SA, int SB, int DS, int GS, bool SYM>
+template <int WR, int NT, int SA, int SB, int DS, int GS, bool SYM, int BITS>
 cudaError_t launch_cfg(const Layout& L, const GemmArgs& base, const uint16_t* xa, int64_t M, int ks,
                        bool after_gather, cudaStream_t stream) {
-  using C = Cfg<WR, NT, SA, SB, DS>;
+  using C = Cfg<WR, NT, SA, SB, DS, BITS>;
   CUtensorMap map;
   cudaError_t e = make_x_map(&map, xa, M, L.K, NT);
   if (e != cudaSuccess) return e;
-  auto kern = gemm_kernel<WR, NT, SA, SB, DS, GS, SYM>;
+  auto kern = gemm_kernel<WR, NT, SA, SB, DS, GS, SYM, BITS>;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, int(cudaSharedmemCarveoutMaxShared));
@@ -556,19 +609,33 @@ cudaError_t launch_cfg(const Layout& L, const GemmArgs& base, const uint16_t* xa
   return cudaGetLastError();
 }
 
-template <int WR, int NT, int SA, int SB, int DS>
+template <int WR, int NT, int SA, int SB, int DS, int BITS>
 cudaError_t launch_scheme(const Layout& L, const GemmArgs& a, const uint16_t* xa, int64_t M, int ks,
                           bool after_gather, cudaStream_t stream) {
+  constexpr int S = fit_sb(WR, NT, SA, SB, BITS);
   switch (L.gsize) {
     case 32:
-      return L.sym ? launch_cfg<WR, NT, SA, SB, DS, 32, true>(L, a, xa, M, ks, after_gather, stream)
-                   : launch_cfg<WR, NT, SA, SB, DS, 32, false>(L, a, xa, M, ks, after_gather, stream);
+      return L.sym ? launch_cfg<WR, NT, SA, S, DS, 32, true, BITS>(L, a, xa, M, ks, after_gather, stream)
+                   : launch_cfg<WR, NT, SA, S, DS, 32, false, BITS>(L, a, xa, M, ks, after_gather, stream);
     case 64:
-      return L.sym ? launch_cfg<WR, NT, SA, SB, DS, 64, true>(L, a, xa, M, ks, after_gather, stream)
-                   : launch_cfg<WR, NT, SA, SB, DS, 64, false>(L, a, xa, M, ks, after_gather, stream);
+      return L.sym ? launch_cfg<WR, NT, SA, S, DS, 64, true, BITS>(L, a, xa, M, ks, after_gather, stream)
+                   : launch_cfg<WR, NT, SA, S, DS, 64, false, BITS>(L, a, xa, M, ks, after_gather, stream);
     default:
-      return L.sym ? launch_cfg<WR, NT, SA, SB, DS, 128, true>(L, a, xa, M, ks, after_gather, stream)
-                   : launch_cfg<WR, NT, SA, SB, DS, 128, false>(L, a, xa, M, ks, after_gather, stream);
+      return L.sym ? launch_cfg<WR, NT, SA, S, DS, 128, true, BITS>(L, a, xa, M, ks, after_gather, stream)
+                   : launch_cfg<WR, NT, SA, S, DS, 128, false, BITS>(L, a, xa, M, ks, after_gather, stream);
+  }
+}
+
+template <int BITS>
+cudaError_t launch_tile(int tile, const Layout& L, const GemmArgs& a, const uint16_t* xa, int64_t M, int ks,
+                        bool g, cudaStream_t stream) {
+  switch (tile) {
+    case 1: return launch_scheme<1, 256, 8, 6, 2, BITS>(L, a, xa, M, ks, g, stream);
+    case 2: return launch_scheme<2, 128, 4, 8, 2, BITS>(L, a, xa, M, ks, g, stream);
+    case 4: return launch_scheme<1, 256, 8, 6, 1, BITS>(L, a, xa, M, ks, g, stream);
+    case 5: return launch_scheme<1, 128, 4, 5, 2, BITS>(L, a, xa, M, ks, g, stream);
+    case 6: return launch_scheme<1, 64, 4, 8, 2, BITS>(L, a, xa, M, ks, g, stream);
+    default: return launch_scheme<1, 256, 8, 6, 4, BITS>(L, a, xa, M, ks, g, stream);
   }
 }
 
@@ -636,14 +703,8 @@ cudaError_t launch_gemm(const Layout& L, const void* blob, const uint16_t* x, ui
   a.KB = int(L.KB);
   const bool g = L.act;
   const int ks = plan.ksplit;
-  switch (plan.tile) {
-    case 1: return launch_scheme<1, 256, 8, 6, 2>(L, a, xa, M, ks, g, stream);
-    case 2: return launch_scheme<2, 128, 4, 8, 2>(L, a, xa, M, ks, g, stream);
-    case 4: return launch_scheme<1, 256, 8, 6, 1>(L, a, xa, M, ks, g, stream);
-    case 5: return launch_scheme<1, 128, 4, 5, 2>(L, a, xa, M, ks, g, stream);
-    case 6: return launch_scheme<1, 64, 4, 8, 2>(L, a, xa, M, ks, g, stream);
-    default: return launch_scheme<1, 256, 8, 6, 4>(L, a, xa, M, ks, g, stream);
-  }
+  return L.bits == 8 ? launch_tile<8>(plan.tile, L, a, xa, M, ks, g, stream)
+                     : launch_tile<4>(plan.tile, L, a, xa, M, ks, g, stream);
 }
 
 cudaError_t take_pipeline_timeouts(unsigned int* count) {

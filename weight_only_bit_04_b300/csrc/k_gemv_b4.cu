@@ -1,0 +1,13 @@
+// The decode-sized product compiled for 4-bit codes.
+#include "gemv_impl.cuh"
+
+namespace w4a16 {
+
+cudaError_t launch_gemv_b4(const Layout& L, const void* blob, const uint16_t* x, uint16_t* y, int M,
+                           const GemvPlan& plan, uint32_t flags, cudaStream_t stream) {
+  return launch_gemv_bits<4>(L, blob, x, y, M, plan, flags, stream);
+}
+
+cudaError_t take_gemv_timeouts_b4(unsigned int* count) { return take_local_gemv_timeouts(count); }
+
+}  // namespace w4a16

@@ -1,13 +1,22 @@
-// Device layout of the packed W4A16 blob, shared by the host API and the kernels.
+// Device layout of the packed blob, shared by the host API and the kernels.
 //
 // The blob holds, each on a 256-byte boundary:
-//   qweight  [NR][KB] tiles of 4096 bytes (128 rows x 64 columns of 4-bit codes)
+//   qweight  [NR][KB] tiles of 128 rows x 64 columns of codes: 4096 bytes
+//            (4-bit) or 8192 bytes (8-bit)
 //   scales   [NR][G][8 r16][8 g][2] fp16: for 16-row tile r16 and lane group g
 //            the pair (row r16*16+g, row r16*16+g+8)
-//   zeros    [NR][G][8 r16][8 g] bytes: low nibble row r16*16+g, high nibble
-//            row r16*16+g+8 (asymmetric formats only)
+//   zeros    (asymmetric formats only) 4-bit: [NR][G][8 r16][8 g] bytes, low
+//            nibble row r16*16+g, high nibble row r16*16+g+8; 8-bit:
+//            [NR][G][8 r16][8 g][2] bytes, row r16*16+g then row r16*16+g+8
 //   perm     [K] int32: packed column -> original column (act order only)
 //
+// 8-bit codes: the 2048 words of a tile are ordered [r16 (8)][p (2)][lane (32)]
+// [jj (2)][h (2)]: lane L = 4*g + t loads its eight words as two 16-byte parts
+// p (each part of a warp is 512 contiguous bytes); word (r16, p, L, jj, h)
+// holds the codes of row r16*16 + g + 8h, columns 16*j + 4*t + {0, 1, 2, 3}
+// with j = 2p + jj (byte kk = column 4t + kk).
+//
+// 4-bit codes:
 // Inside a 4096-byte tile the 1024 32-bit words are ordered [r16 (8)][lane (32)][j (4)]:
 // lane L = 4*g + t of the warp owning 16-row tile r16 loads its four words (j = 0..3,
 // one per 16-column step) with one 16-byte load. Word (r16, L, j) holds the codes of
@@ -28,10 +37,13 @@ namespace w4a16 {
 
 constexpr int kRowsPerBlock = 128;
 constexpr int kColsPerBlock = 64;
-constexpr int kTileBytes = 4096;
+constexpr int kTileBytes = 4096;   // 4-bit codes; 8-bit tiles are twice as large
 constexpr int kTileWords = 1024;
 constexpr int kScaleBytesPerGroupBlock = 256;
-constexpr int kZeroBytesPerGroupBlock = 64;
+constexpr int kZeroBytesPerGroupBlock = 64;  // 4-bit; 8-bit zero points take twice as much
+
+__host__ __device__ constexpr int tile_bytes(int bits) { return kTileBytes * bits / 4; }
+__host__ __device__ constexpr int zero_bytes(int bits) { return kZeroBytesPerGroupBlock * bits / 4; }
 
 __host__ __device__ inline size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
 
@@ -40,6 +52,7 @@ __host__ __device__ inline int nibble_index(int kk, int h) { return (kk & 1) * 4
 struct Layout {
   int64_t N, K, NR, KB, G;
   int gsize;
+  int bits;  // 4 or 8
   bool sym, act;
   size_t q_off, q_bytes, s_off, s_bytes, z_off, z_bytes, p_off, p_bytes, total;
 };
@@ -49,17 +62,18 @@ inline Layout make_layout(const w4a16_format& f) {
   L.N = f.N;
   L.K = f.K;
   L.gsize = f.group_size;
+  L.bits = f.bits;
   L.sym = f.symmetric != 0;
   L.act = f.has_g_idx != 0;
   L.NR = (f.N + kRowsPerBlock - 1) / kRowsPerBlock;
   L.KB = (f.K + kColsPerBlock - 1) / kColsPerBlock;
   L.G = f.K / f.group_size;
   L.q_off = 0;
-  L.q_bytes = size_t(L.NR) * size_t(L.KB) * kTileBytes;
+  L.q_bytes = size_t(L.NR) * size_t(L.KB) * tile_bytes(f.bits);
   L.s_off = align256(L.q_off + L.q_bytes);
   L.s_bytes = size_t(L.NR) * size_t(L.G) * kScaleBytesPerGroupBlock;
   L.z_off = align256(L.s_off + L.s_bytes);
-  L.z_bytes = L.sym ? 0 : size_t(L.NR) * size_t(L.G) * kZeroBytesPerGroupBlock;
+  L.z_bytes = L.sym ? 0 : size_t(L.NR) * size_t(L.G) * zero_bytes(f.bits);
   L.p_off = align256(L.z_off + L.z_bytes);
   L.p_bytes = L.act ? size_t(L.K) * 4 : 0;
   L.total = align256(L.p_off + L.p_bytes);
