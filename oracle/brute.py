@@ -91,3 +91,14 @@ def pack_word(codes, bits=4):
     for i, c in enumerate(codes):
         w |= (c & ((1 << bits) - 1)) << (bits * i)
     return w
+
+
+def awq_linear(x, W, act_scale, group_size, sym, g_idx=None, bits=4):
+    """Unfolded AWQ, element by element: W'[n][k] = f16(W[n][k] * s[k]) is
+    quantized, x'[m][k] = f16(x[m][k] / s[k]); returns (y, q, s, z, x')."""
+    K = len(W[0])
+    Ws = [[f16(W[n][k] * act_scale[k]) for k in range(K)] for n in range(len(W))]
+    xs = [[f16(x[m][k] / act_scale[k]) for k in range(K)] for m in range(len(x))]
+    q, s, z = quantize(Ws, group_size, sym, g_idx, bits)
+    gi = g_idx if g_idx is not None else [k // group_size for k in range(K)]
+    return linear(xs, dequant(q, s, z, gi)), q, s, z, xs

@@ -40,6 +40,17 @@ What it computes, step by step, and where each step comes from:
    compactly"), with the per-element bound B = |x| . |w_hat|^T used by the
    acceptance test |y_gpu - y| <= 2e-3 * B + 1e-3.
 
+7. AWQ with the per-input-channel scale kept apart ("The two algorithms,
+   compactly": AWQ multiplies the weights of salient input channels by a
+   scale s > 1 before quantizing and divides the activations by the same
+   scale; folding 1/s into the preceding operation is the usual deployment).
+   Unfolded, the layer stores s (fp16 [K]) and computes
+   y = fp16(x / s) . dequant(quantize(fp16(W * s)))^T: both the product and
+   the quotient are exact in fp64 and rounded once to fp16. The scale search
+   of the same section (s = s_x ** alpha, s_x = mean |x| per channel, alpha
+   from a grid over [0, 1], keep the alpha with the smallest output error)
+   produces s from calibration activations.
+
 No blocking, fusion or reordering beyond these definitions; library matmuls
 (``@``) are used for the sums.
 """
@@ -296,3 +307,83 @@ def packed_bytes_closed_form(N: int, K: int, group_size: int, sym: bool, bits: i
 
 def bits_per_weight(group_size: int, sym: bool, bits: int = 4) -> float:
     return bits + 16 / group_size + (0 if sym else bits / group_size)
+
+
+# ---------------------------------------------------------------------------
+# Step 7: AWQ, per-input-channel scale kept apart from the weights
+# ---------------------------------------------------------------------------
+def _check_act_scale(act_scale, K: int) -> np.ndarray:
+    a = np.asarray(act_scale)
+    if a.dtype != np.float16 or a.shape != (K,):
+        raise TypeError("act_scale must be float16 [K]")
+    if not np.all(np.isfinite(a)) or np.any(a.astype(np.float64) <= 0):
+        raise ValueError("act_scale must be finite and positive")
+    return a.astype(np.float64)
+
+
+def awq_scale_weights(W, act_scale) -> np.ndarray:
+    """fp16(W[n, k] * s[k]): the salient channels' weights scaled up before
+    quantizing. The fp64 product of two fp16 values is exact."""
+    W = np.asarray(W)
+    if W.dtype != np.float16:
+        raise TypeError("W must be float16")
+    s = _check_act_scale(act_scale, W.shape[1])
+    return fp16_rne(W.astype(np.float64) * s[None, :])
+
+
+def awq_scale_activations(x, act_scale) -> np.ndarray:
+    """fp16(x[m, k] / s[k]): the activations divided by the same scale. The
+    fp64 quotient of two fp16 values is rounded once (fp64 carries more than
+    2 * 11 + 2 bits, so rounding through it equals rounding the exact
+    quotient)."""
+    x = np.asarray(x)
+    if x.dtype != np.float16:
+        raise TypeError("x must be float16")
+    s = _check_act_scale(act_scale, x.shape[1])
+    return fp16_rne(x.astype(np.float64) / s[None, :])
+
+
+def awq_linear(x, W, act_scale, group_size: int, sym: bool, g_idx=None, bits: int = 4):
+    """Unfolded AWQ layer: quantize fp16(W * s), divide x by s, multiply.
+
+    Returns (y, B, (q, scales, zeros), w_hat, x_scaled); B = |x_scaled| . |w_hat|^T.
+    """
+    Ws = awq_scale_weights(W, act_scale)
+    q, s, z = rtn_quantize(Ws, group_size, sym, g_idx, bits)
+    w_hat = dequant(q, s, z, group_size, g_idx)
+    xs = awq_scale_activations(x, act_scale)
+    y, B = linear_ref(xs, w_hat)
+    return y, B, (q, s, z), w_hat, xs
+
+
+def awq_grid(n_grid: int = 20) -> np.ndarray:
+    """alpha = 0, 1/n, ..., 1 (the section's grid over [0, 1], ends included)."""
+    return np.arange(n_grid + 1, dtype=np.float64) / n_grid
+
+
+def awq_search(W, x, group_size: int, sym: bool, bits: int = 4, n_grid: int = 20):
+    """AWQ's scale search for one linear layer, in the section's order.
+
+    x: calibration activations [tokens, K] (fp16). Per input channel
+    s_x = mean_t |x[t, k]|; for every alpha of the grid s = fp16(s_x ** alpha)
+    (a channel with s_x = 0 carries no activation and keeps s = 1);
+    Wq = dequant(quantize(fp16(W * s))) / s; loss = ||x W^T - x Wq^T||_F.
+    Returns (s of the smallest loss, its alpha, all losses); ties keep the
+    smaller alpha.
+    """
+    W = np.asarray(W)
+    xd = np.asarray(x, dtype=np.float64)
+    s_x = np.mean(np.abs(xd), axis=0)
+    y_ref = xd @ W.astype(np.float64).T
+    losses = []
+    best = None
+    for alpha in awq_grid(n_grid):
+        sc = np.where(s_x > 0, s_x ** alpha if alpha > 0 else 1.0, 1.0)
+        s16 = fp16_rne(sc)
+        q, s, z = rtn_quantize(awq_scale_weights(W, s16), group_size, sym, bits=bits)
+        Wq = dequant(q, s, z, group_size).astype(np.float64) / s16.astype(np.float64)[None, :]
+        loss = float(np.linalg.norm(y_ref - xd @ Wq.T))
+        losses.append(loss)
+        if best is None or loss < best[0]:
+            best = (loss, s16, float(alpha))
+    return best[1], best[2], np.array(losses)
