@@ -81,6 +81,17 @@ typedef enum {
  *                  pack time ("The two algorithms, compactly": act order
  *                  quantizes the columns with the largest activations first).
  *   N, K        1 <= N <= 2^20, group_size <= K <= 2^20.
+ *   has_act_scale 0: none;
+ *               1: unfolded AWQ -- the blob carries a per-input-channel
+ *                  scale s (fp16 [K], finite, > 0). The weights were
+ *                  quantized as fp16(W[n][k] * s[k]) and every product
+ *                  divides the activations by s as it loads them:
+ *                  y = fp16(x / s) . W_hat^T ("AWQ + GPTQ Quantization, in
+ *                  depth", section "The two algorithms, compactly": the
+ *                  salient channels' weights are multiplied by s before
+ *                  quantizing and the activations divided by it; here the
+ *                  division is not folded into the preceding operation).
+ *                  Pack with w4a16_pack_awq.
  */
 typedef struct {
   int32_t bits;
@@ -89,13 +100,14 @@ typedef struct {
   int32_t has_g_idx;
   int64_t N;
   int64_t K;
+  int32_t has_act_scale;
 } w4a16_format;
 
 /*
  * Packed blob (device memory, 256-byte aligned, produced by w4a16_pack).
  * With NR = ceil(N / 128) row blocks, KB = ceil(K / 64) column blocks and
- * G = K / group_size, it holds four sub-arrays, each starting on a 256-byte
- * boundary, in this order:
+ * G = K / group_size, it holds up to five sub-arrays, each starting on a
+ * 256-byte boundary, in this order:
  *   qweight  NR*KB*512*b bytes: for every (row block, column block) a tile
  *            of 128 rows x 64 columns of b-bit codes (4 or 8 KiB), arranged
  *            so that a warp's 16-byte loads yield tensor-core operand
@@ -103,6 +115,7 @@ typedef struct {
  *   scales   NR*G*256 bytes: fp16 scales, 128 rows per (row block, group).
  *   zeros    NR*G*16*b bytes (asymmetric only): b-bit zero points.
  *   perm     K*4 bytes (act order only): packed column -> original column.
+ *   act_scale K*2 bytes (has_act_scale only): fp16 s in packed column order.
  * Rows beyond N and columns beyond K are padding. The blob's meaning is fixed
  * by w4a16_dequant; its internal arrangement is private and may change.
  */
@@ -195,6 +208,27 @@ W4A16_API w4a16_status w4a16_pack(const w4a16_format* f, const uint8_t* q, const
                         size_t packed_bytes, w4a16_stream_t stream);
 
 /*
+ * Unfolded AWQ ("The two algorithms, compactly"): the round-to-nearest
+ * quantizer applied to fp16_rne(w[n][k] * act_scale[k]) (the fp32 product of
+ * two fp16 values is exact, it is rounded once), and the packer that also
+ * stores act_scale in the blob. Arguments as for w4a16_quantize_rtn and
+ * w4a16_pack, plus
+ *   act_scale  fp16 [K] in original column order, 2-byte aligned, every
+ *              value finite and > 0 (not checked on the device: a zero or
+ *              negative scale gives undefined outputs).
+ * f->has_act_scale must be 1. w4a16_pack and w4a16_quantize_rtn reject a
+ * format with has_act_scale = 1 (W4A16_ERR_INVALID_ARG), so a blob cannot
+ * lose its scale by accident.
+ */
+W4A16_API w4a16_status w4a16_quantize_rtn_awq(const w4a16_format* f, const uint16_t* w,
+                                const uint16_t* act_scale, const int32_t* g_idx, uint8_t* q,
+                                uint16_t* scales, uint8_t* zeros, void* workspace,
+                                size_t workspace_bytes, w4a16_stream_t stream);
+W4A16_API w4a16_status w4a16_pack_awq(const w4a16_format* f, const uint8_t* q, const uint16_t* scales,
+                        const uint8_t* zeros, const int32_t* g_idx, const uint16_t* act_scale,
+                        void* packed, size_t packed_bytes, w4a16_stream_t stream);
+
+/*
  * Expand the blob to fp16 weights: w_out[n][k] = fp16_rne((q - z) * s), in
  * the original column order; bit-exact ("The Math of Quantization":
  * x_approx = (q - Z) * S, rounded once to fp16).
@@ -212,9 +246,11 @@ W4A16_API w4a16_status w4a16_dequant(const w4a16_format* f, const void* packed, 
  *   x        fp16 [M][K] row-major, 16-byte aligned.
  *   y        fp16 [M][N] row-major, 16-byte aligned; must not overlap x.
  * Error per element is within 2e-3 * sum_k |x[m][k] * W_hat[n][k]| + 1e-3 of
- * the exact product with the dequantized weights. Under act order (or when K
- * is not a multiple of 64) a thread block gathers its slice of x into shared
- * memory, which bounds M * K / ksplit; a shape beyond that bound returns
+ * the exact product with the dequantized weights (with an act scale: x
+ * replaced by fp16_rne(x / s), rounded once, in both places). Under act
+ * order, with an act scale, or when K is not a multiple of 64 a thread block
+ * gathers its slice of x into shared memory (dividing by s there), which
+ * bounds M * K / ksplit; a shape beyond that bound returns
  * W4A16_ERR_UNSUPPORTED.
  */
 W4A16_API w4a16_status w4a16_gemv(const w4a16_format* f, const void* packed, size_t packed_bytes,
@@ -230,8 +266,9 @@ W4A16_API w4a16_status w4a16_gemv(const w4a16_format* f, const void* packed, siz
  * operand; the activations are streamed by TMA; fp32 accumulators live in
  * tensor memory. Same arguments and error bound as w4a16_gemv, plus
  *   workspace / workspace_bytes: >= w4a16_gemm_workspace_bytes(f, M)
- *            (the activations reordered to the packed column order when the
- *            format has act order: M*K*2 bytes; else 0, may be NULL),
+ *            (the activations reordered to the packed column order and
+ *            divided by the act scale, when the format has act order or an
+ *            act scale: M*K*2 bytes; else 0, may be NULL),
  *            16-byte aligned, overlapping neither x nor y.
  * 1 <= M <= 2^20. Needs a Blackwell GPU (compute capability 10.x); returns
  * W4A16_ERR_UNSUPPORTED on older devices.

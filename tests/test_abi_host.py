@@ -172,3 +172,38 @@ def test_dequant_checks(lib):
     assert lib.w4a16_dequant(ctypes.byref(f), FAKE, nb, None, None) == INVALID
     assert lib.w4a16_dequant(ctypes.byref(f), FAKE, nb, FAKE + 2, None) == MISALIGNED
     assert lib.w4a16_dequant(ctypes.byref(f), FAKE, 10, FAKE, None) == SMALL
+
+
+def test_act_scale_format_and_entry_points(lib):
+    """Unfolded AWQ: the blob grows by the fp16 act scale; the plain packer and
+    quantizer refuse such a format, the AWQ ones require it and its scale."""
+    f = W.make_format(256, 512, 128, False, False, act_scale=True)
+    plain = fmt()
+    assert W.check_format(f) == OK
+    assert W.packed_bytes(f) == W.packed_bytes(plain) + 512 * 2          # K fp16 (a multiple of 256 here)
+    assert W.packed_bytes(W.make_format(256, 96, 32, act_scale=True)) == \
+        W.packed_bytes(W.make_format(256, 96, 32)) + 256                   # rounded up to 256 bytes
+    bad = W.make_format(256, 512, act_scale=True)
+    bad.has_act_scale = 2
+    assert W.check_format(bad) == INVALID
+    nb = W.packed_bytes(f)
+    # plain packer: refuses (the scale would be lost); AWQ packer: needs the scale
+    assert lib.w4a16_pack(ctypes.byref(f), FAKE, FAKE, FAKE, None, FAKE, nb, None) == INVALID
+    assert lib.w4a16_pack_awq(ctypes.byref(f), FAKE, FAKE, FAKE, None, None, FAKE, nb, None) == INVALID
+    assert lib.w4a16_pack_awq(ctypes.byref(f), FAKE, FAKE, FAKE, None, FAKE + 1, FAKE, nb, None) == MISALIGNED
+    assert lib.w4a16_pack_awq(ctypes.byref(f), FAKE, FAKE, FAKE, None, FAKE, FAKE, nb - 1, None) == SMALL
+    assert lib.w4a16_pack_awq(ctypes.byref(plain), FAKE, FAKE, FAKE, None, FAKE, FAKE,
+                              W.packed_bytes(plain), None) == INVALID     # format without a scale
+    # quantizers
+    assert lib.w4a16_quantize_rtn(ctypes.byref(f), FAKE, None, FAKE, FAKE, FAKE, None, 0, None) == INVALID
+    assert lib.w4a16_quantize_rtn_noalloc(ctypes.byref(f), FAKE, None, FAKE, FAKE, FAKE, None) == INVALID
+    assert lib.w4a16_quantize_rtn_awq(ctypes.byref(f), FAKE, None, None, FAKE, FAKE, FAKE, None, 0,
+                                      None) == INVALID                    # scale missing
+    assert lib.w4a16_quantize_rtn_awq(ctypes.byref(f), FAKE, FAKE + 1, None, FAKE, FAKE, FAKE, None, 0,
+                                      None) == MISALIGNED
+    assert lib.w4a16_quantize_rtn_awq(ctypes.byref(plain), FAKE, FAKE, None, FAKE, FAKE, FAKE, None, 0,
+                                      None) == INVALID
+    # the GEMM stages x / s in the workspace even without act order
+    assert lib.w4a16_gemm_workspace_bytes(ctypes.byref(f), 100) == 100 * 512 * 2
+    X, Y = FAKE * 16, FAKE * 4096
+    assert lib.w4a16_gemm(ctypes.byref(f), FAKE, nb, X, Y, 100, None, 0, None) == SMALL

@@ -32,6 +32,7 @@ w4a16_status format_status(const w4a16_format* f) {
   if (f == nullptr) return W4A16_ERR_INVALID_ARG;
   if (f->symmetric != 0 && f->symmetric != 1) return W4A16_ERR_INVALID_ARG;
   if (f->has_g_idx != 0 && f->has_g_idx != 1) return W4A16_ERR_INVALID_ARG;
+  if (f->has_act_scale != 0 && f->has_act_scale != 1) return W4A16_ERR_INVALID_ARG;
   if (f->N < 1 || f->K < 1 || f->N > (int64_t(1) << 20) || f->K > (int64_t(1) << 20))
     return W4A16_ERR_INVALID_ARG;
   if (f->bits != 4 && f->bits != 8) return W4A16_ERR_UNSUPPORTED;
@@ -124,15 +125,16 @@ size_t w4a16_quantize_workspace_bytes(const w4a16_format* f) {
   return f->has_g_idx ? size_t(f->K) * 4 : 0;
 }
 
-w4a16_status w4a16_quantize_rtn(const w4a16_format* f, const uint16_t* w, const int32_t* g_idx,
-                                uint8_t* q, uint16_t* scales, uint8_t* zeros, void* workspace,
-                                size_t workspace_bytes, w4a16_stream_t stream) {
+static w4a16_status quantize_common(const w4a16_format* f, const uint16_t* w, const uint16_t* act_scale,
+                                    const int32_t* g_idx, uint8_t* q, uint16_t* scales, uint8_t* zeros,
+                                    void* workspace, size_t workspace_bytes, w4a16_stream_t stream) {
   w4a16_status s = format_status(f);
   if (s != W4A16_OK) return s;
   if (w == nullptr || q == nullptr || scales == nullptr) return W4A16_ERR_INVALID_ARG;
   if ((zeros == nullptr) != (f->symmetric != 0)) return W4A16_ERR_INVALID_ARG;
   if ((g_idx == nullptr) != (f->has_g_idx == 0)) return W4A16_ERR_INVALID_ARG;
-  if (!aligned(w, 16) || !aligned(scales, 2)) return W4A16_ERR_MISALIGNED;
+  if ((act_scale == nullptr) != (f->has_act_scale == 0)) return W4A16_ERR_INVALID_ARG;
+  if (!aligned(w, 16) || !aligned(scales, 2) || !aligned(act_scale, 2)) return W4A16_ERR_MISALIGNED;
   const size_t need = f->has_g_idx ? size_t(f->K) * 4 : 0;
   if (workspace_bytes < need) return W4A16_ERR_BUFFER_TOO_SMALL;
   if (need > 0 && workspace == nullptr) return W4A16_ERR_INVALID_ARG;
@@ -146,19 +148,33 @@ w4a16_status w4a16_quantize_rtn(const w4a16_format* f, const uint16_t* w, const 
     if (e != cudaSuccess) return cuda_fail(e);
     perm_dev = static_cast<const int32_t*>(workspace);
   }
-  cudaError_t e = launch_quantize_rtn(L, w, perm_dev, q, scales, zeros, stream);
+  cudaError_t e = launch_quantize_rtn(L, w, perm_dev, act_scale, q, scales, zeros, stream);
   return e == cudaSuccess ? W4A16_OK : cuda_fail(e);
 }
 
-w4a16_status w4a16_pack(const w4a16_format* f, const uint8_t* q, const uint16_t* scales,
-                        const uint8_t* zeros, const int32_t* g_idx, void* packed, size_t packed_bytes,
-                        w4a16_stream_t stream) {
+w4a16_status w4a16_quantize_rtn(const w4a16_format* f, const uint16_t* w, const int32_t* g_idx,
+                                uint8_t* q, uint16_t* scales, uint8_t* zeros, void* workspace,
+                                size_t workspace_bytes, w4a16_stream_t stream) {
+  return quantize_common(f, w, nullptr, g_idx, q, scales, zeros, workspace, workspace_bytes, stream);
+}
+
+w4a16_status w4a16_quantize_rtn_awq(const w4a16_format* f, const uint16_t* w, const uint16_t* act_scale,
+                                    const int32_t* g_idx, uint8_t* q, uint16_t* scales, uint8_t* zeros,
+                                    void* workspace, size_t workspace_bytes, w4a16_stream_t stream) {
+  if (f != nullptr && f->has_act_scale != 1) return W4A16_ERR_INVALID_ARG;
+  return quantize_common(f, w, act_scale, g_idx, q, scales, zeros, workspace, workspace_bytes, stream);
+}
+
+static w4a16_status pack_common(const w4a16_format* f, const uint8_t* q, const uint16_t* scales,
+                                const uint8_t* zeros, const int32_t* g_idx, const uint16_t* act_scale,
+                                void* packed, size_t packed_bytes, w4a16_stream_t stream) {
   w4a16_status s = format_status(f);
   if (s != W4A16_OK) return s;
   if (q == nullptr || scales == nullptr || packed == nullptr) return W4A16_ERR_INVALID_ARG;
   if ((zeros == nullptr) != (f->symmetric != 0)) return W4A16_ERR_INVALID_ARG;
   if ((g_idx == nullptr) != (f->has_g_idx == 0)) return W4A16_ERR_INVALID_ARG;
-  if (!aligned(packed, 256) || !aligned(scales, 2)) return W4A16_ERR_MISALIGNED;
+  if ((act_scale == nullptr) != (f->has_act_scale == 0)) return W4A16_ERR_INVALID_ARG;
+  if (!aligned(packed, 256) || !aligned(scales, 2) || !aligned(act_scale, 2)) return W4A16_ERR_MISALIGNED;
   const Layout L = make_layout(*f);
   if (packed_bytes < L.total) return W4A16_ERR_BUFFER_TOO_SMALL;
   if (f->has_g_idx) {
@@ -168,8 +184,21 @@ w4a16_status w4a16_pack(const w4a16_format* f, const uint8_t* q, const uint16_t*
                                     cudaMemcpyHostToDevice, stream);
     if (e != cudaSuccess) return cuda_fail(e);
   }
-  cudaError_t e = launch_pack(L, q, scales, zeros, packed, stream);
+  cudaError_t e = launch_pack(L, q, scales, zeros, act_scale, packed, stream);
   return e == cudaSuccess ? W4A16_OK : cuda_fail(e);
+}
+
+w4a16_status w4a16_pack(const w4a16_format* f, const uint8_t* q, const uint16_t* scales,
+                        const uint8_t* zeros, const int32_t* g_idx, void* packed, size_t packed_bytes,
+                        w4a16_stream_t stream) {
+  return pack_common(f, q, scales, zeros, g_idx, nullptr, packed, packed_bytes, stream);
+}
+
+w4a16_status w4a16_pack_awq(const w4a16_format* f, const uint8_t* q, const uint16_t* scales,
+                            const uint8_t* zeros, const int32_t* g_idx, const uint16_t* act_scale,
+                            void* packed, size_t packed_bytes, w4a16_stream_t stream) {
+  if (f != nullptr && f->has_act_scale != 1) return W4A16_ERR_INVALID_ARG;
+  return pack_common(f, q, scales, zeros, g_idx, act_scale, packed, packed_bytes, stream);
 }
 
 w4a16_status w4a16_dequant(const w4a16_format* f, const void* packed, size_t packed_bytes,
@@ -235,7 +264,7 @@ w4a16_status w4a16_gemv_ex(const w4a16_format* f, const void* packed, size_t pac
 
 size_t w4a16_gemm_workspace_bytes(const w4a16_format* f, int64_t M) {
   if (format_status(f) != W4A16_OK || M < 1) return 0;
-  return f->has_g_idx ? size_t(M) * size_t(f->K) * 2 : 0;
+  return (f->has_g_idx || f->has_act_scale) ? size_t(M) * size_t(f->K) * 2 : 0;
 }
 
 static w4a16_status gemm_common(const w4a16_format* f, const void* packed, size_t packed_bytes,

@@ -13,6 +13,14 @@ __device__ __forceinline__ uint32_t lop3_and_or(uint32_t a, uint32_t b, uint32_t
   return d;
 }
 
+// x / s for one fp16 activation and its act scale: the fp32 quotient of two
+// fp16 values, correctly rounded, rounds to the same fp16 as the exact
+// quotient (24 >= 2 * 11 + 2 bits, so the double rounding is innocuous).
+__device__ __forceinline__ uint16_t div_act(uint16_t xv, uint16_t sv) {
+  return __half_as_ushort(
+      __float2half_rn(__fdiv_rn(__half2float(__ushort_as_half(xv)), __half2float(__ushort_as_half(sv)))));
+}
+
 __device__ __forceinline__ uint32_t hsub2_u32(uint32_t a, uint32_t b) {
   uint32_t d;
   asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));

@@ -25,9 +25,10 @@
 //    Summation order differs from the dequantize-then-multiply definition;
 //    the error stays within the stated tolerance (products are exact, sums
 //    are fp32).
-//  * Under act order (and when K is not a multiple of 64) a thread block
-//    first gathers its columns of x into shared memory in packed order, with
-//    the padding columns zero.
+//  * Under act order, with an unfolded AWQ act scale, and when K is not a
+//    multiple of 64, a thread block first gathers its columns of x into
+//    shared memory in packed order (divided by the act scale), with the
+//    padding columns zero.
 //  * Warps sharing rows reduce through shared memory; thread blocks of a
 //    cluster that split K reduce through distributed shared memory in rank
 //    order (deterministic, no atomics).
@@ -68,6 +69,7 @@ struct GemvArgs {
   const uint32_t* scales2;  // scale pairs (row g, row g+8)
   const uint8_t* zeros;     // nullptr when symmetric
   const int32_t* perm;      // packed -> original column, or nullptr
+  const uint16_t* ascale;   // activation divisor per packed column (unfolded AWQ), or nullptr
   const uint16_t* x;
   uint16_t* y;
   int M, N, K, G, KB;
@@ -265,20 +267,23 @@ __device__ __forceinline__ void compute_unit(const UnitRegs<GS, BITS>& r, const 
 // stride `stride` halves), in packed order (through perm when given), with
 // zeros beyond K. Without perm the copy moves 16 bytes per thread and step.
 __device__ __forceinline__ void stage_activations(const uint16_t* __restrict__ x, const int32_t* __restrict__ perm,
-                                                  uint16_t* xs, int M, int K, int p0, int span, int stride,
-                                                  int tid, int nthreads) {
+                                                  const uint16_t* __restrict__ ascale, uint16_t* xs, int M, int K,
+                                                  int p0, int span, int stride, int tid, int nthreads) {
   if (perm == nullptr) {
     const int chunks = span / 8;  // span is a multiple of 64
     for (int e = tid; e < M * chunks; e += nthreads) {
       const int tok = e / chunks, c = (e - tok * chunks) * 8;
       const int p = p0 + c;
       uint4 v;
-      if (p + 8 <= K) {
+      if (p + 8 <= K && ascale == nullptr) {
         v = *reinterpret_cast<const uint4*>(x + size_t(tok) * K + p);
       } else {
         uint16_t h[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) h[i] = p + i < K ? x[size_t(tok) * K + p + i] : uint16_t(0);
+        for (int i = 0; i < 8; ++i) {
+          h[i] = p + i < K ? x[size_t(tok) * K + p + i] : uint16_t(0);
+          if (ascale != nullptr && p + i < K) h[i] = div_act(h[i], ascale[p + i]);
+        }
         v = make_uint4(h[0] | (uint32_t(h[1]) << 16), h[2] | (uint32_t(h[3]) << 16), h[4] | (uint32_t(h[5]) << 16),
                        h[6] | (uint32_t(h[7]) << 16));
       }
@@ -288,7 +293,9 @@ __device__ __forceinline__ void stage_activations(const uint16_t* __restrict__ x
     for (int e = tid; e < M * span; e += nthreads) {
       const int tok = e / span, c = e - tok * span;
       const int p = p0 + c;
-      xs[tok * stride + c] = p < K ? x[size_t(tok) * K + perm[p]] : uint16_t(0);
+      uint16_t v = p < K ? x[size_t(tok) * K + perm[p]] : uint16_t(0);
+      if (ascale != nullptr && p < K) v = div_act(v, ascale[p]);
+      xs[tok * stride + c] = v;
     }
   }
 }
@@ -309,6 +316,11 @@ struct WbSlot {
   static constexpr int kZeroOff = kScaleOff + kMetaFields * kThreads * 4;
   static constexpr int kBytes = kZeroOff + kMetaFields * kThreads * 4;
 };
+// Ring depth: 4 units of 4-bit codes, 2 of 8-bit codes -- the same bytes in
+// flight, and a ring small enough for three thread blocks per SM.
+template <int BITS>
+constexpr int kWbSlots = BITS == 8 ? 2 : 4;
+
 __host__ __device__ inline int wb_slot_bytes(int GS, int bits) {
   if (bits == 8) return GS == 128 ? WbSlot<128, 8>::kBytes : GS == 64 ? WbSlot<64, 8>::kBytes : WbSlot<32, 8>::kBytes;
   return GS == 128 ? WbSlot<128, 4>::kBytes : GS == 64 ? WbSlot<64, 4>::kBytes : WbSlot<32, 4>::kBytes;
@@ -365,7 +377,7 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const GemvArgs a) {
 
   // ---- asynchronous-copy ring: this thread's entries of every slot
   using SL = WbSlot<GS, BITS>;
-  constexpr int D = 4;  // units in flight per thread
+  constexpr int D = kWbSlots<BITS>;  // units in flight per thread
   const int tid = int(threadIdx.x);
   unsigned char* ringb = smem + a.wb_off;
   auto issue_unit = [&](int i) {  // unit u0 + i into slot i % D, one commit group
@@ -425,7 +437,7 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const GemvArgs a) {
     const int span = span_blk * kColsPerBlock;
     const int stride = span + 8;
     uint16_t* xs = reinterpret_cast<uint16_t*>(smem);
-    stage_activations(a.x, a.perm, xs, M, a.K, kb_lo * kColsPerBlock, span, stride, int(threadIdx.x), kThreads);
+    stage_activations(a.x, a.perm, a.ascale, xs, M, a.K, kb_lo * kColsPerBlock, span, stride, int(threadIdx.x), kThreads);
     __syncthreads();
     const int c0 = (u0 * U::kBlocks - kb_lo) * kColsPerBlock + 4 * t;
     xl0 = xs + tok0 * stride + c0;
@@ -622,16 +634,17 @@ RingSmem ring_smem(const Layout& L, int M, int kb_per_cta, bool staged, bool wb,
   }
   r.wb_off = int((base + 127) / 128 * 128);
   r.slot_bytes = wb_slot_bytes(L.gsize, L.bits);
-  r.total = size_t(r.wb_off) + size_t(4) * r.slot_bytes;  // 4 slots
+  r.total = size_t(r.wb_off) + size_t(L.bits == 8 ? kWbSlots<8> : kWbSlots<4>) * r.slot_bytes;
   (void)depth;
   return r;
 }
 
 constexpr size_t kMaxGemvSmem = 200 * 1024;
 
-// Activations go through shared memory under act order, or when the last
-// 64-column block is ragged (its padding columns must read as zero).
-bool gemv_staged(const Layout& L) { return L.act || (L.K % kColsPerBlock) != 0; }
+// Activations go through shared memory under act order, with an act scale
+// (divided on the way), or when the last 64-column block is ragged (its
+// padding columns must read as zero).
+bool gemv_staged(const Layout& L) { return L.act || L.awq || (L.K % kColsPerBlock) != 0; }
 
 // 64-column blocks per thread block of a K split: whole groups.
 int kb_per_cta_of(const Layout& L, int ksplit) {
@@ -653,6 +666,7 @@ cudaError_t launch_gemv_bits(const Layout& L, const void* blob, const uint16_t* 
   a.scales2 = reinterpret_cast<const uint32_t*>(B.scales);
   a.zeros = B.zeros;
   a.perm = B.perm;
+  a.ascale = B.ascale;
   a.x = x;
   a.y = y;
   a.M = M;

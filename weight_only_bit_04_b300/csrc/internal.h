@@ -19,12 +19,15 @@ cudaError_t device_info(DeviceInfo* out);
 // Record e for w4a16_last_cuda_error() (calling thread) and return W4A16_ERR_CUDA.
 w4a16_status cuda_error_status(cudaError_t e);
 
+// ascale: per-input-channel scale (original column order) applied to the
+// weights before quantizing, or nullptr.
 cudaError_t launch_quantize_rtn(const Layout& L, const uint16_t* w, const int32_t* perm_dev,
-                                uint8_t* q, uint16_t* scales, uint8_t* zeros,
+                                const uint16_t* ascale, uint8_t* q, uint16_t* scales, uint8_t* zeros,
                                 cudaStream_t stream);
 
+// ascale: the act scale to store (original column order) when L.awq.
 cudaError_t launch_pack(const Layout& L, const uint8_t* q, const uint16_t* scales,
-                        const uint8_t* zeros, void* blob, cudaStream_t stream);
+                        const uint8_t* zeros, const uint16_t* ascale, void* blob, cudaStream_t stream);
 
 cudaError_t launch_dequant(const Layout& L, const void* blob, uint16_t* w_out,
                            cudaStream_t stream);

@@ -20,8 +20,11 @@ namespace {
 // ---------------------------------------------------------------------------
 // Round-to-nearest quantization: one warp per (row, group).
 // ---------------------------------------------------------------------------
+// With an act scale (unfolded AWQ) the group's members are fp16(w * s[col]):
+// the fp32 product of two fp16 values is exact and is rounded once.
 __global__ void __launch_bounds__(256) quantize_rtn_kernel(Layout L, const uint16_t* __restrict__ w,
                                                            const int32_t* __restrict__ perm,
+                                                           const uint16_t* __restrict__ ascale,
                                                            uint8_t* __restrict__ q,
                                                            uint16_t* __restrict__ scales,
                                                            uint8_t* __restrict__ zeros) {
@@ -42,6 +45,7 @@ __global__ void __launch_bounds__(256) quantize_rtn_kernel(Layout L, const uint1
       const int64_t p = t * gs + i * 32 + lane;  // position in group-sorted order
       col[i] = perm ? perm[p] : p;
       v[i] = __half2float(__ushort_as_half(w[n * L.K + col[i]]));
+      if (ascale) v[i] = __half2float(__float2half_rn(v[i] * __half2float(__ushort_as_half(ascale[col[i]]))));
       mn = fminf(mn, v[i]);
       mx = fmaxf(mx, v[i]);
       amax = fmaxf(amax, fabsf(v[i]));
@@ -171,6 +175,15 @@ __global__ void __launch_bounds__(256) pack_meta_kernel(Layout L, const uint16_t
   }
 }
 
+// The act scale in packed column order: out[p] = ascale[perm[p]].
+__global__ void __launch_bounds__(256) pack_act_scale_kernel(Layout L, const uint16_t* __restrict__ ascale,
+                                                             const int32_t* __restrict__ perm,
+                                                             uint16_t* __restrict__ out) {
+  const int64_t p = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (p >= L.K) return;
+  out[p] = ascale[perm ? perm[p] : p];
+}
+
 // ---------------------------------------------------------------------------
 // Dequantization: one thread per packed word, w_hat = fp16_rne((q - z) * s).
 // (1024 + q) - (1024 + z) is exact in fp16, the product is rounded once.
@@ -228,14 +241,15 @@ inline unsigned blocks_for(int64_t threads, int per_block) {
 }  // namespace
 
 cudaError_t launch_quantize_rtn(const Layout& L, const uint16_t* w, const int32_t* perm_dev,
-                                uint8_t* q, uint16_t* scales, uint8_t* zeros, cudaStream_t stream) {
+                                const uint16_t* ascale, uint8_t* q, uint16_t* scales, uint8_t* zeros,
+                                cudaStream_t stream) {
   const int64_t threads = L.N * L.G * 32;
-  quantize_rtn_kernel<<<blocks_for(threads, 256), 256, 0, stream>>>(L, w, perm_dev, q, scales, zeros);
+  quantize_rtn_kernel<<<blocks_for(threads, 256), 256, 0, stream>>>(L, w, perm_dev, ascale, q, scales, zeros);
   return cudaGetLastError();
 }
 
 cudaError_t launch_pack(const Layout& L, const uint8_t* q, const uint16_t* scales,
-                        const uint8_t* zeros, void* blob, cudaStream_t stream) {
+                        const uint8_t* zeros, const uint16_t* ascale, void* blob, cudaStream_t stream) {
   char* b = static_cast<char*>(blob);
   const int32_t* perm = L.act ? reinterpret_cast<const int32_t*>(b + L.p_off) : nullptr;
   const int64_t words = L.NR * L.KB * kTileWords * L.bits / 4;
@@ -247,6 +261,10 @@ cudaError_t launch_pack(const Layout& L, const uint8_t* q, const uint16_t* scale
   pack_meta_kernel<<<blocks_for(metas, 256), 256, 0, stream>>>(
       L, scales, L.sym ? nullptr : zeros, reinterpret_cast<uint32_t*>(b + L.s_off),
       L.sym ? nullptr : reinterpret_cast<uint8_t*>(b + L.z_off));
+  e = cudaGetLastError();
+  if (e != cudaSuccess || !L.awq) return e;
+  pack_act_scale_kernel<<<blocks_for(L.K, 256), 256, 0, stream>>>(L, ascale, perm,
+                                                                  reinterpret_cast<uint16_t*>(b + L.a_off));
   return cudaGetLastError();
 }
 

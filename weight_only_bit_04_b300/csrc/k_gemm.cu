@@ -23,6 +23,8 @@
 //    16-byte stores.
 //  * Under act order the packed columns are in group order; a gather kernel
 //    first writes x with its columns in that order to the caller's workspace.
+//    With an unfolded AWQ act scale the same kernel divides x by it on the
+//    way (and runs without act order too).
 //  * Every wait is bounded in time: a wait that gives up raises the device's
 //    pipeline-timeout count (w4a16_pipeline_timeouts), the block drains what
 //    it has in flight and returns without writing y.
@@ -473,12 +475,14 @@ __global__ void __launch_bounds__(Cfg<WR, NT, SA, SB, DS, BITS>::kThreads, 1)
   }
 }
 
-// x_perm[m][p] = x[m][perm[p]]: activations in the packed (group-sorted)
-// column order. One thread block per token row: the row is staged in shared
-// memory with 16-byte loads, then written back permuted with 16-byte stores.
+// x_perm[m][p] = x[m][perm[p]] / ascale[p]: activations in the packed
+// (group-sorted) column order, divided by the act scale when there is one.
+// One thread block per token row: the row is staged in shared memory with
+// 16-byte loads, then written back permuted with 16-byte stores.
 constexpr int kGatherThreads = 256;
 __global__ void __launch_bounds__(kGatherThreads) gather_cols_kernel(const uint16_t* __restrict__ x,
                                                                      const int32_t* __restrict__ perm,
+                                                                     const uint16_t* __restrict__ ascale,
                                                                      uint16_t* __restrict__ xp, int K) {
   extern __shared__ __align__(16) uint16_t row_s[];
   pdl_launch_dependents();
@@ -491,18 +495,28 @@ __global__ void __launch_bounds__(kGatherThreads) gather_cols_kernel(const uint1
   const int4* pv = reinterpret_cast<const int4*>(perm);
   for (int c = threadIdx.x; c < chunks; c += kGatherThreads) {
     const int4 p0 = pv[2 * c], p1 = pv[2 * c + 1];
+    uint16_t h[8] = {row_s[p0.x], row_s[p0.y], row_s[p0.z], row_s[p0.w],
+                     row_s[p1.x], row_s[p1.y], row_s[p1.z], row_s[p1.w]};
+    if (ascale != nullptr) {
+      const uint4 sv = reinterpret_cast<const uint4*>(ascale)[c];
+      const uint32_t sw[4] = {sv.x, sv.y, sv.z, sv.w};
+#pragma unroll
+      for (int i = 0; i < 8; ++i) h[i] = div_act(h[i], uint16_t(sw[i >> 1] >> (16 * (i & 1))));
+    }
     uint4 o;
-    o.x = uint32_t(row_s[p0.x]) | (uint32_t(row_s[p0.y]) << 16);
-    o.y = uint32_t(row_s[p0.z]) | (uint32_t(row_s[p0.w]) << 16);
-    o.z = uint32_t(row_s[p1.x]) | (uint32_t(row_s[p1.y]) << 16);
-    o.w = uint32_t(row_s[p1.z]) | (uint32_t(row_s[p1.w]) << 16);
+    o.x = uint32_t(h[0]) | (uint32_t(h[1]) << 16);
+    o.y = uint32_t(h[2]) | (uint32_t(h[3]) << 16);
+    o.z = uint32_t(h[4]) | (uint32_t(h[5]) << 16);
+    o.w = uint32_t(h[6]) | (uint32_t(h[7]) << 16);
     dst[c] = o;
   }
 }
 
-// The same gather for rows too long to stage in shared memory.
+// The same for rows too long to stage in shared memory, and for the act
+// scale alone (perm == nullptr: contiguous 16-byte loads).
 __global__ void __launch_bounds__(256) gather_cols_global_kernel(const uint16_t* __restrict__ x,
                                                                  const int32_t* __restrict__ perm,
+                                                                 const uint16_t* __restrict__ ascale,
                                                                  uint16_t* __restrict__ xp, int64_t M, int K) {
   pdl_launch_dependents();
   const int64_t chunks = int64_t(K) / 8;
@@ -511,11 +525,25 @@ __global__ void __launch_bounds__(256) gather_cols_global_kernel(const uint16_t*
   const int64_t m = i / chunks;
   const int p0 = int(i - m * chunks) * 8;
   const uint16_t* row = x + m * K;
-  uint32_t w[4];
+  uint16_t h[8];
+  if (perm == nullptr) {
+    const uint4 v = *reinterpret_cast<const uint4*>(row + p0);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-  for (int j = 0; j < 4; ++j)
-    w[j] = uint32_t(row[perm[p0 + 2 * j]]) | (uint32_t(row[perm[p0 + 2 * j + 1]]) << 16);
-  *reinterpret_cast<uint4*>(xp + m * K + p0) = make_uint4(w[0], w[1], w[2], w[3]);
+    for (int j = 0; j < 8; ++j) h[j] = uint16_t(w[j >> 1] >> (16 * (j & 1)));
+  } else {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) h[j] = row[perm[p0 + j]];
+  }
+  if (ascale != nullptr) {
+    const uint4 sv = *reinterpret_cast<const uint4*>(ascale + p0);
+    const uint32_t sw[4] = {sv.x, sv.y, sv.z, sv.w};
+#pragma unroll
+    for (int j = 0; j < 8; ++j) h[j] = div_act(h[j], uint16_t(sw[j >> 1] >> (16 * (j & 1))));
+  }
+  *reinterpret_cast<uint4*>(xp + m * K + p0) =
+      make_uint4(uint32_t(h[0]) | (uint32_t(h[1]) << 16), uint32_t(h[2]) | (uint32_t(h[3]) << 16),
+                 uint32_t(h[4]) | (uint32_t(h[5]) << 16), uint32_t(h[6]) | (uint32_t(h[7]) << 16));
 }
 constexpr size_t kGatherMaxSmem = 160 * 1024;
 
@@ -674,18 +702,19 @@ cudaError_t launch_gemm(const Layout& L, const void* blob, const uint16_t* x, ui
                         void* workspace, const GemmPlan& plan, cudaStream_t stream) {
   const BlobView B = view_of(L, blob);
   const uint16_t* xa = x;
-  if (L.act) {
+  if (L.act || L.awq) {
     uint16_t* xp = static_cast<uint16_t*>(workspace);
     const size_t smem = size_t(L.K) * 2;
     cudaError_t e = cudaSuccess;
-    if (smem <= kGatherMaxSmem && M <= 0x7FFFFFFF) {
+    if (L.act && smem <= kGatherMaxSmem && M <= 0x7FFFFFFF) {
       if (smem > 48 * 1024)
         e = cudaFuncSetAttribute(gather_cols_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
       if (e != cudaSuccess) return e;
-      gather_cols_kernel<<<unsigned(M), kGatherThreads, smem, stream>>>(x, B.perm, xp, int(L.K));
+      gather_cols_kernel<<<unsigned(M), kGatherThreads, smem, stream>>>(x, B.perm, B.ascale, xp, int(L.K));
     } else {
       const int64_t chunks = M * (L.K / 8);
-      gather_cols_global_kernel<<<unsigned((chunks + 255) / 256), 256, 0, stream>>>(x, B.perm, xp, M, int(L.K));
+      gather_cols_global_kernel<<<unsigned((chunks + 255) / 256), 256, 0, stream>>>(x, B.perm, B.ascale, xp, M,
+                                                                                  int(L.K));
     }
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
@@ -701,7 +730,7 @@ cudaError_t launch_gemm(const Layout& L, const void* blob, const uint16_t* x, ui
   a.NR = int(L.NR);
   a.G = int(L.G);
   a.KB = int(L.KB);
-  const bool g = L.act;
+  const bool g = L.act || L.awq;
   const int ks = plan.ksplit;
   return L.bits == 8 ? launch_tile<8>(plan.tile, L, a, xa, M, ks, g, stream)
                      : launch_tile<4>(plan.tile, L, a, xa, M, ks, g, stream);

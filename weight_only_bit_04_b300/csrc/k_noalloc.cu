@@ -68,6 +68,7 @@ w4a16_status w4a16_quantize_rtn_noalloc(const w4a16_format* f, const uint16_t* w
   if (w == nullptr || q == nullptr || scales == nullptr) return W4A16_ERR_INVALID_ARG;
   if ((zeros == nullptr) != (f->symmetric != 0)) return W4A16_ERR_INVALID_ARG;
   if ((g_idx == nullptr) != (f->has_g_idx == 0)) return W4A16_ERR_INVALID_ARG;
+  if (f->has_act_scale) return W4A16_ERR_INVALID_ARG;  // the AWQ quantizer takes the scale
   if ((reinterpret_cast<uintptr_t>(w) & 15) != 0 || (reinterpret_cast<uintptr_t>(scales) & 1) != 0)
     return W4A16_ERR_MISALIGNED;
   if (f->has_g_idx && f->K > kNoAllocMaxK) return W4A16_ERR_BUFFER_TOO_SMALL;  // beyond the fixed scratch
@@ -96,7 +97,7 @@ w4a16_status w4a16_quantize_rtn_noalloc(const w4a16_format* f, const uint16_t* w
     if (e != cudaSuccess) return cuda_error_status(e);
     perm_dev = scratch;
   }
-  cudaError_t e = launch_quantize_rtn(L, w, perm_dev, q, scales, zeros, stream);
+  cudaError_t e = launch_quantize_rtn(L, w, perm_dev, nullptr, q, scales, zeros, stream);
   return e == cudaSuccess ? W4A16_OK : cuda_error_status(e);
 }
 

@@ -9,6 +9,8 @@
 //            nibble row r16*16+g, high nibble row r16*16+g+8; 8-bit:
 //            [NR][G][8 r16][8 g][2] bytes, row r16*16+g then row r16*16+g+8
 //   perm     [K] int32: packed column -> original column (act order only)
+//   ascale   [K] fp16: per-input-channel activation divisor (unfolded AWQ
+//            only), in packed column order
 //
 // 8-bit codes: the 2048 words of a tile are ordered [r16 (8)][p (2)][lane (32)]
 // [jj (2)][h (2)]: lane L = 4*g + t loads its eight words as two 16-byte parts
@@ -53,8 +55,8 @@ struct Layout {
   int64_t N, K, NR, KB, G;
   int gsize;
   int bits;  // 4 or 8
-  bool sym, act;
-  size_t q_off, q_bytes, s_off, s_bytes, z_off, z_bytes, p_off, p_bytes, total;
+  bool sym, act, awq;
+  size_t q_off, q_bytes, s_off, s_bytes, z_off, z_bytes, p_off, p_bytes, a_off, a_bytes, total;
 };
 
 inline Layout make_layout(const w4a16_format& f) {
@@ -65,6 +67,7 @@ inline Layout make_layout(const w4a16_format& f) {
   L.bits = f.bits;
   L.sym = f.symmetric != 0;
   L.act = f.has_g_idx != 0;
+  L.awq = f.has_act_scale != 0;
   L.NR = (f.N + kRowsPerBlock - 1) / kRowsPerBlock;
   L.KB = (f.K + kColsPerBlock - 1) / kColsPerBlock;
   L.G = f.K / f.group_size;
@@ -76,7 +79,9 @@ inline Layout make_layout(const w4a16_format& f) {
   L.z_bytes = L.sym ? 0 : size_t(L.NR) * size_t(L.G) * zero_bytes(f.bits);
   L.p_off = align256(L.z_off + L.z_bytes);
   L.p_bytes = L.act ? size_t(L.K) * 4 : 0;
-  L.total = align256(L.p_off + L.p_bytes);
+  L.a_off = align256(L.p_off + L.p_bytes);
+  L.a_bytes = L.awq ? size_t(L.K) * 2 : 0;
+  L.total = align256(L.a_off + L.a_bytes);
   return L;
 }
 
@@ -86,6 +91,7 @@ struct BlobView {
   const uint16_t* scales;   // fp16 bits
   const uint8_t* zeros;     // nullptr when symmetric
   const int32_t* perm;      // nullptr without act order
+  const uint16_t* ascale;   // fp16 bits, packed order; nullptr without an act scale
 };
 
 inline BlobView view_of(const Layout& L, const void* blob) {
@@ -95,6 +101,7 @@ inline BlobView view_of(const Layout& L, const void* blob) {
   v.scales = reinterpret_cast<const uint16_t*>(b + L.s_off);
   v.zeros = L.sym ? nullptr : reinterpret_cast<const uint8_t*>(b + L.z_off);
   v.perm = L.act ? reinterpret_cast<const int32_t*>(b + L.p_off) : nullptr;
+  v.ascale = L.awq ? reinterpret_cast<const uint16_t*>(b + L.a_off) : nullptr;
   return v;
 }
 

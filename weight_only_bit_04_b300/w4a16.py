@@ -45,11 +45,12 @@ class Format(ctypes.Structure):
         ("has_g_idx", ctypes.c_int32),
         ("N", ctypes.c_int64),
         ("K", ctypes.c_int64),
+        ("has_act_scale", ctypes.c_int32),
     ]
 
     def __repr__(self):
         return (f"Format(bits={self.bits}, group_size={self.group_size}, symmetric={self.symmetric}, "
-                f"has_g_idx={self.has_g_idx}, N={self.N}, K={self.K})")
+                f"has_g_idx={self.has_g_idx}, N={self.N}, K={self.K}, has_act_scale={self.has_act_scale})")
 
     @property
     def G(self) -> int:
@@ -67,6 +68,8 @@ SIGNATURES = {
     "w4a16_quantize_rtn": (ctypes.c_int, [_FP, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "w4a16_quantize_rtn_noalloc": (ctypes.c_int, [_FP, _P, _P, _P, _P, _P, _P]),
     "w4a16_pack": (ctypes.c_int, [_FP, _P, _P, _P, _P, _P, _SZ, _P]),
+    "w4a16_quantize_rtn_awq": (ctypes.c_int, [_FP, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
+    "w4a16_pack_awq": (ctypes.c_int, [_FP, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "w4a16_dequant": (ctypes.c_int, [_FP, _P, _SZ, _P, _P]),
     "w4a16_gemv": (ctypes.c_int, [_FP, _P, _SZ, _P, _P, _I64, _P]),
     "w4a16_gemv_ex": (ctypes.c_int, [_FP, _P, _SZ, _P, _P, _I64, _I32, _I32, ctypes.c_uint32, _P]),
@@ -114,8 +117,9 @@ def _check(fn: str, status: int) -> None:
 
 
 def make_format(N: int, K: int, group_size: int = 128, symmetric: bool = False,
-                has_g_idx: bool = False, bits: int = 4) -> Format:
-    return Format(bits, group_size, int(bool(symmetric)), int(bool(has_g_idx)), N, K)
+                has_g_idx: bool = False, bits: int = 4, act_scale: bool = False) -> Format:
+    """``act_scale``: the layer carries an unfolded AWQ per-input-channel scale."""
+    return Format(bits, group_size, int(bool(symmetric)), int(bool(has_g_idx)), N, K, int(bool(act_scale)))
 
 
 def packed_bytes(fmt: Format) -> int:
@@ -157,29 +161,43 @@ def _host_gidx(g_idx, K: int):
     return arr, arr.data_ptr()
 
 
-def quantize_rtn(fmt: Format, w: torch.Tensor, g_idx=None, stream=None):
-    """Round-to-nearest group quantization on the GPU -> (q uint8, scales fp16, zeros uint8|None)."""
+def quantize_rtn(fmt: Format, w: torch.Tensor, g_idx=None, act_scale=None, stream=None):
+    """Round-to-nearest group quantization on the GPU -> (q uint8, scales fp16, zeros uint8|None).
+
+    With ``fmt.has_act_scale`` pass ``act_scale`` (fp16 [K]): the quantized
+    weights are fp16(w * act_scale) (unfolded AWQ).
+    """
     N, K, G = fmt.N, fmt.K, fmt.G
     dev = w.device
     wp = _dev(w, torch.float16, "w", (N, K))
+    ap = None if act_scale is None else _dev(act_scale, torch.float16, "act_scale", (K,))
     q = torch.empty((N, K), dtype=torch.uint8, device=dev)
     scales = torch.empty((N, G), dtype=torch.float16, device=dev)
     zeros = None if fmt.symmetric else torch.empty((N, G), dtype=torch.uint8, device=dev)
     ws_bytes = int(lib().w4a16_quantize_workspace_bytes(ctypes.byref(fmt)))
     ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
     gi, gip = _host_gidx(g_idx, K)
-    st = lib().w4a16_quantize_rtn(ctypes.byref(fmt), wp, gip, q.data_ptr(), scales.data_ptr(),
-                                  None if zeros is None else zeros.data_ptr(),
-                                  ws.data_ptr() if ws_bytes else None, ws_bytes, _stream(stream))
-    _check("w4a16_quantize_rtn", st)
+    zp = None if zeros is None else zeros.data_ptr()
+    wsp = ws.data_ptr() if ws_bytes else None
+    if fmt.has_act_scale:
+        st = lib().w4a16_quantize_rtn_awq(ctypes.byref(fmt), wp, ap, gip, q.data_ptr(), scales.data_ptr(), zp,
+                                          wsp, ws_bytes, _stream(stream))
+        _check("w4a16_quantize_rtn_awq", st)
+    else:
+        if ap is not None:
+            raise ValueError("act_scale given but the format has no act scale")
+        st = lib().w4a16_quantize_rtn(ctypes.byref(fmt), wp, gip, q.data_ptr(), scales.data_ptr(), zp,
+                                      wsp, ws_bytes, _stream(stream))
+        _check("w4a16_quantize_rtn", st)
     if ws_bytes and isinstance(stream, torch.cuda.Stream):
         ws.record_stream(stream)
     return q, scales, zeros
 
 
 def pack(fmt: Format, q: torch.Tensor, scales: torch.Tensor, zeros=None, g_idx=None,
-         out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
-    """Pack canonical codes/scales/zeros into a new (or given) device blob."""
+         out: torch.Tensor | None = None, stream=None, act_scale=None) -> torch.Tensor:
+    """Pack canonical codes/scales/zeros (and the act scale, fp16 [K], when
+    ``fmt.has_act_scale``) into a new (or given) device blob."""
     N, K, G = fmt.N, fmt.K, fmt.G
     nbytes = packed_bytes(fmt)
     if nbytes == 0:
@@ -187,12 +205,19 @@ def pack(fmt: Format, q: torch.Tensor, scales: torch.Tensor, zeros=None, g_idx=N
     qp = _dev(q, torch.uint8, "q", (N, K))
     sp = _dev(scales, torch.float16, "scales", (N, G))
     zp = None if zeros is None else _dev(zeros, torch.uint8, "zeros", (N, G))
+    ap = None if act_scale is None else _dev(act_scale, torch.float16, "act_scale", (K,))
     if out is None:
         out = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
     op = _dev(out, torch.uint8, "out")
     gi, gip = _host_gidx(g_idx, K)
-    st = lib().w4a16_pack(ctypes.byref(fmt), qp, sp, zp, gip, op, out.numel(), _stream(stream))
-    _check("w4a16_pack", st)
+    if fmt.has_act_scale:
+        st = lib().w4a16_pack_awq(ctypes.byref(fmt), qp, sp, zp, gip, ap, op, out.numel(), _stream(stream))
+        _check("w4a16_pack_awq", st)
+    else:
+        if ap is not None:
+            raise ValueError("act_scale given but the format has no act scale")
+        st = lib().w4a16_pack(ctypes.byref(fmt), qp, sp, zp, gip, op, out.numel(), _stream(stream))
+        _check("w4a16_pack", st)
     return out
 
 
