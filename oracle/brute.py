@@ -30,8 +30,9 @@ def _clamp(v: int, lo: int, hi: int) -> int:
 def quantize(W, group_size, sym, g_idx=None, bits=4):
     """W: list of rows of Python floats (fp16 values). Returns q, s, z lists.
 
-    b-bit codes, top = 2^b - 1. Symmetric: 4 bits s = f16(2a/15), z = 8;
-    8 bits (the int8 absmax code) s = f16(a/127), q = clamp(round(w/s), -127, 127) + 128.
+    b-bit codes, top = 2^b - 1. Symmetric: 3 and 4 bits s = f16(2a/top),
+    z = 2^(b-1); 8 bits (the int8 absmax code) s = f16(a/127),
+    q = clamp(round(w/s), -127, 127) + 128.
     """
     top = (1 << bits) - 1
     N, K = len(W), len(W[0])
@@ -47,14 +48,14 @@ def quantize(W, group_size, sym, g_idx=None, bits=4):
             vals = [W[n][k] for k in cols]
             if sym:
                 a = max(abs(v) for v in vals)
-                s = f16(2.0 * a / 15.0) if bits == 4 else f16(a / 127.0)
+                s = f16(a / 127.0) if bits == 8 else f16(2.0 * a / top)
             else:
                 lo, hi = min(vals), max(vals)
                 s = f16((hi - lo) / top)
             if s == 0.0:
                 s = 1.0
             if sym:
-                z = 8 if bits == 4 else 128
+                z = 1 << (bits - 1)
             else:
                 z = _clamp(round(-lo / s), 0, top)
             s_out[n][t] = s
@@ -102,3 +103,17 @@ def awq_linear(x, W, act_scale, group_size, sym, g_idx=None, bits=4):
     q, s, z = quantize(Ws, group_size, sym, g_idx, bits)
     gi = g_idx if g_idx is not None else [k // group_size for k in range(K)]
     return linear(xs, dequant(q, s, z, gi)), q, s, z, xs
+
+
+def pack_stream3(codes):
+    """3-bit codes of one row -> list of uint32 words of the bit stream, code
+    k in stream bits 3k .. 3k+2 (bit i of the stream is bit i % 32 of word
+    i // 32)."""
+    total = 3 * len(codes)
+    words = [0] * (-(-total // 32))
+    for k, c in enumerate(codes):
+        for b in range(3):
+            if (c >> b) & 1:
+                i = 3 * k + b
+                words[i // 32] |= 1 << (i % 32)
+    return words

@@ -17,8 +17,9 @@ What it computes, step by step, and where each step comes from:
    find the range, pick the scale that spreads the integer grid over it, round
    each weight to the nearest grid point). With b-bit codes, qmax = 2^b - 1:
    asymmetric: s = fp16((max - min) / qmax), z = clamp(rint(-min / s), 0, qmax);
-   symmetric, 4 bits: s = fp16(2 * max|w| / 15), z = 8 (the linear formula
-     over [-a, a], which reproduces the fixed zero point 8);
+   symmetric, 3 or 4 bits: s = fp16(2 * max|w| / qmax), z = 2^(b-1) (the
+     linear formula over [-a, a], which reproduces the fixed zero point 8 of
+     4 bits; 4 at 3 bits);
    symmetric, 8 bits: the page's own int8 absmax code, s = fp16(max|w| / 127),
      codes clamp(rint(w / s), -127, 127), stored with the offset z = 128.
    A scale that is zero (constant group, or a range that rounds to 0 in fp16)
@@ -32,6 +33,8 @@ What it computes, step by step, and where each step comes from:
 4. Canonical packing: 32/b codes per uint32 along the packed axis, code j of
    word k // (32/b) in bits b*j .. b*j+b-1 for column k with k % (32/b) == j;
    zero points packed the same way along the group axis, padded with zeros.
+   3-bit codes (32/3 is not whole) form one little-endian bit stream per
+   row: column k in stream bits 3k .. 3k+2, 32 codes per 3 words.
 5. Dequantization w_hat = fp16((q - z) * s) ("The Math of Quantization":
    x_approx = (q - Z) * S). The fp64 product is exact; one round to nearest
    even gives the fp16 weight ("the actual matrix multiply still happens in
@@ -61,17 +64,19 @@ import numpy as np
 
 QMAX = 15  # 4-bit codes are 0..15
 SYM_ZERO = 8  # symmetric 4-bit scheme: zero point fixed at 8
-BITS = (4, 8)  # code widths: W4A16 and W8A16 ("4-bit bigger or 8-bit smaller")
+# code widths: 4 bits, and the other two the pages name ("How do GPTQ and AWQ
+# differ ...", section "The shared setting": 3 and 8 are also possible)
+BITS = (3, 4, 8)
 
 
 def qmax(bits: int) -> int:
     if bits not in BITS:
-        raise ValueError("bits must be 4 or 8")
+        raise ValueError("bits must be 3, 4 or 8")
     return (1 << bits) - 1
 
 
 def sym_zero(bits: int) -> int:
-    """Fixed zero point of the symmetric scheme: 8 (4 bits), 128 (8 bits)."""
+    """Fixed zero point of the symmetric scheme: 4 (3 bits), 8 (4 bits), 128 (8 bits)."""
     return 1 << (bits - 1)
 TOL_REL = 2e-3  # |y_gpu - y_ref| <= TOL_REL * sum|x * w_hat| + TOL_ABS
 TOL_ABS = 1e-3
@@ -150,7 +155,7 @@ def group_scale_zero(w: np.ndarray, sym: bool, bits: int = 4) -> tuple[np.ndarra
     qm = qmax(bits)
     if sym:
         a = np.max(np.abs(w), axis=1)
-        s = fp16_rne(2.0 * a / qm) if bits == 4 else fp16_rne(a / 127.0)
+        s = fp16_rne(a / 127.0) if bits == 8 else fp16_rne(2.0 * a / qm)
     else:
         mn = np.min(w, axis=1)
         mx = np.max(w, axis=1)
@@ -222,9 +227,21 @@ def unpack_nibbles(words: np.ndarray, C: int) -> np.ndarray:
 
 def pack_codes(codes: np.ndarray, bits: int) -> np.ndarray:
     """Pack b-bit codes [R, C] into uint32 [R, ceil(C / (32/b))], code j of a
-    word in bits b*j .. b*j+b-1; missing columns of the last word are zero."""
+    word in bits b*j .. b*j+b-1; missing columns of the last word are zero.
+    3 bits: a bit stream per row, column k in bits 3k .. 3k+2, ceil(3C/32) words."""
     if bits == 4:
         return pack_nibbles(codes)
+    if bits == 3:
+        codes = np.asarray(codes, dtype=np.uint8)
+        if codes.max(initial=0) > 7:
+            raise ValueError("codes must be 0..7")
+        R, C = codes.shape
+        nw = -(-3 * C // 32)
+        stream = np.zeros((R, nw * 32), dtype=np.uint8)  # one bit per entry
+        for b in range(3):
+            stream[:, b:3 * C:3] = (codes >> b) & 1
+        weights = (np.uint64(1) << np.arange(32, dtype=np.uint64))
+        return (stream.reshape(R, nw, 32).astype(np.uint64) * weights).sum(axis=2).astype(np.uint32)
     codes = np.asarray(codes, dtype=np.uint8)
     per = 32 // bits
     R, C = codes.shape
@@ -241,6 +258,14 @@ def unpack_codes(words: np.ndarray, C: int, bits: int) -> np.ndarray:
     """Inverse of ``pack_codes``."""
     if bits == 4:
         return unpack_nibbles(words, C)
+    if bits == 3:
+        words = np.asarray(words, dtype=np.uint32)
+        R, nw = words.shape
+        stream = ((words[:, :, None] >> np.arange(32, dtype=np.uint32)) & 1).reshape(R, nw * 32)
+        out = np.zeros((R, C), dtype=np.uint8)
+        for b in range(3):
+            out |= (stream[:, b:3 * C:3].astype(np.uint8) << b)
+        return out
     words = np.asarray(words, dtype=np.uint32)
     per = 32 // bits
     R, nw = words.shape

@@ -507,3 +507,95 @@ def test_pack_codes_8bit_every_byte_position_and_roundtrip():
     rng = np.random.default_rng(12)
     c = rng.integers(0, 256, (5, 37)).astype(np.uint8)
     assert np.array_equal(O.unpack_codes(O.pack_codes(c, 8), 37, 8), c)
+
+
+# ---------------------------------------------------------------------------
+# 3-bit codes (W3A16): "3 and 8 are also possible" ("How do GPTQ and AWQ
+# differ ...", section "The shared setting"); the same group machinery, 8 levels
+# ---------------------------------------------------------------------------
+def test_3bit_levels_and_bits_per_weight():
+    assert O.qmax(3) == 7 and O.sym_zero(3) == 4
+    assert O.bits_per_weight(128, False, 3) == 3 + 0.125 + 3 / 128 == 3.1484375
+    assert O.bits_per_weight(128, True, 3) == 3.125
+    assert O.packed_bytes_closed_form(4096, 4096, 128, False, 3) * 8 / 4096 ** 2 == 3.1484375
+    with pytest.raises(ValueError):
+        O.qmax(2)
+
+
+def test_3bit_symmetric_hand_example():
+    """a = 3.5 * 2^-4, so s = 2a / 7 = 2^-4 exactly and z = 4; w / s below are
+    -3.5 (-> -4), 3.5 (-> 4, clamped to 7 - 4), 0, 1, 1.5 (tie -> 2),
+    2.5 (tie -> 2), -1, -2.5 (tie -> -2)."""
+    s0 = 2.0 ** -4
+    a = 3.5 * s0
+    W = np.array([[-a, a, 0, s0, 1.5 * s0, 2.5 * s0, -s0, -2.5 * s0]], dtype=np.float16)
+    q, s, z = O.rtn_quantize(W, 8, sym=True, bits=3)
+    assert float(s[0, 0]) == s0 and int(z[0, 0]) == 4
+    assert q[0].tolist() == [0, 7, 4, 5, 6, 6, 3, 2]
+    qb, sb, zb = brute.quantize(W.astype(np.float64).tolist(), 8, True, None, 3)
+    assert qb[0] == q[0].tolist() and sb[0][0] == s0 and zb[0][0] == 4
+
+
+def test_3bit_asymmetric_hand_example():
+    """min -1, max 6: s = 7 / 7 = 1, z = rint(1) = 1; q = rint(w) + 1 with
+    0.5 -> 0 and 2.5 -> 2 (ties to even)."""
+    W = np.array([[-1.0, 6.0, 0.5, 2.5, 3.5, 1.0, -0.5, 4.0]], dtype=np.float16)
+    q, s, z = O.rtn_quantize(W, 8, sym=False, bits=3)
+    assert float(s[0, 0]) == 1.0 and int(z[0, 0]) == 1
+    assert q[0].tolist() == [0, 7, 1, 3, 5, 2, 1, 5]
+
+
+def test_3bit_roundtrip_and_error_bound():
+    rng = np.random.default_rng(13)
+    for s in O.fp16_rne(rng.uniform(1e-4, 0.5, 16)).astype(np.float64):
+        for z in range(8):
+            q = np.arange(8, dtype=np.uint8)
+            w_hat = O.fp16_rne((q.astype(np.float64) - z) * s)
+            assert np.array_equal(O.quantize_codes(w_hat.astype(np.float64), s, z, 3), q)
+    W = synth.weights_np(16, 512, 14)
+    for sym in (False, True):
+        q, sc, zz = O.rtn_quantize(W, 128, sym, bits=3)
+        assert q.max() <= 7
+        w_hat = O.dequant(q, sc, zz, 128).astype(np.float64)
+        sd = np.repeat(sc.astype(np.float64), 128, axis=1)
+        u = 2.0 ** -11
+        # inside the range: half a step; the symmetric maximum is clamped by one more half step
+        lim = sd * (1.0 if sym else 0.5 + 16 * u) + u * np.abs(w_hat)
+        assert np.all(np.abs(W.astype(np.float64) - w_hat) <= lim)
+
+
+@pytest.mark.parametrize("sym", [False, True])
+@pytest.mark.parametrize("g", [8, 32, 64])
+@pytest.mark.parametrize("act_order", [False, True])
+def test_numpy_oracle_matches_pure_python_3bit(sym, g, act_order):
+    N, K, M = 6, 128, 3
+    W = synth.weights_np(N, K, synth.seed_for("brute3", N, K, g, sym, act_order))
+    x = synth.activations_np(M, K, 0.05, synth.seed_for("brute3-x", g))
+    gidx = synth.act_order_g_idx(x, g) if act_order else None
+    y, B, (q, s, z), w_hat = O.w4a16_linear(x, W, g, sym, gidx, bits=3)
+    qb, sb, zb = brute.quantize(W.astype(np.float64).tolist(), g, sym, None if gidx is None else gidx.tolist(), 3)
+    assert q.tolist() == qb and s.astype(np.float64).tolist() == sb and z.tolist() == zb
+    gl = (np.arange(K) // g).tolist() if gidx is None else gidx.tolist()
+    wb = brute.dequant(qb, sb, zb, gl)
+    assert w_hat.astype(np.float64).tolist() == wb
+    assert np.allclose(y, np.array(brute.linear(x.astype(np.float64).tolist(), wb)), rtol=1e-12, atol=1e-12)
+
+
+def test_pack_codes_3bit_stream_every_position_and_roundtrip():
+    """Code k occupies stream bits 3k .. 3k+2; codes 10 and 21 straddle word
+    boundaries (bits 30-32 and 63-65)."""
+    for k in range(32):
+        for v in (1, 5, 7):
+            codes = np.zeros((1, 32), dtype=np.uint8)
+            codes[0, k] = v
+            w = O.pack_codes(codes, 3)
+            assert w.shape == (1, 3)
+            stream = sum(int(w[0, i]) << (32 * i) for i in range(3))
+            assert stream == v << (3 * k)
+            assert w[0].tolist() == brute.pack_stream3(codes[0].tolist())
+    rng = np.random.default_rng(15)
+    c = rng.integers(0, 8, (5, 37)).astype(np.uint8)
+    w = O.pack_codes(c, 3)
+    assert w.shape == (5, 4)  # ceil(3 * 37 / 32)
+    assert all(w[r].tolist() == brute.pack_stream3(c[r].tolist()) for r in range(5))
+    assert np.array_equal(O.unpack_codes(w, 37, 3), c)
