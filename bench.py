@@ -61,13 +61,14 @@ def parse_args():
     p.add_argument("--workload", default="llama2-7b", choices=["llama2-7b", "llama70b", "sweep8192"])
     p.add_argument("--no-gemm", action="store_true")
     p.add_argument("--no-shapes", action="store_true")
-    p.add_argument("--bits", type=int, default=4, choices=[4, 8], help="code width of every packed linear")
+    p.add_argument("--bits", type=int, default=4, choices=[3, 4, 8], help="code width of every packed linear")
     return p.parse_args()
 
 
 def gemv_bytes(N: int, K: int, M: int = 1, g: int = 128, sym: bool = False, bits: int = 4) -> int:
     G = K // g
-    return N * K * bits // 8 + N * G * 2 + (0 if sym else N * G * bits // 8) + M * K * 2 + M * N * 2
+    zero_bits = 8 if bits == 8 else 4  # 3-bit zero points are stored as nibbles
+    return N * K * bits // 8 + N * G * 2 + (0 if sym else N * G * zero_bits // 8) + M * K * 2 + M * N * 2
 
 
 def measured_peaks():
@@ -335,7 +336,7 @@ def run_ours(args, rank, world, local_rank):
                         "down 4096x11008), 224 GEMVs per step")
             frac = synth.LLAMA2_7B_OUTLIER_FRAC
         line = {
-            "metric": METRIC if args.bits == 4 else METRIC.replace("W4A16", "W8A16"),
+            "metric": METRIC if args.bits == 4 else METRIC.replace("W4A16", f"W{args.bits}A16"),
             "value": round(value, 1),
             "unit": "GB/s",
             "n_gpus": world,

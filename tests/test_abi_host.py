@@ -62,6 +62,16 @@ def test_packed_bytes_layout(lib):
     assert W.packed_bytes(fmt(200, 96, g=32)) == 2 * 2 * 4096 + 2 * 3 * 256 + 512
 
 
+def test_packed_bytes_3bit(lib):
+    """3-bit codes: 3 KiB tiles; zero points stay nibble pairs (64 B per group block)."""
+    f3 = fmt(4096, 4096, bits=3)
+    assert W.check_format(f3) == 0
+    assert W.packed_bytes(f3) == 32 * 64 * 3072 + 32 * 32 * 256 + 32 * 32 * 64
+    # the blob's zero points take 4 bits where the closed form counts 3
+    assert W.packed_bytes(f3) == O.packed_bytes_closed_form(4096, 4096, 128, False, bits=3) + 4096 * 32 / 8
+    assert W.packed_bytes(fmt(4096, 4096, sym=True, bits=3)) == O.packed_bytes_closed_form(4096, 4096, 128, True, 3)
+
+
 def test_packed_bytes_8bit(lib):
     """8-bit codes: twice the code and zero-point bytes, the same scales."""
     for sym in (False, True):
@@ -73,7 +83,7 @@ def test_packed_bytes_8bit(lib):
 
 
 @pytest.mark.parametrize("kw,status", [
-    (dict(bits=3), UNSUPPORTED),
+    (dict(bits=5), UNSUPPORTED),
     (dict(bits=2), UNSUPPORTED),
     (dict(bits=16), UNSUPPORTED),
     (dict(g=16), UNSUPPORTED),

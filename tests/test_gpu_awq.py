@@ -70,7 +70,7 @@ def awq_case(N, K, M, g, sym, act, bits=4, tag="awq"):
     return fmt, packed, to_dev(x), y_ref, B
 
 
-@pytest.mark.parametrize("bits", [4, 8])
+@pytest.mark.parametrize("bits", [3, 4, 8])
 @pytest.mark.parametrize("sym", [False, True])
 @pytest.mark.parametrize("act", [False, True])
 def test_quantize_pack_dequant_bit_exact(cuda_ok, bits, sym, act):
@@ -89,7 +89,7 @@ def test_quantize_pack_dequant_bit_exact(cuda_ok, bits, sym, act):
     assert np.array_equal(bits16(got), bits16(O.dequant(qo, so, zo, g, gidx)))
 
 
-@pytest.mark.parametrize("bits", [4, 8])
+@pytest.mark.parametrize("bits", [3, 4, 8])
 @pytest.mark.parametrize("g", [32, 128])
 @pytest.mark.parametrize("act", [False, True])
 @pytest.mark.parametrize("M", [1, 5, 16])
@@ -107,7 +107,7 @@ def test_gemv_ragged(cuda_ok, N, K, g):
         assert_within(W.gemv(fmt, packed, xd).cpu().numpy(), y_ref, B)
 
 
-@pytest.mark.parametrize("bits", [4, 8])
+@pytest.mark.parametrize("bits", [3, 4, 8])
 @pytest.mark.parametrize("act", [False, True])
 @pytest.mark.parametrize("tile", TILES)
 def test_gemm(cuda_ok, bits, act, tile):

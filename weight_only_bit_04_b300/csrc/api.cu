@@ -35,7 +35,7 @@ w4a16_status format_status(const w4a16_format* f) {
   if (f->has_act_scale != 0 && f->has_act_scale != 1) return W4A16_ERR_INVALID_ARG;
   if (f->N < 1 || f->K < 1 || f->N > (int64_t(1) << 20) || f->K > (int64_t(1) << 20))
     return W4A16_ERR_INVALID_ARG;
-  if (f->bits != 4 && f->bits != 8) return W4A16_ERR_UNSUPPORTED;
+  if (f->bits != 3 && f->bits != 4 && f->bits != 8) return W4A16_ERR_UNSUPPORTED;
   if (f->group_size != 32 && f->group_size != 64 && f->group_size != 128) return W4A16_ERR_UNSUPPORTED;
   if (f->K % f->group_size != 0) return W4A16_ERR_UNSUPPORTED;  // no ragged last group
   return W4A16_OK;

@@ -91,15 +91,15 @@ struct GroupFactors {
 // Exact float of a 4-bit value without an int-to-float conversion.
 __device__ __forceinline__ float nib_to_float(uint32_t v) { return __uint_as_float(0x4B000000u | v) - 8388608.f; }
 
-// zraw: 4 bits: one byte, row g in the low nibble, row g+8 in the high one;
-// 8 bits: two bytes, row g then row g+8. 4-bit rows g+8 sit at 2^-20 (high
-// nibbles), everything else at 2^-24.
+// zraw: 3 and 4 bits: one byte, row g in the low nibble, row g+8 in the high
+// one; 8 bits: two bytes, row g then row g+8. 4-bit rows g+8 sit at 2^-20
+// (high nibbles), everything else at 2^-24.
 template <bool SYM, int BITS>
 __device__ __forceinline__ GroupFactors make_factors(uint32_t s2, uint32_t zraw) {
   const float2 sf = __half22float2(*reinterpret_cast<const __half2*>(&s2));
   constexpr float kSymZero = float(1 << (BITS - 1));
-  const float zg = SYM ? kSymZero : nib_to_float(BITS == 4 ? (zraw & 0xFu) : (zraw & 0xFFu));
-  const float zh = SYM ? kSymZero : nib_to_float(BITS == 4 ? (zraw >> 4) & 0xFu : (zraw >> 8) & 0xFFu);
+  const float zg = SYM ? kSymZero : nib_to_float(BITS != 8 ? (zraw & 0xFu) : (zraw & 0xFFu));
+  const float zh = SYM ? kSymZero : nib_to_float(BITS != 8 ? (zraw >> 4) & 0xFu : (zraw >> 8) & 0xFFu);
   GroupFactors f;
   f.sa = sf.x * 16777216.f;
   f.sb = sf.y * (BITS == 4 ? 1048576.f : 16777216.f);
@@ -139,19 +139,44 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
   return d;
 }
 
-// The four A-fragment registers of 16-column step j from the codes the lane
-// loaded (v = the 16-byte part holding step j): values q * 2^-24, or q * 2^-20
-// for the high nibbles of 4-bit codes.
+// 16-byte parts a lane loads per tile and 64-column block: 4 bits one, 8 bits
+// two; 3 bits one per warp tile pair and block (tile 0: a 16-byte part, tile
+// 1: an 8-byte part), read together.
 template <int BITS>
-__device__ __forceinline__ void extract_step(const uint4& v, int j, uint32_t a[4]) {
+constexpr int kParts = BITS == 8 ? 2 : 1;
+
+// The four A-fragment registers of 16-column step j of tile tt from the codes
+// the lane loaded for its two tiles: values q * 2^-24, or q * 2^-20 for the
+// high nibbles of 4-bit codes.
+template <int BITS>
+__device__ __forceinline__ void extract_step(const uint4 (&wb)[2][kParts<BITS>], int tt, int j, uint32_t a[4]) {
   if (BITS == 4) {
-    extract_word(word_of(v, j), a);
-  } else {
+    extract_word(word_of(wb[tt][0], j), a);
+  } else if (BITS == 8) {
+    const uint4& v = wb[tt][(kParts<BITS> - 1) & (j >> 1)];
     const uint32_t wg = word_of(v, 2 * (j & 1)), wh = word_of(v, 2 * (j & 1) + 1);
     a[0] = prmt(wg, 0u, 0x4140u);  // row g,   columns 4t, 4t+1
     a[1] = prmt(wh, 0u, 0x4140u);  // row g+8
     a[2] = prmt(wg, 0u, 0x4342u);  // row g,   columns 4t+2, 4t+3
     a[3] = prmt(wh, 0u, 0x4342u);  // row g+8
+  } else {
+    // the tile's three words: tile 0 A.x, A.y, A.z; tile 1 A.w, B.x, B.y
+    const uint4& A = wb[0][0];
+    const uint4& Bp = wb[1][0];
+    const uint32_t w0 = tt == 0 ? A.x : A.w, w1 = tt == 0 ? A.y : Bp.x, w2 = tt == 0 ? A.z : Bp.y;
+    constexpr uint32_t M = 0x00070007u;
+    if (j < 3) {
+      const uint32_t w = j == 0 ? w0 : j == 1 ? w1 : w2;
+      a[0] = w & M;
+      a[1] = (w >> 9) & M;
+      a[2] = (w >> 3) & M;
+      a[3] = (w >> 12) & M;
+    } else {
+      a[0] = (w0 >> 6) & M;
+      a[1] = (w1 >> 6) & M;
+      a[2] = (w2 >> 6) & M;
+      a[3] = ((w0 >> 15) & 0x00010001u) | ((w1 >> 14) & 0x00020002u) | ((w2 >> 13) & 0x00040004u);
+    }
   }
 }
 
@@ -174,7 +199,7 @@ struct Unit {
 
 template <int GS, int BITS>
 struct UnitRegs {
-  uint4 w[Unit<GS>::kBlocks][kTilesPerWarp][BITS / 4];  // a lane's codes: 16 bytes per 4 bits of width
+  uint4 w[Unit<GS>::kBlocks][kTilesPerWarp][kParts<BITS>];  // a lane's codes
   uint32_t s[Unit<GS>::kGroups][kTilesPerWarp];
   uint32_t z[Unit<GS>::kGroups][kTilesPerWarp];
 };
@@ -185,7 +210,25 @@ struct CodeWords {
   static constexpr int kBlock = kTileWords * BITS / 4;
   static constexpr int kRow16 = 128 * BITS / 4;
   static constexpr int kPart = 128;  // 8 bits: words between a lane's two 16-byte parts
+  // words from a lane's first code word to part `part` of tile tt; 3 bits:
+  // tile 1 is the 8-byte part after the pair's 512 bytes of 16-byte parts
+  __device__ static __forceinline__ int off(int tt, int part, int lane) {
+    return BITS == 3 ? (tt == 0 ? 0 : 128 - 2 * lane) : tt * kRow16 + part * kPart;
+  }
+  static constexpr bool narrow(int tt) { return BITS == 3 && tt == 1; }  // an 8-byte part
 };
+
+__device__ __forceinline__ int lane_id() { return int(threadIdx.x & 31); }
+
+// Zero-point bytes per (row pair, group): a nibble pair, or two bytes.
+template <int BITS>
+constexpr int kZeroMul = BITS == 8 ? 2 : 1;
+
+__device__ __forceinline__ uint4 ldg_stream_u2(const uint32_t* p) {
+  uint2 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
+  return make_uint4(v.x, v.y, 0u, 0u);
+}
 
 __device__ __forceinline__ uint32_t ldg_nc_u16(const void* p) {
   uint16_t v;
@@ -204,8 +247,10 @@ __device__ __forceinline__ void load_unit(UnitRegs<GS, BITS>& r, const uint32_t*
 #pragma unroll
     for (int tt = 0; tt < kTilesPerWarp; ++tt)
 #pragma unroll
-      for (int part = 0; part < BITS / 4; ++part)
-        r.w[bb][tt][part] = ldg_stream_u4(qp + (unit * U::kBlocks + bb) * CW::kBlock + tt * CW::kRow16 + part * CW::kPart);
+      for (int part = 0; part < kParts<BITS>; ++part) {
+        const uint32_t* src = qp + (unit * U::kBlocks + bb) * CW::kBlock + CW::off(tt, part, lane_id());
+        r.w[bb][tt][part] = CW::narrow(tt) ? ldg_stream_u2(src) : ldg_stream_u4(src);
+      }
 #pragma unroll
   for (int gg = 0; gg < U::kGroups; ++gg) {
     // (32-column groups only: a ragged last block's second half has no group;
@@ -214,7 +259,7 @@ __device__ __forceinline__ void load_unit(UnitRegs<GS, BITS>& r, const uint32_t*
 #pragma unroll
     for (int tt = 0; tt < kTilesPerWarp; ++tt) {
       r.s[gg][tt] = ldg_nc_u32(sp + gi * 64 + tt * 8);
-      r.z[gg][tt] = SYM ? 0u : BITS == 4 ? ldg_nc_u8(zp + gi * 64 + tt * 8) : ldg_nc_u16(zp + gi * 128 + tt * 16);
+      r.z[gg][tt] = SYM ? 0u : BITS != 8 ? ldg_nc_u8(zp + gi * 64 + tt * 8) : ldg_nc_u16(zp + gi * 128 + tt * 16);
     }
   }
 }
@@ -247,7 +292,7 @@ __device__ __forceinline__ void compute_unit(const UnitRegs<GS, BITS>& r, const 
 #pragma unroll
       for (int tt = 0; tt < kTilesPerWarp; ++tt) {
         uint32_t af[4];
-        extract_step<BITS>(r.w[bb][tt][BITS == 8 ? (j >> 1) : 0], j, af);
+        extract_step<BITS>(r.w[bb], tt, j, af);
 #pragma unroll
         for (int nb = 0; nb < NB; ++nb)
           mma_16816(acc[tt][nb], af, bx[j][nb].x, bx[j][nb].y, fresh ? zero4 : acc[tt][nb]);
@@ -310,7 +355,7 @@ __device__ __forceinline__ void stage_activations(const uint16_t* __restrict__ x
 //   zero words [kGroups][2 tiles] 4 B (the word holding this row pair's byte).
 template <int GS, int BITS>
 struct WbSlot {
-  static constexpr int kCodeFields = Unit<GS>::kBlocks * kTilesPerWarp * (BITS / 4);
+  static constexpr int kCodeFields = Unit<GS>::kBlocks * kTilesPerWarp * kParts<BITS>;
   static constexpr int kMetaFields = Unit<GS>::kGroups * kTilesPerWarp;
   static constexpr int kScaleOff = kCodeFields * kThreads * 16;
   static constexpr int kZeroOff = kScaleOff + kMetaFields * kThreads * 4;
@@ -323,9 +368,14 @@ constexpr int kWbSlots = BITS == 8 ? 2 : 4;
 
 __host__ __device__ inline int wb_slot_bytes(int GS, int bits) {
   if (bits == 8) return GS == 128 ? WbSlot<128, 8>::kBytes : GS == 64 ? WbSlot<64, 8>::kBytes : WbSlot<32, 8>::kBytes;
+  static_assert(WbSlot<128, 3>::kBytes == WbSlot<128, 4>::kBytes, "3-bit slots reuse the 4-bit size");
   return GS == 128 ? WbSlot<128, 4>::kBytes : GS == 64 ? WbSlot<64, 4>::kBytes : WbSlot<32, 4>::kBytes;
 }
 
+__device__ __forceinline__ void cp_async_8(void* smem_dst, const void* gmem_src) {
+  const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(smem_dst));
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(d), "l"(gmem_src) : "memory");
+}
 __device__ __forceinline__ void cp_async_4(void* smem_dst, const void* gmem_src) {
   const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(smem_dst));
   asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(d), "l"(gmem_src) : "memory");
@@ -370,7 +420,7 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const GemvArgs a) {
                        size_t(u0) * U::kBlocks * CW::kBlock;
   const uint32_t* sp = a.scales2 + (size_t(R) * G * 8 + r16) * 8 + g + size_t(u0) * U::kGroups * 64;
   const uint8_t* zp = SYM ? nullptr
-                          : a.zeros + ((size_t(R) * G * 8 + r16) * 8 + g + size_t(u0) * U::kGroups * 64) * (BITS / 4);
+                          : a.zeros + ((size_t(R) * G * 8 + r16) * 8 + g + size_t(u0) * U::kGroups * 64) * kZeroMul<BITS>;
 
   const bool early = (a.flags & kGemvWeightsReady) != 0;
   const int M = a.M;
@@ -388,9 +438,14 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const GemvArgs a) {
 #pragma unroll
         for (int tt = 0; tt < kTilesPerWarp; ++tt)
 #pragma unroll
-          for (int part = 0; part < BITS / 4; ++part)
-            cp_async_16(slot + (((bb * kTilesPerWarp + tt) * (BITS / 4) + part) * kThreads + tid) * 16,
-                        qp + (i * U::kBlocks + bb) * CW::kBlock + tt * CW::kRow16 + part * CW::kPart);
+          for (int part = 0; part < kParts<BITS>; ++part) {
+            unsigned char* dst = slot + (((bb * kTilesPerWarp + tt) * kParts<BITS> + part) * kThreads + tid) * 16;
+            const uint32_t* src = qp + (i * U::kBlocks + bb) * CW::kBlock + CW::off(tt, part, lane);
+            if (CW::narrow(tt))
+              cp_async_8(dst, src);
+            else
+              cp_async_16(dst, src);
+          }
 #pragma unroll
       for (int gg = 0; gg < U::kGroups; ++gg) {
         const int gi = GS == 32 ? min(i * U::kGroups + gg, gmax) : i * U::kGroups + gg;
@@ -401,7 +456,7 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const GemvArgs a) {
           if (!SYM)  // the aligned word holding this lane's zero point(s)
             cp_async_4(slot + SL::kZeroOff + (f * kThreads + tid) * 4,
                        reinterpret_cast<const uint32_t*>(
-                           reinterpret_cast<uintptr_t>(zp + (gi * 64 + tt * 8) * (BITS / 4)) & ~uintptr_t(3)));
+                           reinterpret_cast<uintptr_t>(zp + (gi * 64 + tt * 8) * kZeroMul<BITS>) & ~uintptr_t(3)));
         }
       }
     }
@@ -467,9 +522,9 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const GemvArgs a) {
 #pragma unroll
         for (int tt = 0; tt < kTilesPerWarp; ++tt)
 #pragma unroll
-          for (int part = 0; part < BITS / 4; ++part)
-            r.w[bb][tt][part] =
-                *reinterpret_cast<const uint4*>(slot + (((bb * kTilesPerWarp + tt) * (BITS / 4) + part) * kThreads + tid) * 16);
+          for (int part = 0; part < kParts<BITS>; ++part)
+            r.w[bb][tt][part] = *reinterpret_cast<const uint4*>(
+                slot + (((bb * kTilesPerWarp + tt) * kParts<BITS> + part) * kThreads + tid) * 16);
 #pragma unroll
       for (int gg = 0; gg < U::kGroups; ++gg)
 #pragma unroll
@@ -478,7 +533,7 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const GemvArgs a) {
           r.s[gg][tt] = *reinterpret_cast<const uint32_t*>(slot + SL::kScaleOff + (f * kThreads + tid) * 4);
           r.z[gg][tt] = SYM ? 0u
                             : (*reinterpret_cast<const uint32_t*>(slot + SL::kZeroOff + (f * kThreads + tid) * 4) >>
-                               zshift) & (BITS == 4 ? 0xFFu : 0xFFFFu);
+                               zshift) & (BITS != 8 ? 0xFFu : 0xFFFFu);
         }
       const int xo = i * U::kBlocks * kColsPerBlock;
       compute_unit<NB, GS, SYM, STAGED, BITS>(r, xl0 + xo, xl1 + xo, tot);

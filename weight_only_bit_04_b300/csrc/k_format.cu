@@ -58,7 +58,7 @@ __global__ void __launch_bounds__(256) quantize_rtn_kernel(Layout L, const uint1
     amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
   }
   // fp64 from here on; every fp16 value and difference of two is exact in fp64.
-  // b-bit codes, qmax = 2^b - 1. Symmetric: 4 bits s = 2a/15, z = 8; 8 bits
+  // b-bit codes, qmax = 2^b - 1. Symmetric: 3, 4 bits s = 2a/qmax, z = 2^(b-1); 8 bits
   // the int8 absmax code, s = a/127, codes clamp(rint(w/s), -127, 127) + 128.
   const double qmax = double((1 << L.bits) - 1);
   const bool sym8 = L.sym && L.bits == 8;
@@ -145,6 +145,39 @@ __global__ void __launch_bounds__(256) pack_qweight_kernel(Layout L, const uint8
   qweight[wi] = word;
 }
 
+// 3-bit codes: one thread per (tile, 16-row tile, lane) composes that lane's
+// three words (the sixteenth code of a step is spread over three words).
+__global__ void __launch_bounds__(256) pack_qweight3_kernel(Layout L, const uint8_t* __restrict__ q,
+                                                            const int32_t* __restrict__ perm,
+                                                            uint32_t* __restrict__ qweight) {
+  const int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= L.NR * L.KB * 256) return;
+  const int64_t tile = i >> 8;
+  const int r16 = int((i >> 5) & 7), lane = int(i & 31);
+  const int64_t R = tile / L.KB;
+  const int64_t b = tile - R * L.KB;
+  const int g = lane >> 2, t = lane & 3;
+  uint32_t w[3] = {0u, 0u, 0u};
+  for (int j = 0; j < 4; ++j)
+    for (int a = 0; a < 4; ++a) {
+      int wi, sh;
+      w3_field(j, a, &wi, &sh);
+      const int64_t n = R * kRowsPerBlock + r16 * 16 + g + 8 * (a & 1);
+      for (int h2 = 0; h2 < 2; ++h2) {
+        const int64_t p = b * kColsPerBlock + 16 * j + 4 * t + 2 * (a >> 1) + h2;
+        if (p >= L.K || n >= L.N) continue;
+        const uint32_t code = q[n * L.K + (perm ? perm[p] : p)] & 7u;
+        if (wi >= 0) {
+          w[wi] |= code << (sh + 16 * h2);
+        } else {
+          for (int bt = 0; bt < 3; ++bt) w[bt] |= ((code >> bt) & 1u) << (15 + 16 * h2);
+        }
+      }
+    }
+  uint32_t* tw = qweight + tile * 768;
+  for (int wi = 0; wi < 3; ++wi) tw[w3_word_index(r16, lane, wi)] = w[wi];
+}
+
 // One thread per (row block, group, 16-row tile, lane group): a scale pair and
 // the zero points of the two rows (one byte of two nibbles, or two bytes).
 __global__ void __launch_bounds__(256) pack_meta_kernel(Layout L, const uint16_t* __restrict__ scales,
@@ -164,7 +197,7 @@ __global__ void __launch_bounds__(256) pack_meta_kernel(Layout L, const uint16_t
   const uint32_t s1 = n1 < L.N ? scales[n1 * L.G + gi] : 0u;
   s_out[i] = s0 | (s1 << 16);
   if (z_out) {
-    if (L.bits == 4) {
+    if (L.bits != 8) {
       const uint32_t z0 = n0 < L.N ? (zeros[n0 * L.G + gi] & 0xF) : 0u;
       const uint32_t z1 = n1 < L.N ? (zeros[n1 * L.G + gi] & 0xF) : 0u;
       z_out[i] = uint8_t(z0 | (z1 << 4));
@@ -234,6 +267,44 @@ __global__ void __launch_bounds__(256) dequant_kernel(Layout L, BlobView B, uint
   }
 }
 
+// 3-bit codes: one thread per (tile, 16-row tile, lane), as in the packer.
+__global__ void __launch_bounds__(256) dequant3_kernel(Layout L, BlobView B, uint16_t* __restrict__ out) {
+  const int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= L.NR * L.KB * 256) return;
+  const int64_t tile = i >> 8;
+  const int r16 = int((i >> 5) & 7), lane = int(i & 31);
+  const int64_t R = tile / L.KB;
+  const int64_t b = tile - R * L.KB;
+  const int g = lane >> 2, t = lane & 3;
+  const uint32_t* tw = B.qweight + tile * 768;
+  uint32_t w[3];
+  for (int wi = 0; wi < 3; ++wi) w[wi] = tw[w3_word_index(r16, lane, wi)];
+  for (int j = 0; j < 4; ++j)
+    for (int a = 0; a < 4; ++a) {
+      int wi, sh;
+      w3_field(j, a, &wi, &sh);
+      const int h = a & 1;
+      const int64_t n = R * kRowsPerBlock + r16 * 16 + g + 8 * h;
+      for (int h2 = 0; h2 < 2; ++h2) {
+        const int64_t p = b * kColsPerBlock + 16 * j + 4 * t + 2 * (a >> 1) + h2;
+        if (p >= L.K || n >= L.N) continue;
+        uint32_t code = 0;
+        if (wi >= 0) {
+          code = (w[wi] >> (sh + 16 * h2)) & 7u;
+        } else {
+          for (int bt = 0; bt < 3; ++bt) code |= ((w[bt] >> (15 + 16 * h2)) & 1u) << bt;
+        }
+        const int64_t gi = p / L.gsize;
+        const int64_t mi = ((R * L.G + gi) * 8 + r16) * 8 + g;
+        const uint32_t z = B.zeros ? ((B.zeros[mi] >> (4 * h)) & 0xF) : 4u;
+        const __half s = __ushort_as_half(B.scales[2 * mi + h]);
+        const __half d = __hsub(__ushort_as_half(uint16_t(0x6400u | code)),
+                                __ushort_as_half(uint16_t(0x6400u | z)));
+        out[n * L.K + (B.perm ? B.perm[p] : p)] = __half_as_ushort(__hmul(d, s));
+      }
+    }
+}
+
 inline unsigned blocks_for(int64_t threads, int per_block) {
   return unsigned((threads + per_block - 1) / per_block);
 }
@@ -252,9 +323,14 @@ cudaError_t launch_pack(const Layout& L, const uint8_t* q, const uint16_t* scale
                         const uint8_t* zeros, const uint16_t* ascale, void* blob, cudaStream_t stream) {
   char* b = static_cast<char*>(blob);
   const int32_t* perm = L.act ? reinterpret_cast<const int32_t*>(b + L.p_off) : nullptr;
-  const int64_t words = L.NR * L.KB * kTileWords * L.bits / 4;
-  pack_qweight_kernel<<<blocks_for(words, 256), 256, 0, stream>>>(
-      L, q, perm, reinterpret_cast<uint32_t*>(b + L.q_off));
+  if (L.bits == 3) {
+    pack_qweight3_kernel<<<blocks_for(L.NR * L.KB * 256, 256), 256, 0, stream>>>(
+        L, q, perm, reinterpret_cast<uint32_t*>(b + L.q_off));
+  } else {
+    const int64_t words = L.NR * L.KB * kTileWords * L.bits / 4;
+    pack_qweight_kernel<<<blocks_for(words, 256), 256, 0, stream>>>(
+        L, q, perm, reinterpret_cast<uint32_t*>(b + L.q_off));
+  }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int64_t metas = L.NR * L.G * 64;
@@ -269,6 +345,10 @@ cudaError_t launch_pack(const Layout& L, const uint8_t* q, const uint16_t* scale
 }
 
 cudaError_t launch_dequant(const Layout& L, const void* blob, uint16_t* w_out, cudaStream_t stream) {
+  if (L.bits == 3) {
+    dequant3_kernel<<<blocks_for(L.NR * L.KB * 256, 256), 256, 0, stream>>>(L, view_of(L, blob), w_out);
+    return cudaGetLastError();
+  }
   const int64_t words = L.NR * L.KB * kTileWords * L.bits / 4;
   dequant_kernel<<<blocks_for(words, 256), 256, 0, stream>>>(L, view_of(L, blob), w_out);
   return cudaGetLastError();

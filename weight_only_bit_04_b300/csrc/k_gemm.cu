@@ -52,22 +52,22 @@ constexpr uint64_t kWaitLimitNs = 1000ull * 1000ull * 1000ull;  // 1 s per wait
 // activations; DS: dequantization warp sets, set d producing the 64-column
 // steps kb = d (mod DS), so that each scheduler interleaves DS independent
 // dequantization streams.
-// Packed-weight part of a stage, per 128-row tile: the code tile (4 KiB of
-// 4-bit or 8 KiB of 8-bit codes), then up to two groups of scale pairs (256 B
+// Packed-weight part of a stage, per 128-row tile: the code tile (3, 4 or
+// 8 KiB of 3-, 4- or 8-bit codes), then up to two groups of scale pairs (256 B
 // each) and of zero points (64 B of nibble pairs or 128 B of byte pairs each).
 template <int BITS>
 struct WTile {
   static constexpr int kCodes = 4096 * BITS / 4;
-  static constexpr int kR16 = kCodes / 8;  // bytes of one 16-row tile
+  static constexpr int kR16 = kCodes / 8;  // bytes of one 16-row tile (3 bits: half a tile pair)
   static constexpr int kScaleOff = kCodes;
-  static constexpr int kZeroGroup = 64 * BITS / 4;
+  static constexpr int kZeroGroup = BITS == 8 ? 128 : 64;
   static constexpr int kZeroOff = kScaleOff + 2 * 256;
   static constexpr int kBytes = kZeroOff + 2 * kZeroGroup;
 };
 
 constexpr int kMaxSmem = 232448;
 constexpr int stage_bytes(int WR, int NT, int BITS) {
-  return (NT * 128 + WR * (4096 * BITS / 4 + 512 + 2 * 64 * BITS / 4) + 1023) / 1024 * 1024;
+  return (NT * 128 + WR * (4096 * BITS / 4 + 512 + 2 * (BITS == 8 ? 128 : 64)) + 1023) / 1024 * 1024;
 }
 // Activation stages of a tile, reduced for 8-bit codes until the block's
 // shared memory fits.
@@ -148,10 +148,15 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, vol
   return false;
 }
 
+// 16-byte parts of packed codes per 16-row tile (3 bits: tile 0 a 16-byte
+// part, tile 1 an 8-byte part, read together).
+template <int BITS>
+constexpr int kGemmParts = BITS == 8 ? 2 : 1;
+
 template <int GS, bool SYM, int BITS>
 struct StepRegs {
   static constexpr int kGroups = GS == 32 ? 2 : 1;  // groups in one 64-column step
-  uint4 w[2][BITS / 4];       // packed words of the warp's two 16-row tiles
+  uint4 w[2][kGemmParts<BITS>];  // packed words of the warp's two 16-row tiles
   uint32_t s[2][kGroups];     // scale pairs
   uint32_t z[2][kGroups];     // zero points (nibble pair, or byte pair)
 };
@@ -173,7 +178,8 @@ __device__ __forceinline__ int step_groups(int kb, int G) {
 // tcgen05.st 16x256b.x4: per 16-column group j, (row g, columns 4t..4t+1),
 // (row g, 4t+2..4t+3), (row g+8, 4t..4t+1), (row g+8, 4t+2..4t+3).
 // 8-bit codes: PRMT places code bytes under the exponent byte 0x64, giving
-// fp16 1024 + q; subtracting 1024 + z leaves the exact q - z.
+// fp16 1024 + q; subtracting 1024 + z leaves the exact q - z. 3-bit codes: the
+// register's pair of fields, shifted down and masked, ORed under 0x6400.
 template <int GS, bool SYM, int BITS>
 __device__ __forceinline__ void dequant_tile(const StepRegs<GS, SYM, BITS>& r, int i, uint32_t (&v)[16]) {
   constexpr int NG = StepRegs<GS, SYM, BITS>::kGroups;
@@ -185,6 +191,11 @@ __device__ __forceinline__ void dequant_tile(const StepRegs<GS, SYM, BITS>& r, i
       const uint32_t zhi = SYM ? 8u : (r.z[i][gg] >> 4);
       za[gg] = zero_lo_const(zlo);
       zb[gg] = zero_hi_const(zhi);
+    } else if (BITS == 3) {
+      const uint32_t zg = SYM ? 4u : (r.z[i][gg] & 0xFu);
+      const uint32_t zh = SYM ? 4u : (r.z[i][gg] >> 4);
+      za[gg] = (0x6400u + zg) * 0x00010001u;
+      zb[gg] = (0x6400u + zh) * 0x00010001u;
     } else {
       const uint32_t zg = SYM ? 128u : (r.z[i][gg] & 0xFFu);
       const uint32_t zh = SYM ? 128u : (r.z[i][gg] >> 8);
@@ -206,8 +217,30 @@ __device__ __forceinline__ void dequant_tile(const StepRegs<GS, SYM, BITS>& r, i
       v[4 * j + 1] = hmul2_u32(a[2], sg[gg]);
       v[4 * j + 2] = hmul2_u32(a[1], sh[gg]);
       v[4 * j + 3] = hmul2_u32(a[3], sh[gg]);
+    } else if (BITS == 3) {
+      const uint4& A = r.w[0][0];
+      const uint4& Bp = r.w[1][0];
+      const uint32_t w0 = i == 0 ? A.x : A.w, w1 = i == 0 ? A.y : Bp.x, w2 = i == 0 ? A.z : Bp.y;
+      constexpr uint32_t M = 0x00070007u;
+      uint32_t c[4];  // fragment registers a0..a3 (row g / g+8, column pairs 4t, 4t+2)
+      if (j < 3) {
+        const uint32_t w = j == 0 ? w0 : j == 1 ? w1 : w2;
+        c[0] = w & M;
+        c[1] = (w >> 9) & M;
+        c[2] = (w >> 3) & M;
+        c[3] = (w >> 12) & M;
+      } else {
+        c[0] = (w0 >> 6) & M;
+        c[1] = (w1 >> 6) & M;
+        c[2] = (w2 >> 6) & M;
+        c[3] = ((w0 >> 15) & 0x00010001u) | ((w1 >> 14) & 0x00020002u) | ((w2 >> 13) & 0x00040004u);
+      }
+      v[4 * j + 0] = hmul2_u32(hsub2_u32(c[0] | 0x64006400u, za[gg]), sg[gg]);
+      v[4 * j + 1] = hmul2_u32(hsub2_u32(c[2] | 0x64006400u, za[gg]), sg[gg]);
+      v[4 * j + 2] = hmul2_u32(hsub2_u32(c[1] | 0x64006400u, zb[gg]), sh[gg]);
+      v[4 * j + 3] = hmul2_u32(hsub2_u32(c[3] | 0x64006400u, zb[gg]), sh[gg]);
     } else {
-      const uint4& wv = r.w[i][(BITS / 4 - 1) & (j >> 1)];
+      const uint4& wv = r.w[i][(kGemmParts<BITS> - 1) & (j >> 1)];
       const uint32_t wg = (j & 1) ? wv.z : wv.x;  // row g, columns 4t .. 4t+3
       const uint32_t wh = (j & 1) ? wv.w : wv.y;  // row g+8
       v[4 * j + 0] = hmul2_u32(hsub2_u32(prmt_u32(wg, 0x64646464u, 0x5150u), za[gg]), sg[gg]);
@@ -300,15 +333,25 @@ __global__ void __launch_bounds__(Cfg<WR, NT, SA, SB, DS, BITS>::kThreads, 1)
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           const int r16 = 2 * q4 + h;
+          if (BITS == 3) {
+            // the pair's 16-byte parts, then its 8-byte parts (768 bytes per pair)
+            if (h == 0) {
+              r.w[0][0] = *reinterpret_cast<const uint4*>(ws + q4 * 768 + lane * 16);
+            } else {
+              const uint2 b2 = *reinterpret_cast<const uint2*>(ws + q4 * 768 + 512 + lane * 8);
+              r.w[1][0] = make_uint4(b2.x, b2.y, 0u, 0u);
+            }
+          } else {
 #pragma unroll
-          for (int part = 0; part < BITS / 4; ++part)
-            r.w[h][part] = *reinterpret_cast<const uint4*>(ws + r16 * WT::kR16 + part * 512 + lane * 16);
+            for (int part = 0; part < kGemmParts<BITS>; ++part)
+              r.w[h][part] = *reinterpret_cast<const uint4*>(ws + r16 * WT::kR16 + part * 512 + lane * 16);
+          }
 #pragma unroll
           for (int gg = 0; gg < StepRegs<GS, SYM, BITS>::kGroups; ++gg) {
             const int gs = min(gg, ng - 1);  // the padding half of a ragged last step reuses the last group
             r.s[h][gg] = *reinterpret_cast<const uint32_t*>(ws + WT::kScaleOff + gs * 256 + (r16 * 8 + g) * 4);
             r.z[h][gg] = SYM ? 0u
-                         : BITS == 4
+                         : BITS != 8
                              ? uint32_t(ws[WT::kZeroOff + gs * 64 + r16 * 8 + g])
                              : uint32_t(*reinterpret_cast<const uint16_t*>(ws + WT::kZeroOff + gs * 128 + (r16 * 8 + g) * 2));
           }
@@ -732,8 +775,9 @@ cudaError_t launch_gemm(const Layout& L, const void* blob, const uint16_t* x, ui
   a.KB = int(L.KB);
   const bool g = L.act || L.awq;
   const int ks = plan.ksplit;
-  return L.bits == 8 ? launch_tile<8>(plan.tile, L, a, xa, M, ks, g, stream)
-                     : launch_tile<4>(plan.tile, L, a, xa, M, ks, g, stream);
+  if (L.bits == 8) return launch_tile<8>(plan.tile, L, a, xa, M, ks, g, stream);
+  if (L.bits == 3) return launch_tile<3>(plan.tile, L, a, xa, M, ks, g, stream);
+  return launch_tile<4>(plan.tile, L, a, xa, M, ks, g, stream);
 }
 
 cudaError_t take_pipeline_timeouts(unsigned int* count) {

@@ -1,14 +1,17 @@
 // Planning and dispatch of the decode-sized product. The kernels live in
-// gemv_impl.cuh; k_gemv_b4.cu and k_gemv_b8.cu compile them for 4-bit and
-// 8-bit codes.
+// gemv_impl.cuh; k_gemv_b3.cu, k_gemv_b4.cu and k_gemv_b8.cu compile them for
+// 3-, 4- and 8-bit codes.
 #include "gemv_impl.cuh"
 
 namespace w4a16 {
 
+cudaError_t launch_gemv_b3(const Layout& L, const void* blob, const uint16_t* x, uint16_t* y, int M,
+                           const GemvPlan& plan, uint32_t flags, cudaStream_t stream);
 cudaError_t launch_gemv_b4(const Layout& L, const void* blob, const uint16_t* x, uint16_t* y, int M,
                            const GemvPlan& plan, uint32_t flags, cudaStream_t stream);
 cudaError_t launch_gemv_b8(const Layout& L, const void* blob, const uint16_t* x, uint16_t* y, int M,
                            const GemvPlan& plan, uint32_t flags, cudaStream_t stream);
+cudaError_t take_gemv_timeouts_b3(unsigned int* count);
 cudaError_t take_gemv_timeouts_b4(unsigned int* count);
 cudaError_t take_gemv_timeouts_b8(unsigned int* count);
 
@@ -56,17 +59,20 @@ GemvPlan gemv_default_plan(const Layout& L, int M, const DeviceInfo& dev, int ki
 
 cudaError_t launch_gemv(const Layout& L, const void* blob, const uint16_t* x, uint16_t* y, int M,
                         const GemvPlan& plan, uint32_t flags, cudaStream_t stream) {
-  return L.bits == 8 ? launch_gemv_b8(L, blob, x, y, M, plan, flags, stream)
-                     : launch_gemv_b4(L, blob, x, y, M, plan, flags, stream);
+  if (L.bits == 8) return launch_gemv_b8(L, blob, x, y, M, plan, flags, stream);
+  if (L.bits == 3) return launch_gemv_b3(L, blob, x, y, M, plan, flags, stream);
+  return launch_gemv_b4(L, blob, x, y, M, plan, flags, stream);
 }
 
 cudaError_t take_gemv_timeouts(unsigned int* count) {
-  unsigned int a = 0, b = 0;
+  unsigned int a = 0, b = 0, c = 0;
   cudaError_t e = take_gemv_timeouts_b4(&a);
   if (e != cudaSuccess) return e;
   e = take_gemv_timeouts_b8(&b);
   if (e != cudaSuccess) return e;
-  *count = a + b;
+  e = take_gemv_timeouts_b3(&c);
+  if (e != cudaSuccess) return e;
+  *count = a + b + c;
   return cudaSuccess;
 }
 

@@ -1,0 +1,13 @@
+// The decode-sized product compiled for 3-bit codes.
+#include "gemv_impl.cuh"
+
+namespace w4a16 {
+
+cudaError_t launch_gemv_b3(const Layout& L, const void* blob, const uint16_t* x, uint16_t* y, int M,
+                           const GemvPlan& plan, uint32_t flags, cudaStream_t stream) {
+  return launch_gemv_bits<3>(L, blob, x, y, M, plan, flags, stream);
+}
+
+cudaError_t take_gemv_timeouts_b3(unsigned int* count) { return take_local_gemv_timeouts(count); }
+
+}  // namespace w4a16

@@ -1,12 +1,12 @@
 // Device layout of the packed blob, shared by the host API and the kernels.
 //
 // The blob holds, each on a 256-byte boundary:
-//   qweight  [NR][KB] tiles of 128 rows x 64 columns of codes: 4096 bytes
-//            (4-bit) or 8192 bytes (8-bit)
+//   qweight  [NR][KB] tiles of 128 rows x 64 columns of codes: 3072 bytes
+//            (3-bit), 4096 bytes (4-bit) or 8192 bytes (8-bit)
 //   scales   [NR][G][8 r16][8 g][2] fp16: for 16-row tile r16 and lane group g
 //            the pair (row r16*16+g, row r16*16+g+8)
-//   zeros    (asymmetric formats only) 4-bit: [NR][G][8 r16][8 g] bytes, low
-//            nibble row r16*16+g, high nibble row r16*16+g+8; 8-bit:
+//   zeros    (asymmetric formats only) 3- and 4-bit: [NR][G][8 r16][8 g]
+//            bytes, low nibble row r16*16+g, high nibble row r16*16+g+8; 8-bit:
 //            [NR][G][8 r16][8 g][2] bytes, row r16*16+g then row r16*16+g+8
 //   perm     [K] int32: packed column -> original column (act order only)
 //   ascale   [K] fp16: per-input-channel activation divisor (unfolded AWQ
@@ -17,6 +17,20 @@
 // p (each part of a warp is 512 contiguous bytes); word (r16, p, L, jj, h)
 // holds the codes of row r16*16 + g + 8h, columns 16*j + 4*t + {0, 1, 2, 3}
 // with j = 2p + jj (byte kk = column 4t + kk).
+//
+// 3-bit codes: the 768 words of a tile are ordered [pair (4)][A: lane (32) x 4]
+// [B: lane (32) x 2], pair p holding 16-row tiles r16 = 2p (h = 0) and 2p + 1
+// (h = 1): a warp's two tiles are one 16-byte and one 8-byte load per lane.
+// Lane L = 4*g + t owns three words of each tile: h = 0: A.x, A.y, A.z;
+// h = 1: A.w, B.x, B.y. The two 16-bit halves of a word belong to the two
+// columns of one m16n8k16 register; each half holds five 3-bit codes at bits
+// 0, 3, 6, 9, 12 and one bit of a sixteenth code at bit 15. Fragment register
+// a of 16-column step j (a = 0: row g, columns 4t, 4t+1; 1: row g+8, same
+// columns; 2: row g, columns 4t+2, 4t+3; 3: row g+8, same) sits in
+//   j < 3: word j at bit {0, 9, 3, 12}[a]
+//   j = 3: a < 3: word a at bit 6; a = 3: bit 15 of words 0, 1, 2 (code bits
+//          0, 1, 2)
+// so (w >> shift) & 0x00070007 is the register's pair of codes.
 //
 // 4-bit codes:
 // Inside a 4096-byte tile the 1024 32-bit words are ordered [r16 (8)][lane (32)][j (4)]:
@@ -45,16 +59,37 @@ constexpr int kScaleBytesPerGroupBlock = 256;
 constexpr int kZeroBytesPerGroupBlock = 64;  // 4-bit; 8-bit zero points take twice as much
 
 __host__ __device__ constexpr int tile_bytes(int bits) { return kTileBytes * bits / 4; }
-__host__ __device__ constexpr int zero_bytes(int bits) { return kZeroBytesPerGroupBlock * bits / 4; }
+__host__ __device__ constexpr int zero_bytes(int bits) { return bits == 8 ? 2 * kZeroBytesPerGroupBlock : kZeroBytesPerGroupBlock; }
 
 __host__ __device__ inline size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
 
 __host__ __device__ inline int nibble_index(int kk, int h) { return (kk & 1) * 4 + (kk >> 1) * 2 + h; }
 
+// 3-bit codes: index, inside a tile, of word wi (0..2) of 16-row tile r16 for a lane.
+__host__ __device__ inline int w3_word_index(int r16, int lane, int wi) {
+  const int base = (r16 >> 1) * 192;
+  if ((r16 & 1) == 0) return base + lane * 4 + wi;
+  return wi == 0 ? base + lane * 4 + 3 : base + 128 + lane * 2 + (wi - 1);
+}
+// Word and bit of fragment register a of step j (a = 3 of step 3 is spread
+// over bit 15 of words 0..2; returns wi = -1 for it).
+__host__ __device__ inline void w3_field(int j, int a, int* wi, int* shift) {
+  if (j < 3) {
+    *wi = j;
+    *shift = a == 0 ? 0 : a == 1 ? 9 : a == 2 ? 3 : 12;
+  } else if (a < 3) {
+    *wi = a;
+    *shift = 6;
+  } else {
+    *wi = -1;
+    *shift = 15;
+  }
+}
+
 struct Layout {
   int64_t N, K, NR, KB, G;
   int gsize;
-  int bits;  // 4 or 8
+  int bits;  // 3, 4 or 8
   bool sym, act, awq;
   size_t q_off, q_bytes, s_off, s_bytes, z_off, z_bytes, p_off, p_bytes, a_off, a_bytes, total;
 };
