@@ -43,11 +43,17 @@ NOMINAL_HBM_GBPS = 8000.0
 # Fallback peaks (one earlier B300 measurement) when the measured file is absent.
 FALLBACK_HBM_GBPS = 6400.0
 FALLBACK_BF16_TFLOPS = 1800.0
-# ncu DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of the GEMV
-# kernel, bytes per launch averaged over one layer's seven launches of the
-# Llama-2-7B sweep (4-bit codes); valid only for the kernel sources it was
-# taken on (GEMV_SOURCES).
-GEMV_TRAFFIC = {"source_sha1": "8f5c0995a1a8d601d2dcce6bdbadec135cd15ee3", "bytes_per_launch": 15054446}
+# ncu DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) per launch of
+# the headline kernel of each schedule on the Llama-2-7B sweep (4-bit codes),
+# {schedule: {"source_sha1", "bytes_per_launch"}}; valid only for the kernel
+# sources it was taken on (GEMV_SOURCES).
+GEMV_TRAFFIC = {}
+SCHEDULE_TEXT = {
+    "chain": ("chain: the step is one persistent launch; q, k, v wait for the previous layer's down, o for "
+              "q..v, gate and up for o, down for gate and up (device completion counters)"),
+    "decode": ("decode: one launch per GEMV; k, v and up do not wait for the GEMV before them (same input); "
+               "q, o, gate, down wait for their predecessor (programmatic dependent launch)"),
+}
 GEMV_SOURCES = ("gemv_impl.cuh", "k_gemv.cu", "k_gemv_b4.cu")
 L2_FLUSH_BYTES = 256 << 20
 
@@ -62,6 +68,8 @@ def parse_args():
     p.add_argument("--no-gemm", action="store_true")
     p.add_argument("--no-shapes", action="store_true")
     p.add_argument("--bits", type=int, default=4, choices=[3, 4, 8], help="code width of every packed linear")
+    p.add_argument("--schedule", default="decode", choices=["chain", "decode"],
+                   help="headline schedule: one chained launch per step, or one launch per GEMV")
     return p.parse_args()
 
 
@@ -244,6 +252,27 @@ def run_ours(args, rank, world, local_rank):
     # none waits (all activations of this workload are precomputed).
     same_input = {"k", "v", "up"}
 
+    # "chain": the whole step as one persistent launch (w4a16_chain_*) with
+    # the data dependencies of a decoder layer: q, k, v read the previous
+    # layer's down output; o waits for q..v; gate and up wait for o; down
+    # waits for gate and up. Strictly more waits than "decode".
+    chain_layers = []
+    for li, lins in enumerate(layers):
+        base = li * len(lins)
+        names = [n for n, _, _ in lins]
+        idx = {n: base + j for j, n in enumerate(names)}
+        for j, (name, fmt, packed) in enumerate(lins):
+            if name in ("q", "k", "v"):
+                wait = None if li == 0 else (base - 1, base - 1)
+            elif name == "o":
+                wait = (idx["q"], idx["v"])
+            elif name in ("gate", "up"):
+                wait = (idx["o"], idx["o"])
+            else:
+                wait = (idx["gate"], idx["up"])
+            chain_layers.append((fmt, packed, xs[fmt.K], ys[li][j], wait))
+    chain = W.Chain(chain_layers, 1)
+
     def sweep(schedule):
         for li, lins in enumerate(layers):
             for j, (name, fmt, packed) in enumerate(lins):
@@ -252,16 +281,17 @@ def run_ours(args, rank, world, local_rank):
 
     stream = torch.cuda.Stream(device=dev)
     graphs = {}
-    for schedule in ("decode", "dependent", "independent"):
+    for schedule in ("chain", "decode", "dependent", "independent"):
+        run = (lambda: chain.run(stream)) if schedule == "chain" else (lambda s=schedule: sweep(s))
         with torch.cuda.stream(stream):
-            sweep(schedule)
+            run()
         torch.cuda.synchronize()
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
-            sweep(schedule)
+            run()
         torch.cuda.synchronize()
         graphs[schedule] = g
-    graph = graphs["decode"]
+    graph = graphs[args.schedule]
 
     # Warm-up, then exactly `steps` timed replays, barrier + synchronize on both sides.
     for _ in range(args.warmup):
@@ -278,13 +308,15 @@ def run_ours(args, rank, world, local_rank):
         ms = float(t.item())
     value = world * step_bytes / (ms * 1e-3) / 1e9
     schedules = {}
-    for schedule in ("dependent", "independent"):
+    for schedule in [s for s in ("chain", "decode", "dependent", "independent") if s != args.schedule]:
         g = graphs[schedule]
         for _ in range(args.warmup):
             g.replay()
         sms = time_graph(torch, g, stream, args.steps)
         schedules[schedule] = {"ms_per_step": round(sms, 4), "GB/s": round(step_bytes / (sms * 1e-3) / 1e9, 1)}
-    schedules["decode"] = {"ms_per_step": round(ms, 4), "GB/s": round(step_bytes / (ms * 1e-3) / 1e9, 1)}
+    schedules[args.schedule] = {"ms_per_step": round(ms, 4), "GB/s": round(step_bytes / (ms * 1e-3) / 1e9, 1)}
+    if W.pipeline_timeouts() != 0:
+        raise RuntimeError("a chained launch gave up a dependency wait")
 
     # End to end through the public API with host buffers: pinned inputs copied
     # in, the step, every output copied back, all inside the timed region.
@@ -323,9 +355,11 @@ def run_ours(args, rank, world, local_rank):
 
     if rank == 0:
         hbm, bf16, peak_kind = measured_peaks()
+        launches = 1 if args.schedule == "chain" else n_launch
         traffic = None
-        if args.bits == 4 and GEMV_TRAFFIC["source_sha1"] == source_sha1(GEMV_SOURCES):
-            traffic = GEMV_TRAFFIC["bytes_per_launch"]
+        ref = GEMV_TRAFFIC.get(args.schedule)
+        if args.bits == 4 and ref and ref["source_sha1"] == source_sha1(GEMV_SOURCES):
+            traffic = ref["bytes_per_launch"]
         per_rank = step_bytes / (ms * 1e-3) / 1e9
         if args.workload == "llama70b":
             workload = ("llama-70b decode weight stream, batch 1: 80 layers x (q,o 8192x8192; k,v 1024x8192; "
@@ -354,19 +388,19 @@ def run_ours(args, rank, world, local_rank):
                        "bytes_per_step": step_bytes, "launches_per_step": n_launch,
                        "l2": f"inputs larger than L2 ({step_bytes / 1e9:.2f} GB of packed weights per step vs 126 MB L2)",
                        "timing": "CUDA graph replay per step, CUDA events on the launching stream",
-                       "schedule": ("decode: k, v and up do not wait for the GEMV before them (same input); "
-                                    "q, o, gate, down wait for their predecessor (programmatic dependent launch)"),
+                       "schedule": SCHEDULE_TEXT[args.schedule],
                        "parallelism": f"replicas x{world}"},
             "pct_of_nominal_hbm": round(100 * per_rank / NOMINAL_HBM_GBPS, 1),
             "roofline": {"bound": "hbm", "achieved": round(per_rank, 1), "peak": hbm, "unit": "GB/s",
                          "frac": round(per_rank / hbm, 4), "traffic": traffic,
-                         "avg_launch_us": round(ms * 1e3 / n_launch, 3),
-                         "alg_bytes_per_launch": round(step_bytes / n_launch),
+                         "avg_launch_us": round(ms * 1e3 / launches, 3),
+                         "alg_bytes_per_launch": round(step_bytes / launches),
                          "peak_source": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)",
-                         "kernel": "gemv_kernel (every launch of the step)"},
+                         "kernel": ("gemv_chain_kernel (one launch per step, after a counter reset)"
+                                    if args.schedule == "chain" else "gemv_kernel (every launch of the step)")},
             "e2e": {"value": round(e2e_value, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)},
-            "gpu_launches": n_launch * args.steps,
+            "gpu_launches": launches * args.steps,
             "clocks": clk.summary(),
             "schedules": schedules,
             "per_shape": shapes,

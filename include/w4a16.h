@@ -257,6 +257,70 @@ W4A16_API w4a16_status w4a16_gemv(const w4a16_format* f, const void* packed, siz
                         const uint16_t* x, uint16_t* y, int64_t M, w4a16_stream_t stream);
 
 /*
+ * Chained decode products: one persistent launch computes y_i = x_i . W_hat_i^T
+ * for a list of layers (1 <= M <= 16 tokens each), e.g. every linear of a
+ * decoder stack for one token step. Each layer is the decode product of
+ * w4a16_gemv, with the same error bound; what the chain adds is the launch:
+ * the per-launch ramp-up and drain of one GEMV per layer ("What W4A16 buys
+ * ...": decode is bandwidth-bound, so idle time between layers is lost
+ * bandwidth) become one stream of weight loads. A work item is 32 rows of a
+ * layer (the full K, split over the warps of a thread block as in
+ * w4a16_gemv); a block claims items in list order, issues an item's first
+ * weight loads, and waits on device-side completion counters only before
+ * reading the item's activations. Results are deterministic.
+ *
+ *   w4a16_chain_layer: packed / packed_bytes (one blob per layer), x
+ *            (fp16 [M][K], 16-byte aligned) and y (fp16 [M][N], 16-byte
+ *            aligned), and the inclusive range [wait_lo, wait_hi] of earlier
+ *            layers (indices < this layer's) whose outputs this layer reads:
+ *            its activations are read only after every one of those layers
+ *            has written all of its y. wait_lo > wait_hi: no dependency (x is
+ *            ready before the launch). Any other overlap between a layer's y
+ *            and another's x or y is the caller's to avoid.
+ *   formats  one w4a16_format per layer. All layers share bits, group_size
+ *            and symmetric; none has act order or an act scale, and K is a
+ *            multiple of 64 (else W4A16_ERR_UNSUPPORTED).
+ *   workspace: >= w4a16_chain_workspace_bytes(formats, n_layers, M) bytes
+ *            (counters and the layer table), 256-byte aligned, device memory
+ *            the chain owns from prepare until the last run; the size is 0
+ *            for an invalid or unsupported list.
+ *
+ * w4a16_chain_prepare validates everything on the host, writes the layer
+ * table into the workspace with a synchronous host-to-device copy, and fills
+ * *info (host memory, caller-owned). w4a16_chain_run then resets the
+ * counters and launches the chain on `stream` (both asynchronous; may be
+ * captured in a CUDA graph). Every dependency wait is bounded (1 s); a wait
+ * that gives up stops the launch, leaves later outputs unwritten and is
+ * counted (w4a16_pipeline_timeouts). The launch needs every thread block
+ * resident at once (cooperative launch); it fails with W4A16_ERR_CUDA rather
+ * than wait if the device cannot host them.
+ */
+typedef struct {
+  const void* packed;
+  size_t packed_bytes;
+  const uint16_t* x;
+  uint16_t* y;
+  int32_t wait_lo;
+  int32_t wait_hi;
+} w4a16_chain_layer;
+
+typedef struct {
+  int32_t n_layers;
+  int32_t bits;
+  int32_t group_size;
+  int32_t symmetric;
+  int64_t M;
+  int64_t total_items;  /* work items (32-row groups) over all layers */
+} w4a16_chain_info;
+
+W4A16_API size_t w4a16_chain_workspace_bytes(const w4a16_format* formats, int32_t n_layers, int64_t M);
+W4A16_API w4a16_status w4a16_chain_prepare(const w4a16_format* formats, const w4a16_chain_layer* layers,
+                                 int32_t n_layers, int64_t M, void* workspace, size_t workspace_bytes,
+                                 w4a16_chain_info* info);
+W4A16_API w4a16_status w4a16_chain_run(const w4a16_chain_info* info, void* workspace,
+                             w4a16_stream_t stream);
+
+/*
  * Prefill-sized product y = x . W_hat^T for M >= 1 tokens on the tcgen05
  * tensor cores ("AWQ + GPTQ Quantization, in depth", section "What W4A16 buys
  * and why decoding gets faster": the 4-bit weights are expanded to 16 bits

@@ -217,3 +217,41 @@ def test_act_scale_format_and_entry_points(lib):
     assert lib.w4a16_gemm_workspace_bytes(ctypes.byref(f), 100) == 100 * 512 * 2
     X, Y = FAKE * 16, FAKE * 4096
     assert lib.w4a16_gemm(ctypes.byref(f), FAKE, nb, X, Y, 100, None, 0, None) == SMALL
+
+
+def test_chain_argument_checks(lib):
+    """The chain's host-side validation, before any device work."""
+    n = 3
+    fmts = (W.Format * n)(*[fmt(256, 512) for _ in range(n)])
+    assert lib.w4a16_chain_workspace_bytes(fmts, 0, 1) == 0
+    assert lib.w4a16_chain_workspace_bytes(fmts, n, 17) == 0
+    nb = lib.w4a16_chain_workspace_bytes(fmts, n, 1)
+    # counters (n + 2) x 128 B, then the layer table
+    assert nb % 256 == 0 and nb >= (n + 2) * 128 + n * 64
+    X, Y = FAKE * 16, FAKE * 64
+
+    def layers(waits, x=X, y=Y, packed=FAKE):
+        return (W.ChainLayer * n)(*[W.ChainLayer(packed, W.packed_bytes(fmts[0]), x, y + i * 4096, lo, hi)
+                                    for i, (lo, hi) in enumerate(waits)])
+
+    info = W.ChainInfo()
+    ok_waits = [(0, -1), (0, 0), (0, 1)]
+    prep = lambda f, l, M=1, ws=FAKE, wsb=nb: lib.w4a16_chain_prepare(f, l, n, M, ws, wsb, ctypes.byref(info))
+    assert prep(fmts, layers([(0, -1), (1, 1), (0, 1)])) == INVALID    # waits on itself
+    assert prep(fmts, layers([(0, 0), (0, 0), (0, 1)])) == INVALID     # first layer waits on itself
+    assert prep(fmts, layers([(0, -1), (-1, 0), (0, 1)])) == INVALID   # negative index
+    assert prep(fmts, layers(ok_waits), M=0) == INVALID
+    assert prep(fmts, layers(ok_waits), M=17) == INVALID
+    assert prep(fmts, layers(ok_waits), ws=FAKE + 16) == MISALIGNED
+    assert prep(fmts, layers(ok_waits), wsb=nb - 1) == SMALL
+    assert prep(fmts, layers(ok_waits, x=X + 2)) == MISALIGNED
+    assert prep(fmts, layers(ok_waits, packed=FAKE + 128)) == MISALIGNED
+    assert prep(fmts, layers(ok_waits, y=X)) == INVALID                 # y overlaps x
+    mixed = (W.Format * n)(fmt(256, 512), fmt(256, 512, bits=8), fmt(256, 512))
+    assert prep(mixed, layers(ok_waits)) == UNSUPPORTED
+    act = (W.Format * n)(fmt(256, 512), fmt(256, 512, act=True), fmt(256, 512))
+    assert prep(act, layers(ok_waits)) == UNSUPPORTED
+    ragged = (W.Format * n)(fmt(256, 512), fmt(256, 96, g=32), fmt(256, 512))
+    assert prep(ragged, layers(ok_waits)) == UNSUPPORTED               # K not a multiple of 64
+    bad = W.ChainInfo(n, 4, 128, 0, 1, 0)
+    assert lib.w4a16_chain_run(ctypes.byref(bad), FAKE, None) == INVALID  # no work items

@@ -48,7 +48,9 @@
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cmath>
+#include <type_traits>
 
 #include "device_util.cuh"
 #include "internal.h"
@@ -180,11 +182,21 @@ __device__ __forceinline__ void extract_step(const uint4 (&wb)[2][kParts<BITS>],
   }
 }
 
-template <bool SMEM>
+// Where the activations are read from: the read-only path (x is constant for
+// the kernel), shared memory (staged), or ordinary global loads (x may have
+// been written earlier by other blocks of the same chained launch, so the
+// read-only path is not allowed; these loads follow an acquire of the
+// producer's counter by thread 0 and a block barrier, which makes the
+// producer's writes visible to them).
+constexpr int kXGlobal = 0, kXShared = 1, kXCoherent = 2;
+template <int XM>
 __device__ __forceinline__ uint2 ld_x(const uint16_t* p) {
-  if (SMEM) return *reinterpret_cast<const uint2*>(p);
+  if (XM == kXShared) return *reinterpret_cast<const uint2*>(p);
   uint2 v;
-  asm volatile("ld.global.nc.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
+  if (XM == kXCoherent)
+    asm volatile("ld.global.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p) : "memory");
+  else
+    asm volatile("ld.global.nc.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
   return v;
 }
 
@@ -266,7 +278,7 @@ __device__ __forceinline__ void load_unit(UnitRegs<GS, BITS>& r, const uint32_t*
 
 // Multiply-accumulate one unit. xl0 / xl1 point at this lane's x fragment
 // (token rows g and g+8, column 4t) for the unit's first column.
-template <int NB, int GS, bool SYM, bool STAGED, int BITS>
+template <int NB, int GS, bool SYM, int XM, int BITS>
 __device__ __forceinline__ void compute_unit(const UnitRegs<GS, BITS>& r, const uint16_t* xl0, const uint16_t* xl1,
                                              float tot[kTilesPerWarp][NB][4]) {
   using U = Unit<GS>;
@@ -280,8 +292,8 @@ __device__ __forceinline__ void compute_unit(const UnitRegs<GS, BITS>& r, const 
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const int off = bb * 64 + j * 16;
-      bx[j][0] = ld_x<STAGED>(xl0 + off);
-      if (NB > 1) bx[j][NB - 1] = ld_x<STAGED>(xl1 + off);
+      bx[j][0] = ld_x<XM>(xl0 + off);
+      if (NB > 1) bx[j][NB - 1] = ld_x<XM>(xl1 + off);
     }
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
@@ -536,7 +548,7 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const GemvArgs a) {
                                zshift) & (BITS != 8 ? 0xFFu : 0xFFFFu);
         }
       const int xo = i * U::kBlocks * kColsPerBlock;
-      compute_unit<NB, GS, SYM, STAGED, BITS>(r, xl0 + xo, xl1 + xo, tot);
+      compute_unit<NB, GS, SYM, STAGED ? kXShared : kXGlobal, BITS>(r, xl0 + xo, xl1 + xo, tot);
       issue_unit(i + D);  // refills the slot just read (this thread's own entries)
     }
     cp_async_wait_all();
@@ -547,7 +559,7 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const GemvArgs a) {
         const int i = i0 + s;
         if (i < nunit) {
           const int xo = i * U::kBlocks * kColsPerBlock;
-          compute_unit<NB, GS, SYM, STAGED, BITS>(ring[s], xl0 + xo, xl1 + xo, tot);
+          compute_unit<NB, GS, SYM, STAGED ? kXShared : kXGlobal, BITS>(ring[s], xl0 + xo, xl1 + xo, tot);
           if (i + PF < nunit) load_unit<GS, SYM, BITS>(ring[s], qp, sp, zp, i + PF, gmax);
         }
       }
@@ -744,6 +756,246 @@ cudaError_t launch_gemv_bits(const Layout& L, const void* blob, const uint16_t* 
   if (M <= 4) return launch_gs<4, BITS>(a, gs, L.sym, ring_staged, wb, plan.ksplit, smem, stream);
   if (M <= 8) return launch_gs<8, BITS>(a, gs, L.sym, ring_staged, wb, plan.ksplit, smem, stream);
   return launch_gs<16, BITS>(a, gs, L.sym, ring_staged, wb, plan.ksplit, smem, stream);
+}
+
+// ---------------------------------------------------------------------------
+// Chained products: one persistent launch over the work items of a list of
+// layers (item = 32 rows of one layer, the full K split over the 8 warps,
+// weights through the asynchronous-copy ring). Blocks claim items in list
+// order from a device counter; before reading its activations an item waits
+// until every item of the layers it depends on has finished (device
+// counters, bounded wait), with its first ring slots already in flight.
+// Every block is resident (cooperative launch), items are claimed in order
+// and dependencies point to earlier layers only, so the lowest unfinished
+// item can always make progress.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ unsigned int ld_acquire_u32(const unsigned int* p) {
+  unsigned int v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void red_release_add_u32(unsigned int* p, unsigned int v) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+// Counters of a chain, each in its own 128-byte line (polled by many blocks).
+constexpr int kChainCounterStride = 32;
+
+template <int MP, int GS, bool SYM, int BITS>
+__global__ void __launch_bounds__(kThreads) gemv_chain_kernel(const ChainLaunch c) {
+  // dynamic shared memory: the asynchronous-copy ring; after an item's last
+  // unit it holds the cross-warp reduction ([warp][32 rows][16 tokens] fp32)
+  extern __shared__ __align__(128) unsigned char smem[];
+  __shared__ int s_item, s_abort;
+  constexpr int NB = MP > 8 ? 2 : 1;
+  using U = Unit<GS>;
+  using CW = CodeWords<BITS>;
+  using SL = WbSlot<GS, BITS>;
+  constexpr int D = kWbSlots<BITS>;
+  constexpr int CS = kChainCounterStride;
+  static_assert(kWarps * 512 * 4 <= D * SL::kBytes, "the reduction fits in the ring");
+  const int tid = int(threadIdx.x);
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  const int g = lane >> 2, t = lane & 3;
+  const int M = c.M;
+  const ChainJob* __restrict__ jobs = c.jobs;
+  unsigned int* done = c.done;
+  unsigned int* abort_flag = done + size_t(c.n_jobs) * CS;
+  unsigned int* next_item = done + size_t(c.n_jobs + 1) * CS;
+  float* red_w = reinterpret_cast<float*>(smem);
+  int j = 0;
+  // Items are claimed in increasing order, so every item a block waits for
+  // was claimed earlier by a resident block. The next item is claimed once
+  // the current one no longer waits (its claim latency hides behind the
+  // current item's work).
+  if (tid == 0) s_item = int(atomicAdd(next_item, 1u));
+  __syncthreads();
+  int item = s_item;
+  while (item < c.total_items) {
+    while (j + 1 < c.n_jobs && item >= jobs[j + 1].item0) ++j;
+    const ChainJob& J = jobs[j];
+    const int rg = item - J.item0;
+    const int R = rg >> 2, r16 = (rg & 3) * 2;
+    const int units = (J.KB + U::kBlocks - 1) / U::kBlocks;
+    const int u0 = (units * warp) / kWarps;
+    const int nunit = (units * (warp + 1)) / kWarps - u0;
+    const int G = J.G;
+    const int gmax = G - 1 - u0 * U::kGroups;
+    const uint32_t* qp = J.qweight + (size_t(R) * J.KB * 8 + r16) * CW::kRow16 + lane * 4 +
+                         size_t(u0) * U::kBlocks * CW::kBlock;
+    const uint32_t* sp = J.scales2 + (size_t(R) * G * 8 + r16) * 8 + g + size_t(u0) * U::kGroups * 64;
+    const uint8_t* zp =
+        SYM ? nullptr : J.zeros + ((size_t(R) * G * 8 + r16) * 8 + g + size_t(u0) * U::kGroups * 64) * kZeroMul<BITS>;
+
+    auto issue_unit = [&](int i) {  // unit u0 + i into slot i % D: this thread's own entries
+      if (i < nunit) {
+        unsigned char* slot = smem + size_t(i % D) * SL::kBytes;
+#pragma unroll
+        for (int bb = 0; bb < U::kBlocks; ++bb)
+#pragma unroll
+          for (int tt = 0; tt < kTilesPerWarp; ++tt)
+#pragma unroll
+            for (int part = 0; part < kParts<BITS>; ++part) {
+              unsigned char* dst = slot + (((bb * kTilesPerWarp + tt) * kParts<BITS> + part) * kThreads + tid) * 16;
+              const uint32_t* src = qp + (i * U::kBlocks + bb) * CW::kBlock + CW::off(tt, part, lane);
+              if (CW::narrow(tt))
+                cp_async_8(dst, src);
+              else
+                cp_async_16(dst, src);
+            }
+#pragma unroll
+        for (int gg = 0; gg < U::kGroups; ++gg) {
+          const int gi = GS == 32 ? min(i * U::kGroups + gg, gmax) : i * U::kGroups + gg;
+#pragma unroll
+          for (int tt = 0; tt < kTilesPerWarp; ++tt) {
+            const int f = gg * kTilesPerWarp + tt;
+            cp_async_4(slot + SL::kScaleOff + (f * kThreads + tid) * 4, sp + gi * 64 + tt * 8);
+            if (!SYM)
+              cp_async_4(slot + SL::kZeroOff + (f * kThreads + tid) * 4,
+                         reinterpret_cast<const uint32_t*>(
+                             reinterpret_cast<uintptr_t>(zp + (gi * 64 + tt * 8) * kZeroMul<BITS>) & ~uintptr_t(3)));
+          }
+        }
+      }
+      cp_async_commit();
+    };
+#pragma unroll
+    for (int i = 0; i < D; ++i) issue_unit(i);  // weights first: they do not depend on earlier layers
+
+    if (J.wait_lo <= J.wait_hi) {
+      if (tid == 0) {
+        int ok = 1;
+        const uint64_t t0 = global_timer_ns();
+        for (int d = J.wait_lo; d <= J.wait_hi && ok; ++d) {
+          const unsigned int need = unsigned(jobs[d].items);
+          for (int spin = 0; ld_acquire_u32(done + size_t(d) * CS) < need; ++spin) {
+            if ((spin & 15) == 15 && ld_acquire_u32(abort_flag) != 0) {
+              ok = 0;
+              break;
+            }
+            if (global_timer_ns() - t0 > kTWaitLimitNs) {
+              atomicAdd(&g_gemv_timeouts, 1u);
+              atomicExch(abort_flag, 1u);
+              ok = 0;
+              break;
+            }
+            __nanosleep(128);
+          }
+        }
+        s_abort = ok ? 0 : 1;
+      }
+      __syncthreads();  // also orders the activation loads below after thread 0's acquire
+      if (s_abort) {  // a wait gave up somewhere: every block stops
+        cp_async_wait_all();
+        break;
+      }
+    }
+    unsigned int claimed = 0;
+    if (tid == 0) claimed = atomicAdd(next_item, 1u);
+
+    const int tok0 = min(g, M - 1), tok1 = min(g + 8, M - 1);
+    const int c0 = u0 * U::kBlocks * kColsPerBlock + 4 * t;
+    const uint16_t* xl0 = J.x + size_t(tok0) * J.K + c0;
+    const uint16_t* xl1 = J.x + size_t(tok1) * J.K + c0;
+    float tot[kTilesPerWarp][NB][4];
+#pragma unroll
+    for (int tt = 0; tt < kTilesPerWarp; ++tt)
+#pragma unroll
+      for (int nb = 0; nb < NB; ++nb)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) tot[tt][nb][i] = 0.f;
+    const int zshift = int((reinterpret_cast<uintptr_t>(zp) & 3u) * 8);
+    for (int i = 0; i < nunit; ++i) {
+      cp_async_wait_group<D - 1>();  // unit i has landed (this thread's copies)
+      const unsigned char* slot = smem + size_t(i % D) * SL::kBytes;
+      UnitRegs<GS, BITS> r;
+#pragma unroll
+      for (int bb = 0; bb < U::kBlocks; ++bb)
+#pragma unroll
+        for (int tt = 0; tt < kTilesPerWarp; ++tt)
+#pragma unroll
+          for (int part = 0; part < kParts<BITS>; ++part)
+            r.w[bb][tt][part] = *reinterpret_cast<const uint4*>(
+                slot + (((bb * kTilesPerWarp + tt) * kParts<BITS> + part) * kThreads + tid) * 16);
+#pragma unroll
+      for (int gg = 0; gg < U::kGroups; ++gg)
+#pragma unroll
+        for (int tt = 0; tt < kTilesPerWarp; ++tt) {
+          const int f = gg * kTilesPerWarp + tt;
+          r.s[gg][tt] = *reinterpret_cast<const uint32_t*>(slot + SL::kScaleOff + (f * kThreads + tid) * 4);
+          r.z[gg][tt] = SYM ? 0u
+                            : (*reinterpret_cast<const uint32_t*>(slot + SL::kZeroOff + (f * kThreads + tid) * 4) >>
+                               zshift) & (BITS != 8 ? 0xFFu : 0xFFFFu);
+        }
+      const int xo = i * U::kBlocks * kColsPerBlock;
+      compute_unit<NB, GS, SYM, kXCoherent, BITS>(r, xl0 + xo, xl1 + xo, tot);
+      issue_unit(i + D);
+    }
+    cp_async_wait_all();
+    __syncthreads();  // every thread is done with the ring: it becomes the reduction buffer
+
+#pragma unroll
+    for (int tt = 0; tt < kTilesPerWarp; ++tt)
+#pragma unroll
+      for (int nb = 0; nb < NB; ++nb) {
+        const int tk = nb * 8 + 2 * t;
+        float* rw = red_w + warp * 512 + tt * 256;
+        rw[g * 16 + tk] = tot[tt][nb][0];
+        rw[g * 16 + tk + 1] = tot[tt][nb][1];
+        rw[(g + 8) * 16 + tk] = tot[tt][nb][2];
+        rw[(g + 8) * 16 + tk + 1] = tot[tt][nb][3];
+      }
+    __syncthreads();
+    for (int e = tid; e < 32 * M; e += kThreads) {
+      const int tok = e >> 5, rr = e & 31;
+      float acc = 0.f;
+#pragma unroll
+      for (int k = 0; k < kWarps; ++k) acc += red_w[k * 512 + rr * 16 + tok];
+      const int n = R * kRowsPerBlock + r16 * 16 + rr;
+      if (n < J.N) J.y[size_t(tok) * J.N + n] = __half_as_ushort(__float2half_rn(acc));
+    }
+    if (tid == 0) s_item = int(claimed);
+    __syncthreads();  // every output of the item is written (and the ring is free again)
+    if (tid == 0) red_release_add_u32(done + size_t(j) * CS, 1u);  // publishes them device-wide
+    item = s_item;
+  }
+}
+
+template <int BITS>
+cudaError_t launch_chain_bits(const ChainLaunch& c, cudaStream_t stream) {
+  void (*kern)(const ChainLaunch) = nullptr;
+  auto pick = [&](auto mp) {
+    constexpr int MP = decltype(mp)::value;
+    if (c.gsize == 32) kern = c.sym ? gemv_chain_kernel<MP, 32, true, BITS> : gemv_chain_kernel<MP, 32, false, BITS>;
+    else if (c.gsize == 64) kern = c.sym ? gemv_chain_kernel<MP, 64, true, BITS> : gemv_chain_kernel<MP, 64, false, BITS>;
+    else kern = c.sym ? gemv_chain_kernel<MP, 128, true, BITS> : gemv_chain_kernel<MP, 128, false, BITS>;
+  };
+  if (c.M <= 1) pick(std::integral_constant<int, 1>{});
+  else if (c.M <= 2) pick(std::integral_constant<int, 2>{});
+  else if (c.M <= 4) pick(std::integral_constant<int, 4>{});
+  else if (c.M <= 8) pick(std::integral_constant<int, 8>{});
+  else pick(std::integral_constant<int, 16>{});
+  const int smem = kWbSlots<BITS> * wb_slot_bytes(c.gsize, BITS);
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  int per_sm = 0;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem);
+  if (e != cudaSuccess) return e;
+  if (per_sm < 1) return cudaErrorInvalidConfiguration;
+  const int grid = std::min(c.total_items, per_sm * c.sm_count);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(unsigned(grid), 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = size_t(smem);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;  // every block resident at once
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, kern, c);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
 }
 
 // This translation unit's timeout counter (read and cleared).

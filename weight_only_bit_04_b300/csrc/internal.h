@@ -64,6 +64,32 @@ bool gemm_plan_ok(const Layout& L, const GemmPlan& p);
 cudaError_t launch_gemm(const Layout& L, const void* blob, const uint16_t* x, uint16_t* y,
                         int64_t M, void* workspace, const GemmPlan& plan, cudaStream_t stream);
 
+// Chained decode products (w4a16_chain_*): one persistent launch runs a list
+// of layers. Work item = one 32-row group of a layer (the full K); a layer's
+// items wait for the completion counters of the layers whose outputs they
+// read.
+struct ChainJob {
+  const uint32_t* qweight;
+  const uint32_t* scales2;
+  const uint8_t* zeros;  // nullptr when symmetric
+  const uint16_t* x;
+  uint16_t* y;
+  int N, K, G, KB;
+  int item0, items;      // first global work item and count (32-row groups)
+  int wait_lo, wait_hi;  // layers this layer waits for (none when wait_lo > wait_hi)
+};
+struct ChainLaunch {
+  int bits, gsize, M;
+  bool sym;
+  int n_jobs;
+  int total_items;
+  int sm_count;
+  const ChainJob* jobs;  // device table
+  unsigned int* done;    // per layer a count of finished items, then the abort flag and the next-item
+                         // counter, each in its own 128-byte line
+};
+cudaError_t launch_chain(const ChainLaunch& c, cudaStream_t stream);
+
 // Device-side counts of bounded pipeline waits that gave up, read and reset
 // (k_gemm.cu for the GEMM, k_gemv.cu for the bulk-copy GEMV).
 cudaError_t take_pipeline_timeouts(unsigned int* count);

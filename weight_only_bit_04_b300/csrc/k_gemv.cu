@@ -11,6 +11,9 @@ cudaError_t launch_gemv_b4(const Layout& L, const void* blob, const uint16_t* x,
                            const GemvPlan& plan, uint32_t flags, cudaStream_t stream);
 cudaError_t launch_gemv_b8(const Layout& L, const void* blob, const uint16_t* x, uint16_t* y, int M,
                            const GemvPlan& plan, uint32_t flags, cudaStream_t stream);
+cudaError_t launch_chain_b3(const ChainLaunch& c, cudaStream_t stream);
+cudaError_t launch_chain_b4(const ChainLaunch& c, cudaStream_t stream);
+cudaError_t launch_chain_b8(const ChainLaunch& c, cudaStream_t stream);
 cudaError_t take_gemv_timeouts_b3(unsigned int* count);
 cudaError_t take_gemv_timeouts_b4(unsigned int* count);
 cudaError_t take_gemv_timeouts_b8(unsigned int* count);
@@ -62,6 +65,12 @@ cudaError_t launch_gemv(const Layout& L, const void* blob, const uint16_t* x, ui
   if (L.bits == 8) return launch_gemv_b8(L, blob, x, y, M, plan, flags, stream);
   if (L.bits == 3) return launch_gemv_b3(L, blob, x, y, M, plan, flags, stream);
   return launch_gemv_b4(L, blob, x, y, M, plan, flags, stream);
+}
+
+cudaError_t launch_chain(const ChainLaunch& c, cudaStream_t stream) {
+  if (c.bits == 8) return launch_chain_b8(c, stream);
+  if (c.bits == 3) return launch_chain_b3(c, stream);
+  return launch_chain_b4(c, stream);
 }
 
 cudaError_t take_gemv_timeouts(unsigned int* count) {

@@ -8,6 +8,8 @@ cudaError_t launch_gemv_b4(const Layout& L, const void* blob, const uint16_t* x,
   return launch_gemv_bits<4>(L, blob, x, y, M, plan, flags, stream);
 }
 
+cudaError_t launch_chain_b4(const ChainLaunch& c, cudaStream_t stream) { return launch_chain_bits<4>(c, stream); }
+
 cudaError_t take_gemv_timeouts_b4(unsigned int* count) { return take_local_gemv_timeouts(count); }
 
 }  // namespace w4a16

@@ -59,6 +59,32 @@ class Format(ctypes.Structure):
 
 _FP = ctypes.POINTER(Format)
 
+
+class ChainLayer(ctypes.Structure):
+    """Mirror of ``w4a16_chain_layer``."""
+
+    _fields_ = [
+        ("packed", ctypes.c_void_p),
+        ("packed_bytes", ctypes.c_size_t),
+        ("x", ctypes.c_void_p),
+        ("y", ctypes.c_void_p),
+        ("wait_lo", ctypes.c_int32),
+        ("wait_hi", ctypes.c_int32),
+    ]
+
+
+class ChainInfo(ctypes.Structure):
+    """Mirror of ``w4a16_chain_info``."""
+
+    _fields_ = [
+        ("n_layers", ctypes.c_int32),
+        ("bits", ctypes.c_int32),
+        ("group_size", ctypes.c_int32),
+        ("symmetric", ctypes.c_int32),
+        ("M", ctypes.c_int64),
+        ("total_items", ctypes.c_int64),
+    ]
+
 SIGNATURES = {
     "w4a16_packed_bytes": (_SZ, [_FP]),
     "w4a16_check_format": (ctypes.c_int, [_FP]),
@@ -77,6 +103,10 @@ SIGNATURES = {
     "w4a16_gemm": (ctypes.c_int, [_FP, _P, _SZ, _P, _P, _I64, _P, _SZ, _P]),
     "w4a16_gemm_ex": (ctypes.c_int, [_FP, _P, _SZ, _P, _P, _I64, _P, _SZ, _I32, _I32, _P]),
     "w4a16_pipeline_timeouts": (ctypes.c_int, [ctypes.POINTER(ctypes.c_uint32)]),
+    "w4a16_chain_workspace_bytes": (_SZ, [_FP, _I32, _I64]),
+    "w4a16_chain_prepare": (ctypes.c_int, [_FP, ctypes.POINTER(ChainLayer), _I32, _I64, _P, _SZ,
+                                           ctypes.POINTER(ChainInfo)]),
+    "w4a16_chain_run": (ctypes.c_int, [ctypes.POINTER(ChainInfo), _P, _P]),
 }
 
 _lib = None
@@ -330,3 +360,42 @@ class W4A16Linear:
 
     def __call__(self, x: torch.Tensor, out=None) -> torch.Tensor:
         return linear(self.fmt, self.packed, x, out=out)
+
+
+class Chain:
+    """A list of decode products run by one persistent launch (``w4a16_chain_*``).
+
+    ``layers``: sequence of (fmt, packed, x, y, (wait_lo, wait_hi)) -- x fp16
+    [M, K] and y fp16 [M, N] device tensors; the wait range names earlier
+    layers whose outputs this layer reads (``None`` or an empty range: none).
+    The tensors must stay alive as long as the chain is run.
+    """
+
+    def __init__(self, layers, M: int):
+        n = len(layers)
+        self.n = n
+        fmts = (Format * n)()
+        table = (ChainLayer * n)()
+        keep = []
+        for i, (fmt, packed, x, y, wait) in enumerate(layers):
+            fmts[i] = fmt
+            pp = _dev(packed, torch.uint8, "packed")
+            xp = _dev(x, torch.float16, "x", (M, fmt.K))
+            yp = _dev(y, torch.float16, "y", (M, fmt.N))
+            lo, hi = (0, -1) if wait is None else wait
+            table[i] = ChainLayer(pp, packed.numel(), xp, yp, lo, hi)
+            keep.append((packed, x, y))
+        self._keep = keep
+        nbytes = int(lib().w4a16_chain_workspace_bytes(fmts, n, M))
+        if nbytes == 0:
+            raise ValueError("invalid or unsupported layer list for a chain")
+        dev = layers[0][1].device
+        self.workspace = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+        self.info = ChainInfo()
+        st = lib().w4a16_chain_prepare(fmts, table, n, M, self.workspace.data_ptr(), nbytes,
+                                       ctypes.byref(self.info))
+        _check("w4a16_chain_prepare", st)
+
+    def run(self, stream=None):
+        st = lib().w4a16_chain_run(ctypes.byref(self.info), self.workspace.data_ptr(), _stream(stream))
+        _check("w4a16_chain_run", st)
