@@ -54,6 +54,16 @@ What it computes, step by step, and where each step comes from:
    from a grid over [0, 1], keep the alpha with the smallest output error)
    produces s from calibration activations.
 
+8. GPTQ ("The two algorithms, compactly"): H = 2 X X^T over the calibration
+   inputs, H += damp * mean(diag H) * I (damp 0.01), Hinv = the upper
+   Cholesky factor U of H^-1 (H^-1 = U^T U); columns are taken in order (act
+   order: by descending diag H); each column is quantized to its group's
+   grid, err = (w_j - q_j) / U[j, j] and the columns not yet quantized get
+   W[:, j+1:] -= err U[j, j+1:]. A group's scale and zero point are set when
+   its first column is reached, from the current (already updated) weights
+   of its columns; under act order the groups are runs of group_size
+   columns in processing order.
+
 No blocking, fusion or reordering beyond these definitions; library matmuls
 (``@``) are used for the sums.
 """
@@ -412,3 +422,93 @@ def awq_search(W, x, group_size: int, sym: bool, bits: int = 4, n_grid: int = 20
         if best is None or loss < best[0]:
             best = (loss, s16, float(alpha))
     return best[1], best[2], np.array(losses)
+
+
+# ---------------------------------------------------------------------------
+# Step 8: GPTQ -- quantize one column at a time, push the error onto the rest
+# ---------------------------------------------------------------------------
+GPTQ_DAMP = 0.01
+
+
+def gptq_hessian(x) -> np.ndarray:
+    """H = 2 X X^T with X = x^T (in x tokens): [K, K] fp64."""
+    xd = np.asarray(x, dtype=np.float64)
+    return 2.0 * (xd.T @ xd)
+
+
+def gptq_order(H, act_order: bool) -> np.ndarray:
+    """Processing order: natural, or by descending diag(H), ties to the lower column."""
+    K = H.shape[0]
+    if not act_order:
+        return np.arange(K, dtype=np.int64)
+    return np.argsort(-np.diag(H), kind="stable").astype(np.int64)
+
+
+def gptq_damped(H, damp: float = GPTQ_DAMP) -> np.ndarray:
+    """H + damp * mean(diag H) * I. A zero diagonal (a channel that never
+    fires) is set to 1 first so that H stays invertible; its weights get no
+    error feedback from other columns and none of theirs."""
+    H = np.array(H, dtype=np.float64, copy=True)
+    dead = np.diag(H) == 0
+    H[dead, :] = 0.0
+    H[:, dead] = 0.0
+    H[dead, dead] = 1.0
+    H += damp * np.mean(np.diag(H)) * np.eye(H.shape[0])
+    return H
+
+
+def gptq_factor(Hd) -> np.ndarray:
+    """The upper Cholesky factor U of H^-1 (H^-1 = U^T U)."""
+    Hinv = np.linalg.inv(Hd)
+    return np.linalg.cholesky(Hinv).T  # cholesky gives lower L with Hinv = L L^T; U = L^T
+
+
+def gptq_quantize(W, x, group_size: int, sym: bool, bits: int = 4, act_order: bool = False,
+                  damp: float = GPTQ_DAMP):
+    """GPTQ of fp16 W [N, K] with calibration activations x [tokens, K].
+
+    Returns (q uint8 [N, K] in original column order, scales fp16 [N, G],
+    zeros uint8 [N, G], g_idx int64 [K] or None). Group t of the returned
+    format holds the columns processed in positions t*g .. t*g+g-1.
+    """
+    W = np.asarray(W)
+    if W.dtype != np.float16:
+        raise TypeError("W must be float16")
+    N, K = W.shape
+    if K % group_size:
+        raise ValueError("K must be a multiple of group_size")
+    H = gptq_hessian(x)
+    order = gptq_order(H, act_order)
+    Hd = gptq_damped(H, damp)[np.ix_(order, order)]
+    U = gptq_factor(Hd)
+    Wp = W.astype(np.float64)[:, order]  # working copy, processing order
+    G = K // group_size
+    q = np.zeros((N, K), dtype=np.uint8)
+    scales = np.zeros((N, G), dtype=np.float16)
+    zeros = np.zeros((N, G), dtype=np.uint8)
+    for j in range(K):
+        t = j // group_size
+        if j % group_size == 0:
+            s, z = group_scale_zero(Wp[:, j:j + group_size], sym, bits)
+            scales[:, t], zeros[:, t] = s, z
+        sd = scales[:, t].astype(np.float64)
+        zd = zeros[:, t].astype(np.float64)
+        w = Wp[:, j]
+        qj = sym8_codes(w[:, None], sd[:, None])[:, 0] if (sym and bits == 8) else \
+            quantize_codes(w, sd, zd, bits)
+        wq = (qj.astype(np.float64) - zd) * sd  # the grid point (exact in fp64)
+        err = (w - wq) / U[j, j]
+        Wp[:, j + 1:] -= np.outer(err, U[j, j + 1:])
+        Wp[:, j] = wq
+        q[:, order[j]] = qj
+    g_idx = None
+    if act_order:
+        g_idx = np.empty(K, dtype=np.int64)
+        g_idx[order] = np.arange(K) // group_size
+    return q, scales, zeros, g_idx
+
+
+def layer_error(W, w_hat, x) -> float:
+    """||x W^T - x w_hat^T||_F, the quantity both calibration methods reduce."""
+    xd = np.asarray(x, dtype=np.float64)
+    return float(np.linalg.norm(xd @ np.asarray(W, np.float64).T - xd @ np.asarray(w_hat, np.float64).T))
