@@ -229,6 +229,36 @@ W4A16_API w4a16_status w4a16_pack_awq(const w4a16_format* f, const uint8_t* q, c
                         void* packed, size_t packed_bytes, w4a16_stream_t stream);
 
 /*
+ * GPTQ ("AWQ + GPTQ Quantization, in depth", section "The two algorithms,
+ * compactly"): quantize the layer one input column at a time, pushing each
+ * column's rounding error onto the columns not yet quantized, weighted by the
+ * inverse of H = 2 X X^T of the calibration activations. On the device, in
+ * fp64: H, H += damp * mean(diag H) * I (a channel whose activations are all
+ * zero gets diag 1 first), the upper Cholesky factor U of H^-1, then per
+ * column j (in order, or -- f->has_g_idx -- by descending diag H, ties to the
+ * lower column) q_j = the group's grid point of the current w_j,
+ * W[:, j+1:] -= (w_j - q_j) / U[j, j] * U[j, j+1:]. A group's scale and zero
+ * point are set when its first column is reached, from the current weights of
+ * its columns, with the round-to-nearest rules of w4a16_quantize_rtn.
+ *   w        fp16 [N][K], 2-byte aligned (read only).
+ *   x        fp16 [T][K] calibration activations, 1 <= T <= 2^24.
+ *   damp     >= 0 (0.01 on the page).
+ *   q, scales, zeros   as from w4a16_quantize_rtn (codes in original column
+ *            order; group t = the t-th run of group_size columns in
+ *            processing order).
+ *   g_idx    device int32 [K] (written) when f->has_g_idx -- the act-order
+ *            column-to-group map to give w4a16_pack (copied to the host) --,
+ *            else NULL.
+ *   workspace: >= w4a16_gptq_workspace_bytes(f) (2 K^2 + N K doubles and a
+ *            little more), 256-byte aligned.
+ * Asynchronous on `stream`. Formats with an act scale: W4A16_ERR_UNSUPPORTED.
+ */
+W4A16_API size_t w4a16_gptq_workspace_bytes(const w4a16_format* f);
+W4A16_API w4a16_status w4a16_gptq(const w4a16_format* f, const uint16_t* w, const uint16_t* x, int64_t T,
+                        double damp, uint8_t* q, uint16_t* scales, uint8_t* zeros, int32_t* g_idx,
+                        void* workspace, size_t workspace_bytes, w4a16_stream_t stream);
+
+/*
  * Expand the blob to fp16 weights: w_out[n][k] = fp16_rne((q - z) * s), in
  * the original column order; bit-exact ("The Math of Quantization":
  * x_approx = (q - Z) * S, rounded once to fp16).

@@ -3,6 +3,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <cmath>
 #include <atomic>
 #include <cstdint>
 #include <cstring>
@@ -316,6 +317,30 @@ w4a16_status w4a16_gemm_ex(const w4a16_format* f, const void* packed, size_t pac
                            const uint16_t* x, uint16_t* y, int64_t M, void* workspace,
                            size_t workspace_bytes, int32_t tile, int32_t ksplit, w4a16_stream_t stream) {
   return gemm_common(f, packed, packed_bytes, x, y, M, workspace, workspace_bytes, tile, ksplit, stream);
+}
+
+size_t w4a16_gptq_workspace_bytes(const w4a16_format* f) {
+  if (format_status(f) != W4A16_OK || f->has_act_scale) return 0;
+  return gptq_workspace_bytes(f->N, f->K);
+}
+
+w4a16_status w4a16_gptq(const w4a16_format* f, const uint16_t* w, const uint16_t* x, int64_t T, double damp,
+                        uint8_t* q, uint16_t* scales, uint8_t* zeros, int32_t* g_idx, void* workspace,
+                        size_t workspace_bytes, w4a16_stream_t stream) {
+  w4a16_status s = format_status(f);
+  if (s != W4A16_OK) return s;
+  if (f->has_act_scale) return W4A16_ERR_UNSUPPORTED;
+  if (w == nullptr || x == nullptr || q == nullptr || scales == nullptr || workspace == nullptr)
+    return W4A16_ERR_INVALID_ARG;
+  if ((zeros == nullptr) != (f->symmetric != 0)) return W4A16_ERR_INVALID_ARG;
+  if ((g_idx == nullptr) != (f->has_g_idx == 0)) return W4A16_ERR_INVALID_ARG;
+  if (T < 1 || T > (int64_t(1) << 24) || !(damp >= 0.0) || !std::isfinite(damp)) return W4A16_ERR_INVALID_ARG;
+  if (!aligned(w, 2) || !aligned(x, 2) || !aligned(scales, 2) || !aligned(g_idx, 4) || !aligned(workspace, 256))
+    return W4A16_ERR_MISALIGNED;
+  if (workspace_bytes < gptq_workspace_bytes(f->N, f->K)) return W4A16_ERR_BUFFER_TOO_SMALL;
+  cudaError_t e = launch_gptq(make_layout(*f), w, x, T, damp, q, scales, zeros, g_idx, workspace,
+                              static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? W4A16_OK : cuda_fail(e);
 }
 
 w4a16_status w4a16_pipeline_timeouts(uint32_t* count) {

@@ -64,6 +64,12 @@ bool gemm_plan_ok(const Layout& L, const GemmPlan& p);
 cudaError_t launch_gemm(const Layout& L, const void* blob, const uint16_t* x, uint16_t* y,
                         int64_t M, void* workspace, const GemmPlan& plan, cudaStream_t stream);
 
+// GPTQ (k_gptq.cu): workspace for an N x K layer, and the whole calibration
+// on `stream` (all fp64 on the device).
+size_t gptq_workspace_bytes(int64_t N, int64_t K);
+cudaError_t launch_gptq(const Layout& L, const uint16_t* w, const uint16_t* x, int64_t T, double damp, uint8_t* q,
+                        uint16_t* scales, uint8_t* zeros, int32_t* g_idx, void* workspace, cudaStream_t stream);
+
 // Chained decode products (w4a16_chain_*): one persistent launch runs a list
 // of layers. Work item = one 32-row group of a layer (the full K); a layer's
 // items wait for the completion counters of the layers whose outputs they

@@ -104,6 +104,8 @@ SIGNATURES = {
     "w4a16_gemm_ex": (ctypes.c_int, [_FP, _P, _SZ, _P, _P, _I64, _P, _SZ, _I32, _I32, _P]),
     "w4a16_pipeline_timeouts": (ctypes.c_int, [ctypes.POINTER(ctypes.c_uint32)]),
     "w4a16_chain_workspace_bytes": (_SZ, [_FP, _I32, _I64]),
+    "w4a16_gptq_workspace_bytes": (_SZ, [_FP]),
+    "w4a16_gptq": (ctypes.c_int, [_FP, _P, _P, _I64, ctypes.c_double, _P, _P, _P, _P, _P, _SZ, _P]),
     "w4a16_chain_prepare": (ctypes.c_int, [_FP, ctypes.POINTER(ChainLayer), _I32, _I64, _P, _SZ,
                                            ctypes.POINTER(ChainInfo)]),
     "w4a16_chain_run": (ctypes.c_int, [ctypes.POINTER(ChainInfo), _P, _P]),
@@ -222,6 +224,36 @@ def quantize_rtn(fmt: Format, w: torch.Tensor, g_idx=None, act_scale=None, strea
     if ws_bytes and isinstance(stream, torch.cuda.Stream):
         ws.record_stream(stream)
     return q, scales, zeros
+
+
+def gptq(fmt: Format, w: torch.Tensor, x: torch.Tensor, damp: float = 0.01, stream=None):
+    """GPTQ on the GPU -> (q uint8, scales fp16, zeros uint8|None, g_idx host int32 ndarray|None).
+
+    ``x``: fp16 [T, K] calibration activations. With ``fmt.has_g_idx`` the
+    columns are taken by descending diag(H) and the act-order map is returned
+    (on the host, ready for ``pack``).
+    """
+    N, K, G = fmt.N, fmt.K, fmt.G
+    dev = w.device
+    wp = _dev(w, torch.float16, "w", (N, K))
+    if x.dim() != 2 or x.shape[1] != K:
+        raise ValueError("x must be [T, K]")
+    xp = _dev(x, torch.float16, "x", (x.shape[0], K))
+    q = torch.empty((N, K), dtype=torch.uint8, device=dev)
+    scales = torch.empty((N, G), dtype=torch.float16, device=dev)
+    zeros = None if fmt.symmetric else torch.empty((N, G), dtype=torch.uint8, device=dev)
+    gidx = torch.empty(K, dtype=torch.int32, device=dev) if fmt.has_g_idx else None
+    nbytes = int(lib().w4a16_gptq_workspace_bytes(ctypes.byref(fmt)))
+    if nbytes == 0:
+        _check("w4a16_gptq", check_format(fmt) or 2)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    st = lib().w4a16_gptq(ctypes.byref(fmt), wp, xp, x.shape[0], float(damp), q.data_ptr(), scales.data_ptr(),
+                          None if zeros is None else zeros.data_ptr(), None if gidx is None else gidx.data_ptr(),
+                          ws.data_ptr(), nbytes, _stream(stream))
+    _check("w4a16_gptq", st)
+    if isinstance(stream, torch.cuda.Stream):
+        ws.record_stream(stream)
+    return q, scales, zeros, (None if gidx is None else gidx.cpu().numpy())
 
 
 def pack(fmt: Format, q: torch.Tensor, scales: torch.Tensor, zeros=None, g_idx=None,
