@@ -67,6 +67,7 @@ def parse_args():
     p.add_argument("--workload", default="llama2-7b", choices=["llama2-7b", "llama70b", "sweep8192"])
     p.add_argument("--no-gemm", action="store_true")
     p.add_argument("--no-shapes", action="store_true")
+    p.add_argument("--no-gptq", action="store_true")
     p.add_argument("--bits", type=int, default=4, choices=[3, 4, 8], help="code width of every packed linear")
     p.add_argument("--schedule", default="decode", choices=["chain", "decode"],
                    help="headline schedule: one chained launch per step, or one launch per GEMV")
@@ -352,6 +353,9 @@ def run_ours(args, rank, world, local_rank):
     gemm = None
     if not args.no_gemm and args.workload == "llama2-7b":
         gemm = run_gemm(torch, W, synth, dev, args)
+    gptq = None
+    if not args.no_gptq and args.workload == "llama2-7b" and args.bits == 4:
+        gptq = run_gptq(torch, W, synth, dev)
 
     if rank == 0:
         hbm, bf16, peak_kind = measured_peaks()
@@ -405,6 +409,7 @@ def run_ours(args, rank, world, local_rank):
             "schedules": schedules,
             "per_shape": shapes,
             "gemm": gemm,
+            "gptq": gptq,
         }
         line["cpu_baseline"] = cpu_baseline(world)
         print(json.dumps(line), flush=True)
@@ -471,6 +476,34 @@ def run_gemm(torch, W, synth, dev, args):
     if W.pipeline_timeouts() != 0:
         res["pipeline_timeouts"] = "nonzero: some output tile was not written"
     return res
+
+
+NOMINAL_FP64_TFLOPS = 1.25
+
+
+def run_gptq(torch, W, synth, dev):
+    """GPTQ of one 4096 x 4096 projection with act order on 2048 calibration
+    tokens (fp64 on the device), timed with CUDA events after one warm-up."""
+    N = K = 4096
+    T = 2048
+    w = synth.weights_cuda(N, K, synth.seed_for("gptq-bench", "w"), device=dev)
+    x = synth.activations_cuda(T, K, 0.01, synth.seed_for("gptq-bench", "x"), device=dev)
+    fmt = W.make_format(N, K, 128, False, True)
+    W.gptq(fmt, w, x)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    W.gptq(fmt, w, x)
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1)
+    # multiply-adds: H = 2 x^T x (T K^2), Cholesky (K^3 / 3), triangular inverse (K^3 / 6), column loop (N K^2 / 2)
+    fma = T * K * K + K ** 3 / 3 + K ** 3 / 6 + N * K * K / 2
+    tf = 2 * fma / (ms * 1e-3) / 1e12
+    return {"layer": f"{N}x{K}", "calib_tokens": T, "act_order": True, "ms": round(ms, 1),
+            "fp64_tflops": round(tf, 3), "of_nominal_fp64": round(tf / NOMINAL_FP64_TFLOPS, 3),
+            "peak_source": "nominal B300 FP64 1.25 TFLOP/s (no measured fp64 peak)"}
 
 
 def run_sweep8192(torch, W, synth, dev, args, rank, world, dist):
