@@ -53,6 +53,8 @@ SCHEDULE_TEXT = {
               "q..v, gate and up for o, down for gate and up (device completion counters)"),
     "decode": ("decode: one launch per GEMV; k, v and up do not wait for the GEMV before them (same input); "
                "q, o, gate, down wait for their predecessor (programmatic dependent launch)"),
+    "grouped": ("grouped: q,k,v in one launch and gate,up in one launch (w4a16_gemv_grouped, same input), o and "
+                "down alone: 4 launches per layer, each waiting for the one before (programmatic dependent launch)"),
 }
 GEMV_SOURCES = ("gemv_impl.cuh", "k_gemv.cu", "k_gemv_b4.cu")
 L2_FLUSH_BYTES = 256 << 20
@@ -69,8 +71,8 @@ def parse_args():
     p.add_argument("--no-shapes", action="store_true")
     p.add_argument("--no-gptq", action="store_true")
     p.add_argument("--bits", type=int, default=4, choices=[3, 4, 8], help="code width of every packed linear")
-    p.add_argument("--schedule", default="decode", choices=["chain", "decode"],
-                   help="headline schedule: one chained launch per step, or one launch per GEMV")
+    p.add_argument("--schedule", default="grouped", choices=["chain", "grouped", "decode"],
+                   help="headline schedule: one chained launch per step, grouped launches, or one launch per GEMV")
     return p.parse_args()
 
 
@@ -276,13 +278,25 @@ def run_ours(args, rank, world, local_rank):
 
     def sweep(schedule):
         for li, lins in enumerate(layers):
+            if schedule == "grouped":
+                # the linears that read one input share a launch; every launch waits for the one before
+                by = {name: (j, fmt, packed) for j, (name, fmt, packed) in enumerate(lins)}
+                for group in (("q", "k", "v"), ("o",), ("gate", "up"), ("down",)):
+                    sel = [by[n] for n in group if n in by]
+                    if len(sel) == 1:
+                        j, fmt, packed = sel[0]
+                        W.gemv(fmt, packed, xs[fmt.K], out=ys[li][j], weights_ready=True)
+                    else:
+                        W.gemv_grouped([f for _, f, _ in sel], [p for _, _, p in sel], xs[sel[0][1].K],
+                                       outs=[ys[li][j] for j, _, _ in sel], weights_ready=True)
+                continue
             for j, (name, fmt, packed) in enumerate(lins):
                 ready = schedule == "independent" or (schedule == "decode" and name in same_input)
                 W.gemv(fmt, packed, xs[fmt.K], out=ys[li][j], weights_ready=True, inputs_ready=ready)
 
     stream = torch.cuda.Stream(device=dev)
     graphs = {}
-    for schedule in ("chain", "decode", "dependent", "independent"):
+    for schedule in ("chain", "grouped", "decode", "dependent", "independent"):
         run = (lambda: chain.run(stream)) if schedule == "chain" else (lambda s=schedule: sweep(s))
         with torch.cuda.stream(stream):
             run()
@@ -309,7 +323,7 @@ def run_ours(args, rank, world, local_rank):
         ms = float(t.item())
     value = world * step_bytes / (ms * 1e-3) / 1e9
     schedules = {}
-    for schedule in [s for s in ("chain", "decode", "dependent", "independent") if s != args.schedule]:
+    for schedule in [s for s in ("chain", "grouped", "decode", "dependent", "independent") if s != args.schedule]:
         g = graphs[schedule]
         for _ in range(args.warmup):
             g.replay()
@@ -359,7 +373,7 @@ def run_ours(args, rank, world, local_rank):
 
     if rank == 0:
         hbm, bf16, peak_kind = measured_peaks()
-        launches = 1 if args.schedule == "chain" else n_launch
+        launches = {"chain": 1, "grouped": 4 * len(layers)}.get(args.schedule, n_launch)
         traffic = None
         ref = GEMV_TRAFFIC.get(args.schedule)
         if args.bits == 4 and ref and ref["source_sha1"] == source_sha1(GEMV_SOURCES):
@@ -400,8 +414,9 @@ def run_ours(args, rank, world, local_rank):
                          "avg_launch_us": round(ms * 1e3 / launches, 3),
                          "alg_bytes_per_launch": round(step_bytes / launches),
                          "peak_source": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)",
-                         "kernel": ("gemv_chain_kernel (one launch per step, after a counter reset)"
-                                    if args.schedule == "chain" else "gemv_kernel (every launch of the step)")},
+                         "kernel": {"chain": "gemv_chain_kernel (one launch per step, after a counter reset)",
+                                    "grouped": "gemv_kernel (every launch of the step; q,k,v and gate,up grouped)"}.get(
+                                        args.schedule, "gemv_kernel (every launch of the step)")},
             "e2e": {"value": round(e2e_value, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)},
             "gpu_launches": launches * args.steps,

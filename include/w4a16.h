@@ -287,6 +287,21 @@ W4A16_API w4a16_status w4a16_gemv(const w4a16_format* f, const void* packed, siz
                         const uint16_t* x, uint16_t* y, int64_t M, w4a16_stream_t stream);
 
 /*
+ * Grouped decode product: n (1..4) layers that read the same activations x
+ * (the q, k and v projections of a decoder layer, or gate and up) in one
+ * launch; y[m] = x . W_hat_m^T, each as w4a16_gemv (same bound). The layers
+ * share K, bits, group_size and symmetric (else W4A16_ERR_INVALID_ARG) and
+ * have neither act order nor an act scale (else W4A16_ERR_UNSUPPORTED); N
+ * may differ. formats, packed, packed_bytes and y are HOST arrays of n
+ * entries; x, packed[m] and y[m] are device pointers aligned as for
+ * w4a16_gemv. flags: as w4a16_gemv_ex (W4A16_GEMV_STAGE_ACTIVATIONS
+ * excepted). The launch shape is chosen for the group as a whole.
+ */
+W4A16_API w4a16_status w4a16_gemv_grouped(const w4a16_format* formats, const void* const* packed,
+                                const size_t* packed_bytes, int32_t n, const uint16_t* x,
+                                uint16_t* const* y, int64_t M, uint32_t flags, w4a16_stream_t stream);
+
+/*
  * Chained decode products: one persistent launch computes y_i = x_i . W_hat_i^T
  * for a list of layers (1 <= M <= 16 tokens each), e.g. every linear of a
  * decoder stack for one token step. Each layer is the decode product of

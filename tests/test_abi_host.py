@@ -255,3 +255,28 @@ def test_chain_argument_checks(lib):
     assert prep(ragged, layers(ok_waits)) == UNSUPPORTED               # K not a multiple of 64
     bad = W.ChainInfo(n, 4, 128, 0, 1, 0)
     assert lib.w4a16_chain_run(ctypes.byref(bad), FAKE, None) == INVALID  # no work items
+
+
+def test_gemv_grouped_argument_checks(lib):
+    n = 3
+    fs = [fmt(256, 512), fmt(128, 512), fmt(384, 512)]
+    fa = (W.Format * n)(*fs)
+    pa = (ctypes.c_void_p * n)(FAKE, FAKE * 2, FAKE * 3)
+    ba = (ctypes.c_size_t * n)(*[W.packed_bytes(f) for f in fs])
+    X = FAKE * 64
+    ya = (ctypes.c_void_p * n)(FAKE * 128, FAKE * 256, FAKE * 512)
+    call = lambda f=fa, p=pa, b=ba, k=n, x=X, y=ya, M=1, flags=0: lib.w4a16_gemv_grouped(f, p, b, k, x, y, M, flags,
+                                                                                         None)
+    assert call(k=0) == INVALID
+    assert call(k=5) == INVALID
+    assert call(M=17) == INVALID
+    assert call(x=X + 2) == MISALIGNED
+    assert call(flags=2 | 8) == INVALID                        # both variants
+    assert call(flags=4) == INVALID                            # staging is not offered here
+    mixed = (W.Format * n)(fs[0], fmt(128, 1024), fs[2])       # another K
+    assert call(f=mixed, b=(ctypes.c_size_t * n)(*[W.packed_bytes(f) for f in mixed])) == INVALID
+    act = (W.Format * n)(fs[0], fmt(128, 512, act=True), fs[2])
+    assert call(f=act, b=(ctypes.c_size_t * n)(*[W.packed_bytes(f) for f in act])) == UNSUPPORTED
+    small = (ctypes.c_size_t * n)(ba[0], ba[1] - 1, ba[2])
+    assert call(b=small) == SMALL
+    assert call(y=(ctypes.c_void_p * n)(FAKE * 128, X, FAKE * 512)) == INVALID  # y overlaps x

@@ -263,6 +263,59 @@ w4a16_status w4a16_gemv_ex(const w4a16_format* f, const void* packed, size_t pac
   return gemv_common(f, packed, packed_bytes, x, y, M, shape, ksplit, flags, stream);
 }
 
+w4a16_status w4a16_gemv_grouped(const w4a16_format* formats, const void* const* packed, const size_t* packed_bytes,
+                                int32_t n, const uint16_t* x, uint16_t* const* y, int64_t M, uint32_t flags,
+                                w4a16_stream_t stream) {
+  if (formats == nullptr || packed == nullptr || packed_bytes == nullptr || x == nullptr || y == nullptr)
+    return W4A16_ERR_INVALID_ARG;
+  if (n < 1 || n > 4 || M < 1 || M > 16) return W4A16_ERR_INVALID_ARG;
+  if (!aligned(x, 16)) return W4A16_ERR_MISALIGNED;
+  if ((flags & ~uint32_t(W4A16_GEMV_WEIGHTS_READY | W4A16_GEMV_ASYNC_COPY | W4A16_GEMV_REGISTER_RING |
+                         W4A16_GEMV_INPUTS_READY)) != 0)
+    return W4A16_ERR_INVALID_ARG;
+  if ((flags & W4A16_GEMV_REGISTER_RING) && (flags & W4A16_GEMV_ASYNC_COPY)) return W4A16_ERR_INVALID_ARG;
+  GemvGroup grp;
+  grp.n = n;
+  int64_t nr = 0;
+  const w4a16_format& f0 = formats[0];
+  const char* xb = reinterpret_cast<const char*>(x);
+  const size_t xbytes = size_t(M) * size_t(f0.K) * 2;
+  for (int32_t m = 0; m < n; ++m) {
+    const w4a16_format& f = formats[m];
+    w4a16_status s = blob_status(&f, packed[m], packed_bytes[m]);
+    if (s != W4A16_OK) return s;
+    if (f.bits != f0.bits || f.group_size != f0.group_size || f.symmetric != f0.symmetric || f.K != f0.K)
+      return W4A16_ERR_INVALID_ARG;
+    if (f.has_g_idx || f.has_act_scale) return W4A16_ERR_UNSUPPORTED;
+    if (y[m] == nullptr) return W4A16_ERR_INVALID_ARG;
+    if (!aligned(y[m], 16)) return W4A16_ERR_MISALIGNED;
+    const char* yb = reinterpret_cast<const char*>(y[m]);
+    const size_t ybytes = size_t(M) * size_t(f.N) * 2;
+    if (xb < yb + ybytes && yb < xb + xbytes) return W4A16_ERR_INVALID_ARG;  // y overlaps x
+    const Layout L = make_layout(f);
+    grp.views[m] = view_of(L, packed[m]);
+    grp.NR[m] = L.NR;
+    grp.N[m] = L.N;
+    grp.y[m] = y[m];
+    nr += L.NR;
+  }
+  w4a16_format fc = f0;  // the group as one layer: its row blocks one after another
+  fc.N = nr * 128;
+  if (format_status(&fc) != W4A16_OK) return W4A16_ERR_UNSUPPORTED;
+  const Layout Lc = make_layout(fc);
+  DeviceInfo dev;
+  cudaError_t e = device_info(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  const bool wbulk = (flags & W4A16_GEMV_ASYNC_COPY) != 0 ||
+                     ((flags & W4A16_GEMV_REGISTER_RING) == 0 && Lc.NR >= 64);
+  const GemvPlan plan = gemv_default_plan(Lc, int(M), dev, wbulk ? kGemvAsyncCopy : kGemvRegisterRing);
+  if (!gemv_plan_ok(Lc, int(M), plan)) return W4A16_ERR_UNSUPPORTED;
+  uint32_t kflags = flags & (W4A16_GEMV_WEIGHTS_READY | W4A16_GEMV_INPUTS_READY);
+  if (kflags & W4A16_GEMV_INPUTS_READY) kflags |= W4A16_GEMV_WEIGHTS_READY;
+  e = launch_gemv_group(Lc, grp, x, int(M), plan, kflags, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? W4A16_OK : cuda_fail(e);
+}
+
 size_t w4a16_gemm_workspace_bytes(const w4a16_format* f, int64_t M) {
   if (format_status(f) != W4A16_OK || M < 1) return 0;
   return (f->has_g_idx || f->has_act_scale) ? size_t(M) * size_t(f->K) * 2 : 0;

@@ -60,6 +60,7 @@ namespace w4a16 {
 namespace {  // internal linkage: each including translation unit has its own copy
 
 constexpr int kWarps = 8;
+constexpr int kMaxGroup = 4;  // layers per grouped launch
 constexpr int kThreads = kWarps * 32;
 constexpr int kTilesPerWarp = 2;
 constexpr uint64_t kTWaitLimitNs = 1000ull * 1000ull * 1000ull;  // every pipeline wait gives up after 1 s
@@ -81,6 +82,16 @@ struct GemvArgs {
   int depth;       // warp bulk-copy ring: units in flight per warp
   int wb_off;      // warp bulk-copy ring: byte offset of the rings in shared memory
   int slot_bytes;  // warp bulk-copy ring: bytes of one slot
+  // Grouped launch: up to kMaxGroup layers with the same K, format and input
+  // x, their 128-row blocks one after another along gridDim.x (group m owns
+  // blocks [gstart[m], gstart[m+1])). ngroup == 1: the fields above.
+  int ngroup;
+  int gstart[kMaxGroup + 1];
+  const uint32_t* gq[kMaxGroup];
+  const uint32_t* gs[kMaxGroup];
+  const uint8_t* gz[kMaxGroup];
+  uint16_t* gy[kMaxGroup];
+  int gN[kMaxGroup];
 };
 
 // Scale and zero for the rows (g, g+8) of one tile and one group, folded into
@@ -413,7 +424,24 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const GemvArgs a) {
   const int WK = kWarps / WR;         // warps splitting K per row group
   const int wr = warp % WR;
   const int wk = warp / WR;
-  const int Tc = int(blockIdx.x) * RT;  // first 16-row tile of the block
+  // this block's layer (grouped launch) and its block index within it
+  int bx = int(blockIdx.x);
+  const uint32_t* qweight = a.qweight;
+  const uint32_t* scales2 = a.scales2;
+  const uint8_t* zeros = a.zeros;
+  uint16_t* yout = a.y;
+  int Nl = a.N;
+  if (a.ngroup > 1) {
+    int m = 0;
+    while (m + 1 < a.ngroup && bx >= a.gstart[m + 1]) ++m;
+    bx -= a.gstart[m];
+    qweight = a.gq[m];
+    scales2 = a.gs[m];
+    zeros = a.gz[m];
+    yout = a.gy[m];
+    Nl = a.gN[m];
+  }
+  const int Tc = bx * RT;  // first 16-row tile of the block
   const int R = Tc >> 3;
   const int r16 = (Tc & 7) + wr * kTilesPerWarp;
 
@@ -428,11 +456,11 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const GemvArgs a) {
   const int G = a.G;
   const int gmax = G - 1 - u0 * U::kGroups;  // last group, relative to this warp's first
   using CW = CodeWords<BITS>;
-  const uint32_t* qp = a.qweight + (size_t(R) * a.KB * 8 + r16) * CW::kRow16 + lane * 4 +
+  const uint32_t* qp = qweight + (size_t(R) * a.KB * 8 + r16) * CW::kRow16 + lane * 4 +
                        size_t(u0) * U::kBlocks * CW::kBlock;
-  const uint32_t* sp = a.scales2 + (size_t(R) * G * 8 + r16) * 8 + g + size_t(u0) * U::kGroups * 64;
+  const uint32_t* sp = scales2 + (size_t(R) * G * 8 + r16) * 8 + g + size_t(u0) * U::kGroups * 64;
   const uint8_t* zp = SYM ? nullptr
-                          : a.zeros + ((size_t(R) * G * 8 + r16) * 8 + g + size_t(u0) * U::kGroups * 64) * kZeroMul<BITS>;
+                          : zeros + ((size_t(R) * G * 8 + r16) * 8 + g + size_t(u0) * U::kGroups * 64) * kZeroMul<BITS>;
 
   const bool early = (a.flags & kGemvWeightsReady) != 0;
   const int M = a.M;
@@ -605,16 +633,16 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const GemvArgs a) {
       float acc = 0.f;
       for (int rk = 0; rk < KS; ++rk) acc += ld_dsmem_f32(red_c + e, uint32_t(rk));
       const int tok = e / rows;
-      const int n = int(blockIdx.x) * rows + (e - tok * rows);
-      if (n < a.N) a.y[size_t(tok) * a.N + n] = __half_as_ushort(__float2half_rn(acc));
+      const int n = bx * rows + (e - tok * rows);
+      if (n < Nl) yout[size_t(tok) * Nl + n] = __half_as_ushort(__float2half_rn(acc));
     }
     cluster_sync_all();  // keep this block's shared memory alive until peers are done
   } else {
     __syncthreads();
     for (int e = threadIdx.x; e < nout; e += kThreads) {
       const int tok = e / rows;
-      const int n = int(blockIdx.x) * rows + (e - tok * rows);
-      if (n < a.N) a.y[size_t(tok) * a.N + n] = __half_as_ushort(__float2half_rn(red_c[e]));
+      const int n = bx * rows + (e - tok * rows);
+      if (n < Nl) yout[size_t(tok) * Nl + n] = __half_as_ushort(__float2half_rn(red_c[e]));
     }
   }
 }
@@ -635,7 +663,7 @@ cudaError_t launch_typed(const GemvArgs& a, int KS, size_t smem_bytes, cudaStrea
     if (e != cudaSuccess) return e;
   }
   cudaLaunchConfig_t cfg = {};
-  const int ntiles = ((a.N + kRowsPerBlock - 1) / kRowsPerBlock) * 8;
+  const int ntiles = a.ngroup > 1 ? a.gstart[a.ngroup] * a.rows16 : ((a.N + kRowsPerBlock - 1) / kRowsPerBlock) * 8;
   cfg.gridDim = dim3(unsigned(ntiles / a.rows16), unsigned(KS), 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = smem_bytes;
@@ -744,6 +772,7 @@ cudaError_t launch_gemv_bits(const Layout& L, const void* blob, const uint16_t* 
   a.rows16 = plan.rows16;
   a.kb_per_cta = kb_per_cta_of(L, plan.ksplit);
   a.flags = flags;
+  a.ngroup = 1;
   const bool ring_staged = staged || plan.stage_x;
   const bool wb = plan.kind == kGemvAsyncCopy;
   const RingSmem rs = ring_smem(L, M, a.kb_per_cta, ring_staged, wb, plan.stages);
@@ -756,6 +785,52 @@ cudaError_t launch_gemv_bits(const Layout& L, const void* blob, const uint16_t* 
   if (M <= 4) return launch_gs<4, BITS>(a, gs, L.sym, ring_staged, wb, plan.ksplit, smem, stream);
   if (M <= 8) return launch_gs<8, BITS>(a, gs, L.sym, ring_staged, wb, plan.ksplit, smem, stream);
   return launch_gs<16, BITS>(a, gs, L.sym, ring_staged, wb, plan.ksplit, smem, stream);
+}
+
+// Grouped launch: Lc describes the group as one layer (the sum of the row
+// blocks, the shared K and format); layer m has its own blob and output.
+template <int BITS>
+cudaError_t launch_gemv_group_bits(const Layout& Lc, const GemvGroup& grp, const uint16_t* x, int M,
+                                   const GemvPlan& plan, uint32_t flags, cudaStream_t stream) {
+  GemvArgs a = {};
+  a.perm = nullptr;
+  a.ascale = nullptr;
+  a.x = x;
+  a.M = M;
+  a.N = int(Lc.N);
+  a.K = int(Lc.K);
+  a.G = int(Lc.G);
+  a.KB = int(Lc.KB);
+  a.rows16 = plan.rows16;
+  a.kb_per_cta = kb_per_cta_of(Lc, plan.ksplit);
+  a.flags = flags;
+  a.ngroup = grp.n;
+  a.gstart[0] = 0;
+  for (int m = 0; m < grp.n; ++m) {
+    a.gq[m] = grp.views[m].qweight;
+    a.gs[m] = reinterpret_cast<const uint32_t*>(grp.views[m].scales);
+    a.gz[m] = grp.views[m].zeros;
+    a.gy[m] = grp.y[m];
+    a.gN[m] = int(grp.N[m]);
+    a.gstart[m + 1] = a.gstart[m] + int(grp.NR[m] * 8 / plan.rows16);
+  }
+  a.qweight = a.gq[0];
+  a.scales2 = a.gs[0];
+  a.zeros = a.gz[0];
+  a.y = a.gy[0];
+  const bool staged = gemv_staged(Lc) || plan.stage_x;
+  const bool wb = plan.kind == kGemvAsyncCopy;
+  const RingSmem rs = ring_smem(Lc, M, a.kb_per_cta, staged, wb, plan.stages);
+  a.depth = wb ? plan.stages : 1;
+  a.wb_off = rs.wb_off;
+  a.slot_bytes = rs.slot_bytes;
+  const size_t smem = rs.total;
+  const int gs = Lc.gsize;
+  if (M <= 1) return launch_gs<1, BITS>(a, gs, Lc.sym, staged, wb, plan.ksplit, smem, stream);
+  if (M <= 2) return launch_gs<2, BITS>(a, gs, Lc.sym, staged, wb, plan.ksplit, smem, stream);
+  if (M <= 4) return launch_gs<4, BITS>(a, gs, Lc.sym, staged, wb, plan.ksplit, smem, stream);
+  if (M <= 8) return launch_gs<8, BITS>(a, gs, Lc.sym, staged, wb, plan.ksplit, smem, stream);
+  return launch_gs<16, BITS>(a, gs, Lc.sym, staged, wb, plan.ksplit, smem, stream);
 }
 
 // ---------------------------------------------------------------------------

@@ -64,6 +64,18 @@ bool gemm_plan_ok(const Layout& L, const GemmPlan& p);
 cudaError_t launch_gemm(const Layout& L, const void* blob, const uint16_t* x, uint16_t* y,
                         int64_t M, void* workspace, const GemmPlan& plan, cudaStream_t stream);
 
+// Grouped decode product: up to 4 layers with the same K, format and input,
+// in one launch (their row blocks one after another).
+struct GemvGroup {
+  int n;
+  BlobView views[4];
+  int64_t NR[4];
+  int64_t N[4];
+  uint16_t* y[4];
+};
+cudaError_t launch_gemv_group(const Layout& Lc, const GemvGroup& grp, const uint16_t* x, int M, const GemvPlan& plan,
+                              uint32_t flags, cudaStream_t stream);
+
 // GPTQ (k_gptq.cu): workspace for an N x K layer, and the whole calibration
 // on `stream` (all fp64 on the device).
 size_t gptq_workspace_bytes(int64_t N, int64_t K);

@@ -11,6 +11,12 @@ cudaError_t launch_gemv_b4(const Layout& L, const void* blob, const uint16_t* x,
                            const GemvPlan& plan, uint32_t flags, cudaStream_t stream);
 cudaError_t launch_gemv_b8(const Layout& L, const void* blob, const uint16_t* x, uint16_t* y, int M,
                            const GemvPlan& plan, uint32_t flags, cudaStream_t stream);
+cudaError_t launch_gemv_group_b3(const Layout& Lc, const GemvGroup& grp, const uint16_t* x, int M,
+                                 const GemvPlan& plan, uint32_t flags, cudaStream_t stream);
+cudaError_t launch_gemv_group_b4(const Layout& Lc, const GemvGroup& grp, const uint16_t* x, int M,
+                                 const GemvPlan& plan, uint32_t flags, cudaStream_t stream);
+cudaError_t launch_gemv_group_b8(const Layout& Lc, const GemvGroup& grp, const uint16_t* x, int M,
+                                 const GemvPlan& plan, uint32_t flags, cudaStream_t stream);
 cudaError_t launch_chain_b3(const ChainLaunch& c, cudaStream_t stream);
 cudaError_t launch_chain_b4(const ChainLaunch& c, cudaStream_t stream);
 cudaError_t launch_chain_b8(const ChainLaunch& c, cudaStream_t stream);
@@ -65,6 +71,13 @@ cudaError_t launch_gemv(const Layout& L, const void* blob, const uint16_t* x, ui
   if (L.bits == 8) return launch_gemv_b8(L, blob, x, y, M, plan, flags, stream);
   if (L.bits == 3) return launch_gemv_b3(L, blob, x, y, M, plan, flags, stream);
   return launch_gemv_b4(L, blob, x, y, M, plan, flags, stream);
+}
+
+cudaError_t launch_gemv_group(const Layout& Lc, const GemvGroup& grp, const uint16_t* x, int M, const GemvPlan& plan,
+                              uint32_t flags, cudaStream_t stream) {
+  if (Lc.bits == 8) return launch_gemv_group_b8(Lc, grp, x, M, plan, flags, stream);
+  if (Lc.bits == 3) return launch_gemv_group_b3(Lc, grp, x, M, plan, flags, stream);
+  return launch_gemv_group_b4(Lc, grp, x, M, plan, flags, stream);
 }
 
 cudaError_t launch_chain(const ChainLaunch& c, cudaStream_t stream) {

@@ -8,6 +8,11 @@ cudaError_t launch_gemv_b3(const Layout& L, const void* blob, const uint16_t* x,
   return launch_gemv_bits<3>(L, blob, x, y, M, plan, flags, stream);
 }
 
+cudaError_t launch_gemv_group_b3(const Layout& Lc, const GemvGroup& grp, const uint16_t* x, int M,
+                                 const GemvPlan& plan, uint32_t flags, cudaStream_t stream) {
+  return launch_gemv_group_bits<3>(Lc, grp, x, M, plan, flags, stream);
+}
+
 cudaError_t launch_chain_b3(const ChainLaunch& c, cudaStream_t stream) { return launch_chain_bits<3>(c, stream); }
 
 cudaError_t take_gemv_timeouts_b3(unsigned int* count) { return take_local_gemv_timeouts(count); }

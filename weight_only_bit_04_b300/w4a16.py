@@ -105,6 +105,8 @@ SIGNATURES = {
     "w4a16_pipeline_timeouts": (ctypes.c_int, [ctypes.POINTER(ctypes.c_uint32)]),
     "w4a16_chain_workspace_bytes": (_SZ, [_FP, _I32, _I64]),
     "w4a16_gptq_workspace_bytes": (_SZ, [_FP]),
+    "w4a16_gemv_grouped": (ctypes.c_int, [_FP, ctypes.POINTER(ctypes.c_void_p), ctypes.POINTER(ctypes.c_size_t),
+                                          _I32, _P, ctypes.POINTER(ctypes.c_void_p), _I64, ctypes.c_uint32, _P]),
     "w4a16_gptq": (ctypes.c_int, [_FP, _P, _P, _I64, ctypes.c_double, _P, _P, _P, _P, _P, _SZ, _P]),
     "w4a16_chain_prepare": (ctypes.c_int, [_FP, ctypes.POINTER(ChainLayer), _I32, _I64, _P, _SZ,
                                            ctypes.POINTER(ChainInfo)]),
@@ -224,6 +226,26 @@ def quantize_rtn(fmt: Format, w: torch.Tensor, g_idx=None, act_scale=None, strea
     if ws_bytes and isinstance(stream, torch.cuda.Stream):
         ws.record_stream(stream)
     return q, scales, zeros
+
+
+def gemv_grouped(fmts, packeds, x: torch.Tensor, outs=None, weights_ready: bool = False,
+                 inputs_ready: bool = False, register_ring: bool = False, async_copy: bool = False, stream=None):
+    """y_m = x . W_hat_m^T for up to 4 layers sharing x, K and the format, in one launch."""
+    n = len(fmts)
+    M = x.shape[0]
+    K = fmts[0].K
+    xp = _dev(x, torch.float16, "x", (M, K))
+    if outs is None:
+        outs = [torch.empty((M, f.N), dtype=torch.float16, device=x.device) for f in fmts]
+    fa = (Format * n)(*fmts)
+    pa = (ctypes.c_void_p * n)(*[_dev(p, torch.uint8, "packed") for p in packeds])
+    ba = (ctypes.c_size_t * n)(*[p.numel() for p in packeds])
+    ya = (ctypes.c_void_p * n)(*[_dev(y, torch.float16, "out", (M, f.N)) for y, f in zip(outs, fmts)])
+    flags = ((GEMV_WEIGHTS_READY if weights_ready else 0) | (GEMV_INPUTS_READY if inputs_ready else 0) |
+             (GEMV_REGISTER_RING if register_ring else 0) | (GEMV_ASYNC_COPY if async_copy else 0))
+    st = lib().w4a16_gemv_grouped(fa, pa, ba, n, xp, ya, M, flags, _stream(stream))
+    _check("w4a16_gemv_grouped", st)
+    return outs
 
 
 def gptq(fmt: Format, w: torch.Tensor, x: torch.Tensor, damp: float = 0.01, stream=None):
