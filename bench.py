@@ -82,6 +82,20 @@ def gemv_bytes(N: int, K: int, M: int = 1, g: int = 128, sym: bool = False, bits
     return N * K * bits // 8 + N * G * 2 + (0 if sym else N * G * zero_bits // 8) + M * K * 2 + M * N * 2
 
 
+def max_over_ranks(torch, dist, value: float, device) -> float:
+    """The slowest rank's time (every rank gets it); the value itself on one process."""
+    if dist is None:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def reference_rank_runs(rank: int) -> bool:
+    """The reference arm (the CPU oracle) runs and prints on rank 0 only."""
+    return rank == 0
+
+
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -318,9 +332,7 @@ def run_ours(args, rank, world, local_rank):
         ms = time_graph(torch, graph, stream, args.steps)
     if dist:
         dist.barrier()
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(torch, dist, ms, dev)
     value = world * step_bytes / (ms * 1e-3) / 1e9
     schedules = {}
     for schedule in [s for s in ("chain", "grouped", "decode", "dependent", "independent") if s != args.schedule]:
@@ -356,10 +368,7 @@ def run_ours(args, rank, world, local_rank):
     for _ in range(args.steps):
         e2e_step()
     e2e_ms = (time.perf_counter() - t0) * 1e3 / args.steps
-    if dist:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(torch, dist, e2e_ms, dev)
     e2e_value = world * step_bytes / (e2e_ms * 1e-3) / 1e9
 
     shapes = None if args.no_shapes else per_shape(torch, W, layers, xs, dev)
@@ -614,7 +623,7 @@ def cpu_baseline(world):
 
 
 def run_reference(args, rank, world):
-    if rank != 0:
+    if not reference_rank_runs(rank):
         return
     sample = oracle_sample()
     for _ in range(min(args.warmup, 3)):
