@@ -79,9 +79,9 @@ struct GemvArgs {
   int rows16;      // 16-row tiles per thread block (2, 4 or 8)
   int kb_per_cta;  // 64-column blocks per thread block (the last blocks of a cluster may get fewer)
   uint32_t flags;  // kGemvWeightsReady
-  int depth;       // warp bulk-copy ring: units in flight per warp
-  int wb_off;      // warp bulk-copy ring: byte offset of the rings in shared memory
-  int slot_bytes;  // warp bulk-copy ring: bytes of one slot
+  int depth;       // asynchronous-copy ring: units in flight per thread
+  int wb_off;      // asynchronous-copy ring: byte offset of the ring in shared memory
+  int slot_bytes;  // asynchronous-copy ring: bytes of one slot
   // Grouped launch: up to kMaxGroup layers with the same K, format and input
   // x, their 128-row blocks one after another along gridDim.x (group m owns
   // blocks [gstart[m], gstart[m+1])). ngroup == 1: the fields above.

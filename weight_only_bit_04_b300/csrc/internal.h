@@ -37,7 +37,7 @@ constexpr int kGemvAsyncCopy = 2;    // each thread lands its own weight loads i
 struct GemvPlan {
   int kind;     // kGemvRegisterRing or kGemvAsyncCopy
   int rows16;   // register ring: 16-row tiles per CTA (2, 4, 8)
-  int stages;   // async copy: units in flight (fixed at 4)
+  int stages;   // async copy: units in flight per thread (4; 2 for 8-bit codes)
   int ksplit;   // CTAs per cluster along K
   bool stage_x; // register ring: copy the block's activations to shared memory first
 };
@@ -109,7 +109,8 @@ struct ChainLaunch {
 cudaError_t launch_chain(const ChainLaunch& c, cudaStream_t stream);
 
 // Device-side counts of bounded pipeline waits that gave up, read and reset
-// (k_gemm.cu for the GEMM, k_gemv.cu for the bulk-copy GEMV).
+// (k_gemm.cu for the GEMM; the GEMV translation units for the GEMV's and the
+// chained launch's waits).
 cudaError_t take_pipeline_timeouts(unsigned int* count);
 cudaError_t take_gemv_timeouts(unsigned int* count);
 
