@@ -40,6 +40,8 @@ sys.path.insert(0, ROOT)
 
 METRIC = "W4A16 GEMV achieved HBM GB/s (% of 8 TB/s) at batch 1; GEMM TFLOP/s"
 NOMINAL_HBM_GBPS = 8000.0
+WORKLOAD_7B = ("llama2-7b decode sweep, batch 1: 32 layers x (q,k,v,o 4096x4096; gate,up 11008x4096; "
+               "down 4096x11008), 224 GEMVs per step")
 # Fallback peaks (one earlier B300 measurement) when the measured file is absent.
 FALLBACK_HBM_GBPS = 6400.0
 FALLBACK_BF16_TFLOPS = 1800.0
@@ -393,8 +395,7 @@ def run_ours(args, rank, world, local_rank):
                         "gate,up 28672x8192; down 8192x28672), 560 GEMVs per step, all weights resident")
             frac = synth.LLAMA_70B_OUTLIER_FRAC
         else:
-            workload = ("llama2-7b decode sweep, batch 1: 32 layers x (q,k,v,o 4096x4096; gate,up 11008x4096; "
-                        "down 4096x11008), 224 GEMVs per step")
+            workload = WORKLOAD_7B
             frac = synth.LLAMA2_7B_OUTLIER_FRAC
         line = {
             "metric": METRIC if args.bits == 4 else METRIC.replace("W4A16", f"W{args.bits}A16"),
@@ -650,10 +651,10 @@ def run_reference(args, rank, world):
         "vs_baseline": None,
         "dtype": "f64",
         "data": "synthetic, same recipe as our arm",
-        "config": {"workload": "llama2-7b decode sweep, batch 1 (each step: the CPU oracle on one 4096x4096 GEMV of it)",
-                   "M": 1, "group_size": 128, "scheme": "asymmetric uint4, fp16 scales"},
+        "config": {"workload": WORKLOAD_7B, "M": 1, "group_size": 128, "scheme": "asymmetric uint4, fp16 scales"},
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cpu_cores(), "kind": "oracle",
-                         "sample": "one 4096x4096 GEMV of the sweep per step, NumPy fp64 dequantize-then-matmul"},
+                         "sample": ("each step a bounded sample of the workload: one 4096x4096 GEMV of it, "
+                                    "NumPy fp64 dequantize-then-matmul")},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
