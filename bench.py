@@ -408,7 +408,8 @@ def run_ours(args, rank, world, local_rank):
             "higher_is_better": True,
             "scaling": "weak",
             "vs_baseline": None,
-            "dtype": f"fp16 activations x uint{args.bits} weights, fp32 accumulate",
+            "dtype": "fp16",
+            "precision": f"fp16 activations x uint{args.bits} weights (fp16 scales), fp32 accumulate",
             "data": (f"synthetic: seeded N(0,0.02) weights RTN-quantized on the GPU, N(0,1) fp16 activations "
                      f"with {100 * frac:g}% outlier channels x20"),
             "config": {"workload": workload,
@@ -573,7 +574,8 @@ def run_sweep8192(torch, W, synth, dev, args, rank, world, dist):
         print(json.dumps({
             "metric": METRIC, "value": m1["GB/s"], "unit": "GB/s", "n_gpus": world, "steps": 20, "warmup": 3,
             "ms_per_step": m1["us"] / 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "fp16 activations x uint4 weights, fp32 accumulate", "data": "synthetic",
+            "dtype": "fp16", "precision": "fp16 activations x uint4 weights (fp16 scales), fp32 accumulate",
+            "data": "synthetic",
             "config": {"workload": "8192x8192 batch sweep M in {1..128}, asym uint4 g128 (value: M = 1 GEMV)",
                        "l2": "GEMV: 16 distinct weight copies (cold); GEMM: L2 flushed before each call"},
             "rows": rows, "peaks": {"hbm_gbs": hbm, "bf16_tflops": bf16, "source": kind}}), flush=True)
