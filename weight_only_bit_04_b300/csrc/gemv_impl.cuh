@@ -289,14 +289,20 @@ __device__ __forceinline__ void load_unit(UnitRegs<GS, BITS>& r, const uint32_t*
 
 // Multiply-accumulate one unit. xl0 / xl1 point at this lane's x fragment
 // (token rows g and g+8, column 4t) for the unit's first column.
-template <int NB, int GS, bool SYM, int XM, int BITS>
+// SPLIT: even and odd 16-column steps accumulate into separate sets, twice
+// the independent MMA chains (consecutive MMAs into one accumulator wait for
+// each other). Measured on B300: faster for the register ring (4096x11008:
+// 8.63 -> 7.84 us), slower for the asynchronous-copy ring (28672x8192:
+// 30.3 -> 32.3 us), which therefore keeps one set.
+template <int NB, int GS, bool SYM, int XM, int BITS, bool SPLIT>
 __device__ __forceinline__ void compute_unit(const UnitRegs<GS, BITS>& r, const uint16_t* xl0, const uint16_t* xl1,
                                              float tot[kTilesPerWarp][NB][4]) {
   using U = Unit<GS>;
   const uint32_t ones[4] = {0x00010001u, 0x00010001u, 0x00010001u, 0x00010001u};  // 2^-24 each
   const float zero4[4] = {0.f, 0.f, 0.f, 0.f};
-  float acc[kTilesPerWarp][NB][4];
-  float cx[NB][4];
+  constexpr int NS = SPLIT ? 2 : 1;
+  float acc[NS][kTilesPerWarp][NB][4];
+  float cx[NS][NB][4];
 #pragma unroll
   for (int bb = 0; bb < U::kBlocks; ++bb) {
     uint2 bx[4][NB];
@@ -308,24 +314,39 @@ __device__ __forceinline__ void compute_unit(const UnitRegs<GS, BITS>& r, const 
     }
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      // first 16-column step of a group: start fresh accumulators
-      const bool fresh = (GS == 32) ? (j == 0 || j == 2) : (j == 0 && bb == 0);
+      const int ph = SPLIT ? (j & 1) : 0;
+      // first step of the group (of this parity, with SPLIT): start the set fresh
+      const bool fresh = SPLIT ? ((GS == 32) ? true : (j < 2 && bb == 0))
+                               : ((GS == 32) ? (j == 0 || j == 2) : (j == 0 && bb == 0));
 #pragma unroll
-      for (int nb = 0; nb < NB; ++nb) mma_16816(cx[nb], ones, bx[j][nb].x, bx[j][nb].y, fresh ? zero4 : cx[nb]);
+      for (int nb = 0; nb < NB; ++nb)
+        mma_16816(cx[ph][nb], ones, bx[j][nb].x, bx[j][nb].y, fresh ? zero4 : cx[ph][nb]);
 #pragma unroll
       for (int tt = 0; tt < kTilesPerWarp; ++tt) {
         uint32_t af[4];
         extract_step<BITS>(r.w[bb], tt, j, af);
 #pragma unroll
         for (int nb = 0; nb < NB; ++nb)
-          mma_16816(acc[tt][nb], af, bx[j][nb].x, bx[j][nb].y, fresh ? zero4 : acc[tt][nb]);
+          mma_16816(acc[ph][tt][nb], af, bx[j][nb].x, bx[j][nb].y, fresh ? zero4 : acc[ph][tt][nb]);
       }
       const bool group_end = (GS == 32) ? (j == 1 || j == 3) : (j == 3 && bb == U::kBlocks - 1);
       if (group_end) {
         const int gg = (GS == 32) ? (j >> 1) : 0;
+        float c2[NB][4];
 #pragma unroll
-        for (int tt = 0; tt < kTilesPerWarp; ++tt)
-          finalize<NB>(acc[tt], cx, make_factors<SYM, BITS>(r.s[gg][tt], r.z[gg][tt]), tot[tt]);
+        for (int nb = 0; nb < NB; ++nb)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) c2[nb][i] = SPLIT ? cx[0][nb][i] + cx[NS - 1][nb][i] : cx[0][nb][i];
+#pragma unroll
+        for (int tt = 0; tt < kTilesPerWarp; ++tt) {
+          float a2[NB][4];
+#pragma unroll
+          for (int nb = 0; nb < NB; ++nb)
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              a2[nb][i] = SPLIT ? acc[0][tt][nb][i] + acc[NS - 1][tt][nb][i] : acc[0][tt][nb][i];
+          finalize<NB>(a2, c2, make_factors<SYM, BITS>(r.s[gg][tt], r.z[gg][tt]), tot[tt]);
+        }
       }
     }
   }
@@ -576,7 +597,7 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const GemvArgs a) {
                                zshift) & (BITS != 8 ? 0xFFu : 0xFFFFu);
         }
       const int xo = i * U::kBlocks * kColsPerBlock;
-      compute_unit<NB, GS, SYM, STAGED ? kXShared : kXGlobal, BITS>(r, xl0 + xo, xl1 + xo, tot);
+      compute_unit<NB, GS, SYM, STAGED ? kXShared : kXGlobal, BITS, !WB>(r, xl0 + xo, xl1 + xo, tot);
       issue_unit(i + D);  // refills the slot just read (this thread's own entries)
     }
     cp_async_wait_all();
@@ -587,7 +608,7 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const GemvArgs a) {
         const int i = i0 + s;
         if (i < nunit) {
           const int xo = i * U::kBlocks * kColsPerBlock;
-          compute_unit<NB, GS, SYM, STAGED ? kXShared : kXGlobal, BITS>(ring[s], xl0 + xo, xl1 + xo, tot);
+          compute_unit<NB, GS, SYM, STAGED ? kXShared : kXGlobal, BITS, !WB>(ring[s], xl0 + xo, xl1 + xo, tot);
           if (i + PF < nunit) load_unit<GS, SYM, BITS>(ring[s], qp, sp, zp, i + PF, gmax);
         }
       }
@@ -1003,7 +1024,7 @@ __global__ void __launch_bounds__(kThreads) gemv_chain_kernel(const ChainLaunch 
                                zshift) & (BITS != 8 ? 0xFFu : 0xFFFFu);
         }
       const int xo = i * U::kBlocks * kColsPerBlock;
-      compute_unit<NB, GS, SYM, kXCoherent, BITS>(r, xl0 + xo, xl1 + xo, tot);
+      compute_unit<NB, GS, SYM, kXCoherent, BITS, false>(r, xl0 + xo, xl1 + xo, tot);
       issue_unit(i + D);
     }
     cp_async_wait_all();
