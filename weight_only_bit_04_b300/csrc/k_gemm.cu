@@ -251,6 +251,74 @@ __device__ __forceinline__ void dequant_tile(const StepRegs<GS, SYM, BITS>& r, i
   }
 }
 
+// One 64-column step of a warp's 32 weight rows (two 16-row tiles, lane
+// quarter q4 of the 128-row tile): read the packed codes, scales and zero
+// points of the step from the stage's weight tile `ws`, expand them and store
+// the fp16 A operand into tensor memory at column `col`. ng: groups the step
+// carries; a dead tile (rows beyond N) stores zeros.
+template <int GS, bool SYM, int BITS>
+__device__ __forceinline__ void dequant_step(const unsigned char* ws, int ng, bool live, int q4, int lane,
+                                             uint32_t col) {
+  using WT = WTile<BITS>;
+  const int g = lane >> 2;
+  StepRegs<GS, SYM, BITS> r;
+  if (live) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int r16 = 2 * q4 + h;
+      if (BITS == 3) {
+        // the pair's 16-byte parts, then its 8-byte parts (768 bytes per pair)
+        if (h == 0) {
+          r.w[0][0] = *reinterpret_cast<const uint4*>(ws + q4 * 768 + lane * 16);
+        } else {
+          const uint2 b2 = *reinterpret_cast<const uint2*>(ws + q4 * 768 + 512 + lane * 8);
+          r.w[1][0] = make_uint4(b2.x, b2.y, 0u, 0u);
+        }
+      } else {
+#pragma unroll
+        for (int part = 0; part < kGemmParts<BITS>; ++part)
+          r.w[h][part] = *reinterpret_cast<const uint4*>(ws + r16 * WT::kR16 + part * 512 + lane * 16);
+      }
+#pragma unroll
+      for (int gg = 0; gg < StepRegs<GS, SYM, BITS>::kGroups; ++gg) {
+        const int gs = min(gg, ng - 1);  // the padding half of a ragged last step reuses the last group
+        r.s[h][gg] = *reinterpret_cast<const uint32_t*>(ws + WT::kScaleOff + gs * 256 + (r16 * 8 + g) * 4);
+        r.z[h][gg] = SYM ? 0u
+                     : BITS != 8
+                         ? uint32_t(ws[WT::kZeroOff + gs * 64 + r16 * 8 + g])
+                         : uint32_t(*reinterpret_cast<const uint16_t*>(ws + WT::kZeroOff + gs * 128 + (r16 * 8 + g) * 2));
+      }
+    }
+  }
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    uint32_t v[16];
+    if (live) {
+      dequant_tile<GS, SYM, BITS>(r, h, v);
+    } else {
+#pragma unroll
+      for (int e = 0; e < 16; ++e) v[e] = 0u;
+    }
+    tmem_st_16x256b_x4(col + (uint32_t(32 * q4 + 16 * h) << 16), v);
+  }
+}
+
+// Bulk copies of one step's packed weights of 128-row block R (codes, then
+// the scale pairs and zero points of its ng groups from group g0) to the
+// stage's weight tile at wdst, completing on barrier bar.
+template <bool SYM, int BITS>
+__device__ __forceinline__ void load_weight_step(uint32_t wdst, const GemmArgs& a, int R, int kbg, int g0, int ng,
+                                                 uint32_t bar) {
+  using WT = WTile<BITS>;
+  const unsigned char* qbytes = reinterpret_cast<const unsigned char*>(a.qweight);
+  const unsigned char* sbytes = reinterpret_cast<const unsigned char*>(a.scales2);
+  bulk_copy_g2s(wdst, qbytes + (size_t(R) * a.KB + kbg) * WT::kCodes, WT::kCodes, bar);
+  bulk_copy_g2s(wdst + WT::kScaleOff, sbytes + (size_t(R) * a.G + g0) * 256, uint32_t(ng * 256), bar);
+  if (!SYM)
+    bulk_copy_g2s(wdst + WT::kZeroOff, a.zeros + (size_t(R) * a.G + g0) * WT::kZeroGroup,
+                  uint32_t(ng * WT::kZeroGroup), bar);
+}
+
 template <int WR, int NT, int SA, int SB, int DS, int GS, bool SYM, int BITS>
 __global__ void __launch_bounds__(Cfg<WR, NT, SA, SB, DS, BITS>::kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const GemmArgs a) {
@@ -308,7 +376,6 @@ __global__ void __launch_bounds__(Cfg<WR, NT, SA, SB, DS, BITS>::kThreads, 1)
     const int q4 = warp & 3;   // tensor-memory lane quarter: rows 32*q4 .. 32*q4+31 of the tile
     const int R = rg * WR + at;
     const bool live = R < a.NR;
-    const int g = lane >> 2;
     const int nsteps = KB > ds ? (KB - ds + DS - 1) / DS : 0;  // steps of this set
 
     // The packed weights of a step arrive with its activations (TMA warp);
@@ -327,48 +394,8 @@ __global__ void __launch_bounds__(Cfg<WR, NT, SA, SB, DS, BITS>::kThreads, 1)
       }
       tc_fence_after();
       const unsigned char* ws = smem + size_t(sb) * C::kStage + C::kBStage + at * WT::kBytes;
-      const int ng = step_groups<GS>(kb_lo + kb, a.G);
-      StepRegs<GS, SYM, BITS> r;
-      if (live) {
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int r16 = 2 * q4 + h;
-          if (BITS == 3) {
-            // the pair's 16-byte parts, then its 8-byte parts (768 bytes per pair)
-            if (h == 0) {
-              r.w[0][0] = *reinterpret_cast<const uint4*>(ws + q4 * 768 + lane * 16);
-            } else {
-              const uint2 b2 = *reinterpret_cast<const uint2*>(ws + q4 * 768 + 512 + lane * 8);
-              r.w[1][0] = make_uint4(b2.x, b2.y, 0u, 0u);
-            }
-          } else {
-#pragma unroll
-            for (int part = 0; part < kGemmParts<BITS>; ++part)
-              r.w[h][part] = *reinterpret_cast<const uint4*>(ws + r16 * WT::kR16 + part * 512 + lane * 16);
-          }
-#pragma unroll
-          for (int gg = 0; gg < StepRegs<GS, SYM, BITS>::kGroups; ++gg) {
-            const int gs = min(gg, ng - 1);  // the padding half of a ragged last step reuses the last group
-            r.s[h][gg] = *reinterpret_cast<const uint32_t*>(ws + WT::kScaleOff + gs * 256 + (r16 * 8 + g) * 4);
-            r.z[h][gg] = SYM ? 0u
-                         : BITS != 8
-                             ? uint32_t(ws[WT::kZeroOff + gs * 64 + r16 * 8 + g])
-                             : uint32_t(*reinterpret_cast<const uint16_t*>(ws + WT::kZeroOff + gs * 128 + (r16 * 8 + g) * 2));
-          }
-        }
-      }
-      const uint32_t col = tmem + uint32_t(C::kACol0 + (sa * WR + at) * 32);
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        uint32_t v[16];
-        if (live) {
-          dequant_tile<GS, SYM, BITS>(r, h, v);
-        } else {
-#pragma unroll
-          for (int e = 0; e < 16; ++e) v[e] = 0u;
-        }
-        tmem_st_16x256b_x4(col + (uint32_t(32 * q4 + 16 * h) << 16), v);
-      }
+      dequant_step<GS, SYM, BITS>(ws, step_groups<GS>(kb_lo + kb, a.G), live, q4, lane,
+                                  tmem + uint32_t(C::kACol0 + (sa * WR + at) * 32));
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(full_a(sa));
@@ -430,8 +457,6 @@ __global__ void __launch_bounds__(Cfg<WR, NT, SA, SB, DS, BITS>::kThreads, 1)
       tma_prefetch_desc(&tmap_x);
       pdl_wait();  // x may come from the preceding gather kernel
       int issued = 0;
-      const unsigned char* qbytes = reinterpret_cast<const unsigned char*>(a.qweight);
-      const unsigned char* sbytes = reinterpret_cast<const unsigned char*>(a.scales2);
       for (int kb = 0; kb < KB; ++kb) {
         const int s = kb % SB;
         const int n = kb / SB;
@@ -450,12 +475,7 @@ __global__ void __launch_bounds__(Cfg<WR, NT, SA, SB, DS, BITS>::kThreads, 1)
         for (int t = 0; t < WR; ++t) {
           const int R = rg * WR + t;
           if (R >= a.NR) continue;
-          const uint32_t wdst = stage + uint32_t(C::kBStage + t * WT::kBytes);
-          bulk_copy_g2s(wdst, qbytes + (size_t(R) * a.KB + kbg) * WT::kCodes, WT::kCodes, full_b(s));
-          bulk_copy_g2s(wdst + WT::kScaleOff, sbytes + (size_t(R) * a.G + g0) * 256, uint32_t(ng * 256), full_b(s));
-          if (!SYM)
-            bulk_copy_g2s(wdst + WT::kZeroOff, a.zeros + (size_t(R) * a.G + g0) * WT::kZeroGroup,
-                          uint32_t(ng * WT::kZeroGroup), full_b(s));
+          load_weight_step<SYM, BITS>(stage + uint32_t(C::kBStage + t * WT::kBytes), a, R, kbg, g0, ng, full_b(s));
         }
         ++issued;
       }
