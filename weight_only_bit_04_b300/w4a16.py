@@ -168,8 +168,22 @@ def _stream(stream) -> int:
     if stream is None:
         return torch.cuda.current_stream().cuda_stream
     if isinstance(stream, torch.cuda.Stream):
+        if stream.device.index != torch.cuda.current_device():
+            raise ValueError(f"stream is on {stream.device}, the current device is cuda:{torch.cuda.current_device()}")
         return stream.cuda_stream
     return int(stream)
+
+
+def _keep_alive(stream, *tensors) -> None:
+    """Tensors allocated here and used by a kernel on a caller-given stream:
+    tell the caching allocator, so that their memory is not handed out again
+    before that stream's work is done."""
+    if stream is None:
+        return
+    s = stream if isinstance(stream, torch.cuda.Stream) else torch.cuda.ExternalStream(int(stream))
+    for t in tensors:
+        if t is not None:
+            t.record_stream(s)
 
 
 def _dev(t: torch.Tensor, dtype: torch.dtype, name: str, shape=None) -> int:
@@ -177,6 +191,8 @@ def _dev(t: torch.Tensor, dtype: torch.dtype, name: str, shape=None) -> int:
         raise TypeError(f"{name} must be a torch.Tensor")
     if not t.is_cuda:
         raise ValueError(f"{name} must be a CUDA tensor")
+    if t.device.index != torch.cuda.current_device():
+        raise ValueError(f"{name} is on {t.device}, the current device is cuda:{torch.cuda.current_device()}")
     if t.dtype != dtype:
         raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
     if not t.is_contiguous():
@@ -223,8 +239,7 @@ def quantize_rtn(fmt: Format, w: torch.Tensor, g_idx=None, act_scale=None, strea
         st = lib().w4a16_quantize_rtn(ctypes.byref(fmt), wp, gip, q.data_ptr(), scales.data_ptr(), zp,
                                       wsp, ws_bytes, _stream(stream))
         _check("w4a16_quantize_rtn", st)
-    if ws_bytes and isinstance(stream, torch.cuda.Stream):
-        ws.record_stream(stream)
+    _keep_alive(stream, ws, q, scales, zeros)
     return q, scales, zeros
 
 
@@ -235,7 +250,8 @@ def gemv_grouped(fmts, packeds, x: torch.Tensor, outs=None, weights_ready: bool 
     M = x.shape[0]
     K = fmts[0].K
     xp = _dev(x, torch.float16, "x", (M, K))
-    if outs is None:
+    allocated = outs is None
+    if allocated:
         outs = [torch.empty((M, f.N), dtype=torch.float16, device=x.device) for f in fmts]
     fa = (Format * n)(*fmts)
     pa = (ctypes.c_void_p * n)(*[_dev(p, torch.uint8, "packed") for p in packeds])
@@ -245,6 +261,8 @@ def gemv_grouped(fmts, packeds, x: torch.Tensor, outs=None, weights_ready: bool 
              (GEMV_REGISTER_RING if register_ring else 0) | (GEMV_ASYNC_COPY if async_copy else 0))
     st = lib().w4a16_gemv_grouped(fa, pa, ba, n, xp, ya, M, flags, _stream(stream))
     _check("w4a16_gemv_grouped", st)
+    if allocated:
+        _keep_alive(stream, *outs)
     return outs
 
 
@@ -273,8 +291,7 @@ def gptq(fmt: Format, w: torch.Tensor, x: torch.Tensor, damp: float = 0.01, stre
                           None if zeros is None else zeros.data_ptr(), None if gidx is None else gidx.data_ptr(),
                           ws.data_ptr(), nbytes, _stream(stream))
     _check("w4a16_gptq", st)
-    if isinstance(stream, torch.cuda.Stream):
-        ws.record_stream(stream)
+    _keep_alive(stream, ws, q, scales, zeros, gidx)
     return q, scales, zeros, (None if gidx is None else gidx.cpu().numpy())
 
 
@@ -290,7 +307,8 @@ def pack(fmt: Format, q: torch.Tensor, scales: torch.Tensor, zeros=None, g_idx=N
     sp = _dev(scales, torch.float16, "scales", (N, G))
     zp = None if zeros is None else _dev(zeros, torch.uint8, "zeros", (N, G))
     ap = None if act_scale is None else _dev(act_scale, torch.float16, "act_scale", (K,))
-    if out is None:
+    allocated = out is None
+    if allocated:
         out = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
     op = _dev(out, torch.uint8, "out")
     gi, gip = _host_gidx(g_idx, K)
@@ -302,15 +320,20 @@ def pack(fmt: Format, q: torch.Tensor, scales: torch.Tensor, zeros=None, g_idx=N
             raise ValueError("act_scale given but the format has no act scale")
         st = lib().w4a16_pack(ctypes.byref(fmt), qp, sp, zp, gip, op, out.numel(), _stream(stream))
         _check("w4a16_pack", st)
+    if allocated:
+        _keep_alive(stream, out)
     return out
 
 
 def dequant(fmt: Format, packed: torch.Tensor, out: torch.Tensor | None = None, stream=None):
     pp = _dev(packed, torch.uint8, "packed")
-    if out is None:
+    allocated = out is None
+    if allocated:
         out = torch.empty((fmt.N, fmt.K), dtype=torch.float16, device=packed.device)
     op = _dev(out, torch.float16, "out", (fmt.N, fmt.K))
     _check("w4a16_dequant", lib().w4a16_dequant(ctypes.byref(fmt), pp, packed.numel(), op, _stream(stream)))
+    if allocated:
+        _keep_alive(stream, out)
     return out
 
 
@@ -338,7 +361,8 @@ def gemv(fmt: Format, packed: torch.Tensor, x: torch.Tensor, out: torch.Tensor |
     M = x.shape[0]
     pp = _dev(packed, torch.uint8, "packed")
     xp = _dev(x, torch.float16, "x", (M, fmt.K))
-    if out is None:
+    allocated = out is None
+    if allocated:
         out = torch.empty((M, fmt.N), dtype=torch.float16, device=x.device)
     yp = _dev(out, torch.float16, "out", (M, fmt.N))
     flags = ((GEMV_WEIGHTS_READY if weights_ready else 0) | (GEMV_REGISTER_RING if register_ring else 0)
@@ -350,6 +374,8 @@ def gemv(fmt: Format, packed: torch.Tensor, x: torch.Tensor, out: torch.Tensor |
     else:
         st = lib().w4a16_gemv(ctypes.byref(fmt), pp, packed.numel(), xp, yp, M, _stream(stream))
     _check("w4a16_gemv", st)
+    if allocated:
+        _keep_alive(stream, out)
     return out
 
 
@@ -366,11 +392,13 @@ def gemm(fmt: Format, packed: torch.Tensor, x: torch.Tensor, out: torch.Tensor |
     M = x.shape[0]
     pp = _dev(packed, torch.uint8, "packed")
     xp = _dev(x, torch.float16, "x", (M, fmt.K))
-    if out is None:
+    allocated = out is None
+    if allocated:
         out = torch.empty((M, fmt.N), dtype=torch.float16, device=x.device)
     yp = _dev(out, torch.float16, "out", (M, fmt.N))
     need = gemm_workspace_bytes(fmt, M)
-    if need and workspace is None:
+    own_ws = bool(need) and workspace is None
+    if own_ws:
         workspace = torch.empty(need, dtype=torch.uint8, device=x.device)
     wp = None if not need else _dev(workspace, torch.uint8, "workspace")
     wbytes = 0 if not need else workspace.numel()
@@ -380,6 +408,7 @@ def gemm(fmt: Format, packed: torch.Tensor, x: torch.Tensor, out: torch.Tensor |
     else:
         st = lib().w4a16_gemm(ctypes.byref(fmt), pp, packed.numel(), xp, yp, M, wp, wbytes, _stream(stream))
     _check("w4a16_gemm", st)
+    _keep_alive(stream, out if allocated else None, workspace if own_ws else None)
     return out
 
 
