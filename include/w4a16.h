@@ -68,18 +68,19 @@ typedef enum {
 
 /*
  * Quantization format of one linear layer (out features N x in features K).
- *   bits        4 or 8 (b below; codes 0 .. 2^b - 1).
+ *   bits        3, 4 or 8 (b below; codes 0 .. 2^b - 1).
  *   group_size  32, 64 or 128; K must be a multiple of it (G = K / group_size
- *               groups per row). 128 is the common default; smaller groups
- *               track the weights more closely and cost more bits ("What W4A16
- *               buys ...").
+ *               groups per row). 128 is the common default; a smaller group
+ *               follows the weights better at the price of more metadata bits
+ *               per weight ("What W4A16 buys ...").
  *   symmetric   0: asymmetric, one b-bit zero point per (row, group);
  *               1: symmetric, zero point fixed at 2^(b-1) (8 or 128), no
  *                  zero points stored.
  *   has_g_idx   0: column k belongs to group k / group_size;
  *               1: GPTQ act order -- a column-to-group map g_idx is given at
- *                  pack time ("The two algorithms, compactly": act order
- *                  quantizes the columns with the largest activations first).
+ *                  pack time ("The two algorithms, compactly": under act
+ *                  order the columns are taken in descending order of their
+ *                  activation energy).
  *   N, K        1 <= N <= 2^20, group_size <= K <= 2^20.
  *   has_act_scale 0: none;
  *               1: unfolded AWQ -- the blob carries a per-input-channel
@@ -230,9 +231,9 @@ W4A16_API w4a16_status w4a16_pack_awq(const w4a16_format* f, const uint8_t* q, c
 
 /*
  * GPTQ ("AWQ + GPTQ Quantization, in depth", section "The two algorithms,
- * compactly"): quantize the layer one input column at a time, pushing each
- * column's rounding error onto the columns not yet quantized, weighted by the
- * inverse of H = 2 X X^T of the calibration activations. On the device, in
+ * compactly"): quantize the layer one input column at a time; each column's
+ * rounding error is compensated on the remaining (later) columns, with weights
+ * taken from the inverse of H = 2 X X^T of the calibration activations. On the device, in
  * fp64: H, H += damp * mean(diag H) * I (a channel whose activations are all
  * zero gets diag 1 first), the upper Cholesky factor U of H^-1, then per
  * column j (in order, or -- f->has_g_idx -- by descending diag H, ties to the

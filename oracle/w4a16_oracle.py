@@ -5,8 +5,8 @@ imports this module.
 
 What it computes, step by step, and where each step comes from:
 
-1. Group map. By default input column j belongs to group j // g: "each run of
-   128 consecutive input weights in a row typically shares one scale"
+1. Group map. By default input column j belongs to group j // g: the usual
+   group is 128 neighbouring input columns of one row under one scale
    ("AWQ + GPTQ Quantization, in depth", section "What W4A16 buys and why
    decoding gets faster"). With GPTQ act order a column->group map ``g_idx``
    is given instead ("The two algorithms, compactly": act order; the Q&A page
@@ -14,8 +14,8 @@ What it computes, step by step, and where each step comes from:
    hold exactly g columns.
 2. Scale and zero per (row, group), round to nearest ("LLM Quantization:
    INT8, GPTQ, and AWQ Explained", section "What quantization actually does":
-   find the range, pick the scale that spreads the integer grid over it, round
-   each weight to the nearest grid point). With b-bit codes, qmax = 2^b - 1:
+   find the range, pick the scale that spreads the integer grid over it, and
+   move every weight to its closest grid value). With b-bit codes, qmax = 2^b - 1:
    asymmetric: s = fp16((max - min) / qmax), z = clamp(rint(-min / s), 0, qmax);
    symmetric, 3 or 4 bits: s = fp16(2 * max|w| / qmax), z = 2^(b-1) (the
      linear formula over [-a, a], which reproduces the fixed zero point 8 of
@@ -37,16 +37,17 @@ What it computes, step by step, and where each step comes from:
    row: column k in stream bits 3k .. 3k+2, 32 codes per 3 words.
 5. Dequantization w_hat = fp16((q - z) * s) ("The Math of Quantization":
    x_approx = (q - Z) * S). The fp64 product is exact; one round to nearest
-   even gives the fp16 weight ("the actual matrix multiply still happens in
-   fp16: each block is dequantized back to fp16", INT8/GPTQ/AWQ page).
+   even gives the fp16 weight (the INT8/GPTQ/AWQ page: the product itself is
+   computed in fp16, on weights expanded back to fp16 block by block).
 6. Output y = x . w_hat^T in fp64 (W is "out x in", "The two algorithms,
    compactly"), with the per-element bound B = |x| . |w_hat|^T used by the
    acceptance test |y_gpu - y| <= 2e-3 * B + 1e-3.
 
 7. AWQ with the per-input-channel scale kept apart ("The two algorithms,
-   compactly": AWQ multiplies the weights of salient input channels by a
-   scale s > 1 before quantizing and divides the activations by the same
-   scale; folding 1/s into the preceding operation is the usual deployment).
+   compactly": AWQ enlarges the weights of salient input channels by a factor
+   s > 1 before quantizing and shrinks those activation channels by s to
+   compensate; folding 1/s into the preceding operation is the usual
+   deployment).
    Unfolded, the layer stores s (fp16 [K]) and computes
    y = fp16(x / s) . dequant(quantize(fp16(W * s)))^T: both the product and
    the quotient are exact in fp64 and rounded once to fp16. The scale search
@@ -75,7 +76,7 @@ import numpy as np
 QMAX = 15  # 4-bit codes are 0..15
 SYM_ZERO = 8  # symmetric 4-bit scheme: zero point fixed at 8
 # code widths: 4 bits, and the other two the pages name ("How do GPTQ and AWQ
-# differ ...", section "The shared setting": 3 and 8 are also possible)
+# differ ...", section "The shared setting": 3 and 8 bits)
 BITS = (3, 4, 8)
 
 

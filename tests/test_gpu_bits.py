@@ -1,5 +1,5 @@
-"""3- and 8-bit codes (W3A16, W8A16: "3 and 8 are also possible", "How do
-GPTQ and AWQ differ ...", section "The shared setting") through the same entry
+"""3- and 8-bit codes (W3A16, W8A16: the other widths named in "How do GPTQ
+and AWQ differ ...", section "The shared setting") through the same entry
 points: quantize / pack / dequant bit-exact against the CPU oracle, and both
 products within the per-element bound |y_gpu - y_ref| <= 2e-3 * sum_k |x * w_hat| + 1e-3.
 Every test runs once per width.

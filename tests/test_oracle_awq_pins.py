@@ -1,8 +1,8 @@
 """Pins of the oracle's unfolded-AWQ step (CPU only).
 
 "The two algorithms, compactly" (AWQ + GPTQ Quantization, in depth): AWQ
-multiplies the salient input channels' weights by a scale s > 1 before
-quantizing and divides the activations by the same scale. These tests fix the
+enlarges the weights of the salient input channels by a factor s > 1 before
+quantizing and shrinks those activation channels by s to compensate. These tests fix the
 oracle's version of that step against exact rational arithmetic, against the
 plain layer where the mathematics says the two must agree exactly, against a
 pure-Python restatement, and check the scale search's invariants.

@@ -118,8 +118,8 @@ def test_large_damping_tends_to_round_to_nearest():
 def test_gptq_lowers_the_layer_error_and_act_order_lowers_it_more():
     """The method's purpose: on the calibration inputs the GPTQ layer's output
     error is below round-to-nearest's; act order, which quantizes the
-    largest-activation columns first "while there are still many columns left
-    to absorb their error", lowers it further (synthetic inputs with 2 %
+    largest-activation columns early, when most columns are still free to take
+    up their error, lowers it further (synthetic inputs with 2 %
     outlier channels, otherwise uncorrelated: about -11 % and -23 %)."""
     N, K, T, g = 64, 256, 512, 128
     W = synth.weights_np(N, K, 64)

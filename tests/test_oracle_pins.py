@@ -432,7 +432,7 @@ def test_w4_bigger_vs_w8_smaller_use_similar_memory():
     g = _golden()["w4_3b_vs_w8_1p5b"]["params_B"]
     b4 = g["w4"] * 1e9 * O.bits_per_weight(128, False, 4) / 8
     b8 = g["w8"] * 1e9 * O.bits_per_weight(128, False, 8) / 8
-    assert abs(b4 / b8 - 1) < 0.05  # "similar memory": 1.559 vs 1.535 GB
+    assert abs(b4 / b8 - 1) < 0.05  # about the same weight memory: 1.559 vs 1.535 GB
 
 
 def test_int8_absmax_hand_example():
@@ -510,8 +510,9 @@ def test_pack_codes_8bit_every_byte_position_and_roundtrip():
 
 
 # ---------------------------------------------------------------------------
-# 3-bit codes (W3A16): "3 and 8 are also possible" ("How do GPTQ and AWQ
-# differ ...", section "The shared setting"); the same group machinery, 8 levels
+# 3-bit codes (W3A16): 3 and 8 bits are named as the other widths ("How do
+# GPTQ and AWQ differ ...", section "The shared setting"); the same group
+# machinery, 8 levels
 # ---------------------------------------------------------------------------
 def test_3bit_levels_and_bits_per_weight():
     assert O.qmax(3) == 7 and O.sym_zero(3) == 4

@@ -10,16 +10,16 @@ Recipe (shapes and distributions of the workloads the pages discuss):
 * Weights W [N, K]: N(0, 0.02) drawn in fp32, rounded to fp16.
 * Activations x [M, K]: N(0, 1) in fp32; a seeded set of "outlier channels"
   (the same input channels for every token row, chosen without replacement)
-  is multiplied by 20; then rounded to fp16. Outlier channels -- a few input
-  channels with much larger activations -- are what both calibration methods
+  is multiplied by 20; then rounded to fp16. Such channels, a handful of
+  inputs whose activations dwarf the rest, are what both calibration methods
   react to ("AWQ + GPTQ Quantization, in depth", section "Why small models lose
   more at 4 bits"; "LLM Quantization: INT8, GPTQ, and AWQ Explained", section
   "Round-to-nearest, and where it falls apart").
 * Act order: a synthetic diag(H) with H = 2 X X^T over the workload's own
   activations, d_j = 2 * sum_t x[t, j]^2; columns are ranked by descending d
   (ties: lower column first) and column j goes to group rank(j) // g
-  ("The two algorithms, compactly": act order quantizes the columns with the
-  largest activations first).
+  ("The two algorithms, compactly": under act order the columns are taken in
+  descending order of their activation energy).
 
 Seeds are derived from (workload, layer, linear, tensor) names so every run,
 here or on another machine, draws the same numbers.
