@@ -10,7 +10,7 @@
  * or 8-bit smaller"). The format follows "AWQ + GPTQ Quantization, in depth",
  * section "What W4A16 buys and why decoding gets faster" (packed 4-bit weights
  * expanded to 16 bits in registers with the group's scale and zero point; one
- * scale per run of 128 consecutive input weights of a row) and "LLM
+ * scale per group of 128 neighbouring input columns of a row) and "LLM
  * Quantization: A Deep Dive into GPTQ, AWQ, and Post-Training Quantization",
  * section "The Math of Quantization" (q = round(x/S) + Z, x ~ (q - Z) * S).
  * The knobs -- bits, group_size, symmetric/zero point, act order (desc_act,

@@ -19,7 +19,7 @@ Sources (web pages on 4-bit weight-only quantization):
 
 * "AWQ + GPTQ Quantization, in depth" -- section "What W4A16 buys and why
   decoding gets faster" (4-bit weights, 16-bit activations, one fp16 scale and
-  a 4-bit zero point per run of 128 consecutive input weights) and "The two
+  a 4-bit zero point per group of 128 neighbouring input columns) and "The two
   algorithms, compactly" (W is out x in; act order quantizes columns by
   descending diag(H)).
 * "LLM Quantization: A Deep Dive into GPTQ, AWQ, and Post-Training

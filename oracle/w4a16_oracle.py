@@ -14,7 +14,7 @@ What it computes, step by step, and where each step comes from:
    hold exactly g columns.
 2. Scale and zero per (row, group), round to nearest ("LLM Quantization:
    INT8, GPTQ, and AWQ Explained", section "What quantization actually does":
-   find the range, pick the scale that spreads the integer grid over it, and
+   find the range, choose the scale that stretches the integer levels across it, and
    move every weight to its closest grid value). With b-bit codes, qmax = 2^b - 1:
    asymmetric: s = fp16((max - min) / qmax), z = clamp(rint(-min / s), 0, qmax);
    symmetric, 3 or 4 bits: s = fp16(2 * max|w| / qmax), z = 2^(b-1) (the
@@ -336,7 +336,7 @@ def w4a16_linear(x, W, group_size: int, sym: bool, g_idx=None, bits: int = 4):
 def packed_bytes_closed_form(N: int, K: int, group_size: int, sym: bool, bits: int = 4) -> float:
     """Bytes of one packed linear: codes N*K*b/8, fp16 scales N*G*2, b-bit
     zeros N*G*b/8 (none when symmetric), G = K / group_size ("What W4A16
-    buys": 16-bit scale per 128 weights = 0.125 bit/weight, 4-bit zero ~0.03)."""
+    buys": one fp16 scale for a group of 128 = 0.125 bit/weight, 4-bit zero ~0.03)."""
     G = K / group_size
     return N * K * bits / 8 + N * G * 2 + (0 if sym else N * G * bits / 8)
 

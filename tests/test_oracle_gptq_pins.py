@@ -1,7 +1,7 @@
 """Pins of the oracle's GPTQ step (CPU only).
 
 "The two algorithms, compactly" (AWQ + GPTQ Quantization, in depth): GPTQ
-quantizes one column at a time and, weighted by the inverse of H = 2 X X^T,
+quantizes one column at a time and, with weights from the inverse of H = 2 X X^T,
 pushes each column's rounding error onto the columns not yet quantized. The
 oracle follows the page's Cholesky formulation; these tests tie it to an
 independent restatement (after every column, the remaining weights are the
