@@ -14,8 +14,8 @@ What it computes, step by step, and where each step comes from:
    hold exactly g columns.
 2. Scale and zero per (row, group), round to nearest ("LLM Quantization:
    INT8, GPTQ, and AWQ Explained", section "What quantization actually does":
-   find the range, choose the scale that stretches the integer levels across it, and
-   move every weight to its closest grid value). With b-bit codes, qmax = 2^b - 1:
+   find the range, choose the scale that stretches the integer levels
+   across it, and move every weight to its closest grid value). With b-bit codes, qmax = 2^b - 1:
    asymmetric: s = fp16((max - min) / qmax), z = clamp(rint(-min / s), 0, qmax);
    symmetric, 3 or 4 bits: s = fp16(2 * max|w| / qmax), z = 2^(b-1) (the
      linear formula over [-a, a], which reproduces the fixed zero point 8 of
