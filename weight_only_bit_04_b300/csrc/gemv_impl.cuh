@@ -291,9 +291,10 @@ __device__ __forceinline__ void load_unit(UnitRegs<GS, BITS>& r, const uint32_t*
 // (token rows g and g+8, column 4t) for the unit's first column.
 // SPLIT: even and odd 16-column steps accumulate into separate sets, twice
 // the independent MMA chains (consecutive MMAs into one accumulator wait for
-// each other). Measured on B300: faster for the register ring (4096x11008:
-// 8.63 -> 7.84 us), slower for the asynchronous-copy ring (28672x8192:
-// 30.3 -> 32.3 us), which therefore keeps one set.
+// each other). Measured on B300, it pays only in the 4-bit register ring
+// (4096x11008: 8.63 -> 7.84 us). It is slower in the asynchronous-copy ring
+// (28672x8192: 30.3 -> 32.3 us) and in the 8-bit register ring (4096x4096:
+// 5.48 -> 7.88 us), and 3-bit codes lose 2.5 % of the decode step with it.
 template <int NB, int GS, bool SYM, int XM, int BITS, bool SPLIT>
 __device__ __forceinline__ void compute_unit(const UnitRegs<GS, BITS>& r, const uint16_t* xl0, const uint16_t* xl1,
                                              float tot[kTilesPerWarp][NB][4]) {
@@ -597,7 +598,7 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const GemvArgs a) {
                                zshift) & (BITS != 8 ? 0xFFu : 0xFFFFu);
         }
       const int xo = i * U::kBlocks * kColsPerBlock;
-      compute_unit<NB, GS, SYM, STAGED ? kXShared : kXGlobal, BITS, !WB>(r, xl0 + xo, xl1 + xo, tot);
+      compute_unit<NB, GS, SYM, STAGED ? kXShared : kXGlobal, BITS, !WB && BITS == 4>(r, xl0 + xo, xl1 + xo, tot);
       issue_unit(i + D);  // refills the slot just read (this thread's own entries)
     }
     cp_async_wait_all();
@@ -608,7 +609,7 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const GemvArgs a) {
         const int i = i0 + s;
         if (i < nunit) {
           const int xo = i * U::kBlocks * kColsPerBlock;
-          compute_unit<NB, GS, SYM, STAGED ? kXShared : kXGlobal, BITS, !WB>(ring[s], xl0 + xo, xl1 + xo, tot);
+          compute_unit<NB, GS, SYM, STAGED ? kXShared : kXGlobal, BITS, !WB && BITS == 4>(ring[s], xl0 + xo, xl1 + xo, tot);
           if (i + PF < nunit) load_unit<GS, SYM, BITS>(ring[s], qp, sp, zp, i + PF, gmax);
         }
       }
