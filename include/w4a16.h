@@ -7,7 +7,8 @@
  * of `group_size` input columns, fp16 activations x and outputs y, fp32
  * accumulation. The same entry points take 8-bit codes (W8A16, the wider
  * choice weighed in "AWQ + GPTQ Quantization, in depth", section "4-bit bigger
- * or 8-bit smaller"). The format follows "AWQ + GPTQ Quantization, in depth",
+ * or 8-bit smaller") and 3-bit codes (W3A16; 3 and 8 bits are the other widths
+ * named in "How do GPTQ and AWQ differ ...", section "The shared setting"). The format follows "AWQ + GPTQ Quantization, in depth",
  * section "What W4A16 buys and why decoding gets faster" (packed 4-bit weights
  * expanded to 16 bits in registers with the group's scale and zero point; one
  * scale per group of 128 neighbouring input columns of a row) and "LLM
@@ -60,7 +61,7 @@ typedef struct CUstream_st* w4a16_stream_t;
 typedef enum {
   W4A16_OK = 0,
   W4A16_ERR_INVALID_ARG = 1,     /* NULL pointer, bad size, M out of range, bad g_idx */
-  W4A16_ERR_UNSUPPORTED = 2,     /* valid but not implemented (bits not 4 or 8, group size, ...) */
+  W4A16_ERR_UNSUPPORTED = 2,     /* valid but not implemented (bits not 3, 4 or 8, group size, ...) */
   W4A16_ERR_MISALIGNED = 3,      /* a pointer is not aligned as documented */
   W4A16_ERR_BUFFER_TOO_SMALL = 4,/* packed_bytes or workspace_bytes below the requirement */
   W4A16_ERR_CUDA = 5             /* a CUDA call failed; see w4a16_last_cuda_error() */
@@ -109,12 +110,13 @@ typedef struct {
  * With NR = ceil(N / 128) row blocks, KB = ceil(K / 64) column blocks and
  * G = K / group_size, it holds up to five sub-arrays, each starting on a
  * 256-byte boundary, in this order:
- *   qweight  NR*KB*512*b bytes: for every (row block, column block) a tile
- *            of 128 rows x 64 columns of b-bit codes (4 or 8 KiB), arranged
- *            so that a warp's 16-byte loads yield tensor-core operand
- *            fragments.
+ *   qweight  NR*KB*1024*b bytes: for every (row block, column block) a tile
+ *            of 128 rows x 64 columns of b-bit codes (3, 4 or 8 KiB),
+ *            arranged so that a warp's 16-byte (3 bits: 16- and 8-byte)
+ *            loads yield tensor-core operand fragments.
  *   scales   NR*G*256 bytes: fp16 scales, 128 rows per (row block, group).
- *   zeros    NR*G*16*b bytes (asymmetric only): b-bit zero points.
+ *   zeros    (asymmetric only) NR*G*64 bytes of 4-bit zero points for 3- and
+ *            4-bit codes, NR*G*128 bytes of 8-bit ones for 8-bit codes.
  *   perm     K*4 bytes (act order only): packed column -> original column.
  *   act_scale K*2 bytes (has_act_scale only): fp16 s in packed column order.
  * Rows beyond N and columns beyond K are padding. The blob's meaning is fixed
@@ -140,7 +142,8 @@ W4A16_API int w4a16_last_cuda_error(void);
  * round to the nearest grid point, clamp). Per (row n, group t), in fp64,
  * with qmax = 2^b - 1:
  *   asymmetric: s = fp16_rne((max - min) / qmax), z = clamp(rint(-min / s), 0, qmax)
- *   symmetric, 4 bits: s = fp16_rne(2 * max|w| / 15), z = 8
+ *   symmetric, 3 or 4 bits: s = fp16_rne(2 * max|w| / qmax), z = 2^(b-1)
+ *               (4 at 3 bits, 8 at 4 bits)
  *   symmetric, 8 bits: s = fp16_rne(max|w| / 127), z = 128 (the int8 absmax
  *               code of the same section, stored offset by 128), and
  *               q = clamp(rint(w / s), -127, 127) + 128 (codes 1 .. 255)
@@ -191,11 +194,12 @@ W4A16_API w4a16_status w4a16_quantize_rtn_noalloc(const w4a16_format* f, const u
 
 /*
  * Pack canonical codes, scales and zero points into the device blob.
- *   q        uint8 [N][K], codes 0 .. 2^b - 1 (4 bits: only the low 4 bits
- *            are used).
+ *   q        uint8 [N][K], codes 0 .. 2^b - 1 (3 and 4 bits: only the low b
+ *            bits are used).
  *   scales   fp16 [N][G], 2-byte aligned.
- *   zeros    uint8 [N][G] codes when asymmetric (4 bits: low 4 bits used);
- *            NULL when symmetric.
+ *   zeros    uint8 [N][G] codes 0 .. 2^b - 1 when asymmetric (3 and 4 bits:
+ *            the low 4 bits are stored, so a 3-bit zero point above 7 is
+ *            kept as given; it is not checked); NULL when symmetric.
  *   g_idx    HOST int32 [K] when f->has_g_idx, else NULL. Every group
  *            0..G-1 must have exactly group_size members (checked here);
  *            the blob stores the columns sorted by group (stable), so that
@@ -412,8 +416,8 @@ W4A16_API w4a16_status w4a16_gemm_ex(const w4a16_format* f, const void* packed, 
 
 /*
  * Number of bounded pipeline waits on the current device that gave up since
- * the previous call (each one means a tile of some w4a16_gemm output was not
- * written); the count is reset. Synchronous: waits for the device's pending
+ * the previous call (each one means a tile of some w4a16_gemm output, or the
+ * later outputs of a chained launch, were not written); the count is reset. Synchronous: waits for the device's pending
  * work to finish. Not expected to be nonzero in correct operation.
  */
 W4A16_API w4a16_status w4a16_pipeline_timeouts(uint32_t* count);
