@@ -600,3 +600,30 @@ def test_pack_codes_3bit_stream_every_position_and_roundtrip():
     assert w.shape == (5, 4)  # ceil(3 * 37 / 32)
     assert all(w[r].tolist() == brute.pack_stream3(c[r].tolist()) for r in range(5))
     assert np.array_equal(O.unpack_codes(w, 37, 3), c)
+
+
+# ---------------------------------------------------------------------------
+# The helpers the other pins use only indirectly
+# ---------------------------------------------------------------------------
+def test_acceptance_bound_hand_example():
+    """The stated per-element bound |y - y_ref| <= 2e-3 * B + 1e-3, worked by
+    hand: with B = 0.25 the allowance is 0.0015, so a miss of 0.0015 sits
+    exactly on it (ratio 1) and a miss of 0.003 is twice over."""
+    B = np.array([0.25, 0.25, 0.0, 10.0])
+    y_ref = np.array([1.0, 1.0, -2.0, 0.0])
+    y = np.array([1.0015, 0.997, -2.0005, 0.021])
+    assert np.allclose(O.tolerance(B), [0.0015, 0.0015, 0.001, 0.021])
+    assert np.allclose(O.error_ratio(y, y_ref, B), [1.0, 2.0, 0.5, 1.0])
+
+
+def test_awq_grid_is_the_closed_unit_interval():
+    for n in (1, 4, 20):
+        a = O.awq_grid(n)
+        assert a.size == n + 1 and a[0] == 0.0 and a[-1] == 1.0
+        assert np.allclose(np.diff(a), 1.0 / n)
+
+
+def test_group_members_partition_the_columns_in_order():
+    g_idx = np.array([2, 0, 1, 0, 2, 1, 1, 0, 2], dtype=np.int32)
+    members = O.group_members(g_idx, 3)
+    assert [m.tolist() for m in members] == [[1, 3, 7], [2, 5, 6], [0, 4, 8]]
