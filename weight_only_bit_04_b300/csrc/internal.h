@@ -36,8 +36,8 @@ constexpr int kGemvRegisterRing = 1; // weights loaded straight into a register 
 constexpr int kGemvAsyncCopy = 2;    // each thread lands its own weight loads in a shared-memory ring (cp.async)
 struct GemvPlan {
   int kind;     // kGemvRegisterRing or kGemvAsyncCopy
-  int rows16;   // register ring: 16-row tiles per CTA (2, 4, 8)
-  int stages;   // async copy: units in flight per thread (4; 2 for 8-bit codes)
+  int rows16;   // 16-row tiles per CTA (2, 4, 8), both kernels
+  int stages;   // not read by the kernels: the ring depth is fixed per code width (kWbSlots)
   int ksplit;   // CTAs per cluster along K
   bool stage_x; // register ring: copy the block's activations to shared memory first
 };
