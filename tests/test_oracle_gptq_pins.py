@@ -172,3 +172,85 @@ def test_mutants_are_caught():
             Wp[:, j + 1:] += upd if variant == "sign" else -upd
             qm[:, j] = qj
         assert not np.array_equal(qm, qb), variant
+
+
+# --- damping ("The two algorithms, compactly": before the Cholesky factor, H
+# gets damp * mean(diag H) added on its diagonal, damp = 0.01). The expected
+# matrices below are worked out by hand from that line, not by the oracle.
+
+H3 = np.array([[4.0, 1.0, 0.5],
+               [1.0, 2.0, 0.25],
+               [0.5, 0.25, 6.0]])
+# mean(diag) = (4 + 2 + 6) / 3 = 4, so 0.01 * 4 = 0.04 is added on the diagonal
+H3_DAMPED = np.array([[4.04, 1.0, 0.5],
+                      [1.0, 2.04, 0.25],
+                      [0.5, 0.25, 6.04]])
+# a channel whose activations are all zero (row and column 0 of H are zero):
+# its diagonal becomes 1 first, then mean(diag) = (1 + 3 + 5) / 3 = 3 -> + 0.03
+H_DEAD = np.array([[0.0, 0.0, 0.0],
+                   [0.0, 3.0, 1.0],
+                   [0.0, 1.0, 5.0]])
+H_DEAD_DAMPED = np.array([[1.03, 0.0, 0.0],
+                          [0.0, 3.03, 1.0],
+                          [0.0, 1.0, 5.03]])
+
+
+def test_damping_constant_is_the_pages():
+    assert O.GPTQ_DAMP == 0.01
+
+
+def test_damping_hand_example():
+    np.testing.assert_allclose(O.gptq_damped(H3), H3_DAMPED, rtol=0, atol=1e-15)
+    np.testing.assert_allclose(O.gptq_damped(H3, 0.5), H3 + 2.0 * np.eye(3), rtol=0, atol=1e-15)
+    before = H3.copy()
+    np.testing.assert_array_equal(O.gptq_damped(H3, 0.0), H3)
+    np.testing.assert_array_equal(H3, before)  # the input is left untouched
+
+
+def test_damping_dead_channel_hand_example():
+    np.testing.assert_allclose(O.gptq_damped(H_DEAD), H_DEAD_DAMPED, rtol=0, atol=1e-15)
+
+
+def _mutant_max_diag(H, damp=O.GPTQ_DAMP):
+    H = np.array(H, dtype=np.float64)
+    dead = np.diag(H) == 0
+    H[dead, dead] = 1.0
+    return H + damp * np.max(np.diag(H)) * np.eye(H.shape[0])
+
+
+def _mutant_per_element(H, damp=O.GPTQ_DAMP):
+    H = np.array(H, dtype=np.float64)
+    dead = np.diag(H) == 0
+    H[dead, dead] = 1.0
+    return H + damp * np.diag(np.diag(H))
+
+
+@pytest.mark.parametrize("mutant", [_mutant_max_diag, _mutant_per_element])
+def test_damping_pins_catch_mutants(mutant):
+    assert not np.allclose(mutant(H3), H3_DAMPED, rtol=0, atol=1e-12)
+
+
+def test_damping_dead_channel_pin_catches_late_fix():
+    # damping computed from the raw diagonal (mean 8/3), the dead entry set to 1 afterwards
+    late = H_DEAD + (0.01 * 8.0 / 3.0) * np.eye(3)
+    late[0, 0] = 1.0
+    assert not np.allclose(late, H_DEAD_DAMPED, rtol=0, atol=1e-12)
+    assert not np.allclose(_mutant_max_diag(H_DEAD), H_DEAD_DAMPED, rtol=0, atol=1e-12)
+
+
+def test_dead_channel_codes_are_round_to_nearest():
+    """A channel that never fires gets no error feedback (its row and column of
+    H are zero apart from the damped diagonal): in the first group, whose
+    scale is set before any update, its codes are the round-to-nearest codes."""
+    N, K, g = 16, 64, 32
+    W = synth.weights_np(N, K, synth.seed_for("gptq-dead", "w"))
+    x = synth.activations_np(96, K, 0.05, synth.seed_for("gptq-dead", "x"))
+    dead = 5
+    x[:, dead] = 0
+    q, s, z, g_idx = O.gptq_quantize(W, x, g, False)
+    q_rtn, s_rtn, z_rtn = O.rtn_quantize(W, g, False)
+    np.testing.assert_array_equal(s[:, 0], s_rtn[:, 0])
+    np.testing.assert_array_equal(z[:, 0], z_rtn[:, 0])
+    np.testing.assert_array_equal(q[:, dead], q_rtn[:, dead])
+    # the live columns after it do receive feedback: not all of them stay at RTN
+    assert not np.array_equal(q[:, dead + 1:g], q_rtn[:, dead + 1:g])
