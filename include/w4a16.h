@@ -114,9 +114,11 @@ typedef struct {
  *            of 128 rows x 64 columns of b-bit codes (3, 4 or 8 KiB),
  *            arranged so that a warp's 16-byte (3 bits: 16- and 8-byte)
  *            loads yield tensor-core operand fragments.
- *   scales   NR*G*256 bytes: fp16 scales, 128 rows per (row block, group).
+ *   scales   NR*G*256 bytes: fp16 scales; for every 32-row group its 32
+ *            rows' scales of all G groups are contiguous (64 bytes per group).
  *   zeros    (asymmetric only) NR*G*64 bytes of 4-bit zero points for 3- and
- *            4-bit codes, NR*G*128 bytes of 8-bit ones for 8-bit codes.
+ *            4-bit codes, NR*G*128 bytes of 8-bit ones for 8-bit codes,
+ *            arranged like the scales (16 or 32 bytes per 32 rows and group).
  *   perm     K*4 bytes (act order only): packed column -> original column.
  *   act_scale K*2 bytes (has_act_scale only): fp16 s in packed column order.
  * Rows beyond N and columns beyond K are padding. The blob's meaning is fixed
@@ -180,13 +182,15 @@ W4A16_API w4a16_status w4a16_quantize_rtn(const w4a16_format* f, const uint16_t*
  *   W4A16_ERR_BUFFER_TOO_SMALL (without act order there is no limit beyond
  *   the format's).
  *   No cudaMalloc/cudaFree or other allocation, on the device or the host.
- *   The first call on a device looks up the array's device address
- *   (cudaGetSymbolAddress) with that device current; make that first call
- *   before any stream capture.
+ *   The first call with act order on a device looks up the array's device
+ *   address (cudaGetSymbolAddress) with that device current; make that first
+ *   call before any stream capture. A lookup that fails returns
+ *   W4A16_ERR_CUDA and is tried again on the next call.
  *   Every call shares the one array and leaves its column list there. Calls
  *   that may run at the same time on the GPU (different streams, or different
- *   host threads with their own streams) race on it; calls on one stream do
- *   not. Host-side staging is serialised by a lock.
+ *   host threads with their own streams) race on it. Calls on one stream do
+ *   not, from any number of host threads: a lock is held from the host-side
+ *   staging until the call's copy and its kernel are both queued.
  */
 W4A16_API w4a16_status w4a16_quantize_rtn_noalloc(const w4a16_format* f, const uint16_t* w,
                                 const int32_t* g_idx, uint8_t* q, uint16_t* scales,
@@ -310,14 +314,20 @@ W4A16_API w4a16_status w4a16_gemv_grouped(const w4a16_format* formats, const voi
  * Chained decode products: one persistent launch computes y_i = x_i . W_hat_i^T
  * for a list of layers (1 <= M <= 16 tokens each), e.g. every linear of a
  * decoder stack for one token step. Each layer is the decode product of
- * w4a16_gemv, with the same error bound; what the chain adds is the launch:
- * the per-launch ramp-up and drain of one GEMV per layer ("What W4A16 buys
- * ...": decode is bandwidth-bound, so idle time between layers is lost
- * bandwidth) become one stream of weight loads. A work item is 32 rows of a
- * layer (the full K, split over the warps of a thread block as in
- * w4a16_gemv); a block claims items in list order, issues an item's first
- * weight loads, and waits on device-side completion counters only before
- * reading the item's activations. Results are deterministic.
+ * w4a16_gemv, with the same error bound; what the chain adds is the launch
+ * ("What W4A16 buys ...": decode is bandwidth-bound, so time between layers
+ * -- launch ramp-up, drain, dependency waits -- is lost bandwidth):
+ *   - one thread block per SM; every layer is cut into row groups of 32 rows
+ *     and each block owns a contiguous share of them (full K), the shares
+ *     rotated from layer to layer so that every SM streams the same bytes;
+ *   - a TMA producer per block streams the block's packed weights, scales and
+ *     zero points layer after layer into a shared-memory ring, without ever
+ *     waiting for a dependency (weights do not depend on earlier layers);
+ *   - the block's compute warps read a layer's activations only once every
+ *     layer it depends on has been completed by every block (device-side
+ *     completion counters); a finishing warp adds the warps' partial sums in
+ *     a fixed order and writes y.
+ * Results are deterministic for a given device.
  *
  *   w4a16_chain_layer: packed / packed_bytes (one blob per layer), x
  *            (fp16 [M][K], 16-byte aligned) and y (fp16 [M][N], 16-byte
@@ -331,19 +341,23 @@ W4A16_API w4a16_status w4a16_gemv_grouped(const w4a16_format* formats, const voi
  *            and symmetric; none has act order or an act scale, and K is a
  *            multiple of 64 (else W4A16_ERR_UNSUPPORTED).
  *   workspace: >= w4a16_chain_workspace_bytes(formats, n_layers, M) bytes
- *            (counters and the layer table), 256-byte aligned, device memory
- *            the chain owns from prepare until the last run; the size is 0
- *            for an invalid or unsupported list.
+ *            (counters, the table of layer slices and the TMA tensor maps of
+ *            every blob), 256-byte aligned, device memory the chain owns from
+ *            prepare until the last run; the size is 0 for an invalid or
+ *            unsupported list. It does not depend on the device.
  *
- * w4a16_chain_prepare validates everything on the host, writes the layer
- * table into the workspace with a synchronous host-to-device copy, and fills
- * *info (host memory, caller-owned). w4a16_chain_run then resets the
- * counters and launches the chain on `stream` (both asynchronous; may be
- * captured in a CUDA graph). Every dependency wait is bounded (1 s); a wait
- * that gives up stops the launch, leaves later outputs unwritten and is
- * counted (w4a16_pipeline_timeouts). The launch needs every thread block
- * resident at once (cooperative launch); it fails with W4A16_ERR_CUDA rather
- * than wait if the device cannot host them.
+ * w4a16_chain_prepare validates everything on the host, then -- for the
+ * current device -- cuts layers too large for one pass into slices, encodes
+ * the tensor maps and writes the table into the workspace with synchronous
+ * host-to-device copies, and fills *info (host memory, caller-owned). The
+ * blobs must not move afterwards (the tensor maps hold their addresses).
+ * w4a16_chain_run then resets the counters and launches the chain on `stream`
+ * (both asynchronous; may be captured in a CUDA graph), on a device with the
+ * SM count it was prepared for (else W4A16_ERR_INVALID_ARG). Every wait
+ * inside the launch is bounded (1 s); a wait that gives up stops every block,
+ * leaves the outputs undefined and is counted (w4a16_pipeline_timeouts). The
+ * launch needs one resident thread block per SM (cooperative launch); it
+ * fails with W4A16_ERR_CUDA rather than wait if the device cannot host them.
  */
 typedef struct {
   const void* packed;
@@ -360,7 +374,9 @@ typedef struct {
   int32_t group_size;
   int32_t symmetric;
   int64_t M;
-  int64_t total_items;  /* work items (32-row groups) over all layers */
+  int64_t n_slices;  /* entries of the slice table (>= n_layers) */
+  int32_t blocks;    /* thread blocks (SMs of the device) the table was planned for */
+  int32_t flags;     /* set by prepare for run: bit 0 = activations staged in shared memory */
 } w4a16_chain_info;
 
 W4A16_API size_t w4a16_chain_workspace_bytes(const w4a16_format* formats, int32_t n_layers, int64_t M);

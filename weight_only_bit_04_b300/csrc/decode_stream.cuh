@@ -1,0 +1,671 @@
+// The decode stream: one persistent launch computes y_i = x_i . W_hat_i^T for
+// a list of layers (a decoder's linears for one token step), 1 <= M <= 16.
+//
+// At batch one every packed weight is read once for about two flops ("AWQ +
+// GPTQ Quantization, in depth", section "What W4A16 buys and why decoding gets
+// faster"), so a token step is a stream of weight bytes, and the time lost to
+// launch ramp-up, drain and dependency waits between layers is lost
+// bandwidth. The launch is organised so that the weight stream never waits:
+//
+//  * One thread block per SM. Every layer is cut into row groups of 32 rows;
+//    block b owns a contiguous run of them (the full K of each row group),
+//    with the block positions rotated from layer to layer by the number of
+//    row groups dealt so far, so that every SM streams the same bytes over
+//    the step within about 1 %.
+//  * A producer warp streams the block's units -- codes, scales and zero
+//    points of one row group over 64 or 128 columns -- layer after layer into
+//    a ring of shared-memory slots of about 16 KiB of codes each. The codes
+//    of a slot come by TMA (3-D tensor maps over the blob, no multicast) in
+//    one copy, or a few at a row group's end: measured on B300, a stream of
+//    8 KiB copies tops out near 4 TB/s and one of 16 KiB copies near
+//    6.8 TB/s, so copies must be large. The slot's scales and zero points
+//    (64 and 16 bytes per group and row group) come by cp.async from the
+//    producer warp's lanes, which keeps small copies off the TMA unit.
+//    Weights never depend on earlier layers, so the producer runs ahead
+//    across dependency waits for as long as the ring has room.
+//  * Eight consumer warps share every slot, one unit each (two for narrow
+//    units). Per unit a warp expands the codes into m16n8k16 fragments in
+//    registers and multiplies them on the tensor cores with the activations
+//    (tokens in the n dimension), as the single-layer product does
+//    (gemv_impl.cuh, compute_unit). Each warp keeps one partial sum per row
+//    group and writes it to shared memory.
+//  * A finishing warp adds a row group's partial sums in warp order
+//    (deterministic), rounds to fp16, writes y, fences, and counts the layer
+//    as done on a device counter (one per layer slice, 128-byte lines).
+//  * A dependency warp walks the layers ahead of the consumers: for a layer
+//    that reads earlier layers' outputs it polls their counters with relaxed
+//    loads until every block has finished them, then fences once (acquire).
+//    It then stages the layer's activations in shared memory together with
+//    each group's activation sum (when they fit; otherwise the consumers read
+//    them through L1 after an L1 prefetch and get the group sums from the
+//    tensor cores), and publishes the layer as ready.
+//
+// Every wait is bounded (1 s by the global timer) and also gives up when
+// another block has raised the abort flag; a wait that times out is counted
+// (w4a16_pipeline_timeouts) and raises the flag, and every role then returns,
+// the producer after its copies in flight have landed. Outputs are undefined
+// after an abort.
+#pragma once
+
+#include "gemv_impl.cuh"
+#include "stream_geom.h"
+
+namespace w4a16 {
+namespace {
+
+template <int BITS, int GS>
+struct SGeo {
+  static constexpr int UB = stream_ub(GS);
+  static constexpr int GU = stream_gu(GS);
+  static constexpr int CB = stream_cb(BITS);
+  static constexpr int ZB = stream_zb(BITS);
+  static constexpr int kUnitCode = stream_unit_code(BITS, GS);
+  static constexpr int UPW = stream_upw(BITS, GS);
+  static constexpr int CU = stream_cu(BITS, GS);
+  static constexpr int kScaleOff = stream_scale_off(BITS, GS);
+  static constexpr int kZeroOff = stream_zero_off(BITS, GS);
+  static constexpr int kSlot = stream_slot_bytes(BITS, GS);
+  static constexpr int S = stream_slots(BITS, GS);
+  static constexpr int kScaleChunks = GU * 4;       // 16-byte pieces of a unit's scales
+  static constexpr int kZeroChunks = GU * ZB / 16;  // and of its zero points
+  static_assert(Unit<GS>::kBlocks == UB && Unit<GS>::kGroups == GU, "stream units are the GEMV units");
+  static_assert((CU & (CU - 1)) == 0, "codes copies are power-of-two boxes of units");
+};
+
+// log2 of a power of two up to 16
+__host__ __device__ constexpr int ilog2(int v) { return v >= 16 ? 4 : v >= 8 ? 3 : v >= 4 ? 2 : v >= 2 ? 1 : 0; }
+
+// This block's share of one layer slice.
+struct Span {
+  int rg0;  // first row group (of the layer) owned by this block
+  int n;    // row groups owned
+  int NU;   // units per row group
+  int T;    // units owned (n * NU)
+};
+
+__device__ __forceinline__ Span span_of(const StreamJob& J, int P, int b, int UB) {
+  int p = b - J.rot;
+  if (p < 0) p += P;
+  const int lo = int(int64_t(p) * J.n_rg / P), hi = int(int64_t(p + 1) * J.n_rg / P);
+  Span s;
+  s.rg0 = J.rg_first + lo;
+  s.n = hi - lo;
+  s.NU = J.KB / UB;
+  s.T = s.n * s.NU;
+  return s;
+}
+
+__device__ __forceinline__ StreamJob load_job(const StreamJob* jobs, int j) {
+  StreamJob J;
+  const uint4* src = reinterpret_cast<const uint4*>(jobs + j);
+  uint4* dst = reinterpret_cast<uint4*>(&J);
+#pragma unroll
+  for (int i = 0; i < int(sizeof(StreamJob) / 16); ++i) dst[i] = __ldg(src + i);
+  return J;
+}
+
+// Bounded waits. A wait returns kWaitOk when its condition holds, kWaitTimeout
+// when its time limit ran out (it then raises the abort flag), kWaitAbort when
+// another thread raised the flag first. Warps agree on the outcome with
+// warp_outcome, which counts a timeout once per warp.
+constexpr int kWaitOk = 0, kWaitTimeout = 1, kWaitAbort = 2;
+// A wait looks at another block's abort flag (a global load, one L2 round
+// trip during which it would not see its own condition complete) only once it
+// has lasted this long; ordinary waits never leave the SM.
+constexpr uint64_t kAbortPollNs = 20000;
+struct Guard {
+  unsigned int* abort_flag;
+  uint64_t t0;
+  uint32_t spins;
+  __device__ __forceinline__ void start() {
+    t0 = 0;
+    spins = 0;
+  }
+  // kWaitOk: keep waiting
+  __device__ __forceinline__ int check() {
+    if ((++spins & 63u) != 0) return kWaitOk;
+    const uint64_t now = global_timer_ns();
+    if (t0 == 0) {
+      t0 = now;
+      return kWaitOk;
+    }
+    const uint64_t waited = now - t0;
+    if (waited > kAbortPollNs && ld_relaxed_gpu_u32(abort_flag) != 0) return kWaitAbort;
+    if (waited > kTWaitLimitNs) {
+      atomicExch(abort_flag, 1u);
+      return kWaitTimeout;
+    }
+    return kWaitOk;
+  }
+};
+
+__device__ __forceinline__ int wait_mbar(uint32_t bar, uint32_t parity, Guard& gd) {
+  gd.start();
+  while (!mbar_try_wait(bar, parity)) {
+    const int st = gd.check();
+    if (st != kWaitOk) return st;
+  }
+  return kWaitOk;
+}
+// Wait until the device counter reaches v (relaxed; the caller fences).
+__device__ __forceinline__ int wait_counter_ge(const unsigned int* p, unsigned int v, Guard& gd) {
+  gd.start();
+  while (ld_relaxed_gpu_u32(p) < v) {
+    const int st = gd.check();
+    if (st != kWaitOk) return st;
+  }
+  return kWaitOk;
+}
+// Whole-warp outcome of a wait every lane took part in: true = go on.
+__device__ __forceinline__ bool warp_outcome(int st) {
+  const bool timed = __any_sync(0xffffffffu, st == kWaitTimeout);
+  const bool bad = __any_sync(0xffffffffu, st != kWaitOk);
+  if (timed && (threadIdx.x & 31) == 0) atomicAdd(&g_gemv_timeouts, 1u);
+  return !bad;
+}
+// Whole-warp wait for layer j's phase of a per-layer barrier pair (barrier
+// j & 1, parity (j >> 1) & 1); layers below 0 are complete.
+__device__ __forceinline__ bool wait_layer(uint32_t pair0, int j, Guard& gd) {
+  if (j < 0) return true;
+  return warp_outcome(wait_mbar(pair0 + 8 * (j & 1), uint32_t(j >> 1) & 1u, gd));
+}
+
+// cp.async of 16 bytes, and the arrival on an mbarrier once this thread's
+// cp.async copies so far have landed (.noinc: the arrival is one of the
+// barrier's expected arrivals).
+__device__ __forceinline__ void cp_async_16_cg(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+template <int MP, int GS, bool SYM, int BITS, bool XS>
+__global__ void __launch_bounds__(kStreamThreads, 1) decode_stream_kernel(const StreamLaunch c) {
+  using SG = SGeo<BITS, GS>;
+  constexpr int NB = MP > 8 ? 2 : 1;
+  constexpr int NW = kStreamConsumers;
+  constexpr int S = SG::S;
+  constexpr int CU = SG::CU;
+  constexpr int CS = kStreamCounterStride;
+  constexpr int RGMAX = stream_max_rg(MP);
+  extern __shared__ __align__(1024) unsigned char smem[];
+  const uint32_t ring = smem_addr(smem);
+  // mbarriers: full[S], empty[S] (the ring), then per layer parity (j & 1):
+  // cdone (the consumer warps have written layer j's partial sums), rdy (layer
+  // j's activations may be read), fdone (the finishing warp is done with layer
+  // j). Phase (j >> 1) & 1 of
+  // barrier j & 1 is layer j's; no role runs far enough ahead of another for
+  // that to be ambiguous (see the waits below).
+  const uint32_t full0 = ring + stream_bar_off(BITS, GS);
+  const uint32_t empty0 = full0 + S * 8;
+  const uint32_t cdone0 = empty0 + S * 8;
+  const uint32_t rdy0 = cdone0 + 16;
+  const uint32_t fdone0 = rdy0 + 16;
+  float* part = reinterpret_cast<float*>(smem + stream_part_off(BITS, GS));  // [2][RGMAX][NW][32 rows][MP]
+  uint16_t* xs = reinterpret_cast<uint16_t*>(smem + stream_x_off(BITS, GS, MP));  // [M][stride] (XS)
+
+  const int tid = int(threadIdx.x);
+  const int warp = tid >> 5, lane = tid & 31;
+  const int P = int(gridDim.x), b = int(blockIdx.x);
+  const int M = c.M, nj = c.n_jobs;
+  unsigned int* done = c.done;
+  Guard gd;
+  gd.abort_flag = done + size_t(nj) * CS;
+
+  if (tid == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(full0 + 8 * s, 33);  // lane 0's expect_tx arrival + one cp.async arrival per producer lane
+      mbar_init(empty0 + 8 * s, NW);
+    }
+    for (int q = 0; q < 2; ++q) {
+      mbar_init(cdone0 + 8 * q, NW);
+      mbar_init(rdy0 + 8 * q, 1);
+      mbar_init(fdone0 + 8 * q, 1);
+    }
+    fence_mbarrier_init();
+  }
+  __syncthreads();
+
+  // Every role walks the layer table in order; the next entry is loaded one
+  // layer ahead so that its latency hides behind the current layer.
+  StreamJob Jn = load_job(c.jobs, 0);
+
+  if (warp == NW) {
+    // ---------------- producer warp: lane 0 issues the TMA copies of the codes,
+    // every lane copies its share of the scales and zero points
+    int slot = 0;
+    uint32_t phase = 0;
+    int issued = 0;  // slots filled (for the drain after an abort)
+    bool alive = true;
+    for (int j = 0; j < nj && alive; ++j) {
+      const StreamJob J = Jn;
+      if (j + 1 < nj) Jn = load_job(c.jobs, j + 1);
+      const Span s = span_of(J, P, b, SG::UB);
+      if (s.T == 0) continue;
+      const CUtensorMap* m = c.maps + J.map;
+      const int R = (s.T + CU - 1) / CU;
+      const uint32_t* sc_base = J.scales2;
+      const uint8_t* z_base = J.zeros;
+      const int G = J.G, KB = J.KB, NU = s.NU;
+      int rgl0 = 0, ku0 = 0;  // (row group, unit) of the slot's first unit, advanced without dividing
+      for (int k = 0; k < R; ++k) {
+        if (!warp_outcome(wait_mbar(empty0 + 8 * slot, phase ^ 1u, gd))) {
+          alive = false;
+          break;
+        }
+        const uint32_t full = full0 + 8 * slot;
+        const uint32_t sb = ring + uint32_t(slot) * SG::kSlot;
+        const int nu_slot = min(CU, s.T - k * CU);
+        // the codes first (most of the bytes), then the scales and zero points
+        if (lane == 0) {
+          mbar_arrive_expect_tx(full, uint32_t(nu_slot) * SG::kUnitCode);
+          int rg = s.rg0 + rgl0, ku = ku0, d = 0;
+          while (d < nu_slot) {
+            int nu = min(nu_slot - d, NU - ku);  // units of this row group in the slot
+            const int rb = rg >> 2, pr = rg & 3;
+            const int c1 = BITS == 3 ? pr : 2 * pr;
+            int c2 = rb * KB + ku * SG::UB;
+            int box = CU;
+            while (nu > 0) {  // power-of-two boxes, largest first (one box in the common case)
+              while (box > nu) box >>= 1;
+              tma_load_3d(sb + d * SG::kUnitCode, m + (ilog2(CU) - ilog2(box)), 0, c1, c2, full);
+              c2 += box * SG::UB;
+              d += box;
+              ku += box;
+              nu -= box;
+            }
+            if (ku == NU) {
+              ku = 0;
+              ++rg;
+            }
+          }
+        }
+        // scales (SG::kScaleChunks 16-byte pieces per unit) and zero points
+        // (SG::kZeroChunks per unit): unit d of the slot is (rgl0, ku0 + d),
+        // wrapping into the following row groups
+        for (int q = lane; q < nu_slot * SG::kScaleChunks; q += 32) {
+          const int d = q / SG::kScaleChunks, p = q - d * SG::kScaleChunks;
+          int ku = ku0 + d, rg = s.rg0 + rgl0;
+          while (ku >= NU) {
+            ku -= NU;
+            ++rg;
+          }
+          // row group rg's scales: 64 contiguous bytes per group, groups back to back
+          const int gg = p >> 2;
+          const uint32_t* src = sc_base + (size_t(rg) * G + ku * SG::GU + gg) * 16 + (p & 3) * 4;
+          cp_async_16_cg(sb + SG::kScaleOff + (d * SG::GU + gg) * 64 + (p & 3) * 16, src);
+        }
+        if (!SYM) {
+          for (int q = lane; q < nu_slot * SG::kZeroChunks; q += 32) {
+            const int d = q / SG::kZeroChunks, p = q - d * SG::kZeroChunks;
+            int ku = ku0 + d, rg = s.rg0 + rgl0;
+            while (ku >= NU) {
+              ku -= NU;
+              ++rg;
+            }
+            const int gg = p / (SG::ZB / 16), h = p - gg * (SG::ZB / 16);
+            const uint8_t* src = z_base + (size_t(rg) * G + ku * SG::GU + gg) * SG::ZB + h * 16;
+            cp_async_16_cg(sb + SG::kZeroOff + (d * SG::GU + gg) * SG::ZB + h * 16, src);
+          }
+        }
+        cp_async_arrive_noinc(full);
+        ++issued;
+        if (++slot == S) {
+          slot = 0;
+          phase ^= 1u;
+        }
+        ku0 += CU;
+        while (ku0 >= NU) {
+          ku0 -= NU;
+          ++rgl0;
+        }
+      }
+    }
+    cp_async_wait_all();
+    if (!alive && lane == 0) {
+      // Let the TMA copies in flight land before the block can exit: the last
+      // min(issued, S) fills, each in its own slot.
+      const int nf = min(issued, S);
+      for (int k = 1; k <= nf; ++k) {
+        const int q = issued - k;
+        const uint32_t bar = full0 + 8 * (q % S);
+        const uint32_t par = uint32_t(q / S) & 1u;
+        const uint64_t t0 = global_timer_ns();
+        while (!mbar_try_wait(bar, par) && global_timer_ns() - t0 < kTWaitLimitNs) {
+        }
+      }
+    }
+    return;
+  }
+
+  if (warp == NW + 1) {
+    // ---------------- dependency warp
+    int known = -1;     // every layer <= known has been seen complete, and acquired
+    bool stale = true;  // the staged activations may be out of date
+    const uint16_t* loaded = nullptr;
+    int loaded_k = 0;
+    for (int j = 0; j < nj; ++j) {
+      const StreamJob J = Jn;
+      if (j + 1 < nj) Jn = load_job(c.jobs, j + 1);
+      // one layer ahead: every consumer warp has finished layer j - 2 (they
+      // cannot finish layer j before this warp publishes it)
+      if (!wait_layer(cdone0, j - 2, gd)) return;
+      if (J.wait_lo <= J.wait_hi && J.wait_hi > known) {
+        // every lane polls with acquire loads (one transaction per poll), so
+        // each lane's later loads see what those layers wrote
+        int st = kWaitOk;
+        for (int d = known + 1; d <= J.wait_hi && st == kWaitOk; ++d) {
+          gd.start();
+          while (ld_acquire_gpu_u32(done + size_t(d) * CS) < unsigned(P)) {
+            st = gd.check();
+            if (st != kWaitOk) break;
+          }
+        }
+        if (!warp_outcome(st)) return;
+        known = J.wait_hi;
+        stale = true;
+      }
+      const Span s = span_of(J, P, b, SG::UB);
+      if (s.n > 0) {
+        if (XS) {
+          if (stale || J.x != loaded || J.K != loaded_k) {
+            // the buffer still holds the previous layer's activations
+            if (!wait_layer(cdone0, j - 1, gd)) return;
+            // Stage x: every lane lands 16-byte chunks with cp.async, all in
+            // flight at once; then each lane adds whole groups of one token
+            // row from shared memory (fixed order per group; the chunk order
+            // is rotated by the group so that lanes hit different banks).
+            const int64_t stride = stream_x_stride(J.K, M);
+            float* xsum = reinterpret_cast<float*>(xs + stream_xsum_off(J.K, M) / 2);
+            const int cpr = J.K / 8, total = M * cpr;
+            {
+              int tok = 0, kc = lane;
+              while (kc >= cpr) {
+                kc -= cpr;
+                ++tok;
+              }
+              for (int q = lane; q < total; q += 32) {
+                cp_async_16_cg(smem_addr(xs + tok * stride + kc * 8), J.x + size_t(tok) * J.K + kc * 8);
+                kc += 32;
+                while (kc >= cpr) {
+                  kc -= cpr;
+                  ++tok;
+                }
+              }
+            }
+            cp_async_wait_all();
+            __syncwarp();
+            constexpr int CPG = GS / 8;  // chunks per group
+            const int ng = J.G;
+            for (int p = lane; p < M * ng; p += 32) {
+              const int tok = p / ng, gi = p - tok * ng;
+              const uint16_t* gx = xs + tok * stride + gi * GS;
+              float acc = 0.f;
+#pragma unroll
+              for (int c = 0; c < CPG; ++c) {
+                const int cc = (c + gi) & (CPG - 1);
+                const uint4 v = *reinterpret_cast<const uint4*>(gx + cc * 8);
+                const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                  const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&wv[e]));
+                  acc += f.x;
+                  acc += f.y;
+                }
+              }
+              xsum[gi * MP + tok] = acc;
+            }
+            __syncwarp();
+            loaded = J.x;
+            loaded_k = J.K;
+            stale = false;
+          }
+        } else {
+          const char* xb = reinterpret_cast<const char*>(J.x);
+          const int bytes = M * J.K * 2;
+          for (int off = lane * 128; off < bytes; off += 32 * 128) prefetch_l1(xb + off);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(rdy0 + 8 * (j & 1));
+    }
+    return;
+  }
+
+  if (warp == NW + 2) {
+    // ---------------- finishing warp: partial sums -> y, then the layer's counter
+    for (int j = 0; j < nj; ++j) {
+      const StreamJob J = Jn;
+      if (j + 1 < nj) Jn = load_job(c.jobs, j + 1);
+      // the consumers cannot finish layer j + 2 before this warp is done with layer j
+      if (!wait_layer(cdone0, j, gd)) return;
+      const Span s = span_of(J, P, b, SG::UB);
+      if (s.n > 0) {
+        const float* pb = part + size_t(j & 1) * RGMAX * NW * 32 * MP;
+        for (int rgl = 0; rgl < s.n; ++rgl) {
+          // warps holding a piece of this row group: all of them unless it has fewer units than a slot
+          uint32_t mask = (1u << NW) - 1u;
+          if (s.NU < CU) {
+            mask = 0;
+            for (int u = rgl * s.NU; u < rgl * s.NU + s.NU; ++u) mask |= 1u << ((u % CU) / SG::UPW);
+          }
+          const int n = (s.rg0 + rgl) * 32 + lane;
+          for (int tok = 0; tok < M; ++tok) {
+            float acc = 0.f;
+            for (int w = 0; w < NW; ++w)  // warp order
+              if (mask & (1u << w)) acc += pb[(size_t(rgl * NW + w) * 32 + lane) * MP + tok];
+            if (n < J.N) J.y[size_t(tok) * J.N + n] = __half_as_ushort(__float2half_rn(acc));
+          }
+        }
+        fence_acq_rel_gpu();  // this lane's stores are visible device-wide
+      }
+      __syncwarp();
+      if (lane == 0) {
+        red_relaxed_gpu_add_u32(done + size_t(j) * CS, 1u);
+        mbar_arrive(fdone0 + 8 * (j & 1));
+      }
+    }
+    return;
+  }
+
+  // ---------------- consumer warps
+  const int g = lane >> 2, t = lane & 3;
+  const int tok0 = min(g, M - 1), tok1 = min(g + 8, M - 1);
+  int slot = 0;
+  uint32_t phase = 0;
+  for (int j = 0; j < nj; ++j) {
+    const StreamJob J = Jn;
+    if (j + 1 < nj) Jn = load_job(c.jobs, j + 1);
+    const Span s = span_of(J, P, b, SG::UB);
+    // Layer j's activations are readable, and the finishing warp is done
+    // with layer j - 2 (partial buffer j & 1 is free). Every warp waits for
+    // both in every layer, with or without units in it, so that no warp runs
+    // two layers ahead of the dependency and finishing warps: each
+    // per-layer barrier then has at most one phase of its parity in flight.
+    if (!wait_layer(rdy0, j, gd)) return;
+    if (!wait_layer(fdone0, j - 2, gd)) return;
+    if (s.T > 0) {
+      const int R = (s.T + CU - 1) / CU;
+      const uint16_t* xl0;
+      const uint16_t* xl1;
+      const float* xsum = reinterpret_cast<const float*>(xs + stream_xsum_off(J.K, M) / 2);
+      if (XS) {
+        const int64_t stride = stream_x_stride(J.K, M);
+        xl0 = xs + tok0 * stride + 4 * t;
+        xl1 = xs + tok1 * stride + 4 * t;
+      } else {
+        xl0 = J.x + size_t(tok0) * J.K + 4 * t;
+        xl1 = J.x + size_t(tok1) * J.K + 4 * t;
+      }
+      float* pb = part + size_t(j & 1) * RGMAX * NW * 32 * MP;
+      float tot[kTilesPerWarp][NB][4];
+      int cur = -1;
+      auto flush = [&](int rgl) {
+        float* pe = pb + size_t(rgl * NW + warp) * 32 * MP;
+#pragma unroll
+        for (int tt = 0; tt < kTilesPerWarp; ++tt)
+#pragma unroll
+          for (int nb = 0; nb < NB; ++nb) {
+            const int tk = nb * 8 + 2 * t;
+            const int r0 = tt * 16 + g, r1 = r0 + 8;
+            if (tk < M) {
+              pe[r0 * MP + tk] = tot[tt][nb][0];
+              pe[r1 * MP + tk] = tot[tt][nb][2];
+            }
+            if (tk + 1 < M) {
+              pe[r0 * MP + tk + 1] = tot[tt][nb][1];
+              pe[r1 * MP + tk + 1] = tot[tt][nb][3];
+            }
+          }
+      };
+      // (row group, unit) of this warp's first unit in slot k, advanced by CU
+      // units per slot without dividing
+      int rgl0 = 0, ku0 = warp * SG::UPW;
+      while (ku0 >= s.NU) {
+        ku0 -= s.NU;
+        ++rgl0;
+      }
+      for (int k = 0; k < R; ++k) {
+        if (!warp_outcome(wait_mbar(full0 + 8 * slot, phase, gd))) return;
+        const unsigned char* sb = smem + size_t(slot) * SG::kSlot;
+        int rgl = rgl0, ku = ku0;
+#pragma unroll
+        for (int i = 0; i < SG::UPW; ++i) {
+          const int d = warp * SG::UPW + i;
+          if (k * CU + d < s.T) {
+            if (rgl != cur) {
+              if (cur >= 0) flush(cur);
+#pragma unroll
+              for (int tt = 0; tt < kTilesPerWarp; ++tt)
+#pragma unroll
+                for (int nb = 0; nb < NB; ++nb)
+#pragma unroll
+                  for (int e = 0; e < 4; ++e) tot[tt][nb][e] = 0.f;
+              cur = rgl;
+            }
+            UnitRegs<GS, BITS> rr;
+#pragma unroll
+            for (int bb = 0; bb < SG::UB; ++bb) {
+              const unsigned char* cb = sb + d * SG::kUnitCode + bb * SG::CB;
+              if (BITS == 3) {
+                rr.w[bb][0][0] = *reinterpret_cast<const uint4*>(cb + lane * 16);
+                const uint2 v = *reinterpret_cast<const uint2*>(cb + 512 + lane * 8);
+                rr.w[bb][1][0] = make_uint4(v.x, v.y, 0u, 0u);
+              } else {
+#pragma unroll
+                for (int tt = 0; tt < kTilesPerWarp; ++tt)
+#pragma unroll
+                  for (int pp = 0; pp < kParts<BITS>; ++pp)
+                    rr.w[bb][tt][pp] =
+                        *reinterpret_cast<const uint4*>(cb + tt * (SG::CB / 2) + pp * 512 + lane * 16);
+              }
+            }
+#pragma unroll
+            for (int gg = 0; gg < SG::GU; ++gg)
+#pragma unroll
+              for (int tt = 0; tt < kTilesPerWarp; ++tt) {
+                const int gi = d * SG::GU + gg;
+                rr.s[gg][tt] = *reinterpret_cast<const uint32_t*>(sb + SG::kScaleOff + gi * 64 + tt * 32 + g * 4);
+                if (SYM)
+                  rr.z[gg][tt] = 0u;
+                else if (BITS == 8)
+                  rr.z[gg][tt] =
+                      *reinterpret_cast<const uint16_t*>(sb + SG::kZeroOff + gi * 32 + (tt * 8 + g) * 2);
+                else
+                  rr.z[gg][tt] = sb[SG::kZeroOff + gi * 16 + tt * 8 + g];
+              }
+            const int xo = ku * SG::UB * kColsPerBlock;
+            if (XS) {
+              // the unit's group sums, staged with the activations
+              float xsg[SG::GU][NB][2];
+#pragma unroll
+              for (int gg = 0; gg < SG::GU; ++gg)
+#pragma unroll
+                for (int nb = 0; nb < NB; ++nb) {
+                  const int tk = min(nb * 8 + 2 * t, MP - 1);
+                  xsg[gg][nb][0] = xsum[(ku * SG::GU + gg) * MP + tk];
+                  xsg[gg][nb][1] = xsum[(ku * SG::GU + gg) * MP + min(tk + 1, MP - 1)];
+                }
+              compute_unit<NB, GS, SYM, kXShared, BITS, BITS == 4, true, MP == 1>(rr, xl0 + xo, xl1 + xo, tot, xsg);
+            } else {
+              compute_unit<NB, GS, SYM, kXCoherent, BITS, BITS == 4>(rr, xl0 + xo, xl1 + xo, tot);
+            }
+          }
+          if (++ku == s.NU) {  // the warp's next unit in this slot
+            ku = 0;
+            ++rgl;
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty0 + 8 * slot);
+        if (++slot == S) {
+          slot = 0;
+          phase ^= 1u;
+        }
+        ku0 += CU;  // the same position in the next slot
+        while (ku0 >= s.NU) {
+          ku0 -= s.NU;
+          ++rgl0;
+        }
+      }
+      if (cur >= 0) flush(cur);
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(cdone0 + 8 * (j & 1));
+  }
+}
+
+template <int MP, int GS, bool SYM, int BITS, bool XS>
+cudaError_t launch_stream_typed(const StreamLaunch& c, int sm_count, cudaStream_t stream) {
+  auto kern = decode_stream_kernel<MP, GS, SYM, BITS, XS>;
+  const int smem = kStreamSmem;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  int per_sm = 0;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kStreamThreads, smem);
+  if (e != cudaSuccess) return e;
+  if (per_sm < 1) return cudaErrorInvalidConfiguration;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(unsigned(sm_count), 1, 1);
+  cfg.blockDim = dim3(kStreamThreads, 1, 1);
+  cfg.dynamicSmemBytes = size_t(smem);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;  // every block resident at once
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, kern, c);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+template <int GS, bool SYM, int BITS, bool XS>
+cudaError_t launch_stream_mp(const StreamLaunch& c, int sm_count, cudaStream_t stream) {
+  switch (stream_mp(c.M)) {
+    case 1: return launch_stream_typed<1, GS, SYM, BITS, XS>(c, sm_count, stream);
+    case 2: return launch_stream_typed<2, GS, SYM, BITS, XS>(c, sm_count, stream);
+    case 4: return launch_stream_typed<4, GS, SYM, BITS, XS>(c, sm_count, stream);
+    case 8: return launch_stream_typed<8, GS, SYM, BITS, XS>(c, sm_count, stream);
+    default: return launch_stream_typed<16, GS, SYM, BITS, XS>(c, sm_count, stream);
+  }
+}
+
+template <int GS, bool SYM, int BITS>
+cudaError_t launch_stream_x(const StreamLaunch& c, int sm_count, cudaStream_t stream) {
+  return c.x_staged ? launch_stream_mp<GS, SYM, BITS, true>(c, sm_count, stream)
+                    : launch_stream_mp<GS, SYM, BITS, false>(c, sm_count, stream);
+}
+
+template <int BITS>
+cudaError_t launch_stream_bits(const StreamLaunch& c, int gsize, bool sym, int sm_count, cudaStream_t stream) {
+  if (gsize == 32)
+    return sym ? launch_stream_x<32, true, BITS>(c, sm_count, stream) : launch_stream_x<32, false, BITS>(c, sm_count, stream);
+  if (gsize == 64)
+    return sym ? launch_stream_x<64, true, BITS>(c, sm_count, stream) : launch_stream_x<64, false, BITS>(c, sm_count, stream);
+  return sym ? launch_stream_x<128, true, BITS>(c, sm_count, stream) : launch_stream_x<128, false, BITS>(c, sm_count, stream);
+}
+
+}  // namespace
+}  // namespace w4a16

@@ -281,8 +281,8 @@ __device__ __forceinline__ void load_unit(UnitRegs<GS, BITS>& r, const uint32_t*
     const int gi = GS == 32 ? min(unit * U::kGroups + gg, gmax) : unit * U::kGroups + gg;
 #pragma unroll
     for (int tt = 0; tt < kTilesPerWarp; ++tt) {
-      r.s[gg][tt] = ldg_nc_u32(sp + gi * 64 + tt * 8);
-      r.z[gg][tt] = SYM ? 0u : BITS != 8 ? ldg_nc_u8(zp + gi * 64 + tt * 8) : ldg_nc_u16(zp + gi * 128 + tt * 16);
+      r.s[gg][tt] = ldg_nc_u32(sp + gi * 16 + tt * 8);
+      r.z[gg][tt] = SYM ? 0u : BITS != 8 ? ldg_nc_u8(zp + gi * 16 + tt * 8) : ldg_nc_u16(zp + gi * 32 + tt * 16);
     }
   }
 }
@@ -295,9 +295,14 @@ __device__ __forceinline__ void load_unit(UnitRegs<GS, BITS>& r, const uint32_t*
 // (4096x11008: 8.63 -> 7.84 us). It is slower in the asynchronous-copy ring
 // (28672x8192: 30.3 -> 32.3 us) and in the 8-bit register ring (4096x4096:
 // 5.48 -> 7.88 us), and 3-bit codes lose 2.5 % of the decode step with it.
-template <int NB, int GS, bool SYM, int XM, int BITS, bool SPLIT>
+// XSUM: the group activation sums come from the caller (xsg[gg][nb][e] =
+// sum of the group's activations for token nb * 8 + 2t + e, plain units)
+// instead of the all-2^-24 MMA. ONE: a single token; only the accumulator
+// elements of token 0 (0 and 2) are finalized.
+template <int NB, int GS, bool SYM, int XM, int BITS, bool SPLIT, bool XSUM = false, bool ONE = false>
 __device__ __forceinline__ void compute_unit(const UnitRegs<GS, BITS>& r, const uint16_t* xl0, const uint16_t* xl1,
-                                             float tot[kTilesPerWarp][NB][4]) {
+                                             float tot[kTilesPerWarp][NB][4],
+                                             const float (*xsg)[NB][2] = nullptr) {
   using U = Unit<GS>;
   const uint32_t ones[4] = {0x00010001u, 0x00010001u, 0x00010001u, 0x00010001u};  // 2^-24 each
   const float zero4[4] = {0.f, 0.f, 0.f, 0.f};
@@ -319,9 +324,11 @@ __device__ __forceinline__ void compute_unit(const UnitRegs<GS, BITS>& r, const 
       // first step of the group (of this parity, with SPLIT): start the set fresh
       const bool fresh = SPLIT ? ((GS == 32) ? true : (j < 2 && bb == 0))
                                : ((GS == 32) ? (j == 0 || j == 2) : (j == 0 && bb == 0));
+      if (!XSUM) {
 #pragma unroll
-      for (int nb = 0; nb < NB; ++nb)
-        mma_16816(cx[ph][nb], ones, bx[j][nb].x, bx[j][nb].y, fresh ? zero4 : cx[ph][nb]);
+        for (int nb = 0; nb < NB; ++nb)
+          mma_16816(cx[ph][nb], ones, bx[j][nb].x, bx[j][nb].y, fresh ? zero4 : cx[ph][nb]);
+      }
 #pragma unroll
       for (int tt = 0; tt < kTilesPerWarp; ++tt) {
         uint32_t af[4];
@@ -335,9 +342,15 @@ __device__ __forceinline__ void compute_unit(const UnitRegs<GS, BITS>& r, const 
         const int gg = (GS == 32) ? (j >> 1) : 0;
         float c2[NB][4];
 #pragma unroll
-        for (int nb = 0; nb < NB; ++nb)
+        for (int nb = 0; nb < NB; ++nb) {
+          if (XSUM) {
+            c2[nb][0] = c2[nb][2] = xsg[gg][nb][0] * 5.9604644775390625e-8f;  // 2^-24
+            c2[nb][1] = c2[nb][3] = xsg[gg][nb][1] * 5.9604644775390625e-8f;
+          } else {
 #pragma unroll
-          for (int i = 0; i < 4; ++i) c2[nb][i] = SPLIT ? cx[0][nb][i] + cx[NS - 1][nb][i] : cx[0][nb][i];
+            for (int i = 0; i < 4; ++i) c2[nb][i] = SPLIT ? cx[0][nb][i] + cx[NS - 1][nb][i] : cx[0][nb][i];
+          }
+        }
 #pragma unroll
         for (int tt = 0; tt < kTilesPerWarp; ++tt) {
           float a2[NB][4];
@@ -346,7 +359,13 @@ __device__ __forceinline__ void compute_unit(const UnitRegs<GS, BITS>& r, const 
 #pragma unroll
             for (int i = 0; i < 4; ++i)
               a2[nb][i] = SPLIT ? acc[0][tt][nb][i] + acc[NS - 1][tt][nb][i] : acc[0][tt][nb][i];
-          finalize<NB>(a2, c2, make_factors<SYM, BITS>(r.s[gg][tt], r.z[gg][tt]), tot[tt]);
+          const GroupFactors f = make_factors<SYM, BITS>(r.s[gg][tt], r.z[gg][tt]);
+          if (ONE) {
+            tot[tt][0][0] = fmaf(f.sa, a2[0][0], fmaf(f.za, c2[0][0], tot[tt][0][0]));
+            tot[tt][0][2] = fmaf(f.sb, a2[0][2], fmaf(f.zb, c2[0][2], tot[tt][0][2]));
+          } else {
+            finalize<NB>(a2, c2, f, tot[tt]);
+          }
         }
       }
     }
@@ -480,9 +499,9 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const GemvArgs a) {
   using CW = CodeWords<BITS>;
   const uint32_t* qp = qweight + (size_t(R) * a.KB * 8 + r16) * CW::kRow16 + lane * 4 +
                        size_t(u0) * U::kBlocks * CW::kBlock;
-  const uint32_t* sp = scales2 + (size_t(R) * G * 8 + r16) * 8 + g + size_t(u0) * U::kGroups * 64;
-  const uint8_t* zp = SYM ? nullptr
-                          : zeros + ((size_t(R) * G * 8 + r16) * 8 + g + size_t(u0) * U::kGroups * 64) * kZeroMul<BITS>;
+  // the warp's row group (r16 is even) from the unit's first group on; entries per group: [tt][g]
+  const uint32_t* sp = scales2 + meta_index(R, int64_t(u0) * U::kGroups, r16, g, G);
+  const uint8_t* zp = SYM ? nullptr : zeros + meta_index(R, int64_t(u0) * U::kGroups, r16, g, G) * kZeroMul<BITS>;
 
   const bool early = (a.flags & kGemvWeightsReady) != 0;
   const int M = a.M;
@@ -514,11 +533,11 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const GemvArgs a) {
 #pragma unroll
         for (int tt = 0; tt < kTilesPerWarp; ++tt) {
           const int f = gg * kTilesPerWarp + tt;
-          cp_async_4(slot + SL::kScaleOff + (f * kThreads + tid) * 4, sp + gi * 64 + tt * 8);
+          cp_async_4(slot + SL::kScaleOff + (f * kThreads + tid) * 4, sp + gi * 16 + tt * 8);
           if (!SYM)  // the aligned word holding this lane's zero point(s)
             cp_async_4(slot + SL::kZeroOff + (f * kThreads + tid) * 4,
                        reinterpret_cast<const uint32_t*>(
-                           reinterpret_cast<uintptr_t>(zp + (gi * 64 + tt * 8) * kZeroMul<BITS>) & ~uintptr_t(3)));
+                           reinterpret_cast<uintptr_t>(zp + (gi * 16 + tt * 8) * kZeroMul<BITS>) & ~uintptr_t(3)));
         }
       }
     }
@@ -853,246 +872,6 @@ cudaError_t launch_gemv_group_bits(const Layout& Lc, const GemvGroup& grp, const
   if (M <= 4) return launch_gs<4, BITS>(a, gs, Lc.sym, staged, wb, plan.ksplit, smem, stream);
   if (M <= 8) return launch_gs<8, BITS>(a, gs, Lc.sym, staged, wb, plan.ksplit, smem, stream);
   return launch_gs<16, BITS>(a, gs, Lc.sym, staged, wb, plan.ksplit, smem, stream);
-}
-
-// ---------------------------------------------------------------------------
-// Chained products: one persistent launch over the work items of a list of
-// layers (item = 32 rows of one layer, the full K split over the 8 warps,
-// weights through the asynchronous-copy ring). Blocks claim items in list
-// order from a device counter; before reading its activations an item waits
-// until every item of the layers it depends on has finished (device
-// counters, bounded wait), with its first ring slots already in flight.
-// Every block is resident (cooperative launch), items are claimed in order
-// and dependencies point to earlier layers only, so the lowest unfinished
-// item can always make progress.
-// ---------------------------------------------------------------------------
-__device__ __forceinline__ unsigned int ld_acquire_u32(const unsigned int* p) {
-  unsigned int v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-__device__ __forceinline__ void red_release_add_u32(unsigned int* p, unsigned int v) {
-  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-// Counters of a chain, each in its own 128-byte line (polled by many blocks).
-constexpr int kChainCounterStride = 32;
-
-template <int MP, int GS, bool SYM, int BITS>
-__global__ void __launch_bounds__(kThreads) gemv_chain_kernel(const ChainLaunch c) {
-  // dynamic shared memory: the asynchronous-copy ring; after an item's last
-  // unit it holds the cross-warp reduction ([warp][32 rows][16 tokens] fp32)
-  extern __shared__ __align__(128) unsigned char smem[];
-  __shared__ int s_item, s_abort;
-  constexpr int NB = MP > 8 ? 2 : 1;
-  using U = Unit<GS>;
-  using CW = CodeWords<BITS>;
-  using SL = WbSlot<GS, BITS>;
-  constexpr int D = kWbSlots<BITS>;
-  constexpr int CS = kChainCounterStride;
-  static_assert(kWarps * 512 * 4 <= D * SL::kBytes, "the reduction fits in the ring");
-  const int tid = int(threadIdx.x);
-  const int warp = tid >> 5;
-  const int lane = tid & 31;
-  const int g = lane >> 2, t = lane & 3;
-  const int M = c.M;
-  const ChainJob* __restrict__ jobs = c.jobs;
-  unsigned int* done = c.done;
-  unsigned int* abort_flag = done + size_t(c.n_jobs) * CS;
-  unsigned int* next_item = done + size_t(c.n_jobs + 1) * CS;
-  float* red_w = reinterpret_cast<float*>(smem);
-  int j = 0;
-  // Items are claimed in increasing order, so every item a block waits for
-  // was claimed earlier by a resident block. The next item is claimed once
-  // the current one no longer waits (its claim latency hides behind the
-  // current item's work).
-  if (tid == 0) s_item = int(atomicAdd(next_item, 1u));
-  __syncthreads();
-  int item = s_item;
-  while (item < c.total_items) {
-    while (j + 1 < c.n_jobs && item >= jobs[j + 1].item0) ++j;
-    const ChainJob& J = jobs[j];
-    const int rg = item - J.item0;
-    const int R = rg >> 2, r16 = (rg & 3) * 2;
-    const int units = (J.KB + U::kBlocks - 1) / U::kBlocks;
-    const int u0 = (units * warp) / kWarps;
-    const int nunit = (units * (warp + 1)) / kWarps - u0;
-    const int G = J.G;
-    const int gmax = G - 1 - u0 * U::kGroups;
-    const uint32_t* qp = J.qweight + (size_t(R) * J.KB * 8 + r16) * CW::kRow16 + lane * 4 +
-                         size_t(u0) * U::kBlocks * CW::kBlock;
-    const uint32_t* sp = J.scales2 + (size_t(R) * G * 8 + r16) * 8 + g + size_t(u0) * U::kGroups * 64;
-    const uint8_t* zp =
-        SYM ? nullptr : J.zeros + ((size_t(R) * G * 8 + r16) * 8 + g + size_t(u0) * U::kGroups * 64) * kZeroMul<BITS>;
-
-    auto issue_unit = [&](int i) {  // unit u0 + i into slot i % D: this thread's own entries
-      if (i < nunit) {
-        unsigned char* slot = smem + size_t(i % D) * SL::kBytes;
-#pragma unroll
-        for (int bb = 0; bb < U::kBlocks; ++bb)
-#pragma unroll
-          for (int tt = 0; tt < kTilesPerWarp; ++tt)
-#pragma unroll
-            for (int part = 0; part < kParts<BITS>; ++part) {
-              unsigned char* dst = slot + (((bb * kTilesPerWarp + tt) * kParts<BITS> + part) * kThreads + tid) * 16;
-              const uint32_t* src = qp + (i * U::kBlocks + bb) * CW::kBlock + CW::off(tt, part, lane);
-              if (CW::narrow(tt))
-                cp_async_8(dst, src);
-              else
-                cp_async_16(dst, src);
-            }
-#pragma unroll
-        for (int gg = 0; gg < U::kGroups; ++gg) {
-          const int gi = GS == 32 ? min(i * U::kGroups + gg, gmax) : i * U::kGroups + gg;
-#pragma unroll
-          for (int tt = 0; tt < kTilesPerWarp; ++tt) {
-            const int f = gg * kTilesPerWarp + tt;
-            cp_async_4(slot + SL::kScaleOff + (f * kThreads + tid) * 4, sp + gi * 64 + tt * 8);
-            if (!SYM)
-              cp_async_4(slot + SL::kZeroOff + (f * kThreads + tid) * 4,
-                         reinterpret_cast<const uint32_t*>(
-                             reinterpret_cast<uintptr_t>(zp + (gi * 64 + tt * 8) * kZeroMul<BITS>) & ~uintptr_t(3)));
-          }
-        }
-      }
-      cp_async_commit();
-    };
-#pragma unroll
-    for (int i = 0; i < D; ++i) issue_unit(i);  // weights first: they do not depend on earlier layers
-
-    if (J.wait_lo <= J.wait_hi) {
-      if (tid == 0) {
-        int ok = 1;
-        const uint64_t t0 = global_timer_ns();
-        for (int d = J.wait_lo; d <= J.wait_hi && ok; ++d) {
-          const unsigned int need = unsigned(jobs[d].items);
-          for (int spin = 0; ld_acquire_u32(done + size_t(d) * CS) < need; ++spin) {
-            if ((spin & 15) == 15 && ld_acquire_u32(abort_flag) != 0) {
-              ok = 0;
-              break;
-            }
-            if (global_timer_ns() - t0 > kTWaitLimitNs) {
-              atomicAdd(&g_gemv_timeouts, 1u);
-              atomicExch(abort_flag, 1u);
-              ok = 0;
-              break;
-            }
-            __nanosleep(128);
-          }
-        }
-        s_abort = ok ? 0 : 1;
-      }
-      __syncthreads();  // also orders the activation loads below after thread 0's acquire
-      if (s_abort) {  // a wait gave up somewhere: every block stops
-        cp_async_wait_all();
-        break;
-      }
-    }
-    unsigned int claimed = 0;
-    if (tid == 0) claimed = atomicAdd(next_item, 1u);
-
-    const int tok0 = min(g, M - 1), tok1 = min(g + 8, M - 1);
-    const int c0 = u0 * U::kBlocks * kColsPerBlock + 4 * t;
-    const uint16_t* xl0 = J.x + size_t(tok0) * J.K + c0;
-    const uint16_t* xl1 = J.x + size_t(tok1) * J.K + c0;
-    float tot[kTilesPerWarp][NB][4];
-#pragma unroll
-    for (int tt = 0; tt < kTilesPerWarp; ++tt)
-#pragma unroll
-      for (int nb = 0; nb < NB; ++nb)
-#pragma unroll
-        for (int i = 0; i < 4; ++i) tot[tt][nb][i] = 0.f;
-    const int zshift = int((reinterpret_cast<uintptr_t>(zp) & 3u) * 8);
-    for (int i = 0; i < nunit; ++i) {
-      cp_async_wait_group<D - 1>();  // unit i has landed (this thread's copies)
-      const unsigned char* slot = smem + size_t(i % D) * SL::kBytes;
-      UnitRegs<GS, BITS> r;
-#pragma unroll
-      for (int bb = 0; bb < U::kBlocks; ++bb)
-#pragma unroll
-        for (int tt = 0; tt < kTilesPerWarp; ++tt)
-#pragma unroll
-          for (int part = 0; part < kParts<BITS>; ++part)
-            r.w[bb][tt][part] = *reinterpret_cast<const uint4*>(
-                slot + (((bb * kTilesPerWarp + tt) * kParts<BITS> + part) * kThreads + tid) * 16);
-#pragma unroll
-      for (int gg = 0; gg < U::kGroups; ++gg)
-#pragma unroll
-        for (int tt = 0; tt < kTilesPerWarp; ++tt) {
-          const int f = gg * kTilesPerWarp + tt;
-          r.s[gg][tt] = *reinterpret_cast<const uint32_t*>(slot + SL::kScaleOff + (f * kThreads + tid) * 4);
-          r.z[gg][tt] = SYM ? 0u
-                            : (*reinterpret_cast<const uint32_t*>(slot + SL::kZeroOff + (f * kThreads + tid) * 4) >>
-                               zshift) & (BITS != 8 ? 0xFFu : 0xFFFFu);
-        }
-      const int xo = i * U::kBlocks * kColsPerBlock;
-      compute_unit<NB, GS, SYM, kXCoherent, BITS, false>(r, xl0 + xo, xl1 + xo, tot);
-      issue_unit(i + D);
-    }
-    cp_async_wait_all();
-    __syncthreads();  // every thread is done with the ring: it becomes the reduction buffer
-
-#pragma unroll
-    for (int tt = 0; tt < kTilesPerWarp; ++tt)
-#pragma unroll
-      for (int nb = 0; nb < NB; ++nb) {
-        const int tk = nb * 8 + 2 * t;
-        float* rw = red_w + warp * 512 + tt * 256;
-        rw[g * 16 + tk] = tot[tt][nb][0];
-        rw[g * 16 + tk + 1] = tot[tt][nb][1];
-        rw[(g + 8) * 16 + tk] = tot[tt][nb][2];
-        rw[(g + 8) * 16 + tk + 1] = tot[tt][nb][3];
-      }
-    __syncthreads();
-    for (int e = tid; e < 32 * M; e += kThreads) {
-      const int tok = e >> 5, rr = e & 31;
-      float acc = 0.f;
-#pragma unroll
-      for (int k = 0; k < kWarps; ++k) acc += red_w[k * 512 + rr * 16 + tok];
-      const int n = R * kRowsPerBlock + r16 * 16 + rr;
-      if (n < J.N) J.y[size_t(tok) * J.N + n] = __half_as_ushort(__float2half_rn(acc));
-    }
-    if (tid == 0) s_item = int(claimed);
-    __syncthreads();  // every output of the item is written (and the ring is free again)
-    if (tid == 0) red_release_add_u32(done + size_t(j) * CS, 1u);  // publishes them device-wide
-    item = s_item;
-  }
-}
-
-template <int BITS>
-cudaError_t launch_chain_bits(const ChainLaunch& c, cudaStream_t stream) {
-  void (*kern)(const ChainLaunch) = nullptr;
-  auto pick = [&](auto mp) {
-    constexpr int MP = decltype(mp)::value;
-    if (c.gsize == 32) kern = c.sym ? gemv_chain_kernel<MP, 32, true, BITS> : gemv_chain_kernel<MP, 32, false, BITS>;
-    else if (c.gsize == 64) kern = c.sym ? gemv_chain_kernel<MP, 64, true, BITS> : gemv_chain_kernel<MP, 64, false, BITS>;
-    else kern = c.sym ? gemv_chain_kernel<MP, 128, true, BITS> : gemv_chain_kernel<MP, 128, false, BITS>;
-  };
-  if (c.M <= 1) pick(std::integral_constant<int, 1>{});
-  else if (c.M <= 2) pick(std::integral_constant<int, 2>{});
-  else if (c.M <= 4) pick(std::integral_constant<int, 4>{});
-  else if (c.M <= 8) pick(std::integral_constant<int, 8>{});
-  else pick(std::integral_constant<int, 16>{});
-  const int smem = kWbSlots<BITS> * wb_slot_bytes(c.gsize, BITS);
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (e != cudaSuccess) return e;
-  int per_sm = 0;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem);
-  if (e != cudaSuccess) return e;
-  if (per_sm < 1) return cudaErrorInvalidConfiguration;
-  const int grid = std::min(c.total_items, per_sm * c.sm_count);
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(unsigned(grid), 1, 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = size_t(smem);
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeCooperative;  // every block resident at once
-  attr[0].val.cooperative = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, kern, c);
-  if (e != cudaSuccess) return e;
-  return cudaGetLastError();
 }
 
 // This translation unit's timeout counter (read and cleared).

@@ -2,6 +2,7 @@
 // Every launcher only enqueues work on `stream` and returns the launch status.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "layout.h"
@@ -82,31 +83,41 @@ size_t gptq_workspace_bytes(int64_t N, int64_t K);
 cudaError_t launch_gptq(const Layout& L, const uint16_t* w, const uint16_t* x, int64_t T, double damp, uint8_t* q,
                         uint16_t* scales, uint8_t* zeros, int32_t* g_idx, void* workspace, cudaStream_t stream);
 
-// Chained decode products (w4a16_chain_*): one persistent launch runs a list
-// of layers. Work item = one 32-row group of a layer (the full K); a layer's
-// items wait for the completion counters of the layers whose outputs they
-// read.
-struct ChainJob {
-  const uint32_t* qweight;
-  const uint32_t* scales2;
-  const uint8_t* zeros;  // nullptr when symmetric
-  const uint16_t* x;
-  uint16_t* y;
-  int N, K, G, KB;
-  int item0, items;      // first global work item and count (32-row groups)
-  int wait_lo, wait_hi;  // layers this layer waits for (none when wait_lo > wait_hi)
+// Chained decode products (w4a16_chain_*), run by the decode stream
+// (decode_stream.cuh): one persistent launch over a table of layer slices.
+// A slice is a run of row groups (32 rows) of one layer; thread block b owns
+// a contiguous share of every slice's row groups (positions rotated by `rot`)
+// and waits on the completion counters of the slices [wait_lo, wait_hi]
+// before it reads the slice's activations.
+struct StreamJob {
+  const uint16_t* x;        // fp16 [M][K]
+  uint16_t* y;              // fp16 [M][N]
+  const uint32_t* scales2;  // the blob's scale pairs
+  const uint8_t* zeros;     // the blob's zero points (nullptr when symmetric)
+  int N, K, KB, G;          // the layer's shape (KB 64-column blocks, G groups)
+  int rg_first, n_rg;       // this slice's row groups
+  int rot;                  // block position of the slice's first share
+  int wait_lo, wait_hi;     // slices to wait for (none when wait_lo > wait_hi)
+  int map;                  // index of the layer's first tensor map (the codes as boxes of
+                            // CU, CU/2, ..., 1 units, CU = units per ring slot)
+  int pad[2];
 };
-struct ChainLaunch {
-  int bits, gsize, M;
-  bool sym;
-  int n_jobs;
-  int total_items;
-  int sm_count;
-  const ChainJob* jobs;  // device table
-  unsigned int* done;    // per layer a count of finished items, then the abort flag and the next-item
-                         // counter, each in its own 128-byte line
+static_assert(sizeof(StreamJob) == 80, "the layer table is read as 16-byte vectors");
+struct StreamLaunch {
+  const StreamJob* jobs;    // device table
+  const CUtensorMap* maps;  // device array, 64-byte aligned
+  unsigned int* done;       // per slice a count of finished blocks (128-byte stride), then the abort flag
+  int n_jobs, M;
+  int x_staged;             // every layer's activations fit in shared memory
 };
-cudaError_t launch_chain(const ChainLaunch& c, cudaStream_t stream);
+cudaError_t launch_stream(const StreamLaunch& c, int bits, int gsize, bool sym, int sm_count, cudaStream_t stream);
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (k_gemm.cu):
+// a tensor of `rank` dimensions (dims[0] innermost), byte strides of the
+// outer dimensions, a box per copy; no interleave, no swizzle, 256-byte L2
+// promotion, out-of-range elements read as zero.
+cudaError_t encode_tiled_map(CUtensorMap* map, CUtensorMapDataType type, int rank, const void* base,
+                             const uint64_t* dims, const uint64_t* strides, const uint32_t* box);
 
 // Device-side counts of bounded pipeline waits that gave up, read and reset
 // (k_gemm.cu for the GEMM; the GEMV translation units for the GEMV's and the

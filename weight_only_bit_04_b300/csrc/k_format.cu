@@ -179,7 +179,8 @@ __global__ void __launch_bounds__(256) pack_qweight3_kernel(Layout L, const uint
 }
 
 // One thread per (row block, group, 16-row tile, lane group): a scale pair and
-// the zero points of the two rows (one byte of two nibbles, or two bytes).
+// the zero points of the two rows (one byte of two nibbles, or two bytes),
+// stored at meta_index (row-group-major).
 __global__ void __launch_bounds__(256) pack_meta_kernel(Layout L, const uint16_t* __restrict__ scales,
                                                         const uint8_t* __restrict__ zeros,
                                                         uint32_t* __restrict__ s_out,
@@ -193,17 +194,18 @@ __global__ void __launch_bounds__(256) pack_meta_kernel(Layout L, const uint16_t
   const int64_t gi = rg - R * L.G;
   const int64_t n0 = R * kRowsPerBlock + r16 * 16 + g;
   const int64_t n1 = n0 + 8;
+  const int64_t mi = meta_index(R, gi, r16, g, L.G);
   const uint32_t s0 = n0 < L.N ? scales[n0 * L.G + gi] : 0u;
   const uint32_t s1 = n1 < L.N ? scales[n1 * L.G + gi] : 0u;
-  s_out[i] = s0 | (s1 << 16);
+  s_out[mi] = s0 | (s1 << 16);
   if (z_out) {
     if (L.bits != 8) {
       const uint32_t z0 = n0 < L.N ? (zeros[n0 * L.G + gi] & 0xF) : 0u;
       const uint32_t z1 = n1 < L.N ? (zeros[n1 * L.G + gi] & 0xF) : 0u;
-      z_out[i] = uint8_t(z0 | (z1 << 4));
+      z_out[mi] = uint8_t(z0 | (z1 << 4));
     } else {
-      z_out[2 * i] = n0 < L.N ? zeros[n0 * L.G + gi] : uint8_t(0);
-      z_out[2 * i + 1] = n1 < L.N ? zeros[n1 * L.G + gi] : uint8_t(0);
+      z_out[2 * mi] = n0 < L.N ? zeros[n0 * L.G + gi] : uint8_t(0);
+      z_out[2 * mi + 1] = n1 < L.N ? zeros[n1 * L.G + gi] : uint8_t(0);
     }
   }
 }
@@ -243,7 +245,7 @@ __global__ void __launch_bounds__(256) dequant_kernel(Layout L, BlobView B, uint
     const int64_t p = p0 + kk;
     if (p >= L.K) continue;
     const int64_t gi = p / L.gsize;
-    const int64_t mi = ((R * L.G + gi) * 8 + r16) * 8 + g;
+    const int64_t mi = meta_index(R, gi, r16, g, L.G);
     const int64_t c = B.perm ? B.perm[p] : p;
 #pragma unroll
     for (int hh = 0; hh < 2; ++hh) {
@@ -295,7 +297,7 @@ __global__ void __launch_bounds__(256) dequant3_kernel(Layout L, BlobView B, uin
           for (int bt = 0; bt < 3; ++bt) code |= ((w[bt] >> (15 + 16 * h2)) & 1u) << bt;
         }
         const int64_t gi = p / L.gsize;
-        const int64_t mi = ((R * L.G + gi) * 8 + r16) * 8 + g;
+        const int64_t mi = meta_index(R, gi, r16, g, L.G);
         const uint32_t z = B.zeros ? ((B.zeros[mi] >> (4 * h)) & 0xF) : 4u;
         const __half s = __ushort_as_half(B.scales[2 * mi + h]);
         const __half d = __hsub(__ushort_as_half(uint16_t(0x6400u | code)),

@@ -304,8 +304,8 @@ __device__ __forceinline__ void dequant_step(const unsigned char* ws, int ng, bo
 }
 
 // Bulk copies of one step's packed weights of 128-row block R (codes, then
-// the scale pairs and zero points of its ng groups from group g0) to the
-// stage's weight tile at wdst, completing on barrier bar.
+// the scale pairs and zero points of its ng groups from group g0, four row
+// groups each) to the stage's weight tile at wdst, completing on barrier bar.
 template <bool SYM, int BITS>
 __device__ __forceinline__ void load_weight_step(uint32_t wdst, const GemmArgs& a, int R, int kbg, int g0, int ng,
                                                  uint32_t bar) {
@@ -313,10 +313,17 @@ __device__ __forceinline__ void load_weight_step(uint32_t wdst, const GemmArgs& 
   const unsigned char* qbytes = reinterpret_cast<const unsigned char*>(a.qweight);
   const unsigned char* sbytes = reinterpret_cast<const unsigned char*>(a.scales2);
   bulk_copy_g2s(wdst, qbytes + (size_t(R) * a.KB + kbg) * WT::kCodes, WT::kCodes, bar);
-  bulk_copy_g2s(wdst + WT::kScaleOff, sbytes + (size_t(R) * a.G + g0) * 256, uint32_t(ng * 256), bar);
-  if (!SYM)
-    bulk_copy_g2s(wdst + WT::kZeroOff, a.zeros + (size_t(R) * a.G + g0) * WT::kZeroGroup,
-                  uint32_t(ng * WT::kZeroGroup), bar);
+  // the blob keeps each 32-row group's metadata together: one copy per (row
+  // group, group), landed in the tile's [group][16-row tile][lane group] order
+  for (int gs = 0; gs < ng; ++gs)
+#pragma unroll
+    for (int pr = 0; pr < 4; ++pr) {
+      const size_t mi = size_t(meta_index(R, g0 + gs, 2 * pr, 0, a.G));
+      bulk_copy_g2s(wdst + WT::kScaleOff + gs * 256 + pr * 64, sbytes + mi * 4, 64u, bar);
+      if (!SYM)
+        bulk_copy_g2s(wdst + WT::kZeroOff + gs * WT::kZeroGroup + pr * (WT::kZeroGroup / 4),
+                      a.zeros + mi * (WT::kZeroGroup / 64), uint32_t(WT::kZeroGroup / 4), bar);
+    }
 }
 
 template <int WR, int NT, int SA, int SB, int DS, int GS, bool SYM, int BITS>
@@ -735,6 +742,25 @@ int tile_tokens(int tile) { return tile == 2 ? 128 : tile == 5 ? 128 : tile == 6
 int tile_rows(int tile) { return tile == 2 ? 256 : 128; }
 
 }  // namespace
+
+cudaError_t encode_tiled_map(CUtensorMap* map, CUtensorMapDataType type, int rank, const void* base,
+                             const uint64_t* dims, const uint64_t* strides, const uint32_t* box) {
+  EncodeTiledFn enc = nullptr;
+  cudaError_t e = encode_fn(&enc);
+  if (e != cudaSuccess) return e;
+  cuuint64_t d[5], st[4];
+  cuuint32_t bx[5], es[5];
+  for (int i = 0; i < rank; ++i) {
+    d[i] = cuuint64_t(dims[i]);
+    bx[i] = cuuint32_t(box[i]);
+    es[i] = 1u;
+    if (i + 1 < rank) st[i] = cuuint64_t(strides[i]);
+  }
+  const CUresult r = enc(map, type, cuuint32_t(rank), const_cast<void*>(base), d, st, bx, es,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
 
 GemmPlan gemm_default_plan(const Layout& L, int64_t M, int sm_count) {
   // Few tokens: a narrow tile (two blocks per SM) and K split over a cluster

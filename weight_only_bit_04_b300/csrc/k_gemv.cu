@@ -1,5 +1,5 @@
 // Planning and dispatch of the decode-sized product. The kernels live in
-// gemv_impl.cuh; k_gemv_b3.cu, k_gemv_b4.cu and k_gemv_b8.cu compile them for
+// gemv_impl.cuh (one layer or a group) and decode_stream.cuh (a list of layers); k_gemv_b3.cu, k_gemv_b4.cu and k_gemv_b8.cu compile them for
 // 3-, 4- and 8-bit codes.
 #include "gemv_impl.cuh"
 
@@ -17,9 +17,9 @@ cudaError_t launch_gemv_group_b4(const Layout& Lc, const GemvGroup& grp, const u
                                  const GemvPlan& plan, uint32_t flags, cudaStream_t stream);
 cudaError_t launch_gemv_group_b8(const Layout& Lc, const GemvGroup& grp, const uint16_t* x, int M,
                                  const GemvPlan& plan, uint32_t flags, cudaStream_t stream);
-cudaError_t launch_chain_b3(const ChainLaunch& c, cudaStream_t stream);
-cudaError_t launch_chain_b4(const ChainLaunch& c, cudaStream_t stream);
-cudaError_t launch_chain_b8(const ChainLaunch& c, cudaStream_t stream);
+cudaError_t launch_stream_b3(const StreamLaunch& c, int gsize, bool sym, int sm_count, cudaStream_t stream);
+cudaError_t launch_stream_b4(const StreamLaunch& c, int gsize, bool sym, int sm_count, cudaStream_t stream);
+cudaError_t launch_stream_b8(const StreamLaunch& c, int gsize, bool sym, int sm_count, cudaStream_t stream);
 cudaError_t take_gemv_timeouts_b3(unsigned int* count);
 cudaError_t take_gemv_timeouts_b4(unsigned int* count);
 cudaError_t take_gemv_timeouts_b8(unsigned int* count);
@@ -80,10 +80,10 @@ cudaError_t launch_gemv_group(const Layout& Lc, const GemvGroup& grp, const uint
   return launch_gemv_group_b4(Lc, grp, x, M, plan, flags, stream);
 }
 
-cudaError_t launch_chain(const ChainLaunch& c, cudaStream_t stream) {
-  if (c.bits == 8) return launch_chain_b8(c, stream);
-  if (c.bits == 3) return launch_chain_b3(c, stream);
-  return launch_chain_b4(c, stream);
+cudaError_t launch_stream(const StreamLaunch& c, int bits, int gsize, bool sym, int sm_count, cudaStream_t stream) {
+  if (bits == 8) return launch_stream_b8(c, gsize, sym, sm_count, stream);
+  if (bits == 3) return launch_stream_b3(c, gsize, sym, sm_count, stream);
+  return launch_stream_b4(c, gsize, sym, sm_count, stream);
 }
 
 cudaError_t take_gemv_timeouts(unsigned int* count) {

@@ -1,5 +1,5 @@
 // The decode-sized product compiled for 4-bit codes.
-#include "gemv_impl.cuh"
+#include "decode_stream.cuh"
 
 namespace w4a16 {
 
@@ -13,7 +13,9 @@ cudaError_t launch_gemv_group_b4(const Layout& Lc, const GemvGroup& grp, const u
   return launch_gemv_group_bits<4>(Lc, grp, x, M, plan, flags, stream);
 }
 
-cudaError_t launch_chain_b4(const ChainLaunch& c, cudaStream_t stream) { return launch_chain_bits<4>(c, stream); }
+cudaError_t launch_stream_b4(const StreamLaunch& c, int gsize, bool sym, int sm_count, cudaStream_t stream) {
+  return launch_stream_bits<4>(c, gsize, sym, sm_count, stream);
+}
 
 cudaError_t take_gemv_timeouts_b4(unsigned int* count) { return take_local_gemv_timeouts(count); }
 

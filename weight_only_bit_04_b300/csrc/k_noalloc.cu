@@ -25,15 +25,17 @@ constexpr int64_t kNoAllocMaxGroups = kNoAllocMaxK / 32;
 
 static __device__ __align__(256) int32_t g_rtn_scratch[kNoAllocMaxK];
 
-// Device address of g_rtn_scratch, looked up once per device with that device
-// current (in host code the symbol's name is only a host-side stand-in).
+// Device address of g_rtn_scratch per device, looked up with that device
+// current (in host code the symbol's name is only a host-side stand-in). A
+// successful lookup is kept; a failed one is tried again on the next call.
 constexpr int kMaxDevices = 64;
-std::once_flag g_addr_once[kMaxDevices];
+std::mutex g_addr_mutex;
 int32_t* g_addr[kMaxDevices];
-cudaError_t g_addr_err[kMaxDevices];
 
 // Host staging for the column list and the group counts: static, shared by
-// all calls, serialised by this mutex.
+// all calls, serialised by this mutex, which is held until the call's copy
+// and its kernel have both been queued (so that on one stream every copy is
+// followed by its own kernel).
 std::mutex g_host_mutex;
 int32_t g_host_perm[kNoAllocMaxK];
 int32_t g_host_count[kNoAllocMaxGroups];
@@ -43,12 +45,13 @@ cudaError_t scratch_address(int32_t** out) {
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  std::call_once(g_addr_once[dev], [dev]() {
+  std::lock_guard<std::mutex> lock(g_addr_mutex);
+  if (g_addr[dev] == nullptr) {
     void* p = nullptr;
-    g_addr_err[dev] = cudaGetSymbolAddress(&p, g_rtn_scratch);
+    e = cudaGetSymbolAddress(&p, g_rtn_scratch);
+    if (e != cudaSuccess) return e;
     g_addr[dev] = static_cast<int32_t*>(p);
-  });
-  if (g_addr_err[dev] != cudaSuccess) return g_addr_err[dev];
+  }
   *out = g_addr[dev];
   return cudaSuccess;
 }
@@ -73,31 +76,32 @@ w4a16_status w4a16_quantize_rtn_noalloc(const w4a16_format* f, const uint16_t* w
     return W4A16_ERR_MISALIGNED;
   if (f->has_g_idx && f->K > kNoAllocMaxK) return W4A16_ERR_BUFFER_TOO_SMALL;  // beyond the fixed scratch
   const Layout L = make_layout(*f);
-  const int32_t* perm_dev = nullptr;
-  if (f->has_g_idx) {
-    int32_t* scratch = nullptr;
-    cudaError_t e = scratch_address(&scratch);
-    if (e != cudaSuccess) return cuda_error_status(e);
-    std::lock_guard<std::mutex> lock(g_host_mutex);
-    const int64_t K = f->K, G = f->K / f->group_size;
-    for (int64_t t = 0; t < G; ++t) g_host_count[t] = 0;
-    for (int64_t k = 0; k < K; ++k) {
-      const int32_t t = g_idx[k];
-      if (t < 0 || t >= G) return W4A16_ERR_INVALID_ARG;
-      ++g_host_count[t];
-    }
-    // Every group has exactly group_size members; stable group-sorted order.
-    for (int64_t t = 0; t < G; ++t) {
-      if (g_host_count[t] != f->group_size) return W4A16_ERR_INVALID_ARG;
-      g_host_count[t] = int32_t(t * f->group_size);  // next free slot of group t
-    }
-    for (int64_t k = 0; k < K; ++k) g_host_perm[g_host_count[g_idx[k]]++] = int32_t(k);
-    // Pageable source: the call returns once the host buffer has been read.
-    e = cudaMemcpyAsync(scratch, g_host_perm, size_t(K) * 4, cudaMemcpyHostToDevice, stream);
-    if (e != cudaSuccess) return cuda_error_status(e);
-    perm_dev = scratch;
+  if (!f->has_g_idx) {
+    const cudaError_t e = launch_quantize_rtn(L, w, nullptr, nullptr, q, scales, zeros, stream);
+    return e == cudaSuccess ? W4A16_OK : cuda_error_status(e);
   }
-  cudaError_t e = launch_quantize_rtn(L, w, perm_dev, nullptr, q, scales, zeros, stream);
+  int32_t* scratch = nullptr;
+  cudaError_t e = scratch_address(&scratch);
+  if (e != cudaSuccess) return cuda_error_status(e);
+  std::lock_guard<std::mutex> lock(g_host_mutex);
+  const int64_t K = f->K, G = f->K / f->group_size;
+  for (int64_t t = 0; t < G; ++t) g_host_count[t] = 0;
+  for (int64_t k = 0; k < K; ++k) {
+    const int32_t t = g_idx[k];
+    if (t < 0 || t >= G) return W4A16_ERR_INVALID_ARG;
+    ++g_host_count[t];
+  }
+  // Every group has exactly group_size members; stable group-sorted order.
+  for (int64_t t = 0; t < G; ++t) {
+    if (g_host_count[t] != f->group_size) return W4A16_ERR_INVALID_ARG;
+    g_host_count[t] = int32_t(t * f->group_size);  // next free slot of group t
+  }
+  for (int64_t k = 0; k < K; ++k) g_host_perm[g_host_count[g_idx[k]]++] = int32_t(k);
+  // Pageable source: the copy has read the host buffer when it returns.
+  e = cudaMemcpyAsync(scratch, g_host_perm, size_t(K) * 4, cudaMemcpyHostToDevice, stream);
+  if (e != cudaSuccess) return cuda_error_status(e);
+  // Queued while the lock is held: the next call's copy lands after this kernel on the same stream.
+  e = launch_quantize_rtn(L, w, scratch, nullptr, q, scales, zeros, stream);
   return e == cudaSuccess ? W4A16_OK : cuda_error_status(e);
 }
 

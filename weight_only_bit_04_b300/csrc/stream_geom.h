@@ -1,0 +1,92 @@
+// Geometry of the decode stream (the chained decode products): how a layer's
+// packed weights are cut into the units a thread block streams, the
+// shared-memory ring that holds them, and the rest of the block's shared
+// memory. Shared by the host (tensor-map boxes, shared-memory size, the split
+// of large layers, whether activations fit in shared memory) and the kernel.
+//
+// Terms
+//   row group   32 consecutive weight rows (two 16-row tiles of a 128-row
+//               block); a thread block always owns whole row groups of a layer,
+//               with the full K, so no output row is split between blocks.
+//   unit        the codes, scales and zero points of one row group over
+//               `stream_ub` 64-column blocks (one group of 128 columns, or one
+//               64-column block holding one or two groups of 64 / 32).
+//   slot        one ring entry: `stream_cu` consecutive units of the block's
+//               share (row group after row group), `stream_upw` for each
+//               consumer warp. Its codes arrive by TMA in one to a few copies
+//               (about 16 KiB together: the TMA stream needs large copies),
+//               its scales and zero points by the producer warp's cp.async.
+#pragma once
+
+namespace w4a16 {
+
+constexpr int kStreamConsumers = 8;  // consumer warps per thread block
+constexpr int kStreamWarps = kStreamConsumers + 3;  // + producer, dependency and finishing warps
+constexpr int kStreamThreads = kStreamWarps * 32;
+constexpr int kStreamCounterStride = 32;  // 32-bit words between completion counters (one 128-byte line each)
+constexpr int kStreamSmem = 227 * 1024;  // shared memory of one thread block (the opt-in maximum)
+constexpr int kStreamRingBudget = 136 * 1024;  // bytes of ring entries
+
+__host__ __device__ constexpr int stream_align128(int v) { return (v + 127) / 128 * 128; }
+// 64-column blocks per unit and groups per unit.
+__host__ __device__ constexpr int stream_ub(int gs) { return gs == 128 ? 2 : 1; }
+__host__ __device__ constexpr int stream_gu(int gs) { return gs == 32 ? 2 : 1; }
+// Code bytes of one row group per 64-column block: 768 / 1024 / 2048 for 3 / 4 / 8 bits.
+__host__ __device__ constexpr int stream_cb(int bits) { return bits * 256; }
+// Zero-point bytes of one row group per group: 3- and 4-bit nibble pairs
+// (one byte per row pair), 8-bit byte pairs.
+__host__ __device__ constexpr int stream_zb(int bits) { return bits == 8 ? 32 : 16; }
+__host__ __device__ constexpr int stream_unit_code(int bits, int gs) { return stream_ub(gs) * stream_cb(bits); }
+// Units per consumer warp and slot: about 16 KiB of codes per slot.
+__host__ __device__ constexpr int stream_upw(int bits, int gs) {
+  return stream_unit_code(bits, gs) * kStreamConsumers >= 12288 ? 1 : 2;
+}
+__host__ __device__ constexpr int stream_cu(int bits, int gs) { return kStreamConsumers * stream_upw(bits, gs); }
+// Slot layout: the codes of its units back to back, then their scales (64
+// bytes per group), then their zero points (stream_zb bytes per group).
+__host__ __device__ constexpr int stream_scale_off(int bits, int gs) {
+  return stream_align128(stream_cu(bits, gs) * stream_unit_code(bits, gs));
+}
+__host__ __device__ constexpr int stream_zero_off(int bits, int gs) {
+  return stream_scale_off(bits, gs) + stream_cu(bits, gs) * stream_gu(gs) * 64;
+}
+__host__ __device__ constexpr int stream_slot_bytes(int bits, int gs) {
+  return stream_align128(stream_zero_off(bits, gs) + stream_cu(bits, gs) * stream_gu(gs) * stream_zb(bits));
+}
+__host__ __device__ constexpr int stream_slots(int bits, int gs) {
+  return kStreamRingBudget / stream_slot_bytes(bits, gs) < 3 ? 3 : kStreamRingBudget / stream_slot_bytes(bits, gs);
+}
+// Padded token count of the kernel instance for M tokens.
+__host__ __device__ constexpr int stream_mp(int M) { return M <= 1 ? 1 : M <= 2 ? 2 : M <= 4 ? 4 : M <= 8 ? 8 : 16; }
+// Row groups one thread block may own in one layer slice; larger layers are
+// cut into slices. Each owned row group has one partial-sum entry per consumer
+// warp (32 rows x MP tokens of fp32), in two buffers (consecutive slices).
+__host__ __device__ constexpr int stream_max_rg(int mp) { return mp <= 2 ? 8 : mp == 4 ? 4 : mp == 8 ? 2 : 1; }
+__host__ __device__ constexpr int stream_part_bytes(int mp) { return 2 * stream_max_rg(mp) * kStreamConsumers * 32 * mp * 4; }
+
+// Shared memory of one thread block: ring | barriers (full and empty per
+// slot, three pairs per layer parity) | two partial-sum buffers | staged
+// activations and their group sums (the rest, up to kStreamSmem).
+__host__ __device__ constexpr int stream_bar_off(int bits, int gs) {
+  return stream_slots(bits, gs) * stream_slot_bytes(bits, gs);
+}
+__host__ __device__ constexpr int stream_part_off(int bits, int gs) {
+  return stream_bar_off(bits, gs) + stream_align128((2 * stream_slots(bits, gs) + 6) * 8);
+}
+__host__ __device__ constexpr int stream_x_off(int bits, int gs, int mp) {
+  return stream_part_off(bits, gs) + stream_part_bytes(mp);
+}
+__host__ __device__ constexpr int stream_x_bytes(int bits, int gs, int mp) { return kStreamSmem - stream_x_off(bits, gs, mp); }
+// Row stride (halves) of the staged activations: one row per token; rows
+// after the first are offset by 32 bytes so that the lanes of a warp reading
+// different tokens fall on different banks. The group sums of the
+// activations (fp32 [G][MP]) follow the rows.
+__host__ __device__ constexpr long long stream_x_stride(long long K, int M) { return M == 1 ? K : K + 16; }
+__host__ __device__ constexpr long long stream_xsum_off(long long K, int M) {  // bytes from the staged rows
+  return M * stream_x_stride(K, M) * 2;
+}
+__host__ __device__ constexpr bool stream_x_fits(long long K, int M, int bits, int gs) {
+  return stream_xsum_off(K, M) + (K / gs) * stream_mp(M) * 4 <= stream_x_bytes(bits, gs, stream_mp(M));
+}
+
+}  // namespace w4a16

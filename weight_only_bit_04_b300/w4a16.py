@@ -82,7 +82,9 @@ class ChainInfo(ctypes.Structure):
         ("group_size", ctypes.c_int32),
         ("symmetric", ctypes.c_int32),
         ("M", ctypes.c_int64),
-        ("total_items", ctypes.c_int64),
+        ("n_slices", ctypes.c_int64),
+        ("blocks", ctypes.c_int32),
+        ("flags", ctypes.c_int32),
     ]
 
 SIGNATURES = {
