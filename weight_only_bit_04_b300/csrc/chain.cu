@@ -17,7 +17,7 @@ using namespace w4a16;
 namespace {
 
 constexpr int32_t kChainMaxLayers = 1 << 16;
-constexpr int kMapsPerLayer = 5;  // the codes as boxes of CU, CU/2, ..., 1 units (CU <= 16)
+constexpr int kMapsPerLayer = 6;  // the codes as boxes of CU, CU/2, ..., 1 units (CU <= 32)
 
 bool aligned_to(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 

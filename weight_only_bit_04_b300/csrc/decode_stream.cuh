@@ -69,11 +69,13 @@ struct SGeo {
   static constexpr int kScaleChunks = GU * 4;       // 16-byte pieces of a unit's scales
   static constexpr int kZeroChunks = GU * ZB / 16;  // and of its zero points
   static_assert(Unit<GS>::kBlocks == UB && Unit<GS>::kGroups == GU, "stream units are the GEMV units");
-  static_assert((CU & (CU - 1)) == 0, "codes copies are power-of-two boxes of units");
+  static_assert((CU & (CU - 1)) == 0 && CU <= 32, "codes copies are power-of-two boxes of at most 32 units");
 };
 
-// log2 of a power of two up to 16
-__host__ __device__ constexpr int ilog2(int v) { return v >= 16 ? 4 : v >= 8 ? 3 : v >= 4 ? 2 : v >= 2 ? 1 : 0; }
+// log2 of a power of two up to 32
+__host__ __device__ constexpr int ilog2(int v) {
+  return v >= 32 ? 5 : v >= 16 ? 4 : v >= 8 ? 3 : v >= 4 ? 2 : v >= 2 ? 1 : 0;
+}
 
 // This block's share of one layer slice.
 struct Span {

@@ -99,7 +99,7 @@ struct StreamJob {
   int rot;                  // block position of the slice's first share
   int wait_lo, wait_hi;     // slices to wait for (none when wait_lo > wait_hi)
   int map;                  // index of the layer's first tensor map (the codes as boxes of
-                            // CU, CU/2, ..., 1 units, CU = units per ring slot)
+                            // CU, CU/2, ..., 1 units, CU = units per ring slot, at most 32)
   int pad[2];
 };
 static_assert(sizeof(StreamJob) == 80, "the layer table is read as 16-byte vectors");

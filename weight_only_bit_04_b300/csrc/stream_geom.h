@@ -14,7 +14,7 @@
 //   slot        one ring entry: `stream_cu` consecutive units of the block's
 //               share (row group after row group), `stream_upw` for each
 //               consumer warp. Its codes arrive by TMA in one to a few copies
-//               (about 16 KiB together: the TMA stream needs large copies),
+//               (24 to 32 KiB together: the TMA stream needs large copies),
 //               its scales and zero points by the producer warp's cp.async.
 #pragma once
 
@@ -37,9 +37,15 @@ __host__ __device__ constexpr int stream_cb(int bits) { return bits * 256; }
 // (one byte per row pair), 8-bit byte pairs.
 __host__ __device__ constexpr int stream_zb(int bits) { return bits == 8 ? 32 : 16; }
 __host__ __device__ constexpr int stream_unit_code(int bits, int gs) { return stream_ub(gs) * stream_cb(bits); }
-// Units per consumer warp and slot: about 16 KiB of codes per slot.
+// Units per consumer warp and slot: the largest power of two that keeps a
+// slot's codes within 32 KiB. Measured on B300 (8 x 28672x8192, no
+// dependencies): one 2 KiB unit per warp 3.66 TB/s, two 4.92 TB/s -- each
+// warp's two units overlap their latency chains, and the per-slot barrier
+// waits are paid half as often.
 __host__ __device__ constexpr int stream_upw(int bits, int gs) {
-  return stream_unit_code(bits, gs) * kStreamConsumers >= 12288 ? 1 : 2;
+  return stream_unit_code(bits, gs) * kStreamConsumers * 4 <= 32768   ? 4
+         : stream_unit_code(bits, gs) * kStreamConsumers * 2 <= 32768 ? 2
+                                                                      : 1;
 }
 __host__ __device__ constexpr int stream_cu(int bits, int gs) { return kStreamConsumers * stream_upw(bits, gs); }
 // Slot layout: the codes of its units back to back, then their scales (64
