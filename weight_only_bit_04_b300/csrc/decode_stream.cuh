@@ -528,75 +528,93 @@ __global__ void __launch_bounds__(kStreamThreads, 1) decode_stream_kernel(const 
         ku0 -= s.NU;
         ++rgl0;
       }
+      // registers of unit d of slot sb (codes, scale pairs, zero points, and
+      // with staged activations the group sums of the unit's columns ku)
+      struct UnitIn {
+        UnitRegs<GS, BITS> r;
+        float xsg[SG::GU][NB][2];
+      };
+      auto load_unit_in = [&](const unsigned char* sb, int d, int ku, UnitIn& in) {
+#pragma unroll
+        for (int bb = 0; bb < SG::UB; ++bb) {
+          const unsigned char* cb = sb + d * SG::kUnitCode + bb * SG::CB;
+          if (BITS == 3) {
+            in.r.w[bb][0][0] = *reinterpret_cast<const uint4*>(cb + lane * 16);
+            const uint2 v = *reinterpret_cast<const uint2*>(cb + 512 + lane * 8);
+            in.r.w[bb][1][0] = make_uint4(v.x, v.y, 0u, 0u);
+          } else {
+#pragma unroll
+            for (int tt = 0; tt < kTilesPerWarp; ++tt)
+#pragma unroll
+              for (int pp = 0; pp < kParts<BITS>; ++pp)
+                in.r.w[bb][tt][pp] = *reinterpret_cast<const uint4*>(cb + tt * (SG::CB / 2) + pp * 512 + lane * 16);
+          }
+        }
+#pragma unroll
+        for (int gg = 0; gg < SG::GU; ++gg) {
+#pragma unroll
+          for (int tt = 0; tt < kTilesPerWarp; ++tt) {
+            const int gi = d * SG::GU + gg;
+            in.r.s[gg][tt] = *reinterpret_cast<const uint32_t*>(sb + SG::kScaleOff + gi * 64 + tt * 32 + g * 4);
+            if (SYM)
+              in.r.z[gg][tt] = 0u;
+            else if (BITS == 8)
+              in.r.z[gg][tt] = *reinterpret_cast<const uint16_t*>(sb + SG::kZeroOff + gi * 32 + (tt * 8 + g) * 2);
+            else
+              in.r.z[gg][tt] = sb[SG::kZeroOff + gi * 16 + tt * 8 + g];
+          }
+          if (XS) {
+#pragma unroll
+            for (int nb = 0; nb < NB; ++nb) {
+              const int tk = min(nb * 8 + 2 * t, MP - 1);
+              in.xsg[gg][nb][0] = xsum[(ku * SG::GU + gg) * MP + tk];
+              in.xsg[gg][nb][1] = xsum[(ku * SG::GU + gg) * MP + min(tk + 1, MP - 1)];
+            }
+          }
+        }
+      };
+      auto compute_in = [&](const UnitIn& in, int ku) {
+        const int xo = ku * SG::UB * kColsPerBlock;
+        if (XS)
+          compute_unit<NB, GS, SYM, kXShared, BITS, BITS == 4, true, MP == 1>(in.r, xl0 + xo, xl1 + xo, tot, in.xsg);
+        else
+          compute_unit<NB, GS, SYM, kXCoherent, BITS, BITS == 4>(in.r, xl0 + xo, xl1 + xo, tot);
+      };
       for (int k = 0; k < R; ++k) {
         if (!warp_outcome(wait_mbar(full0 + 8 * slot, phase, gd))) return;
         const unsigned char* sb = smem + size_t(slot) * SG::kSlot;
-        int rgl = rgl0, ku = ku0;
+        if (k * CU + (warp + 1) * SG::UPW <= s.T && ku0 + SG::UPW <= s.NU && rgl0 == cur) {
+          // common case: all of the warp's units exist and continue its row
+          // group -- straight-line code, every load ahead of the arithmetic
+          UnitIn in[SG::UPW];
 #pragma unroll
-        for (int i = 0; i < SG::UPW; ++i) {
-          const int d = warp * SG::UPW + i;
-          if (k * CU + d < s.T) {
-            if (rgl != cur) {
-              if (cur >= 0) flush(cur);
+          for (int i = 0; i < SG::UPW; ++i) load_unit_in(sb, warp * SG::UPW + i, ku0 + i, in[i]);
 #pragma unroll
-              for (int tt = 0; tt < kTilesPerWarp; ++tt)
+          for (int i = 0; i < SG::UPW; ++i) compute_in(in[i], ku0 + i);
+        } else {
+          int rgl = rgl0, ku = ku0;
 #pragma unroll
-                for (int nb = 0; nb < NB; ++nb)
-#pragma unroll
-                  for (int e = 0; e < 4; ++e) tot[tt][nb][e] = 0.f;
-              cur = rgl;
-            }
-            UnitRegs<GS, BITS> rr;
-#pragma unroll
-            for (int bb = 0; bb < SG::UB; ++bb) {
-              const unsigned char* cb = sb + d * SG::kUnitCode + bb * SG::CB;
-              if (BITS == 3) {
-                rr.w[bb][0][0] = *reinterpret_cast<const uint4*>(cb + lane * 16);
-                const uint2 v = *reinterpret_cast<const uint2*>(cb + 512 + lane * 8);
-                rr.w[bb][1][0] = make_uint4(v.x, v.y, 0u, 0u);
-              } else {
+          for (int i = 0; i < SG::UPW; ++i) {
+            const int d = warp * SG::UPW + i;
+            if (k * CU + d < s.T) {
+              if (rgl != cur) {
+                if (cur >= 0) flush(cur);
 #pragma unroll
                 for (int tt = 0; tt < kTilesPerWarp; ++tt)
 #pragma unroll
-                  for (int pp = 0; pp < kParts<BITS>; ++pp)
-                    rr.w[bb][tt][pp] =
-                        *reinterpret_cast<const uint4*>(cb + tt * (SG::CB / 2) + pp * 512 + lane * 16);
+                  for (int nb = 0; nb < NB; ++nb)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) tot[tt][nb][e] = 0.f;
+                cur = rgl;
               }
+              UnitIn in;
+              load_unit_in(sb, d, ku, in);
+              compute_in(in, ku);
             }
-#pragma unroll
-            for (int gg = 0; gg < SG::GU; ++gg)
-#pragma unroll
-              for (int tt = 0; tt < kTilesPerWarp; ++tt) {
-                const int gi = d * SG::GU + gg;
-                rr.s[gg][tt] = *reinterpret_cast<const uint32_t*>(sb + SG::kScaleOff + gi * 64 + tt * 32 + g * 4);
-                if (SYM)
-                  rr.z[gg][tt] = 0u;
-                else if (BITS == 8)
-                  rr.z[gg][tt] =
-                      *reinterpret_cast<const uint16_t*>(sb + SG::kZeroOff + gi * 32 + (tt * 8 + g) * 2);
-                else
-                  rr.z[gg][tt] = sb[SG::kZeroOff + gi * 16 + tt * 8 + g];
-              }
-            const int xo = ku * SG::UB * kColsPerBlock;
-            if (XS) {
-              // the unit's group sums, staged with the activations
-              float xsg[SG::GU][NB][2];
-#pragma unroll
-              for (int gg = 0; gg < SG::GU; ++gg)
-#pragma unroll
-                for (int nb = 0; nb < NB; ++nb) {
-                  const int tk = min(nb * 8 + 2 * t, MP - 1);
-                  xsg[gg][nb][0] = xsum[(ku * SG::GU + gg) * MP + tk];
-                  xsg[gg][nb][1] = xsum[(ku * SG::GU + gg) * MP + min(tk + 1, MP - 1)];
-                }
-              compute_unit<NB, GS, SYM, kXShared, BITS, BITS == 4, true, MP == 1>(rr, xl0 + xo, xl1 + xo, tot, xsg);
-            } else {
-              compute_unit<NB, GS, SYM, kXCoherent, BITS, BITS == 4>(rr, xl0 + xo, xl1 + xo, tot);
+            if (++ku == s.NU) {  // the warp's next unit in this slot
+              ku = 0;
+              ++rgl;
             }
-          }
-          if (++ku == s.NU) {  // the warp's next unit in this slot
-            ku = 0;
-            ++rgl;
           }
         }
         __syncwarp();
