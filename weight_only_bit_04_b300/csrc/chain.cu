@@ -173,10 +173,15 @@ w4a16_status w4a16_chain_prepare(const w4a16_format* formats, const w4a16_chain_
   info->M = M;
   info->n_slices = n_slices;
   info->blocks = int32_t(P);
-  int32_t staged = 1;  // every layer's activations fit in the block's shared memory
+  // Staged activations: one buffer big enough for every layer; two when they
+  // fit (the next layer's activations then land while this one computes).
+  long long xbuf = 0;
   for (int32_t i = 0; i < n_layers; ++i)
-    if (!stream_x_fits(formats[i].K, int(M), formats[0].bits, formats[0].group_size)) staged = 0;
-  info->flags = staged;
+    xbuf = std::max(xbuf, stream_x_buf(formats[i].K, int(M), formats[0].group_size));
+  const long long xroom = stream_x_bytes(formats[0].bits, formats[0].group_size, stream_mp(int(M)));
+  const int32_t nbuf = 2 * xbuf <= xroom ? 2 : xbuf <= xroom ? 1 : 0;
+  info->flags = nbuf;            // staged-activation buffers (0: read through L1)
+  info->reserved_x = int32_t(xbuf);
   return W4A16_OK;
 }
 
@@ -201,7 +206,8 @@ w4a16_status w4a16_chain_run(const w4a16_chain_info* info, void* workspace, w4a1
   c.done = reinterpret_cast<unsigned int*>(ws);
   c.n_jobs = int(info->n_slices);
   c.M = int(info->M);
-  c.x_staged = (info->flags & 1) != 0;
+  c.x_nbuf = info->flags & 3;
+  c.x_buf_bytes = c.x_nbuf ? info->reserved_x : 0;
   e = launch_stream(c, info->bits, info->group_size, info->symmetric != 0, info->blocks, st);
   return e == cudaSuccess ? W4A16_OK : cuda_error_status(e);
 }

@@ -205,7 +205,8 @@ __global__ void __launch_bounds__(kStreamThreads, 1) decode_stream_kernel(const 
   const uint32_t rdy0 = cdone0 + 16;
   const uint32_t fdone0 = rdy0 + 16;
   float* part = reinterpret_cast<float*>(smem + stream_part_off(BITS, GS));  // [2][RGMAX][NW][32 rows][MP]
-  uint16_t* xs = reinterpret_cast<uint16_t*>(smem + stream_x_off(BITS, GS, MP));  // [M][stride] (XS)
+  unsigned char* xbase = smem + stream_x_off(BITS, GS, MP);  // staged-activation buffers (XS)
+  int* xsel = reinterpret_cast<int*>(smem + stream_xsel_off(BITS, GS));  // per layer parity: byte offset of its buffer
 
   const int tid = int(threadIdx.x);
   const int warp = tid >> 5, lane = tid & 31;
@@ -347,6 +348,8 @@ __global__ void __launch_bounds__(kStreamThreads, 1) decode_stream_kernel(const 
     bool stale = true;  // the staged activations may be out of date
     const uint16_t* loaded = nullptr;
     int loaded_k = 0;
+    int cur = 0;                // buffer holding the current activations
+    int last_use[2] = {-1, -1};  // last layer that read each buffer
     for (int j = 0; j < nj; ++j) {
       const StreamJob J = Jn;
       if (j + 1 < nj) Jn = load_job(c.jobs, j + 1);
@@ -372,8 +375,12 @@ __global__ void __launch_bounds__(kStreamThreads, 1) decode_stream_kernel(const 
       if (s.n > 0) {
         if (XS) {
           if (stale || J.x != loaded || J.K != loaded_k) {
-            // the buffer still holds the previous layer's activations
-            if (!wait_layer(cdone0, j - 1, gd)) return;
+            // the other buffer when there are two; it was last read by layer
+            // j - 1 at the latest, and every layer before j - 1 is done
+            const int nb = c.x_nbuf == 2 ? cur ^ 1 : 0;
+            if (last_use[nb] == j - 1 && !wait_layer(cdone0, j - 1, gd)) return;
+            cur = nb;
+            uint16_t* xs = reinterpret_cast<uint16_t*>(xbase + size_t(nb) * c.x_buf_bytes);
             // Stage x: every lane lands 16-byte chunks with cp.async, all in
             // flight at once; then each lane adds whole groups of one token
             // row from shared memory (fixed order per group; the chunk order
@@ -403,7 +410,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1) decode_stream_kernel(const 
             for (int p = lane; p < M * ng; p += 32) {
               const int tok = p / ng, gi = p - tok * ng;
               const uint16_t* gx = xs + tok * stride + gi * GS;
-              float acc = 0.f;
+              float acc[4] = {0.f, 0.f, 0.f, 0.f};  // one chain per word of a chunk
 #pragma unroll
               for (int c = 0; c < CPG; ++c) {
                 const int cc = (c + gi) & (CPG - 1);
@@ -412,17 +419,18 @@ __global__ void __launch_bounds__(kStreamThreads, 1) decode_stream_kernel(const 
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                   const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&wv[e]));
-                  acc += f.x;
-                  acc += f.y;
+                  acc[e] += f.x;
+                  acc[e] += f.y;
                 }
               }
-              xsum[gi * MP + tok] = acc;
+              xsum[gi * MP + tok] = (acc[0] + acc[1]) + (acc[2] + acc[3]);
             }
             __syncwarp();
             loaded = J.x;
             loaded_k = J.K;
             stale = false;
           }
+          last_use[cur] = j;
         } else {
           const char* xb = reinterpret_cast<const char*>(J.x);
           const int bytes = M * J.K * 2;
@@ -430,7 +438,10 @@ __global__ void __launch_bounds__(kStreamThreads, 1) decode_stream_kernel(const 
         }
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(rdy0 + 8 * (j & 1));
+      if (lane == 0) {
+        xsel[j & 1] = cur * c.x_buf_bytes;
+        mbar_arrive(rdy0 + 8 * (j & 1));  // release: the staged rows, sums and xsel
+      }
     }
     return;
   }
@@ -491,6 +502,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1) decode_stream_kernel(const 
       const int R = (s.T + CU - 1) / CU;
       const uint16_t* xl0;
       const uint16_t* xl1;
+      const uint16_t* xs = reinterpret_cast<const uint16_t*>(xbase + (XS ? xsel[j & 1] : 0));
       const float* xsum = reinterpret_cast<const float*>(xs + stream_xsum_off(J.K, M) / 2);
       if (XS) {
         const int64_t stride = stream_x_stride(J.K, M);
@@ -674,7 +686,7 @@ cudaError_t launch_stream_mp(const StreamLaunch& c, int sm_count, cudaStream_t s
 
 template <int GS, bool SYM, int BITS>
 cudaError_t launch_stream_x(const StreamLaunch& c, int sm_count, cudaStream_t stream) {
-  return c.x_staged ? launch_stream_mp<GS, SYM, BITS, true>(c, sm_count, stream)
+  return c.x_nbuf ? launch_stream_mp<GS, SYM, BITS, true>(c, sm_count, stream)
                     : launch_stream_mp<GS, SYM, BITS, false>(c, sm_count, stream);
 }
 

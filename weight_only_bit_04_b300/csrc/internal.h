@@ -108,7 +108,8 @@ struct StreamLaunch {
   const CUtensorMap* maps;  // device array, 64-byte aligned
   unsigned int* done;       // per slice a count of finished blocks (128-byte stride), then the abort flag
   int n_jobs, M;
-  int x_staged;             // every layer's activations fit in shared memory
+  int x_buf_bytes;          // bytes of one staged-activation buffer (0: activations not staged)
+  int x_nbuf;               // staged-activation buffers, 1 or 2
 };
 cudaError_t launch_stream(const StreamLaunch& c, int bits, int gsize, bool sym, int sm_count, cudaStream_t stream);
 

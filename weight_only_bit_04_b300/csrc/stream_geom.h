@@ -71,13 +71,18 @@ __host__ __device__ constexpr int stream_max_rg(int mp) { return mp <= 2 ? 8 : m
 __host__ __device__ constexpr int stream_part_bytes(int mp) { return 2 * stream_max_rg(mp) * kStreamConsumers * 32 * mp * 4; }
 
 // Shared memory of one thread block: ring | barriers (full and empty per
-// slot, three pairs per layer parity) | two partial-sum buffers | staged
-// activations and their group sums (the rest, up to kStreamSmem).
+// slot, three pairs per layer parity) and two buffer-selection words | two
+// partial-sum buffers | one or two staged-activation buffers (rows and group
+// sums; the rest of the block's shared memory, up to kStreamSmem).
 __host__ __device__ constexpr int stream_bar_off(int bits, int gs) {
   return stream_slots(bits, gs) * stream_slot_bytes(bits, gs);
 }
+// after the barriers: two words naming the staged-activation buffer of each layer parity
+__host__ __device__ constexpr int stream_xsel_off(int bits, int gs) {
+  return stream_bar_off(bits, gs) + (2 * stream_slots(bits, gs) + 6) * 8;
+}
 __host__ __device__ constexpr int stream_part_off(int bits, int gs) {
-  return stream_bar_off(bits, gs) + stream_align128((2 * stream_slots(bits, gs) + 6) * 8);
+  return stream_bar_off(bits, gs) + stream_align128((2 * stream_slots(bits, gs) + 6) * 8 + 16);
 }
 __host__ __device__ constexpr int stream_x_off(int bits, int gs, int mp) {
   return stream_part_off(bits, gs) + stream_part_bytes(mp);
@@ -91,8 +96,9 @@ __host__ __device__ constexpr long long stream_x_stride(long long K, int M) { re
 __host__ __device__ constexpr long long stream_xsum_off(long long K, int M) {  // bytes from the staged rows
   return M * stream_x_stride(K, M) * 2;
 }
-__host__ __device__ constexpr bool stream_x_fits(long long K, int M, int bits, int gs) {
-  return stream_xsum_off(K, M) + (K / gs) * stream_mp(M) * 4 <= stream_x_bytes(bits, gs, stream_mp(M));
+// Bytes of one staged-activation buffer for a layer (rows, then group sums).
+__host__ __device__ constexpr long long stream_x_buf(long long K, int M, int gs) {
+  return (stream_xsum_off(K, M) + (K / gs) * stream_mp(M) * 4 + 127) / 128 * 128;
 }
 
 }  // namespace w4a16

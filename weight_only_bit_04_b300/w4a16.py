@@ -85,6 +85,8 @@ class ChainInfo(ctypes.Structure):
         ("n_slices", ctypes.c_int64),
         ("blocks", ctypes.c_int32),
         ("flags", ctypes.c_int32),
+        ("reserved_x", ctypes.c_int32),
+        ("reserved", ctypes.c_int32),
     ]
 
 SIGNATURES = {
