@@ -30,15 +30,18 @@
 //    (gemv_impl.cuh, compute_unit). Each warp keeps one partial sum per row
 //    group and writes it to shared memory.
 //  * A finishing warp adds a row group's partial sums in warp order
-//    (deterministic), rounds to fp16, writes y, fences, and counts the layer
-//    as done on a device counter (one per layer slice, 128-byte lines).
+//    (deterministic), releases the partial buffer to the consumers, rounds
+//    to fp16, writes y, fences, and counts the layer as done on a device
+//    counter (one per layer slice, 128-byte lines).
 //  * A dependency warp walks the layers ahead of the consumers: for a layer
-//    that reads earlier layers' outputs it polls their counters with relaxed
-//    loads until every block has finished them, then fences once (acquire).
-//    It then stages the layer's activations in shared memory together with
-//    each group's activation sum (when they fit; otherwise the consumers read
-//    them through L1 after an L1 prefetch and get the group sums from the
-//    tensor cores), and publishes the layer as ready.
+//    that reads earlier layers' outputs it polls their counters (acquire
+//    loads) until every block has finished them. The layer's activations
+//    are staged in shared memory together with each group's activation sum
+//    when they fit (otherwise the consumers read them through L1 after an L1
+//    prefetch and get the group sums from the tensor cores): by this warp,
+//    ahead of the consumers, when no dependency was just acquired; by the
+//    eight consumer warps together, which would otherwise idle, right after
+//    one was. The warp then publishes the layer as ready.
 //
 // Every wait is bounded (1 s by the global timer) and also gives up when
 // another block has raised the abort flag; a wait that times out is counted
@@ -88,7 +91,9 @@ struct Span {
 __device__ __forceinline__ Span span_of(const StreamJob& J, int P, int b, int UB) {
   int p = b - J.rot;
   if (p < 0) p += P;
-  const int lo = int(int64_t(p) * J.n_rg / P), hi = int(int64_t(p + 1) * J.n_rg / P);
+  // 32-bit: a slice has at most stream_max_rg(MP) row groups per block
+  const int lo = int(uint32_t(p) * uint32_t(J.n_rg) / uint32_t(P));
+  const int hi = int(uint32_t(p + 1) * uint32_t(J.n_rg) / uint32_t(P));
   Span s;
   s.rg0 = J.rg_first + lo;
   s.n = hi - lo;
@@ -149,15 +154,6 @@ __device__ __forceinline__ int wait_mbar(uint32_t bar, uint32_t parity, Guard& g
   }
   return kWaitOk;
 }
-// Wait until the device counter reaches v (relaxed; the caller fences).
-__device__ __forceinline__ int wait_counter_ge(const unsigned int* p, unsigned int v, Guard& gd) {
-  gd.start();
-  while (ld_relaxed_gpu_u32(p) < v) {
-    const int st = gd.check();
-    if (st != kWaitOk) return st;
-  }
-  return kWaitOk;
-}
 // Whole-warp outcome of a wait every lane took part in: true = go on.
 __device__ __forceinline__ bool warp_outcome(int st) {
   const bool timed = __any_sync(0xffffffffu, st == kWaitTimeout);
@@ -182,6 +178,51 @@ __device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
   asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
 }
 
+constexpr int kConsumersStage = 1 << 30;
+constexpr int kConsumerBarrier = 1;  // named barrier of the consumer warps
+
+// Land the activations of a layer (M rows of K) in a staged buffer and add
+// each group of each row (fixed order per group). `tid` / `nt`: this thread's
+// index among the `nt` threads that share the work; the caller makes the
+// copies visible to all of them (cp.async.wait_all + barrier) between the two.
+template <int GS, int MP>
+__device__ __forceinline__ void stage_copy(const uint16_t* x, int K, int M, uint16_t* xs, int tid, int nt) {
+  const int64_t stride = stream_x_stride(K, M);
+  const int cpr = K / 8, total = M * cpr;
+  int tok = tid / cpr, kc = tid - tok * cpr;  // chunk (tok, kc) advanced by nt without dividing
+  for (int q = tid; q < total; q += nt) {
+    cp_async_16_cg(smem_addr(xs + tok * stride + kc * 8), x + size_t(tok) * K + kc * 8);
+    kc += nt;
+    while (kc >= cpr) {
+      kc -= cpr;
+      ++tok;
+    }
+  }
+}
+template <int GS, int MP>
+__device__ __forceinline__ void stage_sums(int K, int M, int G, const uint16_t* xs, float* xsum, int tid, int nt) {
+  constexpr int CPG = GS / 8;  // 16-byte chunks per group
+  const int64_t stride = stream_x_stride(K, M);
+  for (int p = tid; p < M * G; p += nt) {
+    const int tok = p / G, gi = p - tok * G;
+    const uint16_t* gx = xs + tok * stride + gi * GS;
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};  // one chain per word of a chunk
+#pragma unroll
+    for (int c = 0; c < CPG; ++c) {
+      const int cc = (c + gi) & (CPG - 1);  // rotated start: lanes on different banks
+      const uint4 v = *reinterpret_cast<const uint4*>(gx + cc * 8);
+      const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&wv[e]));
+        acc[e] += f.x;
+        acc[e] += f.y;
+      }
+    }
+    xsum[gi * MP + tok] = (acc[0] + acc[1]) + (acc[2] + acc[3]);
+  }
+}
+
 template <int MP, int GS, bool SYM, int BITS, bool XS>
 __global__ void __launch_bounds__(kStreamThreads, 1) decode_stream_kernel(const StreamLaunch c) {
   using SG = SGeo<BITS, GS>;
@@ -195,10 +236,10 @@ __global__ void __launch_bounds__(kStreamThreads, 1) decode_stream_kernel(const 
   const uint32_t ring = smem_addr(smem);
   // mbarriers: full[S], empty[S] (the ring), then per layer parity (j & 1):
   // cdone (the consumer warps have written layer j's partial sums), rdy (layer
-  // j's activations may be read), fdone (the finishing warp is done with layer
-  // j). Phase (j >> 1) & 1 of
-  // barrier j & 1 is layer j's; no role runs far enough ahead of another for
-  // that to be ambiguous (see the waits below).
+  // j's activations may be read), fdone (the finishing warp has read layer j's
+  // partial sums). Phase (j >> 1) & 1 of barrier j & 1 is layer j's; no role
+  // runs far enough ahead of another for that to be ambiguous (see the waits
+  // below).
   const uint32_t full0 = ring + stream_bar_off(BITS, GS);
   const uint32_t empty0 = full0 + S * 8;
   const uint32_t cdone0 = empty0 + S * 8;
@@ -206,7 +247,9 @@ __global__ void __launch_bounds__(kStreamThreads, 1) decode_stream_kernel(const 
   const uint32_t fdone0 = rdy0 + 16;
   float* part = reinterpret_cast<float*>(smem + stream_part_off(BITS, GS));  // [2][RGMAX][NW][32 rows][MP]
   unsigned char* xbase = smem + stream_x_off(BITS, GS, MP);  // staged-activation buffers (XS)
-  int* xsel = reinterpret_cast<int*>(smem + stream_xsel_off(BITS, GS));  // per layer parity: byte offset of its buffer
+  // per layer parity: byte offset of the layer's staged-activation buffer;
+  // kConsumersStage set when the consumer warps stage it themselves
+  int* xsel = reinterpret_cast<int*>(smem + stream_xsel_off(BITS, GS));
 
   const int tid = int(threadIdx.x);
   const int warp = tid >> 5, lane = tid & 31;
@@ -348,14 +391,16 @@ __global__ void __launch_bounds__(kStreamThreads, 1) decode_stream_kernel(const 
     bool stale = true;  // the staged activations may be out of date
     const uint16_t* loaded = nullptr;
     int loaded_k = 0;
-    int cur = 0;                // buffer holding the current activations
-    int last_use[2] = {-1, -1};  // last layer that read each buffer
+    int cur = 0;                    // buffer holding the current activations
+    int last_use0 = -1, last_use1 = -1;  // last layer that read buffer 0 / 1
     for (int j = 0; j < nj; ++j) {
       const StreamJob J = Jn;
       if (j + 1 < nj) Jn = load_job(c.jobs, j + 1);
       // one layer ahead: every consumer warp has finished layer j - 2 (they
       // cannot finish layer j before this warp publishes it)
       if (!wait_layer(cdone0, j - 2, gd)) return;
+      bool fresh = false;  // a dependency of this layer was acquired just now
+      int xmode = 0;
       if (J.wait_lo <= J.wait_hi && J.wait_hi > known) {
         // every lane polls with acquire loads (one transaction per poll), so
         // each lane's later loads see what those layers wrote
@@ -370,6 +415,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1) decode_stream_kernel(const 
         if (!warp_outcome(st)) return;
         known = J.wait_hi;
         stale = true;
+        fresh = true;
       }
       const Span s = span_of(J, P, b, SG::UB);
       if (s.n > 0) {
@@ -378,59 +424,28 @@ __global__ void __launch_bounds__(kStreamThreads, 1) decode_stream_kernel(const 
             // the other buffer when there are two; it was last read by layer
             // j - 1 at the latest, and every layer before j - 1 is done
             const int nb = c.x_nbuf == 2 ? cur ^ 1 : 0;
-            if (last_use[nb] == j - 1 && !wait_layer(cdone0, j - 1, gd)) return;
+            if ((nb ? last_use1 : last_use0) == j - 1 && !wait_layer(cdone0, j - 1, gd)) return;
             cur = nb;
             uint16_t* xs = reinterpret_cast<uint16_t*>(xbase + size_t(nb) * c.x_buf_bytes);
-            // Stage x: every lane lands 16-byte chunks with cp.async, all in
-            // flight at once; then each lane adds whole groups of one token
-            // row from shared memory (fixed order per group; the chunk order
-            // is rotated by the group so that lanes hit different banks).
-            const int64_t stride = stream_x_stride(J.K, M);
-            float* xsum = reinterpret_cast<float*>(xs + stream_xsum_off(J.K, M) / 2);
-            const int cpr = J.K / 8, total = M * cpr;
-            {
-              int tok = 0, kc = lane;
-              while (kc >= cpr) {
-                kc -= cpr;
-                ++tok;
-              }
-              for (int q = lane; q < total; q += 32) {
-                cp_async_16_cg(smem_addr(xs + tok * stride + kc * 8), J.x + size_t(tok) * J.K + kc * 8);
-                kc += 32;
-                while (kc >= cpr) {
-                  kc -= cpr;
-                  ++tok;
-                }
-              }
+            if (!fresh) {
+              // ahead of the consumers (no dependency was just acquired):
+              // stage here, overlapped with their work on earlier layers
+              float* xsum = reinterpret_cast<float*>(xs + stream_xsum_off(J.K, M) / 2);
+              stage_copy<GS, MP>(J.x, J.K, M, xs, lane, 32);
+              cp_async_wait_all();
+              __syncwarp();
+              stage_sums<GS, MP>(J.K, M, J.G, xs, xsum, lane, 32);
+              __syncwarp();
             }
-            cp_async_wait_all();
-            __syncwarp();
-            constexpr int CPG = GS / 8;  // chunks per group
-            const int ng = J.G;
-            for (int p = lane; p < M * ng; p += 32) {
-              const int tok = p / ng, gi = p - tok * ng;
-              const uint16_t* gx = xs + tok * stride + gi * GS;
-              float acc[4] = {0.f, 0.f, 0.f, 0.f};  // one chain per word of a chunk
-#pragma unroll
-              for (int c = 0; c < CPG; ++c) {
-                const int cc = (c + gi) & (CPG - 1);
-                const uint4 v = *reinterpret_cast<const uint4*>(gx + cc * 8);
-                const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                  const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&wv[e]));
-                  acc[e] += f.x;
-                  acc[e] += f.y;
-                }
-              }
-              xsum[gi * MP + tok] = (acc[0] + acc[1]) + (acc[2] + acc[3]);
-            }
-            __syncwarp();
+            xmode = fresh ? kConsumersStage : 0;
             loaded = J.x;
             loaded_k = J.K;
             stale = false;
           }
-          last_use[cur] = j;
+          if (cur)
+            last_use1 = j;
+          else
+            last_use0 = j;
         } else {
           const char* xb = reinterpret_cast<const char*>(J.x);
           const int bytes = M * J.K * 2;
@@ -439,7 +454,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1) decode_stream_kernel(const 
       }
       __syncwarp();
       if (lane == 0) {
-        xsel[j & 1] = cur * c.x_buf_bytes;
+        xsel[j & 1] = cur * c.x_buf_bytes + xmode;
         mbar_arrive(rdy0 + 8 * (j & 1));  // release: the staged rows, sums and xsel
       }
     }
@@ -454,30 +469,47 @@ __global__ void __launch_bounds__(kStreamThreads, 1) decode_stream_kernel(const 
       // the consumers cannot finish layer j + 2 before this warp is done with layer j
       if (!wait_layer(cdone0, j, gd)) return;
       const Span s = span_of(J, P, b, SG::UB);
+      // Row `lane` of each owned row group, every token: the partial sums in
+      // warp order (deterministic), kept in registers so that the partial
+      // buffer is released before the stores and the fence.
+      float acc[RGMAX][MP];
       if (s.n > 0) {
         const float* pb = part + size_t(j & 1) * RGMAX * NW * 32 * MP;
-        for (int rgl = 0; rgl < s.n; ++rgl) {
+#pragma unroll
+        for (int rgl = 0; rgl < RGMAX; ++rgl) {
+          if (rgl >= s.n) break;
           // warps holding a piece of this row group: all of them unless it has fewer units than a slot
           uint32_t mask = (1u << NW) - 1u;
           if (s.NU < CU) {
             mask = 0;
             for (int u = rgl * s.NU; u < rgl * s.NU + s.NU; ++u) mask |= 1u << ((u % CU) / SG::UPW);
           }
-          const int n = (s.rg0 + rgl) * 32 + lane;
-          for (int tok = 0; tok < M; ++tok) {
-            float acc = 0.f;
-            for (int w = 0; w < NW; ++w)  // warp order
-              if (mask & (1u << w)) acc += pb[(size_t(rgl * NW + w) * 32 + lane) * MP + tok];
-            if (n < J.N) J.y[size_t(tok) * J.N + n] = __half_as_ushort(__float2half_rn(acc));
+#pragma unroll
+          for (int tok = 0; tok < MP; ++tok) {
+            float a = 0.f;
+            if (tok < M)
+#pragma unroll
+              for (int w = 0; w < NW; ++w)
+                if (mask & (1u << w)) a += pb[(size_t(rgl * NW + w) * 32 + lane) * MP + tok];
+            acc[rgl][tok] = a;
           }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(fdone0 + 8 * (j & 1));  // partial buffer j & 1 is free
+      if (s.n > 0) {
+#pragma unroll
+        for (int rgl = 0; rgl < RGMAX; ++rgl) {
+          if (rgl >= s.n) break;
+          const int n = (s.rg0 + rgl) * 32 + lane;
+#pragma unroll
+          for (int tok = 0; tok < MP; ++tok)
+            if (tok < M && n < J.N) J.y[size_t(tok) * J.N + n] = __half_as_ushort(__float2half_rn(acc[rgl][tok]));
         }
         fence_acq_rel_gpu();  // this lane's stores are visible device-wide
       }
       __syncwarp();
-      if (lane == 0) {
-        red_relaxed_gpu_add_u32(done + size_t(j) * CS, 1u);
-        mbar_arrive(fdone0 + 8 * (j & 1));
-      }
+      if (lane == 0) red_relaxed_gpu_add_u32(done + size_t(j) * CS, 1u);
     }
     return;
   }
@@ -498,11 +530,25 @@ __global__ void __launch_bounds__(kStreamThreads, 1) decode_stream_kernel(const 
     // per-layer barrier then has at most one phase of its parity in flight.
     if (!wait_layer(rdy0, j, gd)) return;
     if (!wait_layer(fdone0, j - 2, gd)) return;
+    if (XS && (xsel[j & 1] & kConsumersStage)) {
+      // a dependency was just acquired: the consumer warps stage the
+      // activations together (the dependency warp's acquire happens before
+      // the ready barrier this warp waited on)
+      uint16_t* xs_st = reinterpret_cast<uint16_t*>(xbase + (xsel[j & 1] & ~kConsumersStage));
+      stage_copy<GS, MP>(J.x, J.K, M, xs_st, tid, NW * 32);
+      cp_async_wait_all();
+      __syncwarp();  // bar.sync is warp-aligned: converge after the divergent loop
+      named_bar_sync(kConsumerBarrier, NW * 32);
+      stage_sums<GS, MP>(J.K, M, J.G, xs_st, reinterpret_cast<float*>(xs_st + stream_xsum_off(J.K, M) / 2), tid,
+                         NW * 32);
+      __syncwarp();
+      named_bar_sync(kConsumerBarrier, NW * 32);
+    }
     if (s.T > 0) {
       const int R = (s.T + CU - 1) / CU;
       const uint16_t* xl0;
       const uint16_t* xl1;
-      const uint16_t* xs = reinterpret_cast<const uint16_t*>(xbase + (XS ? xsel[j & 1] : 0));
+      const uint16_t* xs = reinterpret_cast<const uint16_t*>(xbase + (XS ? (xsel[j & 1] & ~kConsumersStage) : 0));
       const float* xsum = reinterpret_cast<const float*>(xs + stream_xsum_off(J.K, M) / 2);
       if (XS) {
         const int64_t stride = stream_x_stride(J.K, M);
