@@ -199,27 +199,48 @@ __device__ __forceinline__ void stage_copy(const uint16_t* x, int K, int M, uint
     }
   }
 }
-template <int GS, int MP>
-__device__ __forceinline__ void stage_sums(int K, int M, int G, const uint16_t* xs, float* xsum, int tid, int nt) {
+// Sum of the eight halves of a 16-byte chunk, in a fixed order.
+__device__ __forceinline__ float chunk_sum(const uint4 v) {
+  const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&v.x));
+  const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&v.y));
+  const float2 c = __half22float2(*reinterpret_cast<const __half2*>(&v.z));
+  const float2 d = __half22float2(*reinterpret_cast<const __half2*>(&v.w));
+  return ((a.x + a.y) + (b.x + b.y)) + ((c.x + c.y) + (d.x + d.y));
+}
+// Group sums: chunk c of a group is added by lane c of an aligned run of
+// GS / 8 lanes, and the run adds its chunk sums as a butterfly (every lane
+// gets the same value). The result does not depend on how many threads share
+// the work, so the dependency warp alone and the consumer warps together
+// produce identical sums.
+template <int GS, int MP, int U>  // U: rounds in flight at once
+__device__ __forceinline__ void stage_sums(int K, int M, const uint16_t* xs, float* xsum, int tid, int nt) {
   constexpr int CPG = GS / 8;  // 16-byte chunks per group
   const int64_t stride = stream_x_stride(K, M);
-  for (int p = tid; p < M * G; p += nt) {
-    const int tok = p / G, gi = p - tok * G;
-    const uint16_t* gx = xs + tok * stride + gi * GS;
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};  // one chain per word of a chunk
+  const int cpr = K / 8, total = M * cpr;
+  const int lane = tid & 31;
+  int tok = tid / cpr, kc = tid - tok * cpr;  // this thread's chunk, advanced by nt without dividing
+  for (int q0 = 0; q0 < total; q0 += U * nt) {  // the same trip count for every thread (shuffles below)
+    float v[U];
+    int tk[U], kk[U];
 #pragma unroll
-    for (int c = 0; c < CPG; ++c) {
-      const int cc = (c + gi) & (CPG - 1);  // rotated start: lanes on different banks
-      const uint4 v = *reinterpret_cast<const uint4*>(gx + cc * 8);
-      const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&wv[e]));
-        acc[e] += f.x;
-        acc[e] += f.y;
+    for (int u = 0; u < U; ++u) {
+      tk[u] = tok;
+      kk[u] = kc;
+      // a run of CPG lanes is valid or not as a whole: total and nt are multiples of CPG
+      v[u] = q0 + u * nt + tid < total ? chunk_sum(*reinterpret_cast<const uint4*>(xs + tok * stride + kc * 8)) : 0.f;
+      kc += nt;
+      while (kc >= cpr) {
+        kc -= cpr;
+        ++tok;
       }
     }
-    xsum[gi * MP + tok] = (acc[0] + acc[1]) + (acc[2] + acc[3]);
+#pragma unroll
+    for (int o = 1; o < CPG; o <<= 1)
+#pragma unroll
+      for (int u = 0; u < U; ++u) v[u] += __shfl_xor_sync(0xffffffffu, v[u], o);
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+      if (q0 + u * nt + tid < total && (lane & (CPG - 1)) == 0) xsum[(kk[u] / CPG) * MP + tk[u]] = v[u];
   }
 }
 
@@ -396,9 +417,11 @@ __global__ void __launch_bounds__(kStreamThreads, 1) decode_stream_kernel(const 
     for (int j = 0; j < nj; ++j) {
       const StreamJob J = Jn;
       if (j + 1 < nj) Jn = load_job(c.jobs, j + 1);
-      // one layer ahead: every consumer warp has finished layer j - 2 (they
-      // cannot finish layer j before this warp publishes it)
-      if (!wait_layer(cdone0, j - 2, gd)) return;
+      // This warp publishes layer j only once every consumer warp has finished
+      // layer j - 2 (so that no per-layer barrier has two phases of one parity
+      // in flight); before that it already polls layer j's dependencies and
+      // stages its activations when their buffer is free.
+      bool seen2 = false;  // layer j - 2's consumer barrier observed in this iteration
       bool fresh = false;  // a dependency of this layer was acquired just now
       int xmode = 0;
       if (J.wait_lo <= J.wait_hi && J.wait_hi > known) {
@@ -421,10 +444,17 @@ __global__ void __launch_bounds__(kStreamThreads, 1) decode_stream_kernel(const 
       if (s.n > 0) {
         if (XS) {
           if (stale || J.x != loaded || J.K != loaded_k) {
-            // the other buffer when there are two; it was last read by layer
-            // j - 1 at the latest, and every layer before j - 1 is done
+            // the other buffer when there are two. Its last reader finished
+            // if that was layer j - 3 or earlier (this warp saw layer j - 3's
+            // consumer barrier one layer ago); layers j - 2 and j - 1 are
+            // waited for here, in order.
             const int nb = c.x_nbuf == 2 ? cur ^ 1 : 0;
-            if ((nb ? last_use1 : last_use0) == j - 1 && !wait_layer(cdone0, j - 1, gd)) return;
+            const int lu = nb ? last_use1 : last_use0;
+            if (lu >= j - 2) {
+              if (!wait_layer(cdone0, j - 2, gd)) return;
+              seen2 = true;
+            }
+            if (lu == j - 1 && !wait_layer(cdone0, j - 1, gd)) return;
             cur = nb;
             uint16_t* xs = reinterpret_cast<uint16_t*>(xbase + size_t(nb) * c.x_buf_bytes);
             if (!fresh) {
@@ -434,7 +464,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1) decode_stream_kernel(const 
               stage_copy<GS, MP>(J.x, J.K, M, xs, lane, 32);
               cp_async_wait_all();
               __syncwarp();
-              stage_sums<GS, MP>(J.K, M, J.G, xs, xsum, lane, 32);
+              stage_sums<GS, MP, 8>(J.K, M, xs, xsum, lane, 32);
               __syncwarp();
             }
             xmode = fresh ? kConsumersStage : 0;
@@ -452,6 +482,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1) decode_stream_kernel(const 
           for (int off = lane * 128; off < bytes; off += 32 * 128) prefetch_l1(xb + off);
         }
       }
+      if (!seen2 && !wait_layer(cdone0, j - 2, gd)) return;  // also frees xsel[j & 1]
       __syncwarp();
       if (lane == 0) {
         xsel[j & 1] = cur * c.x_buf_bytes + xmode;
@@ -539,8 +570,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1) decode_stream_kernel(const 
       cp_async_wait_all();
       __syncwarp();  // bar.sync is warp-aligned: converge after the divergent loop
       named_bar_sync(kConsumerBarrier, NW * 32);
-      stage_sums<GS, MP>(J.K, M, J.G, xs_st, reinterpret_cast<float*>(xs_st + stream_xsum_off(J.K, M) / 2), tid,
-                         NW * 32);
+      stage_sums<GS, MP, 2>(J.K, M, xs_st, reinterpret_cast<float*>(xs_st + stream_xsum_off(J.K, M) / 2), tid, NW * 32);
       __syncwarp();
       named_bar_sync(kConsumerBarrier, NW * 32);
     }
@@ -641,9 +671,19 @@ __global__ void __launch_bounds__(kStreamThreads, 1) decode_stream_kernel(const 
       for (int k = 0; k < R; ++k) {
         if (!warp_outcome(wait_mbar(full0 + 8 * slot, phase, gd))) return;
         const unsigned char* sb = smem + size_t(slot) * SG::kSlot;
-        if (k * CU + (warp + 1) * SG::UPW <= s.T && ku0 + SG::UPW <= s.NU && rgl0 == cur) {
-          // common case: all of the warp's units exist and continue its row
+        if (k * CU + (warp + 1) * SG::UPW <= s.T && ku0 + SG::UPW <= s.NU) {
+          // common case: all of the warp's units exist and lie in one row
           // group -- straight-line code, every load ahead of the arithmetic
+          if (rgl0 != cur) {
+            if (cur >= 0) flush(cur);
+#pragma unroll
+            for (int tt = 0; tt < kTilesPerWarp; ++tt)
+#pragma unroll
+              for (int nb = 0; nb < NB; ++nb)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) tot[tt][nb][e] = 0.f;
+            cur = rgl0;
+          }
           UnitIn in[SG::UPW];
 #pragma unroll
           for (int i = 0; i < SG::UPW; ++i) load_unit_in(sb, warp * SG::UPW + i, ku0 + i, in[i]);
