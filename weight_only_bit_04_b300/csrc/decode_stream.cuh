@@ -483,6 +483,8 @@ __global__ void __launch_bounds__(kStreamThreads, 1) decode_stream_kernel(const 
         }
       }
       if (!seen2 && !wait_layer(cdone0, j - 2, gd)) return;  // also frees xsel[j & 1]
+      // and the finishing warp has read layer j - 2's partial sums (buffer j & 1)
+      if (!wait_layer(fdone0, j - 2, gd)) return;
       __syncwarp();
       if (lane == 0) {
         xsel[j & 1] = cur * c.x_buf_bytes + xmode;
@@ -550,17 +552,18 @@ __global__ void __launch_bounds__(kStreamThreads, 1) decode_stream_kernel(const 
   const int tok0 = min(g, M - 1), tok1 = min(g + 8, M - 1);
   int slot = 0;
   uint32_t phase = 0;
+  bool ready = false;  // the full barrier of ring slot `slot` was seen complete
   for (int j = 0; j < nj; ++j) {
     const StreamJob J = Jn;
     if (j + 1 < nj) Jn = load_job(c.jobs, j + 1);
     const Span s = span_of(J, P, b, SG::UB);
-    // Layer j's activations are readable, and the finishing warp is done
-    // with layer j - 2 (partial buffer j & 1 is free). Every warp waits for
-    // both in every layer, with or without units in it, so that no warp runs
-    // two layers ahead of the dependency and finishing warps: each
-    // per-layer barrier then has at most one phase of its parity in flight.
+    // Layer j's activations are readable, and (the dependency warp waited for
+    // it before publishing layer j) the finishing warp has read layer j - 2's
+    // partial sums, so partial buffer j & 1 is free. Every warp waits in every
+    // layer, with or without units in it, so that no warp runs two layers
+    // ahead of the dependency and finishing warps: each per-layer barrier
+    // then has at most one phase of its parity in flight.
     if (!wait_layer(rdy0, j, gd)) return;
-    if (!wait_layer(fdone0, j - 2, gd)) return;
     if (XS && (xsel[j & 1] & kConsumersStage)) {
       // a dependency was just acquired: the consumer warps stage the
       // activations together (the dependency warp's acquire happens before
@@ -669,7 +672,13 @@ __global__ void __launch_bounds__(kStreamThreads, 1) decode_stream_kernel(const 
           compute_unit<NB, GS, SYM, kXCoherent, BITS, BITS == 4>(in.r, xl0 + xo, xl1 + xo, tot);
       };
       for (int k = 0; k < R; ++k) {
-        if (!warp_outcome(wait_mbar(full0 + 8 * slot, phase, gd))) return;
+        if (!ready && !warp_outcome(wait_mbar(full0 + 8 * slot, phase, gd))) return;
+        // the ring's next slot (the next layer's, after this layer's last
+        // slot), tested now so that the answer is there after this slot
+        {
+          const int ns = slot + 1 == S ? 0 : slot + 1;
+          ready = mbar_test_wait(full0 + 8 * ns, ns == 0 ? phase ^ 1u : phase);
+        }
         const unsigned char* sb = smem + size_t(slot) * SG::kSlot;
         if (k * CU + (warp + 1) * SG::UPW <= s.T && ku0 + SG::UPW <= s.NU) {
           // common case: all of the warp's units exist and lie in one row
