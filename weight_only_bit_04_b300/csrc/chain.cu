@@ -161,6 +161,11 @@ w4a16_status w4a16_chain_prepare(const w4a16_format* formats, const w4a16_chain_
       J.map = i * kMapsPerLayer;
     }
   }
+  // Blocks finish their slices in table order, so "every block counted slice
+  // h" means every block finished every slice up to h: a wait for the range
+  // [lo, hi] polls slice hi's counter alone, and only such slices are counted.
+  for (const StreamJob& J : jobs)
+    if (J.wait_lo <= J.wait_hi) jobs[size_t(J.wait_hi)].signal = 1;
   char* ws = static_cast<char*>(workspace);
   e = cudaMemcpy(ws + wl.jobs, jobs.data(), jobs.size() * sizeof(StreamJob), cudaMemcpyHostToDevice);
   if (e == cudaSuccess)

@@ -31,8 +31,9 @@
 //    group and writes it to shared memory.
 //  * A finishing warp adds a row group's partial sums in warp order
 //    (deterministic), releases the partial buffer to the consumers, rounds
-//    to fp16, writes y, fences, and counts the layer as done on a device
-//    counter (one per layer slice, 128-byte lines).
+//    to fp16 and writes y. When a later layer waits for this one, it then
+//    fences and counts the layer as done on a device counter (one per layer
+//    slice, 128-byte lines).
 //  * A dependency warp walks the layers ahead of the consumers: for a layer
 //    that reads earlier layers' outputs it polls their counters (acquire
 //    loads) until every block has finished them. The layer's activations
@@ -87,6 +88,18 @@ struct Span {
   int NU;   // units per row group
   int T;    // units owned (n * NU)
 };
+
+// What the consumer warps need of layer j, written by the dependency warp
+// into shared memory (record j & 1) before it publishes the layer.
+struct alignas(16) LayerRec {
+  const uint16_t* x;  // activations in global memory
+  int K;
+  int T;     // units this block owns
+  int NU;    // units per row group
+  int xsel;  // byte offset of the staged-activation buffer, | kConsumersStage
+  int pad[2];
+};
+static_assert(sizeof(LayerRec) == kStreamRecBytes, "layer record size");
 
 __device__ __forceinline__ Span span_of(const StreamJob& J, int P, int b, int UB) {
   int p = b - J.rot;
@@ -268,9 +281,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1) decode_stream_kernel(const 
   const uint32_t fdone0 = rdy0 + 16;
   float* part = reinterpret_cast<float*>(smem + stream_part_off(BITS, GS));  // [2][RGMAX][NW][32 rows][MP]
   unsigned char* xbase = smem + stream_x_off(BITS, GS, MP);  // staged-activation buffers (XS)
-  // per layer parity: byte offset of the layer's staged-activation buffer;
-  // kConsumersStage set when the consumer warps stage it themselves
-  int* xsel = reinterpret_cast<int*>(smem + stream_xsel_off(BITS, GS));
+  LayerRec* rec = reinterpret_cast<LayerRec*>(smem + stream_rec_off(BITS, GS));  // per layer parity
 
   const int tid = int(threadIdx.x);
   const int warp = tid >> 5, lane = tid & 31;
@@ -425,15 +436,16 @@ __global__ void __launch_bounds__(kStreamThreads, 1) decode_stream_kernel(const 
       bool fresh = false;  // a dependency of this layer was acquired just now
       int xmode = 0;
       if (J.wait_lo <= J.wait_hi && J.wait_hi > known) {
-        // every lane polls with acquire loads (one transaction per poll), so
-        // each lane's later loads see what those layers wrote
+        // Every lane polls the counter of the range's last slice with acquire
+        // loads (one transaction per poll), so that each lane's later loads
+        // see what those layers wrote. The finishing warps count slices in
+        // table order, so once every block has counted the last slice of the
+        // range, every block has finished (and fenced) all slices up to it.
         int st = kWaitOk;
-        for (int d = known + 1; d <= J.wait_hi && st == kWaitOk; ++d) {
-          gd.start();
-          while (ld_acquire_gpu_u32(done + size_t(d) * CS) < unsigned(P)) {
-            st = gd.check();
-            if (st != kWaitOk) break;
-          }
+        gd.start();
+        while (ld_acquire_gpu_u32(done + size_t(J.wait_hi) * CS) < unsigned(P)) {
+          st = gd.check();
+          if (st != kWaitOk) break;
         }
         if (!warp_outcome(st)) return;
         known = J.wait_hi;
@@ -482,13 +494,20 @@ __global__ void __launch_bounds__(kStreamThreads, 1) decode_stream_kernel(const 
           for (int off = lane * 128; off < bytes; off += 32 * 128) prefetch_l1(xb + off);
         }
       }
-      if (!seen2 && !wait_layer(cdone0, j - 2, gd)) return;  // also frees xsel[j & 1]
+      if (!seen2 && !wait_layer(cdone0, j - 2, gd)) return;  // also frees record j & 1
       // and the finishing warp has read layer j - 2's partial sums (buffer j & 1)
       if (!wait_layer(fdone0, j - 2, gd)) return;
       __syncwarp();
       if (lane == 0) {
-        xsel[j & 1] = cur * c.x_buf_bytes + xmode;
-        mbar_arrive(rdy0 + 8 * (j & 1));  // release: the staged rows, sums and xsel
+        LayerRec r;
+        r.x = J.x;
+        r.K = J.K;
+        r.T = s.T;
+        r.NU = s.NU;
+        r.xsel = cur * c.x_buf_bytes + xmode;
+        r.pad[0] = r.pad[1] = 0;
+        rec[j & 1] = r;
+        mbar_arrive(rdy0 + 8 * (j & 1));  // release: the staged rows, sums and the record
       }
     }
     return;
@@ -539,10 +558,14 @@ __global__ void __launch_bounds__(kStreamThreads, 1) decode_stream_kernel(const 
           for (int tok = 0; tok < MP; ++tok)
             if (tok < M && n < J.N) J.y[size_t(tok) * J.N + n] = __half_as_ushort(__float2half_rn(acc[rgl][tok]));
         }
-        fence_acq_rel_gpu();  // this lane's stores are visible device-wide
       }
-      __syncwarp();
-      if (lane == 0) red_relaxed_gpu_add_u32(done + size_t(j) * CS, 1u);
+      if (J.signal) {
+        // this lane's stores, of this slice and every earlier one, are
+        // visible device-wide before the slice is counted
+        fence_acq_rel_gpu();
+        __syncwarp();
+        if (lane == 0) red_relaxed_gpu_add_u32(done + size_t(j) * CS, 1u);
+      }
     }
     return;
   }
@@ -552,44 +575,47 @@ __global__ void __launch_bounds__(kStreamThreads, 1) decode_stream_kernel(const 
   const int tok0 = min(g, M - 1), tok1 = min(g + 8, M - 1);
   int slot = 0;
   uint32_t phase = 0;
-  bool ready = false;  // the full barrier of ring slot `slot` was seen complete
+  bool ready = false;      // the full barrier of ring slot `slot` was seen complete
+  bool rdy_ready = false;  // layer j's ready barrier was seen complete
   for (int j = 0; j < nj; ++j) {
-    const StreamJob J = Jn;
-    if (j + 1 < nj) Jn = load_job(c.jobs, j + 1);
-    const Span s = span_of(J, P, b, SG::UB);
     // Layer j's activations are readable, and (the dependency warp waited for
     // it before publishing layer j) the finishing warp has read layer j - 2's
     // partial sums, so partial buffer j & 1 is free. Every warp waits in every
     // layer, with or without units in it, so that no warp runs two layers
     // ahead of the dependency and finishing warps: each per-layer barrier
     // then has at most one phase of its parity in flight.
-    if (!wait_layer(rdy0, j, gd)) return;
-    if (XS && (xsel[j & 1] & kConsumersStage)) {
+    if (!rdy_ready && !wait_layer(rdy0, j, gd)) return;
+    rdy_ready = false;
+    const LayerRec L = rec[j & 1];
+    if (XS && (L.xsel & kConsumersStage)) {
       // a dependency was just acquired: the consumer warps stage the
       // activations together (the dependency warp's acquire happens before
       // the ready barrier this warp waited on)
-      uint16_t* xs_st = reinterpret_cast<uint16_t*>(xbase + (xsel[j & 1] & ~kConsumersStage));
-      stage_copy<GS, MP>(J.x, J.K, M, xs_st, tid, NW * 32);
+      uint16_t* xs_st = reinterpret_cast<uint16_t*>(xbase + (L.xsel & ~kConsumersStage));
+      stage_copy<GS, MP>(L.x, L.K, M, xs_st, tid, NW * 32);
       cp_async_wait_all();
       __syncwarp();  // bar.sync is warp-aligned: converge after the divergent loop
       named_bar_sync(kConsumerBarrier, NW * 32);
-      stage_sums<GS, MP, 2>(J.K, M, xs_st, reinterpret_cast<float*>(xs_st + stream_xsum_off(J.K, M) / 2), tid, NW * 32);
+      stage_sums<GS, MP, 2>(L.K, M, xs_st, reinterpret_cast<float*>(xs_st + stream_xsum_off(L.K, M) / 2), tid, NW * 32);
       __syncwarp();
       named_bar_sync(kConsumerBarrier, NW * 32);
     }
+    Span s;
+    s.T = L.T;
+    s.NU = L.NU;
     if (s.T > 0) {
       const int R = (s.T + CU - 1) / CU;
       const uint16_t* xl0;
       const uint16_t* xl1;
-      const uint16_t* xs = reinterpret_cast<const uint16_t*>(xbase + (XS ? (xsel[j & 1] & ~kConsumersStage) : 0));
-      const float* xsum = reinterpret_cast<const float*>(xs + stream_xsum_off(J.K, M) / 2);
+      const uint16_t* xs = reinterpret_cast<const uint16_t*>(xbase + (XS ? (L.xsel & ~kConsumersStage) : 0));
+      const float* xsum = reinterpret_cast<const float*>(xs + stream_xsum_off(L.K, M) / 2);
       if (XS) {
-        const int64_t stride = stream_x_stride(J.K, M);
+        const int64_t stride = stream_x_stride(L.K, M);
         xl0 = xs + tok0 * stride + 4 * t;
         xl1 = xs + tok1 * stride + 4 * t;
       } else {
-        xl0 = J.x + size_t(tok0) * J.K + 4 * t;
-        xl1 = J.x + size_t(tok1) * J.K + 4 * t;
+        xl0 = L.x + size_t(tok0) * L.K + 4 * t;
+        xl1 = L.x + size_t(tok1) * L.K + 4 * t;
       }
       float* pb = part + size_t(j & 1) * RGMAX * NW * 32 * MP;
       float tot[kTilesPerWarp][NB][4];
@@ -679,6 +705,8 @@ __global__ void __launch_bounds__(kStreamThreads, 1) decode_stream_kernel(const 
           const int ns = slot + 1 == S ? 0 : slot + 1;
           ready = mbar_test_wait(full0 + 8 * ns, ns == 0 ? phase ^ 1u : phase);
         }
+        // in the layer's last slot, the next layer's ready barrier likewise
+        if (k == R - 1 && j + 1 < nj) rdy_ready = mbar_test_wait(rdy0 + 8 * ((j + 1) & 1), uint32_t((j + 1) >> 1) & 1u);
         const unsigned char* sb = smem + size_t(slot) * SG::kSlot;
         if (k * CU + (warp + 1) * SG::UPW <= s.T && ku0 + SG::UPW <= s.NU) {
           // common case: all of the warp's units exist and lie in one row

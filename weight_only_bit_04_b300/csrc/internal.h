@@ -87,8 +87,9 @@ cudaError_t launch_gptq(const Layout& L, const uint16_t* w, const uint16_t* x, i
 // (decode_stream.cuh): one persistent launch over a table of layer slices.
 // A slice is a run of row groups (32 rows) of one layer; thread block b owns
 // a contiguous share of every slice's row groups (positions rotated by `rot`)
-// and waits on the completion counters of the slices [wait_lo, wait_hi]
-// before it reads the slice's activations.
+// and, before it reads the slice's activations, waits until every block has
+// counted slice wait_hi: blocks finish slices in table order, so that covers
+// the whole range [wait_lo, wait_hi].
 struct StreamJob {
   const uint16_t* x;        // fp16 [M][K]
   uint16_t* y;              // fp16 [M][N]
@@ -100,7 +101,9 @@ struct StreamJob {
   int wait_lo, wait_hi;     // slices to wait for (none when wait_lo > wait_hi)
   int map;                  // index of the layer's first tensor map (the codes as boxes of
                             // CU, CU/2, ..., 1 units, CU = units per ring slot, at most 32)
-  int pad[2];
+  int signal;               // 1: a later slice waits for this one as the last of its range,
+                            // so every block counts it as done (fenced); 0: not counted
+  int pad;
 };
 static_assert(sizeof(StreamJob) == 80, "the layer table is read as 16-byte vectors");
 struct StreamLaunch {
