@@ -4,22 +4,36 @@
 Default workload (one step): the Llama-2-7B-shaped decode sweep at batch 1 --
 32 layers x 7 linear layers (q, k, v, o 4096x4096; gate, up 11008x4096; down
 4096x11008), each with its own seeded weights (N(0, 0.02), round-to-nearest
-asymmetric uint4, group 128): 224 GEMV launches streaming 3.37 GB of packed
-weights, far more than the 126 MB L2, so every step reads cold weights from
-HBM. The launches of one step are captured in a CUDA graph through the
-library's public API and replayed once per step.
+asymmetric uint4, group 128): 224 GEMVs streaming 3.37 GB of packed weights,
+far more than the 126 MB L2, so every step reads cold weights from HBM. The
+headline schedule streams the whole sweep in one persistent launch of the
+library's chained decode product (w4a16_chain_*); every GEMV reads its own
+precomputed synthetic activations, so no GEMV waits for another. The same
+launch with a decoder's data dependencies (q, k, v after the previous
+layer's down; o after q..v; gate, up after o; down after gate and up) and
+the per-launch schedules are reported beside it. The launch is captured in a
+CUDA graph through the public API and replayed once per step.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
-                    [--workload llama2-7b|llama70b|sweep8192]
+                    [--workload llama2-7b|llama70b|sweep8192] [--schedule S]
+    python bench.py --profile-case gemv|gemm|stream --case N K M [--calls C]
+                    [--layers L] [--act] [--bits B]
 
 Prints one JSON line (rank 0). `value` is GEMV throughput in algorithmic GB/s
-(packed codes + fp16 scales + 4-bit zeros + activations + outputs per launch)
+(packed codes + fp16 scales + 4-bit zeros + activations + outputs per GEMV)
 summed over the ranks; with N > 1 every rank runs an independent replica
-(weak scaling: the path has no cross-GPU exchange). Alongside: each distinct
-layer shape timed on its own, and the prefill GEMM (M = 2048, GPTQ act order)
-on the tensor cores with an fp16 cuBLAS GEMM on the same shapes for reference.
+(weak scaling: the path has no cross-GPU exchange). Extra keys carry the other
+workloads: the single 256x512 linear (microseconds per call), the 8192x8192
+batch sweep with its group-size and symmetric variants, the Llama-70B-shaped
+weight stream, and the prefill GEMM (M = 2048, GPTQ act order) on the tensor
+cores with an fp16 cuBLAS GEMM on the same shapes for reference.
 `--impl reference` times the CPU oracle (NumPy fp64 dequantize-then-matmul)
 on a bounded sample of the same workload.
+
+`--profile-case` makes a few calls of one entry point on one seeded layer (or,
+for `stream`, one chained launch over L copies of it) and exits 0 when the
+device reports no pipeline timeout: a small, fixed command for a profiler
+that skips the first calls (-s) and captures the next few (-c).
 """
 
 from __future__ import annotations
@@ -42,6 +56,8 @@ METRIC = "W4A16 GEMV achieved HBM GB/s (% of 8 TB/s) at batch 1; GEMM TFLOP/s"
 NOMINAL_HBM_GBPS = 8000.0
 WORKLOAD_7B = ("llama2-7b decode sweep, batch 1: 32 layers x (q,k,v,o 4096x4096; gate,up 11008x4096; "
                "down 4096x11008), 224 GEMVs per step")
+WORKLOAD_70B = ("llama-70b decode weight stream, batch 1: 80 layers x (q,o 8192x8192; k,v 1024x8192; "
+                "gate,up 28672x8192; down 8192x28672), 560 GEMVs per step, all weights resident")
 # Fallback peaks (one earlier B300 measurement) when the measured file is absent.
 FALLBACK_HBM_GBPS = 6400.0
 FALLBACK_BF16_TFLOPS = 1800.0
@@ -49,8 +65,10 @@ FALLBACK_BF16_TFLOPS = 1800.0
 # the headline kernel of each schedule on the Llama-2-7B sweep (4-bit codes),
 # {schedule: {"source_sha1", "bytes_per_launch"}}; valid only for the kernel
 # sources it was taken on (GEMV_SOURCES).
-GEMV_TRAFFIC = {"grouped": {"source_sha1": "18c6cb450ce2b06244d9e937beb86d3d63078d63", "bytes_per_launch": 26322272}}
+GEMV_TRAFFIC = {}
 SCHEDULE_TEXT = {
+    "stream": ("stream: the step is one persistent launch of the chained decode product (decode_stream_kernel); "
+               "each GEMV reads its own precomputed activations, so none waits for another"),
     "chain": ("chain: the step is one persistent launch; q, k, v wait for the previous layer's down, o for "
               "q..v, gate and up for o, down for gate and up (device completion counters)"),
     "decode": ("decode: one launch per GEMV; k, v and up do not wait for the GEMV before them (same input); "
@@ -59,6 +77,9 @@ SCHEDULE_TEXT = {
                 "down alone: 4 launches per layer, each waiting for the one before (programmatic dependent launch)"),
 }
 GEMV_SOURCES = ("gemv_impl.cuh", "k_gemv.cu", "k_gemv_b4.cu")
+STREAM_SOURCES = ("decode_stream.cuh", "stream_geom.h", "gemv_impl.cuh", "chain.cu", "k_gemv_b4.cu")
+SCHEDULES = ("stream", "chain", "grouped", "decode", "dependent", "independent")
+NOMINAL_FP16_TFLOPS = 2250.0
 L2_FLUSH_BYTES = 256 << 20
 
 
@@ -73,8 +94,16 @@ def parse_args():
     p.add_argument("--no-shapes", action="store_true")
     p.add_argument("--no-gptq", action="store_true")
     p.add_argument("--bits", type=int, default=4, choices=[3, 4, 8], help="code width of every packed linear")
-    p.add_argument("--schedule", default="grouped", choices=["chain", "grouped", "decode"],
-                   help="headline schedule: one chained launch per step, grouped launches, or one launch per GEMV")
+    p.add_argument("--schedule", default="stream", choices=list(SCHEDULES),
+                   help="headline schedule: one persistent launch per step (without or with the decoder's "
+                        "dependencies), grouped launches, or one launch per GEMV")
+    p.add_argument("--no-extra", action="store_true",
+                   help="skip the other workloads (single linear, 8192x8192 sweep, 70B stream)")
+    p.add_argument("--profile-case", choices=["gemv", "gemm", "stream"], default=None)
+    p.add_argument("--case", type=int, nargs=3, metavar=("N", "K", "M"), default=(4096, 4096, 1))
+    p.add_argument("--calls", type=int, default=3)
+    p.add_argument("--layers", type=int, default=8, help="--profile-case stream: copies of the layer")
+    p.add_argument("--act", action="store_true", help="--profile-case gemm: GPTQ act order")
     return p.parse_args()
 
 
@@ -116,52 +145,128 @@ def source_sha1(names) -> str:
     return h.hexdigest()
 
 
+class _Nvml:
+    """The few NVML queries the clock sampler needs, through the nvidia-ml-py
+    module when it is installed, else straight from the driver's
+    libnvidia-ml.so.1 with ctypes."""
+
+    CLOCK_SM = 1  # NVML_CLOCK_SM
+
+    def __init__(self):
+        import ctypes
+        self.ct = ctypes
+        self.py = None
+        try:
+            import pynvml
+            pynvml.nvmlInit()
+            self.py = pynvml
+            return
+        except ImportError:
+            pass
+        self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if self.lib.nvmlInit_v2() != 0:
+            raise RuntimeError("nvmlInit_v2 failed")
+        self._reasons = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            self.lib.nvmlDeviceGetCurrentClocksThrottleReasons
+
+    def handle(self, uuid, index):
+        if self.py is not None:
+            try:
+                return self.py.nvmlDeviceGetHandleByUUID(uuid)
+            except Exception:
+                return self.py.nvmlDeviceGetHandleByIndex(index)
+        h = self.ct.c_void_p()
+        if uuid is None or self.lib.nvmlDeviceGetHandleByUUID(self.ct.c_char_p(uuid.encode()), self.ct.byref(h)) != 0:
+            if self.lib.nvmlDeviceGetHandleByIndex_v2(self.ct.c_uint(index), self.ct.byref(h)) != 0:
+                raise RuntimeError("no NVML handle")
+        return h
+
+    def clock(self, h, maximum=False):
+        if self.py is not None:
+            fn = self.py.nvmlDeviceGetMaxClockInfo if maximum else self.py.nvmlDeviceGetClockInfo
+            return float(fn(h, self.py.NVML_CLOCK_SM))
+        v = self.ct.c_uint()
+        fn = self.lib.nvmlDeviceGetMaxClockInfo if maximum else self.lib.nvmlDeviceGetClockInfo
+        if fn(h, self.ct.c_int(self.CLOCK_SM), self.ct.byref(v)) != 0:
+            raise RuntimeError("clock query failed")
+        return float(v.value)
+
+    def reasons(self, h):
+        if self.py is not None:
+            fn = getattr(self.py, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                self.py.nvmlDeviceGetCurrentClocksThrottleReasons
+            return int(fn(h))
+        v = self.ct.c_ulonglong()
+        if self._reasons(h, self.ct.byref(v)) != 0:
+            raise RuntimeError("reasons query failed")
+        return int(v.value)
+
+
 class ClockSampler:
-    """Samples SM clocks and throttle reasons with nvidia-smi while running."""
+    """Samples the SM clock and the clock-event (throttle) reasons of one GPU
+    every `period` seconds on a host thread (NVML), from __enter__ to
+    __exit__; `summary()` keeps the samples taken while `timed` was set."""
 
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = (("hw_slowdown", 0x8), ("hw_thermal_slowdown", 0x40), ("sw_thermal_slowdown", 0x20),
+               ("sw_power_cap", 0x4), ("hw_power_brake", 0x80))
 
-    def __init__(self, index: int):
-        self.index = index
-        self.proc = None
-        self.samples = []
+    def __init__(self, torch, device, period=0.0005):
+        import threading
+        self.period = period
+        self.samples = []  # (timed, sm_mhz, reasons bitmask)
+        self.max_mhz = None
+        self.timed = False
+        self.error = None
+        self._stop = threading.Event()
+        self._thread = None
+        self._nvml = None
+        self._handle = None
+        try:
+            if torch is None:
+                raise RuntimeError("no device")
+            self._nvml = _Nvml()
+            uuid = str(torch.cuda.get_device_properties(device).uuid)
+            uuid = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+            self._handle = self._nvml.handle(uuid, device.index or 0)
+            self.max_mhz = self._nvml.clock(self._handle, maximum=True)
+        except Exception as e:  # reported in the summary
+            self.error = f"NVML unavailable: {type(e).__name__}: {e}"
+            self._handle = None
+
+    def _run(self):
+        nv, h = self._nvml, self._handle
+        while not self._stop.is_set():
+            try:
+                mhz = nv.clock(h)
+                reasons = nv.reasons(h)
+                self.samples.append((self.timed, mhz, reasons))
+            except Exception as e:
+                self.error = f"NVML query failed: {type(e).__name__}"
+                return
+            time.sleep(self.period)
 
     def __enter__(self):
-        try:
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
-                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-        except Exception:
-            self.proc = None
+        import threading
+        if self._handle is not None:
+            self._thread = threading.Thread(target=self._run, daemon=True)
+            self._thread.start()
         return self
 
     def __exit__(self, *exc):
-        if self.proc is None:
-            return False
-        self.proc.terminate()
-        try:
-            out, _ = self.proc.communicate(timeout=5)
-        except Exception:
-            self.proc.kill()
-            out = ""
-        for line in out.splitlines():
-            parts = [p.strip() for p in line.split(",")]
-            if len(parts) >= 9:
-                self.samples.append(parts)
+        self._stop.set()
+        if self._thread is not None:
+            self._thread.join(timeout=5)
         return False
 
     def summary(self):
-        if not self.samples:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
-        sm = [float(s[1]) for s in self.samples if s[1].replace(".", "").isdigit()]
-        mx = [float(s[2]) for s in self.samples if s[2].replace(".", "").isdigit()]
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for s in self.samples for i in range(4) if s[5 + i] == "Active"})
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
-                "reasons": reasons, "samples": len(self.samples)}
+        timed = [(m, r) for t, m, r in self.samples if t]
+        if not timed:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": ["unsampled"],
+                    "error": self.error or "no sample fell inside the timed region"}
+        reasons = sorted({name for _, r in timed for name, bit in self.REASONS if r & bit})
+        return {"sm_mhz": statistics.median(m for m, _ in timed), "sm_max_mhz": self.max_mhz,
+                "reasons": reasons, "samples": len(timed), "min_mhz": min(m for m, _ in timed),
+                "source": f"NVML every {self.period * 1e3:g} ms during the timed region"}
 
 
 # ---------------------------------------------------------------------------
@@ -260,42 +365,132 @@ def run_ours(args, rank, world, local_rank):
         return
 
     layers, xs, ys, yall = build_stack(torch, W, synth, dev, args.workload, args.bits)
-    n_launch = sum(len(l) for l in layers)
-    step_bytes = sum(gemv_bytes(fmt.N, fmt.K, bits=fmt.bits) for lins in layers for _, fmt, _ in lins)
+    step = time_stack(torch, W, dev, layers, xs, ys, yall, args, dist, world, local_rank)
+    shapes = None if args.no_shapes else per_shape(torch, W, layers, xs, dev)
+    del layers, xs, ys, yall
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    gemm = None
+    if not args.no_gemm and args.workload == "llama2-7b":
+        gemm = run_gemm(torch, W, synth, dev, args)
+    gptq = None
+    if not args.no_gptq and args.workload == "llama2-7b" and args.bits == 4:
+        gptq = run_gptq(torch, W, synth, dev)
+    extra = {}
+    if not args.no_extra and args.workload == "llama2-7b" and args.bits == 4:
+        extra["single_linear_256x512"] = run_single_linear(torch, W, synth, dev)
+        extra["sweep_8192x8192"] = sweep8192_rows(torch, W, synth, dev, variants=True)
+        torch.cuda.empty_cache()
+        extra["llama70b_stream"] = run_70b(torch, W, synth, dev, args, dist, world, local_rank)
+        torch.cuda.empty_cache()
 
-    # Dependency schedules of the sweep. "decode": the launches that read the
-    # same activations as the one before (k and v after q, up after gate) do
-    # not wait for it -- the independence of a real decoder layer; every
-    # other GEMV waits for its predecessor (programmatic dependent launch,
-    # weights streamed early). "dependent": every GEMV waits. "independent":
-    # none waits (all activations of this workload are precomputed).
-    same_input = {"k", "v", "up"}
+    if rank == 0:
+        hbm, bf16, peak_kind = measured_peaks()
+        ms = step["ms"]
+        launches = {"stream": 1, "chain": 1, "grouped": 4 * step["n_layers"]}.get(args.schedule, step["n_launch"])
+        traffic = None
+        ref = GEMV_TRAFFIC.get(args.schedule)
+        srcs = STREAM_SOURCES if args.schedule in ("stream", "chain") else GEMV_SOURCES
+        if args.bits == 4 and ref and ref["source_sha1"] == source_sha1(srcs):
+            traffic = ref["bytes_per_launch"]
+        step_bytes = step["step_bytes"]
+        per_rank = step_bytes / (ms * 1e-3) / 1e9
+        if args.workload == "llama70b":
+            workload = WORKLOAD_70B
+            frac = synth.LLAMA_70B_OUTLIER_FRAC
+        else:
+            workload = WORKLOAD_7B
+            frac = synth.LLAMA2_7B_OUTLIER_FRAC
+        kernel = {"stream": "decode_stream_kernel (one persistent launch per step, after a counter reset)",
+                  "chain": "decode_stream_kernel (one persistent launch per step, after a counter reset)",
+                  "grouped": "gemv_kernel (every launch of the step; q,k,v and gate,up grouped)"}.get(
+                      args.schedule, "gemv_kernel (every launch of the step)")
+        line = {
+            "metric": METRIC if args.bits == 4 else METRIC.replace("W4A16", f"W{args.bits}A16"),
+            "value": round(step["value"], 1),
+            "unit": "GB/s",
+            "n_gpus": world,
+            "steps": args.steps,
+            "warmup": args.warmup,
+            "ms_per_step": round(ms, 4),
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "fp16",
+            "precision": f"fp16 activations x uint{args.bits} weights (fp16 scales), fp32 accumulate",
+            "data": (f"synthetic: seeded N(0,0.02) weights RTN-quantized on the GPU, N(0,1) fp16 activations "
+                     f"with {100 * frac:g}% outlier channels x20"),
+            "config": {"workload": workload,
+                       "M": 1, "group_size": 128, "scheme": f"asymmetric uint{args.bits}, fp16 scales",
+                       "bytes_per_step": step_bytes, "gemvs_per_step": step["n_launch"],
+                       "l2": f"inputs larger than L2 ({step_bytes / 1e9:.2f} GB of packed weights per step vs 126 MB L2)",
+                       "timing": "CUDA graph replay per step, CUDA events on the launching stream",
+                       "schedule": SCHEDULE_TEXT[args.schedule],
+                       "parallelism": f"replicas x{world}"},
+            "pct_of_nominal_hbm": round(100 * per_rank / NOMINAL_HBM_GBPS, 1),
+            "roofline": {"bound": "hbm", "achieved": round(per_rank, 1), "peak": hbm, "unit": "GB/s",
+                         "frac": round(per_rank / hbm, 4), "traffic": traffic,
+                         "avg_launch_us": round(ms * 1e3 / launches, 3),
+                         "alg_bytes_per_launch": round(step_bytes / launches),
+                         "peak_source": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)",
+                         "kernel": kernel},
+            "e2e": step["e2e"],
+            "gpu_launches": launches * args.steps,
+            "clocks": step["clocks"],
+            "decode_step_with_dependencies": step["schedules"].get("chain"),
+            "schedules": step["schedules"],
+            "per_shape": shapes,
+            "gemm": gemm,
+            "gptq": gptq,
+        }
+        line.update(extra)
+        line["cpu_baseline"] = cpu_baseline(world)
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
 
-    # "chain": the whole step as one persistent launch (w4a16_chain_*) with
-    # the data dependencies of a decoder layer: q, k, v read the previous
-    # layer's down output; o waits for q..v; gate and up wait for o; down
-    # waits for gate and up. Strictly more waits than "decode".
+
+def chain_of(W, layers, xs, ys, deps):
+    """The step as one chained launch: without waits, or with a decoder's
+    data dependencies (q, k, v after the previous layer's down; o after q..v;
+    gate, up after o; down after gate and up)."""
     chain_layers = []
     for li, lins in enumerate(layers):
         base = li * len(lins)
-        names = [n for n, _, _ in lins]
-        idx = {n: base + j for j, n in enumerate(names)}
+        idx = {n: base + j for j, (n, _, _) in enumerate(lins)}
         for j, (name, fmt, packed) in enumerate(lins):
-            if name in ("q", "k", "v"):
-                wait = None if li == 0 else (base - 1, base - 1)
-            elif name == "o":
-                wait = (idx["q"], idx["v"])
-            elif name in ("gate", "up"):
-                wait = (idx["o"], idx["o"])
-            else:
-                wait = (idx["gate"], idx["up"])
+            wait = None
+            if deps:
+                if name in ("q", "k", "v"):
+                    wait = None if li == 0 else (base - 1, base - 1)
+                elif name == "o":
+                    wait = (idx["q"], idx["v"])
+                elif name in ("gate", "up"):
+                    wait = (idx["o"], idx["o"])
+                else:
+                    wait = (idx["gate"], idx["up"])
             chain_layers.append((fmt, packed, xs[fmt.K], ys[li][j], wait))
-    chain = W.Chain(chain_layers, 1)
+    return W.Chain(chain_layers, 1)
+
+
+def time_stack(torch, W, dev, layers, xs, ys, yall, args, dist, world, local_rank, schedules=SCHEDULES, e2e=True):
+    """Every schedule of the sweep captured in a graph; the headline one timed
+    with exactly `steps` replays (barrier + synchronize on both sides, clocks
+    sampled), the others after it, and the end-to-end step."""
+    n_launch = sum(len(l) for l in layers)
+    step_bytes = sum(gemv_bytes(fmt.N, fmt.K, bits=fmt.bits) for lins in layers for _, fmt, _ in lins)
+    # Per-launch schedules. "decode": the launches that read the same
+    # activations as the one before (k and v after q, up after gate) do not
+    # wait for it; every other GEMV waits for its predecessor (programmatic
+    # dependent launch, weights streamed early). "dependent": every GEMV
+    # waits. "independent": none waits. "grouped": q,k,v and gate,up share
+    # launches, every launch waits for the one before.
+    same_input = {"k", "v", "up"}
+    chains = {"stream": chain_of(W, layers, xs, ys, False), "chain": chain_of(W, layers, xs, ys, True)}
 
     def sweep(schedule):
         for li, lins in enumerate(layers):
             if schedule == "grouped":
-                # the linears that read one input share a launch; every launch waits for the one before
                 by = {name: (j, fmt, packed) for j, (name, fmt, packed) in enumerate(lins)}
                 for group in (("q", "k", "v"), ("o",), ("gate", "up"), ("down",)):
                     sel = [by[n] for n in group if n in by]
@@ -312,8 +507,8 @@ def run_ours(args, rank, world, local_rank):
 
     stream = torch.cuda.Stream(device=dev)
     graphs = {}
-    for schedule in ("chain", "grouped", "decode", "dependent", "independent"):
-        run = (lambda: chain.run(stream)) if schedule == "chain" else (lambda s=schedule: sweep(s))
+    for schedule in schedules:
+        run = (lambda c=chains[schedule]: c.run(stream)) if schedule in chains else (lambda s=schedule: sweep(s))
         with torch.cuda.stream(stream):
             run()
         torch.cuda.synchronize()
@@ -322,125 +517,106 @@ def run_ours(args, rank, world, local_rank):
             run()
         torch.cuda.synchronize()
         graphs[schedule] = g
-    graph = graphs[args.schedule]
+    head = args.schedule if args.schedule in graphs else schedules[0]
+    graph = graphs[head]
 
-    # Warm-up, then exactly `steps` timed replays, barrier + synchronize on both sides.
-    for _ in range(args.warmup):
-        graph.replay()
-    torch.cuda.synchronize()
-    if dist:
-        dist.barrier()
-    with ClockSampler(local_rank) as clk:
+    # Warm-up, then exactly `steps` timed replays, barrier + synchronize on
+    # both sides; clocks sampled from before the warm-up, kept for the timed region.
+    with ClockSampler(torch, dev) as clk:
+        for _ in range(args.warmup):
+            graph.replay()
+        torch.cuda.synchronize()
+        if dist:
+            dist.barrier()
+        clk.timed = True
         ms = time_graph(torch, graph, stream, args.steps)
+        clk.timed = False
     if dist:
         dist.barrier()
     ms = max_over_ranks(torch, dist, ms, dev)
     value = world * step_bytes / (ms * 1e-3) / 1e9
-    schedules = {}
-    for schedule in [s for s in ("chain", "grouped", "decode", "dependent", "independent") if s != args.schedule]:
+    results = {head: {"ms_per_step": round(ms, 4), "GB/s": round(step_bytes / (ms * 1e-3) / 1e9, 1)}}
+    # The other schedules, each after 30 warm-up replays and over at least 100
+    # (the waiting schedules take about 30 replays to settle after another one).
+    for schedule in schedules:
+        if schedule == head:
+            continue
         g = graphs[schedule]
-        for _ in range(args.warmup):
+        for _ in range(max(args.warmup, 30)):
             g.replay()
-        sms = time_graph(torch, g, stream, args.steps)
-        schedules[schedule] = {"ms_per_step": round(sms, 4), "GB/s": round(step_bytes / (sms * 1e-3) / 1e9, 1)}
-    schedules[args.schedule] = {"ms_per_step": round(ms, 4), "GB/s": round(step_bytes / (ms * 1e-3) / 1e9, 1)}
+        sms = time_graph(torch, g, stream, max(args.steps, 100))
+        results[schedule] = {"ms_per_step": round(sms, 4), "GB/s": round(step_bytes / (sms * 1e-3) / 1e9, 1)}
+    for name in chains:
+        if name in results:
+            results[name]["launches_per_step"] = 1
     if W.pipeline_timeouts() != 0:
-        raise RuntimeError("a chained launch gave up a dependency wait")
+        raise RuntimeError("a chained launch gave up a bounded wait: its outputs are undefined")
 
-    # End to end through the public API with host buffers: pinned inputs copied
-    # in, the step, every output copied back, all inside the timed region.
-    x_host = {K: x.cpu().pin_memory() for K, x in xs.items()}
-    y_host = torch.empty(yall.shape, dtype=yall.dtype).pin_memory()
-    h2d = sum(x.numel() * x.element_size() for x in x_host.values())
-    d2h = y_host.numel() * y_host.element_size()
+    e2e_rec = None
+    if e2e:
+        # End to end through the public API with host buffers: pinned inputs
+        # copied in, the step, every output copied back, all inside the timed region.
+        x_host = {K: x.cpu().pin_memory() for K, x in xs.items()}
+        y_host = torch.empty(yall.shape, dtype=yall.dtype).pin_memory()
+        h2d = sum(x.numel() * x.element_size() for x in x_host.values())
+        d2h = y_host.numel() * y_host.element_size()
 
-    def e2e_step():
-        with torch.cuda.stream(stream):
-            for K, x in xs.items():
-                x.copy_(x_host[K], non_blocking=True)
-            graph.replay()
-            y_host.copy_(yall, non_blocking=True)
-        stream.synchronize()
+        def e2e_step():
+            with torch.cuda.stream(stream):
+                for K, x in xs.items():
+                    x.copy_(x_host[K], non_blocking=True)
+                graph.replay()
+                y_host.copy_(yall, non_blocking=True)
+            stream.synchronize()
 
-    for _ in range(args.warmup):
-        e2e_step()
-    if dist:
-        dist.barrier()
-    t0 = time.perf_counter()
-    for _ in range(args.steps):
-        e2e_step()
-    e2e_ms = (time.perf_counter() - t0) * 1e3 / args.steps
-    e2e_ms = max_over_ranks(torch, dist, e2e_ms, dev)
-    e2e_value = world * step_bytes / (e2e_ms * 1e-3) / 1e9
+        for _ in range(args.warmup):
+            e2e_step()
+        if dist:
+            dist.barrier()
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            e2e_step()
+        e2e_ms = (time.perf_counter() - t0) * 1e3 / args.steps
+        e2e_ms = max_over_ranks(torch, dist, e2e_ms, dev)
+        e2e_rec = {"value": round(world * step_bytes / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+                   "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)}
+    del graph, graphs, chains
+    return {"ms": ms, "value": value, "step_bytes": step_bytes, "n_launch": n_launch, "n_layers": len(layers),
+            "schedules": results, "clocks": clk.summary(), "e2e": e2e_rec}
 
-    shapes = None if args.no_shapes else per_shape(torch, W, layers, xs, dev)
-    del graph, graphs
-    gemm = None
-    if not args.no_gemm and args.workload == "llama2-7b":
-        gemm = run_gemm(torch, W, synth, dev, args)
-    gptq = None
-    if not args.no_gptq and args.workload == "llama2-7b" and args.bits == 4:
-        gptq = run_gptq(torch, W, synth, dev)
 
-    if rank == 0:
-        hbm, bf16, peak_kind = measured_peaks()
-        launches = {"chain": 1, "grouped": 4 * len(layers)}.get(args.schedule, n_launch)
-        traffic = None
-        ref = GEMV_TRAFFIC.get(args.schedule)
-        if args.bits == 4 and ref and ref["source_sha1"] == source_sha1(GEMV_SOURCES):
-            traffic = ref["bytes_per_launch"]
-        per_rank = step_bytes / (ms * 1e-3) / 1e9
-        if args.workload == "llama70b":
-            workload = ("llama-70b decode weight stream, batch 1: 80 layers x (q,o 8192x8192; k,v 1024x8192; "
-                        "gate,up 28672x8192; down 8192x28672), 560 GEMVs per step, all weights resident")
-            frac = synth.LLAMA_70B_OUTLIER_FRAC
-        else:
-            workload = WORKLOAD_7B
-            frac = synth.LLAMA2_7B_OUTLIER_FRAC
-        line = {
-            "metric": METRIC if args.bits == 4 else METRIC.replace("W4A16", f"W{args.bits}A16"),
-            "value": round(value, 1),
-            "unit": "GB/s",
-            "n_gpus": world,
-            "steps": args.steps,
-            "warmup": args.warmup,
-            "ms_per_step": round(ms, 4),
-            "higher_is_better": True,
-            "scaling": "weak",
-            "vs_baseline": None,
-            "dtype": "fp16",
-            "precision": f"fp16 activations x uint{args.bits} weights (fp16 scales), fp32 accumulate",
-            "data": (f"synthetic: seeded N(0,0.02) weights RTN-quantized on the GPU, N(0,1) fp16 activations "
-                     f"with {100 * frac:g}% outlier channels x20"),
-            "config": {"workload": workload,
-                       "M": 1, "group_size": 128, "scheme": f"asymmetric uint{args.bits}, fp16 scales",
-                       "bytes_per_step": step_bytes, "launches_per_step": n_launch,
-                       "l2": f"inputs larger than L2 ({step_bytes / 1e9:.2f} GB of packed weights per step vs 126 MB L2)",
-                       "timing": "CUDA graph replay per step, CUDA events on the launching stream",
-                       "schedule": SCHEDULE_TEXT[args.schedule],
-                       "parallelism": f"replicas x{world}"},
-            "pct_of_nominal_hbm": round(100 * per_rank / NOMINAL_HBM_GBPS, 1),
-            "roofline": {"bound": "hbm", "achieved": round(per_rank, 1), "peak": hbm, "unit": "GB/s",
-                         "frac": round(per_rank / hbm, 4), "traffic": traffic,
-                         "avg_launch_us": round(ms * 1e3 / launches, 3),
-                         "alg_bytes_per_launch": round(step_bytes / launches),
-                         "peak_source": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)",
-                         "kernel": {"chain": "gemv_chain_kernel (one launch per step, after a counter reset)",
-                                    "grouped": "gemv_kernel (every launch of the step; q,k,v and gate,up grouped)"}.get(
-                                        args.schedule, "gemv_kernel (every launch of the step)")},
-            "e2e": {"value": round(e2e_value, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)},
-            "gpu_launches": launches * args.steps,
-            "clocks": clk.summary(),
-            "schedules": schedules,
-            "per_shape": shapes,
-            "gemm": gemm,
-            "gptq": gptq,
-        }
-        line["cpu_baseline"] = cpu_baseline(world)
-        print(json.dumps(line), flush=True)
-    if dist:
-        dist.destroy_process_group()
+def run_70b(torch, W, synth, dev, args, dist, world, local_rank):
+    """The Llama-70B-shaped weight stream at batch 1 (80 layers, ~37 GB
+    packed, resident): the step as one chained launch, without and with the
+    decoder's dependencies."""
+    layers, xs, ys, yall = build_stack(torch, W, synth, dev, "llama70b", 4)
+    step = time_stack(torch, W, dev, layers, xs, ys, yall, args, dist, world, local_rank,
+                      schedules=("stream", "chain"), e2e=False)
+    del layers, xs, ys, yall
+    rec = {"workload": WORKLOAD_70B, "us_per_step": round(step["ms"] * 1e3, 1), "GB/s": round(step["value"], 1),
+           "bytes_per_step": step["step_bytes"], "schedules": step["schedules"], "clocks": step["clocks"],
+           "schedule": SCHEDULE_TEXT["stream"]}
+    c = step["schedules"].get("chain")
+    if c:
+        rec["with_dependencies"] = {"us_per_step": round(c["ms_per_step"] * 1e3, 1), "GB/s": c["GB/s"]}
+    return rec
+
+
+def run_single_linear(torch, W, synth, dev):
+    """The single 256x512 linear at batch 1 (asymmetric uint4, group 128):
+    microseconds per w4a16_gemv call, L2 flushed before each call."""
+    N, K = 256, 512
+    fmt = W.make_format(N, K, 128, False, False)
+    w = synth.weights_cuda(N, K, synth.seed_for("single", "w"), device=dev)
+    q, s, z = W.quantize_rtn(fmt, w)
+    packed = W.pack(fmt, q, s, z)
+    x = synth.activations_cuda(1, K, 0.01, synth.seed_for("single", "x"), device=dev)
+    y = torch.empty((1, N), dtype=torch.float16, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    ms = timed_calls(torch, lambda: W.gemv(fmt, packed, x, out=y), 50, flush)
+    return {"shape": f"{N}x{K}", "M": 1, "us": round(ms * 1e3, 2),
+            "GB/s": round(gemv_bytes(N, K) / (ms * 1e-3) / 1e9, 1),
+            "timing": "median of 50 calls, CUDA events, L2 flushed before each (launch latency dominates)"}
 
 
 def timed_calls(torch, fn, reps, flush):
@@ -492,6 +668,8 @@ def run_gemm(torch, W, synth, dev, args):
     _, bf16, kind = measured_peaks()
     tf = total_flop / total_ms / 1e9
     res.update({"tflops": round(tf, 1), "unit": "TFLOP/s", "M": M, "act_order": True,
+                "pct_of_nominal_fp16": round(100 * tf / NOMINAL_FP16_TFLOPS, 1),
+                "nominal_fp16_tflops": NOMINAL_FP16_TFLOPS,
                 "includes": "act-order activation gather kernel + tcgen05 GEMM kernel",
                 "l2": "flushed (256 MB write) before every timed call",
                 "cublas_fp16_tflops": round(total_flop / total_cublas / 1e9, 1),
@@ -499,8 +677,12 @@ def run_gemm(torch, W, synth, dev, args):
                              "frac": round(tf / bf16, 4),
                              "peak_source": f"{kind} cuBLAS bf16 burst (MEASURED_PEAKS.json bf16_tflops); "
                                             "fp16 and bf16 dense rates are equal"}})
-    if W.pipeline_timeouts() != 0:
-        res["pipeline_timeouts"] = "nonzero: some output tile was not written"
+    # A bounded wait that gave up leaves some output tile unwritten: the
+    # record is then not a valid measurement.
+    timeouts = W.pipeline_timeouts()
+    res["valid"] = timeouts == 0
+    if timeouts:
+        res["invalid"] = f"{timeouts} pipeline wait(s) gave up: outputs undefined, timings not valid"
     return res
 
 
@@ -532,53 +714,120 @@ def run_gptq(torch, W, synth, dev):
             "peak_source": "nominal B300 FP64 1.25 TFLOP/s (no measured fp64 peak)"}
 
 
-def run_sweep8192(torch, W, synth, dev, args, rank, world, dist):
-    """8192x8192 asym uint4 g128 weight: GEMV for M <= 16, GEMM for M >= 16."""
+def sweep8192_rows(torch, W, synth, dev, variants=False):
+    """8192x8192 uint4 weight, M in {1..128}: the GEMV for M <= 16 (16
+    distinct weight copies, 560 MB, so that launches read cold weights), the
+    GEMM for M >= 16 (L2 flushed before each call). With `variants`, also the
+    GEMV at M = 1 and 16 for group sizes 32 and 64 and for the symmetric
+    scheme (zero fixed at 8)."""
     N = K = 8192
-    copies = 16  # 16 distinct weight copies (560 MB) so that GEMV launches read cold weights
-    fmt = W.make_format(N, K, 128, False, False)
-    w = synth.weights_cuda(N, K, synth.seed_for("sweep8192", "w"), device=dev)
-    q, s, z = W.quantize_rtn(fmt, w)
-    p0 = W.pack(fmt, q, s, z)
-    packs = [p0] + [p0.clone() for _ in range(copies - 1)]
-    del w, q, s, z
+    copies = 16
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def packs_for(g, sym):
+        fmt = W.make_format(N, K, g, sym, False)
+        w = synth.weights_cuda(N, K, synth.seed_for("sweep8192", "w"), device=dev)
+        q, s, z = W.quantize_rtn(fmt, w)
+        p0 = W.pack(fmt, q, s, z)
+        del w, q, s, z
+        return fmt, [p0] + [p0.clone() for _ in range(copies - 1)]
+
+    def gemv_us(fmt, packs, x, y):
+        stream = torch.cuda.Stream(device=dev)
+        with torch.cuda.stream(stream):
+            for p in packs:
+                W.gemv(fmt, p, x, out=y, weights_ready=True)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for p in packs:
+                W.gemv(fmt, p, x, out=y, weights_ready=True)
+        for _ in range(3):
+            g.replay()
+        ms = time_graph(torch, g, stream, 20) / copies
+        del g
+        return ms
+
     rows = []
+    fmt, packs = packs_for(128, False)
     for M in synth.SWEEP_M:
         x = synth.activations_cuda(M, K, 0.01, synth.seed_for("sweep8192", "x", M), device=dev)
         y = torch.empty((M, N), dtype=torch.float16, device=dev)
         nbytes = gemv_bytes(N, K, M)
         flop = 2.0 * M * N * K
         if M <= 16:
-            stream = torch.cuda.Stream(device=dev)
-            with torch.cuda.stream(stream):
-                for p in packs:
-                    W.gemv(fmt, p, x, out=y, weights_ready=True)
-            torch.cuda.synchronize()
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g, stream=stream):
-                for p in packs:
-                    W.gemv(fmt, p, x, out=y, weights_ready=True)
-            for _ in range(3):
-                g.replay()
-            ms = time_graph(torch, g, stream, 20) / copies
-            rows.append({"M": M, "kernel": "gemv", "us": round(ms * 1e3, 2),
+            ms = gemv_us(fmt, packs, x, y)
+            rows.append({"M": M, "group_size": 128, "scheme": "asym", "kernel": "gemv", "us": round(ms * 1e3, 2),
                          "GB/s": round(nbytes / (ms * 1e-3) / 1e9, 1), "TFLOP/s": round(flop / ms / 1e9, 2)})
         if M >= 16:
             ms = timed_calls(torch, lambda: W.gemm(fmt, packs[0], x, out=y), 20, flush)
-            rows.append({"M": M, "kernel": "gemm", "us": round(ms * 1e3, 2),
+            rows.append({"M": M, "group_size": 128, "scheme": "asym", "kernel": "gemm", "us": round(ms * 1e3, 2),
                          "GB/s": round(nbytes / (ms * 1e-3) / 1e9, 1), "TFLOP/s": round(flop / ms / 1e9, 2)})
+    del packs
+    if variants:
+        for g, sym in ((32, False), (64, False), (128, True)):
+            fmt, packs = packs_for(g, sym)
+            for M in (1, 16):
+                x = synth.activations_cuda(M, K, 0.01, synth.seed_for("sweep8192", "x", M), device=dev)
+                y = torch.empty((M, N), dtype=torch.float16, device=dev)
+                nbytes = gemv_bytes(N, K, M, g=g, sym=sym)
+                ms = gemv_us(fmt, packs, x, y)
+                rows.append({"M": M, "group_size": g, "scheme": "sym" if sym else "asym", "kernel": "gemv",
+                             "us": round(ms * 1e3, 2), "GB/s": round(nbytes / (ms * 1e-3) / 1e9, 1),
+                             "TFLOP/s": round(2.0 * M * N * K / ms / 1e9, 2)})
+            del packs
+    if W.pipeline_timeouts() != 0:
+        raise RuntimeError("a GEMV or GEMM gave up a bounded wait: its outputs are undefined")
+    return {"shape": "8192x8192", "rows": rows,
+            "l2": "GEMV: 16 distinct weight copies (cold); GEMM: L2 flushed before each call"}
+
+
+def run_sweep8192(torch, W, synth, dev, args, rank, world, dist):
+    rec = sweep8192_rows(torch, W, synth, dev, variants=True)
     if rank == 0:
         hbm, bf16, kind = measured_peaks()
-        m1 = rows[0]
+        m1 = rec["rows"][0]
         print(json.dumps({
             "metric": METRIC, "value": m1["GB/s"], "unit": "GB/s", "n_gpus": world, "steps": 20, "warmup": 3,
             "ms_per_step": m1["us"] / 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "fp16", "precision": "fp16 activations x uint4 weights (fp16 scales), fp32 accumulate",
             "data": "synthetic",
             "config": {"workload": "8192x8192 batch sweep M in {1..128}, asym uint4 g128 (value: M = 1 GEMV)",
-                       "l2": "GEMV: 16 distinct weight copies (cold); GEMM: L2 flushed before each call"},
-            "rows": rows, "peaks": {"hbm_gbs": hbm, "bf16_tflops": bf16, "source": kind}}), flush=True)
+                       "l2": rec["l2"]},
+            "rows": rec["rows"], "peaks": {"hbm_gbs": hbm, "bf16_tflops": bf16, "source": kind}}), flush=True)
+
+
+def run_profile_case(args):
+    """A few calls of one entry point on one seeded layer (asymmetric, group
+    128), for a profiler; exit status 0 when no bounded wait gave up."""
+    import torch
+    from weight_only_bit_04_b300 import synth
+    from weight_only_bit_04_b300 import w4a16 as W
+    N, K, M = args.case
+    dev = torch.device("cuda", 0)
+    x = synth.activations_cuda(M, K, 0.01, synth.seed_for("profile", "x", M, K), device=dev)
+    gidx = synth.act_order_g_idx(x.float().cpu().numpy(), 128) if (args.act and args.profile_case == "gemm") else None
+    fmt = W.make_format(N, K, 128, False, gidx is not None, bits=args.bits)
+    q, s, z = W.quantize_rtn(fmt, synth.weights_cuda(N, K, synth.seed_for("profile", "w", N, K), device=dev), gidx)
+    packed = W.pack(fmt, q, s, z, gidx)
+    del q, s, z
+    if args.profile_case == "stream":
+        packs = [packed] + [packed.clone() for _ in range(args.layers - 1)]
+        ys = [torch.empty((M, N), dtype=torch.float16, device=dev) for _ in packs]
+        chain = W.Chain([(fmt, p, x, y, None) for p, y in zip(packs, ys)], M)
+        for _ in range(args.calls):
+            chain.run()
+    else:
+        y = torch.empty((M, N), dtype=torch.float16, device=dev)
+        for _ in range(args.calls):
+            if args.profile_case == "gemm":
+                W.gemm(fmt, packed, x, out=y)
+            else:
+                W.gemv(fmt, packed, x, out=y)
+    torch.cuda.synchronize()
+    n = W.pipeline_timeouts()
+    print(f"{args.profile_case} {N}x{K} M={M} bits={args.bits}: {args.calls} calls, pipeline timeouts {n}")
+    return 0 if n == 0 else 1
 
 
 # ---------------------------------------------------------------------------
@@ -668,6 +917,8 @@ def main():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     world = max(world, 1)
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.profile_case:
+        sys.exit(run_profile_case(args))
     if args.impl == "reference":
         run_reference(args, rank, world)
     else:

@@ -114,11 +114,10 @@ typedef struct {
  *            of 128 rows x 64 columns of b-bit codes (3, 4 or 8 KiB),
  *            arranged so that a warp's 16-byte (3 bits: 16- and 8-byte)
  *            loads yield tensor-core operand fragments.
- *   scales   NR*G*256 bytes: fp16 scales; for every 32-row group its 32
- *            rows' scales of all G groups are contiguous (64 bytes per group).
+ *   scales   NR*G*256 bytes: fp16 scales, 128 rows per (row block, group).
  *   zeros    (asymmetric only) NR*G*64 bytes of 4-bit zero points for 3- and
  *            4-bit codes, NR*G*128 bytes of 8-bit ones for 8-bit codes,
- *            arranged like the scales (16 or 32 bytes per 32 rows and group).
+ *            arranged like the scales.
  *   perm     K*4 bytes (act order only): packed column -> original column.
  *   act_scale K*2 bytes (has_act_scale only): fp16 s in packed column order.
  * Rows beyond N and columns beyond K are padding. The blob's meaning is fixed

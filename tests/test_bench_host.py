@@ -44,24 +44,28 @@ def test_measured_peaks_reads_the_file_or_falls_back(tmp_path, monkeypatch):
     assert bench.measured_peaks() == (6000.5, 1700.0, "measured")
 
 
-def sampler_with(rows):
-    s = bench.ClockSampler(0)
-    s.samples = [[p.strip() for p in r.split(",")] for r in rows]
+def sampler_with(samples, max_mhz=2032.0):
+    # no NVML here: the constructor records why and keeps no handle
+    s = bench.ClockSampler(None, None)
+    s.samples = list(samples)
+    s.max_mhz = max_mhz
     return s
 
 
 def test_clock_summary_median_max_and_reasons():
-    rows = [
-        "0, 2032, 2032, 650.1, 0x0, Not Active, Not Active, Not Active, Not Active",
-        "0, 1980, 2032, 900.0, 0x4, Not Active, Not Active, Not Active, Active",
-        "0, 2010, 2032, 880.2, 0x0, Not Active, Not Active, Not Active, Not Active",
-    ]
+    rows = [(True, 2032.0, 0x0), (True, 1980.0, 0x4), (True, 2010.0, 0x0),
+            (False, 900.0, 0x8)]  # outside the timed region: ignored
     s = sampler_with(rows).summary()
     assert s["sm_mhz"] == 2010.0 and s["sm_max_mhz"] == 2032.0 and s["samples"] == 3
-    assert s["reasons"] == ["sw_power_cap"]
-    hot = sampler_with(rows + ["0, 1500, 2032, 1000.0, 0x40, Not Active, Active, Not Active, Not Active"]).summary()
+    assert s["reasons"] == ["sw_power_cap"] and s["min_mhz"] == 1980.0
+    hot = sampler_with(rows + [(True, 1500.0, 0x40)]).summary()
     assert hot["reasons"] == ["hw_thermal_slowdown", "sw_power_cap"]
+    slow = sampler_with([(True, 2000.0, 0x8 | 0x20)]).summary()
+    assert slow["reasons"] == ["hw_slowdown", "sw_thermal_slowdown"]
 
 
 def test_clock_summary_without_samples():
-    assert bench.ClockSampler(0).summary() == {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+    s = bench.ClockSampler(None, None).summary()
+    assert s["sm_mhz"] is None and s["reasons"] == ["unsampled"] and s["error"]
+    outside = sampler_with([(False, 2032.0, 0)]).summary()
+    assert outside["reasons"] == ["unsampled"]

@@ -369,9 +369,10 @@ __global__ void __launch_bounds__(kStreamThreads, 1) decode_stream_kernel(const 
             ku -= NU;
             ++rg;
           }
-          // row group rg's scales: 64 contiguous bytes per group, groups back to back
+          // row group rg's scales of one group: 64 contiguous bytes (its
+          // two 16-row tiles in the row block's [group][16-row tile] order)
           const int gg = p >> 2;
-          const uint32_t* src = sc_base + (size_t(rg) * G + ku * SG::GU + gg) * 16 + (p & 3) * 4;
+          const uint32_t* src = sc_base + meta_index(rg >> 2, ku * SG::GU + gg, 2 * (rg & 3), 0, G) + (p & 3) * 4;
           cp_async_16_cg(sb + SG::kScaleOff + (d * SG::GU + gg) * 64 + (p & 3) * 16, src);
         }
         if (!SYM) {
@@ -383,7 +384,8 @@ __global__ void __launch_bounds__(kStreamThreads, 1) decode_stream_kernel(const 
               ++rg;
             }
             const int gg = p / (SG::ZB / 16), h = p - gg * (SG::ZB / 16);
-            const uint8_t* src = z_base + (size_t(rg) * G + ku * SG::GU + gg) * SG::ZB + h * 16;
+            const uint8_t* src =
+                z_base + meta_index(rg >> 2, ku * SG::GU + gg, 2 * (rg & 3), 0, G) * (SG::ZB / 16) + h * 16;
             cp_async_16_cg(sb + SG::kZeroOff + (d * SG::GU + gg) * SG::ZB + h * 16, src);
           }
         }

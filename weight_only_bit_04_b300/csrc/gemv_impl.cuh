@@ -281,8 +281,10 @@ __device__ __forceinline__ void load_unit(UnitRegs<GS, BITS>& r, const uint32_t*
     const int gi = GS == 32 ? min(unit * U::kGroups + gg, gmax) : unit * U::kGroups + gg;
 #pragma unroll
     for (int tt = 0; tt < kTilesPerWarp; ++tt) {
-      r.s[gg][tt] = ldg_nc_u32(sp + gi * 16 + tt * 8);
-      r.z[gg][tt] = SYM ? 0u : BITS != 8 ? ldg_nc_u8(zp + gi * 16 + tt * 8) : ldg_nc_u16(zp + gi * 32 + tt * 16);
+      r.s[gg][tt] = ldg_nc_u32(sp + gi * kMetaGroupStride + tt * 8);
+      r.z[gg][tt] = SYM ? 0u
+                    : BITS != 8 ? ldg_nc_u8(zp + gi * kMetaGroupStride + tt * 8)
+                                : ldg_nc_u16(zp + (gi * kMetaGroupStride + tt * 8) * 2);
     }
   }
 }
@@ -533,11 +535,11 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const GemvArgs a) {
 #pragma unroll
         for (int tt = 0; tt < kTilesPerWarp; ++tt) {
           const int f = gg * kTilesPerWarp + tt;
-          cp_async_4(slot + SL::kScaleOff + (f * kThreads + tid) * 4, sp + gi * 16 + tt * 8);
+          cp_async_4(slot + SL::kScaleOff + (f * kThreads + tid) * 4, sp + gi * kMetaGroupStride + tt * 8);
           if (!SYM)  // the aligned word holding this lane's zero point(s)
             cp_async_4(slot + SL::kZeroOff + (f * kThreads + tid) * 4,
                        reinterpret_cast<const uint32_t*>(
-                           reinterpret_cast<uintptr_t>(zp + (gi * 16 + tt * 8) * kZeroMul<BITS>) & ~uintptr_t(3)));
+                           reinterpret_cast<uintptr_t>(zp + (gi * kMetaGroupStride + tt * 8) * kZeroMul<BITS>) & ~uintptr_t(3)));
         }
       }
     }

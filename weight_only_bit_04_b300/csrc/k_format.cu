@@ -180,7 +180,7 @@ __global__ void __launch_bounds__(256) pack_qweight3_kernel(Layout L, const uint
 
 // One thread per (row block, group, 16-row tile, lane group): a scale pair and
 // the zero points of the two rows (one byte of two nibbles, or two bytes),
-// stored at meta_index (row-group-major).
+// stored at meta_index.
 __global__ void __launch_bounds__(256) pack_meta_kernel(Layout L, const uint16_t* __restrict__ scales,
                                                         const uint8_t* __restrict__ zeros,
                                                         uint32_t* __restrict__ s_out,

@@ -313,17 +313,12 @@ __device__ __forceinline__ void load_weight_step(uint32_t wdst, const GemmArgs& 
   const unsigned char* qbytes = reinterpret_cast<const unsigned char*>(a.qweight);
   const unsigned char* sbytes = reinterpret_cast<const unsigned char*>(a.scales2);
   bulk_copy_g2s(wdst, qbytes + (size_t(R) * a.KB + kbg) * WT::kCodes, WT::kCodes, bar);
-  // the blob keeps each 32-row group's metadata together: one copy per (row
-  // group, group), landed in the tile's [group][16-row tile][lane group] order
-  for (int gs = 0; gs < ng; ++gs)
-#pragma unroll
-    for (int pr = 0; pr < 4; ++pr) {
-      const size_t mi = size_t(meta_index(R, g0 + gs, 2 * pr, 0, a.G));
-      bulk_copy_g2s(wdst + WT::kScaleOff + gs * 256 + pr * 64, sbytes + mi * 4, 64u, bar);
-      if (!SYM)
-        bulk_copy_g2s(wdst + WT::kZeroOff + gs * WT::kZeroGroup + pr * (WT::kZeroGroup / 4),
-                      a.zeros + mi * (WT::kZeroGroup / 64), uint32_t(WT::kZeroGroup / 4), bar);
-    }
+  // the step's groups of this row block are contiguous in the blob
+  // ([group][16-row tile][lane group]): one copy for the scales, one for the zeros
+  const size_t mi = size_t(meta_index(R, g0, 0, 0, a.G));
+  bulk_copy_g2s(wdst + WT::kScaleOff, sbytes + mi * 4, uint32_t(ng * 256), bar);
+  if (!SYM)
+    bulk_copy_g2s(wdst + WT::kZeroOff, a.zeros + mi * (WT::kZeroGroup / 64), uint32_t(ng * WT::kZeroGroup), bar);
 }
 
 template <int WR, int NT, int SA, int SB, int DS, int GS, bool SYM, int BITS>

@@ -3,13 +3,13 @@
 // The blob holds, each on a 256-byte boundary:
 //   qweight  [NR][KB] tiles of 128 rows x 64 columns of codes: 3072 bytes
 //            (3-bit), 4096 bytes (4-bit) or 8192 bytes (8-bit)
-//   scales   [NR * 4 row groups][G][2 tt][8 g][2] fp16: for the 32-row group
-//            rg = 4 R + (r16 >> 1), tile tt = r16 & 1 and lane group g the
-//            pair (row r16*16+g, row r16*16+g+8); one row group's scales are
-//            contiguous along the groups (64 bytes per group)
-//   zeros    (asymmetric formats only) 3- and 4-bit: [NR * 4][G][2 tt][8 g]
+//   scales   [NR][G][8 r16][8 g][2] fp16: for 16-row tile r16 and lane group g
+//            the pair (row r16*16+g, row r16*16+g+8); a row block's 128 rows
+//            of one group are 256 contiguous bytes (one copy for the GEMM),
+//            a 32-row group's are 64 (the decode stream's unit)
+//   zeros    (asymmetric formats only) 3- and 4-bit: [NR][G][8 r16][8 g]
 //            bytes, low nibble row r16*16+g, high nibble row r16*16+g+8; 8-bit:
-//            [NR * 4][G][2 tt][8 g][2] bytes, row r16*16+g then row r16*16+g+8
+//            [NR][G][8 r16][8 g][2] bytes, row r16*16+g then row r16*16+g+8
 //   perm     [K] int32: packed column -> original column (act order only)
 //   ascale   [K] fp16: per-input-channel activation divisor (unfolded AWQ
 //            only), in packed column order
@@ -68,11 +68,12 @@ __host__ __device__ inline size_t align256(size_t v) { return (v + 255) & ~size_
 __host__ __device__ inline int nibble_index(int kk, int h) { return (kk & 1) * 4 + (kk >> 1) * 2 + h; }
 
 // Index of the scale pair (and of the zero-point byte, or byte pair) of
-// 16-row tile r16 of row block R, group gi, lane group g: row group
-// 4 R + (r16 >> 1) holds 16 entries per group, [tt = r16 & 1][g].
+// 16-row tile r16 of row block R, group gi, lane group g.
 __host__ __device__ inline int64_t meta_index(int64_t R, int64_t gi, int r16, int g, int64_t G) {
-  return ((R * 4 + (r16 >> 1)) * G + gi) * 16 + (r16 & 1) * 8 + g;
+  return ((R * G + gi) * 8 + r16) * 8 + g;
 }
+// Entries between the same (r16, g) of consecutive groups.
+constexpr int kMetaGroupStride = 64;
 
 // 3-bit codes: index, inside a tile, of word wi (0..2) of 16-row tile r16 for a lane.
 __host__ __device__ inline int w3_word_index(int r16, int lane, int wi) {
