@@ -353,7 +353,8 @@ W4A16_API w4a16_status w4a16_gemv_grouped(const w4a16_format* formats, const voi
  * w4a16_chain_run then resets the counters and launches the chain on `stream`
  * (both asynchronous; may be captured in a CUDA graph), on a device with the
  * SM count it was prepared for (else W4A16_ERR_INVALID_ARG). Every wait
- * inside the launch is bounded (1 s); a wait that gives up stops every block,
+ * inside the launch is bounded (1 s, see w4a16_set_wait_limit_ns); a wait
+ * that gives up stops every block,
  * leaves the outputs undefined and is counted (w4a16_pipeline_timeouts). The
  * launch needs one resident thread block per SM (cooperative launch); it
  * fails with W4A16_ERR_CUDA rather than wait if the device cannot host them.
@@ -403,9 +404,9 @@ W4A16_API w4a16_status w4a16_chain_run(const w4a16_chain_info* info, void* works
  *            16-byte aligned, overlapping neither x nor y.
  * 1 <= M <= 2^20. Needs a Blackwell GPU (compute capability 10.x); returns
  * W4A16_ERR_UNSUPPORTED on older devices.
- * Every pipeline wait inside the kernel is bounded (1 s); a wait that gives
- * up leaves y unwritten for its tile and is counted on the device, see
- * w4a16_pipeline_timeouts().
+ * Every pipeline wait inside the kernel is bounded (1 s, see
+ * w4a16_set_wait_limit_ns); a wait that gives up leaves y unwritten for its
+ * tile and is counted on the device, see w4a16_pipeline_timeouts().
  */
 W4A16_API size_t w4a16_gemm_workspace_bytes(const w4a16_format* f, int64_t M);
 W4A16_API w4a16_status w4a16_gemm(const w4a16_format* f, const void* packed, size_t packed_bytes,
@@ -434,10 +435,44 @@ W4A16_API w4a16_status w4a16_gemm_ex(const w4a16_format* f, const void* packed, 
 /*
  * Number of bounded pipeline waits on the current device that gave up since
  * the previous call (each one means a tile of some w4a16_gemm output, or the
- * later outputs of a chained launch, were not written); the count is reset. Synchronous: waits for the device's pending
- * work to finish. Not expected to be nonzero in correct operation.
+ * later outputs of a chained launch, were not written); the count is reset.
+ * Synchronous: waits for the device's pending work to finish. Not expected to
+ * be nonzero in correct operation. Whenever it is nonzero, the outputs of the
+ * launches it covers are undefined, and so is any timing taken of them.
  */
 W4A16_API w4a16_status w4a16_pipeline_timeouts(uint32_t* count);
+
+/*
+ * Limit, in nanoseconds, of every bounded pipeline wait inside the kernels
+ * (w4a16_gemm, w4a16_chain_run) launched after this call; 0 restores the
+ * default, 1 s. Returns the previous limit. Process-wide. A launch captured in
+ * a CUDA graph keeps the limit in force when it was captured. Meant for tests
+ * of the timeout path: a limit shorter than the work the waits cover makes
+ * them give up (counted by w4a16_pipeline_timeouts, outputs undefined) and the
+ * launch return; waits that only let copies already issued land before a
+ * thread block exits keep their own 1 s.
+ */
+W4A16_API uint64_t w4a16_set_wait_limit_ns(uint64_t ns);
+
+/*
+ * Test hook: the next call (from any thread) that would launch device work
+ * launches nothing and returns W4A16_ERR_CUDA, with w4a16_last_cuda_error()
+ * == error in the calling thread. One-shot; 0 clears a pending error. Lets a
+ * caller's handling of a failed launch be tested without a device fault.
+ */
+W4A16_API void w4a16_debug_fail_next_launch(int error);
+
+/*
+ * Debug flavor of the library (libw4a16_debug.so, built with
+ * -DW4A16_DEBUG_CHECKS): the decode stream checks the indices of its code,
+ * scale and zero-point copies, of the staged activations and group sums, of
+ * the slot units and of the partial sums it reads and writes; a failed check
+ * skips the access and records its code (the first one wins; 0x1xx producer,
+ * 0x2xx staging, 0x3xx consumer warps, 0x4xx layer shares). Synchronizes the
+ * device, then stores the recorded code (0: none) in *word and resets it.
+ * W4A16_ERR_UNSUPPORTED (and *word = 0) in the release library.
+ */
+W4A16_API w4a16_status w4a16_debug_check_word(uint32_t* word);
 
 /*
  * w4a16_gemv with options.

@@ -74,6 +74,19 @@ bool build_perm(const w4a16_format& f, const int32_t* g_idx, std::vector<int32_t
 
 w4a16_status cuda_error_status(cudaError_t e) { return cuda_fail(e); }
 
+namespace {
+constexpr unsigned long long kDefaultWaitNs = 1000ull * 1000ull * 1000ull;  // 1 s
+std::atomic<unsigned long long> g_wait_ns{kDefaultWaitNs};
+std::atomic<int> g_injected{0};
+}  // namespace
+
+unsigned long long wait_limit_ns() { return g_wait_ns.load(std::memory_order_relaxed); }
+
+cudaError_t take_injected_launch_error() {
+  if (g_injected.load(std::memory_order_relaxed) == 0) return cudaSuccess;
+  return cudaError_t(g_injected.exchange(0));
+}
+
 cudaError_t device_info(DeviceInfo* out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -121,6 +134,27 @@ const char* w4a16_status_string(w4a16_status s) {
 
 int w4a16_last_cuda_error(void) { return g_last_cuda_error; }
 
+uint64_t w4a16_set_wait_limit_ns(uint64_t ns) {
+  return g_wait_ns.exchange(ns == 0 ? kDefaultWaitNs : ns);
+}
+
+void w4a16_debug_fail_next_launch(int error) { g_injected.store(error); }
+
+w4a16_status w4a16_debug_check_word(uint32_t* word) {
+  if (word == nullptr) return W4A16_ERR_INVALID_ARG;
+  *word = 0;
+#ifdef W4A16_DEBUG_CHECKS
+  cudaError_t e = cudaDeviceSynchronize();
+  unsigned int w = 0;
+  if (e == cudaSuccess) e = take_debug_error(&w);
+  if (e != cudaSuccess) return cuda_fail(e);
+  *word = w;
+  return W4A16_OK;
+#else
+  return W4A16_ERR_UNSUPPORTED;
+#endif
+}
+
 size_t w4a16_quantize_workspace_bytes(const w4a16_format* f) {
   if (format_status(f) != W4A16_OK) return 0;
   return f->has_g_idx ? size_t(f->K) * 4 : 0;
@@ -149,7 +183,8 @@ static w4a16_status quantize_common(const w4a16_format* f, const uint16_t* w, co
     if (e != cudaSuccess) return cuda_fail(e);
     perm_dev = static_cast<const int32_t*>(workspace);
   }
-  cudaError_t e = launch_quantize_rtn(L, w, perm_dev, act_scale, q, scales, zeros, stream);
+  cudaError_t e = take_injected_launch_error();
+  if (e == cudaSuccess) e = launch_quantize_rtn(L, w, perm_dev, act_scale, q, scales, zeros, stream);
   return e == cudaSuccess ? W4A16_OK : cuda_fail(e);
 }
 
@@ -185,7 +220,8 @@ static w4a16_status pack_common(const w4a16_format* f, const uint8_t* q, const u
                                     cudaMemcpyHostToDevice, stream);
     if (e != cudaSuccess) return cuda_fail(e);
   }
-  cudaError_t e = launch_pack(L, q, scales, zeros, act_scale, packed, stream);
+  cudaError_t e = take_injected_launch_error();
+  if (e == cudaSuccess) e = launch_pack(L, q, scales, zeros, act_scale, packed, stream);
   return e == cudaSuccess ? W4A16_OK : cuda_fail(e);
 }
 
@@ -208,7 +244,8 @@ w4a16_status w4a16_dequant(const w4a16_format* f, const void* packed, size_t pac
   if (s != W4A16_OK) return s;
   if (w_out == nullptr) return W4A16_ERR_INVALID_ARG;
   if (!aligned(w_out, 16)) return W4A16_ERR_MISALIGNED;
-  cudaError_t e = launch_dequant(make_layout(*f), packed, w_out, stream);
+  cudaError_t e = take_injected_launch_error();
+  if (e == cudaSuccess) e = launch_dequant(make_layout(*f), packed, w_out, stream);
   return e == cudaSuccess ? W4A16_OK : cuda_fail(e);
 }
 
@@ -248,7 +285,8 @@ static w4a16_status gemv_common(const w4a16_format* f, const void* packed, size_
   if (!gemv_plan_ok(L, int(M), plan)) return (shape || ksplit) ? W4A16_ERR_INVALID_ARG : W4A16_ERR_UNSUPPORTED;
   uint32_t kflags = flags & (W4A16_GEMV_WEIGHTS_READY | W4A16_GEMV_INPUTS_READY);
   if (kflags & W4A16_GEMV_INPUTS_READY) kflags |= W4A16_GEMV_WEIGHTS_READY;  // inputs ready implies weights ready
-  e = launch_gemv(L, packed, x, y, int(M), plan, kflags, stream);
+  e = take_injected_launch_error();
+  if (e == cudaSuccess) e = launch_gemv(L, packed, x, y, int(M), plan, kflags, stream);
   return e == cudaSuccess ? W4A16_OK : cuda_fail(e);
 }
 
@@ -312,7 +350,8 @@ w4a16_status w4a16_gemv_grouped(const w4a16_format* formats, const void* const* 
   if (!gemv_plan_ok(Lc, int(M), plan)) return W4A16_ERR_UNSUPPORTED;
   uint32_t kflags = flags & (W4A16_GEMV_WEIGHTS_READY | W4A16_GEMV_INPUTS_READY);
   if (kflags & W4A16_GEMV_INPUTS_READY) kflags |= W4A16_GEMV_WEIGHTS_READY;
-  e = launch_gemv_group(Lc, grp, x, int(M), plan, kflags, static_cast<cudaStream_t>(stream));
+  e = take_injected_launch_error();
+  if (e == cudaSuccess) e = launch_gemv_group(Lc, grp, x, int(M), plan, kflags, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? W4A16_OK : cuda_fail(e);
 }
 
@@ -356,7 +395,8 @@ static w4a16_status gemm_common(const w4a16_format* f, const void* packed, size_
   }
   if (ksplit != 0) plan.ksplit = ksplit;
   if (!gemm_plan_ok(L, plan)) return W4A16_ERR_INVALID_ARG;
-  e = launch_gemm(L, packed, x, y, M, workspace, plan, stream);
+  e = take_injected_launch_error();
+  if (e == cudaSuccess) e = launch_gemm(L, packed, x, y, M, workspace, plan, stream);
   return e == cudaSuccess ? W4A16_OK : cuda_fail(e);
 }
 
@@ -391,7 +431,8 @@ w4a16_status w4a16_gptq(const w4a16_format* f, const uint16_t* w, const uint16_t
   if (!aligned(w, 2) || !aligned(x, 2) || !aligned(scales, 2) || !aligned(g_idx, 4) || !aligned(workspace, 256))
     return W4A16_ERR_MISALIGNED;
   if (workspace_bytes < gptq_workspace_bytes(f->N, f->K)) return W4A16_ERR_BUFFER_TOO_SMALL;
-  cudaError_t e = launch_gptq(make_layout(*f), w, x, T, damp, q, scales, zeros, g_idx, workspace,
+  cudaError_t e = take_injected_launch_error();
+  if (e == cudaSuccess) e = launch_gptq(make_layout(*f), w, x, T, damp, q, scales, zeros, g_idx, workspace,
                               static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? W4A16_OK : cuda_fail(e);
 }

@@ -213,7 +213,9 @@ w4a16_status w4a16_chain_run(const w4a16_chain_info* info, void* workspace, w4a1
   c.M = int(info->M);
   c.x_nbuf = info->flags & 3;
   c.x_buf_bytes = c.x_nbuf ? info->reserved_x : 0;
-  e = launch_stream(c, info->bits, info->group_size, info->symmetric != 0, info->blocks, st);
+  c.wait_ns = wait_limit_ns();
+  e = take_injected_launch_error();
+  if (e == cudaSuccess) e = launch_stream(c, info->bits, info->group_size, info->symmetric != 0, info->blocks, st);
   return e == cudaSuccess ? W4A16_OK : cuda_error_status(e);
 }
 

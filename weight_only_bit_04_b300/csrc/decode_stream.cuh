@@ -44,7 +44,8 @@
 //    eight consumer warps together, which would otherwise idle, right after
 //    one was. The warp then publishes the layer as ready.
 //
-// Every wait is bounded (1 s by the global timer) and also gives up when
+// Every wait is bounded (1 s by the global timer unless the host set
+// another limit, w4a16_set_wait_limit_ns) and also gives up when
 // another block has raised the abort flag; a wait that times out is counted
 // (w4a16_pipeline_timeouts) and raises the flag, and every role then returns,
 // the producer after its copies in flight have landed. Outputs are undefined
@@ -135,15 +136,17 @@ constexpr int kWaitOk = 0, kWaitTimeout = 1, kWaitAbort = 2;
 constexpr uint64_t kAbortPollNs = 20000;
 struct Guard {
   unsigned int* abort_flag;
+  uint64_t limit;  // ns
   uint64_t t0;
   uint32_t spins;
   __device__ __forceinline__ void start() {
     t0 = 0;
     spins = 0;
   }
-  // kWaitOk: keep waiting
+  // kWaitOk: keep waiting. The clock is read on the first spin and then
+  // every eighth (a spin is at least an L2 round trip or an mbarrier test).
   __device__ __forceinline__ int check() {
-    if ((++spins & 63u) != 0) return kWaitOk;
+    if ((++spins & 7u) != 1u) return kWaitOk;
     const uint64_t now = global_timer_ns();
     if (t0 == 0) {
       t0 = now;
@@ -151,7 +154,7 @@ struct Guard {
     }
     const uint64_t waited = now - t0;
     if (waited > kAbortPollNs && ld_relaxed_gpu_u32(abort_flag) != 0) return kWaitAbort;
-    if (waited > kTWaitLimitNs) {
+    if (waited > limit) {
       atomicExch(abort_flag, 1u);
       return kWaitTimeout;
     }
@@ -192,7 +195,6 @@ __device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
 }
 
 constexpr int kConsumersStage = 1 << 30;
-constexpr int kConsumerBarrier = 1;  // named barrier of the consumer warps
 
 // Land the activations of a layer (M rows of K) in a staged buffer and add
 // each group of each row (fixed order per group). `tid` / `nt`: this thread's
@@ -253,7 +255,8 @@ __device__ __forceinline__ void stage_sums(int K, int M, const uint16_t* xs, flo
       for (int u = 0; u < U; ++u) v[u] += __shfl_xor_sync(0xffffffffu, v[u], o);
 #pragma unroll
     for (int u = 0; u < U; ++u)
-      if (q0 + u * nt + tid < total && (lane & (CPG - 1)) == 0) xsum[(kk[u] / CPG) * MP + tk[u]] = v[u];
+      if (q0 + u * nt + tid < total && (lane & (CPG - 1)) == 0 && W4A16_CHECK(tk[u] < M && kk[u] < cpr, 0x203u))
+        xsum[(kk[u] / CPG) * MP + tk[u]] = v[u];
   }
 }
 
@@ -268,7 +271,8 @@ __global__ void __launch_bounds__(kStreamThreads, 1) decode_stream_kernel(const 
   constexpr int RGMAX = stream_max_rg(MP);
   extern __shared__ __align__(1024) unsigned char smem[];
   const uint32_t ring = smem_addr(smem);
-  // mbarriers: full[S], empty[S] (the ring), then per layer parity (j & 1):
+  // mbarriers: full[S], empty[S] (the ring), the consumer warps' staging
+  // barrier after the per-layer ones, and per layer parity (j & 1):
   // cdone (the consumer warps have written layer j's partial sums), rdy (layer
   // j's activations may be read), fdone (the finishing warp has read layer j's
   // partial sums). Phase (j >> 1) & 1 of barrier j & 1 is layer j's; no role
@@ -279,6 +283,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1) decode_stream_kernel(const 
   const uint32_t cdone0 = empty0 + S * 8;
   const uint32_t rdy0 = cdone0 + 16;
   const uint32_t fdone0 = rdy0 + 16;
+  const uint32_t stg = fdone0 + 16;  // the consumer warps' staging barrier
   float* part = reinterpret_cast<float*>(smem + stream_part_off(BITS, GS));  // [2][RGMAX][NW][32 rows][MP]
   unsigned char* xbase = smem + stream_x_off(BITS, GS, MP);  // staged-activation buffers (XS)
   LayerRec* rec = reinterpret_cast<LayerRec*>(smem + stream_rec_off(BITS, GS));  // per layer parity
@@ -290,6 +295,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1) decode_stream_kernel(const 
   unsigned int* done = c.done;
   Guard gd;
   gd.abort_flag = done + size_t(nj) * CS;
+  gd.limit = c.wait_ns;
 
   if (tid == 0) {
     for (int s = 0; s < S; ++s) {
@@ -301,6 +307,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1) decode_stream_kernel(const 
       mbar_init(rdy0 + 8 * q, 1);
       mbar_init(fdone0 + 8 * q, 1);
     }
+    mbar_init(stg, NW);
     fence_mbarrier_init();
   }
   __syncthreads();
@@ -326,6 +333,8 @@ __global__ void __launch_bounds__(kStreamThreads, 1) decode_stream_kernel(const 
       const uint32_t* sc_base = J.scales2;
       const uint8_t* z_base = J.zeros;
       const int G = J.G, KB = J.KB, NU = s.NU;
+      const int64_t ntiles = int64_t((J.N + 127) / 128) * KB;  // 128x64 code tiles of the blob
+      const int64_t nmeta = ntiles / KB * G * 64;               // scale pairs of the blob
       int rgl0 = 0, ku0 = 0;  // (row group, unit) of the slot's first unit, advanced without dividing
       for (int k = 0; k < R; ++k) {
         if (!warp_outcome(wait_mbar(empty0 + 8 * slot, phase ^ 1u, gd))) {
@@ -347,7 +356,8 @@ __global__ void __launch_bounds__(kStreamThreads, 1) decode_stream_kernel(const 
             int box = CU;
             while (nu > 0) {  // power-of-two boxes, largest first (one box in the common case)
               while (box > nu) box >>= 1;
-              tma_load_3d(sb + d * SG::kUnitCode, m + (ilog2(CU) - ilog2(box)), 0, c1, c2, full);
+              if (W4A16_CHECK(d + box <= CU && int64_t(c2) + box * SG::UB <= ntiles, 0x101u))
+                tma_load_3d(sb + d * SG::kUnitCode, m + (ilog2(CU) - ilog2(box)), 0, c1, c2, full);
               c2 += box * SG::UB;
               d += box;
               ku += box;
@@ -372,8 +382,9 @@ __global__ void __launch_bounds__(kStreamThreads, 1) decode_stream_kernel(const 
           // row group rg's scales of one group: 64 contiguous bytes (its
           // two 16-row tiles in the row block's [group][16-row tile] order)
           const int gg = p >> 2;
-          const uint32_t* src = sc_base + meta_index(rg >> 2, ku * SG::GU + gg, 2 * (rg & 3), 0, G) + (p & 3) * 4;
-          cp_async_16_cg(sb + SG::kScaleOff + (d * SG::GU + gg) * 64 + (p & 3) * 16, src);
+          const int64_t e = meta_index(rg >> 2, ku * SG::GU + gg, 2 * (rg & 3), 0, G) + (p & 3) * 4;
+          const int dst = SG::kScaleOff + (d * SG::GU + gg) * 64 + (p & 3) * 16;
+          if (W4A16_CHECK(e + 4 <= nmeta && dst + 16 <= SG::kZeroOff, 0x102u)) cp_async_16_cg(sb + dst, sc_base + e);
         }
         if (!SYM) {
           for (int q = lane; q < nu_slot * SG::kZeroChunks; q += 32) {
@@ -384,9 +395,10 @@ __global__ void __launch_bounds__(kStreamThreads, 1) decode_stream_kernel(const 
               ++rg;
             }
             const int gg = p / (SG::ZB / 16), h = p - gg * (SG::ZB / 16);
-            const uint8_t* src =
-                z_base + meta_index(rg >> 2, ku * SG::GU + gg, 2 * (rg & 3), 0, G) * (SG::ZB / 16) + h * 16;
-            cp_async_16_cg(sb + SG::kZeroOff + (d * SG::GU + gg) * SG::ZB + h * 16, src);
+            const int64_t e = meta_index(rg >> 2, ku * SG::GU + gg, 2 * (rg & 3), 0, G) * (SG::ZB / 16) + h * 16;
+            const int dst = SG::kZeroOff + (d * SG::GU + gg) * SG::ZB + h * 16;
+            if (W4A16_CHECK(e + 16 <= nmeta * (SG::ZB / 16) && dst + 16 <= SG::kSlot, 0x103u))
+              cp_async_16_cg(sb + dst, z_base + e);
           }
         }
         cp_async_arrive_noinc(full);
@@ -403,9 +415,11 @@ __global__ void __launch_bounds__(kStreamThreads, 1) decode_stream_kernel(const 
       }
     }
     cp_async_wait_all();
-    if (!alive && lane == 0) {
+    if (lane == 0) {
       // Let the TMA copies in flight land before the block can exit: the last
-      // min(issued, S) fills, each in its own slot.
+      // min(issued, S) fills, each in its own slot. After a normal run every
+      // one has been consumed and each test returns at once; after an abort
+      // (this warp's or another role's) some may still be landing.
       const int nf = min(issued, S);
       for (int k = 1; k <= nf; ++k) {
         const int q = issued - k;
@@ -455,6 +469,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1) decode_stream_kernel(const 
         fresh = true;
       }
       const Span s = span_of(J, P, b, SG::UB);
+      if (!W4A16_CHECK(s.n <= RGMAX, 0x402u)) return;
       if (s.n > 0) {
         if (XS) {
           if (stale || J.x != loaded || J.K != loaded_k) {
@@ -471,6 +486,10 @@ __global__ void __launch_bounds__(kStreamThreads, 1) decode_stream_kernel(const 
             if (lu == j - 1 && !wait_layer(cdone0, j - 1, gd)) return;
             cur = nb;
             uint16_t* xs = reinterpret_cast<uint16_t*>(xbase + size_t(nb) * c.x_buf_bytes);
+            if (!W4A16_CHECK(stream_x_buf(J.K, M, GS) <= c.x_buf_bytes &&
+                                 stream_x_off(BITS, GS, MP) + int64_t(nb + 1) * c.x_buf_bytes <= kStreamSmem,
+                             0x202u))
+              return;
             if (!fresh) {
               // ahead of the consumers (no dependency was just acquired):
               // stage here, overlapped with their work on earlier layers
@@ -579,6 +598,16 @@ __global__ void __launch_bounds__(kStreamThreads, 1) decode_stream_kernel(const 
   uint32_t phase = 0;
   bool ready = false;      // the full barrier of ring slot `slot` was seen complete
   bool rdy_ready = false;  // layer j's ready barrier was seen complete
+  // Every consumer warp at one point, with a bounded wait (a warp that gave
+  // up never arrives, and the others then give up too instead of hanging).
+  uint32_t stg_parity = 0;
+  auto consumers_sync = [&]() -> bool {
+    __syncwarp();
+    if (lane == 0) mbar_arrive(stg);  // release: this warp's copies and stores
+    const bool ok = warp_outcome(wait_mbar(stg, stg_parity, gd));
+    stg_parity ^= 1u;
+    return ok;
+  };
   for (int j = 0; j < nj; ++j) {
     // Layer j's activations are readable, and (the dependency warp waited for
     // it before publishing layer j) the finishing warp has read layer j - 2's
@@ -596,11 +625,9 @@ __global__ void __launch_bounds__(kStreamThreads, 1) decode_stream_kernel(const 
       uint16_t* xs_st = reinterpret_cast<uint16_t*>(xbase + (L.xsel & ~kConsumersStage));
       stage_copy<GS, MP>(L.x, L.K, M, xs_st, tid, NW * 32);
       cp_async_wait_all();
-      __syncwarp();  // bar.sync is warp-aligned: converge after the divergent loop
-      named_bar_sync(kConsumerBarrier, NW * 32);
+      if (!consumers_sync()) return;
       stage_sums<GS, MP, 2>(L.K, M, xs_st, reinterpret_cast<float*>(xs_st + stream_xsum_off(L.K, M) / 2), tid, NW * 32);
-      __syncwarp();
-      named_bar_sync(kConsumerBarrier, NW * 32);
+      if (!consumers_sync()) return;
     }
     Span s;
     s.T = L.T;
@@ -623,6 +650,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1) decode_stream_kernel(const 
       float tot[kTilesPerWarp][NB][4];
       int cur = -1;
       auto flush = [&](int rgl) {
+        if (!W4A16_CHECK(rgl >= 0 && rgl < RGMAX, 0x302u)) return;
         float* pe = pb + size_t(rgl * NW + warp) * 32 * MP;
 #pragma unroll
         for (int tt = 0; tt < kTilesPerWarp; ++tt)
@@ -654,6 +682,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1) decode_stream_kernel(const 
         float xsg[SG::GU][NB][2];
       };
       auto load_unit_in = [&](const unsigned char* sb, int d, int ku, UnitIn& in) {
+        if (!W4A16_CHECK(d >= 0 && d < CU && ku >= 0 && ku < s.NU, 0x301u)) d = 0, ku = 0;
 #pragma unroll
         for (int bb = 0; bb < SG::UB; ++bb) {
           const unsigned char* cb = sb + d * SG::kUnitCode + bb * SG::CB;

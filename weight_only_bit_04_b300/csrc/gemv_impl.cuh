@@ -67,6 +67,21 @@ constexpr uint64_t kTWaitLimitNs = 1000ull * 1000ull * 1000ull;  // every pipeli
 // bounded waits that gave up (see w4a16_pipeline_timeouts); one per translation unit
 static __device__ unsigned int g_gemv_timeouts;
 
+// Debug builds (-DW4A16_DEBUG_CHECKS): index checks on the decode stream's
+// shared- and global-memory accesses. A failed check records its code (the
+// first one wins) in this word and the access is skipped; nothing traps. In
+// other builds every check is the constant true.
+static __device__ unsigned int g_debug_error;
+#ifdef W4A16_DEBUG_CHECKS
+__device__ __forceinline__ bool debug_check(bool ok, unsigned int code) {
+  if (!ok) atomicCAS(&g_debug_error, 0u, code);
+  return ok;
+}
+#define W4A16_CHECK(cond, code) debug_check(bool(cond), (code))
+#else
+#define W4A16_CHECK(cond, code) true
+#endif
+
 struct GemvArgs {
   const uint32_t* qweight;
   const uint32_t* scales2;  // scale pairs (row g, row g+8)
@@ -877,6 +892,19 @@ cudaError_t launch_gemv_group_bits(const Layout& Lc, const GemvGroup& grp, const
 }
 
 // This translation unit's timeout counter (read and cleared).
+cudaError_t take_local_debug_error(unsigned int* word) {
+  unsigned int w = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(&w, g_debug_error, sizeof(w));
+  if (e != cudaSuccess) return e;
+  if (w != 0) {
+    const unsigned int zero = 0;
+    e = cudaMemcpyToSymbol(g_debug_error, &zero, sizeof(zero));
+    if (e != cudaSuccess) return e;
+  }
+  *word = w;
+  return cudaSuccess;
+}
+
 cudaError_t take_local_gemv_timeouts(unsigned int* count) {
   unsigned int c = 0;
   cudaError_t e = cudaMemcpyFromSymbol(&c, g_gemv_timeouts, sizeof(c));

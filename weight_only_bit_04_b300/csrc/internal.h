@@ -20,6 +20,13 @@ cudaError_t device_info(DeviceInfo* out);
 // Record e for w4a16_last_cuda_error() (calling thread) and return W4A16_ERR_CUDA.
 w4a16_status cuda_error_status(cudaError_t e);
 
+// Limit of the kernels' bounded waits for launches issued now (w4a16_set_wait_limit_ns).
+unsigned long long wait_limit_ns();
+// The error w4a16_debug_fail_next_launch left for the next launch, taken
+// (cudaSuccess when none): every entry point calls this just before it
+// launches and reports a non-success value as if the launch had failed.
+cudaError_t take_injected_launch_error();
+
 // ascale: per-input-channel scale (original column order) applied to the
 // weights before quantizing, or nullptr.
 cudaError_t launch_quantize_rtn(const Layout& L, const uint16_t* w, const int32_t* perm_dev,
@@ -113,6 +120,7 @@ struct StreamLaunch {
   int n_jobs, M;
   int x_buf_bytes;          // bytes of one staged-activation buffer (0: activations not staged)
   int x_nbuf;               // staged-activation buffers, 1 or 2
+  unsigned long long wait_ns;  // limit of every bounded wait (wait_limit_ns() at launch)
 };
 cudaError_t launch_stream(const StreamLaunch& c, int bits, int gsize, bool sym, int sm_count, cudaStream_t stream);
 
@@ -128,5 +136,7 @@ cudaError_t encode_tiled_map(CUtensorMap* map, CUtensorMapDataType type, int ran
 // chained launch's waits).
 cudaError_t take_pipeline_timeouts(unsigned int* count);
 cudaError_t take_gemv_timeouts(unsigned int* count);
+// First failed index check of a debug build (-DW4A16_DEBUG_CHECKS), read and reset.
+cudaError_t take_debug_error(unsigned int* word);
 
 }  // namespace w4a16

@@ -45,7 +45,9 @@ __device__ unsigned int g_pipeline_timeouts;
 
 namespace {
 
-constexpr uint64_t kWaitLimitNs = 1000ull * 1000ull * 1000ull;  // 1 s per wait
+// Limit of the waits that let copies and MMAs already issued land before the
+// block exits after an abort; the pipeline's own waits use GemmArgs::wait_ns.
+constexpr uint64_t kWaitLimitNs = 1000ull * 1000ull * 1000ull;  // 1 s
 
 // WR: 128-row weight blocks per thread block; NT: tokens per thread block;
 // SA: tensor-memory stages of dequantized weights; SB: shared-memory stages of
@@ -110,6 +112,7 @@ struct GemmArgs {
   uint16_t* y;
   int M, N, NR, G, KB;
   int tok_blocks;
+  unsigned long long wait_ns;  // limit of the pipeline's bounded waits
   // K split over the blocks of a cluster (gridDim.y): block r takes the
   // 64-column steps [KB*r/ks, KB*(r+1)/ks); the partial sums are added
   // through distributed shared memory in rank order.
@@ -141,9 +144,10 @@ __device__ __forceinline__ void note_timeout(volatile int* abort_flag) {
 }
 
 // Bounded wait that also gives up once another role of the block has.
-__device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+__device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                              uint64_t limit_ns) {
   if (*abort_flag) return false;
-  if (mbar_wait_bounded(bar, parity, kWaitLimitNs)) return true;
+  if (mbar_wait_bounded(bar, parity, limit_ns)) return true;
   note_timeout(abort_flag);
   return false;
 }
@@ -386,11 +390,11 @@ __global__ void __launch_bounds__(Cfg<WR, NT, SA, SB, DS, BITS>::kThreads, 1)
     for (int i = 0; i < nsteps && ok; ++i) {
       const int kb = ds + i * DS;  // local step
       const int sb = kb % SB, sa = kb % SA;
-      if (!wait_or_abort(full_b(sb), uint32_t(kb / SB) & 1u, abort_flag)) {
+      if (!wait_or_abort(full_b(sb), uint32_t(kb / SB) & 1u, abort_flag, a.wait_ns)) {
         ok = false;
         break;
       }
-      if (kb >= SA && !wait_or_abort(empty_a(sa), uint32_t(kb / SA - 1) & 1u, abort_flag)) {
+      if (kb >= SA && !wait_or_abort(empty_a(sa), uint32_t(kb / SA - 1) & 1u, abort_flag, a.wait_ns)) {
         ok = false;
         break;
       }
@@ -407,7 +411,7 @@ __global__ void __launch_bounds__(Cfg<WR, NT, SA, SB, DS, BITS>::kThreads, 1)
     // Each warp transposes its 32 rows x NT/DS tokens through a private
     // shared-memory slice (no block-wide barrier, so a warp that gave up
     // cannot stall the others) and writes 64-byte row segments.
-    if (ok && wait_or_abort(acc_bar, 0u, abort_flag)) {
+    if (ok && wait_or_abort(acc_bar, 0u, abort_flag, a.wait_ns)) {
       tc_fence_after();
       constexpr int ET = C::kEpiTokens;
       const int t0 = ds * ET;  // first token of this set
@@ -462,7 +466,7 @@ __global__ void __launch_bounds__(Cfg<WR, NT, SA, SB, DS, BITS>::kThreads, 1)
       for (int kb = 0; kb < KB; ++kb) {
         const int s = kb % SB;
         const int n = kb / SB;
-        if (kb >= SB && !wait_or_abort(empty_b(s), uint32_t(n - 1) & 1u, abort_flag)) break;
+        if (kb >= SB && !wait_or_abort(empty_b(s), uint32_t(n - 1) & 1u, abort_flag, a.wait_ns)) break;
         const int kbg = kb_lo + kb;  // global 64-column step
         const int g0 = kbg * 64 / GS;
         const int ng = step_groups<GS>(kbg, a.G);
@@ -481,11 +485,12 @@ __global__ void __launch_bounds__(Cfg<WR, NT, SA, SB, DS, BITS>::kThreads, 1)
         }
         ++issued;
       }
-      if (*abort_flag) {
-        // drain: the last loads issued must land before the block's shared memory goes away
-        for (int kb = max(issued - SB, 0); kb < issued; ++kb)
-          mbar_wait_bounded(full_b(kb % SB), uint32_t(kb / SB) & 1u, kWaitLimitNs);
-      }
+      // drain: the last loads issued must land before the block's shared
+      // memory goes away (after a normal run they have all been consumed and
+      // each test returns at once; another role may abort after this warp's
+      // last issue)
+      for (int kb = max(issued - SB, 0); kb < issued; ++kb)
+        mbar_wait_bounded(full_b(kb % SB), uint32_t(kb / SB) & 1u, kWaitLimitNs);
     }
   } else if (warp == C::kMmaWarp) {
     // ---------------- MMA issue (one thread)
@@ -493,8 +498,8 @@ __global__ void __launch_bounds__(Cfg<WR, NT, SA, SB, DS, BITS>::kThreads, 1)
       const uint32_t idesc = idesc_f16<NT>();
       for (int kb = 0; kb < KB; ++kb) {
         const int sa = kb % SA, sb = kb % SB;
-        if (!wait_or_abort(full_b(sb), uint32_t(kb / SB) & 1u, abort_flag)) break;
-        if (!wait_or_abort(full_a(sa), uint32_t(kb / SA) & 1u, abort_flag)) break;
+        if (!wait_or_abort(full_b(sb), uint32_t(kb / SB) & 1u, abort_flag, a.wait_ns)) break;
+        if (!wait_or_abort(full_a(sa), uint32_t(kb / SA) & 1u, abort_flag, a.wait_ns)) break;
         tc_fence_after();
         const uint32_t b_addr = sbase + uint32_t(sb * C::kStage);
 #pragma unroll
@@ -814,6 +819,7 @@ cudaError_t launch_gemm(const Layout& L, const void* blob, const uint16_t* x, ui
   a.NR = int(L.NR);
   a.G = int(L.G);
   a.KB = int(L.KB);
+  a.wait_ns = wait_limit_ns();
   const bool g = L.act || L.awq;
   const int ks = plan.ksplit;
   if (L.bits == 8) return launch_tile<8>(plan.tile, L, a, xa, M, ks, g, stream);

@@ -23,6 +23,9 @@ cudaError_t launch_stream_b8(const StreamLaunch& c, int gsize, bool sym, int sm_
 cudaError_t take_gemv_timeouts_b3(unsigned int* count);
 cudaError_t take_gemv_timeouts_b4(unsigned int* count);
 cudaError_t take_gemv_timeouts_b8(unsigned int* count);
+cudaError_t take_debug_error_b3(unsigned int* word);
+cudaError_t take_debug_error_b4(unsigned int* word);
+cudaError_t take_debug_error_b8(unsigned int* word);
 
 bool gemv_plan_ok(const Layout& L, int M, const GemvPlan& p) {
   if (!valid_ksplit(p.ksplit)) return false;
@@ -84,6 +87,16 @@ cudaError_t launch_stream(const StreamLaunch& c, int bits, int gsize, bool sym, 
   if (bits == 8) return launch_stream_b8(c, gsize, sym, sm_count, stream);
   if (bits == 3) return launch_stream_b3(c, gsize, sym, sm_count, stream);
   return launch_stream_b4(c, gsize, sym, sm_count, stream);
+}
+
+cudaError_t take_debug_error(unsigned int* word) {
+  unsigned int w[3] = {0, 0, 0};
+  cudaError_t e = take_debug_error_b4(&w[0]);
+  if (e == cudaSuccess) e = take_debug_error_b8(&w[1]);
+  if (e == cudaSuccess) e = take_debug_error_b3(&w[2]);
+  if (e != cudaSuccess) return e;
+  *word = w[0] ? w[0] : w[1] ? w[1] : w[2];
+  return cudaSuccess;
 }
 
 cudaError_t take_gemv_timeouts(unsigned int* count) {

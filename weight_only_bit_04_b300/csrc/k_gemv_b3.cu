@@ -18,5 +18,6 @@ cudaError_t launch_stream_b3(const StreamLaunch& c, int gsize, bool sym, int sm_
 }
 
 cudaError_t take_gemv_timeouts_b3(unsigned int* count) { return take_local_gemv_timeouts(count); }
+cudaError_t take_debug_error_b3(unsigned int* word) { return take_local_debug_error(word); }
 
 }  // namespace w4a16

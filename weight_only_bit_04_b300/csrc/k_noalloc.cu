@@ -77,7 +77,8 @@ w4a16_status w4a16_quantize_rtn_noalloc(const w4a16_format* f, const uint16_t* w
   if (f->has_g_idx && f->K > kNoAllocMaxK) return W4A16_ERR_BUFFER_TOO_SMALL;  // beyond the fixed scratch
   const Layout L = make_layout(*f);
   if (!f->has_g_idx) {
-    const cudaError_t e = launch_quantize_rtn(L, w, nullptr, nullptr, q, scales, zeros, stream);
+    cudaError_t e = take_injected_launch_error();
+    if (e == cudaSuccess) e = launch_quantize_rtn(L, w, nullptr, nullptr, q, scales, zeros, stream);
     return e == cudaSuccess ? W4A16_OK : cuda_error_status(e);
   }
   int32_t* scratch = nullptr;
@@ -97,6 +98,8 @@ w4a16_status w4a16_quantize_rtn_noalloc(const w4a16_format* f, const uint16_t* w
     g_host_count[t] = int32_t(t * f->group_size);  // next free slot of group t
   }
   for (int64_t k = 0; k < K; ++k) g_host_perm[g_host_count[g_idx[k]]++] = int32_t(k);
+  e = take_injected_launch_error();
+  if (e != cudaSuccess) return cuda_error_status(e);
   // Pageable source: the copy has read the host buffer when it returns.
   e = cudaMemcpyAsync(scratch, g_host_perm, size_t(K) * 4, cudaMemcpyHostToDevice, stream);
   if (e != cudaSuccess) return cuda_error_status(e);

@@ -71,20 +71,20 @@ __host__ __device__ constexpr int stream_max_rg(int mp) { return mp <= 2 ? 8 : m
 __host__ __device__ constexpr int stream_part_bytes(int mp) { return 2 * stream_max_rg(mp) * kStreamConsumers * 32 * mp * 4; }
 
 // Shared memory of one thread block: ring | barriers (full and empty per
-// slot, three pairs per layer parity) and two layer records (one per layer
-// parity, 32 bytes each) | two partial-sum buffers | one or two
-// staged-activation buffers (rows and group sums; the rest of the block's
-// shared memory, up to kStreamSmem).
+// slot, three pairs per layer parity, the consumer warps' staging barrier and
+// a spare word) and two layer records (one per layer parity, 32 bytes each) |
+// two partial-sum buffers | one or two staged-activation buffers (rows and
+// group sums; the rest of the block's shared memory, up to kStreamSmem).
 __host__ __device__ constexpr int stream_bar_off(int bits, int gs) {
   return stream_slots(bits, gs) * stream_slot_bytes(bits, gs);
 }
 // after the barriers (16-byte aligned): the two layer records
 constexpr int kStreamRecBytes = 32;
 __host__ __device__ constexpr int stream_rec_off(int bits, int gs) {
-  return stream_bar_off(bits, gs) + (2 * stream_slots(bits, gs) + 6) * 8;
+  return stream_bar_off(bits, gs) + (2 * stream_slots(bits, gs) + 8) * 8;
 }
 __host__ __device__ constexpr int stream_part_off(int bits, int gs) {
-  return stream_bar_off(bits, gs) + stream_align128((2 * stream_slots(bits, gs) + 6) * 8 + 2 * kStreamRecBytes);
+  return stream_bar_off(bits, gs) + stream_align128((2 * stream_slots(bits, gs) + 8) * 8 + 2 * kStreamRecBytes);
 }
 __host__ __device__ constexpr int stream_x_off(int bits, int gs, int mp) {
   return stream_part_off(bits, gs) + stream_part_bytes(mp);

@@ -107,6 +107,9 @@ SIGNATURES = {
     "w4a16_gemm": (ctypes.c_int, [_FP, _P, _SZ, _P, _P, _I64, _P, _SZ, _P]),
     "w4a16_gemm_ex": (ctypes.c_int, [_FP, _P, _SZ, _P, _P, _I64, _P, _SZ, _I32, _I32, _P]),
     "w4a16_pipeline_timeouts": (ctypes.c_int, [ctypes.POINTER(ctypes.c_uint32)]),
+    "w4a16_set_wait_limit_ns": (ctypes.c_uint64, [ctypes.c_uint64]),
+    "w4a16_debug_fail_next_launch": (None, [ctypes.c_int]),
+    "w4a16_debug_check_word": (ctypes.c_int, [ctypes.POINTER(ctypes.c_uint32)]),
     "w4a16_chain_workspace_bytes": (_SZ, [_FP, _I32, _I64]),
     "w4a16_gptq_workspace_bytes": (_SZ, [_FP]),
     "w4a16_gemv_grouped": (ctypes.c_int, [_FP, ctypes.POINTER(ctypes.c_void_p), ctypes.POINTER(ctypes.c_size_t),
@@ -421,6 +424,27 @@ def pipeline_timeouts() -> int:
     c = ctypes.c_uint32(0)
     _check("w4a16_pipeline_timeouts", lib().w4a16_pipeline_timeouts(ctypes.byref(c)))
     return int(c.value)
+
+
+def set_wait_limit_ns(ns: int) -> int:
+    """Limit of the kernels' bounded waits for later launches (0: the 1 s default); returns the previous one."""
+    return int(lib().w4a16_set_wait_limit_ns(int(ns)))
+
+
+def debug_fail_next_launch(error: int) -> None:
+    """Test hook: the next launching call returns W4A16_ERR_CUDA with this cudaError_t (0 clears)."""
+    lib().w4a16_debug_fail_next_launch(int(error))
+
+
+def debug_check_word():
+    """First failed index check since the last call (0: none), read and reset;
+    None when the loaded library is not the debug build."""
+    w = ctypes.c_uint32(0)
+    st = lib().w4a16_debug_check_word(ctypes.byref(w))
+    if st == 2:  # W4A16_ERR_UNSUPPORTED: built without the checks
+        return None
+    _check("w4a16_debug_check_word", st)
+    return int(w.value)
 
 
 def linear(fmt: Format, packed: torch.Tensor, x: torch.Tensor, out=None, workspace=None, stream=None):
