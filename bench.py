@@ -65,7 +65,7 @@ FALLBACK_BF16_TFLOPS = 1800.0
 # the headline kernel of each schedule on the Llama-2-7B sweep (4-bit codes),
 # {schedule: {"source_sha1", "bytes_per_launch"}}; valid only for the kernel
 # sources it was taken on (GEMV_SOURCES).
-GEMV_TRAFFIC = {}
+GEMV_TRAFFIC = {"stream": {"source_sha1": "f2656f40e3303e161d563e9d52319be0ac4aa840", "bytes_per_launch": 3364728576 + 5539840}}
 SCHEDULE_TEXT = {
     "stream": ("stream: the step is one persistent launch of the chained decode product (decode_stream_kernel); "
                "each GEMV reads its own precomputed activations, so none waits for another"),
@@ -97,6 +97,8 @@ def parse_args():
     p.add_argument("--schedule", default="stream", choices=list(SCHEDULES),
                    help="headline schedule: one persistent launch per step (without or with the decoder's "
                         "dependencies), grouped launches, or one launch per GEMV")
+    p.add_argument("--schedules", default=",".join(SCHEDULES),
+                   help="comma-separated schedules to capture and time (the headline one is always included)")
     p.add_argument("--no-extra", action="store_true",
                    help="skip the other workloads (single linear, 8192x8192 sweep, 70B stream)")
     p.add_argument("--profile-case", choices=["gemv", "gemm", "stream"], default=None)
@@ -365,7 +367,9 @@ def run_ours(args, rank, world, local_rank):
         return
 
     layers, xs, ys, yall = build_stack(torch, W, synth, dev, args.workload, args.bits)
-    step = time_stack(torch, W, dev, layers, xs, ys, yall, args, dist, world, local_rank)
+    wanted = [x for x in args.schedules.split(",") if x]
+    scheds = tuple(x for x in SCHEDULES if x == args.schedule or x in wanted)
+    step = time_stack(torch, W, dev, layers, xs, ys, yall, args, dist, world, local_rank, schedules=scheds)
     shapes = None if args.no_shapes else per_shape(torch, W, layers, xs, dev)
     del layers, xs, ys, yall
     torch.cuda.synchronize()
