@@ -355,18 +355,53 @@ __device__ __forceinline__ void compute_unit(const UnitRegs<GS, BITS>& r, const 
           mma_16816(acc[ph][tt][nb], af, bx[j][nb].x, bx[j][nb].y, fresh ? zero4 : acc[ph][tt][nb]);
       }
       const bool group_end = (GS == 32) ? (j == 1 || j == 3) : (j == 3 && bb == U::kBlocks - 1);
-      if (group_end) {
+      if (XSUM && group_end) {
+        // tot += s * (2^k acc - z xs) per row, 2^k undoing the accumulator's
+        // scale (2^24; 2^20 for the high-nibble rows of 4-bit codes). The zero
+        // point enters as f = 2^23 + z, exact from its bits with one OR, and
+        // -z xs = fma(f, -xs, 2^23 xs) with one rounding.
+        const int gg = (GS == 32) ? (j >> 1) : 0;
+        constexpr float kA = 16777216.f;
+        constexpr float kB = BITS == 4 ? 1048576.f : 16777216.f;
+        constexpr float kSymZero = float(1 << (BITS - 1));
+        float xs[NB][2], x23[NB][2];
+#pragma unroll
+        for (int nb = 0; nb < NB; ++nb)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            xs[nb][e] = xsg[gg][nb][e];
+            x23[nb][e] = SYM ? -kSymZero * xs[nb][e] : xs[nb][e] * 8388608.f;
+          }
+#pragma unroll
+        for (int tt = 0; tt < kTilesPerWarp; ++tt) {
+          float a2[NB][4];
+#pragma unroll
+          for (int nb = 0; nb < NB; ++nb)
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              a2[nb][i] = SPLIT ? acc[0][tt][nb][i] + acc[NS - 1][tt][nb][i] : acc[0][tt][nb][i];
+          const float2 sf = __half22float2(*reinterpret_cast<const __half2*>(&r.s[gg][tt]));
+          const uint32_t zr = r.z[gg][tt];
+          const float fg = __uint_as_float(0x4B000000u | (BITS != 8 ? (zr & 0xFu) : (zr & 0xFFu)));
+          const float fh = __uint_as_float(0x4B000000u | (BITS != 8 ? ((zr >> 4) & 0xFu) : ((zr >> 8) & 0xFFu)));
+#pragma unroll
+          for (int nb = 0; nb < NB; ++nb)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              if (ONE && (nb > 0 || e > 0)) continue;  // a single token: elements 0 and 2 only
+              const float zg = SYM ? x23[nb][e] : fmaf(fg, -xs[nb][e], x23[nb][e]);
+              const float zh = SYM ? x23[nb][e] : fmaf(fh, -xs[nb][e], x23[nb][e]);
+              tot[tt][nb][e] = fmaf(sf.x, fmaf(a2[nb][e], kA, zg), tot[tt][nb][e]);
+              tot[tt][nb][e + 2] = fmaf(sf.y, fmaf(a2[nb][e + 2], kB, zh), tot[tt][nb][e + 2]);
+            }
+        }
+      } else if (group_end) {
         const int gg = (GS == 32) ? (j >> 1) : 0;
         float c2[NB][4];
 #pragma unroll
         for (int nb = 0; nb < NB; ++nb) {
-          if (XSUM) {
-            c2[nb][0] = c2[nb][2] = xsg[gg][nb][0] * 5.9604644775390625e-8f;  // 2^-24
-            c2[nb][1] = c2[nb][3] = xsg[gg][nb][1] * 5.9604644775390625e-8f;
-          } else {
 #pragma unroll
-            for (int i = 0; i < 4; ++i) c2[nb][i] = SPLIT ? cx[0][nb][i] + cx[NS - 1][nb][i] : cx[0][nb][i];
-          }
+          for (int i = 0; i < 4; ++i) c2[nb][i] = SPLIT ? cx[0][nb][i] + cx[NS - 1][nb][i] : cx[0][nb][i];
         }
 #pragma unroll
         for (int tt = 0; tt < kTilesPerWarp; ++tt) {
@@ -377,12 +412,7 @@ __device__ __forceinline__ void compute_unit(const UnitRegs<GS, BITS>& r, const 
             for (int i = 0; i < 4; ++i)
               a2[nb][i] = SPLIT ? acc[0][tt][nb][i] + acc[NS - 1][tt][nb][i] : acc[0][tt][nb][i];
           const GroupFactors f = make_factors<SYM, BITS>(r.s[gg][tt], r.z[gg][tt]);
-          if (ONE) {
-            tot[tt][0][0] = fmaf(f.sa, a2[0][0], fmaf(f.za, c2[0][0], tot[tt][0][0]));
-            tot[tt][0][2] = fmaf(f.sb, a2[0][2], fmaf(f.zb, c2[0][2], tot[tt][0][2]));
-          } else {
-            finalize<NB>(a2, c2, f, tot[tt]);
-          }
+          finalize<NB>(a2, c2, f, tot[tt]);
         }
       }
     }
