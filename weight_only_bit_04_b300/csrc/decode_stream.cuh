@@ -260,6 +260,91 @@ __device__ __forceinline__ void stage_sums(int K, int M, const uint16_t* xs, flo
   }
 }
 
+// NU units of one warp multiplied together, 16-column step by 16-column step
+// (compute_unit's arithmetic with the group sums from the caller): NU times
+// the independent MMA chains between dependent operations. xo[u]: column of
+// unit u's first activation; xsg[u]: its group sums.
+template <int NU, int NB, int GS, bool SYM, int BITS, bool ONE>
+__device__ __forceinline__ void compute_units(const UnitRegs<GS, BITS> (&r)[NU], const uint16_t* xl0,
+                                              const uint16_t* xl1, const int (&xo)[NU],
+                                              const float (&xsg)[NU][Unit<GS>::kGroups][NB][2],
+                                              float tot[kTilesPerWarp][NB][4]) {
+  using U = Unit<GS>;
+  constexpr bool SPLIT = BITS == 4;  // even and odd steps in separate accumulators
+  constexpr int NS = SPLIT ? 2 : 1;
+  const float zero4[4] = {0.f, 0.f, 0.f, 0.f};
+  float acc[NU][NS][kTilesPerWarp][NB][4];
+#pragma unroll
+  for (int bb = 0; bb < U::kBlocks; ++bb) {
+    uint2 bx[NU][4][NB];
+#pragma unroll
+    for (int u = 0; u < NU; ++u)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int off = xo[u] + bb * 64 + j * 16;
+        bx[u][j][0] = ld_x<kXShared>(xl0 + off);
+        if (NB > 1) bx[u][j][NB - 1] = ld_x<kXShared>(xl1 + off);
+      }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int ph = SPLIT ? (j & 1) : 0;
+      const bool fresh = SPLIT ? ((GS == 32) ? true : (j < 2 && bb == 0))
+                               : ((GS == 32) ? (j == 0 || j == 2) : (j == 0 && bb == 0));
+#pragma unroll
+      for (int u = 0; u < NU; ++u)
+#pragma unroll
+        for (int tt = 0; tt < kTilesPerWarp; ++tt) {
+          uint32_t af[4];
+          extract_step<BITS>(r[u].w[bb], tt, j, af);
+#pragma unroll
+          for (int nb = 0; nb < NB; ++nb)
+            mma_16816(acc[u][ph][tt][nb], af, bx[u][j][nb].x, bx[u][j][nb].y, fresh ? zero4 : acc[u][ph][tt][nb]);
+        }
+      const bool group_end = (GS == 32) ? (j == 1 || j == 3) : (j == 3 && bb == U::kBlocks - 1);
+      if (group_end) {
+        // tot += s * (2^k acc - z xs) per row, as in compute_unit
+        const int gg = (GS == 32) ? (j >> 1) : 0;
+        constexpr float kA = 16777216.f;
+        constexpr float kB = BITS == 4 ? 1048576.f : 16777216.f;
+        constexpr float kSymZero = float(1 << (BITS - 1));
+#pragma unroll
+        for (int u = 0; u < NU; ++u) {
+          float xs[NB][2], x23[NB][2];
+#pragma unroll
+          for (int nb = 0; nb < NB; ++nb)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              xs[nb][e] = xsg[u][gg][nb][e];
+              x23[nb][e] = SYM ? -kSymZero * xs[nb][e] : xs[nb][e] * 8388608.f;
+            }
+#pragma unroll
+          for (int tt = 0; tt < kTilesPerWarp; ++tt) {
+            const float2 sf = __half22float2(*reinterpret_cast<const __half2*>(&r[u].s[gg][tt]));
+            const uint32_t zr = r[u].z[gg][tt];
+            const float fg = __uint_as_float(0x4B000000u | (BITS != 8 ? (zr & 0xFu) : (zr & 0xFFu)));
+            const float fh = __uint_as_float(0x4B000000u | (BITS != 8 ? ((zr >> 4) & 0xFu) : ((zr >> 8) & 0xFFu)));
+#pragma unroll
+            for (int nb = 0; nb < NB; ++nb)
+#pragma unroll
+              for (int e = 0; e < 2; ++e) {
+                if (ONE && (nb > 0 || e > 0)) continue;
+                float a_g = acc[u][0][tt][nb][e], a_h = acc[u][0][tt][nb][e + 2];
+                if (SPLIT) {
+                  a_g += acc[u][NS - 1][tt][nb][e];
+                  a_h += acc[u][NS - 1][tt][nb][e + 2];
+                }
+                const float zg = SYM ? x23[nb][e] : fmaf(fg, -xs[nb][e], x23[nb][e]);
+                const float zh = SYM ? x23[nb][e] : fmaf(fh, -xs[nb][e], x23[nb][e]);
+                tot[tt][nb][e] = fmaf(sf.x, fmaf(a_g, kA, zg), tot[tt][nb][e]);
+                tot[tt][nb][e + 2] = fmaf(sf.y, fmaf(a_h, kB, zh), tot[tt][nb][e + 2]);
+              }
+          }
+        }
+      }
+    }
+  }
+}
+
 template <int MP, int GS, bool SYM, int BITS, bool XS>
 __global__ void __launch_bounds__(kStreamThreads, 1) decode_stream_kernel(const StreamLaunch c) {
   using SG = SGeo<BITS, GS>;
@@ -755,8 +840,27 @@ __global__ void __launch_bounds__(kStreamThreads, 1) decode_stream_kernel(const 
           UnitIn in[SG::UPW];
 #pragma unroll
           for (int i = 0; i < SG::UPW; ++i) load_unit_in(sb, warp * SG::UPW + i, ku0 + i, in[i]);
+          if (XS) {
+            UnitRegs<GS, BITS> rr[SG::UPW];
+            float xg[SG::UPW][SG::GU][NB][2];
+            int xo[SG::UPW];
 #pragma unroll
-          for (int i = 0; i < SG::UPW; ++i) compute_in(in[i], ku0 + i);
+            for (int i = 0; i < SG::UPW; ++i) {
+              rr[i] = in[i].r;
+              xo[i] = (ku0 + i) * SG::UB * kColsPerBlock;
+#pragma unroll
+              for (int gg = 0; gg < SG::GU; ++gg)
+#pragma unroll
+                for (int nb = 0; nb < NB; ++nb) {
+                  xg[i][gg][nb][0] = in[i].xsg[gg][nb][0];
+                  xg[i][gg][nb][1] = in[i].xsg[gg][nb][1];
+                }
+            }
+            compute_units<SG::UPW, NB, GS, SYM, BITS, MP == 1>(rr, xl0, xl1, xo, xg, tot);
+          } else {
+#pragma unroll
+            for (int i = 0; i < SG::UPW; ++i) compute_in(in[i], ku0 + i);
+          }
         } else {
           int rgl = rgl0, ku = ku0;
 #pragma unroll
