@@ -91,7 +91,7 @@ struct Span {
 };
 
 // What the consumer warps need of layer j, written by the dependency warp
-// into shared memory (record j & 1) before it publishes the layer.
+// into shared memory (record j % stream_part_depth) before it publishes the layer.
 struct alignas(16) LayerRec {
   const uint16_t* x;  // activations in global memory
   int K;
@@ -177,11 +177,12 @@ __device__ __forceinline__ bool warp_outcome(int st) {
   if (timed && (threadIdx.x & 31) == 0) atomicAdd(&g_gemv_timeouts, 1u);
   return !bad;
 }
-// Whole-warp wait for layer j's phase of a per-layer barrier pair (barrier
-// j & 1, parity (j >> 1) & 1); layers below 0 are complete.
-__device__ __forceinline__ bool wait_layer(uint32_t pair0, int j, Guard& gd) {
+// Whole-warp wait for layer j's phase of a set of D per-layer barriers
+// (barrier j % D, parity (j / D) & 1); layers below 0 are complete.
+template <int D = 2>
+__device__ __forceinline__ bool wait_layer(uint32_t bar0, int j, Guard& gd) {
   if (j < 0) return true;
-  return warp_outcome(wait_mbar(pair0 + 8 * (j & 1), uint32_t(j >> 1) & 1u, gd));
+  return warp_outcome(wait_mbar(bar0 + 8 * (j % D), uint32_t(j / D) & 1u, gd));
 }
 
 // cp.async of 16 bytes, and the arrival on an mbarrier once this thread's
@@ -356,22 +357,37 @@ __global__ void __launch_bounds__(kStreamThreads, 1) decode_stream_kernel(const 
   constexpr int RGMAX = stream_max_rg(MP);
   extern __shared__ __align__(1024) unsigned char smem[];
   const uint32_t ring = smem_addr(smem);
-  // mbarriers: full[S], empty[S] (the ring), the consumer warps' staging
-  // barrier after the per-layer ones, and per layer parity (j & 1):
-  // cdone (the consumer warps have written layer j's partial sums), rdy (layer
-  // j's activations may be read), fdone (the finishing warp has read layer j's
-  // partial sums). Phase (j >> 1) & 1 of barrier j & 1 is layer j's; no role
-  // runs far enough ahead of another for that to be ambiguous (see the waits
-  // below).
+  // mbarriers: full[S], empty[S] (the ring); per layer slot (layer j uses
+  // slot j % PD, PD = stream_part_depth(MP)): cdone (the consumer warps have
+  // written layer j's partial sums, in partial buffer j % PD), rdy (layer j's
+  // activations and record j % PD may be read), fdone (the finishing warp has
+  // read layer j's partial sums); then the consumer warps' staging barrier.
+  // Layer j's phase is phase (j / PD) & 1 of its slot's barrier. It is never
+  // ambiguous: a waiter on a set has seen layer j - PD's phase of the same
+  // barrier before it waits for layer j's, and no barrier completes layer
+  // j + PD's phase before every waiter has seen layer j's:
+  //  * rdy: consumers wait in layer order; the dependency warp publishes
+  //    j + PD only after cdone(j), i.e. after every consumer warp saw rdy(j);
+  //  * cdone: the finishing warp waits in layer order; the dependency warp
+  //    waits for cdone(j - PD) before publishing j, and for cdone(l) of a
+  //    staged buffer's last reader l in (j - 1 - PD, j) (it has seen
+  //    cdone(l - PD) one publication earlier). The consumers complete
+  //    cdone(j + PD) only after rdy(j + PD), which the dependency warp
+  //    publishes after fdone(j) (the finishing warp saw cdone(j)) and once it
+  //    is past every such wait;
+  //  * fdone: the dependency warp waits in layer order (fdone(j - PD) before
+  //    publishing j); the finishing warp completes fdone(j + PD) only after
+  //    cdone(j + PD), after rdy(j + PD), published after fdone(j) was seen.
   const uint32_t full0 = ring + stream_bar_off(BITS, GS);
   const uint32_t empty0 = full0 + S * 8;
-  const uint32_t cdone0 = empty0 + S * 8;
-  const uint32_t rdy0 = cdone0 + 16;
-  const uint32_t fdone0 = rdy0 + 16;
-  const uint32_t stg = fdone0 + 16;  // the consumer warps' staging barrier
+  constexpr int PD = stream_part_depth(MP);  // partial buffers; cdone and fdone barriers
+  const uint32_t cdone0 = empty0 + S * 8;   // 4 words
+  const uint32_t rdy0 = cdone0 + 32;        // 4 words
+  const uint32_t fdone0 = rdy0 + 32;        // 4 words
+  const uint32_t stg = fdone0 + 32;         // the consumer warps' staging barrier
   float* part = reinterpret_cast<float*>(smem + stream_part_off(BITS, GS));  // [2][RGMAX][NW][32 rows][MP]
   unsigned char* xbase = smem + stream_x_off(BITS, GS, MP);  // staged-activation buffers (XS)
-  LayerRec* rec = reinterpret_cast<LayerRec*>(smem + stream_rec_off(BITS, GS));  // per layer parity
+  LayerRec* rec = reinterpret_cast<LayerRec*>(smem + stream_rec_off(BITS, GS));  // per layer slot
 
   const int tid = int(threadIdx.x);
   const int warp = tid >> 5, lane = tid & 31;
@@ -387,7 +403,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1) decode_stream_kernel(const 
       mbar_init(full0 + 8 * s, 33);  // lane 0's expect_tx arrival + one cp.async arrival per producer lane
       mbar_init(empty0 + 8 * s, NW);
     }
-    for (int q = 0; q < 2; ++q) {
+    for (int q = 0; q < PD; ++q) {
       mbar_init(cdone0 + 8 * q, NW);
       mbar_init(rdy0 + 8 * q, 1);
       mbar_init(fdone0 + 8 * q, 1);
@@ -530,10 +546,9 @@ __global__ void __launch_bounds__(kStreamThreads, 1) decode_stream_kernel(const 
       const StreamJob J = Jn;
       if (j + 1 < nj) Jn = load_job(c.jobs, j + 1);
       // This warp publishes layer j only once every consumer warp has finished
-      // layer j - 2 (so that no per-layer barrier has two phases of one parity
-      // in flight); before that it already polls layer j's dependencies and
-      // stages its activations when their buffer is free.
-      bool seen2 = false;  // layer j - 2's consumer barrier observed in this iteration
+      // layer j - PD (see the barrier comments above); before that it already
+      // polls layer j's dependencies and stages its activations when their
+      // buffer is free.
       bool fresh = false;  // a dependency of this layer was acquired just now
       int xmode = 0;
       if (J.wait_lo <= J.wait_hi && J.wait_hi > known) {
@@ -559,16 +574,12 @@ __global__ void __launch_bounds__(kStreamThreads, 1) decode_stream_kernel(const 
         if (XS) {
           if (stale || J.x != loaded || J.K != loaded_k) {
             // the other buffer when there are two. Its last reader finished
-            // if that was layer j - 3 or earlier (this warp saw layer j - 3's
-            // consumer barrier one layer ago); layers j - 2 and j - 1 are
-            // waited for here, in order.
+            // if that was layer j - 1 - PD or earlier (this warp saw that
+            // layer's consumer barrier one publication ago); a later last
+            // reader is waited for here.
             const int nb = c.x_nbuf == 2 ? cur ^ 1 : 0;
             const int lu = nb ? last_use1 : last_use0;
-            if (lu >= j - 2) {
-              if (!wait_layer(cdone0, j - 2, gd)) return;
-              seen2 = true;
-            }
-            if (lu == j - 1 && !wait_layer(cdone0, j - 1, gd)) return;
+            if (lu > j - 1 - PD && !wait_layer<PD>(cdone0, lu, gd)) return;
             cur = nb;
             uint16_t* xs = reinterpret_cast<uint16_t*>(xbase + size_t(nb) * c.x_buf_bytes);
             if (!W4A16_CHECK(stream_x_buf(J.K, M, GS) <= c.x_buf_bytes &&
@@ -600,9 +611,9 @@ __global__ void __launch_bounds__(kStreamThreads, 1) decode_stream_kernel(const 
           for (int off = lane * 128; off < bytes; off += 32 * 128) prefetch_l1(xb + off);
         }
       }
-      if (!seen2 && !wait_layer(cdone0, j - 2, gd)) return;  // also frees record j & 1
-      // and the finishing warp has read layer j - 2's partial sums (buffer j & 1)
-      if (!wait_layer(fdone0, j - 2, gd)) return;
+      if (!wait_layer<PD>(cdone0, j - PD, gd)) return;  // frees record j % PD
+      // and the finishing warp has read layer j - PD's partial sums (buffer j % PD)
+      if (!wait_layer<PD>(fdone0, j - PD, gd)) return;
       __syncwarp();
       if (lane == 0) {
         LayerRec r;
@@ -612,8 +623,8 @@ __global__ void __launch_bounds__(kStreamThreads, 1) decode_stream_kernel(const 
         r.NU = s.NU;
         r.xsel = cur * c.x_buf_bytes + xmode;
         r.pad[0] = r.pad[1] = 0;
-        rec[j & 1] = r;
-        mbar_arrive(rdy0 + 8 * (j & 1));  // release: the staged rows, sums and the record
+        rec[j % PD] = r;
+        mbar_arrive(rdy0 + 8 * (j % PD));  // release: the staged rows, sums and the record
       }
     }
     return;
@@ -624,15 +635,15 @@ __global__ void __launch_bounds__(kStreamThreads, 1) decode_stream_kernel(const 
     for (int j = 0; j < nj; ++j) {
       const StreamJob J = Jn;
       if (j + 1 < nj) Jn = load_job(c.jobs, j + 1);
-      // the consumers cannot finish layer j + 2 before this warp is done with layer j
-      if (!wait_layer(cdone0, j, gd)) return;
+      // the consumers cannot finish layer j + PD before this warp is done with layer j
+      if (!wait_layer<PD>(cdone0, j, gd)) return;
       const Span s = span_of(J, P, b, SG::UB);
       // Row `lane` of each owned row group, every token: the partial sums in
       // warp order (deterministic), kept in registers so that the partial
       // buffer is released before the stores and the fence.
       float acc[RGMAX][MP];
       if (s.n > 0) {
-        const float* pb = part + size_t(j & 1) * RGMAX * NW * 32 * MP;
+        const float* pb = part + size_t(j % PD) * RGMAX * NW * 32 * MP;
 #pragma unroll
         for (int rgl = 0; rgl < RGMAX; ++rgl) {
           if (rgl >= s.n) break;
@@ -654,7 +665,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1) decode_stream_kernel(const 
         }
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(fdone0 + 8 * (j & 1));  // partial buffer j & 1 is free
+      if (lane == 0) mbar_arrive(fdone0 + 8 * (j % PD));  // partial buffer j % PD is free
       if (s.n > 0) {
 #pragma unroll
         for (int rgl = 0; rgl < RGMAX; ++rgl) {
@@ -695,14 +706,13 @@ __global__ void __launch_bounds__(kStreamThreads, 1) decode_stream_kernel(const 
   };
   for (int j = 0; j < nj; ++j) {
     // Layer j's activations are readable, and (the dependency warp waited for
-    // it before publishing layer j) the finishing warp has read layer j - 2's
-    // partial sums, so partial buffer j & 1 is free. Every warp waits in every
-    // layer, with or without units in it, so that no warp runs two layers
-    // ahead of the dependency and finishing warps: each per-layer barrier
-    // then has at most one phase of its parity in flight.
-    if (!rdy_ready && !wait_layer(rdy0, j, gd)) return;
+    // it before publishing layer j) the finishing warp has read layer j - PD's
+    // partial sums, so partial buffer j % PD is free. Every warp waits in
+    // every layer, with or without units in it, so that no warp runs ahead of
+    // the dependency warp's publication (see the barrier comments above).
+    if (!rdy_ready && !wait_layer<PD>(rdy0, j, gd)) return;
     rdy_ready = false;
-    const LayerRec L = rec[j & 1];
+    const LayerRec L = rec[j % PD];
     if (XS && (L.xsel & kConsumersStage)) {
       // a dependency was just acquired: the consumer warps stage the
       // activations together (the dependency warp's acquire happens before
@@ -731,7 +741,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1) decode_stream_kernel(const 
         xl0 = L.x + size_t(tok0) * L.K + 4 * t;
         xl1 = L.x + size_t(tok1) * L.K + 4 * t;
       }
-      float* pb = part + size_t(j & 1) * RGMAX * NW * 32 * MP;
+      float* pb = part + size_t(j % PD) * RGMAX * NW * 32 * MP;
       float tot[kTilesPerWarp][NB][4];
       int cur = -1;
       auto flush = [&](int rgl) {
@@ -822,7 +832,8 @@ __global__ void __launch_bounds__(kStreamThreads, 1) decode_stream_kernel(const 
           ready = mbar_test_wait(full0 + 8 * ns, ns == 0 ? phase ^ 1u : phase);
         }
         // in the layer's last slot, the next layer's ready barrier likewise
-        if (k == R - 1 && j + 1 < nj) rdy_ready = mbar_test_wait(rdy0 + 8 * ((j + 1) & 1), uint32_t((j + 1) >> 1) & 1u);
+        if (k == R - 1 && j + 1 < nj)
+          rdy_ready = mbar_test_wait(rdy0 + 8 * ((j + 1) % PD), uint32_t((j + 1) / PD) & 1u);
         const unsigned char* sb = smem + size_t(slot) * SG::kSlot;
         if (k * CU + (warp + 1) * SG::UPW <= s.T && ku0 + SG::UPW <= s.NU) {
           // common case: all of the warp's units exist and lie in one row
@@ -902,7 +913,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1) decode_stream_kernel(const 
       if (cur >= 0) flush(cur);
     }
     __syncwarp();
-    if (lane == 0) mbar_arrive(cdone0 + 8 * (j & 1));
+    if (lane == 0) mbar_arrive(cdone0 + 8 * (j % PD));
   }
 }
 

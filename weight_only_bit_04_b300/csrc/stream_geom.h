@@ -66,25 +66,35 @@ __host__ __device__ constexpr int stream_slots(int bits, int gs) {
 __host__ __device__ constexpr int stream_mp(int M) { return M <= 1 ? 1 : M <= 2 ? 2 : M <= 4 ? 4 : M <= 8 ? 8 : 16; }
 // Row groups one thread block may own in one layer slice; larger layers are
 // cut into slices. Each owned row group has one partial-sum entry per consumer
-// warp (32 rows x MP tokens of fp32), in two buffers (consecutive slices).
+// warp (32 rows x MP tokens of fp32), in stream_part_depth buffers (slice j
+// uses buffer j % depth): four at one token, two otherwise. The same depth
+// sets how far the dependency warp may publish ahead of the consumer warps.
 __host__ __device__ constexpr int stream_max_rg(int mp) { return mp <= 2 ? 8 : mp == 4 ? 4 : mp == 8 ? 2 : 1; }
-__host__ __device__ constexpr int stream_part_bytes(int mp) { return 2 * stream_max_rg(mp) * kStreamConsumers * 32 * mp * 4; }
+__host__ __device__ constexpr int stream_part_depth(int mp) { return mp == 1 ? 4 : 2; }
+__host__ __device__ constexpr int stream_part_bytes(int mp) {
+  return stream_part_depth(mp) * stream_max_rg(mp) * kStreamConsumers * 32 * mp * 4;
+}
 
 // Shared memory of one thread block: ring | barriers (full and empty per
-// slot, three pairs per layer parity, the consumer warps' staging barrier and
-// a spare word) and two layer records (one per layer parity, 32 bytes each) |
-// two partial-sum buffers | one or two staged-activation buffers (rows and
-// group sums; the rest of the block's shared memory, up to kStreamSmem).
+// slot; consumer-done, ready and finishing-done per layer slot, four words
+// each; the consumer warps' staging barrier; a spare word) and four layer
+// records (32 bytes each) | the partial-sum buffers | one or two
+// staged-activation buffers (rows and group sums; the rest of the block's
+// shared memory, up to kStreamSmem). Layer j uses layer slot j % depth
+// (stream_part_depth) of each per-layer set.
+constexpr int kStreamLayerBars = 14;  // 4 cdone + 4 rdy + 4 fdone + staging + spare
+constexpr int kStreamRecs = 4;
 __host__ __device__ constexpr int stream_bar_off(int bits, int gs) {
   return stream_slots(bits, gs) * stream_slot_bytes(bits, gs);
 }
 // after the barriers (16-byte aligned): the two layer records
 constexpr int kStreamRecBytes = 32;
 __host__ __device__ constexpr int stream_rec_off(int bits, int gs) {
-  return stream_bar_off(bits, gs) + (2 * stream_slots(bits, gs) + 8) * 8;
+  return stream_bar_off(bits, gs) + (2 * stream_slots(bits, gs) + kStreamLayerBars) * 8;
 }
 __host__ __device__ constexpr int stream_part_off(int bits, int gs) {
-  return stream_bar_off(bits, gs) + stream_align128((2 * stream_slots(bits, gs) + 8) * 8 + 2 * kStreamRecBytes);
+  return stream_bar_off(bits, gs) +
+         stream_align128((2 * stream_slots(bits, gs) + kStreamLayerBars) * 8 + kStreamRecs * kStreamRecBytes);
 }
 __host__ __device__ constexpr int stream_x_off(int bits, int gs, int mp) {
   return stream_part_off(bits, gs) + stream_part_bytes(mp);
