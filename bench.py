@@ -307,6 +307,14 @@ def build_stack(torch, W, synth, dev, workload, bits=4):
     return layers, xs, ys, yall
 
 
+def warm_graph(torch, graph, stream, reps):
+    """Untimed replays on the timing stream, finished before the timed region starts."""
+    with torch.cuda.stream(stream):
+        for _ in range(reps):
+            graph.replay()
+    torch.cuda.synchronize()
+
+
 def time_graph(torch, graph, stream, reps):
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
@@ -341,9 +349,7 @@ def per_shape(torch, W, layers, xs, dev):
         with torch.cuda.graph(g, stream=stream):
             for lins in layers:
                 W.gemv(fmt, lins[j][2], xs[fmt.K], out=y, weights_ready=True)
-        for _ in range(3):
-            g.replay()
-        torch.cuda.synchronize()
+        warm_graph(torch, g, stream, 3)
         ms = time_graph(torch, g, stream, 20) / len(layers)
         nb = gemv_bytes(fmt.N, fmt.K, bits=fmt.bits)
         res[key] = {"us": round(ms * 1e3, 2), "GB/s": round(nb / (ms * 1e-3) / 1e9, 1), "linears": name}
@@ -527,9 +533,7 @@ def time_stack(torch, W, dev, layers, xs, ys, yall, args, dist, world, local_ran
     # Warm-up, then exactly `steps` timed replays, barrier + synchronize on
     # both sides; clocks sampled from before the warm-up, kept for the timed region.
     with ClockSampler(torch, dev) as clk:
-        for _ in range(args.warmup):
-            graph.replay()
-        torch.cuda.synchronize()
+        warm_graph(torch, graph, stream, args.warmup)
         if dist:
             dist.barrier()
         clk.timed = True
@@ -540,14 +544,12 @@ def time_stack(torch, W, dev, layers, xs, ys, yall, args, dist, world, local_ran
     ms = max_over_ranks(torch, dist, ms, dev)
     value = world * step_bytes / (ms * 1e-3) / 1e9
     results = {head: {"ms_per_step": round(ms, 4), "GB/s": round(step_bytes / (ms * 1e-3) / 1e9, 1)}}
-    # The other schedules, each after 30 warm-up replays and over at least 100
-    # (the waiting schedules take about 30 replays to settle after another one).
+    # The other schedules, each over at least 100 replays after its warm-up.
     for schedule in schedules:
         if schedule == head:
             continue
         g = graphs[schedule]
-        for _ in range(max(args.warmup, 30)):
-            g.replay()
+        warm_graph(torch, g, stream, args.warmup)
         sms = time_graph(torch, g, stream, max(args.steps, 100))
         results[schedule] = {"ms_per_step": round(sms, 4), "GB/s": round(step_bytes / (sms * 1e-3) / 1e9, 1)}
     for name in chains:
@@ -746,8 +748,7 @@ def sweep8192_rows(torch, W, synth, dev, variants=False):
         with torch.cuda.graph(g, stream=stream):
             for p in packs:
                 W.gemv(fmt, p, x, out=y, weights_ready=True)
-        for _ in range(3):
-            g.replay()
+        warm_graph(torch, g, stream, 3)
         ms = time_graph(torch, g, stream, 20) / copies
         del g
         return ms
