@@ -65,7 +65,7 @@ FALLBACK_BF16_TFLOPS = 1800.0
 # the headline kernel of each schedule on the Llama-2-7B sweep (4-bit codes),
 # {schedule: {"source_sha1", "bytes_per_launch"}}; valid only for the kernel
 # sources it was taken on (GEMV_SOURCES).
-GEMV_TRAFFIC = {"stream": {"source_sha1": "f2656f40e3303e161d563e9d52319be0ac4aa840", "bytes_per_launch": 3364728576 + 5539840}}
+GEMV_TRAFFIC = {"stream": {"source_sha1": "e3d418539abf045bc91d61d3ac7d09e275eb3bea", "bytes_per_launch": 3364724736 + 5540096}}
 SCHEDULE_TEXT = {
     "stream": ("stream: the step is one persistent launch of the chained decode product (decode_stream_kernel); "
                "each GEMV reads its own precomputed activations, so none waits for another"),
