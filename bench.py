@@ -560,35 +560,88 @@ def time_stack(torch, W, dev, layers, xs, ys, yall, args, dist, world, local_ran
 
     e2e_rec = None
     if e2e:
-        # End to end through the public API with host buffers: pinned inputs
-        # copied in, the step, every output copied back, all inside the timed region.
-        x_host = {K: x.cpu().pin_memory() for K, x in xs.items()}
-        y_host = torch.empty(yall.shape, dtype=yall.dtype).pin_memory()
-        h2d = sum(x.numel() * x.element_size() for x in x_host.values())
-        d2h = y_host.numel() * y_host.element_size()
+        e2e_rec = time_e2e(torch, W, dev, layers, xs, ys, yall, graph, chains.get(head), head, stream, step_bytes,
+                           args, dist, world)
+    del graph, graphs, chains
+    return {"ms": ms, "value": value, "step_bytes": step_bytes, "n_launch": n_launch, "n_layers": len(layers),
+            "schedules": results, "clocks": clk.summary(), "e2e": e2e_rec}
 
-        def e2e_step():
+
+def time_e2e(torch, W, dev, layers, xs, ys, yall, graph, chain, head, stream, step_bytes, args, dist, world):
+    """End to end through the public API with host buffers: every step copies
+    its inputs in from pinned host memory, runs, and copies every output back
+    to pinned host memory, all inside the timed region. For the one-launch
+    schedules the steps are pipelined over two output buffers: step i's
+    readback (a copy stream) overlaps step i + 1's compute, which is how a
+    server streams independent steps; the per-launch schedules run one step at
+    a time."""
+    x_host = {K: x.cpu().pin_memory() for K, x in xs.items()}
+    h2d = sum(x.numel() * x.element_size() for x in x_host.values())
+    d2h = yall.numel() * yall.element_size()
+    if chain is None:
+        y_host = torch.empty(yall.shape, dtype=yall.dtype).pin_memory()
+
+        def e2e_step(i):
             with torch.cuda.stream(stream):
                 for K, x in xs.items():
                     x.copy_(x_host[K], non_blocking=True)
                 graph.replay()
                 y_host.copy_(yall, non_blocking=True)
             stream.synchronize()
+        overlap = "none: inputs in, the step, outputs out, then a host synchronization, every step"
+    else:
+        # a second output buffer and its own chained launch
+        yall2 = torch.empty_like(yall)
+        ys2, off = [], 0
+        for row in ys:
+            r2 = []
+            for y in row:
+                r2.append(yall2[off:off + y.shape[1]].view(1, y.shape[1]))
+                off += y.shape[1]
+            ys2.append(r2)
+        chain2 = chain_of(W, layers, xs, ys2, head == "chain")
+        with torch.cuda.stream(stream):
+            chain2.run(stream)
+        torch.cuda.synchronize()
+        graph2 = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph2, stream=stream):
+            chain2.run(stream)
+        torch.cuda.synchronize()
+        graphs2, youts = (graph, graph2), (yall, yall2)
+        y_host = [torch.empty(yall.shape, dtype=yall.dtype).pin_memory() for _ in range(2)]
+        copy_stream = torch.cuda.Stream(device=dev)
+        computed = [torch.cuda.Event(), torch.cuda.Event()]
+        copied = [torch.cuda.Event(), torch.cuda.Event()]
 
-        for _ in range(args.warmup):
-            e2e_step()
-        if dist:
-            dist.barrier()
-        t0 = time.perf_counter()
-        for _ in range(args.steps):
-            e2e_step()
-        e2e_ms = (time.perf_counter() - t0) * 1e3 / args.steps
-        e2e_ms = max_over_ranks(torch, dist, e2e_ms, dev)
-        e2e_rec = {"value": round(world * step_bytes / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
-                   "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)}
-    del graph, graphs, chains
-    return {"ms": ms, "value": value, "step_bytes": step_bytes, "n_launch": n_launch, "n_layers": len(layers),
-            "schedules": results, "clocks": clk.summary(), "e2e": e2e_rec}
+        def e2e_step(i):
+            b = i & 1
+            with torch.cuda.stream(stream):
+                stream.wait_event(copied[b])  # buffer b's previous readback is done
+                for K, x in xs.items():
+                    x.copy_(x_host[K], non_blocking=True)
+                graphs2[b].replay()
+                computed[b].record(stream)
+            with torch.cuda.stream(copy_stream):
+                copy_stream.wait_event(computed[b])
+                y_host[b].copy_(youts[b], non_blocking=True)
+                copied[b].record(copy_stream)
+        overlap = ("step i's output readback (copy stream) overlaps step i+1's compute over two output "
+                   "buffers; every step's input and output copies are inside the timed region")
+
+    for i in range(args.warmup):
+        e2e_step(i)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        e2e_step(i)
+    torch.cuda.synchronize()
+    e2e_ms = (time.perf_counter() - t0) * 1e3 / args.steps
+    e2e_ms = max_over_ranks(torch, dist, e2e_ms, dev)
+    return {"value": round(world * step_bytes / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4),
+            "overlap": overlap}
 
 
 def run_70b(torch, W, synth, dev, args, dist, world, local_rank):
