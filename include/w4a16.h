@@ -376,8 +376,8 @@ typedef struct {
   int64_t M;
   int64_t n_slices;  /* entries of the slice table (>= n_layers) */
   int32_t blocks;    /* thread blocks (SMs of the device) the table was planned for */
-  int32_t flags;     /* set by prepare for run: activation buffers in shared memory (0, 1 or 2) */
-  int32_t reserved_x;/* set by prepare for run: bytes of one such buffer */
+  int32_t flags;     /* set by prepare for run: activation buffers in shared memory (0 or 2) */
+  int32_t reserved_x;/* set by prepare for run: bytes of the area the two buffers share */
   int32_t reserved;
 } w4a16_chain_info;
 

@@ -178,15 +178,17 @@ w4a16_status w4a16_chain_prepare(const w4a16_format* formats, const w4a16_chain_
   info->M = M;
   info->n_slices = n_slices;
   info->blocks = int32_t(P);
-  // Staged activations: one buffer big enough for every layer; two when they
-  // fit (the next layer's activations then land while this one computes).
+  // Staged activations when every layer's fit the block's activation area:
+  // two buffers, one from each end of the area, each sized for the layer it
+  // holds (the next layer's activations land while this one computes unless
+  // the two layers' together exceed the area).
   long long xbuf = 0;
   for (int32_t i = 0; i < n_layers; ++i)
     xbuf = std::max(xbuf, stream_x_buf(formats[i].K, int(M), formats[0].group_size));
   const long long xroom = stream_x_bytes(formats[0].bits, formats[0].group_size, stream_mp(int(M)));
-  const int32_t nbuf = 2 * xbuf <= xroom ? 2 : xbuf <= xroom ? 1 : 0;
+  const int32_t nbuf = xbuf <= xroom ? 2 : 0;
   info->flags = nbuf;            // staged-activation buffers (0: read through L1)
-  info->reserved_x = int32_t(xbuf);
+  info->reserved_x = nbuf ? int32_t(xroom) : 0;
   return W4A16_OK;
 }
 

@@ -540,8 +540,11 @@ __global__ void __launch_bounds__(kStreamThreads, 1) decode_stream_kernel(const 
     bool stale = true;  // the staged activations may be out of date
     const uint16_t* loaded = nullptr;
     int loaded_k = 0;
-    int cur = 0;                    // buffer holding the current activations
+    int cur = 0;                         // buffer holding the current activations
     int last_use0 = -1, last_use1 = -1;  // last layer that read buffer 0 / 1
+    // bytes in use: buffer 0 holds [0, size0) of the area, buffer 1 [room - size1, room)
+    const int room = c.x_buf_bytes;
+    int size0 = 0, size1 = 0;
     for (int j = 0; j < nj; ++j) {
       const StreamJob J = Jn;
       if (j + 1 < nj) Jn = load_job(c.jobs, j + 1);
@@ -573,17 +576,26 @@ __global__ void __launch_bounds__(kStreamThreads, 1) decode_stream_kernel(const 
       if (s.n > 0) {
         if (XS) {
           if (stale || J.x != loaded || J.K != loaded_k) {
-            // the other buffer when there are two. Its last reader finished
-            // if that was layer j - 1 - PD or earlier (this warp saw that
-            // layer's consumer barrier one publication ago); a later last
-            // reader is waited for here.
-            const int nb = c.x_nbuf == 2 ? cur ^ 1 : 0;
+            // the other buffer. Its last reader finished if that was layer
+            // j - 1 - PD or earlier (this warp saw that layer's consumer
+            // barrier one publication ago); a later last reader is waited for
+            // here, and so is the current buffer's when the two layers'
+            // activations do not fit in the area together.
+            const int nb = cur ^ 1;
+            const int sz = int(stream_x_buf(J.K, M, GS));
             const int lu = nb ? last_use1 : last_use0;
             if (lu > j - 1 - PD && !wait_layer<PD>(cdone0, lu, gd)) return;
+            const int lo = nb ? last_use0 : last_use1;
+            const bool overlap = nb ? room - sz < size0 : sz > room - size1;
+            if (overlap && lo > j - 1 - PD && !wait_layer<PD>(cdone0, lo, gd)) return;
             cur = nb;
-            uint16_t* xs = reinterpret_cast<uint16_t*>(xbase + size_t(nb) * c.x_buf_bytes);
-            if (!W4A16_CHECK(stream_x_buf(J.K, M, GS) <= c.x_buf_bytes &&
-                                 stream_x_off(BITS, GS, MP) + int64_t(nb + 1) * c.x_buf_bytes <= kStreamSmem,
+            if (nb)
+              size1 = sz;
+            else
+              size0 = sz;
+            const int xoff = nb ? room - sz : 0;
+            uint16_t* xs = reinterpret_cast<uint16_t*>(xbase + xoff);
+            if (!W4A16_CHECK(xoff >= 0 && xoff + sz <= room && stream_x_off(BITS, GS, MP) + room <= kStreamSmem,
                              0x202u))
               return;
             if (!fresh) {
@@ -621,7 +633,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1) decode_stream_kernel(const 
         r.K = J.K;
         r.T = s.T;
         r.NU = s.NU;
-        r.xsel = cur * c.x_buf_bytes + xmode;
+        r.xsel = (cur ? room - size1 : 0) + xmode;
         r.pad[0] = r.pad[1] = 0;
         rec[j % PD] = r;
         mbar_arrive(rdy0 + 8 * (j % PD));  // release: the staged rows, sums and the record

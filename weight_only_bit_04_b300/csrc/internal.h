@@ -118,8 +118,9 @@ struct StreamLaunch {
   const CUtensorMap* maps;  // device array, 64-byte aligned
   unsigned int* done;       // per slice a count of finished blocks (128-byte stride), then the abort flag
   int n_jobs, M;
-  int x_buf_bytes;          // bytes of one staged-activation buffer (0: activations not staged)
-  int x_nbuf;               // staged-activation buffers, 1 or 2
+  int x_buf_bytes;          // bytes of the staged-activation area (0: activations not staged)
+  int x_nbuf;               // 2: two staged-activation buffers, the first at the start of the area
+                            // and the second ending at its end, each sized for its layer; 0: none
   unsigned long long wait_ns;  // limit of every bounded wait (wait_limit_ns() at launch)
 };
 cudaError_t launch_stream(const StreamLaunch& c, int bits, int gsize, bool sym, int sm_count, cudaStream_t stream);

@@ -69,7 +69,7 @@ __host__ __device__ constexpr int stream_mp(int M) { return M <= 1 ? 1 : M <= 2 
 // warp (32 rows x MP tokens of fp32), in stream_part_depth buffers (slice j
 // uses buffer j % depth): four at one token, two otherwise. The same depth
 // sets how far the dependency warp may publish ahead of the consumer warps.
-__host__ __device__ constexpr int stream_max_rg(int mp) { return mp <= 2 ? 8 : mp == 4 ? 4 : mp == 8 ? 2 : 1; }
+__host__ __device__ constexpr int stream_max_rg(int mp) { return mp == 1 ? 4 : mp == 2 ? 8 : mp == 4 ? 4 : mp == 8 ? 2 : 1; }
 __host__ __device__ constexpr int stream_part_depth(int mp) { return mp == 1 ? 4 : 2; }
 __host__ __device__ constexpr int stream_part_bytes(int mp) {
   return stream_part_depth(mp) * stream_max_rg(mp) * kStreamConsumers * 32 * mp * 4;
