@@ -472,34 +472,63 @@ __global__ void __launch_bounds__(kStreamThreads, 1) decode_stream_kernel(const 
         }
         // scales (SG::kScaleChunks 16-byte pieces per unit) and zero points
         // (SG::kZeroChunks per unit): unit d of the slot is (rgl0, ku0 + d),
-        // wrapping into the following row groups
-        for (int q = lane; q < nu_slot * SG::kScaleChunks; q += 32) {
-          const int d = q / SG::kScaleChunks, p = q - d * SG::kScaleChunks;
-          int ku = ku0 + d, rg = s.rg0 + rgl0;
-          while (ku >= NU) {
-            ku -= NU;
-            ++rg;
+        // wrapping into the following row groups. A row group's scales of
+        // one group are 64 contiguous bytes (its two 16-row tiles in the row
+        // block's [group][16-row tile] order), those of the next group
+        // kMetaGroupStride entries further on.
+        if (NU >= CU) {
+          // at most one row-group boundary in the slot: units d < dx lie in
+          // row group rg, the rest in rg + 1; an entry is a per-slot base plus
+          // a lane constant
+          const int rg = s.rg0 + rgl0, dx = NU - ku0;
+          const int64_t eA = (int64_t(rg >> 2) * G) * 64 + (rg & 3) * 16 + int64_t(ku0) * SG::GU * 64;
+          const int64_t eB = (int64_t((rg + 1) >> 2) * G) * 64 + ((rg + 1) & 3) * 16 +
+                             int64_t(ku0 - NU) * SG::GU * 64;
+          for (int q = lane; q < nu_slot * SG::kScaleChunks; q += 32) {
+            const int d = q / SG::kScaleChunks, p = q % SG::kScaleChunks;
+            const int64_t e = (d < dx ? eA : eB) + (d * SG::GU + (p >> 2)) * 64 + (p & 3) * 4;
+            const int dst = SG::kScaleOff + (d * SG::GU + (p >> 2)) * 64 + (p & 3) * 16;
+            if (W4A16_CHECK(e + 4 <= nmeta && dst + 16 <= SG::kZeroOff, 0x102u)) cp_async_16_cg(sb + dst, sc_base + e);
           }
-          // row group rg's scales of one group: 64 contiguous bytes (its
-          // two 16-row tiles in the row block's [group][16-row tile] order)
-          const int gg = p >> 2;
-          const int64_t e = meta_index(rg >> 2, ku * SG::GU + gg, 2 * (rg & 3), 0, G) + (p & 3) * 4;
-          const int dst = SG::kScaleOff + (d * SG::GU + gg) * 64 + (p & 3) * 16;
-          if (W4A16_CHECK(e + 4 <= nmeta && dst + 16 <= SG::kZeroOff, 0x102u)) cp_async_16_cg(sb + dst, sc_base + e);
-        }
-        if (!SYM) {
-          for (int q = lane; q < nu_slot * SG::kZeroChunks; q += 32) {
-            const int d = q / SG::kZeroChunks, p = q - d * SG::kZeroChunks;
+          if (!SYM) {
+            constexpr int ZC = SG::ZB / 16;  // 16-byte pieces of a row group's zero points of one group
+            for (int q = lane; q < nu_slot * SG::kZeroChunks; q += 32) {
+              const int d = q / SG::kZeroChunks, p = q % SG::kZeroChunks;
+              const int gg = p / ZC, h = p % ZC;
+              const int64_t e = ((d < dx ? eA : eB) + (d * SG::GU + gg) * 64) * ZC + h * 16;
+              const int dst = SG::kZeroOff + (d * SG::GU + gg) * SG::ZB + h * 16;
+              if (W4A16_CHECK(e + 16 <= nmeta * ZC && dst + 16 <= SG::kSlot, 0x103u))
+                cp_async_16_cg(sb + dst, z_base + e);
+            }
+          }
+        } else {
+          // short row groups (fewer units than a slot): walk each unit's row group
+          for (int q = lane; q < nu_slot * SG::kScaleChunks; q += 32) {
+            const int d = q / SG::kScaleChunks, p = q - d * SG::kScaleChunks;
             int ku = ku0 + d, rg = s.rg0 + rgl0;
             while (ku >= NU) {
               ku -= NU;
               ++rg;
             }
-            const int gg = p / (SG::ZB / 16), h = p - gg * (SG::ZB / 16);
-            const int64_t e = meta_index(rg >> 2, ku * SG::GU + gg, 2 * (rg & 3), 0, G) * (SG::ZB / 16) + h * 16;
-            const int dst = SG::kZeroOff + (d * SG::GU + gg) * SG::ZB + h * 16;
-            if (W4A16_CHECK(e + 16 <= nmeta * (SG::ZB / 16) && dst + 16 <= SG::kSlot, 0x103u))
-              cp_async_16_cg(sb + dst, z_base + e);
+            const int gg = p >> 2;
+            const int64_t e = meta_index(rg >> 2, ku * SG::GU + gg, 2 * (rg & 3), 0, G) + (p & 3) * 4;
+            const int dst = SG::kScaleOff + (d * SG::GU + gg) * 64 + (p & 3) * 16;
+            if (W4A16_CHECK(e + 4 <= nmeta && dst + 16 <= SG::kZeroOff, 0x102u)) cp_async_16_cg(sb + dst, sc_base + e);
+          }
+          if (!SYM) {
+            for (int q = lane; q < nu_slot * SG::kZeroChunks; q += 32) {
+              const int d = q / SG::kZeroChunks, p = q - d * SG::kZeroChunks;
+              int ku = ku0 + d, rg = s.rg0 + rgl0;
+              while (ku >= NU) {
+                ku -= NU;
+                ++rg;
+              }
+              const int gg = p / (SG::ZB / 16), h = p - gg * (SG::ZB / 16);
+              const int64_t e = meta_index(rg >> 2, ku * SG::GU + gg, 2 * (rg & 3), 0, G) * (SG::ZB / 16) + h * 16;
+              const int dst = SG::kZeroOff + (d * SG::GU + gg) * SG::ZB + h * 16;
+              if (W4A16_CHECK(e + 16 <= nmeta * (SG::ZB / 16) && dst + 16 <= SG::kSlot, 0x103u))
+                cp_async_16_cg(sb + dst, z_base + e);
+            }
           }
         }
         cp_async_arrive_noinc(full);

@@ -87,7 +87,7 @@ constexpr int kStreamRecs = 4;
 __host__ __device__ constexpr int stream_bar_off(int bits, int gs) {
   return stream_slots(bits, gs) * stream_slot_bytes(bits, gs);
 }
-// after the barriers (16-byte aligned): the two layer records
+// after the barriers (16-byte aligned): the kStreamRecs layer records
 constexpr int kStreamRecBytes = 32;
 __host__ __device__ constexpr int stream_rec_off(int bits, int gs) {
   return stream_bar_off(bits, gs) + (2 * stream_slots(bits, gs) + kStreamLayerBars) * 8;
