@@ -64,8 +64,9 @@ FALLBACK_BF16_TFLOPS = 1800.0
 # ncu DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) per launch of
 # the headline kernel of each schedule on the Llama-2-7B sweep (4-bit codes),
 # {schedule: {"source_sha1", "bytes_per_launch"}}; valid only for the kernel
-# sources it was taken on (GEMV_SOURCES).
-GEMV_TRAFFIC = {"stream": {"source_sha1": "e3d418539abf045bc91d61d3ac7d09e275eb3bea", "bytes_per_launch": 3364724736 + 5540096}}
+# sources it was taken on (STREAM_SOURCES for the stream and chain schedules,
+# GEMV_SOURCES for the others).
+GEMV_TRAFFIC = {"stream": {"source_sha1": "370108c0893914aca4db57e37be0be715c3c5f1d", "bytes_per_launch": 3364779264 + 5534720}}
 SCHEDULE_TEXT = {
     "stream": ("stream: the step is one persistent launch of the chained decode product (decode_stream_kernel); "
                "each GEMV reads its own precomputed activations, so none waits for another"),
