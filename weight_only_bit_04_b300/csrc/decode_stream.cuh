@@ -355,6 +355,8 @@ __global__ void __launch_bounds__(kStreamThreads, 1) decode_stream_kernel(const 
   constexpr int CU = SG::CU;
   constexpr int CS = kStreamCounterStride;
   constexpr int RGMAX = stream_max_rg(MP);
+  // ring, barriers, records and partial-sum buffers within the block's shared memory
+  static_assert(stream_x_off(BITS, GS, MP) <= kStreamSmem, "the stream's shared-memory layout does not fit");
   extern __shared__ __align__(1024) unsigned char smem[];
   const uint32_t ring = smem_addr(smem);
   // mbarriers: full[S], empty[S] (the ring); per layer slot (layer j uses
