@@ -20,7 +20,9 @@
 //    8 KiB copies tops out near 4 TB/s and one of 16 KiB copies near
 //    6.8 TB/s, so copies must be large. The slot's scales and zero points
 //    (64 and 16 bytes per group and row group) come by cp.async from the
-//    producer warp's lanes, which keeps small copies off the TMA unit.
+//    lanes of a second producer warp (the metadata warp), which keeps small
+//    copies off the TMA unit and their instructions off the sub-partition
+//    of the warp issuing the codes.
 //    Weights never depend on earlier layers, so the producer runs ahead
 //    across dependency waits for as long as the ring has room.
 //  * Eight consumer warps share every slot, one unit each (two for narrow
@@ -402,7 +404,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1) decode_stream_kernel(const 
 
   if (tid == 0) {
     for (int s = 0; s < S; ++s) {
-      mbar_init(full0 + 8 * s, 33);  // lane 0's expect_tx arrival + one cp.async arrival per producer lane
+      mbar_init(full0 + 8 * s, 33);  // the codes warp's expect_tx arrival + one cp.async arrival per metadata-warp lane
       mbar_init(empty0 + 8 * s, NW);
     }
     for (int q = 0; q < PD; ++q) {
@@ -419,9 +421,14 @@ __global__ void __launch_bounds__(kStreamThreads, 1) decode_stream_kernel(const 
   // layer ahead so that its latency hides behind the current layer.
   StreamJob Jn = load_job(c.jobs, 0);
 
-  if (warp == NW) {
-    // ---------------- producer warp: lane 0 issues the TMA copies of the codes,
-    // every lane copies its share of the scales and zero points
+  if (warp == NW || warp == NW + 3) {
+    // ---------------- producer warps, walking the ring together: in the codes
+    // warp lane 0 issues the TMA copies of the codes; every lane of the
+    // metadata warp copies its share of the scales and zero points. The two
+    // sit on different SM sub-partitions, each beside two consumer warps
+    // (one warp doing both measured slower on B300: its sub-partition issued
+    // ~20 % more instructions than the others).
+    const bool codes = warp == NW;
     int slot = 0;
     uint32_t phase = 0;
     int issued = 0;  // slots filled (for the drain after an abort)
@@ -447,8 +454,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1) decode_stream_kernel(const 
         const uint32_t full = full0 + 8 * slot;
         const uint32_t sb = ring + uint32_t(slot) * SG::kSlot;
         const int nu_slot = min(CU, s.T - k * CU);
-        // the codes first (most of the bytes), then the scales and zero points
-        if (lane == 0) {
+        if (codes && lane == 0) {
           mbar_arrive_expect_tx(full, uint32_t(nu_slot) * SG::kUnitCode);
           int rg = s.rg0 + rgl0, ku = ku0, d = 0;
           while (d < nu_slot) {
@@ -472,68 +478,70 @@ __global__ void __launch_bounds__(kStreamThreads, 1) decode_stream_kernel(const 
             }
           }
         }
-        // scales (SG::kScaleChunks 16-byte pieces per unit) and zero points
-        // (SG::kZeroChunks per unit): unit d of the slot is (rgl0, ku0 + d),
-        // wrapping into the following row groups. A row group's scales of
-        // one group are 64 contiguous bytes (its two 16-row tiles in the row
-        // block's [group][16-row tile] order), those of the next group
-        // kMetaGroupStride entries further on.
-        if (NU >= CU) {
-          // at most one row-group boundary in the slot: units d < dx lie in
-          // row group rg, the rest in rg + 1; an entry is a per-slot base plus
-          // a lane constant
-          const int rg = s.rg0 + rgl0, dx = NU - ku0;
-          const int64_t eA = (int64_t(rg >> 2) * G) * 64 + (rg & 3) * 16 + int64_t(ku0) * SG::GU * 64;
-          const int64_t eB = (int64_t((rg + 1) >> 2) * G) * 64 + ((rg + 1) & 3) * 16 +
-                             int64_t(ku0 - NU) * SG::GU * 64;
-          for (int q = lane; q < nu_slot * SG::kScaleChunks; q += 32) {
-            const int d = q / SG::kScaleChunks, p = q % SG::kScaleChunks;
-            const int64_t e = (d < dx ? eA : eB) + (d * SG::GU + (p >> 2)) * 64 + (p & 3) * 4;
-            const int dst = SG::kScaleOff + (d * SG::GU + (p >> 2)) * 64 + (p & 3) * 16;
-            if (W4A16_CHECK(e + 4 <= nmeta && dst + 16 <= SG::kZeroOff, 0x102u)) cp_async_16_cg(sb + dst, sc_base + e);
-          }
-          if (!SYM) {
-            constexpr int ZC = SG::ZB / 16;  // 16-byte pieces of a row group's zero points of one group
-            for (int q = lane; q < nu_slot * SG::kZeroChunks; q += 32) {
-              const int d = q / SG::kZeroChunks, p = q % SG::kZeroChunks;
-              const int gg = p / ZC, h = p % ZC;
-              const int64_t e = ((d < dx ? eA : eB) + (d * SG::GU + gg) * 64) * ZC + h * 16;
-              const int dst = SG::kZeroOff + (d * SG::GU + gg) * SG::ZB + h * 16;
-              if (W4A16_CHECK(e + 16 <= nmeta * ZC && dst + 16 <= SG::kSlot, 0x103u))
-                cp_async_16_cg(sb + dst, z_base + e);
+        if (!codes) {
+          // scales (SG::kScaleChunks 16-byte pieces per unit) and zero points
+          // (SG::kZeroChunks per unit): unit d of the slot is (rgl0, ku0 + d),
+          // wrapping into the following row groups. A row group's scales of
+          // one group are 64 contiguous bytes (its two 16-row tiles in the row
+          // block's [group][16-row tile] order), those of the next group
+          // kMetaGroupStride entries further on.
+          if (NU >= CU) {
+            // at most one row-group boundary in the slot: units d < dx lie in
+            // row group rg, the rest in rg + 1; an entry is a per-slot base plus
+            // a lane constant
+            const int rg = s.rg0 + rgl0, dx = NU - ku0;
+            const int64_t eA = (int64_t(rg >> 2) * G) * 64 + (rg & 3) * 16 + int64_t(ku0) * SG::GU * 64;
+            const int64_t eB = (int64_t((rg + 1) >> 2) * G) * 64 + ((rg + 1) & 3) * 16 +
+                               int64_t(ku0 - NU) * SG::GU * 64;
+            for (int q = lane; q < nu_slot * SG::kScaleChunks; q += 32) {
+              const int d = q / SG::kScaleChunks, p = q % SG::kScaleChunks;
+              const int64_t e = (d < dx ? eA : eB) + (d * SG::GU + (p >> 2)) * 64 + (p & 3) * 4;
+              const int dst = SG::kScaleOff + (d * SG::GU + (p >> 2)) * 64 + (p & 3) * 16;
+              if (W4A16_CHECK(e + 4 <= nmeta && dst + 16 <= SG::kZeroOff, 0x102u)) cp_async_16_cg(sb + dst, sc_base + e);
             }
-          }
-        } else {
-          // short row groups (fewer units than a slot): walk each unit's row group
-          for (int q = lane; q < nu_slot * SG::kScaleChunks; q += 32) {
-            const int d = q / SG::kScaleChunks, p = q - d * SG::kScaleChunks;
-            int ku = ku0 + d, rg = s.rg0 + rgl0;
-            while (ku >= NU) {
-              ku -= NU;
-              ++rg;
+            if (!SYM) {
+              constexpr int ZC = SG::ZB / 16;  // 16-byte pieces of a row group's zero points of one group
+              for (int q = lane; q < nu_slot * SG::kZeroChunks; q += 32) {
+                const int d = q / SG::kZeroChunks, p = q % SG::kZeroChunks;
+                const int gg = p / ZC, h = p % ZC;
+                const int64_t e = ((d < dx ? eA : eB) + (d * SG::GU + gg) * 64) * ZC + h * 16;
+                const int dst = SG::kZeroOff + (d * SG::GU + gg) * SG::ZB + h * 16;
+                if (W4A16_CHECK(e + 16 <= nmeta * ZC && dst + 16 <= SG::kSlot, 0x103u))
+                  cp_async_16_cg(sb + dst, z_base + e);
+              }
             }
-            const int gg = p >> 2;
-            const int64_t e = meta_index(rg >> 2, ku * SG::GU + gg, 2 * (rg & 3), 0, G) + (p & 3) * 4;
-            const int dst = SG::kScaleOff + (d * SG::GU + gg) * 64 + (p & 3) * 16;
-            if (W4A16_CHECK(e + 4 <= nmeta && dst + 16 <= SG::kZeroOff, 0x102u)) cp_async_16_cg(sb + dst, sc_base + e);
-          }
-          if (!SYM) {
-            for (int q = lane; q < nu_slot * SG::kZeroChunks; q += 32) {
-              const int d = q / SG::kZeroChunks, p = q - d * SG::kZeroChunks;
+          } else {
+            // short row groups (fewer units than a slot): walk each unit's row group
+            for (int q = lane; q < nu_slot * SG::kScaleChunks; q += 32) {
+              const int d = q / SG::kScaleChunks, p = q - d * SG::kScaleChunks;
               int ku = ku0 + d, rg = s.rg0 + rgl0;
               while (ku >= NU) {
                 ku -= NU;
                 ++rg;
               }
-              const int gg = p / (SG::ZB / 16), h = p - gg * (SG::ZB / 16);
-              const int64_t e = meta_index(rg >> 2, ku * SG::GU + gg, 2 * (rg & 3), 0, G) * (SG::ZB / 16) + h * 16;
-              const int dst = SG::kZeroOff + (d * SG::GU + gg) * SG::ZB + h * 16;
-              if (W4A16_CHECK(e + 16 <= nmeta * (SG::ZB / 16) && dst + 16 <= SG::kSlot, 0x103u))
-                cp_async_16_cg(sb + dst, z_base + e);
+              const int gg = p >> 2;
+              const int64_t e = meta_index(rg >> 2, ku * SG::GU + gg, 2 * (rg & 3), 0, G) + (p & 3) * 4;
+              const int dst = SG::kScaleOff + (d * SG::GU + gg) * 64 + (p & 3) * 16;
+              if (W4A16_CHECK(e + 4 <= nmeta && dst + 16 <= SG::kZeroOff, 0x102u)) cp_async_16_cg(sb + dst, sc_base + e);
+            }
+            if (!SYM) {
+              for (int q = lane; q < nu_slot * SG::kZeroChunks; q += 32) {
+                const int d = q / SG::kZeroChunks, p = q - d * SG::kZeroChunks;
+                int ku = ku0 + d, rg = s.rg0 + rgl0;
+                while (ku >= NU) {
+                  ku -= NU;
+                  ++rg;
+                }
+                const int gg = p / (SG::ZB / 16), h = p - gg * (SG::ZB / 16);
+                const int64_t e = meta_index(rg >> 2, ku * SG::GU + gg, 2 * (rg & 3), 0, G) * (SG::ZB / 16) + h * 16;
+                const int dst = SG::kZeroOff + (d * SG::GU + gg) * SG::ZB + h * 16;
+                if (W4A16_CHECK(e + 16 <= nmeta * (SG::ZB / 16) && dst + 16 <= SG::kSlot, 0x103u))
+                  cp_async_16_cg(sb + dst, z_base + e);
+              }
             }
           }
+          cp_async_arrive_noinc(full);
         }
-        cp_async_arrive_noinc(full);
         ++issued;
         if (++slot == S) {
           slot = 0;
@@ -547,7 +555,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1) decode_stream_kernel(const 
       }
     }
     cp_async_wait_all();
-    if (lane == 0) {
+    if (codes && lane == 0) {
       // Let the TMA copies in flight land before the block can exit: the last
       // min(issued, S) fills, each in its own slot. After a normal run every
       // one has been consumed and each test returns at once; after an abort

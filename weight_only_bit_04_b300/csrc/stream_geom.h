@@ -21,7 +21,7 @@
 namespace w4a16 {
 
 constexpr int kStreamConsumers = 8;  // consumer warps per thread block
-constexpr int kStreamWarps = kStreamConsumers + 3;  // + producer, dependency and finishing warps
+constexpr int kStreamWarps = kStreamConsumers + 4;  // + codes, dependency, finishing and metadata warps
 constexpr int kStreamThreads = kStreamWarps * 32;
 constexpr int kStreamCounterStride = 32;  // 32-bit words between completion counters (one 128-byte line each)
 constexpr int kStreamSmem = 227 * 1024;  // shared memory of one thread block (the opt-in maximum)
