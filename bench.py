@@ -572,10 +572,10 @@ def time_e2e(torch, W, dev, layers, xs, ys, yall, graph, chain, head, stream, st
     """End to end through the public API with host buffers: every step copies
     its inputs in from pinned host memory, runs, and copies every output back
     to pinned host memory, all inside the timed region. For the one-launch
-    schedules the steps are pipelined over two output buffers: step i's
-    readback (a copy stream) overlaps step i + 1's compute, which is how a
-    server streams independent steps; the per-launch schedules run one step at
-    a time."""
+    schedules the steps are pipelined over two input and two output buffers:
+    step i + 1's inputs load (an input stream) and step i - 1's outputs read
+    back (a copy stream) while step i computes, which is how a server streams
+    independent steps; the per-launch schedules run one step at a time."""
     x_host = {K: x.cpu().pin_memory() for K, x in xs.items()}
     h2d = sum(x.numel() * x.element_size() for x in x_host.values())
     d2h = yall.numel() * yall.element_size()
@@ -591,7 +591,10 @@ def time_e2e(torch, W, dev, layers, xs, ys, yall, graph, chain, head, stream, st
             stream.synchronize()
         overlap = "none: inputs in, the step, outputs out, then a host synchronization, every step"
     else:
-        # a second output buffer and its own chained launch
+        # a second input and output buffer set and its own chained launch
+        xs2 = {K: torch.empty_like(x) for K, x in xs.items()}
+        for K in xs:
+            xs2[K].copy_(xs[K])
         yall2 = torch.empty_like(yall)
         ys2, off = [], 0
         for row in ys:
@@ -600,7 +603,7 @@ def time_e2e(torch, W, dev, layers, xs, ys, yall, graph, chain, head, stream, st
                 r2.append(yall2[off:off + y.shape[1]].view(1, y.shape[1]))
                 off += y.shape[1]
             ys2.append(r2)
-        chain2 = chain_of(W, layers, xs, ys2, head == "chain")
+        chain2 = chain_of(W, layers, xs2, ys2, head == "chain")
         with torch.cuda.stream(stream):
             chain2.run(stream)
         torch.cuda.synchronize()
@@ -608,26 +611,33 @@ def time_e2e(torch, W, dev, layers, xs, ys, yall, graph, chain, head, stream, st
         with torch.cuda.graph(graph2, stream=stream):
             chain2.run(stream)
         torch.cuda.synchronize()
-        graphs2, youts = (graph, graph2), (yall, yall2)
+        graphs2, xins, youts = (graph, graph2), (xs, xs2), (yall, yall2)
         y_host = [torch.empty(yall.shape, dtype=yall.dtype).pin_memory() for _ in range(2)]
+        in_stream = torch.cuda.Stream(device=dev)
         copy_stream = torch.cuda.Stream(device=dev)
+        loaded = [torch.cuda.Event(), torch.cuda.Event()]
         computed = [torch.cuda.Event(), torch.cuda.Event()]
         copied = [torch.cuda.Event(), torch.cuda.Event()]
 
         def e2e_step(i):
             b = i & 1
-            with torch.cuda.stream(stream):
-                stream.wait_event(copied[b])  # buffer b's previous readback is done
-                for K, x in xs.items():
+            with torch.cuda.stream(in_stream):
+                in_stream.wait_event(computed[b])  # step i - 2 has read input set b
+                for K, x in xins[b].items():
                     x.copy_(x_host[K], non_blocking=True)
+                loaded[b].record(in_stream)
+            with torch.cuda.stream(stream):
+                stream.wait_event(loaded[b])
+                stream.wait_event(copied[b])  # output set b of step i - 2 is read back
                 graphs2[b].replay()
                 computed[b].record(stream)
             with torch.cuda.stream(copy_stream):
                 copy_stream.wait_event(computed[b])
                 y_host[b].copy_(youts[b], non_blocking=True)
                 copied[b].record(copy_stream)
-        overlap = ("step i's output readback (copy stream) overlaps step i+1's compute over two output "
-                   "buffers; every step's input and output copies are inside the timed region")
+        overlap = ("two input and two output buffer sets: step i+1's inputs load (input stream) and step "
+                   "i-1's outputs read back (copy stream) while step i computes; every step's input and "
+                   "output copies are inside the timed region")
 
     for i in range(args.warmup):
         e2e_step(i)
