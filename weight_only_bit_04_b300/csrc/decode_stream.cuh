@@ -14,7 +14,7 @@
 //    the step within about 1 %.
 //  * A producer warp streams the block's units -- codes, scales and zero
 //    points of one row group over 64 or 128 columns -- layer after layer into
-//    a ring of shared-memory slots of about 16 KiB of codes each. The codes
+//    a ring of shared-memory slots of up to 32 KiB of codes each. The codes
 //    of a slot come by TMA (3-D tensor maps over the blob, no multicast) in
 //    one copy, or a few at a row group's end: measured on B300, a stream of
 //    8 KiB copies tops out near 4 TB/s and one of 16 KiB copies near
@@ -22,15 +22,16 @@
 //    (64 and 16 bytes per group and row group) come by cp.async from the
 //    lanes of a second producer warp (the metadata warp), which keeps small
 //    copies off the TMA unit and their instructions off the sub-partition
-//    of the warp issuing the codes.
-//    Weights never depend on earlier layers, so the producer runs ahead
-//    across dependency waits for as long as the ring has room.
-//  * Eight consumer warps share every slot, one unit each (two for narrow
-//    units). Per unit a warp expands the codes into m16n8k16 fragments in
-//    registers and multiplies them on the tensor cores with the activations
-//    (tokens in the n dimension), as the single-layer product does
-//    (gemv_impl.cuh, compute_unit). Each warp keeps one partial sum per row
-//    group and writes it to shared memory.
+//    of the warp issuing the codes. Weights never depend on earlier layers,
+//    so the producers run ahead across dependency waits for as long as the
+//    ring has room.
+//  * Eight consumer warps share every slot, one, two or four units each
+//    (stream_upw: the most that keep a slot within 32 KiB of codes), all
+//    loaded before any is multiplied. Per unit a warp expands the codes into
+//    m16n8k16 fragments in registers and multiplies them on the tensor cores
+//    with the activations (tokens in the n dimension), as the single-layer
+//    product does (gemv_impl.cuh, compute_unit). Each warp keeps one partial
+//    sum per row group and writes it to shared memory.
 //  * A finishing warp adds a row group's partial sums in warp order
 //    (deterministic), releases the partial buffer to the consumers, rounds
 //    to fp16 and writes y. When a later layer waits for this one, it then
