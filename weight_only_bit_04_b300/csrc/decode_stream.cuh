@@ -309,7 +309,7 @@ __device__ __forceinline__ void compute_units(const UnitRegs<GS, BITS> (&r)[NU],
         // tot += s * (2^k acc - z xs) per row, as in compute_unit
         const int gg = (GS == 32) ? (j >> 1) : 0;
         constexpr float kA = 16777216.f;
-        constexpr float kB = BITS == 4 ? 1048576.f : 16777216.f;
+        constexpr float kB = BITS == 4 ? 1048576.f : BITS == 3 ? 2097152.f : 16777216.f;
         constexpr float kSymZero = float(1 << (BITS - 1));
 #pragma unroll
         for (int u = 0; u < NU; ++u) {

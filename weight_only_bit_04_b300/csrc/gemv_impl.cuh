@@ -112,7 +112,7 @@ struct GemvArgs {
 // Scale and zero for the rows (g, g+8) of one tile and one group, folded into
 // the two per-element factors of the finalisation.
 struct GroupFactors {
-  float sa, sb;  // s_g * 2^24, s_{g+8} * 2^20      (acc holds q-sums at 2^-24 / 2^-20)
+  float sa, sb;  // s_g * 2^24, s_{g+8} * 2^20 / 2^21 / 2^24 (4 / 3 / 8 bits): acc holds q-sums at the inverse scales
   float za, zb;  // -s_g * z_g * 2^24, -s_{g+8} * z_{g+8} * 2^24   (cx holds x-sums at 2^-24)
 };
 
@@ -120,8 +120,8 @@ struct GroupFactors {
 __device__ __forceinline__ float nib_to_float(uint32_t v) { return __uint_as_float(0x4B000000u | v) - 8388608.f; }
 
 // zraw: 3 and 4 bits: one byte, row g in the low nibble, row g+8 in the high
-// one; 8 bits: two bytes, row g then row g+8. 4-bit rows g+8 sit at 2^-20
-// (high nibbles), everything else at 2^-24.
+// one; 8 bits: two bytes, row g then row g+8. Rows g+8 sit at 2^-20 (4-bit
+// high nibbles) or 2^-21 (3-bit codes at bits 3..5), everything else at 2^-24.
 template <bool SYM, int BITS>
 __device__ __forceinline__ GroupFactors make_factors(uint32_t s2, uint32_t zraw) {
   const float2 sf = __half22float2(*reinterpret_cast<const __half2*>(&s2));
@@ -130,7 +130,7 @@ __device__ __forceinline__ GroupFactors make_factors(uint32_t s2, uint32_t zraw)
   const float zh = SYM ? kSymZero : nib_to_float(BITS != 8 ? (zraw >> 4) & 0xFu : (zraw >> 8) & 0xFFu);
   GroupFactors f;
   f.sa = sf.x * 16777216.f;
-  f.sb = sf.y * (BITS == 4 ? 1048576.f : 16777216.f);
+  f.sb = sf.y * (BITS == 4 ? 1048576.f : BITS == 3 ? 2097152.f : 16777216.f);
   f.za = f.sa * -zg;
   f.zb = sf.y * -zh * 16777216.f;
   return f;
@@ -174,8 +174,9 @@ template <int BITS>
 constexpr int kParts = BITS == 8 ? 2 : 1;
 
 // The four A-fragment registers of 16-column step j of tile tt from the codes
-// the lane loaded for its two tiles: values q * 2^-24, or q * 2^-20 for the
-// high nibbles of 4-bit codes.
+// the lane loaded for its two tiles: values q * 2^-24, or for the rows g+8
+// (registers 1 and 3) q * 2^-20 with 4-bit codes (high nibbles) and q * 2^-21
+// with 3-bit codes (bits 3..5 of each half, see w3_field).
 template <int BITS>
 __device__ __forceinline__ void extract_step(const uint4 (&wb)[2][kParts<BITS>], int tt, int j, uint32_t a[4]) {
   if (BITS == 4) {
@@ -192,18 +193,21 @@ __device__ __forceinline__ void extract_step(const uint4 (&wb)[2][kParts<BITS>],
     const uint4& A = wb[0][0];
     const uint4& Bp = wb[1][0];
     const uint32_t w0 = tt == 0 ? A.x : A.w, w1 = tt == 0 ? A.y : Bp.x, w2 = tt == 0 ? A.z : Bp.y;
-    constexpr uint32_t M = 0x00070007u;
+    // rows g at q * 2^-24 (codes at bits 0..2), rows g+8 at q * 2^-21 (bits 3..5)
+    constexpr uint32_t M = 0x00070007u, M8 = 0x00380038u;
     if (j < 3) {
       const uint32_t w = j == 0 ? w0 : j == 1 ? w1 : w2;
+      const uint32_t w6 = w >> 6;
       a[0] = w & M;
-      a[1] = (w >> 9) & M;
-      a[2] = (w >> 3) & M;
-      a[3] = (w >> 12) & M;
+      a[1] = w & M8;
+      a[2] = w6 & M;
+      a[3] = w6 & M8;
     } else {
-      a[0] = (w0 >> 6) & M;
-      a[1] = (w1 >> 6) & M;
-      a[2] = (w2 >> 6) & M;
-      a[3] = ((w0 >> 15) & 0x00010001u) | ((w1 >> 14) & 0x00020002u) | ((w2 >> 13) & 0x00040004u);
+      const uint32_t w0s = w0 >> 12;
+      a[0] = w0s & M;
+      a[1] = (w1 >> 9) & M8;
+      a[2] = (w2 >> 12) & M;
+      a[3] = (w0s & 0x00080008u) | ((w1 >> 11) & 0x00100010u) | ((w2 >> 10) & 0x00200020u);
     }
   }
 }
@@ -362,7 +366,7 @@ __device__ __forceinline__ void compute_unit(const UnitRegs<GS, BITS>& r, const 
         // -z xs = fma(f, -xs, 2^23 xs) with one rounding.
         const int gg = (GS == 32) ? (j >> 1) : 0;
         constexpr float kA = 16777216.f;
-        constexpr float kB = BITS == 4 ? 1048576.f : 16777216.f;
+        constexpr float kB = BITS == 4 ? 1048576.f : BITS == 3 ? 2097152.f : 16777216.f;
         constexpr float kSymZero = float(1 << (BITS - 1));
         float xs[NB][2], x23[NB][2];
 #pragma unroll

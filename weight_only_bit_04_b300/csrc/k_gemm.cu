@@ -227,16 +227,16 @@ __device__ __forceinline__ void dequant_tile(const StepRegs<GS, SYM, BITS>& r, i
       const uint32_t w0 = i == 0 ? A.x : A.w, w1 = i == 0 ? A.y : Bp.x, w2 = i == 0 ? A.z : Bp.y;
       constexpr uint32_t M = 0x00070007u;
       uint32_t c[4];  // fragment registers a0..a3 (row g / g+8, column pairs 4t, 4t+2)
-      if (j < 3) {
+      if (j < 3) {  // the bit positions of w3_field
         const uint32_t w = j == 0 ? w0 : j == 1 ? w1 : w2;
         c[0] = w & M;
-        c[1] = (w >> 9) & M;
-        c[2] = (w >> 3) & M;
-        c[3] = (w >> 12) & M;
+        c[1] = (w >> 3) & M;
+        c[2] = (w >> 6) & M;
+        c[3] = (w >> 9) & M;
       } else {
-        c[0] = (w0 >> 6) & M;
-        c[1] = (w1 >> 6) & M;
-        c[2] = (w2 >> 6) & M;
+        c[0] = (w0 >> 12) & M;
+        c[1] = (w1 >> 12) & M;
+        c[2] = (w2 >> 12) & M;
         c[3] = ((w0 >> 15) & 0x00010001u) | ((w1 >> 14) & 0x00020002u) | ((w2 >> 13) & 0x00040004u);
       }
       v[4 * j + 0] = hmul2_u32(hsub2_u32(c[0] | 0x64006400u, za[gg]), sg[gg]);

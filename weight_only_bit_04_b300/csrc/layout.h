@@ -81,15 +81,19 @@ __host__ __device__ inline int w3_word_index(int r16, int lane, int wi) {
   if ((r16 & 1) == 0) return base + lane * 4 + wi;
   return wi == 0 ? base + lane * 4 + 3 : base + 128 + lane * 2 + (wi - 1);
 }
-// Word and bit of fragment register a of step j (a = 3 of step 3 is spread
-// over bit 15 of words 0..2; returns wi = -1 for it).
+// Word and bit of fragment register a of step j (in each 16-bit half of the
+// word). Steps 0..2 use word j, registers 0..3 at bits 0, 3, 6 and 9: the
+// row-(g+8) registers 1 and 3 then come out of a mask alone, at 8x scale, and
+// registers 2 and 3 out of one shift by 6. Step 3 uses bits 12..15: registers
+// 0..2 at bit 12 of words 0..2, register 3 spread over bit 15 of words 0..2
+// (returns wi = -1 for it).
 __host__ __device__ inline void w3_field(int j, int a, int* wi, int* shift) {
   if (j < 3) {
     *wi = j;
-    *shift = a == 0 ? 0 : a == 1 ? 9 : a == 2 ? 3 : 12;
+    *shift = 3 * a;
   } else if (a < 3) {
     *wi = a;
-    *shift = 6;
+    *shift = 12;
   } else {
     *wi = -1;
     *shift = 15;
