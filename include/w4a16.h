@@ -423,7 +423,7 @@ W4A16_API w4a16_status w4a16_gemm(const w4a16_format* f, const void* packed, siz
  *           fp32 partial sums are added in rank order through distributed
  *           shared memory); 0 = default (1 when `tile` is given).
  * By default up to 64 tokens use tile 6, up to 128 tile 5 and more tokens
- * tile 3, with K split so that the grid covers the SMs (at least 8 steps of
+ * tile 1, with K split so that the grid covers the SMs (at least 8 steps of
  * 64 columns per thread block). Results match w4a16_gemm's within the
  * error bound (the summation order depends on ksplit).
  */

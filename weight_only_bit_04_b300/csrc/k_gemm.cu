@@ -765,7 +765,7 @@ cudaError_t encode_tiled_map(CUtensorMap* map, CUtensorMapDataType type, int ran
 GemmPlan gemm_default_plan(const Layout& L, int64_t M, int sm_count) {
   // Few tokens: a narrow tile (two blocks per SM) and K split over a cluster
   // so that every SM dequantizes; many tokens: the 128 x 256 tile.
-  GemmPlan p{M <= 64 ? 6 : M <= 128 ? 5 : 3, 1};
+  GemmPlan p{M <= 64 ? 6 : M <= 128 ? 5 : 1, 1};
   const int64_t blocks = ((L.NR * 128 + tile_rows(p.tile) - 1) / tile_rows(p.tile)) *
                          ((M + tile_tokens(p.tile) - 1) / tile_tokens(p.tile));
   const double target = (p.tile >= 5 ? 2.0 : 1.0) * sm_count;
