@@ -650,9 +650,25 @@ def time_e2e(torch, W, dev, layers, xs, ys, yall, graph, chain, head, stream, st
     torch.cuda.synchronize()
     e2e_ms = (time.perf_counter() - t0) * 1e3 / args.steps
     e2e_ms = max_over_ranks(torch, dist, e2e_ms, dev)
-    return {"value": round(world * step_bytes / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
-            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4),
-            "overlap": overlap}
+    rec = {"value": round(world * step_bytes / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4),
+           "overlap": overlap}
+    if chain is not None:
+        # the same steps one at a time: inputs in, the step, outputs out, then a
+        # host synchronization before the next step (nothing overlaps)
+        n = min(args.steps, 50)
+        torch.cuda.synchronize()
+        if dist:
+            dist.barrier()
+        t0 = time.perf_counter()
+        for i in range(n):
+            e2e_step(i)
+            torch.cuda.synchronize()
+        serial_ms = max_over_ranks(torch, dist, (time.perf_counter() - t0) * 1e3 / n, dev)
+        rec["serial"] = {"value": round(world * step_bytes / (serial_ms * 1e-3) / 1e9, 1), "ms_per_step":
+                         round(serial_ms, 4), "steps": n,
+                         "how": "each step's copies and launch, then a host synchronization, step after step"}
+    return rec
 
 
 def run_70b(torch, W, synth, dev, args, dist, world, local_rank):
