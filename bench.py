@@ -106,6 +106,8 @@ def parse_args():
     p.add_argument("--case", type=int, nargs=3, metavar=("N", "K", "M"), default=(4096, 4096, 1))
     p.add_argument("--calls", type=int, default=3)
     p.add_argument("--layers", type=int, default=8, help="--profile-case stream: copies of the layer")
+    p.add_argument("--time-calls", type=int, default=0,
+                   help="--profile-case, outside a profiler: time this many more calls back to back")
     p.add_argument("--act", action="store_true", help="--profile-case gemm: GPTQ act order")
     return p.parse_args()
 
@@ -900,18 +902,36 @@ def run_profile_case(args):
         packs = [packed] + [packed.clone() for _ in range(args.layers - 1)]
         ys = [torch.empty((M, N), dtype=torch.float16, device=dev) for _ in packs]
         chain = W.Chain([(fmt, p, x, y, None) for p, y in zip(packs, ys)], M)
-        for _ in range(args.calls):
-            chain.run()
+        call = chain.run
     else:
         y = torch.empty((M, N), dtype=torch.float16, device=dev)
-        for _ in range(args.calls):
-            if args.profile_case == "gemm":
-                W.gemm(fmt, packed, x, out=y)
-            else:
-                W.gemv(fmt, packed, x, out=y)
+        if args.profile_case == "gemm":
+            call = lambda: W.gemm(fmt, packed, x, out=y)  # noqa: E731
+        else:
+            call = lambda: W.gemv(fmt, packed, x, out=y)  # noqa: E731
+    for _ in range(args.calls):
+        call()
     torch.cuda.synchronize()
+    line = f"{args.profile_case} {N}x{K} M={M} bits={args.bits}: {args.calls} calls"
+    if args.time_calls > 0:
+        # outside a profiler only: the calls back to back between two CUDA
+        # events on the launching stream, so host work overlaps the GPU's
+        stream = torch.cuda.current_stream()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.time_calls):
+            call()
+        e1.record(stream)
+        e1.synchronize()
+        ms = e0.elapsed_time(e1) / args.time_calls
+        if args.profile_case == "gemm":
+            rate = f"{2.0 * M * N * K / (ms * 1e-3) / 1e12:.1f} TFLOP/s (L2 not flushed)"
+        else:
+            nbytes = (args.layers if args.profile_case == "stream" else 1) * gemv_bytes(N, K, M, bits=args.bits)
+            rate = f"{nbytes / (ms * 1e-3) / 1e9:.1f} GB/s"
+        line += f"; {args.time_calls} more back to back: {ms * 1e3:.1f} us per call = {rate}"
     n = W.pipeline_timeouts()
-    print(f"{args.profile_case} {N}x{K} M={M} bits={args.bits}: {args.calls} calls, pipeline timeouts {n}")
+    print(f"{line}; pipeline timeouts {n}")
     return 0 if n == 0 else 1
 
 
