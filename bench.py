@@ -807,7 +807,8 @@ def sweep8192_rows(torch, W, synth, dev, variants=False):
     distinct weight copies, 560 MB, so that launches read cold weights), the
     GEMM for M >= 16 (L2 flushed before each call). With `variants`, also the
     GEMV at M = 1 and 16 for group sizes 32 and 64 and for the symmetric
-    scheme (zero fixed at 8)."""
+    scheme (zero fixed at 8), and for every variant at M = 1 and 16 the 16
+    copies as one chained launch (the decode stream), per copy."""
     N = K = 8192
     copies = 16
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
@@ -835,8 +836,35 @@ def sweep8192_rows(torch, W, synth, dev, variants=False):
         del g
         return ms
 
+    def stream_us(fmt, packs, x, M):
+        """The copies as one chained launch (the decode stream), per copy."""
+        ys = [torch.empty((M, N), dtype=torch.float16, device=dev) for _ in packs]
+        chain = W.Chain([(fmt, p, x, y, None) for p, y in zip(packs, ys)], M)
+        stream = torch.cuda.Stream(device=dev)
+        with torch.cuda.stream(stream):
+            chain.run(stream)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            chain.run(stream)
+        warm_graph(torch, g, stream, 3)
+        ms = time_graph(torch, g, stream, 20) / copies
+        del g, chain
+        return ms
+
+    def stream_row(fmt, packs, M, g, sym):
+        x = synth.activations_cuda(M, K, 0.01, synth.seed_for("sweep8192", "x", M), device=dev)
+        nbytes = gemv_bytes(N, K, M, g=g, sym=sym)
+        ms = stream_us(fmt, packs, x, M)
+        return {"M": M, "group_size": g, "scheme": "sym" if sym else "asym", "kernel": "stream",
+                "us": round(ms * 1e3, 2), "GB/s": round(nbytes / (ms * 1e-3) / 1e9, 1),
+                "TFLOP/s": round(2.0 * M * N * K / ms / 1e9, 2)}
+
     rows = []
     fmt, packs = packs_for(128, False)
+    if variants:
+        for M in (1, 16):
+            rows.append(stream_row(fmt, packs, M, 128, False))
     for M in synth.SWEEP_M:
         x = synth.activations_cuda(M, K, 0.01, synth.seed_for("sweep8192", "x", M), device=dev)
         y = torch.empty((M, N), dtype=torch.float16, device=dev)
@@ -862,6 +890,7 @@ def sweep8192_rows(torch, W, synth, dev, variants=False):
                 rows.append({"M": M, "group_size": g, "scheme": "sym" if sym else "asym", "kernel": "gemv",
                              "us": round(ms * 1e3, 2), "GB/s": round(nbytes / (ms * 1e-3) / 1e9, 1),
                              "TFLOP/s": round(2.0 * M * N * K / ms / 1e9, 2)})
+                rows.append(stream_row(fmt, packs, M, g, sym))
             del packs
     if W.pipeline_timeouts() != 0:
         raise RuntimeError("a GEMV or GEMM gave up a bounded wait: its outputs are undefined")
