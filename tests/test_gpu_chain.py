@@ -122,10 +122,12 @@ def test_decoder_layer_dag(cuda_ok, g, sym):
             assert_within(got, y_ref, B)
 
 
-def test_llama2_7b_step_full_size(cuda_ok):
-    """One decode step of the 7B-shaped stack (32 x 7 linears, 3.37 GB) as one
-    chain with the decoder's dependencies; sampled layers within the bound of
-    the oracle on sampled rows, and two runs bit for bit equal."""
+@pytest.mark.parametrize("bits", [4, 3, 8])
+def test_llama2_7b_step_full_size(cuda_ok, bits):
+    """One decode step of the 7B-shaped stack (32 x 7 linears; 3.37 GB at 4
+    bits, 2.56 GB at 3, 6.63 GB at 8) as one chain with the decoder's
+    dependencies; sampled layers within the bound of the oracle on sampled
+    rows, and two runs bit for bit equal."""
     M = 1
     dev = torch.device("cuda")
     xs = {K: synth.activations_cuda(M, K, synth.LLAMA2_7B_OUTLIER_FRAC, synth.seed_for("c7b", K)) for K in (4096, 11008)}
@@ -133,7 +135,7 @@ def test_llama2_7b_step_full_size(cuda_ok):
     for layer in range(synth.LLAMA2_7B_LAYERS):
         base = len(chain_layers)
         for name, N, K in synth.LLAMA2_7B_LINEARS:
-            fmt, packed, qsz = make_layer(N, K, 128, False, 4, synth.seed_for("c7b", layer, name))
+            fmt, packed, qsz = make_layer(N, K, 128, False, bits, synth.seed_for("c7b", bits, layer, name))
             y = torch.empty((M, N), dtype=torch.float16, device=dev)
             wait = {"q": (base - 1, base - 1), "k": (base - 1, base - 1), "v": (base - 1, base - 1),
                     "o": (base, base + 2), "gate": (base + 3, base + 3), "up": (base + 3, base + 3),
